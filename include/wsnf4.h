@@ -1,0 +1,289 @@
+/*
+ * wsnf4.h -- C ABI of libwsnf4.so: the streamed frozen-NF4-base LoRA linear
+ * on one GB300 (sm_103a).
+ *
+ * The method (Poros, "Blockwise residency for frozen-base QLoRA"):
+ *  - the frozen base is stored as 4-bit NormalFloat (NF4) with one fp32
+ *    absmax per 64 consecutive weights of a row; NF4 is the only precision
+ *    whose streamed run is gated bit-for-bit against a resident run
+ *    (docs, "Limitations" page, section "What 0.00e+00 means");
+ *  - every linear computes y = x W'^T + (alpha/r) B A dropout(x) and the
+ *    backward "propagates gradients only to the adapters and block inputs.
+ *    Frozen weights are never differentiated" (research page "Poros");
+ *  - frozen blocks pass through a small GPU window with asynchronous
+ *    prefetch; activations are kept only at block boundaries; the backward
+ *    walks the blocks in reverse, reloads each, recomputes its forward with
+ *    the same dropout randomness and back-propagates (research page
+ *    "Poros", paragraphs "Poros replaces persistent residency..." and
+ *    "The rest of the training step...");
+ *  - recomputation must redraw identical dropout masks (research page,
+ *    "The catch is dropout" / "RNG state capture").  Here masks come from a
+ *    counter-based Philox4x32-10 keyed by (seed, step, layer, linear,
+ *    micro-batch): no RNG state is captured or restored.
+ *
+ * Conventions for every entry point:
+ *  - Return value: ws_status (0 = WS_OK).  Argument and shape errors are
+ *    reported synchronously before anything is enqueued; launch errors come
+ *    back as WS_ERR_CUDA.  Nothing aborts the process; no C++ exception
+ *    crosses the ABI.
+ *  - Memory: the caller owns every buffer.  The library never allocates or
+ *    frees device, pinned or host tensor memory; scratch is a caller-provided
+ *    workspace whose size the *_workspace_size queries return.  Pointers
+ *    documented as "device" must be device (or managed) memory of the current
+ *    CUDA device; "pinned" means cudaHostAlloc'd / registered host memory.
+ *  - Execution: all work is enqueued asynchronously on the given stream(s);
+ *    no call synchronises the host except ws_stack_train_step when asked to
+ *    return the loss (see there).
+ *  - Alignment: every device pointer must be 16-byte aligned
+ *    (WS_ERR_ALIGN otherwise).
+ *  - Shapes: K % 64 == 0 and N % 64 == 0 for NF4 weights; M >= 1;
+ *    r == 16; M*K < 2^34 for the dropout counter (WS_ERR_SHAPE otherwise).
+ *  - bf16 tensors are passed as uint16_t bit patterns.
+ *  - Determinism: every reduction runs in a fixed order that depends only on
+ *    the shapes, so repeated calls, and a streamed versus a resident run,
+ *    give bitwise identical results.
+ *
+ * Layouts (row-major unless stated):
+ *   W (bf16)   [N, K]
+ *   codes      uint8 [N, K/2]; byte j of row n holds k = 2j in the high
+ *              nibble and k = 2j+1 in the low nibble
+ *   absmax     fp32 [K/64, N]  (block-major: absmax[(k/64)*N + n])
+ *   x, dX      [M, K];  y, dY [M, N]
+ *   A          fp32 [r, K];  B fp32 [N, r]
+ *   U          fp32 [M, r] = (mask . x) A^T  (saved by the forward)
+ *   mask       uint32 [M, K/32]; bit (k % 32) of word (m*K + k)/32 is 1 when
+ *              element (m, k) of the LoRA input is kept
+ */
+#ifndef WSNF4_H
+#define WSNF4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ws_stream_t; /* identical to cudaStream_t */
+typedef struct CUevent_st* ws_event_t;   /* identical to cudaEvent_t  */
+
+typedef int32_t ws_status;
+enum {
+  WS_OK = 0,
+  WS_ERR_INVALID = -1,     /* null pointer / bad enum / bad flag          */
+  WS_ERR_SHAPE = -2,       /* shape outside the supported contract        */
+  WS_ERR_ALIGN = -3,       /* pointer not 16-byte aligned                 */
+  WS_ERR_CUDA = -4,        /* a CUDA runtime call or a launch failed      */
+  WS_ERR_TIMEOUT = -5,     /* a bounded device wait gave up               */
+  WS_ERR_OOM = -6,         /* caller-provided buffer or workspace too small */
+  WS_ERR_UNSUPPORTED = -7, /* configuration that would break exactness    */
+  WS_ERR_NOT_PINNED = -8   /* host pointer is not page-locked             */
+};
+
+enum { WS_DTYPE_BF16 = 0, WS_DTYPE_F32 = 1 };
+
+/* Linear ids inside a layer of the synthetic stack. */
+enum { WS_LIN_Q = 0, WS_LIN_K = 1, WS_LIN_V = 2, WS_LIN_O = 3,
+       WS_LIN_GATE = 4, WS_LIN_UP = 5, WS_LIN_DOWN = 6, WS_NLIN = 7 };
+
+/* A frozen NF4 weight [N, K] (device pointers). */
+typedef struct {
+  const uint8_t* codes; /* [N, K/2] */
+  const float* absmax;  /* [K/64, N] */
+  int64_t N, K;
+} ws_nf4;
+
+/* Dropout key of one linear.  Element e = m*K + k of the LoRA input is kept
+ * iff word (e & 3) of Philox4x32-10(counter = (e >> 2, linear | microbatch
+ * << 8, layer, step), key = (seed_lo, seed_hi)) >= ceil(p * 2^32).
+ * p in [0, 1); linear < 256, microbatch < 2^24. */
+typedef struct {
+  uint64_t seed;
+  uint32_t step, layer, linear, microbatch;
+  double p;
+} ws_dropout_key;
+
+/* Shape of one LoRA linear: x [M, K] -> y [M, N], rank r, scale alpha / r. */
+typedef struct {
+  int64_t M, N, K;
+  int32_t r;
+  float alpha;
+} ws_lora_shape;
+
+/* ---- status ------------------------------------------------------------- */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* ws_status_string(ws_status st);
+
+/* Reads (and clears) the library's device error word, which kernels set when
+ * a bounded wait times out.  Synchronises the current device.  *flags = 0
+ * means no kernel reported a problem.  Returns WS_ERR_TIMEOUT if a flag was
+ * set, WS_OK otherwise. */
+ws_status ws_device_error(uint32_t* flags);
+
+/* ---- a0: NF4 quantisation ------------------------------------------------- */
+/* Quantises a bf16 weight W [N, K] (device) into NF4 codes [N, K/2] and
+ * block-major absmax [K/64, N] (device, caller-allocated).
+ * Per 64-block: absmax = max |w| (fp32); v = w / absmax as an IEEE fp32
+ * division; code = number of the 15 midpoints mid_i = fp32(fp32(c_i +
+ * c_{i+1}) * 0.5) that v exceeds (ties go to the lower level); an all-zero
+ * block gives absmax 0 and code 7.  c_i are the 16 NF4 levels
+ * {-1, -0.6962, -0.5251, -0.3949, -0.2844, -0.1848, -0.0911, 0, 0.0796,
+ * 0.1609, 0.2461, 0.3379, 0.4407, 0.5626, 0.7230, 1} as fp32 literals.
+ * Requires K % 64 == 0, N >= 1.  Dequantisation used by the GEMMs is
+ * w' = bf16_RN(fp32(c[code]) * absmax), one rounding. */
+ws_status ws_quantize_nf4(const uint16_t* W, int64_t N, int64_t K, uint8_t* codes,
+                          float* absmax, ws_stream_t stream);
+
+/* ---- a1 + a2: LoRA linear forward ----------------------------------------- */
+/* Workspace (device bytes) needed by ws_lora_linear_fwd / _bwd for a shape. */
+ws_status ws_lora_workspace_size(ws_lora_shape sh, size_t* bytes);
+
+/* y = x W'^T + s * U B^T with U = (mask . x) A^T and s = (alpha/r)/(1-p)
+ * (inverted dropout folded into the scale).  W' is the NF4 weight
+ * dequantised on the fly inside the tensor-core GEMM; nothing dequantised
+ * is ever written to memory.
+ *   x [M,K] bf16, A [r,K] fp32, B [N,r] fp32              (device, in)
+ *   y [M,N] bf16                                            (device, out)
+ *   U_saved [M,r] fp32                                      (device, out, required)
+ *   mask_saved [M,K/32] uint32                              (device, out, may be NULL)
+ *   workspace >= ws_lora_workspace_size(sh)                 (device scratch)
+ * Accumulation: fp32 on the tensor cores (TMEM); the LoRA up projection is an
+ * extra contraction step of the same GEMM with U and s*B split into bf16
+ * high and low parts (about 16 significant bits per factor). */
+ws_status ws_lora_linear_fwd(const ws_nf4* W, const uint16_t* x, const float* A,
+                             const float* B, ws_lora_shape sh, ws_dropout_key key,
+                             uint16_t* y, float* U_saved, uint32_t* mask_saved,
+                             void* workspace, size_t ws_bytes, ws_stream_t stream);
+
+/* ---- a3 + a4 + a5: LoRA linear backward ------------------------------------ */
+/* Given dY [M,N] bf16 computes
+ *   G  = dY B                              (fp32, internal)
+ *   dB = s dY^T U_saved                    [N, r] fp32 (overwritten)
+ *   dA = s G^T (mask . x)                  [r, K] fp32 (overwritten)
+ *   dX = dY W' + s (G A) . mask            [M, K] bf16 or fp32
+ * dX_dtype: WS_DTYPE_BF16 or WS_DTYPE_F32; dX_accumulate != 0 adds into an
+ * existing fp32 dX (fixed order: the new contribution is added to the old
+ * value once, in fp32).  mask_saved may be NULL: the masks are then
+ * regenerated from `key` (bit-identical to the forward's).
+ * No atomics: dA, dB and split contractions are reduced in a fixed order. */
+ws_status ws_lora_linear_bwd(const ws_nf4* W, const uint16_t* x, const float* A,
+                             const float* B, ws_lora_shape sh, ws_dropout_key key,
+                             const float* U_saved, const uint32_t* mask_saved,
+                             const uint16_t* dY, void* dX, int32_t dX_dtype,
+                             int32_t dX_accumulate, float* dA, float* dB,
+                             void* workspace, size_t ws_bytes, ws_stream_t stream);
+
+/* ---- the synthetic stack ----------------------------------------------------- */
+/* One layer: h -> RMSNorm -> q,k,v (NF4-LoRA) -> v repeated across the
+ * H/head_dim query heads (head h reads kv head h / (H/KV)) in place of the
+ * attention core -> o -> residual; -> RMSNorm -> gate, up -> SiLU(gate)*up
+ * -> down -> residual.  RMSNorm has unit gain and eps `eps`, computed in
+ * fp32; the residual stream is fp32; linear inputs and outputs are bf16;
+ * gradients that enter a linear as dY are bf16, all other activation
+ * gradients are fp32.  q and k feed only the replaced attention core, so
+ * their adapters receive exactly zero gradient.  loss = 0.5 mean(h_L^2). */
+typedef struct {
+  int64_t M, H, KV, I, head_dim;
+  int32_t n_layers;
+  int32_t r;
+  float alpha;
+  double p;
+  float eps;
+  uint64_t seed;
+} ws_stack_cfg;
+
+/* Sizes of the stack's buffers for a given block size (layers per block):
+ *   block_weight_bytes : NF4 bytes of one block (one window slot)
+ *   n_params           : fp32 LoRA parameters of the whole stack (A then B
+ *                        of every linear, see ws_stack_param_offset)
+ *   saved_bytes_layer  : activations one layer keeps for its backward
+ *   workspace_bytes    : scratch for block_forward / block_backward_recompute
+ *                        (includes one block of recompute storage) */
+ws_status ws_stack_sizes(const ws_stack_cfg* cfg, int32_t block_layers,
+                         size_t* block_weight_bytes, int64_t* n_params,
+                         size_t* saved_bytes_layer, size_t* workspace_bytes);
+
+/* Offsets inside a block's NF4 image of layer `layer_in_block`, linear `lin`:
+ * codes at byte *off_codes, absmax at byte *off_absmax (both 256-aligned). */
+ws_status ws_stack_weight_offset(const ws_stack_cfg* cfg, int32_t layer_in_block, int32_t lin,
+                                 size_t* off_codes, size_t* off_absmax);
+
+/* Offsets (in floats) of A [r, K] and B [N, r] of (layer, lin) in the
+ * parameter arrays (params, grads and both Adam moments share the layout). */
+ws_status ws_stack_param_offset(const ws_stack_cfg* cfg, int32_t layer, int32_t lin,
+                                int64_t* off_A, int64_t* off_B);
+
+/* a6: forward of layers [first_layer, first_layer + n_layers) whose NF4
+ * weights are the block image at `block_weights` (device).  h_in / h_out
+ * [M, H] fp32 (device; may not alias).  params: device LoRA parameters.
+ * saved: device area of n_layers * saved_bytes_layer that receives every
+ * activation the backward needs (resident mode), or NULL to keep nothing
+ * (streamed mode: only h_out survives).  step keys the dropout masks. */
+ws_status ws_block_forward(const ws_stack_cfg* cfg, const void* block_weights,
+                           int32_t first_layer, int32_t n_layers, const float* params,
+                           uint32_t step, const float* h_in, float* h_out, void* saved,
+                           void* workspace, size_t ws_bytes, ws_stream_t stream);
+
+/* a8: backward of the same layers.  If `saved` is NULL the block's forward is
+ * first recomputed from the boundary activation h_in (same kernels, same
+ * Philox keys, hence bit-identical intermediates) into the workspace; if
+ * `saved` is the area ws_block_forward filled, it is used directly
+ * (resident mode).  dh_out [M,H] fp32 is the gradient at the block output;
+ * dh_in (may alias dh_out) receives the gradient at the block input.
+ * grads: device LoRA gradients (same layout as params); the block's entries
+ * are overwritten. */
+ws_status ws_block_backward_recompute(const ws_stack_cfg* cfg, const void* block_weights,
+                                      int32_t first_layer, int32_t n_layers,
+                                      const float* params, uint32_t step, const float* h_in,
+                                      const void* saved, const float* dh_out, float* dh_in,
+                                      float* grads, void* workspace, size_t ws_bytes,
+                                      ws_stream_t stream);
+
+/* a7: copy one block (bytes) from pinned host memory to a device window slot
+ * on `copy_stream`.  If wait_event is not NULL the copy first waits for it
+ * (the slot's previous user is done); if done_event is not NULL it is
+ * recorded after the copy.  A pageable source gives WS_ERR_NOT_PINNED. */
+ws_status ws_stream_block_h2d(const void* pinned_src, void* dev_dst, size_t bytes,
+                              ws_stream_t copy_stream, ws_event_t wait_event,
+                              ws_event_t done_event);
+
+/* ---- one training step ---------------------------------------------------------- */
+typedef struct {
+  const void* host_weights; /* pinned: all blocks back to back (streamed), else NULL */
+  const void* dev_weights;  /* device: all blocks back to back (resident), else NULL */
+  void* window;             /* device: 2 * block_weight_bytes (streamed)              */
+  float* params;            /* device: n_params LoRA parameters                       */
+  float* grads;             /* device: n_params                                        */
+  float* adam_m;            /* device: n_params, first moment                          */
+  float* adam_v;            /* device: n_params, second moment                         */
+  float* boundary;          /* device: (n_blocks + 1) * M * H fp32 block-boundary h    */
+  void* saved;              /* device: n_layers * saved_bytes_layer (resident), else NULL */
+  float* dh;                /* device: 2 * M * H fp32 gradient ping-pong               */
+  void* workspace;          /* device: workspace_bytes                                  */
+  size_t workspace_bytes;
+  float* loss;              /* device: 1 float, receives the loss                      */
+} ws_stack_buffers;
+
+/* One full training step of the stack: forward over the blocks, loss,
+ * backward over the blocks in reverse, one Adam step (PyTorch defaults:
+ * betas 0.9 / 0.999, eps 1e-8, bias-corrected, no weight decay) with
+ * learning rate lr at Adam step t = step + 1.
+ * streamed != 0: weights come from host_weights through the 2-slot window;
+ *   block b+1's copy (copy_stream) overlaps block b's compute, the backward
+ *   reloads blocks in reverse and recomputes each from its boundary
+ *   activation (saved must be NULL).
+ * streamed == 0: weights are read from dev_weights and every intermediate
+ *   is kept in `saved` (no recompute).
+ * Both modes run the same kernels in the same order on the same data, so
+ * loss, gradients, parameters and Adam moments are bitwise identical.
+ * h0 [M, H] fp32 (device) is the step's input.  Enqueued on `compute`;
+ * returns without waiting for the GPU. */
+ws_status ws_stack_train_step(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
+                              const ws_stack_buffers* buf, uint32_t step, const float* h0,
+                              float lr, ws_stream_t compute, ws_stream_t copy_stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WSNF4_H */

@@ -8,7 +8,7 @@ library and raises if it is missing -- there is no fallback path.
 """
 import importlib
 
-__all__ = ["ops", "synth", "build"]
+__all__ = ["ops", "synth", "build", "stack"]
 
 
 def __getattr__(name):

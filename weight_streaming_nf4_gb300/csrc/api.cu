@@ -1,0 +1,337 @@
+// api.cu -- the C ABI of libwsnf4.so (declared in include/wsnf4.h):
+// argument validation, dispatch to the kernels, the pinned-host -> HBM block
+// copy, and the host-side engine of one streamed or resident training step.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace ws;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ws_status cuda_status(cudaError_t e) { return e == cudaSuccess ? WS_OK : WS_ERR_CUDA; }
+
+ws_status check_linear(const ws_nf4* W, ws_lora_shape sh, const ws_dropout_key& key) {
+  if (!W || !W->codes || !W->absmax) return WS_ERR_INVALID;
+  if (sh.M < 1 || sh.N < 64 || sh.K < 64) return WS_ERR_SHAPE;
+  if (sh.N % 64 || sh.K % 64) return WS_ERR_SHAPE;
+  if (W->N != sh.N || W->K != sh.K) return WS_ERR_SHAPE;
+  if (sh.r != 16) return WS_ERR_SHAPE;
+  if ((double)sh.M * (double)sh.K >= 17179869184.0) return WS_ERR_SHAPE;  // 2^34
+  if (sh.N > (int64_t)1 << 30 || sh.K > (int64_t)1 << 30 || sh.M > (int64_t)1 << 30)
+    return WS_ERR_SHAPE;
+  if (!(key.p >= 0.0 && key.p < 1.0)) return WS_ERR_INVALID;
+  if (key.linear > 255u || key.microbatch > 0xFFFFFFu) return WS_ERR_INVALID;
+  if (!aligned16(W->codes) || !aligned16(W->absmax)) return WS_ERR_ALIGN;
+  return WS_OK;
+}
+
+NF4View view_of(const ws_nf4* W) {
+  NF4View v;
+  v.codes = W->codes;
+  v.absmax = W->absmax;
+  v.N = W->N;
+  v.K = W->K;
+  return v;
+}
+
+float lora_scale(ws_lora_shape sh, double p) {
+  return (float)(((double)sh.alpha / (double)sh.r) / (1.0 - p));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ws_status_string(ws_status st) {
+  switch (st) {
+    case WS_OK: return "WS_OK";
+    case WS_ERR_INVALID: return "WS_ERR_INVALID: invalid argument";
+    case WS_ERR_SHAPE: return "WS_ERR_SHAPE: shape outside the supported contract";
+    case WS_ERR_ALIGN: return "WS_ERR_ALIGN: pointer not 16-byte aligned";
+    case WS_ERR_CUDA: return "WS_ERR_CUDA: CUDA call or kernel launch failed";
+    case WS_ERR_TIMEOUT: return "WS_ERR_TIMEOUT: a bounded device wait gave up";
+    case WS_ERR_OOM: return "WS_ERR_OOM: buffer or workspace too small";
+    case WS_ERR_UNSUPPORTED: return "WS_ERR_UNSUPPORTED: configuration would break exactness";
+    case WS_ERR_NOT_PINNED: return "WS_ERR_NOT_PINNED: host buffer is not page-locked";
+    default: return "WS_ERR_UNKNOWN";
+  }
+}
+
+ws_status ws_device_error(uint32_t* flags) {
+  if (!flags) return WS_ERR_INVALID;
+  *flags = 0;
+  const cudaError_t e = read_and_clear_dev_error(flags);
+  if (e != cudaSuccess) return WS_ERR_CUDA;
+  return *flags ? WS_ERR_TIMEOUT : WS_OK;
+}
+
+ws_status ws_quantize_nf4(const uint16_t* W, int64_t N, int64_t K, uint8_t* codes, float* absmax,
+                          ws_stream_t stream) {
+  if (!W || !codes || !absmax) return WS_ERR_INVALID;
+  if (N < 1 || K < 64 || K % 64) return WS_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(codes) || !aligned16(absmax)) return WS_ERR_ALIGN;
+  return cuda_status(run_quantize_nf4(W, N, K, codes, absmax, (cudaStream_t)stream));
+}
+
+ws_status ws_lora_workspace_size(ws_lora_shape sh, size_t* bytes) {
+  if (!bytes) return WS_ERR_INVALID;
+  if (sh.M < 1 || sh.N < 64 || sh.K < 64 || sh.N % 64 || sh.K % 64 || sh.r != 16)
+    return WS_ERR_SHAPE;
+  *bytes = linear_workspace_bytes(sh.M, sh.N, sh.K);
+  return WS_OK;
+}
+
+ws_status ws_lora_linear_fwd(const ws_nf4* W, const uint16_t* x, const float* A, const float* B,
+                             ws_lora_shape sh, ws_dropout_key key, uint16_t* y, float* U_saved,
+                             uint32_t* mask_saved, void* workspace, size_t ws_bytes,
+                             ws_stream_t stream) {
+  ws_status s = check_linear(W, sh, key);
+  if (s != WS_OK) return s;
+  if (!x || !A || !B || !y || !U_saved || !workspace) return WS_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(y) || !aligned16(U_saved) ||
+      !aligned16(workspace) || (mask_saved && !aligned16(mask_saved)))
+    return WS_ERR_ALIGN;
+  if (ws_bytes < linear_workspace_bytes(sh.M, sh.N, sh.K)) return WS_ERR_OOM;
+  return cuda_status(linear_fwd(view_of(W), x, A, B, sh.M, lora_scale(sh, key.p),
+                                make_drop_key(key), y, U_saved, mask_saved, workspace,
+                                (cudaStream_t)stream));
+}
+
+ws_status ws_lora_linear_bwd(const ws_nf4* W, const uint16_t* x, const float* A, const float* B,
+                             ws_lora_shape sh, ws_dropout_key key, const float* U_saved,
+                             const uint32_t* mask_saved, const uint16_t* dY, void* dX,
+                             int32_t dX_dtype, int32_t dX_accumulate, float* dA, float* dB,
+                             void* workspace, size_t ws_bytes, ws_stream_t stream) {
+  ws_status s = check_linear(W, sh, key);
+  if (s != WS_OK) return s;
+  if (!x || !A || !B || !U_saved || !dY || !dX || !dA || !dB || !workspace) return WS_ERR_INVALID;
+  if (dX_dtype != WS_DTYPE_BF16 && dX_dtype != WS_DTYPE_F32) return WS_ERR_INVALID;
+  if (dX_accumulate && dX_dtype != WS_DTYPE_F32) return WS_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(U_saved) || !aligned16(dY) ||
+      !aligned16(dX) || !aligned16(dA) || !aligned16(dB) || !aligned16(workspace) ||
+      (mask_saved && !aligned16(mask_saved)))
+    return WS_ERR_ALIGN;
+  if (ws_bytes < linear_workspace_bytes(sh.M, sh.N, sh.K)) return WS_ERR_OOM;
+  return cuda_status(linear_bwd(view_of(W), x, A, B, sh.M, lora_scale(sh, key.p),
+                                make_drop_key(key), U_saved, mask_saved, dY, dX,
+                                dX_dtype == WS_DTYPE_F32 ? 1 : 0, dX_accumulate ? 1 : 0, dA, dB,
+                                workspace, (cudaStream_t)stream));
+}
+
+ws_status ws_stack_sizes(const ws_stack_cfg* cfg, int32_t block_layers, size_t* block_weight_bytes,
+                         int64_t* n_params, size_t* saved_bytes_layer, size_t* workspace_bytes) {
+  ws_status s = stack_check(cfg);
+  if (s != WS_OK) return s;
+  if (block_layers < 1 || block_layers > cfg->n_layers) return WS_ERR_SHAPE;
+  if (block_weight_bytes) *block_weight_bytes = stack_block_bytes(*cfg, block_layers);
+  if (n_params) *n_params = stack_n_params(*cfg);
+  if (saved_bytes_layer) *saved_bytes_layer = stack_saved_layer(*cfg);
+  if (workspace_bytes) *workspace_bytes = stack_ws_bytes(*cfg, block_layers);
+  return WS_OK;
+}
+
+ws_status ws_stack_weight_offset(const ws_stack_cfg* cfg, int32_t layer_in_block, int32_t lin,
+                                 size_t* off_codes, size_t* off_absmax) {
+  ws_status s = stack_check(cfg);
+  if (s != WS_OK) return s;
+  if (!off_codes || !off_absmax || lin < 0 || lin >= WS_NLIN || layer_in_block < 0)
+    return WS_ERR_INVALID;
+  stack_weight_offset(*cfg, layer_in_block, lin, off_codes, off_absmax);
+  return WS_OK;
+}
+
+ws_status ws_stack_param_offset(const ws_stack_cfg* cfg, int32_t layer, int32_t lin,
+                                int64_t* off_A, int64_t* off_B) {
+  ws_status s = stack_check(cfg);
+  if (s != WS_OK) return s;
+  if (!off_A || !off_B || lin < 0 || lin >= WS_NLIN || layer < 0 || layer >= cfg->n_layers)
+    return WS_ERR_INVALID;
+  stack_param_offset(*cfg, layer, lin, off_A, off_B);
+  return WS_OK;
+}
+
+ws_status ws_block_forward(const ws_stack_cfg* cfg, const void* block_weights, int32_t first_layer,
+                           int32_t n_layers, const float* params, uint32_t step, const float* h_in,
+                           float* h_out, void* saved, void* workspace, size_t ws_bytes,
+                           ws_stream_t stream) {
+  ws_status s = stack_check(cfg);
+  if (s != WS_OK) return s;
+  if (!block_weights || !params || !h_in || !h_out || !workspace) return WS_ERR_INVALID;
+  if (n_layers < 1 || first_layer < 0 || first_layer + n_layers > cfg->n_layers) return WS_ERR_SHAPE;
+  if (h_in == h_out) return WS_ERR_INVALID;
+  if (!aligned16(block_weights) || !aligned16(params) || !aligned16(h_in) || !aligned16(h_out) ||
+      !aligned16(workspace) || (saved && !aligned16(saved)))
+    return WS_ERR_ALIGN;
+  if (ws_bytes < stack_ws_bytes(*cfg, n_layers)) return WS_ERR_OOM;
+  return cuda_status(block_forward(*cfg, n_layers, block_weights, first_layer, n_layers, params,
+                                   step, h_in, h_out, saved, workspace, (cudaStream_t)stream));
+}
+
+ws_status ws_block_backward_recompute(const ws_stack_cfg* cfg, const void* block_weights,
+                                      int32_t first_layer, int32_t n_layers, const float* params,
+                                      uint32_t step, const float* h_in, const void* saved,
+                                      const float* dh_out, float* dh_in, float* grads,
+                                      void* workspace, size_t ws_bytes, ws_stream_t stream) {
+  ws_status s = stack_check(cfg);
+  if (s != WS_OK) return s;
+  if (!block_weights || !params || !dh_out || !dh_in || !grads || !workspace) return WS_ERR_INVALID;
+  if (!saved && !h_in) return WS_ERR_INVALID;
+  if (n_layers < 1 || first_layer < 0 || first_layer + n_layers > cfg->n_layers) return WS_ERR_SHAPE;
+  if (!aligned16(block_weights) || !aligned16(params) || !aligned16(dh_out) || !aligned16(dh_in) ||
+      !aligned16(grads) || !aligned16(workspace) || (saved && !aligned16(saved)) ||
+      (h_in && !aligned16(h_in)))
+    return WS_ERR_ALIGN;
+  if (ws_bytes < stack_ws_bytes(*cfg, n_layers)) return WS_ERR_OOM;
+  return cuda_status(block_backward(*cfg, n_layers, block_weights, first_layer, n_layers, params,
+                                    step, h_in, saved, dh_out, dh_in, grads, workspace,
+                                    (cudaStream_t)stream));
+}
+
+ws_status ws_stream_block_h2d(const void* pinned_src, void* dev_dst, size_t bytes,
+                              ws_stream_t copy_stream, ws_event_t wait_event,
+                              ws_event_t done_event) {
+  if (!pinned_src || !dev_dst) return WS_ERR_INVALID;
+  if (bytes == 0) return WS_OK;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, pinned_src) != cudaSuccess) {
+    cudaGetLastError();
+    return WS_ERR_NOT_PINNED;
+  }
+  if (attr.type != cudaMemoryTypeHost) return WS_ERR_NOT_PINNED;
+  cudaStream_t st = (cudaStream_t)copy_stream;
+  if (wait_event && cudaStreamWaitEvent(st, (cudaEvent_t)wait_event, 0) != cudaSuccess)
+    return WS_ERR_CUDA;
+  if (cudaMemcpyAsync(dev_dst, pinned_src, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return WS_ERR_CUDA;
+  if (done_event && cudaEventRecord((cudaEvent_t)done_event, st) != cudaSuccess) return WS_ERR_CUDA;
+  return WS_OK;
+}
+
+// One training step.  Streamed mode keeps a 2-slot window: slot s holds
+// block b with s = b % 2.  The copy of block b+1 is issued before block b's
+// compute so it runs on the copy engine meanwhile; a copy into a slot waits
+// for the compute stream's last use of that slot.  A block still resident
+// in its slot (the last two at the forward/backward turnaround) is not
+// copied again.
+ws_status ws_stack_train_step(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
+                              const ws_stack_buffers* buf, uint32_t step, const float* h0, float lr,
+                              ws_stream_t compute, ws_stream_t copy_stream) {
+  ws_status s = stack_check(cfg);
+  if (s != WS_OK) return s;
+  if (!buf || !h0) return WS_ERR_INVALID;
+  if (block_layers < 1 || cfg->n_layers % block_layers) return WS_ERR_SHAPE;
+  if (!buf->params || !buf->grads || !buf->adam_m || !buf->adam_v || !buf->boundary || !buf->dh ||
+      !buf->workspace || !buf->loss)
+    return WS_ERR_INVALID;
+  if (streamed) {
+    if (!buf->host_weights || !buf->window || buf->saved) return WS_ERR_INVALID;
+  } else {
+    if (!buf->dev_weights || !buf->saved) return WS_ERR_INVALID;
+  }
+  if (buf->workspace_bytes < stack_ws_bytes(*cfg, block_layers)) return WS_ERR_OOM;
+  const cudaStream_t cs = (cudaStream_t)compute;
+  const cudaStream_t ps = (cudaStream_t)copy_stream;
+  if (streamed && !ps) return WS_ERR_INVALID;
+
+  const int nb = cfg->n_layers / block_layers;
+  const size_t bbytes = stack_block_bytes(*cfg, block_layers);
+  const size_t slayer = stack_saved_layer(*cfg);
+  const int64_t MH = cfg->M * cfg->H;
+  const int64_t np = stack_n_params(*cfg);
+  float* bnd = buf->boundary;
+
+  cudaEvent_t ev_loaded[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr};
+  int slot_block[2] = {-1, -1};
+  bool slot_used[2] = {false, false};
+  ws_status rc = WS_OK;
+  auto fail = [&](cudaError_t e) {
+    if (e != cudaSuccess && rc == WS_OK) rc = WS_ERR_CUDA;
+    return e != cudaSuccess;
+  };
+  auto cleanup = [&]() {
+    for (int i = 0; i < 2; ++i) {
+      if (ev_loaded[i]) cudaEventDestroy(ev_loaded[i]);
+      if (ev_free[i]) cudaEventDestroy(ev_free[i]);
+    }
+  };
+  if (streamed) {
+    for (int i = 0; i < 2; ++i) {
+      if (fail(cudaEventCreateWithFlags(&ev_loaded[i], cudaEventDisableTiming)) ||
+          fail(cudaEventCreateWithFlags(&ev_free[i], cudaEventDisableTiming))) {
+        cleanup();
+        return rc;
+      }
+    }
+  }
+  const uint8_t* host = static_cast<const uint8_t*>(buf->host_weights);
+  uint8_t* window = static_cast<uint8_t*>(buf->window);
+  auto ensure = [&](int blk) -> ws_status {
+    const int sl = blk % 2;
+    if (slot_block[sl] == blk) return WS_OK;
+    ws_status r = ws_stream_block_h2d(host + (size_t)blk * bbytes, window + (size_t)sl * bbytes,
+                                      bbytes, copy_stream,
+                                      slot_used[sl] ? (ws_event_t)ev_free[sl] : nullptr,
+                                      (ws_event_t)ev_loaded[sl]);
+    if (r == WS_OK) slot_block[sl] = blk;
+    return r;
+  };
+  auto block_ptr = [&](int blk) -> const void* {
+    if (streamed) return window + (size_t)(blk % 2) * bbytes;
+    return static_cast<const uint8_t*>(buf->dev_weights) + (size_t)blk * bbytes;
+  };
+  auto wait_loaded = [&](int blk) {
+    return streamed ? cudaStreamWaitEvent(cs, ev_loaded[blk % 2], 0) : cudaSuccess;
+  };
+  auto release = [&](int blk) {
+    if (!streamed) return cudaSuccess;
+    slot_used[blk % 2] = true;
+    return cudaEventRecord(ev_free[blk % 2], cs);
+  };
+
+  // ---- forward
+  if (fail(cudaMemcpyAsync(bnd, h0, (size_t)MH * 4, cudaMemcpyDeviceToDevice, cs))) goto done;
+  if (streamed && (rc = ensure(0)) != WS_OK) goto done;
+  for (int b = 0; b < nb; ++b) {
+    if (streamed && b + 1 < nb && (rc = ensure(b + 1)) != WS_OK) goto done;
+    if (fail(wait_loaded(b))) goto done;
+    void* sv = streamed ? nullptr : static_cast<uint8_t*>(buf->saved) + (size_t)b * block_layers * slayer;
+    if (fail(block_forward(*cfg, block_layers, block_ptr(b), b * block_layers, block_layers,
+                           buf->params, step, bnd + (size_t)b * MH, bnd + (size_t)(b + 1) * MH, sv,
+                           buf->workspace, cs)))
+      goto done;
+    if (fail(release(b))) goto done;
+  }
+  // ---- loss
+  if (fail(loss_and_grad(*cfg, block_layers, bnd + (size_t)nb * MH, buf->dh, buf->loss,
+                         buf->workspace, cs)))
+    goto done;
+  // ---- backward, blocks in reverse
+  for (int b = nb - 1; b >= 0; --b) {
+    if (streamed) {
+      if ((rc = ensure(b)) != WS_OK) goto done;
+      if (b - 1 >= 0 && (rc = ensure(b - 1)) != WS_OK) goto done;
+    }
+    if (fail(wait_loaded(b))) goto done;
+    const void* sv =
+        streamed ? nullptr : static_cast<uint8_t*>(buf->saved) + (size_t)b * block_layers * slayer;
+    if (fail(block_backward(*cfg, block_layers, block_ptr(b), b * block_layers, block_layers,
+                            buf->params, step, bnd + (size_t)b * MH, sv, buf->dh, buf->dh,
+                            buf->grads, buf->workspace, cs)))
+      goto done;
+    if (fail(release(b))) goto done;
+  }
+  // ---- optimizer
+  if (fail(adam_step(buf->params, buf->grads, buf->adam_m, buf->adam_v, np, (int64_t)step + 1, lr, cs)))
+    goto done;
+done:
+  cleanup();
+  return rc;
+}
+
+}  // extern "C"

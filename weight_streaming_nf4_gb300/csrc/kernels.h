@@ -1,0 +1,116 @@
+// kernels.h -- internal interfaces between the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "wsnf4.h"
+
+namespace ws {
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct NF4View {
+  const uint8_t* codes;  // [N, K/2]
+  const float* absmax;   // [K/64, N]
+  int64_t N, K;
+};
+
+// Arguments of one dequant-GEMM launch (see nf4_gemm.cu).
+struct GemmArgs {
+  int64_t M;            // activation rows
+  int64_t Nout;         // output columns (forward: N, backward: K)
+  int nk_total;         // 64-deep contraction steps in total
+  int ksteps_per_split; // steps per grid-z split
+  int has_lora;         // split 0 runs the extra LoRA step
+  const float* lora_F;  // forward: B [N, 16]; backward: A [16, K]
+  float lora_scale;     // s = (alpha / r) / (1 - p)
+  const uint32_t* mask; // backward: dropout bits [M, K/32]
+  void* out;            // [M, Nout] bf16 or fp32
+  int out_f32, out_accum;
+  float* partial;       // [splits, M, Nout] fp32 when splits > 1
+};
+
+// Tile configuration: a pure function of the shape and the SM count, so a
+// resident and a streamed run always pick the same kernels and split order.
+struct GemmPlan {
+  bool bwd;
+  int um, bn;
+  int mtiles, ntiles, nk;
+  int splits, kps;
+};
+
+int device_sm_count();
+cudaError_t read_and_clear_dev_error(uint32_t* flags);
+GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc);
+size_t gemm_partial_bytes(const GemmPlan& p, int64_t M, int64_t Nout);
+
+// act: [M, Kc] bf16 (forward x, backward dY); lora_act: [M, 64] bf16 split
+// factor (U or G hi/lo) or NULL; lora_F: the other LoRA factor (B or A).
+cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* act, int64_t M,
+                         const uint16_t* lora_act, const float* lora_F, float lora_scale,
+                         const uint32_t* mask, void* out, int out_f32, int out_accum,
+                         float* partial, cudaStream_t st);
+
+// ---- small kernels (lora_small.cu) ----------------------------------------------------
+struct DropKeyHost {
+  uint32_t k0, k1, c1, c2, c3, thresh, drop_all;
+};
+DropKeyHost make_drop_key(const ws_dropout_key& k);
+
+cudaError_t run_quantize_nf4(const uint16_t* W, int64_t N, int64_t K, uint8_t* codes,
+                             float* absmax, cudaStream_t st);
+// U = (mask . x) A^T [M,16] fp32; Uext [M,64] bf16 hi/lo; mask bits (optional).
+cudaError_t run_lora_down(const uint16_t* x, const float* A, int64_t M, int64_t K,
+                          const DropKeyHost& key, float* U, uint16_t* Uext, uint32_t* mask_out,
+                          cudaStream_t st);
+// G = dY B [M,16] fp32 and Gext [M,64] bf16 hi/lo.
+cudaError_t run_lora_G(const uint16_t* dY, const float* B, int64_t M, int64_t N, float* G,
+                       uint16_t* Gext, cudaStream_t st);
+// Weight gradient of a LoRA factor: out = s * P^T Q~ with P [M,16] fp32,
+// Q [M,C] bf16 (masked by `mask` [M, C/32] when not NULL).  out layout is
+// [C,16] (dB) or, when transpose_out, [16,C] (dA).  Fixed-order reduction.
+size_t wgrad_partial_bytes(int64_t M, int64_t C);
+cudaError_t run_lora_wgrad(const float* P, const uint16_t* Q, const uint32_t* mask, int64_t M,
+                           int64_t C, float s, float* out, int transpose_out, float* partial,
+                           cudaStream_t st);
+cudaError_t run_mask_gen(int64_t M, int64_t K, const DropKeyHost& key, uint32_t* mask,
+                         cudaStream_t st);
+
+// ---- one LoRA linear (linear.cu) --------------------------------------------------------
+size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t linear_fwd(const NF4View& W, const uint16_t* x, const float* A, const float* B,
+                       int64_t M, float scale, const DropKeyHost& key, uint16_t* y, float* U,
+                       uint32_t* mask, void* ws, cudaStream_t st);
+cudaError_t linear_bwd(const NF4View& W, const uint16_t* x, const float* A, const float* B,
+                       int64_t M, float scale, const DropKeyHost& key, const float* U,
+                       const uint32_t* mask, const uint16_t* dY, void* dX, int dX_f32,
+                       int dX_accum, float* dA, float* dB, void* ws, cudaStream_t st);
+
+}  // namespace ws
+
+namespace ws {
+// ---- synthetic stack (stack.cu) -------------------------------------------------------
+ws_status stack_check(const ws_stack_cfg* c);
+size_t stack_block_bytes(const ws_stack_cfg& c, int block_layers);
+int64_t stack_n_params(const ws_stack_cfg& c);
+size_t stack_saved_layer(const ws_stack_cfg& c);
+size_t stack_ws_bytes(const ws_stack_cfg& c, int block_layers);
+void stack_weight_offset(const ws_stack_cfg& c, int layer_in_block, int lin, size_t* off_codes,
+                         size_t* off_absmax);
+void stack_param_offset(const ws_stack_cfg& c, int layer, int lin, int64_t* off_A, int64_t* off_B);
+cudaError_t block_forward(const ws_stack_cfg& c, int block_layers_ws, const void* block,
+                          int first_layer, int n_layers, const float* params, uint32_t step,
+                          const float* h_in, float* h_out, void* saved, void* ws, cudaStream_t st);
+cudaError_t block_backward(const ws_stack_cfg& c, int block_layers_ws, const void* block,
+                           int first_layer, int n_layers, const float* params, uint32_t step,
+                           const float* h_in, const void* saved, const float* dh_out, float* dh_in,
+                           float* grads, void* ws, cudaStream_t st);
+cudaError_t loss_and_grad(const ws_stack_cfg& c, int block_layers_ws, const float* h, float* dh,
+                          float* loss, void* ws, cudaStream_t st);
+cudaError_t adam_step(float* p, const float* g, float* m, float* v, int64_t n, int64_t t, float lr,
+                      cudaStream_t st);
+}  // namespace ws

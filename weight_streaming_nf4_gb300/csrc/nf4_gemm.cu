@@ -1,0 +1,642 @@
+// nf4_gemm.cu -- the NF4 dequant GEMM on the 5th-generation tensor cores.
+//
+// Forward (a2):  y[M,N]  = x[M,K] . W'[N,K]^T  (+ s U B^T as an extra step)
+// Backward (a4): dX[M,K] = dY[M,N] . W'[N,K]   (+ s (G A) . mask)
+//
+// W' = bf16_RN(c[code] * absmax) is never materialised in global memory:
+// packed 4-bit codes and the block absmax are staged into shared memory by
+// TMA, dequantised by eight producer warps straight into the 128-byte
+// swizzled operand layout the tensor cores read, and consumed by
+// tcgen05.mma (bf16 x bf16 -> fp32 in TMEM) issued by one thread.
+//
+// CTA = 10 warps:
+//   warp 0     TMA producer (activation tile + code tile + absmax tile)
+//   warp 1     TMEM allocator and MMA issuer
+//   warps 2-9  dequant producers, then the epilogue (TMEM -> registers ->
+//              global), one TMEM lane quarter per warp
+// Tile: 128*UM rows of activations (UM tensor-core atoms of M = 128 sharing
+// one dequantised weight tile), BN output columns, 64-deep contraction steps.
+//
+// The LoRA terms use the same tensor cores: the forward appends one 64-deep
+// step whose A operand is [U_hi | U_lo | U_hi | 0] and whose B operand is
+// [Bs_hi | Bs_hi | Bs_lo | 0] (Bs = s B, bf16 high/low splits), i.e.
+// U Bs^T to about 16 significant bits.  The backward computes s G A the same
+// way into a second TMEM accumulator and adds it under the dropout mask in
+// the epilogue.  Contraction splits (grid z) write fp32 partials that a
+// separate kernel sums in split order: no atomics anywhere.
+#define WS_GEMM_TU 1
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ws {
+
+cudaError_t read_and_clear_dev_error(uint32_t* flags) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(flags, g_dev_error, sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  const uint32_t zero = 0;
+  return cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(uint32_t));
+}
+
+__constant__ float c_nf4_levels[16] = {-1.0f,    -0.6962f, -0.5251f, -0.3949f,
+                                       -0.2844f, -0.1848f, -0.0911f, 0.0f,
+                                       0.0796f,  0.1609f,  0.2461f,  0.3379f,
+                                       0.4407f,  0.5626f,  0.7230f,  1.0f};
+
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kDqWarps = 8;
+constexpr int kDqThreads = kDqWarps * 32;
+
+template <bool BWD, int UM, int BN>
+struct Cfg {
+  static constexpr int BM = 128 * UM;
+  static constexpr uint32_t A_BYTES = BM * 128;   // BM rows x 64 bf16
+  static constexpr uint32_t B_BYTES = BN * 128;   // BN x 64 bf16
+  static constexpr uint32_t C_BYTES = BN * 32;    // codes: BN x 64 nibbles
+  static constexpr uint32_t S_BYTES = BN * 4;     // absmax: BN floats
+  static constexpr int BSTAGES = 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + C_BYTES + S_BYTES;
+  static constexpr int STAGES_RAW =
+      (int)((220u * 1024u - BSTAGES * B_BYTES - 1024u) / STAGE_BYTES);
+  static constexpr int STAGES = STAGES_RAW > 4 ? 4 : STAGES_RAW;
+  static constexpr uint32_t TMEM_COLS = (BWD ? 2u : 1u) * UM * BN;
+  // MN-major operand (backward): 64-element MN groups LBO apart, 8-row K
+  // groups SBO apart.
+  static constexpr uint32_t MN_LBO = 1024;
+  static constexpr uint32_t MN_SBO = (BN / 64) * 1024;
+  static constexpr uint32_t OFF_A = 0;
+  static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr uint32_t OFF_C = OFF_B + BSTAGES * B_BYTES;
+  static constexpr uint32_t OFF_S = OFF_C + STAGES * C_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_S + STAGES * S_BYTES;
+  static constexpr uint32_t N_BARS = 2 * STAGES + 2 * BSTAGES + 2;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+  static_assert(STAGES >= 2, "pipeline needs two stages");
+  static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns");
+  static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory");
+  static_assert(BN == 128 || BN == 256, "BN");
+};
+
+WS_DEVINL void sts128(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
+}
+
+// Dequantise 4 code bytes (8 consecutive weights along k) into a 16-byte
+// chunk of bf16 values: element 2i from the high nibble of byte i, element
+// 2i+1 from its low nibble.
+WS_DEVINL uint4 dq8(uint32_t w, float a, const float* lv) {
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t byte = (w >> (8 * i)) & 0xFFu;
+    const float v0 = lv[byte >> 4] * a;
+    const float v1 = lv[byte & 15u] * a;
+    o[i] = pack_bf16x2(v0, v1);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Forward weight tile, K-major 128B-swizzled: row j = output column n0 + j,
+// 64 contraction elements; chunk cc of row j sits at (cc ^ (j & 7)) * 16.
+template <int BN>
+WS_DEVINL void dequant_fwd(const uint8_t* sC, const float* sS, uint8_t* sB, int t,
+                           const float* lv) {
+  if constexpr (BN == 256) {
+    const int j = t;
+    const uint4 c0 = *reinterpret_cast<const uint4*>(sC + j * 32);
+    const uint4 c1 = *reinterpret_cast<const uint4*>(sC + j * 32 + 16);
+    const float a = sS[j];
+    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    uint8_t* row = sB + j * 128;
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+      const uint4 v = dq8(words[cc], a, lv);
+      sts128(row + ((cc ^ (j & 7)) << 4), v.x, v.y, v.z, v.w);
+    }
+  } else {
+    const int j = t >> 1, half = t & 1;
+    const uint4 c = *reinterpret_cast<const uint4*>(sC + j * 32 + half * 16);
+    const float a = sS[j];
+    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+    uint8_t* row = sB + j * 128;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int cc = half * 4 + q;
+      const uint4 v = dq8(words[q], a, lv);
+      sts128(row + ((cc ^ (j & 7)) << 4), v.x, v.y, v.z, v.w);
+    }
+  }
+}
+
+// Backward weight tile, MN-major 128B-swizzled: the contraction runs over
+// W's rows n (64 per step) and the output over W's columns k (BN per tile),
+// so the tile keeps W's own orientation.  Element (k-col j, n-row c):
+// group (c/8, j/64) at (c/8)*SBO + (j/64)*LBO, row c%8 inside the group,
+// chunk ((j%64)/8) ^ (c%8).
+template <int BN>
+WS_DEVINL void dequant_bwd(const uint8_t* sC, const float* sS, uint8_t* sB, int t,
+                           const float* lv) {
+  using C = Cfg<true, 1, BN>;
+  constexpr int SEGS = BN / 32;                  // 32-column segments per row
+  constexpr int ITEMS = 64 * SEGS / kDqThreads;  // rows*segs per thread
+#pragma unroll
+  for (int it = 0; it < ITEMS; ++it) {
+    const int item = t + it * kDqThreads;
+    const int c = item / SEGS, seg = item % SEGS;
+    const uint4 cw = *reinterpret_cast<const uint4*>(sC + c * (BN / 2) + seg * 16);
+    const float a = sS[((seg * 32) / 64) * 64 + c];
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+    const int mg = (seg * 32) / 64;
+    uint8_t* grp = sB + (c >> 3) * C::MN_SBO + mg * C::MN_LBO + (c & 7) * 128;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int cc = ((seg * 32) % 64) / 8 + q;
+      const uint4 v = dq8(words[q], a, lv);
+      sts128(grp + ((cc ^ (c & 7)) << 4), v.x, v.y, v.z, v.w);
+    }
+  }
+}
+
+// The LoRA weight operand of the extra step, K-major like the forward
+// tile: row j holds [Ws_hi(16) | Ws_hi(16) | Ws_lo(16) | 0(16)] with
+// Ws = s * (row j of the LoRA factor).  Forward: factor row = B[n0+j, :];
+// backward: factor row = A[:, n0+j] (column of A).
+template <bool BWD, int BN>
+WS_DEVINL void lora_tile(const float* F, int64_t rows_total, int64_t ld, int n0, float s,
+                         uint8_t* sB, int t) {
+  constexpr int TPR = kDqThreads / BN;  // threads per row: 1 (BN=256) or 2 (BN=128)
+  const int j = t / TPR, part = t % TPR;
+  const int64_t n = (int64_t)n0 + j;
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float f = 0.0f;
+    if (n < rows_total) f = BWD ? F[(int64_t)i * ld + n] : F[n * 16 + i];
+    v[i] = s * f;
+  }
+  uint32_t hi[8], lo[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float h0 = bf16_lo(pack_bf16x2(v[2 * i], 0.0f));
+    const float h1 = bf16_lo(pack_bf16x2(v[2 * i + 1], 0.0f));
+    hi[i] = pack_bf16x2(h0, h1);
+    lo[i] = pack_bf16x2(v[2 * i] - h0, v[2 * i + 1] - h1);
+  }
+  uint8_t* row = sB + j * 128;
+#pragma unroll
+  for (int q = 0; q < 8 / TPR; ++q) {
+    const int cc = part * (8 / TPR) + q;
+    uint4 val;
+    if (cc == 0 || cc == 2) val = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    else if (cc == 1 || cc == 3) val = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+    else if (cc == 4) val = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    else if (cc == 5) val = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+    else val = make_uint4(0u, 0u, 0u, 0u);
+    sts128(row + ((cc ^ (j & 7)) << 4), val.x, val.y, val.z, val.w);
+  }
+}
+
+template <bool BWD, int UM, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
+               const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmL,
+               const GemmArgs args) {
+  using C = Cfg<BWD, UM, BN>;
+  constexpr int STAGES = C::STAGES;
+  constexpr int BSTAGES = C::BSTAGES;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ float s_lv[16];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem + C::OFF_A;
+  uint8_t* sB = smem + C::OFF_B;
+  uint8_t* sC = smem + C::OFF_C;
+  uint8_t* sS = smem + C::OFF_S;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* full = bars;
+  uint64_t* empty = full + STAGES;
+  uint64_t* bfull = empty + STAGES;
+  uint64_t* bempty = bfull + BSTAGES;
+  uint64_t* accfull = bempty + BSTAGES;
+  uint64_t* drain = accfull + 1;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  uint32_t* tmem_slot = misc;
+  volatile uint32_t* abort_flag = misc + 1;
+  volatile uint32_t* skip_flag = misc + 2;
+
+  const int warp = (int)warp_id();
+  const int lane = (int)lane_id();
+  const int mt = blockIdx.x, nt = blockIdx.y, split = blockIdx.z;
+  const int m0 = mt * C::BM;
+  const int n0 = nt * BN;
+  const int ks_begin = split * args.ksteps_per_split;
+  const int ks_end = min(args.nk_total, ks_begin + args.ksteps_per_split);
+  const bool lora_here = args.has_lora && split == 0;
+  const int nsteps = (ks_end - ks_begin) + (lora_here ? 1 : 0);
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    // an earlier kernel already gave up: do nothing rather than queue more work
+    *skip_flag = (*(volatile uint32_t*)&g_dev_error != 0u || nsteps <= 0) ? 1u : 0u;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1 + kDqWarps);
+    }
+    for (int b = 0; b < BSTAGES; ++b) {
+      mbar_init(&bfull[b], kDqWarps);
+      mbar_init(&bempty[b], 1);
+    }
+    mbar_init(accfull, 1);
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (threadIdx.x < 16) s_lv[threadIdx.x] = c_nf4_levels[threadIdx.x];
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool skip = *skip_flag != 0u;
+
+  if (!skip) {
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmC);
+        tma_prefetch_desc(&tmS);
+        if (lora_here) tma_prefetch_desc(&tmL);
+        int issued = 0;
+        for (int i = 0; i < nsteps; ++i) {
+          const int s = i % STAGES;
+          const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+          if (*abort_flag || !mbar_wait(&empty[s], ph ^ 1u, DERR_TIMEOUT_EMPTY)) {
+            *abort_flag = 1u;
+            break;
+          }
+          const bool is_lora = lora_here && i == nsteps - 1;
+          if (!is_lora) {
+            const int c0 = (ks_begin + i) * 64;
+            mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::C_BYTES + C::S_BYTES);
+            tma_load_2d(sA + s * C::A_BYTES, &tmA, &full[s], c0, m0);
+            if (!BWD) {
+              tma_load_2d(sC + s * C::C_BYTES, &tmC, &full[s], c0 / 2, n0);
+              tma_load_2d(sS + s * C::S_BYTES, &tmS, &full[s], n0, c0 / 64);
+            } else {
+              tma_load_2d(sC + s * C::C_BYTES, &tmC, &full[s], n0 / 2, c0);
+              tma_load_2d(sS + s * C::S_BYTES, &tmS, &full[s], c0, n0 / 64);
+            }
+          } else {
+            mbar_arrive_expect_tx(&full[s], C::A_BYTES);
+            tma_load_2d(sA + s * C::A_BYTES, &tmL, &full[s], 0, m0);
+          }
+          issued = i + 1;
+        }
+        if (*abort_flag) {
+          // let every issued copy land before the CTA can exit
+          for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
+            mbar_wait(&full[i % STAGES], (uint32_t)(i / STAGES) & 1u, DERR_TIMEOUT_DRAIN);
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_main = idesc_bf16_f32(128, BN, BWD ? 1u : 0u);
+        constexpr uint32_t idesc_kmaj = idesc_bf16_f32(128, BN, 0u);
+        for (int i = 0; i < nsteps; ++i) {
+          const int s = i % STAGES;
+          const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+          const int b = i % BSTAGES;
+          const uint32_t bph = (uint32_t)(i / BSTAGES) & 1u;
+          if (*abort_flag || !mbar_wait(&full[s], ph, DERR_TIMEOUT_FULL) ||
+              !mbar_wait(&bfull[b], bph, DERR_TIMEOUT_BFULL)) {
+            *abort_flag = 1u;
+            break;
+          }
+          tc_fence_after();
+          const bool is_lora = lora_here && i == nsteps - 1;
+          const uint32_t a_base = smem_u32(sA + s * C::A_BYTES);
+          const uint32_t b_base = smem_u32(sB + b * C::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            uint64_t bdesc;
+            if (!BWD || is_lora)
+              bdesc = smem_desc_sw128(b_base + kk * 32, 16, 1024);
+            else
+              bdesc = smem_desc_sw128(b_base + kk * 2 * C::MN_SBO, C::MN_LBO, C::MN_SBO);
+#pragma unroll
+            for (int u = 0; u < UM; ++u) {
+              const uint64_t adesc = smem_desc_sw128(a_base + u * 16384 + kk * 32, 16, 1024);
+              uint32_t d = tmem + (uint32_t)(u * BN);
+              uint32_t acc;
+              if (BWD && is_lora) {
+                d += (uint32_t)(UM * BN);
+                acc = kk > 0 ? 1u : 0u;
+              } else {
+                acc = (i > 0 || kk > 0) ? 1u : 0u;
+              }
+              tc_mma_f16(d, adesc, bdesc, is_lora ? idesc_kmaj : idesc_main, acc);
+            }
+          }
+          tc_commit(&empty[s]);
+          tc_commit(&bempty[b]);
+        }
+        tc_commit(accfull);
+      }
+    } else {
+      // ------------------------------------------------------------ dequant producers
+      const int t = (int)threadIdx.x - 64;
+      for (int i = 0; i < nsteps; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+        const int b = i % BSTAGES;
+        const uint32_t bph = (uint32_t)(i / BSTAGES) & 1u;
+        if (*abort_flag || !mbar_wait(&full[s], ph, DERR_TIMEOUT_FULL) ||
+            !mbar_wait(&bempty[b], bph ^ 1u, DERR_TIMEOUT_BEMPTY)) {
+          *abort_flag = 1u;
+          break;
+        }
+        const bool is_lora = lora_here && i == nsteps - 1;
+        uint8_t* Bt = sB + b * C::B_BYTES;
+        if (!is_lora) {
+          const uint8_t* cs = sC + s * C::C_BYTES;
+          const float* ss = reinterpret_cast<const float*>(sS + s * C::S_BYTES);
+          if (!BWD) dequant_fwd<BN>(cs, ss, Bt, t, s_lv);
+          else dequant_bwd<BN>(cs, ss, Bt, t, s_lv);
+        } else {
+          lora_tile<BWD, BN>(args.lora_F, args.Nout, args.Nout, n0, args.lora_scale, Bt, t);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bfull[b]);
+          mbar_arrive(&empty[s]);
+        }
+      }
+
+      // ------------------------------------------------------------ epilogue
+      const bool ok = mbar_wait(accfull, 0u, DERR_TIMEOUT_ACC) && !*abort_flag;
+      tc_fence_after();
+      const int q = warp & 3;          // TMEM lane quarter this warp may read
+      const int h = (warp - 2) >> 2;   // 0 or 1
+      const int r = q * 32 + lane;     // accumulator row inside an atom
+      const int ncols = UM == 2 ? BN : BN / 2;
+      const int u = UM == 2 ? h : 0;
+      const int cbase = UM == 2 ? 0 : h * (BN / 2);
+      const int64_t m = (int64_t)m0 + u * 128 + r;
+      const bool row_ok = ok && m < args.M;
+      for (int cc = 0; cc < ncols; cc += 32) {
+        const int col = cbase + cc;
+        const int64_t n = (int64_t)n0 + col;
+        if (n >= args.Nout) break;  // warp-uniform
+        uint32_t acc[32];
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(u * BN + col);
+        tmem_ld_32x32b_x32(taddr, acc);
+        uint32_t lacc[32];
+        if (BWD && lora_here) tmem_ld_32x32b_x32(taddr + (uint32_t)(UM * BN), lacc);
+        tmem_ld_wait();
+        if (!row_ok) continue;
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(acc[e]);
+        if (BWD && lora_here) {
+          const uint32_t bits = args.mask[(m * args.Nout + n) >> 5];
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if ((bits >> e) & 1u) v[e] += __uint_as_float(lacc[e]);
+        }
+        if (args.partial != nullptr) {
+          float4* dst = reinterpret_cast<float4*>(
+              args.partial + ((int64_t)split * args.M + m) * args.Nout + n);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        } else if (args.out_f32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.out) + m * args.Nout + n);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float4 o = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+            if (args.out_accum) {
+              const float4 p = dst[e];
+              o.x = p.x + o.x;
+              o.y = p.y + o.y;
+              o.z = p.z + o.z;
+              o.w = p.w + o.w;
+            }
+            dst[e] = o;
+          }
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.out) + m * args.Nout + n);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(pack_bf16x2(v[8 * e], v[8 * e + 1]), pack_bf16x2(v[8 * e + 2], v[8 * e + 3]),
+                                pack_bf16x2(v[8 * e + 4], v[8 * e + 5]),
+                                pack_bf16x2(v[8 * e + 6], v[8 * e + 7]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// Fixed-order sum of contraction-split partials: out = sum_s partial[s].
+__global__ void k_split_reduce(const float* __restrict__ partial, int splits, int64_t elems,
+                               void* out, int out_f32, int out_accum) {
+  const int64_t i4 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i4 >= elems) return;
+  float4 acc = *reinterpret_cast<const float4*>(partial + i4);
+  for (int s = 1; s < splits; ++s) {
+    const float4 p = *reinterpret_cast<const float4*>(partial + (int64_t)s * elems + i4);
+    acc.x += p.x;
+    acc.y += p.y;
+    acc.z += p.z;
+    acc.w += p.w;
+  }
+  if (out_f32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + i4);
+    if (out_accum) {
+      const float4 o = *dst;
+      acc.x = o.x + acc.x;
+      acc.y = o.y + acc.y;
+      acc.z = o.z + acc.z;
+      acc.w = o.w + acc.w;
+    }
+    *dst = acc;
+  } else {
+    uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + i4);
+    *dst = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------------- host
+namespace {
+
+PFN_encodeTiled g_encode = nullptr;
+
+bool encode_fn() {
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return false;
+  g_encode = reinterpret_cast<PFN_encodeTiled>(fn);
+  return true;
+}
+
+// 2-D tensor map: inner dimension `inner` elements (contiguous), `outer` rows
+// with a row pitch of `pitch_bytes`; box {box_inner, box_outer}.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+              uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle sw) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {pitch_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool BWD, int UM, int BN>
+cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& tA,
+                       const CUtensorMap& tC, const CUtensorMap& tS, const CUtensorMap& tL,
+                       cudaStream_t st) {
+  using C = Cfg<BWD, UM, BN>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_nf4_gemm<BWD, UM, BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid((unsigned)p.mtiles, (unsigned)p.ntiles, (unsigned)p.splits);
+  k_nf4_gemm<BWD, UM, BN><<<grid, kThreads, C::SMEM_BYTES, st>>>(tA, tC, tS, tL, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int device_sm_count() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  return sms;
+}
+
+GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc) {
+  GemmPlan p{};
+  p.bwd = bwd;
+  p.um = M > 128 ? 2 : 1;
+  p.bn = (!bwd && p.um == 2 && Nout >= 256) ? 256 : 128;
+  p.mtiles = (int)((M + 128 * p.um - 1) / (128 * p.um));
+  p.ntiles = (int)((Nout + p.bn - 1) / p.bn);
+  p.nk = (int)(Kc / 64);
+  const int tiles = p.mtiles * p.ntiles;
+  const int sms = device_sm_count();
+  int splits = 1;
+  if (tiles < sms) {
+    splits = sms / tiles;
+    const int max_by_depth = p.nk / 8;  // keep at least 8 steps per split
+    if (splits > max_by_depth) splits = max_by_depth;
+    if (splits < 1) splits = 1;
+  }
+  p.kps = (p.nk + splits - 1) / splits;
+  p.splits = (p.nk + p.kps - 1) / p.kps;  // no empty split
+  return p;
+}
+
+size_t gemm_partial_bytes(const GemmPlan& p, int64_t M, int64_t Nout) {
+  return p.splits > 1 ? (size_t)p.splits * (size_t)M * (size_t)Nout * sizeof(float) : 0;
+}
+
+cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* act, int64_t M,
+                         const uint16_t* lora_act, const float* lora_F, float lora_scale,
+                         const uint32_t* mask, void* out, int out_f32, int out_accum,
+                         float* partial, cudaStream_t st) {
+  if (!encode_fn()) return cudaErrorNotSupported;
+  const int64_t N = W.N, K = W.K;
+  const int64_t Nout = p.bwd ? K : N;
+  const int64_t Kc = p.bwd ? N : K;
+  const int BM = 128 * p.um;
+  CUtensorMap tA, tC, tS, tL;
+  bool ok = make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, (uint64_t)Kc, (uint64_t)M,
+                     (uint64_t)Kc * 2, 64, (uint32_t)BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!p.bwd) {
+    ok = ok && make_map(&tC, CU_TENSOR_MAP_DATA_TYPE_UINT8, W.codes, (uint64_t)(K / 2),
+                        (uint64_t)N, (uint64_t)(K / 2), 32, (uint32_t)p.bn,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok = ok && make_map(&tS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, W.absmax, (uint64_t)N,
+                        (uint64_t)(K / 64), (uint64_t)N * 4, (uint32_t)p.bn, 1,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else {
+    ok = ok && make_map(&tC, CU_TENSOR_MAP_DATA_TYPE_UINT8, W.codes, (uint64_t)(K / 2),
+                        (uint64_t)N, (uint64_t)(K / 2), (uint32_t)(p.bn / 2), 64,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok = ok && make_map(&tS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, W.absmax, (uint64_t)N,
+                        (uint64_t)(K / 64), (uint64_t)N * 4, 64, (uint32_t)(p.bn / 64),
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  const bool has_lora = lora_act != nullptr && lora_F != nullptr;
+  if (has_lora)
+    ok = ok && make_map(&tL, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lora_act, 64, (uint64_t)M, 128, 64,
+                        (uint32_t)BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    tL = tA;
+  if (!ok) return cudaErrorInvalidValue;
+
+  GemmArgs a{};
+  a.M = M;
+  a.Nout = Nout;
+  a.nk_total = p.nk;
+  a.ksteps_per_split = p.kps;
+  a.has_lora = has_lora ? 1 : 0;
+  a.lora_F = lora_F;
+  a.lora_scale = lora_scale;
+  a.mask = mask;
+  a.out = out;
+  a.out_f32 = out_f32;
+  a.out_accum = out_accum;
+  a.partial = p.splits > 1 ? partial : nullptr;
+
+  cudaError_t e;
+  if (!p.bwd) {
+    if (p.um == 2 && p.bn == 256) e = launch_cfg<false, 2, 256>(p, a, tA, tC, tS, tL, st);
+    else if (p.um == 2) e = launch_cfg<false, 2, 128>(p, a, tA, tC, tS, tL, st);
+    else e = launch_cfg<false, 1, 128>(p, a, tA, tC, tS, tL, st);
+  } else {
+    if (p.um == 2) e = launch_cfg<true, 2, 128>(p, a, tA, tC, tS, tL, st);
+    else e = launch_cfg<true, 1, 128>(p, a, tA, tC, tS, tL, st);
+  }
+  if (e != cudaSuccess) return e;
+  if (p.splits > 1) {
+    const int64_t elems = M * Nout;
+    const int64_t threads = elems / 4;
+    k_split_reduce<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(partial, p.splits, elems, out,
+                                                                     out_f32, out_accum);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace ws

@@ -1,0 +1,543 @@
+// stack.cu -- the synthetic transformer stack around the NF4-LoRA linears,
+// the block forward / backward-with-recompute, and the streamed training
+// step (pinned host -> 2-slot HBM window on a copy stream).
+//
+// Pointwise and row kernels are HBM-bound; each row reduction (RMSNorm,
+// its backward, the loss) sums in a fixed order: per-thread strided sums, a
+// fixed butterfly inside each warp, warps added in index order.
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ws {
+
+namespace {
+
+size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------------------- kernels
+WS_DEVINL float block_sum_256(float v, float* red) {
+  // blockDim.x == 256: butterfly inside each warp, then warp 0 adds the 8
+  // warp totals in index order; every thread returns the same total.
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.0f;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < 8; ++w) t += red[w];
+    red[8] = t;
+  }
+  __syncthreads();
+  return red[8];
+}
+
+__global__ void __launch_bounds__(256) k_rmsnorm_fwd(const float* __restrict__ h, int64_t H,
+                                                     float eps, uint16_t* __restrict__ out,
+                                                     float* __restrict__ rstd) {
+  __shared__ float red[9];
+  const int64_t m = blockIdx.x;
+  const float* row = h + m * H;
+  float ss = 0.0f;
+  for (int64_t i = threadIdx.x; i < H; i += 256) ss = fmaf(row[i], row[i], ss);
+  ss = block_sum_256(ss, red);
+  const float rs = 1.0f / sqrtf(ss / (float)H + eps);
+  if (threadIdx.x == 0) rstd[m] = rs;
+  for (int64_t i = threadIdx.x; i < H; i += 256) out[m * H + i] = f32_to_bf16_bits(row[i] * rs);
+}
+
+// dx += rstd*dy - rstd^3 * x * (dy . x) / H
+__global__ void __launch_bounds__(256) k_rmsnorm_bwd(const float* __restrict__ x,
+                                                     const float* __restrict__ rstd,
+                                                     const float* __restrict__ dy, int64_t H,
+                                                     float* __restrict__ dx) {
+  __shared__ float red[9];
+  const int64_t m = blockIdx.x;
+  const float* xr = x + m * H;
+  const float* dr = dy + m * H;
+  float dot = 0.0f;
+  for (int64_t i = threadIdx.x; i < H; i += 256) dot = fmaf(dr[i], xr[i], dot);
+  dot = block_sum_256(dot, red);
+  const float rs = rstd[m];
+  const float coef = rs * rs * rs * dot / (float)H;
+  for (int64_t i = threadIdx.x; i < H; i += 256) dx[m * H + i] += rs * dr[i] - coef * xr[i];
+}
+
+__global__ void k_silu_mul_fwd(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u,
+                               int64_t n, uint16_t* __restrict__ act) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float gv = bf16_bits_to_f32(g[i]), uv = bf16_bits_to_f32(u[i]);
+  const float sg = 1.0f / (1.0f + expf(-gv));
+  act[i] = f32_to_bf16_bits(gv * sg * uv);
+}
+
+__global__ void k_silu_mul_bwd(const float* __restrict__ dact, const uint16_t* __restrict__ g,
+                               const uint16_t* __restrict__ u, int64_t n, uint16_t* __restrict__ dg,
+                               uint16_t* __restrict__ du) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float gv = bf16_bits_to_f32(g[i]), uv = bf16_bits_to_f32(u[i]), d = dact[i];
+  const float sg = 1.0f / (1.0f + expf(-gv));
+  du[i] = f32_to_bf16_bits(d * gv * sg);
+  dg[i] = f32_to_bf16_bits(d * uv * sg * (1.0f + gv * (1.0f - sg)));
+}
+
+// vr[m, hh*hd + d] = v[m, (hh / rep)*hd + d]
+__global__ void k_repeat_fwd(const uint16_t* __restrict__ v, int64_t M, int64_t H, int64_t KV,
+                             int64_t hd, uint16_t* __restrict__ vr) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= M * H) return;
+  const int64_t m = i / H, c = i % H;
+  const int64_t rep = H / KV;
+  const int64_t hh = c / hd, d = c % hd;
+  vr[i] = v[m * KV + (hh / rep) * hd + d];
+}
+
+// dv[m, kh*hd + d] = bf16( sum_{t < rep} dvr[m, (kh*rep + t)*hd + d] ), t ascending
+__global__ void k_repeat_bwd(const float* __restrict__ dvr, int64_t M, int64_t H, int64_t KV,
+                             int64_t hd, uint16_t* __restrict__ dv) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= M * KV) return;
+  const int64_t m = i / KV, c = i % KV;
+  const int64_t rep = H / KV;
+  const int64_t kh = c / hd, d = c % hd;
+  float s = 0.0f;
+  for (int64_t t = 0; t < rep; ++t) s += dvr[m * H + (kh * rep + t) * hd + d];
+  dv[i] = f32_to_bf16_bits(s);
+}
+
+__global__ void k_add_bf16(const float* __restrict__ h, const uint16_t* __restrict__ y, int64_t n,
+                           float* __restrict__ out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  out[i] = h[i] + bf16_bits_to_f32(y[i]);
+}
+
+__global__ void k_cast_bf16(const float* __restrict__ x, int64_t n, uint16_t* __restrict__ y) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  y[i] = f32_to_bf16_bits(x[i]);
+}
+
+// loss = 0.5 * sum(h^2) / n in two fixed-order passes; dh = h / n.
+constexpr int kLossBlocks = 256;
+__global__ void __launch_bounds__(256) k_loss_partial(const float* __restrict__ h, int64_t n,
+                                                      float* __restrict__ partial,
+                                                      float* __restrict__ dh, float inv_n) {
+  __shared__ float red[9];
+  const int64_t per = (n + kLossBlocks - 1) / kLossBlocks;
+  const int64_t b0 = (int64_t)blockIdx.x * per, b1 = min(n, b0 + per);
+  float s = 0.0f;
+  for (int64_t i = b0 + threadIdx.x; i < b1; i += 256) {
+    const float v = h[i];
+    s = fmaf(v, v, s);
+    dh[i] = v * inv_n;
+  }
+  s = block_sum_256(s, red);
+  if (threadIdx.x == 0) partial[blockIdx.x] = s;
+}
+__global__ void k_loss_final(const float* __restrict__ partial, float inv_n,
+                             float* __restrict__ loss) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  float s = 0.0f;
+  for (int i = 0; i < kLossBlocks; ++i) s += partial[i];
+  *loss = 0.5f * s * inv_n;
+}
+
+// PyTorch-default Adam (no weight decay, bias-corrected).
+__global__ void k_adam(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
+                       float* __restrict__ v, int64_t n, float beta1, float beta2, float eps,
+                       float step_size, float bc2_sqrt) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float gi = g[i];
+  const float mi = beta1 * m[i] + (1.0f - beta1) * gi;
+  const float vi = beta2 * v[i] + (1.0f - beta2) * gi * gi;
+  m[i] = mi;
+  v[i] = vi;
+  const float denom = sqrtf(vi) / bc2_sqrt + eps;
+  p[i] = p[i] - step_size * (mi / denom);
+}
+
+unsigned nblk(int64_t n, int t = 256) { return (unsigned)((n + t - 1) / t); }
+
+// ---------------------------------------------------------------------------- layouts
+struct Shapes {
+  int64_t N[WS_NLIN], K[WS_NLIN];
+};
+Shapes shapes_of(const ws_stack_cfg& c) {
+  Shapes s;
+  const int64_t H = c.H, KV = c.KV, I = c.I;
+  const int64_t N[WS_NLIN] = {H, KV, KV, H, I, I, H};
+  const int64_t K[WS_NLIN] = {H, H, H, H, H, H, I};
+  for (int i = 0; i < WS_NLIN; ++i) {
+    s.N[i] = N[i];
+    s.K[i] = K[i];
+  }
+  return s;
+}
+
+struct SavedLayout {
+  size_t h, a, rstd1, v, vr, h1, b, rstd2, g, u, act, U[WS_NLIN], mask[WS_NLIN], total;
+};
+SavedLayout saved_layout(const ws_stack_cfg& c) {
+  const Shapes s = shapes_of(c);
+  const size_t M = (size_t)c.M, H = (size_t)c.H, KV = (size_t)c.KV, I = (size_t)c.I;
+  SavedLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t r = o;
+    o += al256(bytes);
+    return r;
+  };
+  L.h = take(M * H * 4);
+  L.a = take(M * H * 2);
+  L.rstd1 = take(M * 4);
+  L.v = take(M * KV * 2);
+  L.vr = take(M * H * 2);
+  L.h1 = take(M * H * 4);
+  L.b = take(M * H * 2);
+  L.rstd2 = take(M * 4);
+  L.g = take(M * I * 2);
+  L.u = take(M * I * 2);
+  L.act = take(M * I * 2);
+  for (int i = 0; i < WS_NLIN; ++i) L.U[i] = take(M * 16 * 4);
+  for (int i = 0; i < WS_NLIN; ++i) L.mask[i] = take(M * (size_t)(s.K[i] / 32) * 4);
+  L.total = o;
+  return L;
+}
+
+struct WeightLayout {
+  size_t codes[WS_NLIN], absmax[WS_NLIN], layer_bytes;
+};
+WeightLayout weight_layout(const ws_stack_cfg& c) {
+  const Shapes s = shapes_of(c);
+  WeightLayout L{};
+  size_t o = 0;
+  for (int i = 0; i < WS_NLIN; ++i) {
+    L.codes[i] = o;
+    o += al256((size_t)s.N[i] * (size_t)(s.K[i] / 2));
+    L.absmax[i] = o;
+    o += al256((size_t)(s.K[i] / 64) * (size_t)s.N[i] * 4);
+  }
+  L.layer_bytes = o;
+  return L;
+}
+
+struct ParamLayout {
+  int64_t A[WS_NLIN], B[WS_NLIN], layer_floats;
+};
+ParamLayout param_layout(const ws_stack_cfg& c) {
+  const Shapes s = shapes_of(c);
+  ParamLayout L{};
+  int64_t o = 0;
+  auto al = [](int64_t x) { return (x + 63) & ~int64_t(63); };
+  for (int i = 0; i < WS_NLIN; ++i) {
+    L.A[i] = o;
+    o += al(16 * s.K[i]);
+    L.B[i] = o;
+    o += al(s.N[i] * 16);
+  }
+  L.layer_floats = o;
+  return L;
+}
+
+struct WsLayout {
+  size_t lin, blk, qout, kout, yout, y1, dact, dg, du, db, dvr, dv, lossp, total;
+};
+WsLayout ws_layout(const ws_stack_cfg& c, int block_layers) {
+  const Shapes s = shapes_of(c);
+  const size_t M = (size_t)c.M, H = (size_t)c.H, KV = (size_t)c.KV, I = (size_t)c.I;
+  WsLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t r = o;
+    o += al256(bytes);
+    return r;
+  };
+  size_t lin = 0;
+  for (int i = 0; i < WS_NLIN; ++i) {
+    const size_t b = linear_workspace_bytes(c.M, s.N[i], s.K[i]);
+    if (b > lin) lin = b;
+  }
+  L.lin = take(lin);
+  L.blk = take((size_t)block_layers * saved_layout(c).total);
+  L.qout = take(M * H * 2);
+  L.kout = take(M * KV * 2);
+  L.yout = take(M * H * 2);
+  L.y1 = take(M * H * 2);
+  L.dact = take(M * I * 4);
+  L.dg = take(M * I * 2);
+  L.du = take(M * I * 2);
+  L.db = take(M * H * 4);
+  L.dvr = take(M * H * 4);
+  L.dv = take(M * KV * 2);
+  L.lossp = take(kLossBlocks * 4);
+  L.total = o;
+  return L;
+}
+
+template <class T>
+T* at(const void* base, size_t off) {
+  return reinterpret_cast<T*>(const_cast<uint8_t*>(static_cast<const uint8_t*>(base)) + off);
+}
+
+#define WS_TRY(x)                           \
+  do {                                      \
+    cudaError_t e_ = (x);                   \
+    if (e_ != cudaSuccess) return e_;       \
+  } while (0)
+
+struct Ctx {
+  ws_stack_cfg c;
+  Shapes s;
+  SavedLayout SL;
+  WeightLayout WL;
+  ParamLayout PL;
+  WsLayout WSL;
+  float scale;
+  cudaStream_t st;
+  void* ws;
+};
+
+NF4View wview(const Ctx& x, const void* block, int layer_in_block, int lin) {
+  NF4View v;
+  const uint8_t* base = static_cast<const uint8_t*>(block) + (size_t)layer_in_block * x.WL.layer_bytes;
+  v.codes = base + x.WL.codes[lin];
+  v.absmax = reinterpret_cast<const float*>(base + x.WL.absmax[lin]);
+  v.N = x.s.N[lin];
+  v.K = x.s.K[lin];
+  return v;
+}
+
+DropKeyHost key_of(const Ctx& x, uint32_t step, int layer, int lin) {
+  ws_dropout_key k{};
+  k.seed = x.c.seed;
+  k.step = step;
+  k.layer = (uint32_t)layer;
+  k.linear = (uint32_t)lin;
+  k.microbatch = 0;
+  k.p = x.c.p;
+  return make_drop_key(k);
+}
+
+// Forward of one layer.  S: saved slot of this layer.  with_qk: compute the
+// q and k projections (the first forward does; a recompute skips them since
+// nothing downstream reads them).
+cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const float* params,
+                      uint32_t step, const float* h_in, float* h_out, uint8_t* S, bool with_qk) {
+  const int64_t M = x.c.M, H = x.c.H, KV = x.c.KV, I = x.c.I;
+  const SavedLayout& L = x.SL;
+  cudaStream_t st = x.st;
+  uint8_t* ws = static_cast<uint8_t*>(x.ws);
+  void* lws = ws + x.WSL.lin;
+  const float* P = params + (int64_t)layer * x.PL.layer_floats;
+  auto lin = [&](int li, const uint16_t* in, uint16_t* out) {
+    return linear_fwd(wview(x, block, lib, li), in, P + x.PL.A[li], P + x.PL.B[li], M, x.scale,
+                      key_of(x, step, layer, li), out, at<float>(S, L.U[li]),
+                      at<uint32_t>(S, L.mask[li]), lws, st);
+  };
+  float* h = at<float>(S, L.h);
+  if (h != h_in) WS_TRY(cudaMemcpyAsync(h, h_in, (size_t)M * H * 4, cudaMemcpyDeviceToDevice, st));
+  k_rmsnorm_fwd<<<(unsigned)M, 256, 0, st>>>(h, H, x.c.eps, at<uint16_t>(S, L.a), at<float>(S, L.rstd1));
+  WS_TRY(cudaGetLastError());
+  if (with_qk) {
+    WS_TRY(lin(WS_LIN_Q, at<uint16_t>(S, L.a), at<uint16_t>(ws, x.WSL.qout)));
+    WS_TRY(lin(WS_LIN_K, at<uint16_t>(S, L.a), at<uint16_t>(ws, x.WSL.kout)));
+  }
+  WS_TRY(lin(WS_LIN_V, at<uint16_t>(S, L.a), at<uint16_t>(S, L.v)));
+  k_repeat_fwd<<<nblk(M * H), 256, 0, st>>>(at<uint16_t>(S, L.v), M, H, KV, x.c.head_dim,
+                                            at<uint16_t>(S, L.vr));
+  WS_TRY(cudaGetLastError());
+  uint16_t* y = at<uint16_t>(ws, x.WSL.yout);
+  WS_TRY(lin(WS_LIN_O, at<uint16_t>(S, L.vr), y));
+  k_add_bf16<<<nblk(M * H), 256, 0, st>>>(h, y, M * H, at<float>(S, L.h1));
+  WS_TRY(cudaGetLastError());
+  k_rmsnorm_fwd<<<(unsigned)M, 256, 0, st>>>(at<float>(S, L.h1), H, x.c.eps, at<uint16_t>(S, L.b),
+                                            at<float>(S, L.rstd2));
+  WS_TRY(cudaGetLastError());
+  WS_TRY(lin(WS_LIN_GATE, at<uint16_t>(S, L.b), at<uint16_t>(S, L.g)));
+  WS_TRY(lin(WS_LIN_UP, at<uint16_t>(S, L.b), at<uint16_t>(S, L.u)));
+  k_silu_mul_fwd<<<nblk(M * I), 256, 0, st>>>(at<uint16_t>(S, L.g), at<uint16_t>(S, L.u), M * I,
+                                              at<uint16_t>(S, L.act));
+  WS_TRY(cudaGetLastError());
+  WS_TRY(lin(WS_LIN_DOWN, at<uint16_t>(S, L.act), y));
+  k_add_bf16<<<nblk(M * H), 256, 0, st>>>(at<float>(S, L.h1), y, M * H, h_out);
+  return cudaGetLastError();
+}
+
+// Backward of one layer from its saved slot S; dh holds the gradient at
+// the layer output on entry and at the layer input on exit.
+cudaError_t layer_bwd(const Ctx& x, const void* block, int lib, int layer, const float* params,
+                      uint32_t step, const uint8_t* S, float* dh, float* grads) {
+  const int64_t M = x.c.M, H = x.c.H, KV = x.c.KV, I = x.c.I;
+  const SavedLayout& L = x.SL;
+  cudaStream_t st = x.st;
+  uint8_t* ws = static_cast<uint8_t*>(x.ws);
+  void* lws = ws + x.WSL.lin;
+  const float* P = params + (int64_t)layer * x.PL.layer_floats;
+  float* Gd = grads + (int64_t)layer * x.PL.layer_floats;
+  auto lin = [&](int li, const uint16_t* in, const uint16_t* dY, float* dX, int accum) {
+    return linear_bwd(wview(x, block, lib, li), in, P + x.PL.A[li], P + x.PL.B[li], M, x.scale,
+                      key_of(x, step, layer, li), at<const float>(S, L.U[li]),
+                      at<const uint32_t>(S, L.mask[li]), dY, dX, 1, accum, Gd + x.PL.A[li],
+                      Gd + x.PL.B[li], lws, st);
+  };
+  uint16_t* y1 = at<uint16_t>(ws, x.WSL.y1);
+  float* dact = at<float>(ws, x.WSL.dact);
+  uint16_t* dg = at<uint16_t>(ws, x.WSL.dg);
+  uint16_t* du = at<uint16_t>(ws, x.WSL.du);
+  float* db = at<float>(ws, x.WSL.db);
+  float* dvr = at<float>(ws, x.WSL.dvr);
+  uint16_t* dv = at<uint16_t>(ws, x.WSL.dv);
+
+  k_cast_bf16<<<nblk(M * H), 256, 0, st>>>(dh, M * H, y1);
+  WS_TRY(cudaGetLastError());
+  WS_TRY(lin(WS_LIN_DOWN, at<const uint16_t>(S, L.act), y1, dact, 0));
+  k_silu_mul_bwd<<<nblk(M * I), 256, 0, st>>>(dact, at<const uint16_t>(S, L.g),
+                                              at<const uint16_t>(S, L.u), M * I, dg, du);
+  WS_TRY(cudaGetLastError());
+  WS_TRY(lin(WS_LIN_GATE, at<const uint16_t>(S, L.b), dg, db, 0));
+  WS_TRY(lin(WS_LIN_UP, at<const uint16_t>(S, L.b), du, db, 1));
+  k_rmsnorm_bwd<<<(unsigned)M, 256, 0, st>>>(at<const float>(S, L.h1), at<const float>(S, L.rstd2),
+                                             db, H, dh);
+  WS_TRY(cudaGetLastError());
+  k_cast_bf16<<<nblk(M * H), 256, 0, st>>>(dh, M * H, y1);
+  WS_TRY(cudaGetLastError());
+  WS_TRY(lin(WS_LIN_O, at<const uint16_t>(S, L.vr), y1, dvr, 0));
+  k_repeat_bwd<<<nblk(M * KV), 256, 0, st>>>(dvr, M, H, KV, x.c.head_dim, dv);
+  WS_TRY(cudaGetLastError());
+  WS_TRY(lin(WS_LIN_V, at<const uint16_t>(S, L.a), dv, db, 0));
+  k_rmsnorm_bwd<<<(unsigned)M, 256, 0, st>>>(at<const float>(S, L.h), at<const float>(S, L.rstd1),
+                                             db, H, dh);
+  WS_TRY(cudaGetLastError());
+  // q and k feed only the replaced attention core: exactly zero gradient
+  for (int li : {WS_LIN_Q, WS_LIN_K}) {
+    WS_TRY(cudaMemsetAsync(Gd + x.PL.A[li], 0, sizeof(float) * 16 * (size_t)x.s.K[li], st));
+    WS_TRY(cudaMemsetAsync(Gd + x.PL.B[li], 0, sizeof(float) * 16 * (size_t)x.s.N[li], st));
+  }
+  return cudaSuccess;
+}
+
+Ctx make_ctx(const ws_stack_cfg& c, int block_layers, void* ws, cudaStream_t st) {
+  Ctx x;
+  x.c = c;
+  x.s = shapes_of(c);
+  x.SL = saved_layout(c);
+  x.WL = weight_layout(c);
+  x.PL = param_layout(c);
+  x.WSL = ws_layout(c, block_layers);
+  x.scale = (float)(((double)c.alpha / (double)c.r) / (1.0 - c.p));
+  x.st = st;
+  x.ws = ws;
+  return x;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------- host API
+ws_status stack_check(const ws_stack_cfg* c) {
+  if (!c) return WS_ERR_INVALID;
+  if (c->M < 1 || c->H < 64 || c->KV < 64 || c->I < 64 || c->head_dim < 1 || c->n_layers < 1)
+    return WS_ERR_SHAPE;
+  if (c->H % 64 || c->KV % 64 || c->I % 64) return WS_ERR_SHAPE;
+  if (c->H % c->KV || c->H % c->head_dim || c->KV % c->head_dim) return WS_ERR_SHAPE;
+  if (c->r != 16) return WS_ERR_SHAPE;
+  if (!(c->p >= 0.0 && c->p < 1.0)) return WS_ERR_INVALID;
+  if ((double)c->M * (double)c->I >= 17179869184.0) return WS_ERR_SHAPE;
+  return WS_OK;
+}
+
+size_t stack_block_bytes(const ws_stack_cfg& c, int bl) { return (size_t)bl * weight_layout(c).layer_bytes; }
+int64_t stack_n_params(const ws_stack_cfg& c) { return (int64_t)c.n_layers * param_layout(c).layer_floats; }
+size_t stack_saved_layer(const ws_stack_cfg& c) { return saved_layout(c).total; }
+size_t stack_ws_bytes(const ws_stack_cfg& c, int bl) { return ws_layout(c, bl).total; }
+void stack_weight_offset(const ws_stack_cfg& c, int lib, int lin, size_t* oc, size_t* oa) {
+  const WeightLayout L = weight_layout(c);
+  *oc = (size_t)lib * L.layer_bytes + L.codes[lin];
+  *oa = (size_t)lib * L.layer_bytes + L.absmax[lin];
+}
+void stack_param_offset(const ws_stack_cfg& c, int layer, int lin, int64_t* oA, int64_t* oB) {
+  const ParamLayout L = param_layout(c);
+  *oA = (int64_t)layer * L.layer_floats + L.A[lin];
+  *oB = (int64_t)layer * L.layer_floats + L.B[lin];
+}
+
+cudaError_t block_forward(const ws_stack_cfg& c, int block_layers_ws, const void* block,
+                          int first_layer, int n_layers, const float* params, uint32_t step,
+                          const float* h_in, float* h_out, void* saved, void* ws, cudaStream_t st) {
+  const Ctx x = make_ctx(c, block_layers_ws, ws, st);
+  uint8_t* blk_area = static_cast<uint8_t*>(ws) + x.WSL.blk;
+  // Layer i works in slot S_i: the caller's saved area (kept for the
+  // backward) or, when nothing is kept, one reused workspace slot.  Layer i
+  // reads its input from S_i.h and writes its output into S_{i+1}.h; with a
+  // single reused slot that overwrite happens after the layer's last read of
+  // its input.
+  auto slot = [&](int i) {
+    return saved ? static_cast<uint8_t*>(saved) + (size_t)i * x.SL.total : blk_area;
+  };
+  for (int i = 0; i < n_layers; ++i) {
+    uint8_t* S = slot(i);
+    const float* src = i == 0 ? h_in : at<float>(S, x.SL.h);
+    float* dst = i == n_layers - 1 ? h_out : at<float>(slot(i + 1), x.SL.h);
+    WS_TRY(layer_fwd(x, block, i, first_layer + i, params, step, src, dst, S, true));
+  }
+  return cudaSuccess;
+}
+
+cudaError_t block_backward(const ws_stack_cfg& c, int block_layers_ws, const void* block,
+                           int first_layer, int n_layers, const float* params, uint32_t step,
+                           const float* h_in, const void* saved, const float* dh_out, float* dh_in,
+                           float* grads, void* ws, cudaStream_t st) {
+  const Ctx x = make_ctx(c, block_layers_ws, ws, st);
+  const int64_t MH = c.M * c.H;
+  const uint8_t* area = static_cast<const uint8_t*>(saved);
+  if (!saved) {
+    // recompute the block forward from its boundary activation, keeping
+    // every layer's intermediates in the workspace block area
+    uint8_t* blk = static_cast<uint8_t*>(ws) + x.WSL.blk;
+    for (int i = 0; i < n_layers; ++i) {
+      uint8_t* S = blk + (size_t)i * x.SL.total;
+      const float* src = i == 0 ? h_in : at<float>(S, x.SL.h);
+      float* dst;
+      if (i == n_layers - 1) dst = at<float>(static_cast<uint8_t*>(ws) + x.WSL.dvr, 0);  // unused output
+      else dst = at<float>(blk + (size_t)(i + 1) * x.SL.total, x.SL.h);
+      WS_TRY(layer_fwd(x, block, i, first_layer + i, params, step, src, dst, S, false));
+    }
+    area = blk;
+  }
+  if (dh_in != dh_out)
+    WS_TRY(cudaMemcpyAsync(dh_in, dh_out, (size_t)MH * 4, cudaMemcpyDeviceToDevice, st));
+  for (int i = n_layers - 1; i >= 0; --i)
+    WS_TRY(layer_bwd(x, block, i, first_layer + i, params, step, area + (size_t)i * x.SL.total, dh_in,
+                     grads));
+  return cudaSuccess;
+}
+
+cudaError_t loss_and_grad(const ws_stack_cfg& c, int block_layers_ws, const float* h, float* dh,
+                          float* loss, void* ws, cudaStream_t st) {
+  const WsLayout L = ws_layout(c, block_layers_ws);
+  const int64_t n = c.M * c.H;
+  float* part = at<float>(ws, L.lossp);
+  const float inv_n = (float)(1.0 / (double)n);
+  k_loss_partial<<<kLossBlocks, 256, 0, st>>>(h, n, part, dh, inv_n);
+  WS_TRY(cudaGetLastError());
+  k_loss_final<<<1, 32, 0, st>>>(part, inv_n, loss);
+  return cudaGetLastError();
+}
+
+cudaError_t adam_step(float* p, const float* g, float* m, float* v, int64_t n, int64_t t, float lr,
+                      cudaStream_t st) {
+  const double b1 = 0.9, b2 = 0.999;
+  const double bc1 = 1.0 - pow(b1, (double)t), bc2 = 1.0 - pow(b2, (double)t);
+  k_adam<<<nblk(n), 256, 0, st>>>(p, g, m, v, n, (float)b1, (float)b2, 1e-8f, (float)(lr / bc1),
+                                  (float)sqrt(bc2));
+  return cudaGetLastError();
+}
+
+}  // namespace ws

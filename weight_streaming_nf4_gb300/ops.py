@@ -1,0 +1,296 @@
+"""Thin ctypes binding of libwsnf4.so (C ABI in include/wsnf4.h).
+
+Argument marshalling only: every function here forwards torch tensors'
+device pointers and the current CUDA stream to the entry point of the same
+name (without the ``ws_`` prefix) and raises ``WsError`` on a non-zero
+status.  PyTorch provides device memory, pinned host memory and streams;
+all arithmetic runs in the library's CUDA kernels.  Importing this module
+loads the library and fails loudly if it has not been built -- there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import dataclasses
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libwsnf4.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`"
+        " (nvcc, sm_103a); there is no non-CUDA fallback")
+_lib = C.CDLL(LIB_PATH)
+
+P = C.c_void_p
+i32, i64, u32, u64 = C.c_int32, C.c_int64, C.c_uint32, C.c_uint64
+
+WS_DTYPE_BF16, WS_DTYPE_F32 = 0, 1
+LIN = dict(q=0, k=1, v=2, o=3, gate=4, up=5, down=6)
+LIN_NAMES = ("q", "k", "v", "o", "gate", "up", "down")
+
+
+class WsError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        msg = _lib.ws_status_string(status).decode()
+        super().__init__(f"{fn}: {msg} ({status})")
+
+
+class Nf4(C.Structure):
+    _fields_ = [("codes", P), ("absmax", P), ("N", i64), ("K", i64)]
+
+
+class DropoutKey(C.Structure):
+    _fields_ = [("seed", u64), ("step", u32), ("layer", u32), ("linear", u32),
+                ("microbatch", u32), ("p", C.c_double)]
+
+
+class LoraShape(C.Structure):
+    _fields_ = [("M", i64), ("N", i64), ("K", i64), ("r", i32), ("alpha", C.c_float)]
+
+
+class StackCfgC(C.Structure):
+    _fields_ = [("M", i64), ("H", i64), ("KV", i64), ("I", i64), ("head_dim", i64),
+                ("n_layers", i32), ("r", i32), ("alpha", C.c_float), ("p", C.c_double),
+                ("eps", C.c_float), ("seed", u64)]
+
+
+class StackBuffersC(C.Structure):
+    _fields_ = [("host_weights", P), ("dev_weights", P), ("window", P), ("params", P),
+                ("grads", P), ("adam_m", P), ("adam_v", P), ("boundary", P), ("saved", P),
+                ("dh", P), ("workspace", P), ("workspace_bytes", C.c_size_t), ("loss", P)]
+
+
+def _sig(name, args):
+    f = getattr(_lib, name)
+    f.restype = i32
+    f.argtypes = args
+    return f
+
+
+_lib.ws_status_string.restype = C.c_char_p
+_lib.ws_status_string.argtypes = [i32]
+_sig("ws_device_error", [C.POINTER(u32)])
+_sig("ws_quantize_nf4", [P, i64, i64, P, P, P])
+_sig("ws_lora_workspace_size", [LoraShape, C.POINTER(C.c_size_t)])
+_sig("ws_lora_linear_fwd", [C.POINTER(Nf4), P, P, P, LoraShape, DropoutKey, P, P, P, P,
+                            C.c_size_t, P])
+_sig("ws_lora_linear_bwd", [C.POINTER(Nf4), P, P, P, LoraShape, DropoutKey, P, P, P, P, i32,
+                            i32, P, P, P, C.c_size_t, P])
+_sig("ws_stack_sizes", [C.POINTER(StackCfgC), i32, C.POINTER(C.c_size_t), C.POINTER(i64),
+                        C.POINTER(C.c_size_t), C.POINTER(C.c_size_t)])
+_sig("ws_stack_weight_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(C.c_size_t),
+                                C.POINTER(C.c_size_t)])
+_sig("ws_stack_param_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(i64), C.POINTER(i64)])
+_sig("ws_block_forward", [C.POINTER(StackCfgC), P, i32, i32, P, u32, P, P, P, P, C.c_size_t, P])
+_sig("ws_block_backward_recompute", [C.POINTER(StackCfgC), P, i32, i32, P, u32, P, P, P, P, P,
+                                     P, C.c_size_t, P])
+_sig("ws_stream_block_h2d", [P, P, C.c_size_t, P, P, P])
+_sig("ws_stack_train_step", [C.POINTER(StackCfgC), i32, i32, C.POINTER(StackBuffersC), u32, P,
+                             C.c_float, P, P])
+
+EXPORTED = ("ws_status_string", "ws_device_error", "ws_quantize_nf4", "ws_lora_workspace_size",
+            "ws_lora_linear_fwd", "ws_lora_linear_bwd", "ws_stack_sizes",
+            "ws_stack_weight_offset", "ws_stack_param_offset", "ws_block_forward",
+            "ws_block_backward_recompute", "ws_stream_block_h2d", "ws_stack_train_step")
+
+
+def _check(fn, st):
+    if st != 0:
+        raise WsError(fn, st)
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def status_string(st: int) -> str:
+    return _lib.ws_status_string(st).decode()
+
+
+def device_error() -> int:
+    """Reads and clears the device error word (0 = no kernel timed out)."""
+    f = u32(0)
+    st = _lib.ws_device_error(C.byref(f))
+    if st not in (0, -5):
+        raise WsError("ws_device_error", st)
+    return int(f.value)
+
+
+# ------------------------------------------------------------------------------ a0
+def quantize_nf4(W: torch.Tensor, codes: torch.Tensor = None, absmax: torch.Tensor = None,
+                 stream=None):
+    """W: bf16 [N, K] (device) -> (codes uint8 [N, K/2], absmax fp32 [K/64, N])."""
+    N, K = W.shape
+    if codes is None:
+        codes = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
+    if absmax is None:
+        absmax = torch.empty((K // 64, N), dtype=torch.float32, device=W.device)
+    _check("ws_quantize_nf4", _lib.ws_quantize_nf4(_ptr(W), N, K, _ptr(codes), _ptr(absmax),
+                                                   _stream(stream)))
+    return codes, absmax
+
+
+# ------------------------------------------------------------------------------ linear
+@dataclasses.dataclass
+class NF4Weight:
+    codes: torch.Tensor   # uint8 [N, K/2]
+    absmax: torch.Tensor  # fp32 [K/64, N]
+    N: int
+    K: int
+
+    def c(self):
+        return Nf4(self.codes.data_ptr(), self.absmax.data_ptr(), self.N, self.K)
+
+
+def dropout_key(seed=0, step=0, layer=0, linear=0, microbatch=0, p=0.1):
+    return DropoutKey(seed, step, layer, linear, microbatch, float(p))
+
+
+def lora_workspace_size(M, N, K, r=16) -> int:
+    n = C.c_size_t(0)
+    _check("ws_lora_workspace_size",
+           _lib.ws_lora_workspace_size(LoraShape(M, N, K, r, 32.0), C.byref(n)))
+    return int(n.value)
+
+
+def lora_linear_fwd(W: NF4Weight, x, A, B, key: DropoutKey, alpha=32.0, y=None, U=None,
+                    mask=None, workspace=None, stream=None, keep_mask=True):
+    M, K = x.shape
+    sh = LoraShape(M, W.N, W.K, A.shape[0], alpha)
+    dev = x.device
+    if y is None:
+        y = torch.empty((M, W.N), dtype=torch.bfloat16, device=dev)
+    if U is None:
+        U = torch.empty((M, A.shape[0]), dtype=torch.float32, device=dev)
+    if mask is None and keep_mask:
+        mask = torch.empty((M, K // 32), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(lora_workspace_size(M, W.N, W.K), dtype=torch.uint8, device=dev)
+    w = W.c()
+    _check("ws_lora_linear_fwd",
+           _lib.ws_lora_linear_fwd(C.byref(w), _ptr(x), _ptr(A), _ptr(B), sh, key, _ptr(y),
+                                   _ptr(U), _ptr(mask), _ptr(workspace), workspace.numel(),
+                                   _stream(stream)))
+    return y, U, mask
+
+
+def lora_linear_bwd(W: NF4Weight, x, A, B, key: DropoutKey, U, mask, dY, alpha=32.0,
+                    dX=None, dX_f32=False, accumulate=False, dA=None, dB=None, workspace=None,
+                    stream=None):
+    M, K = x.shape
+    sh = LoraShape(M, W.N, W.K, A.shape[0], alpha)
+    dev = x.device
+    if dX is None:
+        dX = torch.empty((M, K), dtype=torch.float32 if dX_f32 else torch.bfloat16, device=dev)
+    if dA is None:
+        dA = torch.empty_like(A)
+    if dB is None:
+        dB = torch.empty_like(B)
+    if workspace is None:
+        workspace = torch.empty(lora_workspace_size(M, W.N, W.K), dtype=torch.uint8, device=dev)
+    w = W.c()
+    dt = WS_DTYPE_F32 if dX.dtype == torch.float32 else WS_DTYPE_BF16
+    _check("ws_lora_linear_bwd",
+           _lib.ws_lora_linear_bwd(C.byref(w), _ptr(x), _ptr(A), _ptr(B), sh, key, _ptr(U),
+                                   _ptr(mask), _ptr(dY), _ptr(dX), dt, 1 if accumulate else 0,
+                                   _ptr(dA), _ptr(dB), _ptr(workspace), workspace.numel(),
+                                   _stream(stream)))
+    return dX, dA, dB
+
+
+# ------------------------------------------------------------------------------ stack
+@dataclasses.dataclass
+class StackCfg:
+    M: int
+    H: int
+    KV: int
+    I: int
+    head_dim: int
+    n_layers: int
+    r: int = 16
+    alpha: float = 32.0
+    p: float = 0.1
+    eps: float = 1e-6
+    seed: int = 0
+
+    def c(self):
+        return StackCfgC(self.M, self.H, self.KV, self.I, self.head_dim, self.n_layers, self.r,
+                         self.alpha, self.p, self.eps, self.seed)
+
+    def shapes(self):
+        H, KV, I = self.H, self.KV, self.I
+        return [(H, H), (KV, H), (KV, H), (H, H), (I, H), (I, H), (H, I)]
+
+
+def stack_sizes(cfg: StackCfg, block_layers: int):
+    bb, npar, sl, wsb = C.c_size_t(0), i64(0), C.c_size_t(0), C.c_size_t(0)
+    c = cfg.c()
+    _check("ws_stack_sizes", _lib.ws_stack_sizes(C.byref(c), block_layers, C.byref(bb),
+                                                 C.byref(npar), C.byref(sl), C.byref(wsb)))
+    return dict(block_bytes=int(bb.value), n_params=int(npar.value), saved_layer=int(sl.value),
+                workspace=int(wsb.value))
+
+
+def stack_weight_offset(cfg: StackCfg, layer_in_block: int, lin: int):
+    oc, oa = C.c_size_t(0), C.c_size_t(0)
+    c = cfg.c()
+    _check("ws_stack_weight_offset",
+           _lib.ws_stack_weight_offset(C.byref(c), layer_in_block, lin, C.byref(oc), C.byref(oa)))
+    return int(oc.value), int(oa.value)
+
+
+def stack_param_offset(cfg: StackCfg, layer: int, lin: int):
+    oA, oB = i64(0), i64(0)
+    c = cfg.c()
+    _check("ws_stack_param_offset",
+           _lib.ws_stack_param_offset(C.byref(c), layer, lin, C.byref(oA), C.byref(oB)))
+    return int(oA.value), int(oB.value)
+
+
+def block_forward(cfg: StackCfg, block_weights, first_layer, n_layers, params, step, h_in, h_out,
+                  saved, workspace, stream=None):
+    c = cfg.c()
+    _check("ws_block_forward",
+           _lib.ws_block_forward(C.byref(c), _ptr(block_weights), first_layer, n_layers,
+                                 _ptr(params), step, _ptr(h_in), _ptr(h_out), _ptr(saved),
+                                 _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def block_backward_recompute(cfg: StackCfg, block_weights, first_layer, n_layers, params, step,
+                             h_in, saved, dh_out, dh_in, grads, workspace, stream=None):
+    c = cfg.c()
+    _check("ws_block_backward_recompute",
+           _lib.ws_block_backward_recompute(C.byref(c), _ptr(block_weights), first_layer,
+                                            n_layers, _ptr(params), step, _ptr(h_in),
+                                            _ptr(saved), _ptr(dh_out), _ptr(dh_in), _ptr(grads),
+                                            _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def stream_block_h2d(pinned_src: torch.Tensor, dev_dst: torch.Tensor, nbytes: int = None,
+                     copy_stream=None, wait_event=None, done_event=None):
+    """Copies nbytes (default: all of pinned_src) host -> device on copy_stream.
+    Events are raw cudaEvent_t handles (int) or None."""
+    n = pinned_src.numel() * pinned_src.element_size() if nbytes is None else nbytes
+    _check("ws_stream_block_h2d",
+           _lib.ws_stream_block_h2d(_ptr(pinned_src), _ptr(dev_dst), n, _stream(copy_stream),
+                                    C.c_void_p(wait_event) if wait_event else None,
+                                    C.c_void_p(done_event) if done_event else None))
+
+
+def stack_train_step(cfg: StackCfg, block_layers: int, streamed: bool, bufs: StackBuffersC,
+                     step: int, h0, lr: float = 2e-4, stream=None, copy_stream=None):
+    c = cfg.c()
+    _check("ws_stack_train_step",
+           _lib.ws_stack_train_step(C.byref(c), block_layers, 1 if streamed else 0,
+                                    C.byref(bufs), step, _ptr(h0), lr, _stream(stream),
+                                    _stream(copy_stream) if copy_stream is not None else None))
