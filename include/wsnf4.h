@@ -32,8 +32,7 @@
  *    documented as "device" must be device (or managed) memory of the current
  *    CUDA device; "pinned" means cudaHostAlloc'd / registered host memory.
  *  - Execution: all work is enqueued asynchronously on the given stream(s);
- *    no call synchronises the host except ws_stack_train_step when asked to
- *    return the loss (see there).
+ *    no call synchronises the host except ws_device_error.
  *  - Alignment: every device pointer must be 16-byte aligned
  *    (WS_ERR_ALIGN otherwise).
  *  - Shapes: K % 64 == 0 and N % 64 == 0 for NF4 weights; M >= 1;
@@ -121,6 +120,10 @@ const char* ws_status_string(ws_status st);
  * set, WS_OK otherwise. */
 ws_status ws_device_error(uint32_t* flags);
 
+/* Number of CUDA kernels this library has launched in the process so far
+ * (host-side counter; copies are not counted). */
+uint64_t ws_kernel_launches(void);
+
 /* ---- a0: NF4 quantisation ------------------------------------------------- */
 /* Quantises a bf16 weight W [N, K] (device) into NF4 codes [N, K/2] and
  * block-major absmax [K/64, N] (device, caller-allocated).
@@ -174,6 +177,19 @@ ws_status ws_lora_linear_bwd(const ws_nf4* W, const uint16_t* x, const float* A,
                              int32_t dX_accumulate, float* dA, float* dB,
                              void* workspace, size_t ws_bytes, ws_stream_t stream);
 
+/* ---- the frozen NF4 product alone ---------------------------------------------- */
+/* The dequant GEMM of a2 / a4 without adapter or dropout (a frozen NF4
+ * linear):
+ *   transpose_w == 0:  out[M,N] = act[M,K] W'^T   (forward)
+ *   transpose_w != 0:  out[M,K] = act[M,N] W'     (input gradient)
+ * act bf16 (device); out bf16 or fp32 (out_dtype) (device); workspace >=
+ * ws_nf4_matmul_workspace_size() (device scratch for contraction splits). */
+ws_status ws_nf4_matmul_workspace_size(int64_t M, int64_t N, int64_t K, int32_t transpose_w,
+                                       size_t* bytes);
+ws_status ws_nf4_matmul(const ws_nf4* W, const uint16_t* act, int64_t M, int32_t transpose_w,
+                        void* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
+                        ws_stream_t stream);
+
 /* ---- the synthetic stack ----------------------------------------------------- */
 /* One layer: h -> RMSNorm -> q,k,v (NF4-LoRA) -> v repeated across the
  * H/head_dim query heads (head h reads kv head h / (H/KV)) in place of the
@@ -208,6 +224,22 @@ ws_status ws_stack_sizes(const ws_stack_cfg* cfg, int32_t block_layers,
  * codes at byte *off_codes, absmax at byte *off_absmax (both 256-aligned). */
 ws_status ws_stack_weight_offset(const ws_stack_cfg* cfg, int32_t layer_in_block, int32_t lin,
                                  size_t* off_codes, size_t* off_absmax);
+
+/* Activations one layer keeps for its backward (the `saved` areas of
+ * ws_block_forward / ws_stack_buffers, one slot of saved_bytes_layer per
+ * layer): the layer input h [M,H] fp32, a = RMSNorm(h) [M,H] bf16, rstd1 [M]
+ * fp32, v [M,KV] bf16, vr = repeat(v) [M,H] bf16, h1 = h + o [M,H] fp32,
+ * b = RMSNorm(h1) [M,H] bf16, rstd2 [M] fp32, gate and up outputs [M,I]
+ * bf16, act = SiLU(gate)*up [M,I] bf16, and per linear its U [M,16] fp32 and
+ * dropout mask [M,K/32] uint32. */
+enum { WS_SV_H = 0, WS_SV_A = 1, WS_SV_RSTD1 = 2, WS_SV_V = 3, WS_SV_VR = 4, WS_SV_H1 = 5,
+       WS_SV_B = 6, WS_SV_RSTD2 = 7, WS_SV_GATE = 8, WS_SV_UP = 9, WS_SV_ACT = 10,
+       WS_SV_LORA_U = 11, WS_SV_MASK = 12 };
+
+/* Byte offset of field `field` (for WS_SV_LORA_U / WS_SV_MASK: of linear
+ * `lin`) inside one layer's saved slot. */
+ws_status ws_stack_saved_offset(const ws_stack_cfg* cfg, int32_t field, int32_t lin,
+                                size_t* offset);
 
 /* Offsets (in floats) of A [r, K] and B [N, r] of (layer, lin) in the
  * parameter arrays (params, grads and both Adam moments share the layout). */

@@ -27,5 +27,8 @@ from .binding import (  # noqa: F401
     StackCfg,
     stack_fwd_bwd,
     adam_step,
+    rmsnorm_bf16,
+    silu_mul_bf16,
+    repeat_kv,
     LIN_NAMES,
 )

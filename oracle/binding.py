@@ -62,6 +62,9 @@ def lib():
         L.orc_adam_step.argtypes = [i64, P, P, P, P, i64, C.c_double, C.c_double,
                                     C.c_double, C.c_double]
         L.orc_num_threads.restype = C.c_int
+        L.orc_rmsnorm_bf16.argtypes = [i64, i64, C.c_double, P, P, P]
+        L.orc_silu_mul_bf16.argtypes = [i64, P, P, P]
+        L.orc_repeat_kv.argtypes = [i64, i64, i64, i64, P, P]
         _lib = L
     return _lib
 
@@ -253,6 +256,32 @@ def stack_fwd_bwd(cfg: StackCfg, step: int, Wq, A, B, h0, backward=True):
     L.orc_stack_fwd_bwd(C.byref(cc), step, C.byref(prm), _p(h0), C.byref(loss), _p(h_out),
                         pdA, pdB)
     return loss.value, h_out, dA, dB
+
+
+def rmsnorm_bf16(x, eps=1e-6):
+    """x: [M, H] float -> (bf16 bits [M, H], rstd [M])."""
+    x = _c(x, np.float64)
+    M, H = x.shape
+    y = np.empty((M, H), np.uint16)
+    rstd = np.empty(M, np.float64)
+    lib().orc_rmsnorm_bf16(M, H, eps, _p(x), _p(y), _p(rstd))
+    return y, rstd
+
+
+def silu_mul_bf16(g, u):
+    g = _c(g, np.uint16)
+    u = _c(u, np.uint16)
+    act = np.empty_like(g)
+    lib().orc_silu_mul_bf16(g.size, _p(g), _p(u), _p(act))
+    return act
+
+
+def repeat_kv(v, H, head_dim):
+    v = _c(v, np.uint16)
+    M, KV = v.shape
+    vr = np.empty((M, H), np.uint16)
+    lib().orc_repeat_kv(M, H, KV, head_dim, _p(v), _p(vr))
+    return vr
 
 
 def adam_step(p, g, m, v, t, lr=2e-4, beta1=0.9, beta2=0.999, eps=1e-8):

@@ -595,6 +595,36 @@ void orc_stack_fwd_bwd(const orc_stack_cfg* c, uint32_t step,
   free(scratch);
 }
 
+/* ---- stack pieces on their own ------------------------------------------------ */
+void orc_rmsnorm_bf16(int64_t M, int64_t H, double eps, const double* x, uint16_t* y,
+                      double* rstd) {
+  orc_stack_cfg c;
+  memset(&c, 0, sizeof(c));
+  c.M = M;
+  c.eps = eps;
+  c.round_bf16 = 1;
+  double* out = (double*)malloc(sizeof(double) * M * H);
+  rmsnorm_fwd(&c, H, x, out, rstd);
+  for (int64_t i = 0; i < M * H; ++i) y[i] = orc_f64_to_bf16(out[i]);
+  free(out);
+}
+
+void orc_silu_mul_bf16(int64_t n, const uint16_t* g, const uint16_t* u, uint16_t* act) {
+  for (int64_t i = 0; i < n; ++i) {
+    double gv = bf(g[i]);
+    act[i] = orc_f64_to_bf16(gv * sigmoid(gv) * bf(u[i]));
+  }
+}
+
+void orc_repeat_kv(int64_t M, int64_t H, int64_t KV, int64_t head_dim, const uint16_t* v,
+                   uint16_t* vr) {
+  const int64_t rep = H / KV;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t hh = 0; hh < H / head_dim; ++hh)
+      for (int64_t d = 0; d < head_dim; ++d)
+        vr[m * H + hh * head_dim + d] = v[m * KV + (hh / rep) * head_dim + d];
+}
+
 /* ---- Adam -------------------------------------------------------------------- */
 void orc_adam_step(int64_t n, double* p, const double* g, double* m, double* v,
                    int64_t t, double lr, double beta1, double beta2,

@@ -122,6 +122,16 @@ void orc_stack_fwd_bwd(const orc_stack_cfg* cfg, uint32_t step,
                        double* loss, double* h_out,
                        double* const* dA, double* const* dB);
 
+/* The stack's pointwise / row pieces on their own (x in double):
+ * RMSNorm with unit gain -> bf16 bits, rstd per row;
+ * act = bf16(SiLU(g) * u) for bf16 g, u;
+ * repeat of kv heads: vr[m, hh*hd + d] = v[m, (hh / (H/KV))*hd + d]. */
+void orc_rmsnorm_bf16(int64_t M, int64_t H, double eps, const double* x, uint16_t* y,
+                      double* rstd);
+void orc_silu_mul_bf16(int64_t n, const uint16_t* g, const uint16_t* u, uint16_t* act);
+void orc_repeat_kv(int64_t M, int64_t H, int64_t KV, int64_t head_dim, const uint16_t* v,
+                   uint16_t* vr);
+
 /* PyTorch-default Adam (betas 0.9/0.999, eps 1e-8, no weight decay,
  * bias-corrected), one step t >= 1, in double. */
 void orc_adam_step(int64_t n, double* p, const double* g, double* m,

@@ -158,3 +158,19 @@ def test_full_size_sampled_rows(ops, orc, M, N, K, lin):
     assert rel(to_f64(y)[rows], yo) <= TOL
     assert rel(to_f64(dX)[rows], dXo) <= TOL
     assert rel(to_f64(dA), dAo) <= TOL and rel(to_f64(dB), dBo) <= TOL
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 512, 512), (300, 896, 1088), (512, 3584, 3584)])
+def test_nf4_matmul_alone(ops, orc, M, N, K):
+    """The frozen product without adapter: x W'^T and dY W'."""
+    d, W, _ = _linear(ops, orc, M, N, K, f"mm{M}")
+    Wq = orc.dequant_nf4(*orc.quantize_nf4(d["W"]))
+    y = ops.nf4_matmul(W, bf16_to_dev(d["x"]))
+    dX = ops.nf4_matmul(W, bf16_to_dev(d["dY"]), transpose_w=True, out_f32=True)
+    torch.cuda.synchronize()
+    zA = np.zeros_like(d["A"])
+    zB = np.zeros_like(d["B"])
+    yo, _ = orc.lora_fwd(d["x"], Wq, zA, zB, None, 0.0)
+    dXo, _, _ = orc.lora_bwd(d["x"], Wq, zA, zB, None, d["dY"], 0.0)
+    assert rel(to_f64(y), yo) <= TOL
+    assert rel(to_f64(dX), dXo) <= 1e-4

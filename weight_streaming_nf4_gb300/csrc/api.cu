@@ -5,10 +5,18 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
 using namespace ws;
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+void ws::note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
 
@@ -62,6 +70,8 @@ const char* ws_status_string(ws_status st) {
     default: return "WS_ERR_UNKNOWN";
   }
 }
+
+uint64_t ws_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 ws_status ws_device_error(uint32_t* flags) {
   if (!flags) return WS_ERR_INVALID;
@@ -124,6 +134,37 @@ ws_status ws_lora_linear_bwd(const ws_nf4* W, const uint16_t* x, const float* A,
                                 workspace, (cudaStream_t)stream));
 }
 
+ws_status ws_nf4_matmul_workspace_size(int64_t M, int64_t N, int64_t K, int32_t transpose_w,
+                                       size_t* bytes) {
+  if (!bytes) return WS_ERR_INVALID;
+  if (M < 1 || N < 64 || K < 64 || N % 64 || K % 64) return WS_ERR_SHAPE;
+  const GemmPlan p = transpose_w ? plan_gemm(true, M, K, N) : plan_gemm(false, M, N, K);
+  *bytes = gemm_partial_bytes(p, M, transpose_w ? K : N);
+  if (*bytes == 0) *bytes = 256;
+  return WS_OK;
+}
+
+ws_status ws_nf4_matmul(const ws_nf4* W, const uint16_t* act, int64_t M, int32_t transpose_w,
+                        void* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
+                        ws_stream_t stream) {
+  if (!W || !W->codes || !W->absmax || !act || !out || !workspace) return WS_ERR_INVALID;
+  if (out_dtype != WS_DTYPE_BF16 && out_dtype != WS_DTYPE_F32) return WS_ERR_INVALID;
+  if (M < 1 || W->N < 64 || W->K < 64 || W->N % 64 || W->K % 64) return WS_ERR_SHAPE;
+  if (M > (int64_t)1 << 30 || W->N > (int64_t)1 << 30 || W->K > (int64_t)1 << 30)
+    return WS_ERR_SHAPE;
+  if (!aligned16(W->codes) || !aligned16(W->absmax) || !aligned16(act) || !aligned16(out) ||
+      !aligned16(workspace))
+    return WS_ERR_ALIGN;
+  size_t need = 0;
+  ws_nf4_matmul_workspace_size(M, W->N, W->K, transpose_w, &need);
+  if (ws_bytes < need) return WS_ERR_OOM;
+  const bool bwd = transpose_w != 0;
+  const GemmPlan p = bwd ? plan_gemm(true, M, W->K, W->N) : plan_gemm(false, M, W->N, W->K);
+  return cuda_status(run_nf4_gemm(p, view_of(W), act, M, nullptr, nullptr, 0.0f, nullptr, out,
+                                  out_dtype == WS_DTYPE_F32 ? 1 : 0, 0,
+                                  static_cast<float*>(workspace), (cudaStream_t)stream));
+}
+
 ws_status ws_stack_sizes(const ws_stack_cfg* cfg, int32_t block_layers, size_t* block_weight_bytes,
                          int64_t* n_params, size_t* saved_bytes_layer, size_t* workspace_bytes) {
   ws_status s = stack_check(cfg);
@@ -144,6 +185,14 @@ ws_status ws_stack_weight_offset(const ws_stack_cfg* cfg, int32_t layer_in_block
     return WS_ERR_INVALID;
   stack_weight_offset(*cfg, layer_in_block, lin, off_codes, off_absmax);
   return WS_OK;
+}
+
+ws_status ws_stack_saved_offset(const ws_stack_cfg* cfg, int32_t field, int32_t lin,
+                                size_t* offset) {
+  ws_status s = stack_check(cfg);
+  if (s != WS_OK) return s;
+  if (!offset) return WS_ERR_INVALID;
+  return stack_saved_offset(*cfg, field, lin, offset) ? WS_OK : WS_ERR_INVALID;
 }
 
 ws_status ws_stack_param_offset(const ws_stack_cfg* cfg, int32_t layer, int32_t lin,

@@ -44,6 +44,8 @@ struct GemmPlan {
 };
 
 int device_sm_count();
+// Counts every kernel launch the library makes (reported by ws_kernel_launches).
+void note_launch();
 cudaError_t read_and_clear_dev_error(uint32_t* flags);
 GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc);
 size_t gemm_partial_bytes(const GemmPlan& p, int64_t M, int64_t Nout);
@@ -102,6 +104,7 @@ size_t stack_ws_bytes(const ws_stack_cfg& c, int block_layers);
 void stack_weight_offset(const ws_stack_cfg& c, int layer_in_block, int lin, size_t* off_codes,
                          size_t* off_absmax);
 void stack_param_offset(const ws_stack_cfg& c, int layer, int lin, int64_t* off_A, int64_t* off_B);
+bool stack_saved_offset(const ws_stack_cfg& c, int field, int lin, size_t* off);
 cudaError_t block_forward(const ws_stack_cfg& c, int block_layers_ws, const void* block,
                           int first_layer, int n_layers, const float* params, uint32_t step,
                           const float* h_in, float* h_out, void* saved, void* ws, cudaStream_t st);

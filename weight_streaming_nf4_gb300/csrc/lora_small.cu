@@ -319,6 +319,7 @@ cudaError_t run_quantize_nf4(const uint16_t* W, int64_t N, int64_t K, uint8_t* c
                              float* absmax, cudaStream_t st) {
   const int64_t blocks = N * (K / 64);
   const int per = 8;  // warps per CTA
+  note_launch();
   k_quantize_nf4<<<(unsigned)((blocks + per - 1) / per), 32 * per, 0, st>>>(W, N, K, codes, absmax);
   return cudaGetLastError();
 }
@@ -326,6 +327,7 @@ cudaError_t run_quantize_nf4(const uint16_t* W, int64_t N, int64_t K, uint8_t* c
 cudaError_t run_lora_down(const uint16_t* x, const float* A, int64_t M, int64_t K,
                           const DropKeyHost& key, float* U, uint16_t* Uext, uint32_t* mask_out,
                           cudaStream_t st) {
+  note_launch();
   k_lora_down<<<(unsigned)((M + kDownRows - 1) / kDownRows), 256, 0, st>>>(
       x, A, M, K, to_dev(key), U, Uext, reinterpret_cast<uint8_t*>(mask_out));
   return cudaGetLastError();
@@ -333,6 +335,7 @@ cudaError_t run_lora_down(const uint16_t* x, const float* A, int64_t M, int64_t 
 
 cudaError_t run_lora_G(const uint16_t* dY, const float* B, int64_t M, int64_t N, float* G,
                        uint16_t* Gext, cudaStream_t st) {
+  note_launch();
   k_lora_G<<<(unsigned)((M + kDownRows - 1) / kDownRows), 256, 0, st>>>(dY, B, M, N, G, Gext);
   return cudaGetLastError();
 }
@@ -347,10 +350,12 @@ cudaError_t run_lora_wgrad(const float* P, const uint16_t* Q, const uint32_t* ma
   const int chunks = wgrad_chunks(M, C);
   const int rpc = (int)((M + chunks - 1) / chunks);
   dim3 grid((unsigned)((C + kWgradCols - 1) / kWgradCols), (unsigned)chunks);
+  note_launch();
   k_wgrad_partial<<<grid, kWgradCols, 0, st>>>(P, Q, mask, M, C, rpc, partial);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t n = C * 16;
+  note_launch();
   k_wgrad_reduce<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(partial, chunks, C, s, out,
                                                               transpose_out);
   return cudaGetLastError();
@@ -359,6 +364,7 @@ cudaError_t run_lora_wgrad(const float* P, const uint16_t* Q, const uint32_t* ma
 cudaError_t run_mask_gen(int64_t M, int64_t K, const DropKeyHost& key, uint32_t* mask,
                          cudaStream_t st) {
   const int64_t words = M * K / 32;
+  note_launch();
   k_mask_gen<<<(unsigned)((words + 255) / 256), 256, 0, st>>>(words, to_dev(key), mask);
   return cudaGetLastError();
 }

@@ -527,6 +527,7 @@ cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& 
     attr_set = true;
   }
   dim3 grid((unsigned)p.mtiles, (unsigned)p.ntiles, (unsigned)p.splits);
+  note_launch();
   k_nf4_gemm<BWD, UM, BN><<<grid, kThreads, C::SMEM_BYTES, st>>>(tA, tC, tS, tL, a);
   return cudaGetLastError();
 }
@@ -632,6 +633,7 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
   if (p.splits > 1) {
     const int64_t elems = M * Nout;
     const int64_t threads = elems / 4;
+    note_launch();
     k_split_reduce<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(partial, p.splits, elems, out,
                                                                      out_f32, out_accum);
     e = cudaGetLastError();

@@ -344,6 +344,7 @@ cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const
   };
   float* h = at<float>(S, L.h);
   if (h != h_in) WS_TRY(cudaMemcpyAsync(h, h_in, (size_t)M * H * 4, cudaMemcpyDeviceToDevice, st));
+  note_launch();
   k_rmsnorm_fwd<<<(unsigned)M, 256, 0, st>>>(h, H, x.c.eps, at<uint16_t>(S, L.a), at<float>(S, L.rstd1));
   WS_TRY(cudaGetLastError());
   if (with_qk) {
@@ -351,22 +352,27 @@ cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const
     WS_TRY(lin(WS_LIN_K, at<uint16_t>(S, L.a), at<uint16_t>(ws, x.WSL.kout)));
   }
   WS_TRY(lin(WS_LIN_V, at<uint16_t>(S, L.a), at<uint16_t>(S, L.v)));
+  note_launch();
   k_repeat_fwd<<<nblk(M * H), 256, 0, st>>>(at<uint16_t>(S, L.v), M, H, KV, x.c.head_dim,
                                             at<uint16_t>(S, L.vr));
   WS_TRY(cudaGetLastError());
   uint16_t* y = at<uint16_t>(ws, x.WSL.yout);
   WS_TRY(lin(WS_LIN_O, at<uint16_t>(S, L.vr), y));
+  note_launch();
   k_add_bf16<<<nblk(M * H), 256, 0, st>>>(h, y, M * H, at<float>(S, L.h1));
   WS_TRY(cudaGetLastError());
+  note_launch();
   k_rmsnorm_fwd<<<(unsigned)M, 256, 0, st>>>(at<float>(S, L.h1), H, x.c.eps, at<uint16_t>(S, L.b),
                                             at<float>(S, L.rstd2));
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_GATE, at<uint16_t>(S, L.b), at<uint16_t>(S, L.g)));
   WS_TRY(lin(WS_LIN_UP, at<uint16_t>(S, L.b), at<uint16_t>(S, L.u)));
+  note_launch();
   k_silu_mul_fwd<<<nblk(M * I), 256, 0, st>>>(at<uint16_t>(S, L.g), at<uint16_t>(S, L.u), M * I,
                                               at<uint16_t>(S, L.act));
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_DOWN, at<uint16_t>(S, L.act), y));
+  note_launch();
   k_add_bf16<<<nblk(M * H), 256, 0, st>>>(at<float>(S, L.h1), y, M * H, h_out);
   return cudaGetLastError();
 }
@@ -396,23 +402,29 @@ cudaError_t layer_bwd(const Ctx& x, const void* block, int lib, int layer, const
   float* dvr = at<float>(ws, x.WSL.dvr);
   uint16_t* dv = at<uint16_t>(ws, x.WSL.dv);
 
+  note_launch();
   k_cast_bf16<<<nblk(M * H), 256, 0, st>>>(dh, M * H, y1);
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_DOWN, at<const uint16_t>(S, L.act), y1, dact, 0));
+  note_launch();
   k_silu_mul_bwd<<<nblk(M * I), 256, 0, st>>>(dact, at<const uint16_t>(S, L.g),
                                               at<const uint16_t>(S, L.u), M * I, dg, du);
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_GATE, at<const uint16_t>(S, L.b), dg, db, 0));
   WS_TRY(lin(WS_LIN_UP, at<const uint16_t>(S, L.b), du, db, 1));
+  note_launch();
   k_rmsnorm_bwd<<<(unsigned)M, 256, 0, st>>>(at<const float>(S, L.h1), at<const float>(S, L.rstd2),
                                              db, H, dh);
   WS_TRY(cudaGetLastError());
+  note_launch();
   k_cast_bf16<<<nblk(M * H), 256, 0, st>>>(dh, M * H, y1);
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_O, at<const uint16_t>(S, L.vr), y1, dvr, 0));
+  note_launch();
   k_repeat_bwd<<<nblk(M * KV), 256, 0, st>>>(dvr, M, H, KV, x.c.head_dim, dv);
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_V, at<const uint16_t>(S, L.a), dv, db, 0));
+  note_launch();
   k_rmsnorm_bwd<<<(unsigned)M, 256, 0, st>>>(at<const float>(S, L.h), at<const float>(S, L.rstd1),
                                              db, H, dh);
   WS_TRY(cudaGetLastError());
@@ -461,6 +473,19 @@ void stack_weight_offset(const ws_stack_cfg& c, int lib, int lin, size_t* oc, si
   const WeightLayout L = weight_layout(c);
   *oc = (size_t)lib * L.layer_bytes + L.codes[lin];
   *oa = (size_t)lib * L.layer_bytes + L.absmax[lin];
+}
+bool stack_saved_offset(const ws_stack_cfg& c, int field, int lin, size_t* off) {
+  const SavedLayout L = saved_layout(c);
+  const size_t f[] = {L.h, L.a, L.rstd1, L.v, L.vr, L.h1, L.b, L.rstd2, L.g, L.u, L.act};
+  if (field >= 0 && field <= WS_SV_ACT) {
+    *off = f[field];
+    return true;
+  }
+  if (lin < 0 || lin >= WS_NLIN) return false;
+  if (field == WS_SV_LORA_U) *off = L.U[lin];
+  else if (field == WS_SV_MASK) *off = L.mask[lin];
+  else return false;
+  return true;
 }
 void stack_param_offset(const ws_stack_cfg& c, int layer, int lin, int64_t* oA, int64_t* oB) {
   const ParamLayout L = param_layout(c);
@@ -525,8 +550,10 @@ cudaError_t loss_and_grad(const ws_stack_cfg& c, int block_layers_ws, const floa
   const int64_t n = c.M * c.H;
   float* part = at<float>(ws, L.lossp);
   const float inv_n = (float)(1.0 / (double)n);
+  note_launch();
   k_loss_partial<<<kLossBlocks, 256, 0, st>>>(h, n, part, dh, inv_n);
   WS_TRY(cudaGetLastError());
+  note_launch();
   k_loss_final<<<1, 32, 0, st>>>(part, inv_n, loss);
   return cudaGetLastError();
 }
@@ -535,6 +562,7 @@ cudaError_t adam_step(float* p, const float* g, float* m, float* v, int64_t n, i
                       cudaStream_t st) {
   const double b1 = 0.9, b2 = 0.999;
   const double bc1 = 1.0 - pow(b1, (double)t), bc2 = 1.0 - pow(b2, (double)t);
+  note_launch();
   k_adam<<<nblk(n), 256, 0, st>>>(p, g, m, v, n, (float)b1, (float)b2, 1e-8f, (float)(lr / bc1),
                                   (float)sqrt(bc2));
   return cudaGetLastError();

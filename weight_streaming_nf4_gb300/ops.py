@@ -75,17 +75,22 @@ def _sig(name, args):
 _lib.ws_status_string.restype = C.c_char_p
 _lib.ws_status_string.argtypes = [i32]
 _sig("ws_device_error", [C.POINTER(u32)])
+_lib.ws_kernel_launches.restype = u64
+_lib.ws_kernel_launches.argtypes = []
 _sig("ws_quantize_nf4", [P, i64, i64, P, P, P])
 _sig("ws_lora_workspace_size", [LoraShape, C.POINTER(C.c_size_t)])
 _sig("ws_lora_linear_fwd", [C.POINTER(Nf4), P, P, P, LoraShape, DropoutKey, P, P, P, P,
                             C.c_size_t, P])
 _sig("ws_lora_linear_bwd", [C.POINTER(Nf4), P, P, P, LoraShape, DropoutKey, P, P, P, P, i32,
                             i32, P, P, P, C.c_size_t, P])
+_sig("ws_nf4_matmul_workspace_size", [i64, i64, i64, i32, C.POINTER(C.c_size_t)])
+_sig("ws_nf4_matmul", [C.POINTER(Nf4), P, i64, i32, P, i32, P, C.c_size_t, P])
 _sig("ws_stack_sizes", [C.POINTER(StackCfgC), i32, C.POINTER(C.c_size_t), C.POINTER(i64),
                         C.POINTER(C.c_size_t), C.POINTER(C.c_size_t)])
 _sig("ws_stack_weight_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(C.c_size_t),
                                 C.POINTER(C.c_size_t)])
 _sig("ws_stack_param_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(i64), C.POINTER(i64)])
+_sig("ws_stack_saved_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(C.c_size_t)])
 _sig("ws_block_forward", [C.POINTER(StackCfgC), P, i32, i32, P, u32, P, P, P, P, C.c_size_t, P])
 _sig("ws_block_backward_recompute", [C.POINTER(StackCfgC), P, i32, i32, P, u32, P, P, P, P, P,
                                      P, C.c_size_t, P])
@@ -93,9 +98,11 @@ _sig("ws_stream_block_h2d", [P, P, C.c_size_t, P, P, P])
 _sig("ws_stack_train_step", [C.POINTER(StackCfgC), i32, i32, C.POINTER(StackBuffersC), u32, P,
                              C.c_float, P, P])
 
-EXPORTED = ("ws_status_string", "ws_device_error", "ws_quantize_nf4", "ws_lora_workspace_size",
-            "ws_lora_linear_fwd", "ws_lora_linear_bwd", "ws_stack_sizes",
-            "ws_stack_weight_offset", "ws_stack_param_offset", "ws_block_forward",
+EXPORTED = ("ws_status_string", "ws_device_error", "ws_kernel_launches", "ws_quantize_nf4", "ws_lora_workspace_size",
+            "ws_lora_linear_fwd", "ws_lora_linear_bwd", "ws_nf4_matmul_workspace_size",
+            "ws_nf4_matmul", "ws_stack_sizes",
+            "ws_stack_weight_offset", "ws_stack_param_offset", "ws_stack_saved_offset",
+            "ws_block_forward",
             "ws_block_backward_recompute", "ws_stream_block_h2d", "ws_stack_train_step")
 
 
@@ -115,6 +122,11 @@ def _stream(stream=None):
 
 def status_string(st: int) -> str:
     return _lib.ws_status_string(st).decode()
+
+
+def kernel_launches() -> int:
+    """Kernels launched by the library in this process so far."""
+    return int(_lib.ws_kernel_launches())
 
 
 def device_error() -> int:
@@ -208,6 +220,32 @@ def lora_linear_bwd(W: NF4Weight, x, A, B, key: DropoutKey, U, mask, dY, alpha=3
     return dX, dA, dB
 
 
+def nf4_matmul_workspace_size(M, N, K, transpose_w=False) -> int:
+    n = C.c_size_t(0)
+    _check("ws_nf4_matmul_workspace_size",
+           _lib.ws_nf4_matmul_workspace_size(M, N, K, 1 if transpose_w else 0, C.byref(n)))
+    return int(n.value)
+
+
+def nf4_matmul(W: NF4Weight, act, transpose_w=False, out=None, out_f32=False, workspace=None,
+               stream=None):
+    """act [M, K] -> act W'^T [M, N]; with transpose_w, act [M, N] -> act W' [M, K]."""
+    M = act.shape[0]
+    cols = W.K if transpose_w else W.N
+    if out is None:
+        out = torch.empty((M, cols), dtype=torch.float32 if out_f32 else torch.bfloat16,
+                          device=act.device)
+    if workspace is None:
+        workspace = torch.empty(nf4_matmul_workspace_size(M, W.N, W.K, transpose_w),
+                                dtype=torch.uint8, device=act.device)
+    w = W.c()
+    dt = WS_DTYPE_F32 if out.dtype == torch.float32 else WS_DTYPE_BF16
+    _check("ws_nf4_matmul", _lib.ws_nf4_matmul(C.byref(w), _ptr(act), M, 1 if transpose_w else 0,
+                                               _ptr(out), dt, _ptr(workspace), workspace.numel(),
+                                               _stream(stream)))
+    return out
+
+
 # ------------------------------------------------------------------------------ stack
 @dataclasses.dataclass
 class StackCfg:
@@ -255,6 +293,18 @@ def stack_param_offset(cfg: StackCfg, layer: int, lin: int):
     _check("ws_stack_param_offset",
            _lib.ws_stack_param_offset(C.byref(c), layer, lin, C.byref(oA), C.byref(oB)))
     return int(oA.value), int(oB.value)
+
+
+SAVED_FIELDS = dict(h=0, a=1, rstd1=2, v=3, vr=4, h1=5, b=6, rstd2=7, gate=8, up=9, act=10,
+                    lora_u=11, mask=12)
+
+
+def stack_saved_offset(cfg: StackCfg, field: str, lin: int = 0) -> int:
+    off = C.c_size_t(0)
+    c = cfg.c()
+    _check("ws_stack_saved_offset",
+           _lib.ws_stack_saved_offset(C.byref(c), SAVED_FIELDS[field], lin, C.byref(off)))
+    return int(off.value)
 
 
 def block_forward(cfg: StackCfg, block_weights, first_layer, n_layers, params, step, h_in, h_out,

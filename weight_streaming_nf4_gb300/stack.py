@@ -17,9 +17,11 @@ from . import ops
 
 class StackRun:
     def __init__(self, cfg: ops.StackCfg, block_layers: int, streamed: bool, weight_fn,
-                 param_fn, device="cuda"):
+                 param_fn, device="cuda", image_from: "StackRun" = None):
         """weight_fn(layer, lin, N, K) -> bf16 [N, K] device tensor (the frozen base);
-        param_fn(layer, lin, N, K) -> (A [16, K], B [N, 16]) fp32 device tensors."""
+        param_fn(layer, lin, N, K) -> (A [16, K], B [N, 16]) fp32 device tensors.
+        image_from: a resident run of the same config whose quantised image is
+        copied instead of quantising again."""
         assert cfg.n_layers % block_layers == 0
         self.cfg, self.bl, self.streamed = cfg, block_layers, streamed
         self.nb = cfg.n_layers // block_layers
@@ -31,6 +33,7 @@ class StackRun:
         f32 = dict(dtype=torch.float32, device=dev)
         # ---- frozen NF4 base, quantised block by block
         stage = torch.empty(bb, dtype=torch.uint8, device=dev)
+        src_img = None if image_from is None else image_from.dev_weights
         if streamed:
             self.host_weights = torch.empty(self.nb * bb, dtype=torch.uint8, pin_memory=True)
             self.window = torch.empty(2 * bb, dtype=torch.uint8, device=dev)
@@ -42,6 +45,11 @@ class StackRun:
         shapes = cfg.shapes()
         for b in range(self.nb):
             img = stage if streamed else self.dev_weights[b * bb:(b + 1) * bb]
+            if src_img is not None:
+                img.copy_(src_img[b * bb:(b + 1) * bb])
+                if streamed:
+                    self.host_weights[b * bb:(b + 1) * bb].copy_(stage)
+                continue
             for li in range(block_layers):
                 layer = b * block_layers + li
                 for lin, (N, K) in enumerate(shapes):
