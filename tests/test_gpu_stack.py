@@ -209,7 +209,7 @@ def test_forward_local_parity(ops, orc):
             assert rel(f(out), ref) <= TOL
         act = field(layer, "act", (M, I), np.uint16)
         assert ulp_close(act, orc.silu_mul_bf16(g, u))
-        h2 = bnd[layer + 1] if layer == cfg.n_layers - 1 else \
+        h2 = bnd[-1] if layer == cfg.n_layers - 1 else \
             field(layer + 1, "h", (M, H), np.float32).astype(np.float64)
         do, _ = orc.lora_fwd(act, Wq[base + 6], As[base + 6], Bs[base + 6],
                              field(layer, "mask", (M, I // 32), np.uint32, 6), s)
