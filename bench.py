@@ -186,7 +186,7 @@ def run_reference(args, rank):
 
 
 # ------------------------------------------------------------------------------ our arm
-def make_runs(ops, StackRun, torch, cfg, dev):
+def make_runs(ops, StackRun, torch, cfg, dev, streamed=True):
     gens = {}
 
     def gen(layer, lin):
@@ -203,7 +203,7 @@ def make_runs(ops, StackRun, torch, cfg, dev):
         B = torch.randn(N, 16, generator=g, device=dev) * 0.01
         return A, B
     res = StackRun(cfg, BLOCK, False, wfn, pfn, device=dev)
-    stm = StackRun(cfg, BLOCK, True, wfn, pfn, device=dev, image_from=res)
+    stm = StackRun(cfg, BLOCK, True, wfn, pfn, device=dev, image_from=res) if streamed else None
     return res, stm
 
 
@@ -393,6 +393,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the 7B sub-benchmark")
+    ap.add_argument("--profile-step", action="store_true",
+                    help="only the resident run: W warm-up steps and one step inside the NVTX "
+                         "range 'timed'; for an ncu launch list of one step")
     ap.add_argument("--profile-gemm", choices=["gate", "down", "o"], default=None,
                     help="only launch the dequant GEMM (forward + input gradient) twice on one "
                          "32B linear shape at M=512; for an ncu capture of that kernel")
@@ -424,6 +427,13 @@ def main():
     flops = step_flops(M, H, cfg.KV, cfg.I, cfg.n_layers)
     t_setup = time.time()
     torch.cuda.reset_peak_memory_stats(dev)
+    if args.profile_step:
+        res, _ = make_runs(ops, StackRun, torch, cfg, dev, streamed=False)
+        h0 = torch.randn(M * H, device=dev)
+        time_steps(torch, None, res, [h0], 1, args.warmup, torch.cuda.current_stream(), nvtx=True)
+        assert ops.device_error() == 0
+        print(json.dumps({"profile_step": "resident", "launches": ops.kernel_launches()}))
+        return
     res, stm = make_runs(ops, StackRun, torch, cfg, dev)
     setup_s = time.time() - t_setup
     nh0 = 4
