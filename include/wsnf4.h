@@ -190,6 +190,33 @@ ws_status ws_nf4_matmul(const ws_nf4* W, const uint16_t* act, int64_t M, int32_t
                         void* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
                         ws_stream_t stream);
 
+/* Allocation-free variant of ws_nf4_matmul (no counterpart on the method's
+ * pages; an addition for callers that cannot allocate device memory).
+ *
+ * Some callers cannot call cudaMalloc or hand out a workspace: code that runs
+ * under a host framework whose allocator owns all device memory, plugins
+ * with no allocation hooks, or paths that must not allocate at all once
+ * running.  This entry point takes only the inputs and the output; the
+ * scratch it needs (fp32 partials of a split contraction) lives in a
+ * file-scope device array of WS_NOALLOC_SCRATCH_BYTES (32 MiB) inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  Nothing is allocated or freed by the call.
+ *  - The first call on a device looks up that device's address of the
+ *    array (cudaGetSymbolAddress, once per device, with the device current);
+ *    make that first call before any stream capture.
+ *  - Every call shares the one array: calls that overlap on the GPU (other
+ *    streams, other host threads) race on it and must be serialised by the
+ *    caller.  Each call overwrites all scratch it reads, so no clearing is
+ *    needed between calls.
+ *  - A shape whose split partials would exceed the array returns
+ *    WS_ERR_OOM before anything is enqueued (ws_nf4_matmul_workspace_size
+ *    gives the bytes a shape needs).
+ * Arguments, layouts and results are those of ws_nf4_matmul. */
+#define WS_NOALLOC_SCRATCH_BYTES (32u << 20)
+ws_status ws_nf4_matmul_noalloc(const ws_nf4* W, const uint16_t* act, int64_t M,
+                                int32_t transpose_w, void* out, int32_t out_dtype,
+                                ws_stream_t stream);
+
 /* ---- the synthetic stack ----------------------------------------------------- */
 /* One layer: h -> RMSNorm -> q,k,v (NF4-LoRA) -> v repeated across the
  * H/head_dim query heads (head h reads kv head h / (H/KV)) in place of the

@@ -165,6 +165,28 @@ ws_status ws_nf4_matmul(const ws_nf4* W, const uint16_t* act, int64_t M, int32_t
                                   static_cast<float*>(workspace), (cudaStream_t)stream));
 }
 
+ws_status ws_nf4_matmul_noalloc(const ws_nf4* W, const uint16_t* act, int64_t M,
+                                int32_t transpose_w, void* out, int32_t out_dtype,
+                                ws_stream_t stream) {
+  if (!W || !W->codes || !W->absmax || !act || !out) return WS_ERR_INVALID;
+  if (out_dtype != WS_DTYPE_BF16 && out_dtype != WS_DTYPE_F32) return WS_ERR_INVALID;
+  if (M < 1 || W->N < 64 || W->K < 64 || W->N % 64 || W->K % 64) return WS_ERR_SHAPE;
+  if (M > (int64_t)1 << 30 || W->N > (int64_t)1 << 30 || W->K > (int64_t)1 << 30)
+    return WS_ERR_SHAPE;
+  if (!aligned16(W->codes) || !aligned16(W->absmax) || !aligned16(act) || !aligned16(out))
+    return WS_ERR_ALIGN;
+  const bool bwd = transpose_w != 0;
+  const GemmPlan p = bwd ? plan_gemm(true, M, W->K, W->N) : plan_gemm(false, M, W->N, W->K);
+  const size_t need = gemm_partial_bytes(p, M, bwd ? W->K : W->N);
+  float* scratch = nullptr;
+  size_t have = 0;
+  if (noalloc_scratch(&scratch, &have) != cudaSuccess) return WS_ERR_CUDA;
+  if (need > have) return WS_ERR_OOM;
+  return cuda_status(run_nf4_gemm(p, view_of(W), act, M, nullptr, nullptr, 0.0f, nullptr, out,
+                                  out_dtype == WS_DTYPE_F32 ? 1 : 0, 0, scratch,
+                                  (cudaStream_t)stream));
+}
+
 ws_status ws_stack_sizes(const ws_stack_cfg* cfg, int32_t block_layers, size_t* block_weight_bytes,
                          int64_t* n_params, size_t* saved_bytes_layer, size_t* workspace_bytes) {
   ws_status s = stack_check(cfg);

@@ -44,6 +44,9 @@ struct GemmPlan {
 };
 
 int device_sm_count();
+// This device's address and size of the built-in scratch array used by
+// ws_nf4_matmul_noalloc (looked up once per device).
+cudaError_t noalloc_scratch(float** ptr, size_t* bytes);
 // Counts every kernel launch the library makes (reported by ws_kernel_launches).
 void note_launch();
 cudaError_t read_and_clear_dev_error(uint32_t* flags);

@@ -25,6 +25,8 @@
 // the epilogue.  Contraction splits (grid z) write fp32 partials that a
 // separate kernel sums in split order: no atomics anywhere.
 #define WS_GEMM_TU 1
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -533,6 +535,40 @@ cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& 
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------- allocation-free scratch
+// Split-contraction partials for ws_nf4_matmul_noalloc live in this
+// file-scope device array rather than in a caller workspace.  Every device
+// that loads the library holds it until the process exits; every call shares
+// it.  Each split writes every element of its own partial slice before the
+// reduce reads it, so nothing has to start at zero.
+constexpr size_t kNoAllocScratchBytes = (size_t)WS_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+namespace {
+std::mutex g_noalloc_mu;
+constexpr int kMaxDevices = 64;
+float* g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+cudaError_t noalloc_scratch(float** ptr, size_t* bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    // host code cannot use the symbol itself: ask the runtime for this
+    // device's address of the array (once per device)
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *ptr = g_noalloc_ptr[dev];
+  *bytes = kNoAllocScratchBytes;
+  return cudaSuccess;
+}
 
 int device_sm_count() {
   static int sms = 0;

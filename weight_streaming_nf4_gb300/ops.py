@@ -85,6 +85,7 @@ _sig("ws_lora_linear_bwd", [C.POINTER(Nf4), P, P, P, LoraShape, DropoutKey, P, P
                             i32, P, P, P, C.c_size_t, P])
 _sig("ws_nf4_matmul_workspace_size", [i64, i64, i64, i32, C.POINTER(C.c_size_t)])
 _sig("ws_nf4_matmul", [C.POINTER(Nf4), P, i64, i32, P, i32, P, C.c_size_t, P])
+_sig("ws_nf4_matmul_noalloc", [C.POINTER(Nf4), P, i64, i32, P, i32, P])
 _sig("ws_stack_sizes", [C.POINTER(StackCfgC), i32, C.POINTER(C.c_size_t), C.POINTER(i64),
                         C.POINTER(C.c_size_t), C.POINTER(C.c_size_t)])
 _sig("ws_stack_weight_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(C.c_size_t),
@@ -100,7 +101,7 @@ _sig("ws_stack_train_step", [C.POINTER(StackCfgC), i32, i32, C.POINTER(StackBuff
 
 EXPORTED = ("ws_status_string", "ws_device_error", "ws_kernel_launches", "ws_quantize_nf4", "ws_lora_workspace_size",
             "ws_lora_linear_fwd", "ws_lora_linear_bwd", "ws_nf4_matmul_workspace_size",
-            "ws_nf4_matmul", "ws_stack_sizes",
+            "ws_nf4_matmul", "ws_nf4_matmul_noalloc", "ws_stack_sizes",
             "ws_stack_weight_offset", "ws_stack_param_offset", "ws_stack_saved_offset",
             "ws_block_forward",
             "ws_block_backward_recompute", "ws_stream_block_h2d", "ws_stack_train_step")
@@ -243,6 +244,27 @@ def nf4_matmul(W: NF4Weight, act, transpose_w=False, out=None, out_f32=False, wo
     _check("ws_nf4_matmul", _lib.ws_nf4_matmul(C.byref(w), _ptr(act), M, 1 if transpose_w else 0,
                                                _ptr(out), dt, _ptr(workspace), workspace.numel(),
                                                _stream(stream)))
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def nf4_matmul_noalloc(W: NF4Weight, act, transpose_w=False, out=None, out_f32=False,
+                       stream=None):
+    """ws_nf4_matmul without a workspace: the library's built-in scratch array
+    holds the split partials (see include/wsnf4.h).  `out` must be given by
+    callers that cannot allocate."""
+    M = act.shape[0]
+    cols = W.K if transpose_w else W.N
+    if out is None:
+        out = torch.empty((M, cols), dtype=torch.float32 if out_f32 else torch.bfloat16,
+                          device=act.device)
+    w = W.c()
+    dt = WS_DTYPE_F32 if out.dtype == torch.float32 else WS_DTYPE_BF16
+    _check("ws_nf4_matmul_noalloc",
+           _lib.ws_nf4_matmul_noalloc(C.byref(w), _ptr(act), M, 1 if transpose_w else 0,
+                                      _ptr(out), dt, _stream(stream)))
     return out
 
 
