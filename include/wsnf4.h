@@ -197,8 +197,8 @@ ws_status ws_nf4_matmul(const ws_nf4* W, const uint16_t* act, int64_t M, int32_t
  * under a host framework whose allocator owns all device memory, plugins
  * with no allocation hooks, or paths that must not allocate at all once
  * running.  This entry point takes only the inputs and the output; the
- * scratch it needs (fp32 partials of a split contraction) lives in a
- * file-scope device array of WS_NOALLOC_SCRATCH_BYTES (32 MiB) inside the
+ * scratch it needs (fp32 partial tiles of a split contraction) lives in a
+ * file-scope device array of WS_NOALLOC_SCRATCH_BYTES (48 MiB) inside the
  * library, which every GPU that loads the library holds until the process
  * exits.  Nothing is allocated or freed by the call.
  *  - The first call on a device looks up that device's address of the
@@ -212,7 +212,7 @@ ws_status ws_nf4_matmul(const ws_nf4* W, const uint16_t* act, int64_t M, int32_t
  *    WS_ERR_OOM before anything is enqueued (ws_nf4_matmul_workspace_size
  *    gives the bytes a shape needs).
  * Arguments, layouts and results are those of ws_nf4_matmul. */
-#define WS_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define WS_NOALLOC_SCRATCH_BYTES (48u << 20)
 ws_status ws_nf4_matmul_noalloc(const ws_nf4* W, const uint16_t* act, int64_t M,
                                 int32_t transpose_w, void* out, int32_t out_dtype,
                                 ws_stream_t stream);

@@ -141,6 +141,20 @@ WS_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t why) {
   }
 }
 
+// Same, for waits expected to last a whole main loop (epilogue warps): poll
+// with a short sleep so the waiting warps leave issue slots to the producers.
+WS_DEVINL bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, uint32_t why) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(200);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u && globaltimer() - t0 > kWaitLimitNs) {
+      atomicOr(&g_dev_error, why);
+      return false;
+    }
+  }
+}
 #endif
 
 // ---- fences ----------------------------------------------------------------------------

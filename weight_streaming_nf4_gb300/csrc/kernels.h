@@ -23,15 +23,15 @@ struct NF4View {
 struct GemmArgs {
   int64_t M;            // activation rows
   int64_t Nout;         // output columns (forward: N, backward: K)
-  int nk_total;         // 64-deep contraction steps in total
-  int ksteps_per_split; // steps per grid-z split
+  int nk_total;         // 64-deep contraction steps per tile
+  int mtiles, ntiles;   // output tiles (M-tiles vary fastest in the schedule)
   int has_lora;         // split 0 runs the extra LoRA step
   const float* lora_F;  // forward: B [N, 16]; backward: A [16, K]
   float lora_scale;     // s = (alpha / r) / (1 - p)
   const uint32_t* mask; // backward: dropout bits [M, K/32]
   void* out;            // [M, Nout] bf16 or fp32
   int out_f32, out_accum;
-  float* partial;       // [splits, M, Nout] fp32 when splits > 1
+  float* partial;       // [grid, 2, BM, BN] fp32 partial tiles of cut tiles
 };
 
 // Tile configuration: a pure function of the shape and the SM count, so a
@@ -40,10 +40,12 @@ struct GemmPlan {
   bool bwd;
   int um, bn;
   int mtiles, ntiles, nk;
-  int splits, kps;
 };
 
 int device_sm_count();
+// CTAs of the persistent stream-K grid for a plan (with or without the extra
+// LoRA step): min(SM count, iterations / 8), at least 1.
+int64_t grid_ctas(const GemmPlan& p, bool has_lora);
 // This device's address and size of the built-in scratch array used by
 // ws_nf4_matmul_noalloc (looked up once per device).
 cudaError_t noalloc_scratch(float** ptr, size_t* bytes);
@@ -69,12 +71,14 @@ DropKeyHost make_drop_key(const ws_dropout_key& k);
 cudaError_t run_quantize_nf4(const uint16_t* W, int64_t N, int64_t K, uint8_t* codes,
                              float* absmax, cudaStream_t st);
 // U = (mask . x) A^T [M,16] fp32; Uext [M,64] bf16 hi/lo; mask bits (optional).
+// partial: skinny_partial_bytes(M, K) of scratch.
+size_t skinny_partial_bytes(int64_t M, int64_t K);
 cudaError_t run_lora_down(const uint16_t* x, const float* A, int64_t M, int64_t K,
                           const DropKeyHost& key, float* U, uint16_t* Uext, uint32_t* mask_out,
-                          cudaStream_t st);
+                          float* partial, cudaStream_t st);
 // G = dY B [M,16] fp32 and Gext [M,64] bf16 hi/lo.
 cudaError_t run_lora_G(const uint16_t* dY, const float* B, int64_t M, int64_t N, float* G,
-                       uint16_t* Gext, cudaStream_t st);
+                       uint16_t* Gext, float* partial, cudaStream_t st);
 // Weight gradient of a LoRA factor: out = s * P^T Q~ with P [M,16] fp32,
 // Q [M,C] bf16 (masked by `mask` [M, C/32] when not NULL).  out layout is
 // [C,16] (dB) or, when transpose_out, [16,C] (dA).  Fixed-order reduction.

@@ -9,21 +9,29 @@
 // swizzled operand layout the tensor cores read, and consumed by
 // tcgen05.mma (bf16 x bf16 -> fp32 in TMEM) issued by one thread.
 //
-// CTA = 10 warps:
-//   warp 0     TMA producer (activation tile + code tile + absmax tile)
-//   warp 1     TMEM allocator and MMA issuer
-//   warps 2-9  dequant producers, then the epilogue (TMEM -> registers ->
-//              global), one TMEM lane quarter per warp
+// Persistent CTA (one per SM) = 14 warps:
+//   warp 0      TMA producer (activation tile + code tile + absmax tile)
+//   warp 1      TMEM allocator and MMA issuer
+//   warps 2-9   dequant producers
+//   warps 10-13 epilogue (TMEM -> registers -> global), one TMEM lane
+//               quarter per warp, overlapping the next tile's main loop
 // Tile: 128*UM rows of activations (UM tensor-core atoms of M = 128 sharing
 // one dequantised weight tile), BN output columns, 64-deep contraction steps.
+//
+// Schedule: the (tile, step) iterations of the whole problem are cut into
+// gridDim.x equal contiguous ranges, one per CTA (stream-K).  A tile that a
+// range boundary cuts is finished by a fixed-order fix-up kernel that adds
+// the CTAs' fp32 partial tiles in step order; every other tile is written
+// by its CTA's epilogue.  The cut points depend only on the shape and the
+// grid size, so results are deterministic and identical run to run.  No
+// atomics anywhere.
 //
 // The LoRA terms use the same tensor cores: the forward appends one 64-deep
 // step whose A operand is [U_hi | U_lo | U_hi | 0] and whose B operand is
 // [Bs_hi | Bs_hi | Bs_lo | 0] (Bs = s B, bf16 high/low splits), i.e.
 // U Bs^T to about 16 significant bits.  The backward computes s G A the same
 // way into a second TMEM accumulator and adds it under the dropout mask in
-// the epilogue.  Contraction splits (grid z) write fp32 partials that a
-// separate kernel sums in split order: no atomics anywhere.
+// the epilogue.
 #define WS_GEMM_TU 1
 #include <mutex>
 
@@ -48,8 +56,9 @@ __constant__ float c_nf4_levels[16] = {-1.0f,    -0.6962f, -0.5251f, -0.3949f,
 
 namespace {
 
-constexpr int kThreads = 320;
 constexpr int kDqWarps = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = (2 + kDqWarps + kEpiWarps) * 32;
 constexpr int kDqThreads = kDqWarps * 32;
 
 template <bool BWD, int UM, int BN>
@@ -64,7 +73,13 @@ struct Cfg {
   static constexpr int STAGES_RAW =
       (int)((220u * 1024u - BSTAGES * B_BYTES - 1024u) / STAGE_BYTES);
   static constexpr int STAGES = STAGES_RAW > 4 ? 4 : STAGES_RAW;
-  static constexpr uint32_t TMEM_COLS = (BWD ? 2u : 1u) * UM * BN;
+  // one accumulator set: D (and for the backward the LoRA term D2)
+  static constexpr uint32_t ACC_COLS = (BWD ? 2u : 1u) * UM * BN;
+  // double-buffer the accumulator when TMEM has room, so the epilogue of
+  // one tile overlaps the main loop of the next
+  static constexpr int ACC_BUFS = 2 * ACC_COLS <= 512 ? 2 : 1;
+  static constexpr uint32_t TMEM_COLS = ACC_COLS * ACC_BUFS;
+  static constexpr int64_t TILE_FLOATS = (int64_t)BM * BN;
   // MN-major operand (backward): 64-element MN groups LBO apart, 8-row K
   // groups SBO apart.
   static constexpr uint32_t MN_LBO = 1024;
@@ -74,7 +89,7 @@ struct Cfg {
   static constexpr uint32_t OFF_C = OFF_B + BSTAGES * B_BYTES;
   static constexpr uint32_t OFF_S = OFF_C + STAGES * C_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_S + STAGES * S_BYTES;
-  static constexpr uint32_t N_BARS = 2 * STAGES + 2 * BSTAGES + 2;
+  static constexpr uint32_t N_BARS = 2 * STAGES + 2 * BSTAGES + 2 * ACC_BUFS + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
   static_assert(STAGES >= 2, "pipeline needs two stages");
@@ -83,6 +98,13 @@ struct Cfg {
   static_assert(BN == 128 || BN == 256, "BN");
 };
 
+// CTA of the stream-K schedule that owns iteration i: ranges are
+// [floor(g*I/G), floor((g+1)*I/G)), so g = ceil((i+1)*G/I) - 1.
+__host__ __device__ inline int64_t sk_cta_of(int64_t i, int64_t I, int64_t G) {
+  return ((i + 1) * G + I - 1) / I - 1;
+}
+__host__ __device__ inline int64_t sk_begin(int64_t g, int64_t I, int64_t G) { return g * I / G; }
+
 WS_DEVINL void sts128(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
 }
@@ -90,13 +112,21 @@ WS_DEVINL void sts128(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d
 // Dequantise 4 code bytes (8 consecutive weights along k) into a 16-byte
 // chunk of bf16 values: element 2i from the high nibble of byte i, element
 // 2i+1 from its low nibble.
+// Two IEEE fp32 products (round to nearest) in one packed instruction.
+WS_DEVINL void mul2_rn(float x0, float x1, float s, float& r0, float& r1) {
+  asm("{\n .reg .b64 pa, pb, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %4};\n"
+      " mul.rn.f32x2 pd, pa, pb;\n mov.b64 {%0, %1}, pd;\n}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(x0), "f"(x1), "f"(s));
+}
+
 WS_DEVINL uint4 dq8(uint32_t w, float a, const float* lv) {
   uint32_t o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t byte = (w >> (8 * i)) & 0xFFu;
-    const float v0 = lv[byte >> 4] * a;
-    const float v1 = lv[byte & 15u] * a;
+    float v0, v1;
+    mul2_rn(lv[byte >> 4], lv[byte & 15u], a, v0, v1);
     o[i] = pack_bf16x2(v0, v1);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
@@ -210,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<BWD, UM, BN>;
   constexpr int STAGES = C::STAGES;
   constexpr int BSTAGES = C::BSTAGES;
+  constexpr int NACC = C::ACC_BUFS;
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ float s_lv[16];
@@ -225,7 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bfull = empty + STAGES;
   uint64_t* bempty = bfull + BSTAGES;
   uint64_t* accfull = bempty + BSTAGES;
-  uint64_t* drain = accfull + 1;
+  uint64_t* accempty = accfull + NACC;
+  uint64_t* drain = accempty + NACC;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   uint32_t* tmem_slot = misc;
   volatile uint32_t* abort_flag = misc + 1;
@@ -233,18 +265,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = (int)warp_id();
   const int lane = (int)lane_id();
-  const int mt = blockIdx.x, nt = blockIdx.y, split = blockIdx.z;
-  const int m0 = mt * C::BM;
-  const int n0 = nt * BN;
-  const int ks_begin = split * args.ksteps_per_split;
-  const int ks_end = min(args.nk_total, ks_begin + args.ksteps_per_split);
-  const bool lora_here = args.has_lora && split == 0;
-  const int nsteps = (ks_end - ks_begin) + (lora_here ? 1 : 0);
+  // ---- static stream-K schedule
+  const int64_t S = (int64_t)args.nk_total + (args.has_lora ? 1 : 0);  // steps per tile
+  const int64_t T = (int64_t)args.mtiles * args.ntiles;
+  const int64_t I = T * S;
+  const int64_t G = gridDim.x;
+  const int64_t pb = sk_begin(blockIdx.x, I, G);
+  const int64_t pe = sk_begin((int64_t)blockIdx.x + 1, I, G);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
     // an earlier kernel already gave up: do nothing rather than queue more work
-    *skip_flag = (*(volatile uint32_t*)&g_dev_error != 0u || nsteps <= 0) ? 1u : 0u;
+    *skip_flag = (*(volatile uint32_t*)&g_dev_error != 0u || pe <= pb) ? 1u : 0u;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1 + kDqWarps);
@@ -253,7 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bfull[b], kDqWarps);
       mbar_init(&bempty[b], 1);
     }
-    mbar_init(accfull, 1);
+    for (int a = 0; a < NACC; ++a) {
+      mbar_init(&accfull[a], 1);
+      mbar_init(&accempty[a], kEpiWarps);
+    }
     mbar_init(drain, 1);
     fence_barrier_init();
   }
@@ -275,18 +310,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmC);
         tma_prefetch_desc(&tmS);
-        if (lora_here) tma_prefetch_desc(&tmL);
-        int issued = 0;
-        for (int i = 0; i < nsteps; ++i) {
-          const int s = i % STAGES;
-          const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+        if (args.has_lora) tma_prefetch_desc(&tmL);
+        int64_t issued = 0;
+        int s = 0;
+        uint32_t ph = 0;
+        int i = (int)(pb % S);
+        int mt = (int)((pb / S) % args.mtiles);
+        int nt = (int)((pb / S) / args.mtiles);
+        for (int64_t q = 0; q < pe - pb; ++q) {
           if (*abort_flag || !mbar_wait(&empty[s], ph ^ 1u, DERR_TIMEOUT_EMPTY)) {
             *abort_flag = 1u;
             break;
           }
-          const bool is_lora = lora_here && i == nsteps - 1;
-          if (!is_lora) {
-            const int c0 = (ks_begin + i) * 64;
+          const int m0 = mt * C::BM;
+          const int n0 = nt * BN;
+          if (!(args.has_lora && i == args.nk_total)) {
+            const int c0 = i * 64;
             mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::C_BYTES + C::S_BYTES);
             tma_load_2d(sA + s * C::A_BYTES, &tmA, &full[s], c0, m0);
             if (!BWD) {
@@ -300,12 +339,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&full[s], C::A_BYTES);
             tma_load_2d(sA + s * C::A_BYTES, &tmL, &full[s], 0, m0);
           }
-          issued = i + 1;
+          issued = q + 1;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+          if (++i == (int)S) {
+            i = 0;
+            if (++mt == args.mtiles) {
+              mt = 0;
+              ++nt;
+            }
+          }
         }
         if (*abort_flag) {
           // let every issued copy land before the CTA can exit
-          for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
-            mbar_wait(&full[i % STAGES], (uint32_t)(i / STAGES) & 1u, DERR_TIMEOUT_DRAIN);
+          for (int64_t q = (issued > STAGES ? issued - STAGES : 0); q < issued; ++q)
+            mbar_wait(&full[q % STAGES], (uint32_t)(q / STAGES) & 1u, DERR_TIMEOUT_DRAIN);
         }
       }
     } else if (warp == 1) {
@@ -313,68 +363,96 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         constexpr uint32_t idesc_main = idesc_bf16_f32(128, BN, BWD ? 1u : 0u);
         constexpr uint32_t idesc_kmaj = idesc_bf16_f32(128, BN, 0u);
-        for (int i = 0; i < nsteps; ++i) {
-          const int s = i % STAGES;
-          const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
-          const int b = i % BSTAGES;
-          const uint32_t bph = (uint32_t)(i / BSTAGES) & 1u;
-          if (*abort_flag || !mbar_wait(&full[s], ph, DERR_TIMEOUT_FULL) ||
-              !mbar_wait(&bfull[b], bph, DERR_TIMEOUT_BFULL)) {
+        int64_t q = 0;
+        int64_t seg = 0;
+        int ms_s = 0, ms_b = 0;
+        uint32_t ms_ph = 0, ms_bph = 0;
+        for (int64_t p = pb; p < pe && !*abort_flag; ++seg) {
+          const int64_t t = p / S;
+          const int64_t seg_end = min(pe, (t + 1) * S);
+          const int a = (int)(seg % NACC);
+          const uint32_t aph = (uint32_t)(seg / NACC) & 1u;
+          if (!mbar_wait(&accempty[a], aph ^ 1u, DERR_TIMEOUT_ACC)) {
             *abort_flag = 1u;
             break;
           }
           tc_fence_after();
-          const bool is_lora = lora_here && i == nsteps - 1;
-          const uint32_t a_base = smem_u32(sA + s * C::A_BYTES);
-          const uint32_t b_base = smem_u32(sB + b * C::B_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            uint64_t bdesc;
-            if (!BWD || is_lora)
-              bdesc = smem_desc_sw128(b_base + kk * 32, 16, 1024);
-            else
-              bdesc = smem_desc_sw128(b_base + kk * 2 * C::MN_SBO, C::MN_LBO, C::MN_SBO);
-#pragma unroll
-            for (int u = 0; u < UM; ++u) {
-              const uint64_t adesc = smem_desc_sw128(a_base + u * 16384 + kk * 32, 16, 1024);
-              uint32_t d = tmem + (uint32_t)(u * BN);
-              uint32_t acc;
-              if (BWD && is_lora) {
-                d += (uint32_t)(UM * BN);
-                acc = kk > 0 ? 1u : 0u;
-              } else {
-                acc = (i > 0 || kk > 0) ? 1u : 0u;
-              }
-              tc_mma_f16(d, adesc, bdesc, is_lora ? idesc_kmaj : idesc_main, acc);
+          const uint32_t dbase = tmem + (uint32_t)(a * C::ACC_COLS);
+          int i = (int)(p % S);
+          for (int64_t p2 = p; p2 < seg_end; ++p2, ++q, ++i) {
+            const int s = ms_s, b = ms_b;
+            const uint32_t ph = ms_ph, bph = ms_bph;
+            if (++ms_s == STAGES) {
+              ms_s = 0;
+              ms_ph ^= 1u;
             }
+            if (++ms_b == BSTAGES) {
+              ms_b = 0;
+              ms_bph ^= 1u;
+            }
+            if (*abort_flag || !mbar_wait(&full[s], ph, DERR_TIMEOUT_FULL) ||
+                !mbar_wait(&bfull[b], bph, DERR_TIMEOUT_BFULL)) {
+              *abort_flag = 1u;
+              break;
+            }
+            tc_fence_after();
+            const bool is_lora = args.has_lora && i == args.nk_total;
+            const uint32_t a_base = smem_u32(sA + s * C::A_BYTES);
+            const uint32_t b_base = smem_u32(sB + b * C::B_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              uint64_t bdesc;
+              if (!BWD || is_lora)
+                bdesc = smem_desc_sw128(b_base + kk * 32, 16, 1024);
+              else
+                bdesc = smem_desc_sw128(b_base + kk * 2 * C::MN_SBO, C::MN_LBO, C::MN_SBO);
+#pragma unroll
+              for (int u = 0; u < UM; ++u) {
+                const uint64_t adesc = smem_desc_sw128(a_base + u * 16384 + kk * 32, 16, 1024);
+                uint32_t d = dbase + (uint32_t)(u * BN);
+                uint32_t acc;
+                if (BWD && is_lora) {
+                  d += (uint32_t)(UM * BN);
+                  acc = kk > 0 ? 1u : 0u;
+                } else {
+                  acc = (p2 > p || kk > 0) ? 1u : 0u;
+                }
+                tc_mma_f16(d, adesc, bdesc, is_lora ? idesc_kmaj : idesc_main, acc);
+              }
+            }
+            tc_commit(&empty[s]);
+            tc_commit(&bempty[b]);
           }
-          tc_commit(&empty[s]);
-          tc_commit(&bempty[b]);
+          tc_commit(&accfull[a]);
+          p = seg_end;
         }
-        tc_commit(accfull);
+        // every MMA this thread issued has completed before TMEM is freed
+        tc_commit(drain);
+        mbar_wait(drain, 0u, DERR_TIMEOUT_DRAIN);
       }
-    } else {
+    } else if (warp < 2 + kDqWarps) {
       // ------------------------------------------------------------ dequant producers
-      const int t = (int)threadIdx.x - 64;
-      for (int i = 0; i < nsteps; ++i) {
-        const int s = i % STAGES;
-        const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
-        const int b = i % BSTAGES;
-        const uint32_t bph = (uint32_t)(i / BSTAGES) & 1u;
+      const int t_idx = (int)threadIdx.x - 64;
+      int s = 0, b = 0;
+      uint32_t ph = 0, bph = 0;
+      int i = (int)(pb % S);
+      int mt = (int)((pb / S) % args.mtiles);
+      int nt = (int)((pb / S) / args.mtiles);
+      for (int64_t q = 0; q < pe - pb; ++q) {
         if (*abort_flag || !mbar_wait(&full[s], ph, DERR_TIMEOUT_FULL) ||
             !mbar_wait(&bempty[b], bph ^ 1u, DERR_TIMEOUT_BEMPTY)) {
           *abort_flag = 1u;
           break;
         }
-        const bool is_lora = lora_here && i == nsteps - 1;
+        const int n0 = nt * BN;
         uint8_t* Bt = sB + b * C::B_BYTES;
-        if (!is_lora) {
+        if (!(args.has_lora && i == args.nk_total)) {
           const uint8_t* cs = sC + s * C::C_BYTES;
           const float* ss = reinterpret_cast<const float*>(sS + s * C::S_BYTES);
-          if (!BWD) dequant_fwd<BN>(cs, ss, Bt, t, s_lv);
-          else dequant_bwd<BN>(cs, ss, Bt, t, s_lv);
+          if (!BWD) dequant_fwd<BN>(cs, ss, Bt, t_idx, s_lv);
+          else dequant_bwd<BN>(cs, ss, Bt, t_idx, s_lv);
         } else {
-          lora_tile<BWD, BN>(args.lora_F, args.Nout, args.Nout, n0, args.lora_scale, Bt, t);
+          lora_tile<BWD, BN>(args.lora_F, args.Nout, args.Nout, n0, args.lora_scale, Bt, t_idx);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -382,67 +460,107 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bfull[b]);
           mbar_arrive(&empty[s]);
         }
-      }
-
-      // ------------------------------------------------------------ epilogue
-      const bool ok = mbar_wait(accfull, 0u, DERR_TIMEOUT_ACC) && !*abort_flag;
-      tc_fence_after();
-      const int q = warp & 3;          // TMEM lane quarter this warp may read
-      const int h = (warp - 2) >> 2;   // 0 or 1
-      const int r = q * 32 + lane;     // accumulator row inside an atom
-      const int ncols = UM == 2 ? BN : BN / 2;
-      const int u = UM == 2 ? h : 0;
-      const int cbase = UM == 2 ? 0 : h * (BN / 2);
-      const int64_t m = (int64_t)m0 + u * 128 + r;
-      const bool row_ok = ok && m < args.M;
-      for (int cc = 0; cc < ncols; cc += 32) {
-        const int col = cbase + cc;
-        const int64_t n = (int64_t)n0 + col;
-        if (n >= args.Nout) break;  // warp-uniform
-        uint32_t acc[32];
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(u * BN + col);
-        tmem_ld_32x32b_x32(taddr, acc);
-        uint32_t lacc[32];
-        if (BWD && lora_here) tmem_ld_32x32b_x32(taddr + (uint32_t)(UM * BN), lacc);
-        tmem_ld_wait();
-        if (!row_ok) continue;
-        float v[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(acc[e]);
-        if (BWD && lora_here) {
-          const uint32_t bits = args.mask[(m * args.Nout + n) >> 5];
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if ((bits >> e) & 1u) v[e] += __uint_as_float(lacc[e]);
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
         }
-        if (args.partial != nullptr) {
-          float4* dst = reinterpret_cast<float4*>(
-              args.partial + ((int64_t)split * args.M + m) * args.Nout + n);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-        } else if (args.out_f32) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.out) + m * args.Nout + n);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float4 o = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-            if (args.out_accum) {
-              const float4 p = dst[e];
-              o.x = p.x + o.x;
-              o.y = p.y + o.y;
-              o.z = p.z + o.z;
-              o.w = p.w + o.w;
-            }
-            dst[e] = o;
+        if (++b == BSTAGES) {
+          b = 0;
+          bph ^= 1u;
+        }
+        if (++i == (int)S) {
+          i = 0;
+          if (++mt == args.mtiles) {
+            mt = 0;
+            ++nt;
           }
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.out) + m * args.Nout + n);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(pack_bf16x2(v[8 * e], v[8 * e + 1]), pack_bf16x2(v[8 * e + 2], v[8 * e + 3]),
-                                pack_bf16x2(v[8 * e + 4], v[8 * e + 5]),
-                                pack_bf16x2(v[8 * e + 6], v[8 * e + 7]));
         }
+        (void)mt;
+      }
+    } else {
+      // ------------------------------------------------------------ epilogue
+      const int q4 = warp & 3;  // TMEM lane quarter this warp may read
+      const int r = q4 * 32 + lane;
+      int64_t seg = 0;
+      for (int64_t p = pb; p < pe; ++seg) {
+        const int64_t t = p / S;
+        const int64_t i0 = p % S;
+        const int64_t seg_end = min(pe, (t + 1) * S);
+        const int64_t kb = seg_end - t * S;
+        const int a = (int)(seg % NACC);
+        const uint32_t aph = (uint32_t)(seg / NACC) & 1u;
+        const bool ok = !*abort_flag && mbar_wait_backoff(&accfull[a], aph, DERR_TIMEOUT_ACC);
+        tc_fence_after();
+        const int64_t m0 = (t % args.mtiles) * C::BM;
+        const int64_t n0 = (t / args.mtiles) * BN;
+        const bool whole = (i0 == 0 && kb == S);
+        const bool lora_in = args.has_lora && kb == S;
+        // a backward segment made of the LoRA step alone never wrote D
+        const bool main_in = !BWD || i0 < args.nk_total;
+        const int slot = seg == 0 ? 0 : 1;
+        float* part = args.partial + ((int64_t)blockIdx.x * 2 + slot) * C::TILE_FLOATS;
+        const uint32_t dbase = tmem + (uint32_t)(a * C::ACC_COLS);
+#pragma unroll 1
+        for (int u = 0; u < UM; ++u) {
+          const int row = u * 128 + r;
+          const int64_t m = m0 + row;
+          const bool row_ok = ok && m < args.M;
+#pragma unroll 1
+          for (int cc = 0; cc < BN; cc += 32) {
+            const int64_t n = n0 + cc;
+            if (n >= args.Nout) break;  // warp-uniform
+            uint32_t acc[32];
+            const uint32_t taddr = dbase + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(u * BN + cc);
+            tmem_ld_32x32b_x32(taddr, acc);
+            uint32_t lacc[32];
+            if (BWD && lora_in) tmem_ld_32x32b_x32(taddr + (uint32_t)(UM * BN), lacc);
+            tmem_ld_wait();
+            if (!row_ok) continue;
+            float v[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = main_in ? __uint_as_float(acc[e]) : 0.0f;
+            if (BWD && lora_in) {
+              const uint32_t bits = args.mask[(m * args.Nout + n) >> 5];
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if ((bits >> e) & 1u) v[e] += __uint_as_float(lacc[e]);
+            }
+            if (!whole) {
+              float4* dst = reinterpret_cast<float4*>(part + (int64_t)row * BN + cc);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+            } else if (args.out_f32) {
+              float4* dst =
+                  reinterpret_cast<float4*>(static_cast<float*>(args.out) + m * args.Nout + n);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                float4 o = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                if (args.out_accum) {
+                  const float4 pv = dst[e];
+                  o.x = pv.x + o.x;
+                  o.y = pv.y + o.y;
+                  o.z = pv.z + o.z;
+                  o.w = pv.w + o.w;
+                }
+                dst[e] = o;
+              }
+            } else {
+              uint4* dst =
+                  reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.out) + m * args.Nout + n);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dst[e] = make_uint4(pack_bf16x2(v[8 * e], v[8 * e + 1]),
+                                    pack_bf16x2(v[8 * e + 2], v[8 * e + 3]),
+                                    pack_bf16x2(v[8 * e + 4], v[8 * e + 5]),
+                                    pack_bf16x2(v[8 * e + 6], v[8 * e + 7]));
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&accempty[a]);
+        p = seg_end;
       }
     }
   }
@@ -453,32 +571,63 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-// Fixed-order sum of contraction-split partials: out = sum_s partial[s].
-__global__ void k_split_reduce(const float* __restrict__ partial, int splits, int64_t elems,
-                               void* out, int out_f32, int out_accum) {
-  const int64_t i4 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
-  if (i4 >= elems) return;
-  float4 acc = *reinterpret_cast<const float4*>(partial + i4);
-  for (int s = 1; s < splits; ++s) {
-    const float4 p = *reinterpret_cast<const float4*>(partial + (int64_t)s * elems + i4);
-    acc.x += p.x;
-    acc.y += p.y;
-    acc.z += p.z;
-    acc.w += p.w;
-  }
-  if (out_f32) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + i4);
-    if (out_accum) {
-      const float4 o = *dst;
-      acc.x = o.x + acc.x;
-      acc.y = o.y + acc.y;
-      acc.z = o.z + acc.z;
-      acc.w = o.w + acc.w;
+// Tiles cut by a stream-K range boundary: add the CTAs' partial tiles in
+// step order (the CTA holding the tile's first steps first) and store.
+// A partial of CTA g sits in slot 0 when the tile is g's first segment,
+// slot 1 when it is g's last.
+template <int BM, int BN>
+__global__ void __launch_bounds__(256) k_streamk_fixup(const float* __restrict__ partial,
+                                                       int64_t S, int mtiles, int ntiles, int64_t G,
+                                                       int64_t M, int64_t Nout, void* out,
+                                                       int out_f32, int out_accum) {
+  constexpr int kMaxParts = 64;
+  __shared__ const float* s_part[kMaxParts];
+  __shared__ int s_nparts;
+  const int64_t t = blockIdx.x;
+  const int64_t I = (int64_t)mtiles * ntiles * S;
+  const int64_t g1 = sk_cta_of(t * S, I, G);
+  const int64_t g2 = sk_cta_of(t * S + S - 1, I, G);
+  if (g1 == g2) return;
+  if (threadIdx.x == 0) {
+    int n = 0;
+    for (int64_t g = g1; g <= g2 && n < kMaxParts; ++g, ++n) {
+      const int slot = sk_begin(g, I, G) >= t * S ? 0 : 1;
+      s_part[n] = partial + (g * 2 + slot) * (int64_t)BM * BN;
     }
-    *dst = acc;
-  } else {
-    uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + i4);
-    *dst = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    s_nparts = n;
+  }
+  __syncthreads();
+  const int nparts = s_nparts;
+  const int64_t m0 = (t % mtiles) * BM, n0 = (t / mtiles) * BN;
+  const int rows = (int)((M - m0) < BM ? (M - m0) : BM);
+  const int cols = (int)((Nout - n0) < BN ? (Nout - n0) : BN);
+  for (int e4 = threadIdx.x; e4 < BM * BN / 4; e4 += 256) {
+    const int row = (e4 * 4) / BN, col = (e4 * 4) % BN;
+    if (row >= rows || col >= cols) continue;
+    const int off = row * BN + col;
+    float4 acc = *reinterpret_cast<const float4*>(s_part[0] + off);
+    for (int k = 1; k < nparts; ++k) {
+      const float4 v = *reinterpret_cast<const float4*>(s_part[k] + off);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const int64_t m = m0 + row, n = n0 + col;
+    if (out_f32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + m * Nout + n);
+      if (out_accum) {
+        const float4 o = *dst;
+        acc.x = o.x + acc.x;
+        acc.y = o.y + acc.y;
+        acc.z = o.z + acc.z;
+        acc.w = o.w + acc.w;
+      }
+      *dst = acc;
+    } else {
+      uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + m * Nout + n);
+      *dst = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    }
   }
 }
 
@@ -515,6 +664,10 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Persistent grid: one CTA per SM, but at least kMinSteps (tile, step)
+// iterations per CTA so tiny problems are not shredded into partials.
+constexpr int64_t kMinSteps = 8;
+
 template <bool BWD, int UM, int BN>
 cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& tA,
                        const CUtensorMap& tC, const CUtensorMap& tS, const CUtensorMap& tL,
@@ -528,9 +681,16 @@ cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid((unsigned)p.mtiles, (unsigned)p.ntiles, (unsigned)p.splits);
+  const int64_t S = (int64_t)p.nk + (a.has_lora ? 1 : 0);
+  const int64_t I = (int64_t)p.mtiles * p.ntiles * S;
+  const int64_t G = grid_ctas(p, a.has_lora != 0);
   note_launch();
-  k_nf4_gemm<BWD, UM, BN><<<grid, kThreads, C::SMEM_BYTES, st>>>(tA, tC, tS, tL, a);
+  k_nf4_gemm<BWD, UM, BN><<<(unsigned)G, kThreads, C::SMEM_BYTES, st>>>(tA, tC, tS, tL, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || G == 1 || I % G == 0 && (I / G) % S == 0) return e;
+  note_launch();
+  k_streamk_fixup<C::BM, BN><<<(unsigned)(p.mtiles * p.ntiles), 256, 0, st>>>(
+      a.partial, S, p.mtiles, p.ntiles, G, a.M, a.Nout, a.out, a.out_f32, a.out_accum);
   return cudaGetLastError();
 }
 
@@ -581,30 +741,35 @@ int device_sm_count() {
   return sms;
 }
 
+int64_t grid_ctas(const GemmPlan& p, bool has_lora) {
+  const int64_t S = (int64_t)p.nk + (has_lora ? 1 : 0);
+  const int64_t I = (int64_t)p.mtiles * p.ntiles * S;
+  // at least kMinSteps iterations per CTA, and few enough CTAs that one tile
+  // is never cut into more pieces than the fix-up kernel gathers (64)
+  int64_t min_steps = S / 48 + 2;
+  if (min_steps < kMinSteps) min_steps = kMinSteps;
+  int64_t G = (I + min_steps - 1) / min_steps;
+  if (G > device_sm_count()) G = device_sm_count();
+  return G < 1 ? 1 : G;
+}
+
 GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc) {
   GemmPlan p{};
   p.bwd = bwd;
   p.um = M > 128 ? 2 : 1;
-  p.bn = (!bwd && p.um == 2 && Nout >= 256) ? 256 : 128;
+  p.bn = 128;
   p.mtiles = (int)((M + 128 * p.um - 1) / (128 * p.um));
   p.ntiles = (int)((Nout + p.bn - 1) / p.bn);
   p.nk = (int)(Kc / 64);
-  const int tiles = p.mtiles * p.ntiles;
-  const int sms = device_sm_count();
-  int splits = 1;
-  if (tiles < sms) {
-    splits = sms / tiles;
-    const int max_by_depth = p.nk / 8;  // keep at least 8 steps per split
-    if (splits > max_by_depth) splits = max_by_depth;
-    if (splits < 1) splits = 1;
-  }
-  p.kps = (p.nk + splits - 1) / splits;
-  p.splits = (p.nk + p.kps - 1) / p.kps;  // no empty split
   return p;
 }
 
 size_t gemm_partial_bytes(const GemmPlan& p, int64_t M, int64_t Nout) {
-  return p.splits > 1 ? (size_t)p.splits * (size_t)M * (size_t)Nout * sizeof(float) : 0;
+  (void)M;
+  (void)Nout;
+  const int64_t G = grid_ctas(p, true);
+  if (G <= 1) return 0;
+  return (size_t)G * 2 * (size_t)(128 * p.um) * (size_t)p.bn * sizeof(float);
 }
 
 cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* act, int64_t M,
@@ -646,7 +811,8 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
   a.M = M;
   a.Nout = Nout;
   a.nk_total = p.nk;
-  a.ksteps_per_split = p.kps;
+  a.mtiles = p.mtiles;
+  a.ntiles = p.ntiles;
   a.has_lora = has_lora ? 1 : 0;
   a.lora_F = lora_F;
   a.lora_scale = lora_scale;
@@ -654,27 +820,15 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
   a.out = out;
   a.out_f32 = out_f32;
   a.out_accum = out_accum;
-  a.partial = p.splits > 1 ? partial : nullptr;
+  a.partial = partial;
 
-  cudaError_t e;
+  if (partial == nullptr && grid_ctas(p, has_lora) > 1) return cudaErrorInvalidValue;
   if (!p.bwd) {
-    if (p.um == 2 && p.bn == 256) e = launch_cfg<false, 2, 256>(p, a, tA, tC, tS, tL, st);
-    else if (p.um == 2) e = launch_cfg<false, 2, 128>(p, a, tA, tC, tS, tL, st);
-    else e = launch_cfg<false, 1, 128>(p, a, tA, tC, tS, tL, st);
-  } else {
-    if (p.um == 2) e = launch_cfg<true, 2, 128>(p, a, tA, tC, tS, tL, st);
-    else e = launch_cfg<true, 1, 128>(p, a, tA, tC, tS, tL, st);
+    if (p.um == 2) return launch_cfg<false, 2, 128>(p, a, tA, tC, tS, tL, st);
+    return launch_cfg<false, 1, 128>(p, a, tA, tC, tS, tL, st);
   }
-  if (e != cudaSuccess) return e;
-  if (p.splits > 1) {
-    const int64_t elems = M * Nout;
-    const int64_t threads = elems / 4;
-    note_launch();
-    k_split_reduce<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(partial, p.splits, elems, out,
-                                                                     out_f32, out_accum);
-    e = cudaGetLastError();
-  }
-  return e;
+  if (p.um == 2) return launch_cfg<true, 2, 128>(p, a, tA, tC, tS, tL, st);
+  return launch_cfg<true, 1, 128>(p, a, tA, tC, tS, tL, st);
 }
 
 }  // namespace ws

@@ -41,13 +41,24 @@ __global__ void __launch_bounds__(256) k_rmsnorm_fwd(const float* __restrict__ h
                                                      float* __restrict__ rstd) {
   __shared__ float red[9];
   const int64_t m = blockIdx.x;
-  const float* row = h + m * H;
+  const float4* row = reinterpret_cast<const float4*>(h + m * H);
+  const int H4 = (int)(H / 4);
   float ss = 0.0f;
-  for (int64_t i = threadIdx.x; i < H; i += 256) ss = fmaf(row[i], row[i], ss);
+  for (int i = threadIdx.x; i < H4; i += 256) {
+    const float4 v = row[i];
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
   ss = block_sum_256(ss, red);
   const float rs = 1.0f / sqrtf(ss / (float)H + eps);
   if (threadIdx.x == 0) rstd[m] = rs;
-  for (int64_t i = threadIdx.x; i < H; i += 256) out[m * H + i] = f32_to_bf16_bits(row[i] * rs);
+  uint2* o = reinterpret_cast<uint2*>(out + m * H);
+  for (int i = threadIdx.x; i < H4; i += 256) {
+    const float4 v = row[i];
+    o[i] = make_uint2(pack_bf16x2(v.x * rs, v.y * rs), pack_bf16x2(v.z * rs, v.w * rs));
+  }
 }
 
 // dx += rstd*dy - rstd^3 * x * (dy . x) / H
@@ -57,71 +68,132 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(const float* __restrict__ x
                                                      float* __restrict__ dx) {
   __shared__ float red[9];
   const int64_t m = blockIdx.x;
-  const float* xr = x + m * H;
-  const float* dr = dy + m * H;
+  const float4* xr = reinterpret_cast<const float4*>(x + m * H);
+  const float4* dr = reinterpret_cast<const float4*>(dy + m * H);
+  const int H4 = (int)(H / 4);
   float dot = 0.0f;
-  for (int64_t i = threadIdx.x; i < H; i += 256) dot = fmaf(dr[i], xr[i], dot);
+  for (int i = threadIdx.x; i < H4; i += 256) {
+    const float4 a = dr[i], b = xr[i];
+    dot = fmaf(a.x, b.x, dot);
+    dot = fmaf(a.y, b.y, dot);
+    dot = fmaf(a.z, b.z, dot);
+    dot = fmaf(a.w, b.w, dot);
+  }
   dot = block_sum_256(dot, red);
   const float rs = rstd[m];
   const float coef = rs * rs * rs * dot / (float)H;
-  for (int64_t i = threadIdx.x; i < H; i += 256) dx[m * H + i] += rs * dr[i] - coef * xr[i];
+  float4* o = reinterpret_cast<float4*>(dx + m * H);
+  for (int i = threadIdx.x; i < H4; i += 256) {
+    const float4 a = dr[i], b = xr[i];
+    float4 v = o[i];
+    v.x += rs * a.x - coef * b.x;
+    v.y += rs * a.y - coef * b.y;
+    v.z += rs * a.z - coef * b.z;
+    v.w += rs * a.w - coef * b.w;
+    o[i] = v;
+  }
 }
 
+WS_DEVINL float silu_sig(float g) { return 1.0f / (1.0f + expf(-g)); }
+
+// 8 elements per thread (n % 8 == 0)
 __global__ void k_silu_mul_fwd(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u,
                                int64_t n, uint16_t* __restrict__ act) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  const float gv = bf16_bits_to_f32(g[i]), uv = bf16_bits_to_f32(u[i]);
-  const float sg = 1.0f / (1.0f + expf(-gv));
-  act[i] = f32_to_bf16_bits(gv * sg * uv);
+  const int64_t i8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i8 * 8 >= n) return;
+  const uint4 gv = reinterpret_cast<const uint4*>(g)[i8];
+  const uint4 uv = reinterpret_cast<const uint4*>(u)[i8];
+  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float g0 = bf16_lo(gw[k]), g1 = bf16_hi(gw[k]);
+    const float u0 = bf16_lo(uw[k]), u1 = bf16_hi(uw[k]);
+    o[k] = pack_bf16x2(g0 * silu_sig(g0) * u0, g1 * silu_sig(g1) * u1);
+  }
+  reinterpret_cast<uint4*>(act)[i8] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __global__ void k_silu_mul_bwd(const float* __restrict__ dact, const uint16_t* __restrict__ g,
                                const uint16_t* __restrict__ u, int64_t n, uint16_t* __restrict__ dg,
                                uint16_t* __restrict__ du) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  const float gv = bf16_bits_to_f32(g[i]), uv = bf16_bits_to_f32(u[i]), d = dact[i];
-  const float sg = 1.0f / (1.0f + expf(-gv));
-  du[i] = f32_to_bf16_bits(d * gv * sg);
-  dg[i] = f32_to_bf16_bits(d * uv * sg * (1.0f + gv * (1.0f - sg)));
+  const int64_t i8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i8 * 8 >= n) return;
+  const uint4 gv = reinterpret_cast<const uint4*>(g)[i8];
+  const uint4 uv = reinterpret_cast<const uint4*>(u)[i8];
+  const float4 d0 = reinterpret_cast<const float4*>(dact)[2 * i8];
+  const float4 d1 = reinterpret_cast<const float4*>(dact)[2 * i8 + 1];
+  const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+  uint32_t og[4], ou[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float g0 = bf16_lo(gw[k]), g1 = bf16_hi(gw[k]);
+    const float u0 = bf16_lo(uw[k]), u1 = bf16_hi(uw[k]);
+    const float s0 = silu_sig(g0), s1 = silu_sig(g1);
+    ou[k] = pack_bf16x2(d[2 * k] * g0 * s0, d[2 * k + 1] * g1 * s1);
+    og[k] = pack_bf16x2(d[2 * k] * u0 * s0 * (1.0f + g0 * (1.0f - s0)),
+                        d[2 * k + 1] * u1 * s1 * (1.0f + g1 * (1.0f - s1)));
+  }
+  reinterpret_cast<uint4*>(dg)[i8] = make_uint4(og[0], og[1], og[2], og[3]);
+  reinterpret_cast<uint4*>(du)[i8] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
 }
 
-// vr[m, hh*hd + d] = v[m, (hh / rep)*hd + d]
-__global__ void k_repeat_fwd(const uint16_t* __restrict__ v, int64_t M, int64_t H, int64_t KV,
-                             int64_t hd, uint16_t* __restrict__ vr) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= M * H) return;
-  const int64_t m = i / H, c = i % H;
-  const int64_t rep = H / KV;
-  const int64_t hh = c / hd, d = c % hd;
-  vr[i] = v[m * KV + (hh / rep) * hd + d];
+// vr[m, hh*hd + d] = v[m, (hh / rep)*hd + d]; 8 elements per thread
+__global__ void k_repeat_fwd(const uint16_t* __restrict__ v, int M, int H, int KV, int hd,
+                             uint16_t* __restrict__ vr) {
+  const int i8 = blockIdx.x * blockDim.x + threadIdx.x;
+  const int H8 = H / 8;
+  if (i8 >= M * H8) return;
+  const int m = i8 / H8, c = (i8 % H8) * 8;
+  const int rep = H / KV;
+  const int hh = c / hd, d = c % hd;
+  reinterpret_cast<uint4*>(vr)[i8] =
+      *reinterpret_cast<const uint4*>(v + (int64_t)m * KV + (hh / rep) * hd + d);
 }
 
-// dv[m, kh*hd + d] = bf16( sum_{t < rep} dvr[m, (kh*rep + t)*hd + d] ), t ascending
-__global__ void k_repeat_bwd(const float* __restrict__ dvr, int64_t M, int64_t H, int64_t KV,
-                             int64_t hd, uint16_t* __restrict__ dv) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= M * KV) return;
-  const int64_t m = i / KV, c = i % KV;
-  const int64_t rep = H / KV;
-  const int64_t kh = c / hd, d = c % hd;
-  float s = 0.0f;
-  for (int64_t t = 0; t < rep; ++t) s += dvr[m * H + (kh * rep + t) * hd + d];
-  dv[i] = f32_to_bf16_bits(s);
+// dv[m, kh*hd + d] = bf16( sum_{t < rep} dvr[m, (kh*rep + t)*hd + d] ), t ascending;
+// 4 elements per thread
+__global__ void k_repeat_bwd(const float* __restrict__ dvr, int M, int H, int KV, int hd,
+                             uint16_t* __restrict__ dv) {
+  const int i4 = blockIdx.x * blockDim.x + threadIdx.x;
+  const int KV4 = KV / 4;
+  if (i4 >= M * KV4) return;
+  const int m = i4 / KV4, c = (i4 % KV4) * 4;
+  const int rep = H / KV;
+  const int kh = c / hd, d = c % hd;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int t = 0; t < rep; ++t) {
+    const float4 x = *reinterpret_cast<const float4*>(dvr + (int64_t)m * H + (kh * rep + t) * hd + d);
+    s.x += x.x;
+    s.y += x.y;
+    s.z += x.z;
+    s.w += x.w;
+  }
+  reinterpret_cast<uint2*>(dv)[i4] = make_uint2(pack_bf16x2(s.x, s.y), pack_bf16x2(s.z, s.w));
 }
 
+// out = h + float(y); 8 elements per thread
 __global__ void k_add_bf16(const float* __restrict__ h, const uint16_t* __restrict__ y, int64_t n,
                            float* __restrict__ out) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  out[i] = h[i] + bf16_bits_to_f32(y[i]);
+  const int64_t i8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i8 * 8 >= n) return;
+  const uint4 yv = reinterpret_cast<const uint4*>(y)[i8];
+  const float4 h0 = reinterpret_cast<const float4*>(h)[2 * i8];
+  const float4 h1 = reinterpret_cast<const float4*>(h)[2 * i8 + 1];
+  reinterpret_cast<float4*>(out)[2 * i8] =
+      make_float4(h0.x + bf16_lo(yv.x), h0.y + bf16_hi(yv.x), h0.z + bf16_lo(yv.y), h0.w + bf16_hi(yv.y));
+  reinterpret_cast<float4*>(out)[2 * i8 + 1] =
+      make_float4(h1.x + bf16_lo(yv.z), h1.y + bf16_hi(yv.z), h1.z + bf16_lo(yv.w), h1.w + bf16_hi(yv.w));
 }
 
 __global__ void k_cast_bf16(const float* __restrict__ x, int64_t n, uint16_t* __restrict__ y) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  y[i] = f32_to_bf16_bits(x[i]);
+  const int64_t i8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i8 * 8 >= n) return;
+  const float4 a = reinterpret_cast<const float4*>(x)[2 * i8];
+  const float4 b = reinterpret_cast<const float4*>(x)[2 * i8 + 1];
+  reinterpret_cast<uint4*>(y)[i8] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
+                                               pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
 }
 
 // loss = 0.5 * sum(h^2) / n in two fixed-order passes; dh = h / n.
@@ -149,19 +221,31 @@ __global__ void k_loss_final(const float* __restrict__ partial, float inv_n,
   *loss = 0.5f * s * inv_n;
 }
 
-// PyTorch-default Adam (no weight decay, bias-corrected).
+// PyTorch-default Adam (no weight decay, bias-corrected); 4 parameters per thread.
+WS_DEVINL float adam1(float& p, float g, float& m, float& v, float beta1, float beta2, float eps,
+                      float step_size, float bc2_sqrt) {
+  m = beta1 * m + (1.0f - beta1) * g;
+  v = beta2 * v + (1.0f - beta2) * g * g;
+  const float denom = sqrtf(v) / bc2_sqrt + eps;
+  p = p - step_size * (m / denom);
+  return p;
+}
 __global__ void k_adam(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
                        float* __restrict__ v, int64_t n, float beta1, float beta2, float eps,
                        float step_size, float bc2_sqrt) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  const float gi = g[i];
-  const float mi = beta1 * m[i] + (1.0f - beta1) * gi;
-  const float vi = beta2 * v[i] + (1.0f - beta2) * gi * gi;
-  m[i] = mi;
-  v[i] = vi;
-  const float denom = sqrtf(vi) / bc2_sqrt + eps;
-  p[i] = p[i] - step_size * (mi / denom);
+  const int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i4 * 4 >= n) return;
+  float4 pp = reinterpret_cast<float4*>(p)[i4];
+  const float4 gg = reinterpret_cast<const float4*>(g)[i4];
+  float4 mm = reinterpret_cast<float4*>(m)[i4];
+  float4 vv = reinterpret_cast<float4*>(v)[i4];
+  adam1(pp.x, gg.x, mm.x, vv.x, beta1, beta2, eps, step_size, bc2_sqrt);
+  adam1(pp.y, gg.y, mm.y, vv.y, beta1, beta2, eps, step_size, bc2_sqrt);
+  adam1(pp.z, gg.z, mm.z, vv.z, beta1, beta2, eps, step_size, bc2_sqrt);
+  adam1(pp.w, gg.w, mm.w, vv.w, beta1, beta2, eps, step_size, bc2_sqrt);
+  reinterpret_cast<float4*>(p)[i4] = pp;
+  reinterpret_cast<float4*>(m)[i4] = mm;
+  reinterpret_cast<float4*>(v)[i4] = vv;
 }
 
 unsigned nblk(int64_t n, int t = 256) { return (unsigned)((n + t - 1) / t); }
@@ -353,13 +437,13 @@ cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const
   }
   WS_TRY(lin(WS_LIN_V, at<uint16_t>(S, L.a), at<uint16_t>(S, L.v)));
   note_launch();
-  k_repeat_fwd<<<nblk(M * H), 256, 0, st>>>(at<uint16_t>(S, L.v), M, H, KV, x.c.head_dim,
-                                            at<uint16_t>(S, L.vr));
+  k_repeat_fwd<<<nblk(M * H / 8), 256, 0, st>>>(at<uint16_t>(S, L.v), (int)M, (int)H, (int)KV,
+                                                (int)x.c.head_dim, at<uint16_t>(S, L.vr));
   WS_TRY(cudaGetLastError());
   uint16_t* y = at<uint16_t>(ws, x.WSL.yout);
   WS_TRY(lin(WS_LIN_O, at<uint16_t>(S, L.vr), y));
   note_launch();
-  k_add_bf16<<<nblk(M * H), 256, 0, st>>>(h, y, M * H, at<float>(S, L.h1));
+  k_add_bf16<<<nblk(M * H / 8), 256, 0, st>>>(h, y, M * H, at<float>(S, L.h1));
   WS_TRY(cudaGetLastError());
   note_launch();
   k_rmsnorm_fwd<<<(unsigned)M, 256, 0, st>>>(at<float>(S, L.h1), H, x.c.eps, at<uint16_t>(S, L.b),
@@ -368,12 +452,12 @@ cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const
   WS_TRY(lin(WS_LIN_GATE, at<uint16_t>(S, L.b), at<uint16_t>(S, L.g)));
   WS_TRY(lin(WS_LIN_UP, at<uint16_t>(S, L.b), at<uint16_t>(S, L.u)));
   note_launch();
-  k_silu_mul_fwd<<<nblk(M * I), 256, 0, st>>>(at<uint16_t>(S, L.g), at<uint16_t>(S, L.u), M * I,
+  k_silu_mul_fwd<<<nblk(M * I / 8), 256, 0, st>>>(at<uint16_t>(S, L.g), at<uint16_t>(S, L.u), M * I,
                                               at<uint16_t>(S, L.act));
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_DOWN, at<uint16_t>(S, L.act), y));
   note_launch();
-  k_add_bf16<<<nblk(M * H), 256, 0, st>>>(at<float>(S, L.h1), y, M * H, h_out);
+  k_add_bf16<<<nblk(M * H / 8), 256, 0, st>>>(at<float>(S, L.h1), y, M * H, h_out);
   return cudaGetLastError();
 }
 
@@ -403,11 +487,11 @@ cudaError_t layer_bwd(const Ctx& x, const void* block, int lib, int layer, const
   uint16_t* dv = at<uint16_t>(ws, x.WSL.dv);
 
   note_launch();
-  k_cast_bf16<<<nblk(M * H), 256, 0, st>>>(dh, M * H, y1);
+  k_cast_bf16<<<nblk(M * H / 8), 256, 0, st>>>(dh, M * H, y1);
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_DOWN, at<const uint16_t>(S, L.act), y1, dact, 0));
   note_launch();
-  k_silu_mul_bwd<<<nblk(M * I), 256, 0, st>>>(dact, at<const uint16_t>(S, L.g),
+  k_silu_mul_bwd<<<nblk(M * I / 8), 256, 0, st>>>(dact, at<const uint16_t>(S, L.g),
                                               at<const uint16_t>(S, L.u), M * I, dg, du);
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_GATE, at<const uint16_t>(S, L.b), dg, db, 0));
@@ -417,11 +501,11 @@ cudaError_t layer_bwd(const Ctx& x, const void* block, int lib, int layer, const
                                              db, H, dh);
   WS_TRY(cudaGetLastError());
   note_launch();
-  k_cast_bf16<<<nblk(M * H), 256, 0, st>>>(dh, M * H, y1);
+  k_cast_bf16<<<nblk(M * H / 8), 256, 0, st>>>(dh, M * H, y1);
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_O, at<const uint16_t>(S, L.vr), y1, dvr, 0));
   note_launch();
-  k_repeat_bwd<<<nblk(M * KV), 256, 0, st>>>(dvr, M, H, KV, x.c.head_dim, dv);
+  k_repeat_bwd<<<nblk(M * KV / 4), 256, 0, st>>>(dvr, (int)M, (int)H, (int)KV, (int)x.c.head_dim, dv);
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_V, at<const uint16_t>(S, L.a), dv, db, 0));
   note_launch();
@@ -563,7 +647,7 @@ cudaError_t adam_step(float* p, const float* g, float* m, float* v, int64_t n, i
   const double b1 = 0.9, b2 = 0.999;
   const double bc1 = 1.0 - pow(b1, (double)t), bc2 = 1.0 - pow(b2, (double)t);
   note_launch();
-  k_adam<<<nblk(n), 256, 0, st>>>(p, g, m, v, n, (float)b1, (float)b2, 1e-8f, (float)(lr / bc1),
+  k_adam<<<nblk(n / 4), 256, 0, st>>>(p, g, m, v, n, (float)b1, (float)b2, 1e-8f, (float)(lr / bc1),
                                   (float)sqrt(bc2));
   return cudaGetLastError();
 }

@@ -247,7 +247,7 @@ def nf4_matmul(W: NF4Weight, act, transpose_w=False, out=None, out_f32=False, wo
     return out
 
 
-NOALLOC_SCRATCH_BYTES = 32 << 20
+NOALLOC_SCRATCH_BYTES = 48 << 20
 
 
 def nf4_matmul_noalloc(W: NF4Weight, act, transpose_w=False, out=None, out_f32=False,
