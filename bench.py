@@ -160,10 +160,17 @@ def oracle_sample(M_sample, H, KV, I, seed=0):
     return run, flops, oracle.num_threads(), np
 
 
+def arm_config(world):
+    return {"workload": "qwen2.5-32b-shaped stack, 64 layers, seq 512, batch 1, "
+                        "LoRA r16 a32 dropout 0.1, blocks of 4, Adam",
+            "global_batch": world, "seq_len": SHAPE_32B["M"], "parallelism": f"replicas{world}",
+            "l2": "inputs larger than L2 (17.55 GB NF4 base per step)"}
+
+
 def run_reference(args, rank):
     if rank != 0:
         return
-    M_s = 16
+    M_s = 64
     run, flops, cores, _ = oracle_sample(M_s, SHAPE_32B["H"], SHAPE_32B["KV"], SHAPE_32B["I"])
     for _ in range(args.warmup):
         run()
@@ -177,8 +184,7 @@ def run_reference(args, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "qwen2.5-32b-shaped stack, oracle sample", "tokens": M_s,
-                   "layers": 1},
+        "config": arm_config(args.gpus),
         "cpu_baseline": {"value": v, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": v, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -186,6 +192,20 @@ def run_reference(args, rank):
 
 
 # ------------------------------------------------------------------------------ our arm
+class Graphed:
+    """A StackRun whose step is replayed from one captured CUDA graph."""
+
+    def __init__(self, ops, run, lr, stream):
+        l0 = ops.kernel_launches()
+        self.run, self.stream = run, stream
+        self.g = run.graph(lr, stream)
+        self.launches_per_step = ops.kernel_launches() - l0
+        self.loss = run.loss
+
+    def step(self, s, h0):
+        self.g.step(s, h0, self.stream)
+
+
 def make_runs(ops, StackRun, torch, cfg, dev, streamed=True):
     gens = {}
 
@@ -439,29 +459,34 @@ def main():
     nh0 = 4
     h0s = [torch.randn(M * H, device=dev, generator=torch.Generator(device=dev).manual_seed(s))
            for s in range(nh0)]
-    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+    gres = Graphed(ops, res, 2e-4, stream)
+    gstm = Graphed(ops, stm, 2e-4, stream)
 
-    # ---- resident step (value)
-    l0 = ops.kernel_launches()
+    # ---- resident step (value), replayed from one CUDA graph
     with ClockSampler(local) as clk:
-        t_res = time_steps(torch, dist, res, h0s, args.steps, args.warmup, stream, nvtx=True)
-    launches_res = (ops.kernel_launches() - l0) // (args.steps + args.warmup) * args.steps
+        t_res = time_steps(torch, dist, gres, h0s, args.steps, args.warmup, stream, nvtx=True)
+    launches_res = gres.launches_per_step * args.steps
     clocks = clk.summary()
     # ---- streamed step through the public API with host buffers (e2e)
     host_h0 = [h.cpu().pin_memory() for h in h0s]
     dev_h0 = torch.empty(M * H, device=dev)
     host_loss = torch.zeros(args.warmup + args.steps, 1).pin_memory()
     with ClockSampler(local) as clk2:
-        t_stm = time_steps(torch, dist, stm, h0s, args.steps, args.warmup, stream,
+        t_stm = time_steps(torch, dist, gstm, h0s, args.steps, args.warmup, stream,
                            e2e=(host_h0, dev_h0, host_loss))
     clocks2 = clk2.summary()
     err = ops.device_error()
     # bitwise check of the two modes on one extra step
-    res.step(1000, h0s[0])
-    stm.step(1000, h0s[0])
+    gres.step(1000, h0s[0])
+    gstm.step(1000, h0s[0])
     torch.cuda.synchronize()
     bitwise = bool(torch.equal(res.loss, stm.loss) and torch.equal(res.params, stm.params)
                    and torch.equal(res.adam_v, stm.adam_v))
+    # the eager resident step (one launch per kernel), for comparison with the graph replay
+    t_eager = time_steps(torch, dist, res, h0s, 2, 1, stream)
 
     def wmax(t):
         if dist is None:
@@ -492,6 +517,7 @@ def main():
         s_res, s_stm = t_res / args.steps, t_stm / args.steps
         extra["streaming"] = {
             "s_per_step_streamed": s_stm, "s_per_step_resident": s_res,
+            "s_per_step_resident_eager": t_eager / 2,
             "slowdown": s_stm / s_res,
             "h2d_bytes_per_step": h2d_w, "h2d_link_peak_gbs": link,
             "h2d_effective_gbs": h2d_w / s_stm / 1e9,
@@ -506,11 +532,11 @@ def main():
         if not args.quick:
             extra["linear_7b"] = {f"M{m}": linear_7b(ops, torch, dev, m) for m in (512, 2048)}
         if world == 1 and not args.no_cpu_baseline:
-            run, cflops, cores, _ = oracle_sample(48, H, cfg.KV, cfg.I)
+            run, cflops, cores, _ = oracle_sample(256, H, cfg.KV, cfg.I)
             tc = run()
             extra["cpu_baseline"] = {
                 "value": cflops / tc / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-                "sample": (f"one 32B-shaped layer's 7 NF4-LoRA linears fwd+bwd on 48 of 512 tokens "
+                "sample": (f"one 32B-shaped layer's 7 NF4-LoRA linears fwd+bwd on 256 of 512 tokens "
                            f"({cflops / 1e9:.1f} GFLOP, {tc:.1f} s), plain C oracle fp64")}
     if rank == 0:
         out = {
@@ -519,10 +545,7 @@ def main():
             "ms_per_step": 1e3 * t_res / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (random-init NF4 base and adapters, N(0,1) residual input)",
-            "config": {"workload": "qwen2.5-32b-shaped stack, 64 layers, seq 512, batch 1, "
-                                   "LoRA r16 a32 dropout 0.1, blocks of 4, Adam",
-                       "global_batch": world, "seq_len": M, "parallelism": f"replicas{world}",
-                       "l2": "inputs larger than L2 (17.55 GB NF4 base per step)"},
+            "config": arm_config(world),
             "pct_bf16_peak": 100.0 * value / world / pk["bf16_sustained"],
             "e2e": {"value": e2e_val, "unit": "TFLOPS", "h2d_bytes_per_step": h2d_bytes,
                     "d2h_bytes_per_step": 4, "s_per_step": t_stm / args.steps},

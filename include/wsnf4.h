@@ -197,7 +197,8 @@ ws_status ws_nf4_matmul(const ws_nf4* W, const uint16_t* act, int64_t M, int32_t
  * under a host framework whose allocator owns all device memory, plugins
  * with no allocation hooks, or paths that must not allocate at all once
  * running.  This entry point takes only the inputs and the output; the
- * scratch it needs (fp32 partial tiles of a split contraction) lives in a
+ * scratch it needs (fp32 partial tiles of a split contraction and their
+ * completion flags) lives in a
  * file-scope device array of WS_NOALLOC_SCRATCH_BYTES (48 MiB) inside the
  * library, which every GPU that loads the library holds until the process
  * exits.  Nothing is allocated or freed by the call.
@@ -341,6 +342,30 @@ typedef struct {
 ws_status ws_stack_train_step(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
                               const ws_stack_buffers* buf, uint32_t step, const float* h0,
                               float lr, ws_stream_t compute, ws_stream_t copy_stream);
+
+/* ---- the same step as one CUDA graph ---------------------------------------------
+ * ws_stack_graph_create captures everything ws_stack_train_step enqueues
+ * after its first two operations (writing `step` into a device word inside
+ * the workspace, copying h0 into boundary block 0) into one graph: every
+ * block's kernels, the window copies on copy_stream (forked from and joined
+ * back into `compute` inside the graph), the loss and the Adam step.
+ * Kernels that depend on the step (dropout keys, Adam bias corrections) read
+ * it from that device word, so replays with different steps need no
+ * re-capture.  The graph keeps the pointers of *buf, the config, lr and the
+ * copy stream; they must stay valid until ws_stack_graph_destroy.  `compute`
+ * must not be capturing already and may not be the legacy default stream.
+ * ws_stack_graph_step(g, step, h0, compute) enqueues the step-word write,
+ * the h0 copy and the graph on `compute`; results are bitwise those of
+ * ws_stack_train_step with the same arguments.  Errors: the checks of
+ * ws_stack_train_step, WS_ERR_CUDA when capture or instantiation fails
+ * (*out stays NULL). */
+typedef struct ws_step_graph ws_step_graph;
+ws_status ws_stack_graph_create(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
+                                const ws_stack_buffers* buf, float lr, ws_stream_t compute,
+                                ws_stream_t copy_stream, ws_step_graph** out);
+ws_status ws_stack_graph_step(ws_step_graph* g, uint32_t step, const float* h0,
+                              ws_stream_t compute);
+ws_status ws_stack_graph_destroy(ws_step_graph* g);
 
 #ifdef __cplusplus
 }

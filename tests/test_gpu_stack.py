@@ -249,6 +249,35 @@ def test_streamed_equals_resident_bitwise_20_steps(ops):
     assert not torch.equal(fresh, res.params)
 
 
+@pytest.mark.parametrize("streamed", [False, True])
+def test_graph_replay_equals_eager(ops, streamed):
+    """The step captured once as a CUDA graph and replayed with changing step
+    numbers (dropout keys and Adam bias corrections read the step from the
+    device) gives bitwise the eager call's loss, gradients and state."""
+    from weight_streaming_nf4_gb300.stack import StackRun
+    cfg = ops.StackCfg(M=256, H=896, KV=128, I=4864, head_dim=64, n_layers=8)
+    wfn, pfn = _fns(3)
+    eager = StackRun(cfg, 2, streamed, wfn, pfn)
+    wfn, pfn = _fns(3)
+    graphed = StackRun(cfg, 2, streamed, wfn, pfn)
+    cs = torch.cuda.Stream()
+    g = graphed.graph(3e-4, cs)
+    try:
+        for step in (0, 1, 2, 7, 8):
+            h0 = _h0(cfg, step)
+            eager.step(step, h0, lr=3e-4)
+            torch.cuda.synchronize()
+            g.step(step, h0, cs)
+            cs.synchronize()
+            assert torch.equal(eager.loss, graphed.loss), step
+            assert torch.equal(eager.grads, graphed.grads), step
+    finally:
+        g.close()
+    for name in ("params", "adam_m", "adam_v"):
+        assert torch.equal(getattr(eager, name), getattr(graphed, name)), name
+    assert ops.device_error() == 0
+
+
 def test_stream_block_h2d(ops):
     n = 3 * 2 ** 20 + 4096
     src = torch.randint(0, 255, (n,), dtype=torch.uint8).pin_memory()

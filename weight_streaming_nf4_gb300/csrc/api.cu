@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <new>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -241,7 +242,8 @@ ws_status ws_block_forward(const ws_stack_cfg* cfg, const void* block_weights, i
     return WS_ERR_ALIGN;
   if (ws_bytes < stack_ws_bytes(*cfg, n_layers)) return WS_ERR_OOM;
   return cuda_status(block_forward(*cfg, n_layers, block_weights, first_layer, n_layers, params,
-                                   step, h_in, h_out, saved, workspace, (cudaStream_t)stream));
+                                   step, nullptr, h_in, h_out, saved, workspace,
+                                   (cudaStream_t)stream));
 }
 
 ws_status ws_block_backward_recompute(const ws_stack_cfg* cfg, const void* block_weights,
@@ -260,7 +262,7 @@ ws_status ws_block_backward_recompute(const ws_stack_cfg* cfg, const void* block
     return WS_ERR_ALIGN;
   if (ws_bytes < stack_ws_bytes(*cfg, n_layers)) return WS_ERR_OOM;
   return cuda_status(block_backward(*cfg, n_layers, block_weights, first_layer, n_layers, params,
-                                    step, h_in, saved, dh_out, dh_in, grads, workspace,
+                                    step, nullptr, h_in, saved, dh_out, dh_in, grads, workspace,
                                     (cudaStream_t)stream));
 }
 
@@ -284,125 +286,241 @@ ws_status ws_stream_block_h2d(const void* pinned_src, void* dev_dst, size_t byte
   return WS_OK;
 }
 
-// One training step.  Streamed mode keeps a 2-slot window: slot s holds
-// block b with s = b % 2.  The copy of block b+1 is issued before block b's
-// compute so it runs on the copy engine meanwhile; a copy into a slot waits
-// for the compute stream's last use of that slot.  A block still resident
-// in its slot (the last two at the forward/backward turnaround) is not
-// copied again.
-ws_status ws_stack_train_step(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
-                              const ws_stack_buffers* buf, uint32_t step, const float* h0, float lr,
-                              ws_stream_t compute, ws_stream_t copy_stream) {
+}  // extern "C"
+
+// ---------------------------------------------------------------------------- training step
+namespace {
+
+struct StepEvents {
+  cudaEvent_t loaded[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr};
+  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaError_t create() {
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&loaded[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&freed[i], cudaEventDisableTiming);
+    }
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+    return e;
+  }
+  void destroy() {
+    for (int i = 0; i < 2; ++i) {
+      if (loaded[i]) cudaEventDestroy(loaded[i]);
+      if (freed[i]) cudaEventDestroy(freed[i]);
+      loaded[i] = freed[i] = nullptr;
+    }
+    if (fork) cudaEventDestroy(fork);
+    if (join) cudaEventDestroy(join);
+    fork = join = nullptr;
+  }
+};
+
+ws_status check_step(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
+                     const ws_stack_buffers* buf, const void* copy_stream) {
   ws_status s = stack_check(cfg);
   if (s != WS_OK) return s;
-  if (!buf || !h0) return WS_ERR_INVALID;
+  if (!buf) return WS_ERR_INVALID;
   if (block_layers < 1 || cfg->n_layers % block_layers) return WS_ERR_SHAPE;
   if (!buf->params || !buf->grads || !buf->adam_m || !buf->adam_v || !buf->boundary || !buf->dh ||
       !buf->workspace || !buf->loss)
     return WS_ERR_INVALID;
   if (streamed) {
-    if (!buf->host_weights || !buf->window || buf->saved) return WS_ERR_INVALID;
+    if (!buf->host_weights || !buf->window || buf->saved || !copy_stream) return WS_ERR_INVALID;
   } else {
     if (!buf->dev_weights || !buf->saved) return WS_ERR_INVALID;
   }
   if (buf->workspace_bytes < stack_ws_bytes(*cfg, block_layers)) return WS_ERR_OOM;
-  const cudaStream_t cs = (cudaStream_t)compute;
-  const cudaStream_t ps = (cudaStream_t)copy_stream;
-  if (streamed && !ps) return WS_ERR_INVALID;
+  return WS_OK;
+}
 
-  const int nb = cfg->n_layers / block_layers;
-  const size_t bbytes = stack_block_bytes(*cfg, block_layers);
-  const size_t slayer = stack_saved_layer(*cfg);
-  const int64_t MH = cfg->M * cfg->H;
-  const int64_t np = stack_n_params(*cfg);
-  float* bnd = buf->boundary;
-
-  cudaEvent_t ev_loaded[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr};
+// Everything of one step after the step word and boundary[0] (= h0) are
+// set.  Reads the step from the device word, so eager calls and graph
+// replays run the same kernels with the same arguments.
+//
+// Streamed mode keeps a 2-slot window: slot s holds block b with s = b % 2.
+// The copy of block b+1 is issued before block b's compute so it runs on the
+// copy engine meanwhile; a copy into a slot waits for the compute stream's
+// last use of that slot.  A block still resident in its slot (the last two at
+// the forward/backward turnaround) is not copied again.  The copy stream is
+// forked from and joined back into the compute stream, so the whole step
+// can be captured as one graph.
+ws_status step_body(const ws_stack_cfg& cfg, int block_layers, bool streamed,
+                    const ws_stack_buffers& buf, float lr, cudaStream_t cs, cudaStream_t ps,
+                    StepEvents& ev) {
+  const int nb = cfg.n_layers / block_layers;
+  const size_t bbytes = stack_block_bytes(cfg, block_layers);
+  const size_t slayer = stack_saved_layer(cfg);
+  const int64_t MH = cfg.M * cfg.H;
+  const int64_t np = stack_n_params(cfg);
+  float* bnd = buf.boundary;
+  const uint32_t* stepw = stack_step_word(cfg, block_layers, buf.workspace);
   int slot_block[2] = {-1, -1};
   bool slot_used[2] = {false, false};
-  ws_status rc = WS_OK;
-  auto fail = [&](cudaError_t e) {
-    if (e != cudaSuccess && rc == WS_OK) rc = WS_ERR_CUDA;
-    return e != cudaSuccess;
-  };
-  auto cleanup = [&]() {
-    for (int i = 0; i < 2; ++i) {
-      if (ev_loaded[i]) cudaEventDestroy(ev_loaded[i]);
-      if (ev_free[i]) cudaEventDestroy(ev_free[i]);
-    }
-  };
-  if (streamed) {
-    for (int i = 0; i < 2; ++i) {
-      if (fail(cudaEventCreateWithFlags(&ev_loaded[i], cudaEventDisableTiming)) ||
-          fail(cudaEventCreateWithFlags(&ev_free[i], cudaEventDisableTiming))) {
-        cleanup();
-        return rc;
-      }
-    }
-  }
-  const uint8_t* host = static_cast<const uint8_t*>(buf->host_weights);
-  uint8_t* window = static_cast<uint8_t*>(buf->window);
+  const uint8_t* host = static_cast<const uint8_t*>(buf.host_weights);
+  uint8_t* window = static_cast<uint8_t*>(buf.window);
+#define WS_STEP_TRY(x)                          \
+  do {                                          \
+    if ((x) != cudaSuccess) return WS_ERR_CUDA; \
+  } while (0)
   auto ensure = [&](int blk) -> ws_status {
     const int sl = blk % 2;
     if (slot_block[sl] == blk) return WS_OK;
     ws_status r = ws_stream_block_h2d(host + (size_t)blk * bbytes, window + (size_t)sl * bbytes,
-                                      bbytes, copy_stream,
-                                      slot_used[sl] ? (ws_event_t)ev_free[sl] : nullptr,
-                                      (ws_event_t)ev_loaded[sl]);
+                                      bbytes, (ws_stream_t)ps,
+                                      slot_used[sl] ? (ws_event_t)ev.freed[sl] : nullptr,
+                                      (ws_event_t)ev.loaded[sl]);
     if (r == WS_OK) slot_block[sl] = blk;
     return r;
   };
   auto block_ptr = [&](int blk) -> const void* {
     if (streamed) return window + (size_t)(blk % 2) * bbytes;
-    return static_cast<const uint8_t*>(buf->dev_weights) + (size_t)blk * bbytes;
+    return static_cast<const uint8_t*>(buf.dev_weights) + (size_t)blk * bbytes;
   };
-  auto wait_loaded = [&](int blk) {
-    return streamed ? cudaStreamWaitEvent(cs, ev_loaded[blk % 2], 0) : cudaSuccess;
-  };
-  auto release = [&](int blk) {
-    if (!streamed) return cudaSuccess;
-    slot_used[blk % 2] = true;
-    return cudaEventRecord(ev_free[blk % 2], cs);
-  };
-
+  ws_status rc = WS_OK;
+  if (streamed) {
+    WS_STEP_TRY(cudaEventRecord(ev.fork, cs));
+    WS_STEP_TRY(cudaStreamWaitEvent(ps, ev.fork, 0));
+  }
   // ---- forward
-  if (fail(cudaMemcpyAsync(bnd, h0, (size_t)MH * 4, cudaMemcpyDeviceToDevice, cs))) goto done;
-  if (streamed && (rc = ensure(0)) != WS_OK) goto done;
+  if (streamed && (rc = ensure(0)) != WS_OK) return rc;
   for (int b = 0; b < nb; ++b) {
-    if (streamed && b + 1 < nb && (rc = ensure(b + 1)) != WS_OK) goto done;
-    if (fail(wait_loaded(b))) goto done;
-    void* sv = streamed ? nullptr : static_cast<uint8_t*>(buf->saved) + (size_t)b * block_layers * slayer;
-    if (fail(block_forward(*cfg, block_layers, block_ptr(b), b * block_layers, block_layers,
-                           buf->params, step, bnd + (size_t)b * MH, bnd + (size_t)(b + 1) * MH, sv,
-                           buf->workspace, cs)))
-      goto done;
-    if (fail(release(b))) goto done;
+    if (streamed && b + 1 < nb && (rc = ensure(b + 1)) != WS_OK) return rc;
+    if (streamed) WS_STEP_TRY(cudaStreamWaitEvent(cs, ev.loaded[b % 2], 0));
+    void* sv = streamed ? nullptr : static_cast<uint8_t*>(buf.saved) + (size_t)b * block_layers * slayer;
+    WS_STEP_TRY(block_forward(cfg, block_layers, block_ptr(b), b * block_layers, block_layers,
+                              buf.params, 0u, stepw, bnd + (size_t)b * MH, bnd + (size_t)(b + 1) * MH,
+                              sv, buf.workspace, cs));
+    if (streamed) {
+      slot_used[b % 2] = true;
+      WS_STEP_TRY(cudaEventRecord(ev.freed[b % 2], cs));
+    }
   }
   // ---- loss
-  if (fail(loss_and_grad(*cfg, block_layers, bnd + (size_t)nb * MH, buf->dh, buf->loss,
-                         buf->workspace, cs)))
-    goto done;
+  WS_STEP_TRY(loss_and_grad(cfg, block_layers, bnd + (size_t)nb * MH, buf.dh, buf.loss, buf.workspace, cs));
   // ---- backward, blocks in reverse
   for (int b = nb - 1; b >= 0; --b) {
     if (streamed) {
-      if ((rc = ensure(b)) != WS_OK) goto done;
-      if (b - 1 >= 0 && (rc = ensure(b - 1)) != WS_OK) goto done;
+      if ((rc = ensure(b)) != WS_OK) return rc;
+      if (b - 1 >= 0 && (rc = ensure(b - 1)) != WS_OK) return rc;
+      WS_STEP_TRY(cudaStreamWaitEvent(cs, ev.loaded[b % 2], 0));
     }
-    if (fail(wait_loaded(b))) goto done;
     const void* sv =
-        streamed ? nullptr : static_cast<uint8_t*>(buf->saved) + (size_t)b * block_layers * slayer;
-    if (fail(block_backward(*cfg, block_layers, block_ptr(b), b * block_layers, block_layers,
-                            buf->params, step, bnd + (size_t)b * MH, sv, buf->dh, buf->dh,
-                            buf->grads, buf->workspace, cs)))
-      goto done;
-    if (fail(release(b))) goto done;
+        streamed ? nullptr : static_cast<uint8_t*>(buf.saved) + (size_t)b * block_layers * slayer;
+    WS_STEP_TRY(block_backward(cfg, block_layers, block_ptr(b), b * block_layers, block_layers,
+                               buf.params, 0u, stepw, bnd + (size_t)b * MH, sv, buf.dh, buf.dh,
+                               buf.grads, buf.workspace, cs));
+    if (streamed) {
+      slot_used[b % 2] = true;
+      WS_STEP_TRY(cudaEventRecord(ev.freed[b % 2], cs));
+    }
   }
   // ---- optimizer
-  if (fail(adam_step(buf->params, buf->grads, buf->adam_m, buf->adam_v, np, (int64_t)step + 1, lr, cs)))
-    goto done;
-done:
-  cleanup();
-  return rc;
+  WS_STEP_TRY(adam_step(buf.params, buf.grads, buf.adam_m, buf.adam_v, np, stepw, lr, cs));
+  if (streamed) {
+    WS_STEP_TRY(cudaEventRecord(ev.join, ps));
+    WS_STEP_TRY(cudaStreamWaitEvent(cs, ev.join, 0));
+  }
+#undef WS_STEP_TRY
+  return WS_OK;
+}
+
+ws_status step_prologue(const ws_stack_cfg& cfg, int block_layers, const ws_stack_buffers& buf,
+                        uint32_t step, const float* h0, cudaStream_t cs) {
+  uint32_t* stepw = stack_step_word(cfg, block_layers, buf.workspace);
+  if (set_step(stepw, step, cs) != cudaSuccess) return WS_ERR_CUDA;
+  if (cudaMemcpyAsync(buf.boundary, h0, (size_t)(cfg.M * cfg.H) * 4, cudaMemcpyDeviceToDevice,
+                      cs) != cudaSuccess)
+    return WS_ERR_CUDA;
+  return WS_OK;
+}
+
+}  // namespace
+
+struct ws_step_graph {
+  ws_stack_cfg cfg;
+  int32_t block_layers;
+  ws_stack_buffers buf;
+  StepEvents ev;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+extern "C" {
+
+ws_status ws_stack_train_step(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
+                              const ws_stack_buffers* buf, uint32_t step, const float* h0, float lr,
+                              ws_stream_t compute, ws_stream_t copy_stream) {
+  ws_status s = check_step(cfg, block_layers, streamed, buf, copy_stream);
+  if (s != WS_OK) return s;
+  if (!h0) return WS_ERR_INVALID;
+  const cudaStream_t cs = (cudaStream_t)compute;
+  s = step_prologue(*cfg, block_layers, *buf, step, h0, cs);
+  if (s != WS_OK) return s;
+  StepEvents ev;
+  if (streamed && ev.create() != cudaSuccess) {
+    ev.destroy();
+    return WS_ERR_CUDA;
+  }
+  s = step_body(*cfg, block_layers, streamed != 0, *buf, lr, cs, (cudaStream_t)copy_stream, ev);
+  ev.destroy();
+  return s;
+}
+
+ws_status ws_stack_graph_create(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
+                                const ws_stack_buffers* buf, float lr, ws_stream_t compute,
+                                ws_stream_t copy_stream, ws_step_graph** out) {
+  if (!out) return WS_ERR_INVALID;
+  *out = nullptr;
+  ws_status s = check_step(cfg, block_layers, streamed, buf, copy_stream);
+  if (s != WS_OK) return s;
+  ws_step_graph* g = new (std::nothrow) ws_step_graph();
+  if (!g) return WS_ERR_OOM;
+  g->cfg = *cfg;
+  g->block_layers = block_layers;
+  g->buf = *buf;
+  const cudaStream_t cs = (cudaStream_t)compute;
+  if (g->ev.create() != cudaSuccess) {
+    g->ev.destroy();
+    delete g;
+    return WS_ERR_CUDA;
+  }
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+    g->ev.destroy();
+    delete g;
+    return WS_ERR_CUDA;
+  }
+  s = step_body(*cfg, block_layers, streamed != 0, *buf, lr, cs, (cudaStream_t)copy_stream, g->ev);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(cs, &graph);
+  if (s == WS_OK && ec != cudaSuccess) s = WS_ERR_CUDA;
+  if (s == WS_OK && cudaGraphInstantiate(&g->exec, graph, 0) != cudaSuccess) s = WS_ERR_CUDA;
+  g->graph = graph;
+  if (s != WS_OK) {
+    cudaGetLastError();
+    ws_stack_graph_destroy(g);
+    return s;
+  }
+  *out = g;
+  return WS_OK;
+}
+
+ws_status ws_stack_graph_step(ws_step_graph* g, uint32_t step, const float* h0,
+                              ws_stream_t compute) {
+  if (!g || !h0) return WS_ERR_INVALID;
+  const cudaStream_t cs = (cudaStream_t)compute;
+  ws_status s = step_prologue(g->cfg, g->block_layers, g->buf, step, h0, cs);
+  if (s != WS_OK) return s;
+  return cudaGraphLaunch(g->exec, cs) == cudaSuccess ? WS_OK : WS_ERR_CUDA;
+}
+
+ws_status ws_stack_graph_destroy(ws_step_graph* g) {
+  if (!g) return WS_ERR_INVALID;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  g->ev.destroy();
+  delete g;
+  return WS_OK;
 }
 
 }  // extern "C"

@@ -24,6 +24,7 @@ enum : uint32_t {
   DERR_TIMEOUT_ACC = 1u << 4,
   DERR_TIMEOUT_DRAIN = 1u << 5,
   DERR_BAD_CONFIG = 1u << 6,
+  DERR_TIMEOUT_PEER = 1u << 7,
 };
 
 #ifdef WS_GEMM_TU
@@ -84,7 +85,12 @@ struct DropKey {
   uint32_t c1, c2, c3;
   uint32_t thresh;   // keep <=> word >= thresh  (thresh_is_max: drop all)
   uint32_t drop_all; // p == 1 (threshold 2^32)
+  const uint32_t* step_dev;  // when set, the step word c3 is read from here
 };
+// Resolve the step word once per thread (device-resident step for graphs).
+WS_DEVINL void resolve_step(DropKey& k) {
+  if (k.step_dev) k.c3 = *k.step_dev;
+}
 WS_DEVINL uint32_t keep4(const DropKey& k, uint64_t e0) {
   if (k.drop_all) return 0u;
   const u32x4 r = philox4x32_10(u32x4{(uint32_t)(e0 >> 2), k.c1, k.c2, k.c3}, k.k0, k.k1);
@@ -156,6 +162,16 @@ WS_DEVINL bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, uint32_t why) {
   }
 }
 #endif
+
+// ---- cross-CTA flags ---------------------------------------------------------------------
+WS_DEVINL uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+WS_DEVINL void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 // ---- fences ----------------------------------------------------------------------------
 // Make generic-proxy shared-memory writes visible to the async proxy

@@ -31,7 +31,8 @@ struct GemmArgs {
   const uint32_t* mask; // backward: dropout bits [M, K/32]
   void* out;            // [M, Nout] bf16 or fp32
   int out_f32, out_accum;
-  float* partial;       // [grid, 2, BM, BN] fp32 partial tiles of cut tiles
+  float* partial;       // [grid, BM, BN] fp32 partial tile of each CTA's cut first segment
+  uint32_t* flags;      // [grid] set to 1 once that partial is complete (zeroed per launch)
 };
 
 // Tile configuration: a pure function of the shape and the SM count, so a
@@ -65,6 +66,7 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
 // ---- small kernels (lora_small.cu) ----------------------------------------------------
 struct DropKeyHost {
   uint32_t k0, k1, c1, c2, c3, thresh, drop_all;
+  const uint32_t* step_dev;  // device step word (replaces c3) or NULL
 };
 DropKeyHost make_drop_key(const ws_dropout_key& k);
 
@@ -87,6 +89,16 @@ cudaError_t run_lora_wgrad(const float* P, const uint16_t* Q, const uint32_t* ma
                            int64_t C, float s, float* out, int transpose_out, float* partial,
                            cudaStream_t st);
 cudaError_t run_mask_gen(int64_t M, int64_t K, const DropKeyHost& key, uint32_t* mask,
+                         cudaStream_t st);
+// Fixed-order sum of chunk partials [chunks][C][16], scaled by s, into
+// out [C][16] (or [16][C] when transpose_out).
+cudaError_t run_wgrad_reduce(const float* partial, int chunks, int64_t C, float s, float* out,
+                             int transpose_out, cudaStream_t st);
+// The same weight gradients on the tensor cores (nf4_gemm.cu): workspace of
+// wgrad_tc_bytes(M, C).
+size_t wgrad_tc_bytes(int64_t M, int64_t C);
+cudaError_t run_wgrad_tc(const float* P, const uint16_t* Q, const uint32_t* mask, int64_t M,
+                         int64_t C, float s, float* out, int transpose_out, void* ws,
                          cudaStream_t st);
 
 // ---- one LoRA linear (linear.cu) --------------------------------------------------------
@@ -112,15 +124,22 @@ void stack_weight_offset(const ws_stack_cfg& c, int layer_in_block, int lin, siz
                          size_t* off_absmax);
 void stack_param_offset(const ws_stack_cfg& c, int layer, int lin, int64_t* off_A, int64_t* off_B);
 bool stack_saved_offset(const ws_stack_cfg& c, int field, int lin, size_t* off);
+// step_dev: device step word for the dropout keys (NULL: use `step`).
 cudaError_t block_forward(const ws_stack_cfg& c, int block_layers_ws, const void* block,
                           int first_layer, int n_layers, const float* params, uint32_t step,
-                          const float* h_in, float* h_out, void* saved, void* ws, cudaStream_t st);
+                          const uint32_t* step_dev, const float* h_in, float* h_out, void* saved,
+                          void* ws, cudaStream_t st);
 cudaError_t block_backward(const ws_stack_cfg& c, int block_layers_ws, const void* block,
                            int first_layer, int n_layers, const float* params, uint32_t step,
-                           const float* h_in, const void* saved, const float* dh_out, float* dh_in,
-                           float* grads, void* ws, cudaStream_t st);
+                           const uint32_t* step_dev, const float* h_in, const void* saved,
+                           const float* dh_out, float* dh_in, float* grads, void* ws,
+                           cudaStream_t st);
+// Device word reserved in the stack workspace for the step counter.
+uint32_t* stack_step_word(const ws_stack_cfg& c, int block_layers, void* ws);
 cudaError_t loss_and_grad(const ws_stack_cfg& c, int block_layers_ws, const float* h, float* dh,
                           float* loss, void* ws, cudaStream_t st);
-cudaError_t adam_step(float* p, const float* g, float* m, float* v, int64_t n, int64_t t, float lr,
-                      cudaStream_t st);
+// Adam at step t = *step_dev + 1 (bias corrections computed on the device).
+cudaError_t adam_step(float* p, const float* g, float* m, float* v, int64_t n,
+                      const uint32_t* step_dev, float lr, cudaStream_t st);
+cudaError_t set_step(uint32_t* step_dev, uint32_t step, cudaStream_t st);
 }  // namespace ws

@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(256, 2) k_skinny_partial(const uint16_t* __res
                                                            uint8_t* __restrict__ mask_bytes,
                                                            float* __restrict__ partial) {
   __shared__ __align__(16) float sF[16][kSkCols];
+  if (MASKED) resolve_step(key);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m0 = (int64_t)blockIdx.x * kSkRows + warp * 4;
   float acc[64];
@@ -309,7 +310,9 @@ __global__ void k_wgrad_reduce(const float* __restrict__ partial, int chunks, in
 int wgrad_chunks(int64_t M, int64_t C) {
   const int64_t cblocks = (C + kWgradCols - 1) / kWgradCols;
   int64_t want = (2 * device_sm_count() + cblocks - 1) / cblocks;
-  const int64_t maxc = (M + 15) / 16;
+  // at least 64 rows per chunk: below that the partials cost more traffic
+  // than the rows they sum
+  const int64_t maxc = (M + 63) / 64;
   if (want > maxc) want = maxc;
   if (want < 1) want = 1;
   return (int)want;
@@ -319,6 +322,7 @@ int wgrad_chunks(int64_t M, int64_t C) {
 __global__ void k_mask_gen(int64_t words, DropKey key, uint32_t* __restrict__ mask) {
   const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (w >= words) return;
+  resolve_step(key);
   const uint64_t e0 = (uint64_t)w * 32;
   uint32_t bits = 0;
 #pragma unroll
@@ -335,6 +339,7 @@ DropKey to_dev(const DropKeyHost& h) {
   k.c3 = h.c3;
   k.thresh = h.thresh;
   k.drop_all = h.drop_all;
+  k.step_dev = h.step_dev;
   return k;
 }
 
@@ -344,6 +349,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 DropKeyHost make_drop_key(const ws_dropout_key& k) {
   DropKeyHost h{};
+  h.step_dev = nullptr;
   h.k0 = (uint32_t)k.seed;
   h.k1 = (uint32_t)(k.seed >> 32);
   h.c1 = k.linear | (k.microbatch << 8);
@@ -424,6 +430,15 @@ cudaError_t run_lora_wgrad(const float* P, const uint16_t* Q, const uint32_t* ma
   return cudaGetLastError();
 }
 
+cudaError_t run_wgrad_reduce(const float* partial, int chunks, int64_t C, float s, float* out,
+                             int transpose_out, cudaStream_t st) {
+  const int64_t n = C * 16;
+  note_launch();
+  k_wgrad_reduce<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(partial, chunks, C, s, out,
+                                                              transpose_out);
+  return cudaGetLastError();
+}
+
 cudaError_t run_mask_gen(int64_t M, int64_t K, const DropKeyHost& key, uint32_t* mask,
                          cudaStream_t st) {
   const int64_t words = M * K / 32;
@@ -453,8 +468,8 @@ LinWs lin_ws_layout(int64_t M, int64_t N, int64_t K) {
   w.mask = off;
   off += align256((size_t)M * (size_t)(K / 32) * 4);
   w.wgrad = off;
-  const size_t wg = wgrad_partial_bytes(M, N) > wgrad_partial_bytes(M, K) ? wgrad_partial_bytes(M, N)
-                                                                          : wgrad_partial_bytes(M, K);
+  const size_t wg = wgrad_tc_bytes(M, N) > wgrad_tc_bytes(M, K) ? wgrad_tc_bytes(M, N)
+                                                                : wgrad_tc_bytes(M, K);
   off += align256(wg);
   w.skinny = off;
   const size_t sk = skinny_partial_bytes(M, N) > skinny_partial_bytes(M, K) ? skinny_partial_bytes(M, N)
@@ -505,11 +520,11 @@ cudaError_t linear_bwd(const NF4View& W, const uint16_t* x, const float* A, cons
   e = run_lora_G(dY, B, M, W.N, G, Gext, reinterpret_cast<float*>(w + L.skinny), st);
   if (e != cudaSuccess) return e;
   if (dB) {
-    e = run_lora_wgrad(U, dY, nullptr, M, W.N, scale, dB, 0, wg, st);
+    e = run_wgrad_tc(U, dY, nullptr, M, W.N, scale, dB, 0, wg, st);
     if (e != cudaSuccess) return e;
   }
   if (dA) {
-    e = run_lora_wgrad(G, x, mask, M, W.K, scale, dA, 1, wg, st);
+    e = run_wgrad_tc(G, x, mask, M, W.K, scale, dA, 1, wg, st);
     if (e != cudaSuccess) return e;
   }
   if (dX) {

@@ -19,12 +19,15 @@
 // one dequantised weight tile), BN output columns, 64-deep contraction steps.
 //
 // Schedule: the (tile, step) iterations of the whole problem are cut into
-// gridDim.x equal contiguous ranges, one per CTA (stream-K).  A tile that a
-// range boundary cuts is finished by a fixed-order fix-up kernel that adds
-// the CTAs' fp32 partial tiles in step order; every other tile is written
-// by its CTA's epilogue.  The cut points depend only on the shape and the
-// grid size, so results are deterministic and identical run to run.  No
-// atomics anywhere.
+// gridDim.x equal contiguous ranges, one per CTA (stream-K), launched
+// cooperatively so every CTA is resident.  A tile cut by range boundaries is
+// finished by the CTA holding its first steps -- that is always the last
+// segment of that CTA's range, so it runs after the other pieces were made:
+// it adds the later CTAs' fp32 partial tiles to its own accumulator in step
+// order (after waiting, with a time limit, for their completion flags) and
+// stores the tile.  Every other tile is stored by its CTA directly.  The cut
+// points depend only on the shape and the grid size, so results are
+// deterministic and identical run to run.  No atomics on data.
 //
 // The LoRA terms use the same tensor cores: the forward appends one 64-deep
 // step whose A operand is [U_hi | U_lo | U_hi | 0] and whose B operand is
@@ -49,12 +52,17 @@ cudaError_t read_and_clear_dev_error(uint32_t* flags) {
   return cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(uint32_t));
 }
 
-__constant__ float c_nf4_levels[16] = {-1.0f,    -0.6962f, -0.5251f, -0.3949f,
-                                       -0.2844f, -0.1848f, -0.0911f, 0.0f,
-                                       0.0796f,  0.1609f,  0.2461f,  0.3379f,
-                                       0.4407f,  0.5626f,  0.7230f,  1.0f};
 
 namespace {
+
+// Pipeline depths: dequantised-operand buffers and TMA stages (upper bound;
+// the shared-memory budget may allow fewer).
+#ifndef WS_GEMM_BSTAGES
+#define WS_GEMM_BSTAGES 2
+#endif
+#ifndef WS_GEMM_STAGES_MAX
+#define WS_GEMM_STAGES_MAX 4
+#endif
 
 constexpr int kDqWarps = 8;
 constexpr int kEpiWarps = 4;
@@ -68,11 +76,11 @@ struct Cfg {
   static constexpr uint32_t B_BYTES = BN * 128;   // BN x 64 bf16
   static constexpr uint32_t C_BYTES = BN * 32;    // codes: BN x 64 nibbles
   static constexpr uint32_t S_BYTES = BN * 4;     // absmax: BN floats
-  static constexpr int BSTAGES = 2;
+  static constexpr int BSTAGES = WS_GEMM_BSTAGES;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + C_BYTES + S_BYTES;
   static constexpr int STAGES_RAW =
       (int)((220u * 1024u - BSTAGES * B_BYTES - 1024u) / STAGE_BYTES);
-  static constexpr int STAGES = STAGES_RAW > 4 ? 4 : STAGES_RAW;
+  static constexpr int STAGES = STAGES_RAW > WS_GEMM_STAGES_MAX ? WS_GEMM_STAGES_MAX : STAGES_RAW;
   // one accumulator set: D (and for the backward the LoRA term D2)
   static constexpr uint32_t ACC_COLS = (BWD ? 2u : 1u) * UM * BN;
   // double-buffer the accumulator when TMEM has room, so the epilogue of
@@ -109,9 +117,6 @@ WS_DEVINL void sts128(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d
   *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
 }
 
-// Dequantise 4 code bytes (8 consecutive weights along k) into a 16-byte
-// chunk of bf16 values: element 2i from the high nibble of byte i, element
-// 2i+1 from its low nibble.
 // Two IEEE fp32 products (round to nearest) in one packed instruction.
 WS_DEVINL void mul2_rn(float x0, float x1, float s, float& r0, float& r1) {
   asm("{\n .reg .b64 pa, pb, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %4};\n"
@@ -120,14 +125,66 @@ WS_DEVINL void mul2_rn(float x0, float x1, float s, float& r0, float& r1) {
       : "f"(x0), "f"(x1), "f"(s));
 }
 
-WS_DEVINL uint4 dq8(uint32_t w, float a, const float* lv) {
+// Byte permute: bytes of {b, a} (a = bytes 0-3, b = 4-7) picked by the four
+// 4-bit fields of sel.
+WS_DEVINL uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// The 16 dequantised values of one 64-weight block, T[i] = bf16_RN(c_i * a)
+// (one fp32 product, one rounding), split into byte planes: lo[q] holds the
+// low bytes of T[4q..4q+3], hi[q] their high bytes.  A 4-bit code then
+// becomes a bf16 value with byte permutes in registers -- no shared-memory
+// table lookup per weight.
+struct Nf4Table {
+  uint32_t lo[4], hi[4];
+};
+WS_DEVINL Nf4Table make_table(float a) {
+  uint32_t R[8];
+  float v0, v1;
+  mul2_rn(-1.0f, -0.6962f, a, v0, v1);
+  R[0] = pack_bf16x2(v0, v1);
+  mul2_rn(-0.5251f, -0.3949f, a, v0, v1);
+  R[1] = pack_bf16x2(v0, v1);
+  mul2_rn(-0.2844f, -0.1848f, a, v0, v1);
+  R[2] = pack_bf16x2(v0, v1);
+  mul2_rn(-0.0911f, 0.0f, a, v0, v1);
+  R[3] = pack_bf16x2(v0, v1);
+  mul2_rn(0.0796f, 0.1609f, a, v0, v1);
+  R[4] = pack_bf16x2(v0, v1);
+  mul2_rn(0.2461f, 0.3379f, a, v0, v1);
+  R[5] = pack_bf16x2(v0, v1);
+  mul2_rn(0.4407f, 0.5626f, a, v0, v1);
+  R[6] = pack_bf16x2(v0, v1);
+  mul2_rn(0.7230f, 1.0f, a, v0, v1);
+  R[7] = pack_bf16x2(v0, v1);
+  Nf4Table t;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    t.lo[q] = prmt(R[2 * q], R[2 * q + 1], 0x6420u);
+    t.hi[q] = prmt(R[2 * q], R[2 * q + 1], 0x7531u);
+  }
+  return t;
+}
+
+// 4 code bytes (8 consecutive weights along k: byte i holds k = 2i in its
+// high nibble, 2i+1 in its low nibble) -> 8 bf16 values in k order.
+WS_DEVINL uint4 dq8(uint32_t w, const Nf4Table& t) {
+  // nibble-swap each byte so the fields run in k order: field f = code of k = f
+  const uint32_t ws = ((w >> 4) & 0x0F0F0F0Fu) | ((w << 4) & 0xF0F0F0F0u);
+  const uint32_t s7 = ws & 0x77777777u;                           // index within 8 entries
+  const uint32_t s8 = ((ws >> 1) & 0x44444444u) | 0x32103210u;   // which half (code >= 8)
   uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t byte = (w >> (8 * i)) & 0xFFu;
-    float v0, v1;
-    mul2_rn(lv[byte >> 4], lv[byte & 15u], a, v0, v1);
-    o[i] = pack_bf16x2(v0, v1);
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t a7 = h ? (s7 >> 16) : s7;
+    const uint32_t a8 = h ? (s8 >> 16) : s8;
+    const uint32_t lo = prmt(prmt(t.lo[0], t.lo[1], a7), prmt(t.lo[2], t.lo[3], a7), a8);
+    const uint32_t hi = prmt(prmt(t.hi[0], t.hi[1], a7), prmt(t.hi[2], t.hi[3], a7), a8);
+    o[2 * h] = prmt(lo, hi, 0x5140u);
+    o[2 * h + 1] = prmt(lo, hi, 0x7362u);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
@@ -135,30 +192,29 @@ WS_DEVINL uint4 dq8(uint32_t w, float a, const float* lv) {
 // Forward weight tile, K-major 128B-swizzled: row j = output column n0 + j,
 // 64 contraction elements; chunk cc of row j sits at (cc ^ (j & 7)) * 16.
 template <int BN>
-WS_DEVINL void dequant_fwd(const uint8_t* sC, const float* sS, uint8_t* sB, int t,
-                           const float* lv) {
+WS_DEVINL void dequant_fwd(const uint8_t* sC, const float* sS, uint8_t* sB, int t) {
   if constexpr (BN == 256) {
     const int j = t;
     const uint4 c0 = *reinterpret_cast<const uint4*>(sC + j * 32);
     const uint4 c1 = *reinterpret_cast<const uint4*>(sC + j * 32 + 16);
-    const float a = sS[j];
+    const Nf4Table tb = make_table(sS[j]);
     const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
     uint8_t* row = sB + j * 128;
 #pragma unroll
     for (int cc = 0; cc < 8; ++cc) {
-      const uint4 v = dq8(words[cc], a, lv);
+      const uint4 v = dq8(words[cc], tb);
       sts128(row + ((cc ^ (j & 7)) << 4), v.x, v.y, v.z, v.w);
     }
   } else {
     const int j = t >> 1, half = t & 1;
     const uint4 c = *reinterpret_cast<const uint4*>(sC + j * 32 + half * 16);
-    const float a = sS[j];
+    const Nf4Table tb = make_table(sS[j]);
     const uint32_t words[4] = {c.x, c.y, c.z, c.w};
     uint8_t* row = sB + j * 128;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int cc = half * 4 + q;
-      const uint4 v = dq8(words[q], a, lv);
+      const uint4 v = dq8(words[q], tb);
       sts128(row + ((cc ^ (j & 7)) << 4), v.x, v.y, v.z, v.w);
     }
   }
@@ -170,8 +226,7 @@ WS_DEVINL void dequant_fwd(const uint8_t* sC, const float* sS, uint8_t* sB, int 
 // group (c/8, j/64) at (c/8)*SBO + (j/64)*LBO, row c%8 inside the group,
 // chunk ((j%64)/8) ^ (c%8).
 template <int BN>
-WS_DEVINL void dequant_bwd(const uint8_t* sC, const float* sS, uint8_t* sB, int t,
-                           const float* lv) {
+WS_DEVINL void dequant_bwd(const uint8_t* sC, const float* sS, uint8_t* sB, int t) {
   using C = Cfg<true, 1, BN>;
   constexpr int SEGS = BN / 32;                  // 32-column segments per row
   constexpr int ITEMS = 64 * SEGS / kDqThreads;  // rows*segs per thread
@@ -180,14 +235,14 @@ WS_DEVINL void dequant_bwd(const uint8_t* sC, const float* sS, uint8_t* sB, int 
     const int item = t + it * kDqThreads;
     const int c = item / SEGS, seg = item % SEGS;
     const uint4 cw = *reinterpret_cast<const uint4*>(sC + c * (BN / 2) + seg * 16);
-    const float a = sS[((seg * 32) / 64) * 64 + c];
+    const Nf4Table tb = make_table(sS[((seg * 32) / 64) * 64 + c]);
     const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
     const int mg = (seg * 32) / 64;
     uint8_t* grp = sB + (c >> 3) * C::MN_SBO + mg * C::MN_LBO + (c & 7) * 128;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int cc = ((seg * 32) % 64) / 8 + q;
-      const uint4 v = dq8(words[q], a, lv);
+      const uint4 v = dq8(words[q], tb);
       sts128(grp + ((cc ^ (c & 7)) << 4), v.x, v.y, v.z, v.w);
     }
   }
@@ -243,7 +298,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NACC = C::ACC_BUFS;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ float s_lv[16];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem + C::OFF_A;
@@ -292,7 +346,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     fence_barrier_init();
   }
-  if (threadIdx.x < 16) s_lv[threadIdx.x] = c_nf4_levels[threadIdx.x];
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
@@ -449,8 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(args.has_lora && i == args.nk_total)) {
           const uint8_t* cs = sC + s * C::C_BYTES;
           const float* ss = reinterpret_cast<const float*>(sS + s * C::S_BYTES);
-          if (!BWD) dequant_fwd<BN>(cs, ss, Bt, t_idx, s_lv);
-          else dequant_bwd<BN>(cs, ss, Bt, t_idx, s_lv);
+          if (!BWD) dequant_fwd<BN>(cs, ss, Bt, t_idx);
+          else dequant_bwd<BN>(cs, ss, Bt, t_idx);
         } else {
           lora_tile<BWD, BN>(args.lora_F, args.Nout, args.Nout, n0, args.lora_scale, Bt, t_idx);
         }
@@ -494,11 +547,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t m0 = (t % args.mtiles) * C::BM;
         const int64_t n0 = (t / args.mtiles) * BN;
         const bool whole = (i0 == 0 && kb == S);
+        // the tile's first steps with the rest held by later CTAs: finish it here
+        const bool finisher = (i0 == 0 && kb < S);
+        const bool writer = !whole && !finisher;  // a later piece: hand it over
         const bool lora_in = args.has_lora && kb == S;
         // a backward segment made of the LoRA step alone never wrote D
         const bool main_in = !BWD || i0 < args.nk_total;
-        const int slot = seg == 0 ? 0 : 1;
-        float* part = args.partial + ((int64_t)blockIdx.x * 2 + slot) * C::TILE_FLOATS;
+        float* part = args.partial + (int64_t)blockIdx.x * C::TILE_FLOATS;
+        int64_t g_last = blockIdx.x;
+        if (finisher) {
+          g_last = sk_cta_of(t * S + S - 1, I, G);
+          // wait for the later pieces (each CTA publishes at most one)
+          bool got = ok;
+          for (int64_t g = (int64_t)blockIdx.x + 1; g <= g_last && got; ++g) {
+            const uint32_t* f = args.flags + g;
+            if (ld_acquire_gpu(f) != 1u) {
+              const uint64_t t0 = globaltimer();
+              while (ld_acquire_gpu(f) != 1u) {
+                __nanosleep(128);
+                if (globaltimer() - t0 > kWaitLimitNs) {
+                  atomicOr(&g_dev_error, DERR_TIMEOUT_PEER);
+                  got = false;
+                  break;
+                }
+              }
+            }
+          }
+          if (!got) g_last = blockIdx.x;  // timed out: store what is here, flagged as an error
+        }
         const uint32_t dbase = tmem + (uint32_t)(a * C::ACC_COLS);
 #pragma unroll 1
         for (int u = 0; u < UM; ++u) {
@@ -525,12 +601,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 32; ++e)
                 if ((bits >> e) & 1u) v[e] += __uint_as_float(lacc[e]);
             }
-            if (!whole) {
+            if (writer) {
               float4* dst = reinterpret_cast<float4*>(part + (int64_t)row * BN + cc);
 #pragma unroll
               for (int e = 0; e < 8; ++e)
                 dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-            } else if (args.out_f32) {
+              continue;
+            }
+            // finisher: add the later pieces in step order
+            for (int64_t g = (int64_t)blockIdx.x + 1; g <= g_last; ++g) {
+              const float4* src = reinterpret_cast<const float4*>(
+                  args.partial + g * C::TILE_FLOATS + (int64_t)row * BN + cc);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float4 pv = src[e];
+                v[4 * e] += pv.x;
+                v[4 * e + 1] += pv.y;
+                v[4 * e + 2] += pv.z;
+                v[4 * e + 3] += pv.w;
+              }
+            }
+            if (args.out_f32) {
               float4* dst =
                   reinterpret_cast<float4*>(static_cast<float*>(args.out) + m * args.Nout + n);
 #pragma unroll
@@ -557,6 +648,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if (writer) {
+          // publish the piece: every epilogue thread's stores, then one flag
+          __threadfence();
+          named_bar_sync(1, kEpiWarps * 32);
+          if (warp == 2 + kDqWarps && lane == 0) st_release_gpu(args.flags + blockIdx.x, 1u);
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&accempty[a]);
@@ -571,64 +668,196 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-// Tiles cut by a stream-K range boundary: add the CTAs' partial tiles in
-// step order (the CTA holding the tile's first steps first) and store.
-// A partial of CTA g sits in slot 0 when the tile is g's first segment,
-// slot 1 when it is g's last.
-template <int BM, int BN>
-__global__ void __launch_bounds__(256) k_streamk_fixup(const float* __restrict__ partial,
-                                                       int64_t S, int mtiles, int ntiles, int64_t G,
-                                                       int64_t M, int64_t Nout, void* out,
-                                                       int out_f32, int out_accum) {
-  constexpr int kMaxParts = 64;
-  __shared__ const float* s_part[kMaxParts];
-  __shared__ int s_nparts;
-  const int64_t t = blockIdx.x;
-  const int64_t I = (int64_t)mtiles * ntiles * S;
-  const int64_t g1 = sk_cta_of(t * S, I, G);
-  const int64_t g2 = sk_cta_of(t * S + S - 1, I, G);
-  if (g1 == g2) return;
+// ------------------------------------------------------------------------ LoRA weight gradients
+// out[c][j] = s * sum_m P[m][j] * Q~[m][c] (dB: P = U, Q = dY; dA: P = G,
+// Q = x under the dropout mask) as a tensor-core GEMM D = P^T Q:
+//   A = [P_hi^T ; P_lo^T ; 0] (128 x 64 tokens per step, bf16 high/low
+//       parts of the fp32 P, K-major, TMA with 128-byte swizzle),
+//   B = Q tile (64 tokens x 256 columns, MN-major, four TMA boxes of 64
+//       columns), masked in shared memory for dA by four warps,
+//   D = 128 x 256 fp32 in TMEM; rows j and 16+j add up to P^T Q.
+// Grid: 256-column tiles x token chunks; each CTA writes the fp32 partial of
+// its chunk and a second kernel sums the chunks in index order.
+constexpr int kWgThreads = 192;
+constexpr int kWgStages = 4;
+constexpr uint32_t kWgA = 128 * 128;      // A stage bytes
+constexpr uint32_t kWgB = 4 * 64 * 128;   // B stage bytes (4 boxes of 64 rows x 128 B)
+constexpr uint32_t kWgSmem = kWgStages * (kWgA + kWgB) + (3 * kWgStages + 1) * 8 + 16 + 1024;
+
+template <bool MASKED>
+__global__ void __launch_bounds__(kWgThreads, 1)
+    k_wgrad_tc(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
+               const uint32_t* __restrict__ mask, int64_t M, int64_t C, int steps_per_chunk,
+               float* __restrict__ partial) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kWgStages * kWgA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kWgStages * kWgB);
+  uint64_t* masked = full + kWgStages;
+  uint64_t* empty = masked + kWgStages;
+  uint64_t* accfull = empty + kWgStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accfull + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  volatile uint32_t* skip_flag = tmem_slot + 2;
+  const int warp = (int)warp_id(), lane = (int)lane_id();
+  const int64_t c0 = (int64_t)blockIdx.x * 256;
+  const int64_t total_steps = (M + 63) / 64;
+  const int64_t s_begin = (int64_t)blockIdx.y * steps_per_chunk;
+  const int64_t s_end = min(total_steps, s_begin + steps_per_chunk);
+  const int nsteps = (int)(s_end - s_begin);
   if (threadIdx.x == 0) {
-    int n = 0;
-    for (int64_t g = g1; g <= g2 && n < kMaxParts; ++g, ++n) {
-      const int slot = sk_begin(g, I, G) >= t * S ? 0 : 1;
-      s_part[n] = partial + (g * 2 + slot) * (int64_t)BM * BN;
+    *abort_flag = 0u;
+    *skip_flag = (*(volatile uint32_t*)&g_dev_error != 0u || nsteps <= 0) ? 1u : 0u;
+    for (int i = 0; i < kWgStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&masked[i], 4);
+      mbar_init(&empty[i], 1);
     }
-    s_nparts = n;
+    mbar_init(accfull, 1);
+    fence_barrier_init();
   }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
-  const int nparts = s_nparts;
-  const int64_t m0 = (t % mtiles) * BM, n0 = (t / mtiles) * BN;
-  const int rows = (int)((M - m0) < BM ? (M - m0) : BM);
-  const int cols = (int)((Nout - n0) < BN ? (Nout - n0) : BN);
-  for (int e4 = threadIdx.x; e4 < BM * BN / 4; e4 += 256) {
-    const int row = (e4 * 4) / BN, col = (e4 * 4) % BN;
-    if (row >= rows || col >= cols) continue;
-    const int off = row * BN + col;
-    float4 acc = *reinterpret_cast<const float4*>(s_part[0] + off);
-    for (int k = 1; k < nparts; ++k) {
-      const float4 v = *reinterpret_cast<const float4*>(s_part[k] + off);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    const int64_t m = m0 + row, n = n0 + col;
-    if (out_f32) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + m * Nout + n);
-      if (out_accum) {
-        const float4 o = *dst;
-        acc.x = o.x + acc.x;
-        acc.y = o.y + acc.y;
-        acc.z = o.z + acc.z;
-        acc.w = o.w + acc.w;
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (*skip_flag == 0u) {
+    if (warp == 0) {
+      if (lane == 0) {
+        int64_t issued = 0;
+        for (int i = 0; i < nsteps; ++i) {
+          const int st = i % kWgStages;
+          const uint32_t ph = (uint32_t)(i / kWgStages) & 1u;
+          if (*abort_flag || !mbar_wait(&empty[st], ph ^ 1u, DERR_TIMEOUT_EMPTY)) {
+            *abort_flag = 1u;
+            break;
+          }
+          const int t0 = (int)((s_begin + i) * 64);
+          mbar_arrive_expect_tx(&full[st], kWgA + kWgB);
+          tma_load_2d(sA + st * kWgA, &tmP, &full[st], t0, 0);
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            tma_load_2d(sB + st * kWgB + b * 8192, &tmQ, &full[st], (int)(c0 + 64 * b), t0);
+          issued = i + 1;
+        }
+        if (*abort_flag)
+          for (int64_t i = (issued > kWgStages ? issued - kWgStages : 0); i < issued; ++i)
+            mbar_wait(&full[i % kWgStages], (uint32_t)(i / kWgStages) & 1u, DERR_TIMEOUT_DRAIN);
       }
-      *dst = acc;
+    } else if (warp == 1) {
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 1u);
+        for (int i = 0; i < nsteps; ++i) {
+          const int st = i % kWgStages;
+          const uint32_t ph = (uint32_t)(i / kWgStages) & 1u;
+          if (*abort_flag || !mbar_wait(MASKED ? &masked[st] : &full[st], ph, DERR_TIMEOUT_FULL)) {
+            *abort_flag = 1u;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + st * kWgA);
+          const uint32_t b_base = smem_u32(sB + st * kWgB);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_f16(tmem, smem_desc_sw128(a_base + kk * 32, 16, 1024),
+                       smem_desc_sw128(b_base + kk * 2048, 8192, 1024), idesc,
+                       (i > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&empty[st]);
+        }
+        tc_commit(accfull);
+      }
     } else {
-      uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + m * Nout + n);
-      *dst = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+      if (MASKED) {
+        // zero the dropped elements of each landed x tile
+        const int mt = (int)threadIdx.x - 64;  // 0..127
+        for (int i = 0; i < nsteps; ++i) {
+          const int st = i % kWgStages;
+          const uint32_t ph = (uint32_t)(i / kWgStages) & 1u;
+          if (*abort_flag || !mbar_wait(&full[st], ph, DERR_TIMEOUT_FULL)) {
+            *abort_flag = 1u;
+            break;
+          }
+          const int64_t t0 = (s_begin + i) * 64;
+          uint8_t* tile = sB + st * kWgB;
+          const uint8_t* mbytes = reinterpret_cast<const uint8_t*>(mask);
+#pragma unroll 4
+          for (int it = 0; it < 16; ++it) {
+            const int ch = mt + it * 128;       // 0..2047
+            const int r = ch >> 5;              // token row 0..63
+            const int q = ch & 31;              // 16-byte chunk of the 256 columns
+            const int b = q >> 3, q8 = q & 7;
+            const int64_t m = t0 + r;
+            const int64_t c = c0 + q * 8;
+            if (m >= M || c >= C) continue;
+            const uint32_t bits = mbytes[(m * C + c) >> 3];
+            if (bits == 0xFFu) continue;
+            uint4* p4 = reinterpret_cast<uint4*>(tile + b * 8192 + r * 128 + ((q8 ^ (r & 7)) << 4));
+            uint4 v = *p4;
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t keep = ((bits >> (2 * e)) & 1u ? 0x0000FFFFu : 0u) |
+                                    ((bits >> (2 * e + 1)) & 1u ? 0xFFFF0000u : 0u);
+              w[e] &= keep;
+            }
+            *p4 = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&masked[st]);
+        }
+      }
+      if (warp == 4) {
+        // rows 0..31 of D live in TMEM lanes 0..31 (lane quarter of warp 4)
+        const bool ok = mbar_wait(accfull, 0u, DERR_TIMEOUT_ACC) && !*abort_flag;
+        tc_fence_after();
+        for (int cc = 0; cc < 256; cc += 32) {
+          uint32_t acc[32];
+          tmem_ld_32x32b_x32(tmem + (uint32_t)cc, acc);
+          tmem_ld_wait();
+          const int64_t cb = c0 + cc;
+          if (!ok || cb >= C) continue;  // warp-uniform
+          float v[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float x = __uint_as_float(acc[e]);
+            v[e] = x + __shfl_xor_sync(0xffffffffu, x, 16);  // hi row + lo row
+          }
+          if (lane < 16) {
+            float* dst = partial + ((int64_t)blockIdx.y * C + cb) * 16 + lane;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) dst[(int64_t)e * 16] = v[e];
+          }
+        }
+      }
     }
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+// PT [128][Mp]: row j < 16 = bf16 high part of P[:, j], row 16 + j = low
+// part, rows 32..127 zero (the padding rows of the 128-row MMA operand);
+// columns M..Mp-1 zero (Mp = M rounded up to 8, a 16-byte aligned pitch).
+__global__ void k_pt_split(const float* __restrict__ P, int64_t M, int64_t Mp,
+                           uint16_t* __restrict__ PT) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // (row, m)
+  if (t >= 128 * Mp) return;
+  const int64_t row = t / Mp, m = t % Mp;
+  uint16_t v = 0;
+  if (row < 32 && m < M) {
+    const float p = P[m * 16 + (row & 15)];
+    const uint16_t hi = f32_to_bf16_bits(p);
+    v = row < 16 ? hi : f32_to_bf16_bits(p - bf16_bits_to_f32(hi));
+  }
+  PT[t] = v;
 }
 
 }  // namespace
@@ -681,18 +910,25 @@ cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int64_t S = (int64_t)p.nk + (a.has_lora ? 1 : 0);
-  const int64_t I = (int64_t)p.mtiles * p.ntiles * S;
   const int64_t G = grid_ctas(p, a.has_lora != 0);
+  if (G > 1) {
+    cudaError_t e = cudaMemsetAsync(a.flags, 0, (size_t)G * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+  }
+  // cooperative: all CTAs resident at once, so a finisher's wait for a
+  // later CTA's piece always ends
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   note_launch();
-  k_nf4_gemm<BWD, UM, BN><<<(unsigned)G, kThreads, C::SMEM_BYTES, st>>>(tA, tC, tS, tL, a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || G == 1 || I % G == 0 && (I / G) % S == 0) return e;
-  note_launch();
-  k_streamk_fixup<C::BM, BN><<<(unsigned)(p.mtiles * p.ntiles), 256, 0, st>>>(
-      a.partial, S, p.mtiles, p.ntiles, G, a.M, a.Nout, a.out, a.out_f32, a.out_accum);
-  return cudaGetLastError();
-}
+  return cudaLaunchKernelEx(&cfg, k_nf4_gemm<BWD, UM, BN>, tA, tC, tS, tL, a);}
 
 }  // namespace
 
@@ -758,18 +994,27 @@ GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc) {
   p.bwd = bwd;
   p.um = M > 128 ? 2 : 1;
   p.bn = 128;
+  // A 256-wide forward tile halves the activation-tile traffic per flop but
+  // has a single accumulator (no epilogue overlap): worth it only when there
+  // are enough tiles that stream-K pieces stay long.
+  if (!bwd && p.um == 2) {
+    const int64_t mt = (M + 255) / 256, nt = (Nout + 255) / 256;
+    if (mt * nt >= device_sm_count()) p.bn = 256;
+  }
   p.mtiles = (int)((M + 128 * p.um - 1) / (128 * p.um));
   p.ntiles = (int)((Nout + p.bn - 1) / p.bn);
   p.nk = (int)(Kc / 64);
   return p;
 }
 
+// [G][BM][BN] fp32 partial tiles, then [G] uint32 completion flags.
 size_t gemm_partial_bytes(const GemmPlan& p, int64_t M, int64_t Nout) {
   (void)M;
   (void)Nout;
   const int64_t G = grid_ctas(p, true);
   if (G <= 1) return 0;
-  return (size_t)G * 2 * (size_t)(128 * p.um) * (size_t)p.bn * sizeof(float);
+  return (size_t)G * (size_t)(128 * p.um) * (size_t)p.bn * sizeof(float) +
+         (((size_t)G * sizeof(uint32_t) + 255) & ~size_t(255));
 }
 
 cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* act, int64_t M,
@@ -821,14 +1066,79 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
   a.out_f32 = out_f32;
   a.out_accum = out_accum;
   a.partial = partial;
+  a.flags = partial == nullptr ? nullptr
+                               : reinterpret_cast<uint32_t*>(
+                                     partial + grid_ctas(p, true) * (int64_t)(128 * p.um) * p.bn);
 
   if (partial == nullptr && grid_ctas(p, has_lora) > 1) return cudaErrorInvalidValue;
   if (!p.bwd) {
+    if (p.um == 2 && p.bn == 256) return launch_cfg<false, 2, 256>(p, a, tA, tC, tS, tL, st);
     if (p.um == 2) return launch_cfg<false, 2, 128>(p, a, tA, tC, tS, tL, st);
     return launch_cfg<false, 1, 128>(p, a, tA, tC, tS, tL, st);
   }
   if (p.um == 2) return launch_cfg<true, 2, 128>(p, a, tA, tC, tS, tL, st);
   return launch_cfg<true, 1, 128>(p, a, tA, tC, tS, tL, st);
+}
+
+// ------------------------------------------------------------------------ weight gradients (host)
+int wgrad_tc_chunks(int64_t M, int64_t C) {
+  const int64_t steps = (M + 63) / 64;
+  const int64_t ctiles = (C + 255) / 256;
+  int64_t ch = (device_sm_count() + ctiles - 1) / ctiles;
+  if (ch > steps) ch = steps;
+  if (ch < 1) ch = 1;
+  return (int)ch;
+}
+
+size_t wgrad_tc_bytes(int64_t M, int64_t C) {
+  const int64_t Mp = (M + 7) / 8 * 8;
+  const size_t part = (size_t)wgrad_tc_chunks(M, C) * (size_t)C * 16 * sizeof(float);
+  return ((part + 255) & ~size_t(255)) + (((size_t)128 * Mp * 2 + 255) & ~size_t(255));
+}
+
+cudaError_t run_wgrad_tc(const float* P, const uint16_t* Q, const uint32_t* mask, int64_t M,
+                         int64_t C, float s, float* out, int transpose_out, void* ws,
+                         cudaStream_t st) {
+  if (!encode_fn()) return cudaErrorNotSupported;
+  const int64_t Mp = (M + 7) / 8 * 8;
+  const int chunks = wgrad_tc_chunks(M, C);
+  const int64_t steps = (M + 63) / 64;
+  const int spc = (int)((steps + chunks - 1) / chunks);
+  float* partial = static_cast<float*>(ws);
+  const size_t part = (size_t)chunks * (size_t)C * 16 * sizeof(float);
+  uint16_t* PT = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + ((part + 255) & ~size_t(255)));
+  note_launch();
+  k_pt_split<<<(unsigned)((128 * Mp + 255) / 256), 256, 0, st>>>(P, M, Mp, PT);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap tP, tQ;
+  if (!make_map(&tP, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, PT, (uint64_t)Mp, 128, (uint64_t)Mp * 2, 64,
+                128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&tQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, (uint64_t)C, (uint64_t)M, (uint64_t)C * 2,
+                64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  static bool attr0 = false, attr1 = false;
+  if (!attr0) {
+    e = cudaFuncSetAttribute(k_wgrad_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kWgSmem);
+    if (e != cudaSuccess) return e;
+    attr0 = true;
+  }
+  if (!attr1) {
+    e = cudaFuncSetAttribute(k_wgrad_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kWgSmem);
+    if (e != cudaSuccess) return e;
+    attr1 = true;
+  }
+  dim3 grid((unsigned)((C + 255) / 256), (unsigned)chunks);
+  note_launch();
+  if (mask)
+    k_wgrad_tc<true><<<grid, kWgThreads, kWgSmem, st>>>(tP, tQ, mask, M, C, spc, partial);
+  else
+    k_wgrad_tc<false><<<grid, kWgThreads, kWgSmem, st>>>(tP, tQ, nullptr, M, C, spc, partial);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return run_wgrad_reduce(partial, chunks, C, s, out, transpose_out, st);
 }
 
 }  // namespace ws

@@ -221,18 +221,29 @@ __global__ void k_loss_final(const float* __restrict__ partial, float inv_n,
   *loss = 0.5f * s * inv_n;
 }
 
-// PyTorch-default Adam (no weight decay, bias-corrected); 4 parameters per thread.
-WS_DEVINL float adam1(float& p, float g, float& m, float& v, float beta1, float beta2, float eps,
-                      float step_size, float bc2_sqrt) {
+// PyTorch-default Adam (no weight decay, bias-corrected); 4 parameters per
+// thread.  The step t = *step_dev + 1 is read on the device so the same
+// kernel serves eager calls and graph replays; the bias corrections are
+// computed in double, once per block.
+WS_DEVINL void adam1(float& p, float g, float& m, float& v, float beta1, float beta2, float eps,
+                     float step_size, float bc2_sqrt) {
   m = beta1 * m + (1.0f - beta1) * g;
   v = beta2 * v + (1.0f - beta2) * g * g;
   const float denom = sqrtf(v) / bc2_sqrt + eps;
   p = p - step_size * (m / denom);
-  return p;
 }
 __global__ void k_adam(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
-                       float* __restrict__ v, int64_t n, float beta1, float beta2, float eps,
-                       float step_size, float bc2_sqrt) {
+                       float* __restrict__ v, int64_t n, const uint32_t* __restrict__ step_dev,
+                       float lr) {
+  __shared__ float s_coef[2];
+  if (threadIdx.x == 0) {
+    const double t = (double)(*step_dev) + 1.0;
+    s_coef[0] = (float)((double)lr / (1.0 - pow(0.9, t)));
+    s_coef[1] = (float)sqrt(1.0 - pow(0.999, t));
+  }
+  __syncthreads();
+  const float step_size = s_coef[0], bc2_sqrt = s_coef[1];
+  const float beta1 = 0.9f, beta2 = 0.999f, eps = 1e-8f;
   const int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i4 * 4 >= n) return;
   float4 pp = reinterpret_cast<float4*>(p)[i4];
@@ -247,6 +258,8 @@ __global__ void k_adam(float* __restrict__ p, const float* __restrict__ g, float
   reinterpret_cast<float4*>(m)[i4] = mm;
   reinterpret_cast<float4*>(v)[i4] = vv;
 }
+
+__global__ void k_set_step(uint32_t* step_dev, uint32_t step) { *step_dev = step; }
 
 unsigned nblk(int64_t n, int t = 256) { return (unsigned)((n + t - 1) / t); }
 
@@ -332,7 +345,7 @@ ParamLayout param_layout(const ws_stack_cfg& c) {
 }
 
 struct WsLayout {
-  size_t lin, blk, qout, kout, yout, y1, dact, dg, du, db, dvr, dv, lossp, total;
+  size_t lin, blk, qout, kout, yout, y1, dact, dg, du, db, dvr, dv, lossp, stepw, total;
 };
 WsLayout ws_layout(const ws_stack_cfg& c, int block_layers) {
   const Shapes s = shapes_of(c);
@@ -362,6 +375,7 @@ WsLayout ws_layout(const ws_stack_cfg& c, int block_layers) {
   L.dvr = take(M * H * 4);
   L.dv = take(M * KV * 2);
   L.lossp = take(kLossBlocks * 4);
+  L.stepw = take(16);
   L.total = o;
   return L;
 }
@@ -387,6 +401,7 @@ struct Ctx {
   float scale;
   cudaStream_t st;
   void* ws;
+  const uint32_t* step_dev;
 };
 
 NF4View wview(const Ctx& x, const void* block, int layer_in_block, int lin) {
@@ -407,7 +422,9 @@ DropKeyHost key_of(const Ctx& x, uint32_t step, int layer, int lin) {
   k.linear = (uint32_t)lin;
   k.microbatch = 0;
   k.p = x.c.p;
-  return make_drop_key(k);
+  DropKeyHost h = make_drop_key(k);
+  h.step_dev = x.step_dev;
+  return h;
 }
 
 // Forward of one layer.  S: saved slot of this layer.  with_qk: compute the
@@ -520,7 +537,8 @@ cudaError_t layer_bwd(const Ctx& x, const void* block, int lib, int layer, const
   return cudaSuccess;
 }
 
-Ctx make_ctx(const ws_stack_cfg& c, int block_layers, void* ws, cudaStream_t st) {
+Ctx make_ctx(const ws_stack_cfg& c, int block_layers, void* ws, cudaStream_t st,
+             const uint32_t* step_dev) {
   Ctx x;
   x.c = c;
   x.s = shapes_of(c);
@@ -531,6 +549,7 @@ Ctx make_ctx(const ws_stack_cfg& c, int block_layers, void* ws, cudaStream_t st)
   x.scale = (float)(((double)c.alpha / (double)c.r) / (1.0 - c.p));
   x.st = st;
   x.ws = ws;
+  x.step_dev = step_dev;
   return x;
 }
 
@@ -553,6 +572,9 @@ size_t stack_block_bytes(const ws_stack_cfg& c, int bl) { return (size_t)bl * we
 int64_t stack_n_params(const ws_stack_cfg& c) { return (int64_t)c.n_layers * param_layout(c).layer_floats; }
 size_t stack_saved_layer(const ws_stack_cfg& c) { return saved_layout(c).total; }
 size_t stack_ws_bytes(const ws_stack_cfg& c, int bl) { return ws_layout(c, bl).total; }
+uint32_t* stack_step_word(const ws_stack_cfg& c, int block_layers, void* ws) {
+  return at<uint32_t>(ws, ws_layout(c, block_layers).stepw);
+}
 void stack_weight_offset(const ws_stack_cfg& c, int lib, int lin, size_t* oc, size_t* oa) {
   const WeightLayout L = weight_layout(c);
   *oc = (size_t)lib * L.layer_bytes + L.codes[lin];
@@ -579,8 +601,9 @@ void stack_param_offset(const ws_stack_cfg& c, int layer, int lin, int64_t* oA, 
 
 cudaError_t block_forward(const ws_stack_cfg& c, int block_layers_ws, const void* block,
                           int first_layer, int n_layers, const float* params, uint32_t step,
-                          const float* h_in, float* h_out, void* saved, void* ws, cudaStream_t st) {
-  const Ctx x = make_ctx(c, block_layers_ws, ws, st);
+                          const uint32_t* step_dev, const float* h_in, float* h_out, void* saved,
+                          void* ws, cudaStream_t st) {
+  const Ctx x = make_ctx(c, block_layers_ws, ws, st, step_dev);
   uint8_t* blk_area = static_cast<uint8_t*>(ws) + x.WSL.blk;
   // Layer i works in slot S_i: the caller's saved area (kept for the
   // backward) or, when nothing is kept, one reused workspace slot.  Layer i
@@ -601,9 +624,10 @@ cudaError_t block_forward(const ws_stack_cfg& c, int block_layers_ws, const void
 
 cudaError_t block_backward(const ws_stack_cfg& c, int block_layers_ws, const void* block,
                            int first_layer, int n_layers, const float* params, uint32_t step,
-                           const float* h_in, const void* saved, const float* dh_out, float* dh_in,
-                           float* grads, void* ws, cudaStream_t st) {
-  const Ctx x = make_ctx(c, block_layers_ws, ws, st);
+                           const uint32_t* step_dev, const float* h_in, const void* saved,
+                           const float* dh_out, float* dh_in, float* grads, void* ws,
+                           cudaStream_t st) {
+  const Ctx x = make_ctx(c, block_layers_ws, ws, st, step_dev);
   const int64_t MH = c.M * c.H;
   const uint8_t* area = static_cast<const uint8_t*>(saved);
   if (!saved) {
@@ -642,13 +666,16 @@ cudaError_t loss_and_grad(const ws_stack_cfg& c, int block_layers_ws, const floa
   return cudaGetLastError();
 }
 
-cudaError_t adam_step(float* p, const float* g, float* m, float* v, int64_t n, int64_t t, float lr,
-                      cudaStream_t st) {
-  const double b1 = 0.9, b2 = 0.999;
-  const double bc1 = 1.0 - pow(b1, (double)t), bc2 = 1.0 - pow(b2, (double)t);
+cudaError_t adam_step(float* p, const float* g, float* m, float* v, int64_t n,
+                      const uint32_t* step_dev, float lr, cudaStream_t st) {
   note_launch();
-  k_adam<<<nblk(n / 4), 256, 0, st>>>(p, g, m, v, n, (float)b1, (float)b2, 1e-8f, (float)(lr / bc1),
-                                  (float)sqrt(bc2));
+  k_adam<<<nblk(n / 4), 256, 0, st>>>(p, g, m, v, n, step_dev, lr);
+  return cudaGetLastError();
+}
+
+cudaError_t set_step(uint32_t* step_dev, uint32_t step, cudaStream_t st) {
+  note_launch();
+  k_set_step<<<1, 1, 0, st>>>(step_dev, step);
   return cudaGetLastError();
 }
 

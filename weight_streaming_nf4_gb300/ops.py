@@ -98,13 +98,18 @@ _sig("ws_block_backward_recompute", [C.POINTER(StackCfgC), P, i32, i32, P, u32, 
 _sig("ws_stream_block_h2d", [P, P, C.c_size_t, P, P, P])
 _sig("ws_stack_train_step", [C.POINTER(StackCfgC), i32, i32, C.POINTER(StackBuffersC), u32, P,
                              C.c_float, P, P])
+_sig("ws_stack_graph_create", [C.POINTER(StackCfgC), i32, i32, C.POINTER(StackBuffersC), C.c_float,
+                               P, P, C.POINTER(P)])
+_sig("ws_stack_graph_step", [P, u32, P, P])
+_sig("ws_stack_graph_destroy", [P])
 
 EXPORTED = ("ws_status_string", "ws_device_error", "ws_kernel_launches", "ws_quantize_nf4", "ws_lora_workspace_size",
             "ws_lora_linear_fwd", "ws_lora_linear_bwd", "ws_nf4_matmul_workspace_size",
             "ws_nf4_matmul", "ws_nf4_matmul_noalloc", "ws_stack_sizes",
             "ws_stack_weight_offset", "ws_stack_param_offset", "ws_stack_saved_offset",
-            "ws_block_forward",
-            "ws_block_backward_recompute", "ws_stream_block_h2d", "ws_stack_train_step")
+            "ws_block_forward", "ws_block_backward_recompute", "ws_stream_block_h2d",
+            "ws_stack_train_step", "ws_stack_graph_create", "ws_stack_graph_step",
+            "ws_stack_graph_destroy")
 
 
 def _check(fn, st):
@@ -366,3 +371,34 @@ def stack_train_step(cfg: StackCfg, block_layers: int, streamed: bool, bufs: Sta
            _lib.ws_stack_train_step(C.byref(c), block_layers, 1 if streamed else 0,
                                     C.byref(bufs), step, _ptr(h0), lr, _stream(stream),
                                     _stream(copy_stream) if copy_stream is not None else None))
+
+
+class StepGraph:
+    """One training step of the stack captured as a CUDA graph
+    (ws_stack_graph_create); ``step`` replays it for any step number."""
+
+    def __init__(self, cfg: StackCfg, block_layers: int, streamed: bool, bufs: StackBuffersC,
+                 lr: float, stream, copy_stream=None):
+        self._bufs = bufs  # the graph keeps these pointers
+        c = cfg.c()
+        h = C.c_void_p()
+        _check("ws_stack_graph_create",
+               _lib.ws_stack_graph_create(C.byref(c), block_layers, 1 if streamed else 0,
+                                          C.byref(bufs), lr, _stream(stream),
+                                          _stream(copy_stream) if copy_stream is not None else None,
+                                          C.byref(h)))
+        self._h = h
+
+    def step(self, step: int, h0, stream=None):
+        _check("ws_stack_graph_step", _lib.ws_stack_graph_step(self._h, step, _ptr(h0), _stream(stream)))
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            _lib.ws_stack_graph_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

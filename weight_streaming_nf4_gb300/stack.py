@@ -88,8 +88,14 @@ class StackRun:
                                    self.workspace.numel(), p(self.loss))
 
     def step(self, step: int, h0: torch.Tensor, lr: float = 2e-4, stream=None):
+        """Enqueue one training step (ws_stack_train_step) on ``stream``."""
         ops.stack_train_step(self.cfg, self.bl, self.streamed, self.c, step, h0, lr, stream=stream,
                              copy_stream=self.copy_stream)
+
+    def graph(self, lr: float, stream: torch.cuda.Stream) -> "ops.StepGraph":
+        """Capture one training step as a CUDA graph on ``stream`` (a created
+        stream, not the default one); ``g.step(step, h0, stream)`` replays it."""
+        return ops.StepGraph(self.cfg, self.bl, self.streamed, self.c, lr, stream, self.copy_stream)
 
     def param(self, layer: int, lin: int, which: str, t: torch.Tensor = None):
         """View of A [16, K] or B [N, 16] of (layer, lin) inside a parameter-layout array."""
