@@ -232,6 +232,16 @@ WS_DEVINL void tc_commit(uint64_t* bar) {
 }
 // 32 lanes x 32 consecutive 32-bit columns: lane i of the warp receives row
 // (32*(warp%4) + i), columns [col, col+32).
+WS_DEVINL void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
 WS_DEVINL void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -268,6 +278,81 @@ WS_DEVINL uint32_t lane_id() { return threadIdx.x & 31; }
 WS_DEVINL bool elect_lane0() { return lane_id() == 0; }
 
 // Named barrier among `nthreads` threads (id 1..15; id 0 is __syncthreads).
+// ---- thread-block clusters ------------------------------------------------------------
+WS_DEVINL uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+WS_DEVINL uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+WS_DEVINL void st_cluster_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster, releasing this
+// thread's earlier writes at cluster scope.
+WS_DEVINL void mbar_arrive_cluster(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar)
+               : "memory");
+}
+WS_DEVINL bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Commit: the mbarrier at this offset in every CTA of `mask` receives one
+// arrival once this thread's earlier tcgen05 operations have completed.
+WS_DEVINL void tc_commit_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+// Copy `bytes` of this CTA's shared memory to a shared::cluster address in
+// another CTA of the cluster; completion is signalled as transaction bytes
+// on that CTA's mbarrier (cluster address cbar).
+WS_DEVINL void bulk_copy_to_peer(uint32_t cdst, const void* src, uint32_t bytes, uint32_t cbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(cdst), "r"(smem_u32(src)), "r"(bytes), "r"(cbar)
+      : "memory");
+}
+WS_DEVINL void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+WS_DEVINL void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+#ifdef WS_GEMM_TU
+// Same, acquiring at cluster scope (arrivals released by the other CTA of a pair).
+WS_DEVINL bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t why) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 255u) == 0u && globaltimer() - t0 > kWaitLimitNs) {
+      atomicOr(&g_dev_error, why);
+      return false;
+    }
+  }
+}
+
+#endif
+
 WS_DEVINL void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

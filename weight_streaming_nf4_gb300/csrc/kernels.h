@@ -33,12 +33,16 @@ struct GemmArgs {
   int out_f32, out_accum;
   float* partial;       // [grid, BM, BN] fp32 partial tile of each CTA's cut first segment
   uint32_t* flags;      // [grid] set to 1 once that partial is complete (zeroed per launch)
+  const uint8_t* codes; // the weight's packed codes [N, K/2]
+  const float* absmax;  // the weight's block scales [K/64, N]
+  int64_t wN, wK;       // the weight's shape
 };
 
 // Tile configuration: a pure function of the shape and the SM count, so a
 // resident and a streamed run always pick the same kernels and split order.
 struct GemmPlan {
   bool bwd;
+  bool pair;  // two CTAs of a cluster share each weight tile
   int um, bn;
   int mtiles, ntiles, nk;
 };
@@ -47,6 +51,7 @@ int device_sm_count();
 // CTAs of the persistent stream-K grid for a plan (with or without the extra
 // LoRA step): min(SM count, iterations / 8), at least 1.
 int64_t grid_ctas(const GemmPlan& p, bool has_lora);
+int64_t grid_units(const GemmPlan& p, bool has_lora);
 // This device's address and size of the built-in scratch array used by
 // ws_nf4_matmul_noalloc (looked up once per device).
 cudaError_t noalloc_scratch(float** ptr, size_t* bytes);

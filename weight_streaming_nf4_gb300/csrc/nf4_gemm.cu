@@ -55,31 +55,51 @@ cudaError_t read_and_clear_dev_error(uint32_t* flags) {
 
 namespace {
 
-// Pipeline depths: dequantised-operand buffers and TMA stages (upper bound;
-// the shared-memory budget may allow fewer).
+// Pipeline depths: dequantised-operand buffers and activation-tile TMA
+// stages (upper bound; the shared-memory budget may allow fewer).
 #ifndef WS_GEMM_BSTAGES
-#define WS_GEMM_BSTAGES 2
+#define WS_GEMM_BSTAGES 3
 #endif
 #ifndef WS_GEMM_STAGES_MAX
-#define WS_GEMM_STAGES_MAX 4
+#define WS_GEMM_STAGES_MAX 6
 #endif
 
 constexpr int kDqWarps = 8;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kDqWarps + kEpiWarps) * 32;
 constexpr int kDqThreads = kDqWarps * 32;
 
-template <bool BWD, int UM, int BN>
+// Dequant work of one thread per step.  A CTA fills the whole BN-wide
+// weight tile itself, or -- as one CTA of a pair sharing the tile -- the half
+// [rank * BN/2, (rank + 1) * BN/2) of it, written into both CTAs' buffers.
+//   forward: ROWS weight-tile rows (output columns) x 64 codes, TPR threads
+//            per row, each with VB code bytes;
+//   backward: 64 contraction rows x COLS output columns in items of
+//            VB * 2 columns, one item per thread and vector.
+template <bool BWD, int BN, bool PAIR>
+struct DqGeo {
+  static constexpr int COLS = PAIR ? BN / 2 : BN;  // columns (bwd) / rows (fwd) this CTA fills
+  static constexpr int TPR = BWD ? 0 : kDqThreads / COLS;
+  // code bytes per vector and vectors per thread
+  static constexpr int VB = BWD ? (PAIR ? 8 : 16) : (32 / (kDqThreads / COLS) >= 16 ? 16 : 8);
+  static constexpr int NV = BWD ? (64 * COLS / (VB * 2)) / kDqThreads : (32 / TPR) / VB;
+  static constexpr int NS = BWD ? NV : 1;  // block scales per thread
+  static constexpr uint32_t SLOT_BYTES = NV * kDqThreads * VB + NS * kDqThreads * 4;
+  static_assert(NV >= 1 && NV <= 2, "dequant geometry");
+  static_assert(!BWD || (64 * COLS / (VB * 2)) % kDqThreads == 0, "dequant geometry");
+};
+
+template <bool BWD, int UM, int BN, bool PAIR>
 struct Cfg {
   static constexpr int BM = 128 * UM;
   static constexpr uint32_t A_BYTES = BM * 128;   // BM rows x 64 bf16
   static constexpr uint32_t B_BYTES = BN * 128;   // BN x 64 bf16
-  static constexpr uint32_t C_BYTES = BN * 32;    // codes: BN x 64 nibbles
-  static constexpr uint32_t S_BYTES = BN * 4;     // absmax: BN floats
   static constexpr int BSTAGES = WS_GEMM_BSTAGES;
-  static constexpr uint32_t STAGE_BYTES = A_BYTES + C_BYTES + S_BYTES;
+  // per-thread ring of fetched codes (cp.async), CSTAGES steps deep
+  static constexpr int CSTAGES = 4;
+  static constexpr uint32_t CODE_BYTES = DqGeo<BWD, BN, PAIR>::SLOT_BYTES;
   static constexpr int STAGES_RAW =
-      (int)((220u * 1024u - BSTAGES * B_BYTES - 1024u) / STAGE_BYTES);
+      (int)((220u * 1024u - BSTAGES * B_BYTES - CSTAGES * CODE_BYTES - 1024u) / A_BYTES);
   static constexpr int STAGES = STAGES_RAW > WS_GEMM_STAGES_MAX ? WS_GEMM_STAGES_MAX : STAGES_RAW;
   // one accumulator set: D (and for the backward the LoRA term D2)
   static constexpr uint32_t ACC_COLS = (BWD ? 2u : 1u) * UM * BN;
@@ -94,9 +114,8 @@ struct Cfg {
   static constexpr uint32_t MN_SBO = (BN / 64) * 1024;
   static constexpr uint32_t OFF_A = 0;
   static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr uint32_t OFF_C = OFF_B + BSTAGES * B_BYTES;
-  static constexpr uint32_t OFF_S = OFF_C + STAGES * C_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_S + STAGES * S_BYTES;
+  static constexpr uint32_t OFF_CODE = OFF_B + BSTAGES * B_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_CODE + CSTAGES * CODE_BYTES;
   static constexpr uint32_t N_BARS = 2 * STAGES + 2 * BSTAGES + 2 * ACC_BUFS + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
@@ -104,6 +123,7 @@ struct Cfg {
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns");
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory");
   static_assert(BN == 128 || BN == 256, "BN");
+  static_assert(!PAIR || UM == 2, "a pair shares one weight tile between two 256-row halves");
 };
 
 // CTA of the stream-K schedule that owns iteration i: ranges are
@@ -171,52 +191,134 @@ WS_DEVINL Nf4Table make_table(float a) {
 
 // 4 code bytes (8 consecutive weights along k: byte i holds k = 2i in its
 // high nibble, 2i+1 in its low nibble) -> 8 bf16 values in k order.
+// Nibble f of the word is the code of k = f ^ 1; the two interleaving
+// permutes at the end put the pairs back in k order, so the codes need no
+// nibble swap first.
 WS_DEVINL uint4 dq8(uint32_t w, const Nf4Table& t) {
-  // nibble-swap each byte so the fields run in k order: field f = code of k = f
-  const uint32_t ws = ((w >> 4) & 0x0F0F0F0Fu) | ((w << 4) & 0xF0F0F0F0u);
-  const uint32_t s7 = ws & 0x77777777u;                           // index within 8 entries
-  const uint32_t s8 = ((ws >> 1) & 0x44444444u) | 0x32103210u;   // which half (code >= 8)
+  const uint32_t s7 = w & 0x77777777u;                           // index within 8 entries
+  const uint32_t s8 = ((w >> 1) & 0x44444444u) | 0x32103210u;    // which half (code >= 8)
   uint32_t o[4];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const uint32_t a7 = h ? (s7 >> 16) : s7;
     const uint32_t a8 = h ? (s8 >> 16) : s8;
+    // byte p of lo / hi: low / high byte of the value of nibble 4h + p
     const uint32_t lo = prmt(prmt(t.lo[0], t.lo[1], a7), prmt(t.lo[2], t.lo[3], a7), a8);
     const uint32_t hi = prmt(prmt(t.hi[0], t.hi[1], a7), prmt(t.hi[2], t.hi[3], a7), a8);
-    o[2 * h] = prmt(lo, hi, 0x5140u);
-    o[2 * h + 1] = prmt(lo, hi, 0x7362u);
+    o[2 * h] = prmt(lo, hi, 0x4051u);      // k = 4h (nibble 4h+1), k = 4h+1 (nibble 4h)
+    o[2 * h + 1] = prmt(lo, hi, 0x6273u);  // k = 4h+2 (nibble 4h+3), k = 4h+3 (nibble 4h+2)
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Code words and block scales of one dequant thread for one step.
+struct Frag {
+  uint32_t w[8];
+  float a[2];
+};
+
+// Asynchronous 16- / 8- / 4-byte global -> shared copies; src_bytes = 0
+// fills zeros without reading.
+WS_DEVINL void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+WS_DEVINL void cp_async8(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+WS_DEVINL void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+WS_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+WS_DEVINL void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+template <int VB>
+WS_DEVINL void cp_async_v(uint32_t dst, const void* src, bool in) {
+  if constexpr (VB == 16) cp_async16(dst, src, in ? 16u : 0u);
+  else cp_async8(dst, src, in ? 8u : 0u);
+}
+
+// Each dequant thread stages its own codes and scales of a step in a ring
+// slot of shared memory: code vectors at [v][t], scales after them at
+// [v][t], so the reads back are conflict-free.
+// Forward: thread t covers (part of) weight-tile row j, i.e. output column
+// n0 + j.  Backward: item (c, seg) covers weight row i*64 + c (the
+// contraction index) and 2*VB weight columns (the output index).
+// Rows / columns past the weight's edge read as zero codes with scale 0.
+template <bool BWD, int BN, bool PAIR>
+WS_DEVINL void fetch_codes(uint32_t slot, const GemmArgs& g, int i, int n0, int rank, int t) {
+  using D = DqGeo<BWD, BN, PAIR>;
+  const int64_t kb = g.wK / 2;  // code bytes per weight row
+  const int c0 = PAIR ? rank * D::COLS : 0;
+  const uint32_t sc = slot + (uint32_t)(D::NV * kDqThreads * D::VB);
+  if (!BWD) {
+    const int j = c0 + t / D::TPR, part = t % D::TPR;
+    const int64_t n = (int64_t)n0 + j;
+    const bool in = n < g.wN;
+    const int64_t nn = in ? n : 0;
+    const uint8_t* src = g.codes + nn * kb + (int64_t)i * 32 + part * (32 / D::TPR);
+#pragma unroll
+    for (int v = 0; v < D::NV; ++v)
+      cp_async_v<D::VB>(slot + (uint32_t)((v * kDqThreads + t) * D::VB), src + D::VB * v, in);
+    cp_async4(sc + (uint32_t)(t * 4), g.absmax + (int64_t)i * g.wN + nn, in ? 4u : 0u);
+  } else {
+    constexpr int SEGS = D::COLS / (2 * D::VB);
+#pragma unroll
+    for (int it = 0; it < D::NV; ++it) {
+      const int item = t + it * kDqThreads;
+      const int c = item / SEGS, seg = item % SEGS;
+      const int64_t r = (int64_t)i * 64 + c;
+      const int64_t col = (int64_t)n0 + c0 + seg * 2 * D::VB;
+      const bool in = r < g.wN && col < g.wK;
+      const int64_t rr = in ? r : 0, cl = in ? col : 0;
+      cp_async_v<D::VB>(slot + (uint32_t)((it * kDqThreads + t) * D::VB),
+                        g.codes + rr * kb + cl / 2, in);
+      cp_async4(sc + (uint32_t)((it * kDqThreads + t) * 4), g.absmax + (cl / 64) * g.wN + rr,
+                in ? 4u : 0u);
+    }
+  }
+}
+
+template <bool BWD, int BN, bool PAIR>
+WS_DEVINL void read_frag(Frag& f, const uint8_t* slot, int t) {
+  using D = DqGeo<BWD, BN, PAIR>;
+  const float* sc = reinterpret_cast<const float*>(slot + D::NV * kDqThreads * D::VB);
+#pragma unroll
+  for (int v = 0; v < D::NV; ++v) {
+    if constexpr (D::VB == 16) {
+      const uint4 x = *reinterpret_cast<const uint4*>(slot + (v * kDqThreads + t) * 16);
+      f.w[4 * v] = x.x;
+      f.w[4 * v + 1] = x.y;
+      f.w[4 * v + 2] = x.z;
+      f.w[4 * v + 3] = x.w;
+    } else {
+      const uint2 x = *reinterpret_cast<const uint2*>(slot + (v * kDqThreads + t) * 8);
+      f.w[2 * v] = x.x;
+      f.w[2 * v + 1] = x.y;
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < D::NS; ++v) f.a[v] = sc[v * kDqThreads + t];
+}
+
 // Forward weight tile, K-major 128B-swizzled: row j = output column n0 + j,
 // 64 contraction elements; chunk cc of row j sits at (cc ^ (j & 7)) * 16.
-template <int BN>
-WS_DEVINL void dequant_fwd(const uint8_t* sC, const float* sS, uint8_t* sB, int t) {
-  if constexpr (BN == 256) {
-    const int j = t;
-    const uint4 c0 = *reinterpret_cast<const uint4*>(sC + j * 32);
-    const uint4 c1 = *reinterpret_cast<const uint4*>(sC + j * 32 + 16);
-    const Nf4Table tb = make_table(sS[j]);
-    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    uint8_t* row = sB + j * 128;
+template <int BN, bool PAIR>
+WS_DEVINL void dequant_fwd(const Frag& f, uint8_t* Bt, int rank, int t) {
+  using D = DqGeo<false, BN, PAIR>;
+  constexpr int WPT = 8 / D::TPR;  // code words per thread
+  const int j = (PAIR ? rank * D::COLS : 0) + t / D::TPR, part = t % D::TPR;
+  const Nf4Table tb = make_table(f.a[0]);
 #pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-      const uint4 v = dq8(words[cc], tb);
-      sts128(row + ((cc ^ (j & 7)) << 4), v.x, v.y, v.z, v.w);
-    }
-  } else {
-    const int j = t >> 1, half = t & 1;
-    const uint4 c = *reinterpret_cast<const uint4*>(sC + j * 32 + half * 16);
-    const Nf4Table tb = make_table(sS[j]);
-    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-    uint8_t* row = sB + j * 128;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int cc = half * 4 + q;
-      const uint4 v = dq8(words[q], tb);
-      sts128(row + ((cc ^ (j & 7)) << 4), v.x, v.y, v.z, v.w);
-    }
+  for (int q = 0; q < WPT; ++q) {
+    const int cc = part * WPT + q;
+    const uint4 v = dq8(f.w[q], tb);
+    sts128(Bt + j * 128 + ((cc ^ (j & 7)) << 4), v.x, v.y, v.z, v.w);
   }
 }
 
@@ -225,25 +327,24 @@ WS_DEVINL void dequant_fwd(const uint8_t* sC, const float* sS, uint8_t* sB, int 
 // so the tile keeps W's own orientation.  Element (k-col j, n-row c):
 // group (c/8, j/64) at (c/8)*SBO + (j/64)*LBO, row c%8 inside the group,
 // chunk ((j%64)/8) ^ (c%8).
-template <int BN>
-WS_DEVINL void dequant_bwd(const uint8_t* sC, const float* sS, uint8_t* sB, int t) {
-  using C = Cfg<true, 1, BN>;
-  constexpr int SEGS = BN / 32;                  // 32-column segments per row
-  constexpr int ITEMS = 64 * SEGS / kDqThreads;  // rows*segs per thread
+template <int BN, bool PAIR>
+WS_DEVINL void dequant_bwd(const Frag& f, uint8_t* Bt, int rank, int t) {
+  using D = DqGeo<true, BN, PAIR>;
+  constexpr uint32_t SBO = (BN / 64) * 1024;
+  constexpr int WPI = D::VB / 4;  // code words per item: 8 weights each
+  constexpr int SEGS = D::COLS / (2 * D::VB);
 #pragma unroll
-  for (int it = 0; it < ITEMS; ++it) {
+  for (int it = 0; it < D::NV; ++it) {
     const int item = t + it * kDqThreads;
     const int c = item / SEGS, seg = item % SEGS;
-    const uint4 cw = *reinterpret_cast<const uint4*>(sC + c * (BN / 2) + seg * 16);
-    const Nf4Table tb = make_table(sS[((seg * 32) / 64) * 64 + c]);
-    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-    const int mg = (seg * 32) / 64;
-    uint8_t* grp = sB + (c >> 3) * C::MN_SBO + mg * C::MN_LBO + (c & 7) * 128;
+    const int j0 = (PAIR ? rank * D::COLS : 0) + seg * 2 * D::VB;  // first tile column
+    const Nf4Table tb = make_table(f.a[it]);
+    const uint32_t grp = (uint32_t)((c >> 3) * SBO + (j0 / 64) * 1024 + (c & 7) * 128);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int cc = ((seg * 32) % 64) / 8 + q;
-      const uint4 v = dq8(words[q], tb);
-      sts128(grp + ((cc ^ (c & 7)) << 4), v.x, v.y, v.z, v.w);
+    for (int q = 0; q < WPI; ++q) {
+      const int cc = (j0 % 64) / 8 + q;
+      const uint4 v = dq8(f.w[it * WPI + q], tb);
+      sts128(Bt + grp + ((cc ^ (c & 7)) << 4), v.x, v.y, v.z, v.w);
     }
   }
 }
@@ -251,12 +352,14 @@ WS_DEVINL void dequant_bwd(const uint8_t* sC, const float* sS, uint8_t* sB, int 
 // The LoRA weight operand of the extra step, K-major like the forward
 // tile: row j holds [Ws_hi(16) | Ws_hi(16) | Ws_lo(16) | 0(16)] with
 // Ws = s * (row j of the LoRA factor).  Forward: factor row = B[n0+j, :];
-// backward: factor row = A[:, n0+j] (column of A).
-template <bool BWD, int BN>
+// backward: factor row = A[:, n0+j] (column of A).  A CTA of a pair fills
+// its half of the rows.
+template <bool BWD, int BN, bool PAIR>
 WS_DEVINL void lora_tile(const float* F, int64_t rows_total, int64_t ld, int n0, float s,
-                         uint8_t* sB, int t) {
-  constexpr int TPR = kDqThreads / BN;  // threads per row: 1 (BN=256) or 2 (BN=128)
-  const int j = t / TPR, part = t % TPR;
+                         uint8_t* Bt, int rank, int t) {
+  constexpr int ROWS = PAIR ? BN / 2 : BN;
+  constexpr int TPR = kDqThreads / ROWS;  // threads per row
+  const int j = (PAIR ? rank * ROWS : 0) + t / TPR, part = t % TPR;
   const int64_t n = (int64_t)n0 + j;
   float v[16];
 #pragma unroll
@@ -273,7 +376,6 @@ WS_DEVINL void lora_tile(const float* F, int64_t rows_total, int64_t ld, int n0,
     hi[i] = pack_bf16x2(h0, h1);
     lo[i] = pack_bf16x2(v[2 * i] - h0, v[2 * i + 1] - h1);
   }
-  uint8_t* row = sB + j * 128;
 #pragma unroll
   for (int q = 0; q < 8 / TPR; ++q) {
     const int cc = part * (8 / TPR) + q;
@@ -283,16 +385,37 @@ WS_DEVINL void lora_tile(const float* F, int64_t rows_total, int64_t ld, int n0,
     else if (cc == 4) val = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     else if (cc == 5) val = make_uint4(lo[4], lo[5], lo[6], lo[7]);
     else val = make_uint4(0u, 0u, 0u, 0u);
-    sts128(row + ((cc ^ (j & 7)) << 4), val.x, val.y, val.z, val.w);
+    sts128(Bt + j * 128 + ((cc ^ (j & 7)) << 4), val.x, val.y, val.z, val.w);
   }
 }
 
-template <bool BWD, int UM, int BN>
+// Position of a (tile, step) iteration: step i of tile (mt, nt).
+struct Pos {
+  int i, mt, nt;
+  WS_DEVINL void next(int S, int mtiles) {
+    if (++i == S) {
+      i = 0;
+      if (++mt == mtiles) {
+        mt = 0;
+        ++nt;
+      }
+    }
+  }
+};
+
+// PAIR: the CTA is one of a cluster of two that share each weight tile.
+// The pair covers 2 * BM activation rows (rank r takes rows r * BM ...);
+// each CTA dequantises half of the tile's weight columns and writes it into
+// both CTAs' buffers, so every weight is decoded once per 512 rows instead
+// of once per 256.  A buffer is refilled once the MMAs of both CTAs that
+// read it have completed (their commits arrive on both CTAs' barriers).
+// The stream-K schedule runs over pairs; partial tiles and their flags stay
+// per CTA.
+template <bool BWD, int UM, int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
-               const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmL,
+    k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmL,
                const GemmArgs args) {
-  using C = Cfg<BWD, UM, BN>;
+  using C = Cfg<BWD, UM, BN, PAIR>;
   constexpr int STAGES = C::STAGES;
   constexpr int BSTAGES = C::BSTAGES;
   constexpr int NACC = C::ACC_BUFS;
@@ -302,8 +425,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem + C::OFF_A;
   uint8_t* sB = smem + C::OFF_B;
-  uint8_t* sC = smem + C::OFF_C;
-  uint8_t* sS = smem + C::OFF_S;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* full = bars;
   uint64_t* empty = full + STAGES;
@@ -319,13 +440,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = (int)warp_id();
   const int lane = (int)lane_id();
-  // ---- static stream-K schedule
-  const int64_t S = (int64_t)args.nk_total + (args.has_lora ? 1 : 0);  // steps per tile
+  const int rank = PAIR ? (int)cluster_ctarank() : 0;
+  // ---- static stream-K schedule over units (CTAs, or pairs of CTAs)
+  const int S = args.nk_total + (args.has_lora ? 1 : 0);  // steps per tile
   const int64_t T = (int64_t)args.mtiles * args.ntiles;
   const int64_t I = T * S;
-  const int64_t G = gridDim.x;
-  const int64_t pb = sk_begin(blockIdx.x, I, G);
-  const int64_t pe = sk_begin((int64_t)blockIdx.x + 1, I, G);
+  const int64_t U = PAIR ? gridDim.x / 2 : gridDim.x;
+  const int64_t unit = PAIR ? blockIdx.x / 2 : blockIdx.x;
+  const int64_t pb = sk_begin(unit, I, U);
+  const int64_t pe = sk_begin(unit + 1, I, U);
+  const Pos pos0 = {(int)(pb % S), (int)((pb / S) % args.mtiles), (int)((pb / S) / args.mtiles)};
+  constexpr int UROWS = PAIR ? 2 * C::BM : C::BM;  // activation rows per tile
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
@@ -333,11 +458,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     *skip_flag = (*(volatile uint32_t*)&g_dev_error != 0u || pe <= pb) ? 1u : 0u;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + kDqWarps);
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < BSTAGES; ++b) {
       mbar_init(&bfull[b], kDqWarps);
-      mbar_init(&bempty[b], 1);
+      mbar_init(&bempty[b], PAIR ? 2 : 1);
     }
     for (int a = 0; a < NACC; ++a) {
       mbar_init(&accfull[a], 1);
@@ -351,59 +476,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  // both CTAs of a pair have their barriers set up before either arrives remotely
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool skip = *skip_flag != 0u;
 
   if (!skip) {
     if (warp == 0) {
-      // ------------------------------------------------------------ TMA producer
+      // ------------------------------------------------------------ TMA producer (activations)
       if (lane == 0) {
         tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmC);
-        tma_prefetch_desc(&tmS);
         if (args.has_lora) tma_prefetch_desc(&tmL);
         int64_t issued = 0;
         int s = 0;
         uint32_t ph = 0;
-        int i = (int)(pb % S);
-        int mt = (int)((pb / S) % args.mtiles);
-        int nt = (int)((pb / S) / args.mtiles);
+        Pos ps = pos0;
         for (int64_t q = 0; q < pe - pb; ++q) {
           if (*abort_flag || !mbar_wait(&empty[s], ph ^ 1u, DERR_TIMEOUT_EMPTY)) {
             *abort_flag = 1u;
             break;
           }
-          const int m0 = mt * C::BM;
-          const int n0 = nt * BN;
-          if (!(args.has_lora && i == args.nk_total)) {
-            const int c0 = i * 64;
-            mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::C_BYTES + C::S_BYTES);
-            tma_load_2d(sA + s * C::A_BYTES, &tmA, &full[s], c0, m0);
-            if (!BWD) {
-              tma_load_2d(sC + s * C::C_BYTES, &tmC, &full[s], c0 / 2, n0);
-              tma_load_2d(sS + s * C::S_BYTES, &tmS, &full[s], n0, c0 / 64);
-            } else {
-              tma_load_2d(sC + s * C::C_BYTES, &tmC, &full[s], n0 / 2, c0);
-              tma_load_2d(sS + s * C::S_BYTES, &tmS, &full[s], c0, n0 / 64);
-            }
-          } else {
-            mbar_arrive_expect_tx(&full[s], C::A_BYTES);
+          const int m0 = ps.mt * UROWS + rank * C::BM;
+          mbar_arrive_expect_tx(&full[s], C::A_BYTES);
+          if (!(args.has_lora && ps.i == args.nk_total))
+            tma_load_2d(sA + s * C::A_BYTES, &tmA, &full[s], ps.i * 64, m0);
+          else
             tma_load_2d(sA + s * C::A_BYTES, &tmL, &full[s], 0, m0);
-          }
           issued = q + 1;
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
-          if (++i == (int)S) {
-            i = 0;
-            if (++mt == args.mtiles) {
-              mt = 0;
-              ++nt;
-            }
-          }
+          ps.next(S, args.mtiles);
         }
         if (*abort_flag) {
           // let every issued copy land before the CTA can exit
@@ -416,7 +522,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         constexpr uint32_t idesc_main = idesc_bf16_f32(128, BN, BWD ? 1u : 0u);
         constexpr uint32_t idesc_kmaj = idesc_bf16_f32(128, BN, 0u);
-        int64_t q = 0;
         int64_t seg = 0;
         int ms_s = 0, ms_b = 0;
         uint32_t ms_ph = 0, ms_bph = 0;
@@ -432,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t dbase = tmem + (uint32_t)(a * C::ACC_COLS);
           int i = (int)(p % S);
-          for (int64_t p2 = p; p2 < seg_end; ++p2, ++q, ++i) {
+          for (int64_t p2 = p; p2 < seg_end; ++p2, ++i) {
             const int s = ms_s, b = ms_b;
             const uint32_t ph = ms_ph, bph = ms_bph;
             if (++ms_s == STAGES) {
@@ -443,8 +548,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               ms_b = 0;
               ms_bph ^= 1u;
             }
-            if (*abort_flag || !mbar_wait(&full[s], ph, DERR_TIMEOUT_FULL) ||
-                !mbar_wait(&bfull[b], bph, DERR_TIMEOUT_BFULL)) {
+            bool ok = !*abort_flag && mbar_wait(&full[s], ph, DERR_TIMEOUT_FULL);
+            if constexpr (PAIR) ok = ok && mbar_wait_cluster(&bfull[b], bph, DERR_TIMEOUT_BFULL);
+            else ok = ok && mbar_wait(&bfull[b], bph, DERR_TIMEOUT_BFULL);
+            if (!ok) {
               *abort_flag = 1u;
               break;
             }
@@ -474,7 +581,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
             tc_commit(&empty[s]);
-            tc_commit(&bempty[b]);
+            if constexpr (PAIR) tc_commit_multicast(&bempty[b], (uint16_t)0x3);
+            else tc_commit(&bempty[b]);
           }
           tc_commit(&accfull[a]);
           p = seg_end;
@@ -485,55 +593,98 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp < 2 + kDqWarps) {
       // ------------------------------------------------------------ dequant producers
+      // Codes and scales are copied from global memory into this thread's
+      // ring slots CSTAGES - 1 steps ahead of their use; a weight buffer is
+      // refilled once the MMAs that read it have completed.
+      constexpr int CS = C::CSTAGES;
       const int t_idx = (int)threadIdx.x - 64;
-      int s = 0, b = 0;
-      uint32_t ph = 0, bph = 0;
-      int i = (int)(pb % S);
-      int mt = (int)((pb / S) % args.mtiles);
-      int nt = (int)((pb / S) / args.mtiles);
-      for (int64_t q = 0; q < pe - pb; ++q) {
-        if (*abort_flag || !mbar_wait(&full[s], ph, DERR_TIMEOUT_FULL) ||
-            !mbar_wait(&bempty[b], bph ^ 1u, DERR_TIMEOUT_BEMPTY)) {
+      const int64_t n_it = pe - pb;
+      uint8_t* ring = smem + C::OFF_CODE;
+      const uint32_t peer = (uint32_t)(rank ^ 1);
+      int b = 0;
+      uint32_t bph = 0;
+      Pos pc = pos0;  // position of the step being dequantised
+      Pos pf = pos0;  // position of the next fetch
+      int64_t fq = 0;
+      auto fetch = [&]() {
+        if (fq < n_it && !(args.has_lora && pf.i == args.nk_total))
+          fetch_codes<BWD, BN, PAIR>(smem_u32(ring + (fq % CS) * C::CODE_BYTES), args, pf.i,
+                                     pf.nt * BN, rank, t_idx);
+        cp_async_commit();
+        pf.next(S, args.mtiles);
+        ++fq;
+      };
+#pragma unroll 1
+      for (int k = 0; k < CS - 1; ++k) fetch();
+      for (int64_t q = 0; q < n_it; ++q) {
+        fetch();  // refills the slot read in the previous iteration
+        cp_async_wait<CS - 1>();
+        Frag cur;
+        read_frag<BWD, BN, PAIR>(cur, ring + (q % CS) * C::CODE_BYTES, t_idx);
+        bool ok = !*abort_flag;
+        if constexpr (PAIR) ok = ok && mbar_wait_cluster(&bempty[b], bph ^ 1u, DERR_TIMEOUT_BEMPTY);
+        else ok = ok && mbar_wait(&bempty[b], bph ^ 1u, DERR_TIMEOUT_BEMPTY);
+        if (!ok) {
           *abort_flag = 1u;
           break;
         }
-        const int n0 = nt * BN;
         uint8_t* Bt = sB + b * C::B_BYTES;
-        if (!(args.has_lora && i == args.nk_total)) {
-          const uint8_t* cs = sC + s * C::C_BYTES;
-          const float* ss = reinterpret_cast<const float*>(sS + s * C::S_BYTES);
-          if (!BWD) dequant_fwd<BN>(cs, ss, Bt, t_idx);
-          else dequant_bwd<BN>(cs, ss, Bt, t_idx);
+        const bool lora_step = args.has_lora && pc.i == args.nk_total;
+        if (!lora_step) {
+          if (!BWD) dequant_fwd<BN, PAIR>(cur, Bt, rank, t_idx);
+          else dequant_bwd<BN, PAIR>(cur, Bt, rank, t_idx);
         } else {
-          lora_tile<BWD, BN>(args.lora_F, args.Nout, args.Nout, n0, args.lora_scale, Bt, t_idx);
+          lora_tile<BWD, BN, PAIR>(args.lora_F, args.Nout, args.Nout, pc.nt * BN, args.lora_scale,
+                                   Bt, rank, t_idx);
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&bfull[b]);
-          mbar_arrive(&empty[s]);
-        }
-        if (++s == STAGES) {
-          s = 0;
-          ph ^= 1u;
+          if constexpr (PAIR) {
+            // this warp's share of the half tile is one contiguous block:
+            // rows (K-major) or one 8-row contraction group (MN-major);
+            // send it to the same place in the other CTA's buffer
+            constexpr uint32_t WB = C::B_BYTES / 16;
+            const int dw = warp - 2;
+            const uint32_t off =
+                (BWD && !lora_step)
+                    ? (uint32_t)(dw * (int)C::MN_SBO + rank * 1024)
+                    : (uint32_t)((rank * (BN / 2) + dw * (BN / 16)) * 128);
+            mbar_arrive_expect_tx(&bfull[b], WB);
+            bulk_copy_to_peer(mapa_shared(smem_u32(Bt + off), peer), Bt + off, WB,
+                              mapa_shared(smem_u32(&bfull[b]), peer));
+          } else {
+            mbar_arrive(&bfull[b]);
+          }
         }
         if (++b == BSTAGES) {
           b = 0;
           bph ^= 1u;
         }
-        if (++i == (int)S) {
-          i = 0;
-          if (++mt == args.mtiles) {
-            mt = 0;
-            ++nt;
+        pc.next(S, args.mtiles);
+      }
+      cp_async_wait<0>();  // no copy may land after the CTA is gone
+      if constexpr (PAIR) {
+        // the other CTA's MMA commits arrive on this CTA's buffer barriers:
+        // wait for the last of them before the CTA can leave
+        for (int k = 0; k < BSTAGES && !*abort_flag; ++k) {
+          if (!mbar_wait_cluster(&bempty[b], bph ^ 1u, DERR_TIMEOUT_DRAIN)) break;
+          if (++b == BSTAGES) {
+            b = 0;
+            bph ^= 1u;
           }
         }
-        (void)mt;
       }
     } else {
       // ------------------------------------------------------------ epilogue
+      // Eight warps: two per TMEM lane quarter, one for each half of the
+      // tile's columns, 16 columns at a time.
+      const int ew = warp - (2 + kDqWarps);
       const int q4 = warp & 3;  // TMEM lane quarter this warp may read
+      const int half = ew >> 2;
       const int r = q4 * 32 + lane;
+      // CTA holding this CTA's rows of the tile in unit u
+      auto cta_of = [&](int64_t u) -> int64_t { return PAIR ? 2 * u + rank : u; };
       int64_t seg = 0;
       for (int64_t p = pb; p < pe; ++seg) {
         const int64_t t = p / S;
@@ -544,23 +695,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t aph = (uint32_t)(seg / NACC) & 1u;
         const bool ok = !*abort_flag && mbar_wait_backoff(&accfull[a], aph, DERR_TIMEOUT_ACC);
         tc_fence_after();
-        const int64_t m0 = (t % args.mtiles) * C::BM;
+        const int64_t m0 = (t % args.mtiles) * UROWS + rank * C::BM;
         const int64_t n0 = (t / args.mtiles) * BN;
         const bool whole = (i0 == 0 && kb == S);
-        // the tile's first steps with the rest held by later CTAs: finish it here
+        // the tile's first steps with the rest held by later units: finish it here
         const bool finisher = (i0 == 0 && kb < S);
         const bool writer = !whole && !finisher;  // a later piece: hand it over
         const bool lora_in = args.has_lora && kb == S;
         // a backward segment made of the LoRA step alone never wrote D
         const bool main_in = !BWD || i0 < args.nk_total;
         float* part = args.partial + (int64_t)blockIdx.x * C::TILE_FLOATS;
-        int64_t g_last = blockIdx.x;
+        int64_t u_last = unit;
         if (finisher) {
-          g_last = sk_cta_of(t * S + S - 1, I, G);
+          u_last = sk_cta_of(t * S + S - 1, I, U);
           // wait for the later pieces (each CTA publishes at most one)
           bool got = ok;
-          for (int64_t g = (int64_t)blockIdx.x + 1; g <= g_last && got; ++g) {
-            const uint32_t* f = args.flags + g;
+          for (int64_t u = unit + 1; u <= u_last && got; ++u) {
+            const uint32_t* f = args.flags + cta_of(u);
             if (ld_acquire_gpu(f) != 1u) {
               const uint64_t t0 = globaltimer();
               while (ld_acquire_gpu(f) != 1u) {
@@ -573,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-          if (!got) g_last = blockIdx.x;  // timed out: store what is here, flagged as an error
+          if (!got) u_last = unit;  // timed out: store what is here, flagged as an error
         }
         const uint32_t dbase = tmem + (uint32_t)(a * C::ACC_COLS);
 #pragma unroll 1
@@ -582,57 +733,75 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t m = m0 + row;
           const bool row_ok = ok && m < args.M;
 #pragma unroll 1
-          for (int cc = 0; cc < BN; cc += 32) {
+          for (int cc = half * (BN / 2); cc < (half + 1) * (BN / 2); cc += 16) {
             const int64_t n = n0 + cc;
             if (n >= args.Nout) break;  // warp-uniform
-            uint32_t acc[32];
+            uint32_t acc[16];
             const uint32_t taddr = dbase + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(u * BN + cc);
-            tmem_ld_32x32b_x32(taddr, acc);
-            uint32_t lacc[32];
-            if (BWD && lora_in) tmem_ld_32x32b_x32(taddr + (uint32_t)(UM * BN), lacc);
+            tmem_ld_32x32b_x16(taddr, acc);
+            uint32_t lacc[16];
+            if (BWD && lora_in) tmem_ld_32x32b_x16(taddr + (uint32_t)(UM * BN), lacc);
+            // the first later piece's values load while the TMEM read is in flight
+            float4 pv[4];
+            const bool piece = row_ok && !writer && u_last > unit;
+            if (piece) {
+              const float4* src = reinterpret_cast<const float4*>(
+                  args.partial + cta_of(unit + 1) * C::TILE_FLOATS + (int64_t)row * BN + cc);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) pv[e] = src[e];
+            }
             tmem_ld_wait();
             if (!row_ok) continue;
-            float v[32];
+            float v[16];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = main_in ? __uint_as_float(acc[e]) : 0.0f;
+            for (int e = 0; e < 16; ++e) v[e] = main_in ? __uint_as_float(acc[e]) : 0.0f;
             if (BWD && lora_in) {
-              const uint32_t bits = args.mask[(m * args.Nout + n) >> 5];
+              const uint32_t bits = args.mask[(m * args.Nout + n) >> 5] >> (n & 31);
 #pragma unroll
-              for (int e = 0; e < 32; ++e)
+              for (int e = 0; e < 16; ++e)
                 if ((bits >> e) & 1u) v[e] += __uint_as_float(lacc[e]);
             }
             if (writer) {
               float4* dst = reinterpret_cast<float4*>(part + (int64_t)row * BN + cc);
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
+              for (int e = 0; e < 4; ++e)
                 dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
               continue;
             }
             // finisher: add the later pieces in step order
-            for (int64_t g = (int64_t)blockIdx.x + 1; g <= g_last; ++g) {
-              const float4* src = reinterpret_cast<const float4*>(
-                  args.partial + g * C::TILE_FLOATS + (int64_t)row * BN + cc);
+            if (piece) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float4 pv = src[e];
-                v[4 * e] += pv.x;
-                v[4 * e + 1] += pv.y;
-                v[4 * e + 2] += pv.z;
-                v[4 * e + 3] += pv.w;
+              for (int e = 0; e < 4; ++e) {
+                v[4 * e] += pv[e].x;
+                v[4 * e + 1] += pv[e].y;
+                v[4 * e + 2] += pv[e].z;
+                v[4 * e + 3] += pv[e].w;
+              }
+            }
+            for (int64_t uu = unit + 2; uu <= u_last; ++uu) {
+              const float4* src = reinterpret_cast<const float4*>(
+                  args.partial + cta_of(uu) * C::TILE_FLOATS + (int64_t)row * BN + cc);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float4 q = src[e];
+                v[4 * e] += q.x;
+                v[4 * e + 1] += q.y;
+                v[4 * e + 2] += q.z;
+                v[4 * e + 3] += q.w;
               }
             }
             if (args.out_f32) {
               float4* dst =
                   reinterpret_cast<float4*>(static_cast<float*>(args.out) + m * args.Nout + n);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
+              for (int e = 0; e < 4; ++e) {
                 float4 o = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
                 if (args.out_accum) {
-                  const float4 pv = dst[e];
-                  o.x = pv.x + o.x;
-                  o.y = pv.y + o.y;
-                  o.z = pv.z + o.z;
-                  o.w = pv.w + o.w;
+                  const float4 q = dst[e];
+                  o.x = q.x + o.x;
+                  o.y = q.y + o.y;
+                  o.z = q.z + o.z;
+                  o.w = q.w + o.w;
                 }
                 dst[e] = o;
               }
@@ -640,7 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint4* dst =
                   reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.out) + m * args.Nout + n);
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
+              for (int e = 0; e < 2; ++e)
                 dst[e] = make_uint4(pack_bf16x2(v[8 * e], v[8 * e + 1]),
                                     pack_bf16x2(v[8 * e + 2], v[8 * e + 3]),
                                     pack_bf16x2(v[8 * e + 4], v[8 * e + 5]),
@@ -652,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // publish the piece: every epilogue thread's stores, then one flag
           __threadfence();
           named_bar_sync(1, kEpiWarps * 32);
-          if (warp == 2 + kDqWarps && lane == 0) st_release_gpu(args.flags + blockIdx.x, 1u);
+          if (ew == 0 && lane == 0) st_release_gpu(args.flags + blockIdx.x, 1u);
         }
         tc_fence_before();
         __syncwarp();
@@ -663,7 +832,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  // neither CTA of a pair leaves while the other may still write into it
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
@@ -897,22 +1068,53 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 // iterations per CTA so tiny problems are not shredded into partials.
 constexpr int64_t kMinSteps = 8;
 
-template <bool BWD, int UM, int BN>
-cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& tA,
-                       const CUtensorMap& tC, const CUtensorMap& tS, const CUtensorMap& tL,
-                       cudaStream_t st) {
-  using C = Cfg<BWD, UM, BN>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_nf4_gemm<BWD, UM, BN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
+template <bool BWD, int UM, int BN, bool PAIR>
+cudaError_t set_smem_attr() {
+  static cudaError_t e = cudaFuncSetAttribute(k_nf4_gemm<BWD, UM, BN, PAIR>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)Cfg<BWD, UM, BN, PAIR>::SMEM_BYTES);
+  return e;
+}
+
+// Pairs of CTAs that can be resident at once (one CTA per SM).
+template <bool BWD, int BN>
+int64_t pair_capacity_of() {
+  static int64_t cap = -1;
+  if (cap < 0) {
+    cap = 0;
+    if (set_smem_attr<BWD, 2, BN, true>() == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (unsigned)(device_sm_count() / 2));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = Cfg<BWD, 2, BN, true>::SMEM_BYTES;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, k_nf4_gemm<BWD, 2, BN, true>, &cfg) == cudaSuccess)
+        cap = n;
+      else
+        cudaGetLastError();
+    } else {
+      cudaGetLastError();
+    }
   }
+  return cap;
+}
+
+template <bool BWD, int UM, int BN, bool PAIR>
+cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& tA,
+                       const CUtensorMap& tL, cudaStream_t st) {
+  using C = Cfg<BWD, UM, BN, PAIR>;
+  cudaError_t e = set_smem_attr<BWD, UM, BN, PAIR>();
+  if (e != cudaSuccess) return e;
   const int64_t G = grid_ctas(p, a.has_lora != 0);
-  if (G > 1) {
-    cudaError_t e = cudaMemsetAsync(a.flags, 0, (size_t)G * sizeof(uint32_t), st);
+  if (grid_units(p, a.has_lora != 0) > 1) {
+    e = cudaMemsetAsync(a.flags, 0, (size_t)G * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
   }
   // cooperative: all CTAs resident at once, so a finisher's wait for a
@@ -922,13 +1124,18 @@ cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = PAIR ? 2 : 1;
   note_launch();
-  return cudaLaunchKernelEx(&cfg, k_nf4_gemm<BWD, UM, BN>, tA, tC, tS, tL, a);}
+  return cudaLaunchKernelEx(&cfg, k_nf4_gemm<BWD, UM, BN, PAIR>, tA, tL, a);
+}
 
 }  // namespace
 
@@ -977,16 +1184,26 @@ int device_sm_count() {
   return sms;
 }
 
-int64_t grid_ctas(const GemmPlan& p, bool has_lora) {
+int64_t pair_capacity(bool bwd, int bn) {
+  if (bwd) return bn == 128 ? pair_capacity_of<true, 128>() : 0;
+  return bn == 256 ? pair_capacity_of<false, 256>() : pair_capacity_of<false, 128>();
+}
+
+int64_t grid_units(const GemmPlan& p, bool has_lora) {
   const int64_t S = (int64_t)p.nk + (has_lora ? 1 : 0);
   const int64_t I = (int64_t)p.mtiles * p.ntiles * S;
-  // at least kMinSteps iterations per CTA, and few enough CTAs that one tile
-  // is never cut into more pieces than the fix-up kernel gathers (64)
+  // at least kMinSteps iterations per unit, and few enough units that one
+  // tile is never cut into very many pieces
   int64_t min_steps = S / 48 + 2;
   if (min_steps < kMinSteps) min_steps = kMinSteps;
   int64_t G = (I + min_steps - 1) / min_steps;
-  if (G > device_sm_count()) G = device_sm_count();
+  const int64_t cap = p.pair ? pair_capacity(p.bwd, p.bn) : device_sm_count();
+  if (G > cap) G = cap;
   return G < 1 ? 1 : G;
+}
+
+int64_t grid_ctas(const GemmPlan& p, bool has_lora) {
+  return grid_units(p, has_lora) * (p.pair ? 2 : 1);
 }
 
 GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc) {
@@ -994,14 +1211,19 @@ GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc) {
   p.bwd = bwd;
   p.um = M > 128 ? 2 : 1;
   p.bn = 128;
-  // A 256-wide forward tile halves the activation-tile traffic per flop but
-  // has a single accumulator (no epilogue overlap): worth it only when there
-  // are enough tiles that stream-K pieces stay long.
+  // Two CTAs of a cluster share each weight tile when there are rows for
+  // both (one dequantisation per 512 activation rows).
+  p.pair = M > 256 && pair_capacity(bwd, 128) > 0;
+  const int64_t urows = 128 * p.um * (p.pair ? 2 : 1);
   if (!bwd && p.um == 2) {
-    const int64_t mt = (M + 255) / 256, nt = (Nout + 255) / 256;
-    if (mt * nt >= device_sm_count()) p.bn = 256;
+    // A 256-wide forward tile halves the activation-tile traffic per flop
+    // but has a single accumulator (no epilogue overlap): worth it only
+    // when there are enough tiles that stream-K pieces stay long.
+    const int64_t units = p.pair ? pair_capacity(false, 256) : device_sm_count();
+    const int64_t mt = (M + urows - 1) / urows, nt = (Nout + 255) / 256;
+    if (mt * nt >= units && units > 0) p.bn = 256;
   }
-  p.mtiles = (int)((M + 128 * p.um - 1) / (128 * p.um));
+  p.mtiles = (int)((M + urows - 1) / urows);
   p.ntiles = (int)((Nout + p.bn - 1) / p.bn);
   p.nk = (int)(Kc / 64);
   return p;
@@ -1012,7 +1234,7 @@ size_t gemm_partial_bytes(const GemmPlan& p, int64_t M, int64_t Nout) {
   (void)M;
   (void)Nout;
   const int64_t G = grid_ctas(p, true);
-  if (G <= 1) return 0;
+  if (grid_units(p, true) <= 1) return 0;
   return (size_t)G * (size_t)(128 * p.um) * (size_t)p.bn * sizeof(float) +
          (((size_t)G * sizeof(uint32_t) + 255) & ~size_t(255));
 }
@@ -1026,24 +1248,9 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
   const int64_t Nout = p.bwd ? K : N;
   const int64_t Kc = p.bwd ? N : K;
   const int BM = 128 * p.um;
-  CUtensorMap tA, tC, tS, tL;
+  CUtensorMap tA, tL;
   bool ok = make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, (uint64_t)Kc, (uint64_t)M,
                      (uint64_t)Kc * 2, 64, (uint32_t)BM, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!p.bwd) {
-    ok = ok && make_map(&tC, CU_TENSOR_MAP_DATA_TYPE_UINT8, W.codes, (uint64_t)(K / 2),
-                        (uint64_t)N, (uint64_t)(K / 2), 32, (uint32_t)p.bn,
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
-    ok = ok && make_map(&tS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, W.absmax, (uint64_t)N,
-                        (uint64_t)(K / 64), (uint64_t)N * 4, (uint32_t)p.bn, 1,
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
-  } else {
-    ok = ok && make_map(&tC, CU_TENSOR_MAP_DATA_TYPE_UINT8, W.codes, (uint64_t)(K / 2),
-                        (uint64_t)N, (uint64_t)(K / 2), (uint32_t)(p.bn / 2), 64,
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
-    ok = ok && make_map(&tS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, W.absmax, (uint64_t)N,
-                        (uint64_t)(K / 64), (uint64_t)N * 4, 64, (uint32_t)(p.bn / 64),
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
-  }
   const bool has_lora = lora_act != nullptr && lora_F != nullptr;
   if (has_lora)
     ok = ok && make_map(&tL, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lora_act, 64, (uint64_t)M, 128, 64,
@@ -1066,18 +1273,27 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
   a.out_f32 = out_f32;
   a.out_accum = out_accum;
   a.partial = partial;
+  a.codes = W.codes;
+  a.absmax = W.absmax;
+  a.wN = N;
+  a.wK = K;
   a.flags = partial == nullptr ? nullptr
                                : reinterpret_cast<uint32_t*>(
                                      partial + grid_ctas(p, true) * (int64_t)(128 * p.um) * p.bn);
 
-  if (partial == nullptr && grid_ctas(p, has_lora) > 1) return cudaErrorInvalidValue;
+  if (partial == nullptr && grid_units(p, has_lora) > 1) return cudaErrorInvalidValue;
   if (!p.bwd) {
-    if (p.um == 2 && p.bn == 256) return launch_cfg<false, 2, 256>(p, a, tA, tC, tS, tL, st);
-    if (p.um == 2) return launch_cfg<false, 2, 128>(p, a, tA, tC, tS, tL, st);
-    return launch_cfg<false, 1, 128>(p, a, tA, tC, tS, tL, st);
+    if (p.pair) {
+      if (p.bn == 256) return launch_cfg<false, 2, 256, true>(p, a, tA, tL, st);
+      return launch_cfg<false, 2, 128, true>(p, a, tA, tL, st);
+    }
+    if (p.um == 2 && p.bn == 256) return launch_cfg<false, 2, 256, false>(p, a, tA, tL, st);
+    if (p.um == 2) return launch_cfg<false, 2, 128, false>(p, a, tA, tL, st);
+    return launch_cfg<false, 1, 128, false>(p, a, tA, tL, st);
   }
-  if (p.um == 2) return launch_cfg<true, 2, 128>(p, a, tA, tC, tS, tL, st);
-  return launch_cfg<true, 1, 128>(p, a, tA, tC, tS, tL, st);
+  if (p.pair) return launch_cfg<true, 2, 128, true>(p, a, tA, tL, st);
+  if (p.um == 2) return launch_cfg<true, 2, 128, false>(p, a, tA, tL, st);
+  return launch_cfg<true, 1, 128, false>(p, a, tA, tL, st);
 }
 
 // ------------------------------------------------------------------------ weight gradients (host)
