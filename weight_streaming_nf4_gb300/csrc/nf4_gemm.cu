@@ -256,7 +256,7 @@ WS_DEVINL void fetch_codes(uint32_t slot, const GemmArgs& g, int i, int n0, int 
   const int64_t kb = g.wK / 2;  // code bytes per weight row
   const int c0 = PAIR ? rank * D::COLS : 0;
   const uint32_t sc = slot + (uint32_t)(D::NV * kDqThreads * D::VB);
-  if (!BWD) {
+  if constexpr (!BWD) {
     const int j = c0 + t / D::TPR, part = t % D::TPR;
     const int64_t n = (int64_t)n0 + j;
     const bool in = n < g.wN;
@@ -842,57 +842,59 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------------ LoRA weight gradients
 // out[c][j] = s * sum_m P[m][j] * Q~[m][c] (dB: P = U, Q = dY; dA: P = G,
 // Q = x under the dropout mask) as a tensor-core GEMM D = P^T Q:
-//   A = [P_hi^T ; P_lo^T ; 0] (128 x 64 tokens per step, bf16 high/low
-//       parts of the fp32 P, K-major, TMA with 128-byte swizzle),
-//   B = Q tile (64 tokens x 256 columns, MN-major, four TMA boxes of 64
-//       columns), masked in shared memory for dA by four warps,
-//   D = 128 x 256 fp32 in TMEM; rows j and 16+j add up to P^T Q.
-// Grid: 256-column tiles x token chunks; each CTA writes the fp32 partial of
-// its chunk and a second kernel sums the chunks in index order.
+//   A = [P_hi^T ; P_lo^T ; 0] (128 rows x 64 tokens per step, bf16 high /
+//       low parts of the fp32 P), built in shared memory by four warps,
+//   B = Q tile (64 tokens x 128 columns, MN-major, two TMA boxes of 64
+//       columns), masked in shared memory by the same warps for dA,
+//   D = 128 x 128 fp32 in TMEM; rows j and 16+j add up to P^T Q.
+// One CTA per 128 columns runs every token step, so the sum over tokens
+// has one fixed order and the result is written straight out.
 constexpr int kWgThreads = 192;
 constexpr int kWgStages = 4;
-constexpr uint32_t kWgA = 128 * 128;      // A stage bytes
-constexpr uint32_t kWgB = 4 * 64 * 128;   // B stage bytes (4 boxes of 64 rows x 128 B)
+constexpr int kWgBN = 128;
+constexpr uint32_t kWgA = 128 * 128;     // A stage bytes
+constexpr uint32_t kWgB = 2 * 64 * 128;  // B stage bytes (2 boxes of 64 tokens x 128 B)
 constexpr uint32_t kWgSmem = kWgStages * (kWgA + kWgB) + (3 * kWgStages + 1) * 8 + 16 + 1024;
 
 template <bool MASKED>
 __global__ void __launch_bounds__(kWgThreads, 1)
-    k_wgrad_tc(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
-               const uint32_t* __restrict__ mask, int64_t M, int64_t C, int steps_per_chunk,
-               float* __restrict__ partial) {
+    k_wgrad_tc(const __grid_constant__ CUtensorMap tmQ, const float* __restrict__ P,
+               const uint32_t* __restrict__ mask, int64_t M, int64_t C, float s,
+               int transpose_out, float* __restrict__ out) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kWgStages * kWgA;
   uint64_t* full = reinterpret_cast<uint64_t*>(sB + kWgStages * kWgB);
-  uint64_t* masked = full + kWgStages;
-  uint64_t* empty = masked + kWgStages;
+  uint64_t* ready = full + kWgStages;
+  uint64_t* empty = ready + kWgStages;
   uint64_t* accfull = empty + kWgStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accfull + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* skip_flag = tmem_slot + 2;
   const int warp = (int)warp_id(), lane = (int)lane_id();
-  const int64_t c0 = (int64_t)blockIdx.x * 256;
-  const int64_t total_steps = (M + 63) / 64;
-  const int64_t s_begin = (int64_t)blockIdx.y * steps_per_chunk;
-  const int64_t s_end = min(total_steps, s_begin + steps_per_chunk);
-  const int nsteps = (int)(s_end - s_begin);
+  const int64_t c0 = (int64_t)blockIdx.x * kWgBN;
+  const int nsteps = (int)((M + 63) / 64);
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
     *skip_flag = (*(volatile uint32_t*)&g_dev_error != 0u || nsteps <= 0) ? 1u : 0u;
     for (int i = 0; i < kWgStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&masked[i], 4);
+      mbar_init(&ready[i], 4);
       mbar_init(&empty[i], 1);
     }
     mbar_init(accfull, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, kWgBN);
     tmem_relinquish();
   }
+  // rows 32..127 of every A stage stay zero
+  for (uint32_t o = threadIdx.x * 16; o < kWgStages * kWgA; o += kWgThreads * 16)
+    *reinterpret_cast<uint4*>(sA + o) = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -908,12 +910,10 @@ __global__ void __launch_bounds__(kWgThreads, 1)
             *abort_flag = 1u;
             break;
           }
-          const int t0 = (int)((s_begin + i) * 64);
-          mbar_arrive_expect_tx(&full[st], kWgA + kWgB);
-          tma_load_2d(sA + st * kWgA, &tmP, &full[st], t0, 0);
-#pragma unroll
-          for (int b = 0; b < 4; ++b)
-            tma_load_2d(sB + st * kWgB + b * 8192, &tmQ, &full[st], (int)(c0 + 64 * b), t0);
+          const int t0 = i * 64;
+          mbar_arrive_expect_tx(&full[st], kWgB);
+          tma_load_2d(sB + st * kWgB, &tmQ, &full[st], (int)c0, t0);
+          tma_load_2d(sB + st * kWgB + 8192, &tmQ, &full[st], (int)(c0 + 64), t0);
           issued = i + 1;
         }
         if (*abort_flag)
@@ -922,11 +922,11 @@ __global__ void __launch_bounds__(kWgThreads, 1)
       }
     } else if (warp == 1) {
       if (lane == 0) {
-        constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 1u);
+        constexpr uint32_t idesc = idesc_bf16_f32(128, kWgBN, 1u);
         for (int i = 0; i < nsteps; ++i) {
           const int st = i % kWgStages;
           const uint32_t ph = (uint32_t)(i / kWgStages) & 1u;
-          if (*abort_flag || !mbar_wait(MASKED ? &masked[st] : &full[st], ph, DERR_TIMEOUT_FULL)) {
+          if (*abort_flag || !mbar_wait(&ready[st], ph, DERR_TIMEOUT_FULL)) {
             *abort_flag = 1u;
             break;
           }
@@ -943,30 +943,55 @@ __global__ void __launch_bounds__(kWgThreads, 1)
         tc_commit(accfull);
       }
     } else {
-      if (MASKED) {
-        // zero the dropped elements of each landed x tile
-        const int mt = (int)threadIdx.x - 64;  // 0..127
-        for (int i = 0; i < nsteps; ++i) {
-          const int st = i % kWgStages;
-          const uint32_t ph = (uint32_t)(i / kWgStages) & 1u;
-          if (*abort_flag || !mbar_wait(&full[st], ph, DERR_TIMEOUT_FULL)) {
-            *abort_flag = 1u;
-            break;
+      // ---- warps 2-5: build the A tile from P and (dA) mask the Q tile
+      const int t = (int)threadIdx.x - 64;  // 0..127
+      const int jj = t & 15, tg = t >> 4;   // P column, 8-token group
+      for (int i = 0; i < nsteps; ++i) {
+        const int st = i % kWgStages;
+        const uint32_t ph = (uint32_t)(i / kWgStages) & 1u;
+        const int64_t t0 = (int64_t)i * 64;
+        // loads that do not depend on the tile are issued first
+        float pv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int64_t m = t0 + tg * 8 + e;
+          pv[e] = m < M ? __ldg(P + m * 16 + jj) : 0.0f;
+        }
+        uint32_t mw[8];
+        if (MASKED) {
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int ch = t + it * 128;  // 0..1023: token row r, 8-column chunk q
+            const int r = ch >> 4, q = ch & 15;
+            const int64_t m = t0 + r, c = c0 + q * 8;
+            mw[it] = (m < M && c < C) ? __ldg(mask + ((m * C + c) >> 5)) : 0xFFFFFFFFu;
           }
-          const int64_t t0 = (s_begin + i) * 64;
+        }
+        if (*abort_flag || !mbar_wait(&full[st], ph, DERR_TIMEOUT_FULL)) {
+          *abort_flag = 1u;
+          break;
+        }
+        // A rows jj (high parts) and 16 + jj (low parts), tokens 8 tg .. 8 tg + 7
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float h0 = bf16_lo(pack_bf16x2(pv[2 * e], 0.0f));
+          const float h1 = bf16_lo(pack_bf16x2(pv[2 * e + 1], 0.0f));
+          hi[e] = pack_bf16x2(h0, h1);
+          lo[e] = pack_bf16x2(pv[2 * e] - h0, pv[2 * e + 1] - h1);
+        }
+        uint8_t* At = sA + st * kWgA;
+        sts128(At + jj * 128 + ((tg ^ (jj & 7)) << 4), hi[0], hi[1], hi[2], hi[3]);
+        sts128(At + (16 + jj) * 128 + ((tg ^ ((16 + jj) & 7)) << 4), lo[0], lo[1], lo[2], lo[3]);
+        if (MASKED) {
           uint8_t* tile = sB + st * kWgB;
-          const uint8_t* mbytes = reinterpret_cast<const uint8_t*>(mask);
-#pragma unroll 4
-          for (int it = 0; it < 16; ++it) {
-            const int ch = mt + it * 128;       // 0..2047
-            const int r = ch >> 5;              // token row 0..63
-            const int q = ch & 31;              // 16-byte chunk of the 256 columns
-            const int b = q >> 3, q8 = q & 7;
-            const int64_t m = t0 + r;
-            const int64_t c = c0 + q * 8;
-            if (m >= M || c >= C) continue;
-            const uint32_t bits = mbytes[(m * C + c) >> 3];
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int ch = t + it * 128;
+            const int r = ch >> 4, q = ch & 15;
+            const uint32_t bits = (mw[it] >> ((q & 3) * 8)) & 0xFFu;
             if (bits == 0xFFu) continue;
+            const int b = q >> 3, q8 = q & 7;
             uint4* p4 = reinterpret_cast<uint4*>(tile + b * 8192 + r * 128 + ((q8 ^ (r & 7)) << 4));
             uint4 v = *p4;
             uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -978,16 +1003,16 @@ __global__ void __launch_bounds__(kWgThreads, 1)
             }
             *p4 = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&masked[st]);
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ready[st]);
       }
       if (warp == 4) {
         // rows 0..31 of D live in TMEM lanes 0..31 (lane quarter of warp 4)
         const bool ok = mbar_wait(accfull, 0u, DERR_TIMEOUT_ACC) && !*abort_flag;
         tc_fence_after();
-        for (int cc = 0; cc < 256; cc += 32) {
+        for (int cc = 0; cc < kWgBN; cc += 32) {
           uint32_t acc[32];
           tmem_ld_32x32b_x32(tmem + (uint32_t)cc, acc);
           tmem_ld_wait();
@@ -997,12 +1022,28 @@ __global__ void __launch_bounds__(kWgThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const float x = __uint_as_float(acc[e]);
-            v[e] = x + __shfl_xor_sync(0xffffffffu, x, 16);  // hi row + lo row
+            v[e] = s * (x + __shfl_xor_sync(0xffffffffu, x, 16));  // high row + low row
           }
           if (lane < 16) {
-            float* dst = partial + ((int64_t)blockIdx.y * C + cb) * 16 + lane;
+            const int ncol = (int)(C - cb < 32 ? C - cb : 32);
+            if (transpose_out) {
+              float* dst = out + (int64_t)lane * C + cb;
+              if (ncol == 32 && ((C & 3) == 0)) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) dst[(int64_t)e * 16] = v[e];
+                for (int e = 0; e < 8; ++e)
+                  reinterpret_cast<float4*>(dst)[e] =
+                      make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  if (e < ncol) dst[e] = v[e];
+              }
+            } else {
+              float* dst = out + cb * 16 + lane;
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (e < ncol) dst[(int64_t)e * 16] = v[e];
+            }
           }
         }
       }
@@ -1011,24 +1052,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 256);
-}
-
-// PT [128][Mp]: row j < 16 = bf16 high part of P[:, j], row 16 + j = low
-// part, rows 32..127 zero (the padding rows of the 128-row MMA operand);
-// columns M..Mp-1 zero (Mp = M rounded up to 8, a 16-byte aligned pitch).
-__global__ void k_pt_split(const float* __restrict__ P, int64_t M, int64_t Mp,
-                           uint16_t* __restrict__ PT) {
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // (row, m)
-  if (t >= 128 * Mp) return;
-  const int64_t row = t / Mp, m = t % Mp;
-  uint16_t v = 0;
-  if (row < 32 && m < M) {
-    const float p = P[m * 16 + (row & 15)];
-    const uint16_t hi = f32_to_bf16_bits(p);
-    v = row < 16 ? hi : f32_to_bf16_bits(p - bf16_bits_to_f32(hi));
-  }
-  PT[t] = v;
+  if (warp == 1) tmem_dealloc(tmem, kWgBN);
 }
 
 }  // namespace
@@ -1297,64 +1321,35 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
 }
 
 // ------------------------------------------------------------------------ weight gradients (host)
-int wgrad_tc_chunks(int64_t M, int64_t C) {
-  const int64_t steps = (M + 63) / 64;
-  const int64_t ctiles = (C + 255) / 256;
-  int64_t ch = (device_sm_count() + ctiles - 1) / ctiles;
-  if (ch > steps) ch = steps;
-  if (ch < 1) ch = 1;
-  return (int)ch;
-}
-
 size_t wgrad_tc_bytes(int64_t M, int64_t C) {
-  const int64_t Mp = (M + 7) / 8 * 8;
-  const size_t part = (size_t)wgrad_tc_chunks(M, C) * (size_t)C * 16 * sizeof(float);
-  return ((part + 255) & ~size_t(255)) + (((size_t)128 * Mp * 2 + 255) & ~size_t(255));
+  (void)M;
+  (void)C;
+  return 0;
 }
 
 cudaError_t run_wgrad_tc(const float* P, const uint16_t* Q, const uint32_t* mask, int64_t M,
                          int64_t C, float s, float* out, int transpose_out, void* ws,
                          cudaStream_t st) {
+  (void)ws;
   if (!encode_fn()) return cudaErrorNotSupported;
-  const int64_t Mp = (M + 7) / 8 * 8;
-  const int chunks = wgrad_tc_chunks(M, C);
-  const int64_t steps = (M + 63) / 64;
-  const int spc = (int)((steps + chunks - 1) / chunks);
-  float* partial = static_cast<float*>(ws);
-  const size_t part = (size_t)chunks * (size_t)C * 16 * sizeof(float);
-  uint16_t* PT = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + ((part + 255) & ~size_t(255)));
-  note_launch();
-  k_pt_split<<<(unsigned)((128 * Mp + 255) / 256), 256, 0, st>>>(P, M, Mp, PT);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  CUtensorMap tP, tQ;
-  if (!make_map(&tP, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, PT, (uint64_t)Mp, 128, (uint64_t)Mp * 2, 64,
-                128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&tQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, (uint64_t)C, (uint64_t)M, (uint64_t)C * 2,
+  CUtensorMap tQ;
+  if (!make_map(&tQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, (uint64_t)C, (uint64_t)M, (uint64_t)C * 2,
                 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  static bool attr0 = false, attr1 = false;
-  if (!attr0) {
-    e = cudaFuncSetAttribute(k_wgrad_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kWgSmem);
-    if (e != cudaSuccess) return e;
-    attr0 = true;
-  }
-  if (!attr1) {
-    e = cudaFuncSetAttribute(k_wgrad_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kWgSmem);
-    if (e != cudaSuccess) return e;
-    attr1 = true;
-  }
-  dim3 grid((unsigned)((C + 255) / 256), (unsigned)chunks);
+  static cudaError_t attr0 = cudaFuncSetAttribute(
+      k_wgrad_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWgSmem);
+  static cudaError_t attr1 = cudaFuncSetAttribute(
+      k_wgrad_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWgSmem);
+  if (attr0 != cudaSuccess) return attr0;
+  if (attr1 != cudaSuccess) return attr1;
+  const dim3 grid((unsigned)((C + kWgBN - 1) / kWgBN));
   note_launch();
   if (mask)
-    k_wgrad_tc<true><<<grid, kWgThreads, kWgSmem, st>>>(tP, tQ, mask, M, C, spc, partial);
+    k_wgrad_tc<true><<<grid, kWgThreads, kWgSmem, st>>>(tQ, P, mask, M, C, s, transpose_out, out);
   else
-    k_wgrad_tc<false><<<grid, kWgThreads, kWgSmem, st>>>(tP, tQ, nullptr, M, C, spc, partial);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return run_wgrad_reduce(partial, chunks, C, s, out, transpose_out, st);
+    k_wgrad_tc<false><<<grid, kWgThreads, kWgSmem, st>>>(tQ, P, nullptr, M, C, s, transpose_out,
+                                                         out);
+  return cudaGetLastError();
 }
 
 }  // namespace ws
