@@ -193,6 +193,16 @@ WS_DEVINL void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int32
       : "memory");
 }
 
+// Untiled bulk copy global -> shared (16-byte aligned addresses, size a
+// multiple of 16), completing as transaction bytes on a local mbarrier.
+WS_DEVINL void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---- tcgen05 -------------------------------------------------------------------------------
 WS_DEVINL void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -279,6 +289,11 @@ WS_DEVINL bool elect_lane0() { return lane_id() == 0; }
 
 // Named barrier among `nthreads` threads (id 1..15; id 0 is __syncthreads).
 // ---- thread-block clusters ------------------------------------------------------------
+WS_DEVINL uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
 WS_DEVINL uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

@@ -36,6 +36,7 @@
 // way into a second TMEM accumulator and adds it under the dropout mask in
 // the epilogue.
 #define WS_GEMM_TU 1
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -440,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = (int)warp_id();
   const int lane = (int)lane_id();
-  const int rank = PAIR ? (int)cluster_ctarank() : 0;
+  const int rank = PAIR ? (int)(cluster_ctarank() & 1u) : 0;
   // ---- static stream-K schedule over units (CTAs, or pairs of CTAs)
   const int S = args.nk_total + (args.has_lora ? 1 : 0);  // steps per tile
   const int64_t T = (int64_t)args.mtiles * args.ntiles;
@@ -452,10 +453,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Pos pos0 = {(int)(pb % S), (int)((pb / S) % args.mtiles), (int)((pb / S) / args.mtiles)};
   constexpr int UROWS = PAIR ? 2 * C::BM : C::BM;  // activation rows per tile
 
+  // a pair kernel launched without its two-CTA clusters has no partner to
+  // share with: record the configuration error and do nothing
+  const bool bad_cfg = PAIR && (cluster_nctarank() != 2u || (gridDim.x & 1u) != 0u);
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
+    if (bad_cfg) atomicOr(&g_dev_error, DERR_BAD_CONFIG);
     // an earlier kernel already gave up: do nothing rather than queue more work
-    *skip_flag = (*(volatile uint32_t*)&g_dev_error != 0u || pe <= pb) ? 1u : 0u;
+    *skip_flag = (bad_cfg || *(volatile uint32_t*)&g_dev_error != 0u || pe <= pb) ? 1u : 0u;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
@@ -477,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   // both CTAs of a pair have their barriers set up before either arrives remotely
-  if constexpr (PAIR) cluster_sync();
+  if (PAIR && !bad_cfg) cluster_sync();
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -833,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   // neither CTA of a pair leaves while the other may still write into it
-  if constexpr (PAIR) cluster_sync();
+  if (PAIR && !bad_cfg) cluster_sync();
   else __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
@@ -854,7 +859,10 @@ constexpr int kWgStages = 4;
 constexpr int kWgBN = 128;
 constexpr uint32_t kWgA = 128 * 128;     // A stage bytes
 constexpr uint32_t kWgB = 2 * 64 * 128;  // B stage bytes (2 boxes of 64 tokens x 128 B)
-constexpr uint32_t kWgSmem = kWgStages * (kWgA + kWgB) + (3 * kWgStages + 1) * 8 + 16 + 1024;
+constexpr uint32_t kWgP = 64 * 16 * 4;   // P rows of one step, fp32
+constexpr uint32_t kWgMw = 8 * 128 * 4;  // mask words of one step, 8 per builder thread
+constexpr uint32_t kWgSmem =
+    kWgStages * (kWgA + kWgB + kWgP + kWgMw) + (3 * kWgStages + 1) * 8 + 16 + 1024;
 
 template <bool MASKED>
 __global__ void __launch_bounds__(kWgThreads, 1)
@@ -866,7 +874,9 @@ __global__ void __launch_bounds__(kWgThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kWgStages * kWgA;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kWgStages * kWgB);
+  uint8_t* sP = sB + kWgStages * kWgB;
+  uint8_t* sMw = sP + kWgStages * kWgP;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sMw + kWgStages * kWgMw);
   uint64_t* ready = full + kWgStages;
   uint64_t* empty = ready + kWgStages;
   uint64_t* accfull = empty + kWgStages;
@@ -911,9 +921,11 @@ __global__ void __launch_bounds__(kWgThreads, 1)
             break;
           }
           const int t0 = i * 64;
-          mbar_arrive_expect_tx(&full[st], kWgB);
+          const int64_t rows = M - t0 < 64 ? M - t0 : 64;
+          mbar_arrive_expect_tx(&full[st], kWgB + (uint32_t)rows * 64u);
           tma_load_2d(sB + st * kWgB, &tmQ, &full[st], (int)c0, t0);
           tma_load_2d(sB + st * kWgB + 8192, &tmQ, &full[st], (int)(c0 + 64), t0);
+          bulk_load(sP + st * kWgP, P + (int64_t)t0 * 16, (uint32_t)rows * 64u, &full[st]);
           issued = i + 1;
         }
         if (*abort_flag)
@@ -944,32 +956,51 @@ __global__ void __launch_bounds__(kWgThreads, 1)
       }
     } else {
       // ---- warps 2-5: build the A tile from P and (dA) mask the Q tile
+      // P rows arrive with the Q tile; this thread's dropout-mask words are
+      // copied into its own ring slots kWgStages - 1 steps ahead.
       const int t = (int)threadIdx.x - 64;  // 0..127
       const int jj = t & 15, tg = t >> 4;   // P column, 8-token group
-      for (int i = 0; i < nsteps; ++i) {
-        const int st = i % kWgStages;
-        const uint32_t ph = (uint32_t)(i / kWgStages) & 1u;
-        const int64_t t0 = (int64_t)i * 64;
-        // loads that do not depend on the tile are issued first
-        float pv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int64_t m = t0 + tg * 8 + e;
-          pv[e] = m < M ? __ldg(P + m * 16 + jj) : 0.0f;
-        }
-        uint32_t mw[8];
-        if (MASKED) {
+      auto fetch_mask = [&](int i) {
+        if (MASKED && i < nsteps) {
+          const int64_t t0 = (int64_t)i * 64;
+          const uint32_t slot = smem_u32(sMw + (i % kWgStages) * kWgMw);
 #pragma unroll
           for (int it = 0; it < 8; ++it) {
             const int ch = t + it * 128;  // 0..1023: token row r, 8-column chunk q
             const int r = ch >> 4, q = ch & 15;
             const int64_t m = t0 + r, c = c0 + q * 8;
-            mw[it] = (m < M && c < C) ? __ldg(mask + ((m * C + c) >> 5)) : 0xFFFFFFFFu;
+            const bool in = m < M && c < C;
+            cp_async4(slot + (uint32_t)((it * 128 + t) * 4), mask + (in ? (m * C + c) >> 5 : 0),
+                      in ? 4u : 0u);
           }
         }
+        cp_async_commit();
+      };
+#pragma unroll 1
+      for (int k = 0; k < kWgStages - 1; ++k) fetch_mask(k);
+      for (int i = 0; i < nsteps; ++i) {
+        const int st = i % kWgStages;
+        const uint32_t ph = (uint32_t)(i / kWgStages) & 1u;
+        const int64_t t0 = (int64_t)i * 64;
+        fetch_mask(i + kWgStages - 1);  // refills the slot read in the previous step
         if (*abort_flag || !mbar_wait(&full[st], ph, DERR_TIMEOUT_FULL)) {
           *abort_flag = 1u;
           break;
+        }
+        float pv[8];
+        const float* sp = reinterpret_cast<const float*>(sP + st * kWgP);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) pv[e] = (t0 + tg * 8 + e < M) ? sp[(tg * 8 + e) * 16 + jj] : 0.0f;
+        uint32_t mw[8];
+        if (MASKED) {
+          cp_async_wait<kWgStages - 1>();
+          const uint32_t* sm = reinterpret_cast<const uint32_t*>(sMw + st * kWgMw);
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int ch = t + it * 128;
+            const int r = ch >> 4, q = ch & 15;
+            mw[it] = (t0 + r < M && c0 + q * 8 < C) ? sm[it * 128 + t] : 0xFFFFFFFFu;
+          }
         }
         // A rows jj (high parts) and 16 + jj (low parts), tokens 8 tg .. 8 tg + 7
         uint32_t hi[4], lo[4];
@@ -1008,6 +1039,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&ready[st]);
       }
+      cp_async_wait<0>();  // no copy may land after the CTA is gone
       if (warp == 4) {
         // rows 0..31 of D live in TMEM lanes 0..31 (lane quarter of warp 4)
         const bool ok = mbar_wait(accfull, 0u, DERR_TIMEOUT_ACC) && !*abort_flag;
@@ -1155,8 +1187,15 @@ cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& 
   attr[1].val.clusterDim.x = 2;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = PAIR ? 2 : 1;
+  // WS_NF4_COOP=0 drops the cooperative attribute (the grid is sized to be
+  // resident anyway); profilers that cannot launch cooperative clusters
+  // need it.
+  static const bool coop = [] {
+    const char* v = getenv("WS_NF4_COOP");
+    return !(v && v[0] == '0');
+  }();
+  cfg.attrs = coop ? attr : attr + 1;
+  cfg.numAttrs = (coop ? 1 : 0) + (PAIR ? 1 : 0);
   note_launch();
   return cudaLaunchKernelEx(&cfg, k_nf4_gemm<BWD, UM, BN, PAIR>, tA, tL, a);
 }
@@ -1240,12 +1279,12 @@ GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc) {
   p.pair = M > 256 && pair_capacity(bwd, 128) > 0;
   const int64_t urows = 128 * p.um * (p.pair ? 2 : 1);
   if (!bwd && p.um == 2) {
-    // A 256-wide forward tile halves the activation-tile traffic per flop
-    // but has a single accumulator (no epilogue overlap): worth it only
-    // when there are enough tiles that stream-K pieces stay long.
+    // A 256-wide forward tile reads less shared memory per flop (256-wide
+    // MMAs) but has a single accumulator (no epilogue overlap): worth it
+    // when each unit's stream-K range stays long (>= 64 steps).
     const int64_t units = p.pair ? pair_capacity(false, 256) : device_sm_count();
     const int64_t mt = (M + urows - 1) / urows, nt = (Nout + 255) / 256;
-    if (mt * nt >= units && units > 0) p.bn = 256;
+    if (units > 0 && mt * nt * (Kc / 64 + 1) >= 64 * units) p.bn = 256;
   }
   p.mtiles = (int)((M + urows - 1) / urows);
   p.ntiles = (int)((Nout + p.bn - 1) / p.bn);
@@ -1332,6 +1371,8 @@ cudaError_t run_wgrad_tc(const float* P, const uint16_t* Q, const uint32_t* mask
                          cudaStream_t st) {
   (void)ws;
   if (!encode_fn()) return cudaErrorNotSupported;
+  // P rows are fetched with 16-byte bulk copies
+  if ((reinterpret_cast<uintptr_t>(P) & 15u) != 0u) return cudaErrorInvalidValue;
   CUtensorMap tQ;
   if (!make_map(&tQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, (uint64_t)C, (uint64_t)M, (uint64_t)C * 2,
                 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
