@@ -77,30 +77,28 @@ DropKeyHost make_drop_key(const ws_dropout_key& k);
 
 cudaError_t run_quantize_nf4(const uint16_t* W, int64_t N, int64_t K, uint8_t* codes,
                              float* absmax, cudaStream_t st);
-// U = (mask . x) A^T [M,16] fp32; Uext [M,64] bf16 hi/lo; mask bits (optional).
-// partial: skinny_partial_bytes(M, K) of scratch.
+// Scratch of run_skinny_tc / run_lora_down / run_lora_G (chunk partial sums
+// and per-row-block counters).
 size_t skinny_partial_bytes(int64_t M, int64_t K);
+// out [M,16] = X~ F^T on the tensor cores (see nf4_gemm.cu); key != NULL:
+// X under the dropout mask (bits stored to mask_bytes when not NULL).
+cudaError_t run_skinny_tc(const uint16_t* X, const float* F, bool f_kj, int64_t M, int64_t K,
+                          const DropKey* key, uint8_t* mask_bytes, float* partial, float* out,
+                          uint16_t* ext, cudaStream_t st);
+// U = (mask . x) A^T [M,16] fp32; Uext [M,64] bf16 hi/lo; mask bits (optional).
 cudaError_t run_lora_down(const uint16_t* x, const float* A, int64_t M, int64_t K,
                           const DropKeyHost& key, float* U, uint16_t* Uext, uint32_t* mask_out,
                           float* partial, cudaStream_t st);
 // G = dY B [M,16] fp32 and Gext [M,64] bf16 hi/lo.
 cudaError_t run_lora_G(const uint16_t* dY, const float* B, int64_t M, int64_t N, float* G,
                        uint16_t* Gext, float* partial, cudaStream_t st);
-// Weight gradient of a LoRA factor: out = s * P^T Q~ with P [M,16] fp32,
-// Q [M,C] bf16 (masked by `mask` [M, C/32] when not NULL).  out layout is
-// [C,16] (dB) or, when transpose_out, [16,C] (dA).  Fixed-order reduction.
-size_t wgrad_partial_bytes(int64_t M, int64_t C);
-cudaError_t run_lora_wgrad(const float* P, const uint16_t* Q, const uint32_t* mask, int64_t M,
-                           int64_t C, float s, float* out, int transpose_out, float* partial,
-                           cudaStream_t st);
+// Dropout keep bits [M, K/32] of one linear, regenerated from the key.
 cudaError_t run_mask_gen(int64_t M, int64_t K, const DropKeyHost& key, uint32_t* mask,
                          cudaStream_t st);
-// Fixed-order sum of chunk partials [chunks][C][16], scaled by s, into
-// out [C][16] (or [16][C] when transpose_out).
-cudaError_t run_wgrad_reduce(const float* partial, int chunks, int64_t C, float s, float* out,
-                             int transpose_out, cudaStream_t st);
-// The same weight gradients on the tensor cores (nf4_gemm.cu): workspace of
-// wgrad_tc_bytes(M, C).
+// Weight gradient of a LoRA factor on the tensor cores (nf4_gemm.cu):
+// out = s * P^T Q~ with P [M,16] fp32, Q [M,C] bf16 (masked by `mask`
+// [M, C/32] when not NULL).  out layout is [C,16] (dB) or, when
+// transpose_out, [16,C] (dA).  One fixed summation order; no workspace.
 size_t wgrad_tc_bytes(int64_t M, int64_t C);
 cudaError_t run_wgrad_tc(const float* P, const uint16_t* Q, const uint32_t* mask, int64_t M,
                          int64_t C, float s, float* out, int transpose_out, void* ws,

@@ -1087,6 +1087,295 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kWgBN);
 }
 
+// ------------------------------------------------------------------------ LoRA skinny products
+// out[m][j] = sum_k X~[m][k] * F[j][k] for the 16 LoRA columns j (U: X = x
+// under the dropout mask, whose bits this kernel draws and stores, F = A;
+// G: X = dY, F = B^T), on the tensor cores:
+//   A operand = X tile (128 rows x 64 k, TMA, 128-byte swizzle), masked in
+//       shared memory for U,
+//   B operand = [F_hi ; F_mid ; F_lo] (48 rows x 64 k): the fp32 factor
+//       split into three bf16 parts, built in shared memory,
+//   D = 128 x 48 fp32 in TMEM; out = (D_hi + D_mid) + D_lo per column.
+// CTA = one 128-row block x one chunk of k steps; each CTA stores its
+// partial sums, and the last CTA of a row block (counted with an atomic)
+// adds the chunks in index order and writes the result and its bf16 split.
+constexpr int kSkThreads = 320;  // TMA, MMA, 8 builder warps
+constexpr int kSkStages = 4;
+constexpr uint32_t kSkX = 128 * 128;    // X stage bytes
+constexpr uint32_t kSkF = 64 * 16 * 4;  // fp32 factor slice of one step
+constexpr uint32_t kSkB = 64 * 128;     // B operand: 48 rows used of 64
+constexpr uint32_t kSkSmem =
+    kSkStages * (kSkX + kSkF + kSkB) + (3 * kSkStages + 1) * 8 + 16 + 1024;
+
+// F_KJ: the factor is given as [K][16] (B), else as [16][K] (A).
+template <bool MASKED, bool F_KJ>
+__global__ void __launch_bounds__(kSkThreads, 1)
+    k_skinny_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmF,
+                const float* __restrict__ F, int64_t M, int64_t K, int steps_per_chunk,
+                DropKey key, uint8_t* __restrict__ mask_bytes, float* __restrict__ partial,
+                uint32_t* __restrict__ counters, float* __restrict__ out,
+                uint16_t* __restrict__ ext) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sX = smem;
+  uint8_t* sBop = sX + kSkStages * kSkX;
+  uint8_t* sF = sBop + kSkStages * kSkB;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sF + kSkStages * kSkF);
+  uint64_t* ready = full + kSkStages;
+  uint64_t* empty = ready + kSkStages;
+  uint64_t* accfull = empty + kSkStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accfull + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  volatile uint32_t* flags = tmem_slot + 2;  // [0] skip, [1] this CTA finishes the row block
+  const int warp = (int)warp_id(), lane = (int)lane_id();
+  const int64_t m0 = (int64_t)blockIdx.x * 128;
+  const int chunks = (int)gridDim.y;
+  const int64_t nsteps_total = K / 64;
+  const int64_t s_begin = (int64_t)blockIdx.y * steps_per_chunk;
+  const int64_t s_end = min(nsteps_total, s_begin + steps_per_chunk);
+  const int nsteps = (int)(s_end > s_begin ? s_end - s_begin : 0);
+  if (MASKED) resolve_step(key);
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    flags[0] = (*(volatile uint32_t*)&g_dev_error != 0u) ? 1u : 0u;
+    flags[1] = 0u;
+    for (int i = 0; i < kSkStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&ready[i], 8);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(accfull, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 64);
+    tmem_relinquish();
+  }
+  // rows 48..63 of every B-operand stage stay zero
+  for (uint32_t o = threadIdx.x * 16; o < kSkStages * kSkB; o += kSkThreads * 16)
+    *reinterpret_cast<uint4*>(sBop + o) = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool skip = flags[0] != 0u;
+  if (!skip) {
+    if (warp == 0) {
+      if (lane == 0 && nsteps > 0) {
+        int64_t issued = 0;
+        for (int i = 0; i < nsteps; ++i) {
+          const int st = i % kSkStages;
+          const uint32_t ph = (uint32_t)(i / kSkStages) & 1u;
+          if (*abort_flag || !mbar_wait(&empty[st], ph ^ 1u, DERR_TIMEOUT_EMPTY)) {
+            *abort_flag = 1u;
+            break;
+          }
+          const int k0 = (int)((s_begin + i) * 64);
+          mbar_arrive_expect_tx(&full[st], kSkX + kSkF);
+          tma_load_2d(sX + st * kSkX, &tmX, &full[st], k0, (int)m0);
+          if (F_KJ) bulk_load(sF + st * kSkF, F + (int64_t)k0 * 16, kSkF, &full[st]);
+          else tma_load_2d(sF + st * kSkF, &tmF, &full[st], k0, 0);
+          issued = i + 1;
+        }
+        if (*abort_flag)
+          for (int64_t i = (issued > kSkStages ? issued - kSkStages : 0); i < issued; ++i)
+            mbar_wait(&full[i % kSkStages], (uint32_t)(i / kSkStages) & 1u, DERR_TIMEOUT_DRAIN);
+      }
+    } else if (warp == 1) {
+      if (lane == 0 && nsteps > 0) {
+        constexpr uint32_t idesc = idesc_bf16_f32(128, 48, 0u);
+        for (int i = 0; i < nsteps; ++i) {
+          const int st = i % kSkStages;
+          const uint32_t ph = (uint32_t)(i / kSkStages) & 1u;
+          if (*abort_flag || !mbar_wait(&ready[st], ph, DERR_TIMEOUT_FULL)) {
+            *abort_flag = 1u;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sX + st * kSkX);
+          const uint32_t b_base = smem_u32(sBop + st * kSkB);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_f16(tmem, smem_desc_sw128(a_base + kk * 32, 16, 1024),
+                       smem_desc_sw128(b_base + kk * 32, 16, 1024), idesc,
+                       (i > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&empty[st]);
+        }
+        tc_commit(accfull);
+      }
+    } else {
+      // ---- warps 2-9: the split factor operand and (U) the dropout mask
+      const int t = (int)threadIdx.x - 64;  // 0..255
+      for (int i = 0; i < nsteps; ++i) {
+        const int st = i % kSkStages;
+        const uint32_t ph = (uint32_t)(i / kSkStages) & 1u;
+        const int64_t k0 = (s_begin + i) * 64;
+        if (*abort_flag || !mbar_wait(&full[st], ph, DERR_TIMEOUT_FULL)) {
+          *abort_flag = 1u;
+          break;
+        }
+        if (t < 128) {
+          // B rows jj, 16 + jj, 32 + jj: high, middle, low bf16 parts of
+          // F[jj][k0 + 8 kc ...]
+          const int jj = t & 15, kc = t >> 4;
+          const float* fs = reinterpret_cast<const float*>(sF + st * kSkF);
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = F_KJ ? fs[(kc * 8 + e) * 16 + jj] : fs[jj * 64 + kc * 8 + e];
+          uint32_t w[3][4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float a0 = f[2 * e], a1 = f[2 * e + 1];
+#pragma unroll
+            for (int part = 0; part < 3; ++part) {
+              const uint32_t pk = pack_bf16x2(a0, a1);
+              w[part][e] = pk;
+              a0 -= bf16_lo(pk);
+              a1 -= bf16_hi(pk);
+            }
+          }
+          uint8_t* Bt = sBop + st * kSkB;
+#pragma unroll
+          for (int part = 0; part < 3; ++part) {
+            const int row = part * 16 + jj;
+            sts128(Bt + row * 128 + ((kc ^ (row & 7)) << 4), w[part][0], w[part][1], w[part][2],
+                   w[part][3]);
+          }
+        }
+        if (MASKED) {
+          uint8_t* tile = sX + st * kSkX;
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int ch = t + it * 256;  // 0..1023: row r, 8-column chunk q
+            const int r = ch >> 3, q = ch & 7;
+            const int64_t m = m0 + r;
+            if (m >= M) continue;
+            const uint64_t e0 = (uint64_t)m * (uint64_t)K + (uint64_t)(k0 + q * 8);
+            const uint32_t bits = keep4(key, e0) | (keep4(key, e0 + 4) << 4);
+            if (mask_bytes) mask_bytes[e0 >> 3] = (uint8_t)bits;
+            if (bits == 0xFFu) continue;
+            uint4* p4 = reinterpret_cast<uint4*>(tile + r * 128 + ((q ^ (r & 7)) << 4));
+            uint4 v = *p4;
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t keep = ((bits >> (2 * e)) & 1u ? 0x0000FFFFu : 0u) |
+                                    ((bits >> (2 * e + 1)) & 1u ? 0xFFFF0000u : 0u);
+              w[e] &= keep;
+            }
+            *p4 = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ready[st]);
+      }
+      if (warp < 6) {
+        // ---- epilogue, warps 2-5 (TMEM lane quarters 2, 3, 0, 1): this
+        // chunk's partial sums of its rows
+        const int q4 = warp & 3;
+        const int64_t m = m0 + q4 * 32 + lane;
+        const bool ok =
+            nsteps == 0 || (mbar_wait(accfull, 0u, DERR_TIMEOUT_ACC) && !*abort_flag);
+        tc_fence_after();
+        float v[16];
+        if (nsteps > 0) {
+          uint32_t a[32], b[16];
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(q4 * 32) << 16), a);
+          tmem_ld_32x32b_x16(tmem + ((uint32_t)(q4 * 32) << 16) + 32u, b);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            v[j] = (__uint_as_float(a[j]) + __uint_as_float(a[16 + j])) + __uint_as_float(b[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+        }
+        if (ok && m < M) {
+          float4* dst = reinterpret_cast<float4*>(partial + ((int64_t)blockIdx.y * M + m) * 16);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        }
+        // the last chunk of this row block to finish sums them all in order
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (warp == 2 && lane == 0) {
+          const uint32_t done = atomicAdd(counters + blockIdx.x, 1u);
+          if (done >= (uint32_t)chunks) atomicOr(&g_dev_error, DERR_BAD_CONFIG);  // left over
+          flags[1] = (done == (uint32_t)chunks - 1u) ? 1u : 0u;
+        }
+        named_bar_sync(1, 128);
+        if (flags[1] != 0u) {
+          __threadfence();
+          if (ok && m < M) {
+            // chunks are added in index order; loads run eight chunks ahead
+            float acc[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+            const float4* src = reinterpret_cast<const float4*>(partial + m * 16);
+            const int64_t cstride = M * 4;  // float4 per chunk
+            int c = 0;
+            for (; c + 8 <= chunks; c += 8) {
+              float4 q[8][4];
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) q[u][e] = __ldcg(src + (int64_t)(c + u) * cstride + e);
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  acc[4 * e] += q[u][e].x;
+                  acc[4 * e + 1] += q[u][e].y;
+                  acc[4 * e + 2] += q[u][e].z;
+                  acc[4 * e + 3] += q[u][e].w;
+                }
+            }
+            for (; c < chunks; ++c) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float4 q = __ldcg(src + (int64_t)c * cstride + e);
+                acc[4 * e] += q.x;
+                acc[4 * e + 1] += q.y;
+                acc[4 * e + 2] += q.z;
+                acc[4 * e + 3] += q.w;
+              }
+            }
+            float4* o = reinterpret_cast<float4*>(out + m * 16);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              o[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
+            // [hi | lo | hi | 0] bf16 row for the tensor-core LoRA step
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              hi[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
+              lo[e] = pack_bf16x2(acc[2 * e] - bf16_lo(hi[e]), acc[2 * e + 1] - bf16_hi(hi[e]));
+            }
+            uint4* x4 = reinterpret_cast<uint4*>(ext + m * 64);
+            x4[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            x4[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+            x4[2] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            x4[3] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+            x4[4] = x4[0];
+            x4[5] = x4[1];
+            x4[6] = make_uint4(0u, 0u, 0u, 0u);
+            x4[7] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          if (warp == 2 && lane == 0) counters[blockIdx.x] = 0u;  // ready for the next launch
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 64);
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------------- host
@@ -1357,6 +1646,99 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
   if (p.pair) return launch_cfg<true, 2, 128, true>(p, a, tA, tL, st);
   if (p.um == 2) return launch_cfg<true, 2, 128, false>(p, a, tA, tL, st);
   return launch_cfg<true, 1, 128, false>(p, a, tA, tL, st);
+}
+
+// ------------------------------------------------------------------------ skinny products (host)
+int skinny_tc_chunks(int64_t M, int64_t K) {
+  const int64_t atoms = (M + 127) / 128;
+  const int64_t steps = K / 64;
+  int64_t ch = device_sm_count() / (atoms > 0 ? atoms : 1);
+  if (ch > steps) ch = steps;
+  if (ch < 1) ch = 1;
+  const int64_t spc = (steps + ch - 1) / ch;
+  return (int)((steps + spc - 1) / spc);
+}
+
+size_t skinny_partial_bytes(int64_t M, int64_t K) {
+  return (size_t)skinny_tc_chunks(M, K) * (size_t)M * 16 * sizeof(float);
+}
+
+// Arrival counters of the row blocks, one per block of each launch, taken
+// round-robin from a library-owned array.  They start at zero and the last
+// CTA of a row block puts its counter back to zero, so no launch has to
+// clear them first.  Launches in flight at the same time on different
+// streams get different counters unless more than kSkCounters row blocks
+// are enqueued in between.
+constexpr uint32_t kSkCounters = 1u << 16;
+static __device__ uint32_t g_skinny_counters[kSkCounters];
+namespace {
+std::mutex g_skc_mu;
+uint32_t* g_skc_ptr[64] = {};
+uint32_t g_skc_next = 0;
+}  // namespace
+
+static cudaError_t skinny_counters(uint32_t atoms, uint32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || atoms > 1024) return cudaErrorInvalidValue;
+  std::lock_guard<std::mutex> lock(g_skc_mu);
+  if (!g_skc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_skinny_counters);
+    if (e != cudaSuccess) return e;
+    g_skc_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  if (g_skc_next + atoms > kSkCounters) g_skc_next = 0;
+  *out = g_skc_ptr[dev] + g_skc_next;
+  g_skc_next += atoms;
+  return cudaSuccess;
+}
+
+cudaError_t run_skinny_tc(const uint16_t* X, const float* F, bool f_kj, int64_t M, int64_t K,
+                          const DropKey* key, uint8_t* mask_bytes, float* partial, float* out,
+                          uint16_t* ext, cudaStream_t st) {
+  if (!encode_fn()) return cudaErrorNotSupported;
+  if (K % 64 != 0 || M < 1) return cudaErrorInvalidValue;
+  // the factor slices are fetched with 16-byte copies
+  if ((reinterpret_cast<uintptr_t>(F) & 15u) != 0u) return cudaErrorInvalidValue;
+  const int64_t atoms = (M + 127) / 128;
+  const int chunks = skinny_tc_chunks(M, K);
+  const int64_t steps = K / 64;
+  const int spc = (int)((steps + chunks - 1) / chunks);
+  uint32_t* counters = nullptr;
+  cudaError_t e = skinny_counters((uint32_t)atoms, &counters);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tX, tF;
+  if (!make_map(&tX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2,
+                64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (f_kj) tF = tX;
+  else if (!make_map(&tF, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, F, (uint64_t)K, 16, (uint64_t)K * 4, 64,
+                     16, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  static cudaError_t a0 = cudaFuncSetAttribute(
+      k_skinny_tc<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSkSmem);
+  static cudaError_t a1 = cudaFuncSetAttribute(
+      k_skinny_tc<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSkSmem);
+  static cudaError_t a2 = cudaFuncSetAttribute(
+      k_skinny_tc<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSkSmem);
+  if (a0 != cudaSuccess) return a0;
+  if (a1 != cudaSuccess) return a1;
+  if (a2 != cudaSuccess) return a2;
+  const dim3 grid((unsigned)atoms, (unsigned)chunks);
+  DropKey none{};
+  note_launch();
+  if (key && !f_kj)
+    k_skinny_tc<true, false><<<grid, kSkThreads, kSkSmem, st>>>(
+        tX, tF, F, M, K, spc, *key, mask_bytes, partial, counters, out, ext);
+  else if (f_kj)
+    k_skinny_tc<false, true><<<grid, kSkThreads, kSkSmem, st>>>(
+        tX, tF, F, M, K, spc, none, nullptr, partial, counters, out, ext);
+  else
+    k_skinny_tc<false, false><<<grid, kSkThreads, kSkSmem, st>>>(
+        tX, tF, F, M, K, spc, none, nullptr, partial, counters, out, ext);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------------ weight gradients (host)
