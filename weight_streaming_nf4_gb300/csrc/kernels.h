@@ -32,7 +32,8 @@ struct GemmArgs {
   void* out;            // [M, Nout] bf16 or fp32
   int out_f32, out_accum;
   float* partial;       // [grid, BM, BN] fp32 partial tile of each CTA's cut first segment
-  uint32_t* flags;      // [grid] set to 1 once that partial is complete (zeroed per launch)
+  uint32_t* flags;      // [grid] set to 1 once that partial is complete (ring words, zero
+                        // before and after the launch)
   const uint8_t* codes; // the weight's packed codes [N, K/2]
   const float* absmax;  // the weight's block scales [K/64, N]
   int64_t wN, wK;       // the weight's shape
@@ -58,6 +59,8 @@ cudaError_t noalloc_scratch(float** ptr, size_t* bytes);
 // Counts every kernel launch the library makes (reported by ws_kernel_launches).
 void note_launch();
 cudaError_t read_and_clear_dev_error(uint32_t* flags);
+// n zeroed cross-CTA words that the launch using them leaves zeroed again.
+cudaError_t ring_slots(uint32_t n, uint32_t** out);
 GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc);
 size_t gemm_partial_bytes(const GemmPlan& p, int64_t M, int64_t Nout);
 

@@ -44,11 +44,18 @@
 
 namespace ws {
 
+cudaError_t ring_clear();
+
 cudaError_t read_and_clear_dev_error(uint32_t* flags) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return e;
   e = cudaMemcpyFromSymbol(flags, g_dev_error, sizeof(uint32_t));
   if (e != cudaSuccess) return e;
+  if (*flags != 0u) {
+    // a kernel gave up part way: cross-CTA words may be left set
+    e = ring_clear();
+    if (e != cudaSuccess) return e;
+  }
   const uint32_t zero = 0;
   return cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(uint32_t));
 }
@@ -438,6 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = misc;
   volatile uint32_t* abort_flag = misc + 1;
   volatile uint32_t* skip_flag = misc + 2;
+  volatile uint32_t* fin_got = misc + 3;
 
   const int warp = (int)warp_id();
   const int lane = (int)lane_id();
@@ -713,23 +721,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t u_last = unit;
         if (finisher) {
           u_last = sk_cta_of(t * S + S - 1, I, U);
-          // wait for the later pieces (each CTA publishes at most one)
-          bool got = ok;
-          for (int64_t u = unit + 1; u <= u_last && got; ++u) {
-            const uint32_t* f = args.flags + cta_of(u);
-            if (ld_acquire_gpu(f) != 1u) {
-              const uint64_t t0 = globaltimer();
-              while (ld_acquire_gpu(f) != 1u) {
-                __nanosleep(128);
-                if (globaltimer() - t0 > kWaitLimitNs) {
-                  atomicOr(&g_dev_error, DERR_TIMEOUT_PEER);
-                  got = false;
-                  break;
+          // one thread waits for the later pieces (each CTA publishes at
+          // most one); the barrier passes what it acquired to the others
+          if (ew == 0 && lane == 0) {
+            bool got = ok;
+            for (int64_t u = unit + 1; u <= u_last && got; ++u) {
+              const uint32_t* f = args.flags + cta_of(u);
+              if (ld_acquire_gpu(f) != 1u) {
+                const uint64_t t0 = globaltimer();
+                while (ld_acquire_gpu(f) != 1u) {
+                  __nanosleep(128);
+                  if (globaltimer() - t0 > kWaitLimitNs) {
+                    atomicOr(&g_dev_error, DERR_TIMEOUT_PEER);
+                    got = false;
+                    break;
+                  }
                 }
               }
             }
+            *fin_got = got ? 1u : 0u;
+            // consumed: the flags go back to zero for the next launch using them
+            if (got)
+              for (int64_t u = unit + 1; u <= u_last; ++u) args.flags[cta_of(u)] = 0u;
           }
-          if (!got) u_last = unit;  // timed out: store what is here, flagged as an error
+          named_bar_sync(2, kEpiWarps * 32);
+          if (*fin_got == 0u) u_last = unit;  // timed out: store what is here, flagged as an error
         }
         const uint32_t dbase = tmem + (uint32_t)(a * C::ACC_COLS);
 #pragma unroll 1
@@ -1458,10 +1474,6 @@ cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& 
   cudaError_t e = set_smem_attr<BWD, UM, BN, PAIR>();
   if (e != cudaSuccess) return e;
   const int64_t G = grid_ctas(p, a.has_lora != 0);
-  if (grid_units(p, a.has_lora != 0) > 1) {
-    e = cudaMemsetAsync(a.flags, 0, (size_t)G * sizeof(uint32_t), st);
-    if (e != cudaSuccess) return e;
-  }
   // cooperative: all CTAs resident at once, so a finisher's wait for a
   // later CTA's piece always ends
   cudaLaunchConfig_t cfg = {};
@@ -1581,14 +1593,13 @@ GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc) {
   return p;
 }
 
-// [G][BM][BN] fp32 partial tiles, then [G] uint32 completion flags.
+// [G][BM][BN] fp32 partial tiles.
 size_t gemm_partial_bytes(const GemmPlan& p, int64_t M, int64_t Nout) {
   (void)M;
   (void)Nout;
   const int64_t G = grid_ctas(p, true);
   if (grid_units(p, true) <= 1) return 0;
-  return (size_t)G * (size_t)(128 * p.um) * (size_t)p.bn * sizeof(float) +
-         (((size_t)G * sizeof(uint32_t) + 255) & ~size_t(255));
+  return (size_t)G * (size_t)(128 * p.um) * (size_t)p.bn * sizeof(float);
 }
 
 cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* act, int64_t M,
@@ -1629,9 +1640,11 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
   a.absmax = W.absmax;
   a.wN = N;
   a.wK = K;
-  a.flags = partial == nullptr ? nullptr
-                               : reinterpret_cast<uint32_t*>(
-                                     partial + grid_ctas(p, true) * (int64_t)(128 * p.um) * p.bn);
+  a.flags = nullptr;
+  if (grid_units(p, has_lora) > 1) {
+    cudaError_t e = ring_slots((uint32_t)grid_ctas(p, has_lora), &a.flags);
+    if (e != cudaSuccess) return e;
+  }
 
   if (partial == nullptr && grid_units(p, has_lora) > 1) return cudaErrorInvalidValue;
   if (!p.bwd) {
@@ -1663,36 +1676,56 @@ size_t skinny_partial_bytes(int64_t M, int64_t K) {
   return (size_t)skinny_tc_chunks(M, K) * (size_t)M * 16 * sizeof(float);
 }
 
-// Arrival counters of the row blocks, one per block of each launch, taken
-// round-robin from a library-owned array.  They start at zero and the last
-// CTA of a row block puts its counter back to zero, so no launch has to
-// clear them first.  Launches in flight at the same time on different
-// streams get different counters unless more than kSkCounters row blocks
-// are enqueued in between.
-constexpr uint32_t kSkCounters = 1u << 16;
-static __device__ uint32_t g_skinny_counters[kSkCounters];
+// Cross-CTA words of a launch (stream-K completion flags of the dequant
+// GEMM, arrival counters of the skinny products' row blocks), taken
+// round-robin from a library-owned array.  They start at zero and each
+// launch leaves the words it used at zero again (a finisher clears the flags
+// it consumed; the last CTA of a row block clears its counter), so no launch
+// has to clear them first.  Launches in flight at the same time on different
+// streams get different words unless more than kRingWords words are handed
+// out in between.  ws_device_error clears the whole array after a kernel
+// gave up.
+constexpr uint32_t kRingWords = 1u << 20;
+static __device__ uint32_t g_ring_words[kRingWords];
 namespace {
-std::mutex g_skc_mu;
-uint32_t* g_skc_ptr[64] = {};
-uint32_t g_skc_next = 0;
+std::mutex g_ring_mu;
+uint32_t* g_ring_ptr[64] = {};
+uint32_t g_ring_next = 0;
 }  // namespace
 
-static cudaError_t skinny_counters(uint32_t atoms, uint32_t** out) {
+static cudaError_t ring_base(uint32_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || atoms > 1024) return cudaErrorInvalidValue;
-  std::lock_guard<std::mutex> lock(g_skc_mu);
-  if (!g_skc_ptr[dev]) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!g_ring_ptr[dev]) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_skinny_counters);
+    e = cudaGetSymbolAddress(&p, g_ring_words);
     if (e != cudaSuccess) return e;
-    g_skc_ptr[dev] = static_cast<uint32_t*>(p);
+    g_ring_ptr[dev] = static_cast<uint32_t*>(p);
   }
-  if (g_skc_next + atoms > kSkCounters) g_skc_next = 0;
-  *out = g_skc_ptr[dev] + g_skc_next;
-  g_skc_next += atoms;
+  *out = g_ring_ptr[dev];
   return cudaSuccess;
+}
+
+cudaError_t ring_slots(uint32_t n, uint32_t** out) {
+  if (n == 0 || n > 4096) return cudaErrorInvalidValue;
+  std::lock_guard<std::mutex> lock(g_ring_mu);
+  uint32_t* base = nullptr;
+  cudaError_t e = ring_base(&base);
+  if (e != cudaSuccess) return e;
+  if (g_ring_next + n > kRingWords) g_ring_next = 0;
+  *out = base + g_ring_next;
+  g_ring_next += n;
+  return cudaSuccess;
+}
+
+cudaError_t ring_clear() {
+  std::lock_guard<std::mutex> lock(g_ring_mu);
+  uint32_t* base = nullptr;
+  cudaError_t e = ring_base(&base);
+  if (e != cudaSuccess) return e;
+  return cudaMemset(base, 0, (size_t)kRingWords * sizeof(uint32_t));
 }
 
 cudaError_t run_skinny_tc(const uint16_t* X, const float* F, bool f_kj, int64_t M, int64_t K,
@@ -1707,7 +1740,7 @@ cudaError_t run_skinny_tc(const uint16_t* X, const float* F, bool f_kj, int64_t 
   const int64_t steps = K / 64;
   const int spc = (int)((steps + chunks - 1) / chunks);
   uint32_t* counters = nullptr;
-  cudaError_t e = skinny_counters((uint32_t)atoms, &counters);
+  cudaError_t e = ring_slots((uint32_t)atoms, &counters);
   if (e != cudaSuccess) return e;
   CUtensorMap tX, tF;
   if (!make_map(&tX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2,
