@@ -258,10 +258,11 @@ def time_steps(torch, dist, run, h0s, K, W, stream, e2e=None, nvtx=False):
     return e0.elapsed_time(e1) / 1e3
 
 
-def gemm_roofline(ops, torch, res, cfg, peak_bf16):
-    """The dominant kernel alone: the NF4 dequant GEMM (forward and input-
-    gradient directions) on the workload's seven linear shapes, weights read
-    from the resident image (different layers back to back: no L2 reuse)."""
+def roofline_calls(ops, torch, res, cfg):
+    """The dominant kernel's launches: the NF4 dequant GEMM (forward and
+    input-gradient directions) on the workload's seven linear shapes of eight
+    layers, weights read from the resident image (different layers back to
+    back: no L2 reuse)."""
     M = cfg.M
     st = torch.cuda.current_stream()
     shapes = cfg.shapes()
@@ -282,6 +283,14 @@ def gemm_roofline(ops, torch, res, cfg, peak_bf16):
                                  device=st.device)
                 calls.append((W, act, tw, out, ws))
                 flops += 2 * M * N * K
+    return calls, flops
+
+
+def gemm_roofline(ops, torch, res, cfg, peak_bf16):
+    """Average launch of the dominant kernel (roofline_calls), timed with CUDA
+    events on the launching stream."""
+    st = torch.cuda.current_stream()
+    calls, flops = roofline_calls(ops, torch, res, cfg)
     for c in calls:
         ops.nf4_matmul(c[0], c[1], c[2], out=c[3], workspace=c[4])
     torch.cuda.synchronize()
@@ -300,6 +309,23 @@ def gemm_roofline(ops, torch, res, cfg, peak_bf16):
     return dict(bound="tensor", achieved=achieved, peak=peak_bf16, unit="TFLOP/s",
                 frac=achieved / peak_bf16, launches=launches,
                 avg_launch_us=1e6 * t / launches, flops_per_launch=flops / len(calls))
+
+
+def profile_roofline(torch):
+    """The roofline launches on an 8-layer resident image (a few GB): one warm
+    pass, then one pass to capture (skip the first len(calls) launches)."""
+    from weight_streaming_nf4_gb300 import ops
+    from weight_streaming_nf4_gb300.stack import StackRun
+    dev = torch.device("cuda:0")
+    cfg = ops.StackCfg(**dict(SHAPE_32B, n_layers=8))
+    res, _ = make_runs(ops, StackRun, torch, cfg, dev, streamed=False)
+    calls, flops = roofline_calls(ops, torch, res, cfg)
+    for _ in range(2):
+        for c in calls:
+            ops.nf4_matmul(c[0], c[1], c[2], out=c[3], workspace=c[4])
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    print(json.dumps({"profile_roofline": len(calls), "flops_per_launch": flops / len(calls)}))
 
 
 def linear_7b(ops, torch, dev, M, reps=5):
@@ -416,6 +442,9 @@ def main():
     ap.add_argument("--profile-step", action="store_true",
                     help="only the resident run: W warm-up steps and one step inside the NVTX "
                          "range 'timed'; for an ncu launch list of one step")
+    ap.add_argument("--profile-roofline", action="store_true",
+                    help="only launch the roofline's dequant GEMM calls twice on an 8-layer "
+                         "image; for an ncu capture of their DRAM traffic")
     ap.add_argument("--profile-gemm", choices=["gate", "down", "o"], default=None,
                     help="only launch the dequant GEMM (forward + input gradient) twice on one "
                          "32B linear shape at M=512; for an ncu capture of that kernel")
@@ -431,6 +460,9 @@ def main():
     import torch
     if args.profile_gemm:
         profile_gemm(torch, args.profile_gemm)
+        return
+    if args.profile_roofline:
+        profile_roofline(torch)
         return
     dist = None
     if world > 1:
@@ -510,7 +542,8 @@ def main():
         peak_res = torch.cuda.max_memory_allocated(dev)
         extra["roofline"] = {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac",
                                                    "traffic")}
-        extra["roofline"]["kernel"] = "k_nf4_gemm (fwd + input-gradient), 32B shapes, M=512"
+        extra["roofline"]["kernel"] = ("k_nf4_gemm (fwd + input-gradient), the 7 linear shapes "
+                                       "of 8 layers, M=512")
         extra["roofline"]["peak_kind"] = ("bf16 dense burst, " + pk["src"])
         extra["roofline"]["avg_launch_us"] = roof["avg_launch_us"]
         t_copy = h2d_w / (link * 1e9)
