@@ -124,7 +124,7 @@ ws_status ws_device_error(uint32_t* flags);
  * (host-side counter; copies are not counted). */
 uint64_t ws_kernel_launches(void);
 
-/* ---- a0: NF4 quantisation ------------------------------------------------- */
+/* ---- NF4 quantisation ------------------------------------------------------ */
 /* Quantises a bf16 weight W [N, K] (device) into NF4 codes [N, K/2] and
  * block-major absmax [K/64, N] (device, caller-allocated).
  * Per 64-block: absmax = max |w| (fp32); v = w / absmax as an IEEE fp32
@@ -138,7 +138,7 @@ uint64_t ws_kernel_launches(void);
 ws_status ws_quantize_nf4(const uint16_t* W, int64_t N, int64_t K, uint8_t* codes,
                           float* absmax, ws_stream_t stream);
 
-/* ---- a1 + a2: LoRA linear forward ----------------------------------------- */
+/* ---- LoRA linear forward ------------------------------------------------- */
 /* Workspace (device bytes) needed by ws_lora_linear_fwd / _bwd for a shape. */
 ws_status ws_lora_workspace_size(ws_lora_shape sh, size_t* bytes);
 
@@ -159,7 +159,7 @@ ws_status ws_lora_linear_fwd(const ws_nf4* W, const uint16_t* x, const float* A,
                              uint16_t* y, float* U_saved, uint32_t* mask_saved,
                              void* workspace, size_t ws_bytes, ws_stream_t stream);
 
-/* ---- a3 + a4 + a5: LoRA linear backward ------------------------------------ */
+/* ---- LoRA linear backward ------------------------------------------------ */
 /* Given dY [M,N] bf16 computes
  *   G  = dY B                              (fp32, internal)
  *   dB = s dY^T U_saved                    [N, r] fp32 (overwritten)
@@ -274,7 +274,7 @@ ws_status ws_stack_saved_offset(const ws_stack_cfg* cfg, int32_t field, int32_t 
 ws_status ws_stack_param_offset(const ws_stack_cfg* cfg, int32_t layer, int32_t lin,
                                 int64_t* off_A, int64_t* off_B);
 
-/* a6: forward of layers [first_layer, first_layer + n_layers) whose NF4
+/* Forward of layers [first_layer, first_layer + n_layers) whose NF4
  * weights are the block image at `block_weights` (device).  h_in / h_out
  * [M, H] fp32 (device; may not alias).  params: device LoRA parameters.
  * saved: device area of n_layers * saved_bytes_layer that receives every
@@ -285,7 +285,7 @@ ws_status ws_block_forward(const ws_stack_cfg* cfg, const void* block_weights,
                            uint32_t step, const float* h_in, float* h_out, void* saved,
                            void* workspace, size_t ws_bytes, ws_stream_t stream);
 
-/* a8: backward of the same layers.  If `saved` is NULL the block's forward is
+/* Backward of the same layers.  If `saved` is NULL the block's forward is
  * first recomputed from the boundary activation h_in (same kernels, same
  * Philox keys, hence bit-identical intermediates) into the workspace; if
  * `saved` is the area ws_block_forward filled, it is used directly
@@ -300,7 +300,7 @@ ws_status ws_block_backward_recompute(const ws_stack_cfg* cfg, const void* block
                                       float* grads, void* workspace, size_t ws_bytes,
                                       ws_stream_t stream);
 
-/* a7: copy one block (bytes) from pinned host memory to a device window slot
+/* Copy one block (bytes) from pinned host memory to a device window slot
  * on `copy_stream`.  If wait_event is not NULL the copy first waits for it
  * (the slot's previous user is done); if done_event is not NULL it is
  * recorded after the copy.  A pageable source gives WS_ERR_NOT_PINNED. */

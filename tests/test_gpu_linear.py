@@ -1,4 +1,4 @@
-"""GPU parity of the NF4-LoRA linear (a0-a5) against the CPU oracle, through
+"""GPU parity of the NF4-LoRA linear (quantiser, masks, forward, backward) against the CPU oracle, through
 the C ABI.  Integer work (NF4 codes, absmax, dropout bits) must be bit-exact;
 floating outputs (y, dX, dA, dB) within the normwise tolerance TOL of the
 fp64 oracle.

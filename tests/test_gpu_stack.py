@@ -1,4 +1,4 @@
-"""GPU tests of the block engine (a6-a9): block forward / backward with
+"""GPU tests of the block engine: block forward / backward with
 recompute, the streamed training step, and the pinned-host block copy.
 
 - The recompute (forward rerun from the block-boundary activation with the

@@ -19,7 +19,7 @@ __constant__ float c_levels_q[16] = {-1.0f,    -0.6962f, -0.5251f, -0.3949f, -0.
                                      -0.0911f, 0.0f,     0.0796f,  0.1609f,  0.2461f,  0.3379f,
                                      0.4407f,  0.5626f,  0.7230f,  1.0f};
 
-// ------------------------------------------------------------------------ a0: quantise
+// ------------------------------------------------------------------------ NF4 quantisation
 // One warp per 64-weight block; lane i handles weights 2i and 2i+1 and
 // writes code byte i.  The block maximum is a max-reduction (exact in any
 // order); v = w / absmax is an IEEE division; the code counts the midpoints

@@ -1,7 +1,7 @@
 // nf4_gemm.cu -- the NF4 dequant GEMM on the 5th-generation tensor cores.
 //
-// Forward (a2):  y[M,N]  = x[M,K] . W'[N,K]^T  (+ s U B^T as an extra step)
-// Backward (a4): dX[M,K] = dY[M,N] . W'[N,K]   (+ s (G A) . mask)
+// Forward:  y[M,N]  = x[M,K] . W'[N,K]^T  (+ s U B^T as an extra step)
+// Backward: dX[M,K] = dY[M,N] . W'[N,K]   (+ s (G A) . mask)
 //
 // W' = bf16_RN(c[code] * absmax) is never materialised in global memory:
 // packed 4-bit codes and the block absmax are staged into shared memory by
