@@ -531,7 +531,9 @@ def main():
     e2e_val = world * flops * args.steps / t_stm / 1e12
     nb = cfg.n_layers // BLOCK
     bb = res.sizes["block_bytes"]
-    h2d_w = (2 * nb - 2) * bb  # the two turnaround blocks are not reloaded
+    # the two turnaround blocks are not reloaded, and a replayed step starts from
+    # the window the previous step left (blocks 0 and 1)
+    h2d_w = (2 * nb - 4) * bb
     h2d_bytes = h2d_w + M * H * 4
 
     extra = {}

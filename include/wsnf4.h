@@ -349,6 +349,10 @@ ws_status ws_stack_train_step(const ws_stack_cfg* cfg, int32_t block_layers, int
  * the workspace, copying h0 into boundary block 0) into one graph: every
  * block's kernels, the window copies on copy_stream (forked from and joined
  * back into `compute` inside the graph), the loss and the Adam step.
+ * Streamed: a second capture starts from the window the previous step left
+ * (blocks 0 and 1 in slots 0 and 1) and skips their two copies; the first
+ * ws_stack_graph_step replays the full capture, every later one the second,
+ * so the window must not be written between steps of one graph.
  * Kernels that depend on the step (dropout keys, Adam bias corrections) read
  * it from that device word, so replays with different steps need no
  * re-capture.  The graph keeps the pointers of *buf, the config, lr and the

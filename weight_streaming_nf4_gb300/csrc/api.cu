@@ -345,9 +345,11 @@ ws_status check_step(const ws_stack_cfg* cfg, int32_t block_layers, int32_t stre
 // the forward/backward turnaround) is not copied again.  The copy stream is
 // forked from and joined back into the compute stream, so the whole step
 // can be captured as one graph.
+// warm: the window already holds blocks 0 and 1 (slots 0 and 1), as the
+// previous step's backward left it; their copies are skipped.
 ws_status step_body(const ws_stack_cfg& cfg, int block_layers, bool streamed,
                     const ws_stack_buffers& buf, float lr, cudaStream_t cs, cudaStream_t ps,
-                    StepEvents& ev) {
+                    StepEvents& ev, bool warm = false) {
   const int nb = cfg.n_layers / block_layers;
   const size_t bbytes = stack_block_bytes(cfg, block_layers);
   const size_t slayer = stack_saved_layer(cfg);
@@ -357,6 +359,11 @@ ws_status step_body(const ws_stack_cfg& cfg, int block_layers, bool streamed,
   const uint32_t* stepw = stack_step_word(cfg, block_layers, buf.workspace);
   int slot_block[2] = {-1, -1};
   bool slot_used[2] = {false, false};
+  bool slot_copied[2] = {false, false};  // a copy into the slot was issued in this step
+  if (streamed && warm && nb >= 2) {
+    slot_block[0] = 0;
+    slot_block[1] = 1;
+  }
   const uint8_t* host = static_cast<const uint8_t*>(buf.host_weights);
   uint8_t* window = static_cast<uint8_t*>(buf.window);
 #define WS_STEP_TRY(x)                          \
@@ -370,8 +377,16 @@ ws_status step_body(const ws_stack_cfg& cfg, int block_layers, bool streamed,
                                       bbytes, (ws_stream_t)ps,
                                       slot_used[sl] ? (ws_event_t)ev.freed[sl] : nullptr,
                                       (ws_event_t)ev.loaded[sl]);
-    if (r == WS_OK) slot_block[sl] = blk;
+    if (r == WS_OK) {
+      slot_block[sl] = blk;
+      slot_copied[sl] = true;
+    }
     return r;
+  };
+  // the compute stream waits for a slot's copy only if one was issued in this step
+  auto wait_loaded = [&](int blk) -> cudaError_t {
+    const int sl = blk % 2;
+    return slot_copied[sl] ? cudaStreamWaitEvent(cs, ev.loaded[sl], 0) : cudaSuccess;
   };
   auto block_ptr = [&](int blk) -> const void* {
     if (streamed) return window + (size_t)(blk % 2) * bbytes;
@@ -386,7 +401,7 @@ ws_status step_body(const ws_stack_cfg& cfg, int block_layers, bool streamed,
   if (streamed && (rc = ensure(0)) != WS_OK) return rc;
   for (int b = 0; b < nb; ++b) {
     if (streamed && b + 1 < nb && (rc = ensure(b + 1)) != WS_OK) return rc;
-    if (streamed) WS_STEP_TRY(cudaStreamWaitEvent(cs, ev.loaded[b % 2], 0));
+    if (streamed) WS_STEP_TRY(wait_loaded(b));
     void* sv = streamed ? nullptr : static_cast<uint8_t*>(buf.saved) + (size_t)b * block_layers * slayer;
     WS_STEP_TRY(block_forward(cfg, block_layers, block_ptr(b), b * block_layers, block_layers,
                               buf.params, 0u, stepw, bnd + (size_t)b * MH, bnd + (size_t)(b + 1) * MH,
@@ -403,7 +418,7 @@ ws_status step_body(const ws_stack_cfg& cfg, int block_layers, bool streamed,
     if (streamed) {
       if ((rc = ensure(b)) != WS_OK) return rc;
       if (b - 1 >= 0 && (rc = ensure(b - 1)) != WS_OK) return rc;
-      WS_STEP_TRY(cudaStreamWaitEvent(cs, ev.loaded[b % 2], 0));
+      WS_STEP_TRY(wait_loaded(b));
     }
     const void* sv =
         streamed ? nullptr : static_cast<uint8_t*>(buf.saved) + (size_t)b * block_layers * slayer;
@@ -437,13 +452,19 @@ ws_status step_prologue(const ws_stack_cfg& cfg, int block_layers, const ws_stac
 
 }  // namespace
 
+// Two captures of the step: "cold" copies every block it needs; "warm"
+// (streamed only) starts from the window the previous step left behind
+// (blocks 0 and 1 in slots 0 and 1) and skips those two copies.  The first
+// replay is cold, every later one warm.
 struct ws_step_graph {
   ws_stack_cfg cfg;
   int32_t block_layers;
   ws_stack_buffers buf;
-  StepEvents ev;
-  cudaGraph_t graph = nullptr;
-  cudaGraphExec_t exec = nullptr;
+  StepEvents ev[2];
+  cudaGraph_t graph[2] = {nullptr, nullptr};
+  cudaGraphExec_t exec[2] = {nullptr, nullptr};
+  bool warm_ok = false;   // a warm capture exists
+  bool window_warm = false;
 };
 
 extern "C" {
@@ -480,22 +501,24 @@ ws_status ws_stack_graph_create(const ws_stack_cfg* cfg, int32_t block_layers, i
   g->block_layers = block_layers;
   g->buf = *buf;
   const cudaStream_t cs = (cudaStream_t)compute;
-  if (g->ev.create() != cudaSuccess) {
-    g->ev.destroy();
-    delete g;
-    return WS_ERR_CUDA;
+  g->warm_ok = streamed != 0 && cfg->n_layers / block_layers >= 2;
+  for (int v = 0; v < (g->warm_ok ? 2 : 1) && s == WS_OK; ++v) {
+    if (g->ev[v].create() != cudaSuccess) {
+      s = WS_ERR_CUDA;
+      break;
+    }
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+      s = WS_ERR_CUDA;
+      break;
+    }
+    s = step_body(*cfg, block_layers, streamed != 0, *buf, lr, cs, (cudaStream_t)copy_stream,
+                  g->ev[v], v == 1);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ec = cudaStreamEndCapture(cs, &graph);
+    g->graph[v] = graph;
+    if (s == WS_OK && ec != cudaSuccess) s = WS_ERR_CUDA;
+    if (s == WS_OK && cudaGraphInstantiate(&g->exec[v], graph, 0) != cudaSuccess) s = WS_ERR_CUDA;
   }
-  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
-    g->ev.destroy();
-    delete g;
-    return WS_ERR_CUDA;
-  }
-  s = step_body(*cfg, block_layers, streamed != 0, *buf, lr, cs, (cudaStream_t)copy_stream, g->ev);
-  cudaGraph_t graph = nullptr;
-  const cudaError_t ec = cudaStreamEndCapture(cs, &graph);
-  if (s == WS_OK && ec != cudaSuccess) s = WS_ERR_CUDA;
-  if (s == WS_OK && cudaGraphInstantiate(&g->exec, graph, 0) != cudaSuccess) s = WS_ERR_CUDA;
-  g->graph = graph;
   if (s != WS_OK) {
     cudaGetLastError();
     ws_stack_graph_destroy(g);
@@ -511,14 +534,19 @@ ws_status ws_stack_graph_step(ws_step_graph* g, uint32_t step, const float* h0,
   const cudaStream_t cs = (cudaStream_t)compute;
   ws_status s = step_prologue(g->cfg, g->block_layers, g->buf, step, h0, cs);
   if (s != WS_OK) return s;
-  return cudaGraphLaunch(g->exec, cs) == cudaSuccess ? WS_OK : WS_ERR_CUDA;
+  const int v = (g->warm_ok && g->window_warm) ? 1 : 0;
+  if (cudaGraphLaunch(g->exec[v], cs) != cudaSuccess) return WS_ERR_CUDA;
+  g->window_warm = g->warm_ok;
+  return WS_OK;
 }
 
 ws_status ws_stack_graph_destroy(ws_step_graph* g) {
   if (!g) return WS_ERR_INVALID;
-  if (g->exec) cudaGraphExecDestroy(g->exec);
-  if (g->graph) cudaGraphDestroy(g->graph);
-  g->ev.destroy();
+  for (int v = 0; v < 2; ++v) {
+    if (g->exec[v]) cudaGraphExecDestroy(g->exec[v]);
+    if (g->graph[v]) cudaGraphDestroy(g->graph[v]);
+    g->ev[v].destroy();
+  }
   delete g;
   return WS_OK;
 }
