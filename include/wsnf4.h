@@ -178,7 +178,7 @@ ws_status ws_lora_linear_bwd(const ws_nf4* W, const uint16_t* x, const float* A,
                              void* workspace, size_t ws_bytes, ws_stream_t stream);
 
 /* ---- the frozen NF4 product alone ---------------------------------------------- */
-/* The dequant GEMM of a2 / a4 without adapter or dropout (a frozen NF4
+/* The dequant GEMM of the LoRA linear without adapter or dropout (a frozen NF4
  * linear):
  *   transpose_w == 0:  out[M,N] = act[M,K] W'^T   (forward)
  *   transpose_w != 0:  out[M,K] = act[M,N] W'     (input gradient)

@@ -1,11 +1,8 @@
-// lora_small.cu -- the HBM-bound pieces of one NF4-LoRA linear and the
-// orchestration of its forward and backward:
-//   a0  NF4 quantisation of a bf16 weight
-//   a1  dropout bits (Philox4x32-10) + LoRA down projection U = (m.x) A^T
-//   a3  G = dY B and dB = s dY^T U
-//   a5  dA = s G^T (m.x)
-// Every reduction runs in a fixed order (per-lane sequential sums, a fixed
-// butterfly across lanes, fixed-order sums across row chunks): no atomics.
+// lora_small.cu -- the smaller pieces of one NF4-LoRA linear and the
+// orchestration of its forward and backward: NF4 quantisation of a bf16
+// weight, dropout-mask regeneration, the workspace layout, and the order of
+// the kernels (the tensor-core kernels live in nf4_gemm.cu).  Every
+// reduction runs in a fixed order: no atomics on data.
 #include <math.h>
 
 #include "common.cuh"

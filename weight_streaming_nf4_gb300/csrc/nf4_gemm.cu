@@ -1556,10 +1556,11 @@ int64_t pair_capacity(bool bwd, int bn) {
 int64_t grid_units(const GemmPlan& p, bool has_lora) {
   const int64_t S = (int64_t)p.nk + (has_lora ? 1 : 0);
   const int64_t I = (int64_t)p.mtiles * p.ntiles * S;
-  // at least kMinSteps iterations per unit, and at least a third of a tile,
-  // so a tile is cut into at most about four pieces (the finisher adds the
-  // pieces one after the other)
+  // at least kMinSteps iterations per unit, and at least a third of a short
+  // tile, so a short tile is cut into at most about four pieces (the
+  // finisher adds the pieces one after the other); long tiles fill the GPU
   int64_t min_steps = S / 3 + 2;
+  if (min_steps > 64) min_steps = 64;
   if (min_steps < kMinSteps) min_steps = kMinSteps;
   int64_t G = (I + min_steps - 1) / min_steps;
   const int64_t cap = p.pair ? pair_capacity(p.bwd, p.bn) : device_sm_count();
