@@ -33,8 +33,10 @@
 // step whose A operand is [U_hi | U_lo | U_hi | 0] and whose B operand is
 // [Bs_hi | Bs_hi | Bs_lo | 0] (Bs = s B, bf16 high/low splits), i.e.
 // U Bs^T to about 16 significant bits.  The backward computes s G A the same
-// way into a second TMEM accumulator and adds it under the dropout mask in
-// the epilogue.
+// way but as each tile's FIRST step: the epilogue warps then apply the
+// dropout mask to the accumulator in TMEM (load, zero the dropped
+// elements, store back) before the main steps accumulate on top, so one
+// accumulator serves both terms.
 #define WS_GEMM_TU 1
 #include <cstdlib>
 #include <mutex>
@@ -109,8 +111,8 @@ struct Cfg {
   static constexpr int STAGES_RAW =
       (int)((220u * 1024u - BSTAGES * B_BYTES - CSTAGES * CODE_BYTES - 1024u) / A_BYTES);
   static constexpr int STAGES = STAGES_RAW > WS_GEMM_STAGES_MAX ? WS_GEMM_STAGES_MAX : STAGES_RAW;
-  // one accumulator set: D (and for the backward the LoRA term D2)
-  static constexpr uint32_t ACC_COLS = (BWD ? 2u : 1u) * UM * BN;
+  // one accumulator set
+  static constexpr uint32_t ACC_COLS = UM * BN;
   // double-buffer the accumulator when TMEM has room, so the epilogue of
   // one tile overlaps the main loop of the next
   static constexpr int ACC_BUFS = 2 * ACC_COLS <= 512 ? 2 : 1;
@@ -124,7 +126,7 @@ struct Cfg {
   static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr uint32_t OFF_CODE = OFF_B + BSTAGES * B_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_CODE + CSTAGES * CODE_BYTES;
-  static constexpr uint32_t N_BARS = 2 * STAGES + 2 * BSTAGES + 2 * ACC_BUFS + 1;
+  static constexpr uint32_t N_BARS = 2 * STAGES + 2 * BSTAGES + 2 * ACC_BUFS + 3;
   static constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
   static_assert(STAGES >= 2, "pipeline needs two stages");
@@ -278,7 +280,7 @@ WS_DEVINL void fetch_codes(uint32_t slot, const GemmArgs& g, int i, int n0, int 
     constexpr int SEGS = D::COLS / (2 * D::VB);
 #pragma unroll
     for (int it = 0; it < D::NV; ++it) {
-      const int item = t + it * kDqThreads;
+      const int item = t * D::NV + it;  // a warp's items cover whole 8-row groups
       const int c = item / SEGS, seg = item % SEGS;
       const int64_t r = (int64_t)i * 64 + c;
       const int64_t col = (int64_t)n0 + c0 + seg * 2 * D::VB;
@@ -343,7 +345,7 @@ WS_DEVINL void dequant_bwd(const Frag& f, uint8_t* Bt, int rank, int t) {
   constexpr int SEGS = D::COLS / (2 * D::VB);
 #pragma unroll
   for (int it = 0; it < D::NV; ++it) {
-    const int item = t + it * kDqThreads;
+    const int item = t * D::NV + it;
     const int c = item / SEGS, seg = item % SEGS;
     const int j0 = (PAIR ? rank * D::COLS : 0) + seg * 2 * D::VB;  // first tile column
     const Nf4Table tb = make_table(f.a[it]);
@@ -441,6 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* accfull = bempty + BSTAGES;
   uint64_t* accempty = accfull + NACC;
   uint64_t* drain = accempty + NACC;
+  uint64_t* lora_done = drain + 1;    // backward: the tile's LoRA step has completed
+  uint64_t* lora_masked = drain + 2;  // backward: ... and the epilogue masked it
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   uint32_t* tmem_slot = misc;
   volatile uint32_t* abort_flag = misc + 1;
@@ -452,6 +456,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rank = PAIR ? (int)(cluster_ctarank() & 1u) : 0;
   // ---- static stream-K schedule over units (CTAs, or pairs of CTAs)
   const int S = args.nk_total + (args.has_lora ? 1 : 0);  // steps per tile
+  // the LoRA step: last in the forward, first in the backward (where it is
+  // masked before the main steps accumulate on top); kc = contraction step
+  const bool lora_first = BWD && args.has_lora;
+  auto is_lora_step = [&](int i) {
+    return args.has_lora && (lora_first ? i == 0 : i == args.nk_total);
+  };
+  auto kstep = [&](int i) { return lora_first ? i - 1 : i; };
   const int64_t T = (int64_t)args.mtiles * args.ntiles;
   const int64_t I = T * S;
   const int64_t U = PAIR ? gridDim.x / 2 : gridDim.x;
@@ -482,6 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&accempty[a], kEpiWarps);
     }
     mbar_init(drain, 1);
+    mbar_init(lora_done, 1);
+    mbar_init(lora_masked, kEpiWarps);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -513,8 +526,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int m0 = ps.mt * UROWS + rank * C::BM;
           mbar_arrive_expect_tx(&full[s], C::A_BYTES);
-          if (!(args.has_lora && ps.i == args.nk_total))
-            tma_load_2d(sA + s * C::A_BYTES, &tmA, &full[s], ps.i * 64, m0);
+          if (!is_lora_step(ps.i))
+            tma_load_2d(sA + s * C::A_BYTES, &tmA, &full[s], kstep(ps.i) * 64, m0);
           else
             tma_load_2d(sA + s * C::A_BYTES, &tmL, &full[s], 0, m0);
           issued = q + 1;
@@ -538,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t seg = 0;
         int ms_s = 0, ms_b = 0;
         uint32_t ms_ph = 0, ms_bph = 0;
+        uint32_t lora_ph = 0;
         for (int64_t p = pb; p < pe && !*abort_flag; ++seg) {
           const int64_t t = p / S;
           const int64_t seg_end = min(pe, (t + 1) * S);
@@ -569,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            const bool is_lora = args.has_lora && i == args.nk_total;
+            const bool is_lora = is_lora_step(i);
             const uint32_t a_base = smem_u32(sA + s * C::A_BYTES);
             const uint32_t b_base = smem_u32(sB + b * C::B_BYTES);
 #pragma unroll
@@ -582,20 +596,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int u = 0; u < UM; ++u) {
                 const uint64_t adesc = smem_desc_sw128(a_base + u * 16384 + kk * 32, 16, 1024);
-                uint32_t d = dbase + (uint32_t)(u * BN);
-                uint32_t acc;
-                if (BWD && is_lora) {
-                  d += (uint32_t)(UM * BN);
-                  acc = kk > 0 ? 1u : 0u;
-                } else {
-                  acc = (p2 > p || kk > 0) ? 1u : 0u;
-                }
+                const uint32_t d = dbase + (uint32_t)(u * BN);
+                const uint32_t acc = (p2 > p || kk > 0) ? 1u : 0u;
                 tc_mma_f16(d, adesc, bdesc, is_lora ? idesc_kmaj : idesc_main, acc);
               }
             }
             tc_commit(&empty[s]);
             if constexpr (PAIR) tc_commit_multicast(&bempty[b], (uint16_t)0x3);
             else tc_commit(&bempty[b]);
+            if (BWD && is_lora) {
+              // the epilogue masks s G A in TMEM before the main steps add on top
+              tc_commit(lora_done);
+              if (!mbar_wait(lora_masked, lora_ph, DERR_TIMEOUT_ACC)) {
+                *abort_flag = 1u;
+                break;
+              }
+              lora_ph ^= 1u;
+              tc_fence_after();
+            }
           }
           tc_commit(&accfull[a]);
           p = seg_end;
@@ -620,9 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       Pos pf = pos0;  // position of the next fetch
       int64_t fq = 0;
       auto fetch = [&]() {
-        if (fq < n_it && !(args.has_lora && pf.i == args.nk_total))
-          fetch_codes<BWD, BN, PAIR>(smem_u32(ring + (fq % CS) * C::CODE_BYTES), args, pf.i,
-                                     pf.nt * BN, rank, t_idx);
+        if (fq < n_it && !is_lora_step(pf.i))
+          fetch_codes<BWD, BN, PAIR>(smem_u32(ring + (fq % CS) * C::CODE_BYTES), args,
+                                     kstep(pf.i), pf.nt * BN, rank, t_idx);
         cp_async_commit();
         pf.next(S, args.mtiles);
         ++fq;
@@ -642,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         uint8_t* Bt = sB + b * C::B_BYTES;
-        const bool lora_step = args.has_lora && pc.i == args.nk_total;
+        const bool lora_step = is_lora_step(pc.i);
         if (!lora_step) {
           if (!BWD) dequant_fwd<BN, PAIR>(cur, Bt, rank, t_idx);
           else dequant_bwd<BN, PAIR>(cur, Bt, rank, t_idx);
@@ -661,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int dw = warp - 2;
             const uint32_t off =
                 (BWD && !lora_step)
-                    ? (uint32_t)(dw * (int)C::MN_SBO + rank * 1024)
+                    ? (uint32_t)(dw * (int)C::MN_SBO + rank * (BN / 128) * 1024)
                     : (uint32_t)((rank * (BN / 2) + dw * (BN / 16)) * 128);
             mbar_arrive_expect_tx(&bfull[b], WB);
             bulk_copy_to_peer(mapa_shared(smem_u32(Bt + off), peer), Bt + off, WB,
@@ -699,6 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // CTA holding this CTA's rows of the tile in unit u
       auto cta_of = [&](int64_t u) -> int64_t { return PAIR ? 2 * u + rank : u; };
       int64_t seg = 0;
+      uint32_t lora_ph = 0;
       for (int64_t p = pb; p < pe; ++seg) {
         const int64_t t = p / S;
         const int64_t i0 = p % S;
@@ -706,6 +725,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t kb = seg_end - t * S;
         const int a = (int)(seg % NACC);
         const uint32_t aph = (uint32_t)(seg / NACC) & 1u;
+        if (lora_first && i0 == 0) {
+          // the tile's first step was s G A: zero its dropped elements in
+          // TMEM, then let the main steps accumulate on top
+          const bool lok = !*abort_flag && mbar_wait_backoff(lora_done, lora_ph, DERR_TIMEOUT_ACC);
+          lora_ph ^= 1u;
+          tc_fence_after();
+          const int64_t lm0 = (t % args.mtiles) * UROWS + rank * C::BM;
+          const int64_t ln0 = (t / args.mtiles) * BN;
+          const uint32_t lbase = tmem + (uint32_t)(a * C::ACC_COLS);
+#pragma unroll 1
+          for (int u = 0; u < UM; ++u) {
+            const int64_t m = lm0 + u * 128 + r;
+#pragma unroll 1
+            for (int cc = half * (BN / 2); cc < (half + 1) * (BN / 2); cc += 16) {
+              const int64_t n = ln0 + cc;
+              if (n >= args.Nout) break;  // warp-uniform
+              const uint32_t taddr = lbase + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(u * BN + cc);
+              uint32_t v[16];
+              tmem_ld_32x32b_x16(taddr, v);
+              const uint32_t bits =
+                  (lok && m < args.M) ? args.mask[(m * args.Nout + n) >> 5] >> (n & 31) : 0u;
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v[e] = ((bits >> e) & 1u) ? v[e] : 0u;
+              tmem_st_32x32b_x16(taddr, v);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(lora_masked);
+        }
         const bool ok = !*abort_flag && mbar_wait_backoff(&accfull[a], aph, DERR_TIMEOUT_ACC);
         tc_fence_after();
         const int64_t m0 = (t % args.mtiles) * UROWS + rank * C::BM;
@@ -714,9 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the tile's first steps with the rest held by later units: finish it here
         const bool finisher = (i0 == 0 && kb < S);
         const bool writer = !whole && !finisher;  // a later piece: hand it over
-        const bool lora_in = args.has_lora && kb == S;
-        // a backward segment made of the LoRA step alone never wrote D
-        const bool main_in = !BWD || i0 < args.nk_total;
+        (void)kb;
         float* part = args.partial + (int64_t)blockIdx.x * C::TILE_FLOATS;
         int64_t u_last = unit;
         if (finisher) {
@@ -760,8 +809,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc[16];
             const uint32_t taddr = dbase + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(u * BN + cc);
             tmem_ld_32x32b_x16(taddr, acc);
-            uint32_t lacc[16];
-            if (BWD && lora_in) tmem_ld_32x32b_x16(taddr + (uint32_t)(UM * BN), lacc);
             // the first later piece's values load while the TMEM read is in flight
             float4 pv[4];
             const bool piece = row_ok && !writer && u_last > unit;
@@ -775,13 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!row_ok) continue;
             float v[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = main_in ? __uint_as_float(acc[e]) : 0.0f;
-            if (BWD && lora_in) {
-              const uint32_t bits = args.mask[(m * args.Nout + n) >> 5] >> (n & 31);
-#pragma unroll
-              for (int e = 0; e < 16; ++e)
-                if ((bits >> e) & 1u) v[e] += __uint_as_float(lacc[e]);
-            }
+            for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(acc[e]);
             if (writer) {
               float4* dst = reinterpret_cast<float4*>(part + (int64_t)row * BN + cc);
 #pragma unroll
@@ -1549,7 +1590,7 @@ int device_sm_count() {
 }
 
 int64_t pair_capacity(bool bwd, int bn) {
-  if (bwd) return bn == 128 ? pair_capacity_of<true, 128>() : 0;
+  if (bwd) return bn == 256 ? pair_capacity_of<true, 256>() : pair_capacity_of<true, 128>();
   return bn == 256 ? pair_capacity_of<false, 256>() : pair_capacity_of<false, 128>();
 }
 
@@ -1581,11 +1622,11 @@ GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc) {
   // both (one dequantisation per 512 activation rows).
   p.pair = M > 256 && pair_capacity(bwd, 128) > 0;
   const int64_t urows = 128 * p.um * (p.pair ? 2 : 1);
-  if (!bwd && p.um == 2) {
-    // A 256-wide forward tile reads less shared memory per flop (256-wide
-    // MMAs) but has a single accumulator (no epilogue overlap): worth it
-    // when each unit's stream-K range stays long (>= 64 steps).
-    const int64_t units = p.pair ? pair_capacity(false, 256) : device_sm_count();
+  if (p.um == 2 && (!bwd || p.pair)) {
+    // A 256-wide tile reads less shared memory per flop (256-wide MMAs) but
+    // has a single accumulator (no epilogue overlap): worth it when each
+    // unit's stream-K range stays long (>= 64 steps).
+    const int64_t units = p.pair ? pair_capacity(bwd, 256) : device_sm_count();
     const int64_t mt = (M + urows - 1) / urows, nt = (Nout + 255) / 256;
     if (units > 0 && mt * nt * (Kc / 64 + 1) >= 64 * units) p.bn = 256;
   }
@@ -1658,7 +1699,10 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
     if (p.um == 2) return launch_cfg<false, 2, 128, false>(p, a, tA, tL, st);
     return launch_cfg<false, 1, 128, false>(p, a, tA, tL, st);
   }
-  if (p.pair) return launch_cfg<true, 2, 128, true>(p, a, tA, tL, st);
+  if (p.pair) {
+    if (p.bn == 256) return launch_cfg<true, 2, 256, true>(p, a, tA, tL, st);
+    return launch_cfg<true, 2, 128, true>(p, a, tA, tL, st);
+  }
   if (p.um == 2) return launch_cfg<true, 2, 128, false>(p, a, tA, tL, st);
   return launch_cfg<true, 1, 128, false>(p, a, tA, tL, st);
 }

@@ -235,14 +235,9 @@ WS_DEVINL void adam1(float& p, float g, float& m, float& v, float beta1, float b
 __global__ void k_adam(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
                        float* __restrict__ v, int64_t n, const uint32_t* __restrict__ step_dev,
                        float lr) {
-  __shared__ float s_coef[2];
-  if (threadIdx.x == 0) {
-    const double t = (double)(*step_dev) + 1.0;
-    s_coef[0] = (float)((double)lr / (1.0 - pow(0.9, t)));
-    s_coef[1] = (float)sqrt(1.0 - pow(0.999, t));
-  }
-  __syncthreads();
-  const float step_size = s_coef[0], bc2_sqrt = s_coef[1];
+  // bias corrections of this step, computed once by k_set_step
+  const float step_size = lr * __uint_as_float(__ldg(step_dev + 2));
+  const float bc2_sqrt = __uint_as_float(__ldg(step_dev + 3));
   const float beta1 = 0.9f, beta2 = 0.999f, eps = 1e-8f;
   const int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i4 * 4 >= n) return;
@@ -259,7 +254,14 @@ __global__ void k_adam(float* __restrict__ p, const float* __restrict__ g, float
   reinterpret_cast<float4*>(v)[i4] = vv;
 }
 
-__global__ void k_set_step(uint32_t* step_dev, uint32_t step) { *step_dev = step; }
+// The step word and, after it, Adam's bias corrections for step t = step + 1:
+// 1 / (1 - 0.9^t) and sqrt(1 - 0.999^t), computed in double, stored as fp32.
+__global__ void k_set_step(uint32_t* step_dev, uint32_t step) {
+  const double t = (double)step + 1.0;
+  step_dev[0] = step;
+  step_dev[2] = __float_as_uint((float)(1.0 / (1.0 - pow(0.9, t))));
+  step_dev[3] = __float_as_uint((float)sqrt(1.0 - pow(0.999, t)));
+}
 
 unsigned nblk(int64_t n, int t = 256) { return (unsigned)((n + t - 1) / t); }
 
