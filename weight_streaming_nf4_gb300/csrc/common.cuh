@@ -356,6 +356,59 @@ WS_DEVINL void bulk_copy_to_peer(uint32_t cdst, const void* src, uint32_t bytes,
       ::"r"(cdst), "r"(smem_u32(src)), "r"(bytes), "r"(cbar)
       : "memory");
 }
+// ---- CTA pairs: one tensor-core operation across both CTAs of a cluster of two ---------
+// Every tcgen05 instruction of a kernel uses the same CTA group, so a kernel
+// that issues pair MMAs allocates, commits and frees through these.
+// Both CTAs allocate (the same columns in each CTA's tensor memory).
+WS_DEVINL void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+WS_DEVINL void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+WS_DEVINL void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// Issued by the even CTA only: M = 256 rows, the first 128 from the even
+// CTA's A operand and the next 128 from the odd CTA's (same shared-memory
+// offset in each); B's first N/2 columns from the even CTA, the rest from
+// the odd one; D lands in each CTA's tensor memory at the same address.
+WS_DEVINL void tc_mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                               uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+WS_DEVINL void tc_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+WS_DEVINL void tc_commit_pair_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+// Tile load into this CTA's shared memory whose completion bytes go to an
+// mbarrier of either CTA of the pair (cluster address cbar).
+WS_DEVINL void tma_load_2d_pair(void* dst, const CUtensorMap* m, uint32_t cbar, int32_t x,
+                                int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(cbar), "r"(x), "r"(y)
+      : "memory");
+}
+
 WS_DEVINL void fence_proxy_async_cluster() {
   asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }

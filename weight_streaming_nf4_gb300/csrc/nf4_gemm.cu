@@ -4,17 +4,18 @@
 // Backward: dX[M,K] = dY[M,N] . W'[N,K]   (+ s (G A) . mask)
 //
 // W' = bf16_RN(c[code] * absmax) is never materialised in global memory:
-// packed 4-bit codes and the block absmax are staged into shared memory by
-// TMA, dequantised by eight producer warps straight into the 128-byte
+// packed 4-bit codes and the block absmax are staged into shared memory
+// (cp.async), dequantised by eight producer warps straight into the 128-byte
 // swizzled operand layout the tensor cores read, and consumed by
 // tcgen05.mma (bf16 x bf16 -> fp32 in TMEM) issued by one thread.
 //
-// Persistent CTA (one per SM) = 14 warps:
-//   warp 0      TMA producer (activation tile + code tile + absmax tile)
+// Persistent CTA (one per SM) = 18 warps:
+//   warp 0      TMA producer (activation tiles)
 //   warp 1      TMEM allocator and MMA issuer
-//   warps 2-9   dequant producers
-//   warps 10-13 epilogue (TMEM -> registers -> global), one TMEM lane
-//               quarter per warp, overlapping the next tile's main loop
+//   warps 2-9   dequant producers (each stages its own codes and block
+//               scales with cp.async)
+//   warps 10-17 epilogue (TMEM -> registers -> global), two per TMEM lane
+//               quarter, overlapping the next tile's main loop
 // Tile: 128*UM rows of activations (UM tensor-core atoms of M = 128 sharing
 // one dequantised weight tile), BN output columns, 64-deep contraction steps.
 //
@@ -73,6 +74,9 @@ namespace {
 #ifndef WS_GEMM_STAGES_MAX
 #define WS_GEMM_STAGES_MAX 6
 #endif
+#ifndef WS_GEMM_CSTAGES
+#define WS_GEMM_CSTAGES 4
+#endif
 
 constexpr int kDqWarps = 8;
 constexpr int kEpiWarps = 8;
@@ -81,12 +85,14 @@ constexpr int kDqThreads = kDqWarps * 32;
 
 // Dequant work of one thread per step.  A CTA fills the whole BN-wide
 // weight tile itself, or -- as one CTA of a pair sharing the tile -- the half
-// [rank * BN/2, (rank + 1) * BN/2) of it, written into both CTAs' buffers.
+// [rank * BN/2, (rank + 1) * BN/2) of it: PAIR = 1 writes that half into
+// both CTAs' full-width buffers, PAIR = 2 keeps it in a half-width buffer of
+// its own that the pair MMA reads from both CTAs.
 //   forward: ROWS weight-tile rows (output columns) x 64 codes, TPR threads
 //            per row, each with VB code bytes;
 //   backward: 64 contraction rows x COLS output columns in items of
 //            VB * 2 columns, one item per thread and vector.
-template <bool BWD, int BN, bool PAIR>
+template <bool BWD, int BN, int PAIR>
 struct DqGeo {
   static constexpr int COLS = PAIR ? BN / 2 : BN;  // columns (bwd) / rows (fwd) this CTA fills
   static constexpr int TPR = BWD ? 0 : kDqThreads / COLS;
@@ -99,14 +105,20 @@ struct DqGeo {
   static_assert(!BWD || (64 * COLS / (VB * 2)) % kDqThreads == 0, "dequant geometry");
 };
 
-template <bool BWD, int UM, int BN, bool PAIR>
+template <bool BWD, int UM, int BN, int PAIR>
 struct Cfg {
   static constexpr int BM = 128 * UM;
   static constexpr uint32_t A_BYTES = BM * 128;   // BM rows x 64 bf16
-  static constexpr uint32_t B_BYTES = BN * 128;   // BN x 64 bf16
-  static constexpr int BSTAGES = WS_GEMM_BSTAGES;
+  static constexpr bool PM = PAIR == 2;            // one MMA across the pair
+  static constexpr int BW = PM ? BN / 2 : BN;      // weight-tile width held by this CTA
+  static constexpr uint32_t B_BYTES = BW * 128;    // BW x 64 bf16
+#ifdef WS_GEMM_BSTAGES_PM
+  static constexpr int BSTAGES = PM ? WS_GEMM_BSTAGES_PM : WS_GEMM_BSTAGES;
+#else
+  static constexpr int BSTAGES = PM ? WS_GEMM_BSTAGES + 1 : WS_GEMM_BSTAGES;
+#endif
   // per-thread ring of fetched codes (cp.async), CSTAGES steps deep
-  static constexpr int CSTAGES = 4;
+  static constexpr int CSTAGES = WS_GEMM_CSTAGES;
   static constexpr uint32_t CODE_BYTES = DqGeo<BWD, BN, PAIR>::SLOT_BYTES;
   static constexpr int STAGES_RAW =
       (int)((220u * 1024u - BSTAGES * B_BYTES - CSTAGES * CODE_BYTES - 1024u) / A_BYTES);
@@ -121,7 +133,7 @@ struct Cfg {
   // MN-major operand (backward): 64-element MN groups LBO apart, 8-row K
   // groups SBO apart.
   static constexpr uint32_t MN_LBO = 1024;
-  static constexpr uint32_t MN_SBO = (BN / 64) * 1024;
+  static constexpr uint32_t MN_SBO = (BW / 64) * 1024;
   static constexpr uint32_t OFF_A = 0;
   static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr uint32_t OFF_CODE = OFF_B + BSTAGES * B_BYTES;
@@ -134,6 +146,7 @@ struct Cfg {
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory");
   static_assert(BN == 128 || BN == 256, "BN");
   static_assert(!PAIR || UM == 2, "a pair shares one weight tile between two 256-row halves");
+  static_assert(PAIR >= 0 && PAIR <= 2, "pair mode");
 };
 
 // CTA of the stream-K schedule that owns iteration i: ranges are
@@ -260,7 +273,7 @@ WS_DEVINL void cp_async_v(uint32_t dst, const void* src, bool in) {
 // n0 + j.  Backward: item (c, seg) covers weight row i*64 + c (the
 // contraction index) and 2*VB weight columns (the output index).
 // Rows / columns past the weight's edge read as zero codes with scale 0.
-template <bool BWD, int BN, bool PAIR>
+template <bool BWD, int BN, int PAIR>
 WS_DEVINL void fetch_codes(uint32_t slot, const GemmArgs& g, int i, int n0, int rank, int t) {
   using D = DqGeo<BWD, BN, PAIR>;
   const int64_t kb = g.wK / 2;  // code bytes per weight row
@@ -294,7 +307,7 @@ WS_DEVINL void fetch_codes(uint32_t slot, const GemmArgs& g, int i, int n0, int 
   }
 }
 
-template <bool BWD, int BN, bool PAIR>
+template <bool BWD, int BN, int PAIR>
 WS_DEVINL void read_frag(Frag& f, const uint8_t* slot, int t) {
   using D = DqGeo<BWD, BN, PAIR>;
   const float* sc = reinterpret_cast<const float*>(slot + D::NV * kDqThreads * D::VB);
@@ -318,11 +331,12 @@ WS_DEVINL void read_frag(Frag& f, const uint8_t* slot, int t) {
 
 // Forward weight tile, K-major 128B-swizzled: row j = output column n0 + j,
 // 64 contraction elements; chunk cc of row j sits at (cc ^ (j & 7)) * 16.
-template <int BN, bool PAIR>
+template <int BN, int PAIR>
 WS_DEVINL void dequant_fwd(const Frag& f, uint8_t* Bt, int rank, int t) {
   using D = DqGeo<false, BN, PAIR>;
   constexpr int WPT = 8 / D::TPR;  // code words per thread
-  const int j = (PAIR ? rank * D::COLS : 0) + t / D::TPR, part = t % D::TPR;
+  // row in this CTA's buffer
+  const int j = (PAIR == 1 ? rank * D::COLS : 0) + t / D::TPR, part = t % D::TPR;
   const Nf4Table tb = make_table(f.a[0]);
 #pragma unroll
   for (int q = 0; q < WPT; ++q) {
@@ -337,17 +351,17 @@ WS_DEVINL void dequant_fwd(const Frag& f, uint8_t* Bt, int rank, int t) {
 // so the tile keeps W's own orientation.  Element (k-col j, n-row c):
 // group (c/8, j/64) at (c/8)*SBO + (j/64)*LBO, row c%8 inside the group,
 // chunk ((j%64)/8) ^ (c%8).
-template <int BN, bool PAIR>
+template <int BN, int PAIR>
 WS_DEVINL void dequant_bwd(const Frag& f, uint8_t* Bt, int rank, int t) {
   using D = DqGeo<true, BN, PAIR>;
-  constexpr uint32_t SBO = (BN / 64) * 1024;
+  constexpr uint32_t SBO = ((PAIR == 2 ? BN / 2 : BN) / 64) * 1024;  // this CTA's buffer width
   constexpr int WPI = D::VB / 4;  // code words per item: 8 weights each
   constexpr int SEGS = D::COLS / (2 * D::VB);
 #pragma unroll
   for (int it = 0; it < D::NV; ++it) {
     const int item = t * D::NV + it;
     const int c = item / SEGS, seg = item % SEGS;
-    const int j0 = (PAIR ? rank * D::COLS : 0) + seg * 2 * D::VB;  // first tile column
+    const int j0 = (PAIR == 1 ? rank * D::COLS : 0) + seg * 2 * D::VB;  // first buffer column
     const Nf4Table tb = make_table(f.a[it]);
     const uint32_t grp = (uint32_t)((c >> 3) * SBO + (j0 / 64) * 1024 + (c & 7) * 128);
 #pragma unroll
@@ -363,14 +377,14 @@ WS_DEVINL void dequant_bwd(const Frag& f, uint8_t* Bt, int rank, int t) {
 // tile: row j holds [Ws_hi(16) | Ws_hi(16) | Ws_lo(16) | 0(16)] with
 // Ws = s * (row j of the LoRA factor).  Forward: factor row = B[n0+j, :];
 // backward: factor row = A[:, n0+j] (column of A).  A CTA of a pair fills
-// its half of the rows.
-template <bool BWD, int BN, bool PAIR>
+// its half of the rows (PAIR = 2: into its own half-width buffer).
+template <bool BWD, int BN, int PAIR>
 WS_DEVINL void lora_tile(const float* F, int64_t rows_total, int64_t ld, int n0, float s,
                          uint8_t* Bt, int rank, int t) {
   constexpr int ROWS = PAIR ? BN / 2 : BN;
   constexpr int TPR = kDqThreads / ROWS;  // threads per row
-  const int j = (PAIR ? rank * ROWS : 0) + t / TPR, part = t % TPR;
-  const int64_t n = (int64_t)n0 + j;
+  const int j = (PAIR == 1 ? rank * ROWS : 0) + t / TPR, part = t % TPR;  // buffer row
+  const int64_t n = (int64_t)n0 + (PAIR ? rank * ROWS : 0) + t / TPR;
   float v[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -413,15 +427,23 @@ struct Pos {
   }
 };
 
-// PAIR: the CTA is one of a cluster of two that share each weight tile.
-// The pair covers 2 * BM activation rows (rank r takes rows r * BM ...);
-// each CTA dequantises half of the tile's weight columns and writes it into
-// both CTAs' buffers, so every weight is decoded once per 512 rows instead
-// of once per 256.  A buffer is refilled once the MMAs of both CTAs that
-// read it have completed (their commits arrive on both CTAs' barriers).
+// PAIR != 0: the CTA is one of a cluster of two that share each weight
+// tile.  The pair covers 2 * BM activation rows (rank r takes rows r * BM
+// ...) and each CTA dequantises half of the tile's weight columns, so every
+// weight is decoded once per 512 rows instead of once per 256.
+//   PAIR = 1: each CTA copies its half into the other CTA's buffer as well
+//     and issues its own MMAs; a buffer is refilled once the MMAs of both
+//     CTAs that read it have completed (their commits arrive on both CTAs'
+//     barriers).
+//   PAIR = 2: the even CTA issues one M = 256 MMA for both CTAs
+//     (cta_group::2): the tensor cores read each CTA's activation rows and
+//     weight half where they lie, and each CTA's accumulator rows land in its
+//     own tensor memory.  The odd CTA's activation copies, dequant warps and
+//     epilogue warps signal the even CTA's barriers; the even CTA's commits
+//     arrive on both CTAs' barriers.  Nothing is copied between the CTAs.
 // The stream-K schedule runs over pairs; partial tiles and their flags stay
 // per CTA.
-template <bool BWD, int UM, int BN, bool PAIR>
+template <bool BWD, int UM, int BN, int PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmL,
                const GemmArgs args) {
@@ -429,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int STAGES = C::STAGES;
   constexpr int BSTAGES = C::BSTAGES;
   constexpr int NACC = C::ACC_BUFS;
+  constexpr bool PM = C::PM;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -484,22 +507,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
+    // PAIR = 2: the even CTA's full / bfull / accempty / lora_masked count
+    // both CTAs' producers and epilogues: the odd CTA's dequant warps arrive
+    // on its own bfull, and one forwarding thread passes each completed
+    // phase on to the even CTA (one cluster-scope release per step instead
+    // of one per warp)
     for (int b = 0; b < BSTAGES; ++b) {
-      mbar_init(&bfull[b], kDqWarps);
-      mbar_init(&bempty[b], PAIR ? 2 : 1);
+      mbar_init(&bfull[b], (PM && rank == 0) ? kDqWarps + 1 : kDqWarps);
+      mbar_init(&bempty[b], PAIR == 1 ? 2 : 1);
     }
     for (int a = 0; a < NACC; ++a) {
       mbar_init(&accfull[a], 1);
-      mbar_init(&accempty[a], kEpiWarps);
+      mbar_init(&accempty[a], PM ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(drain, 1);
     mbar_init(lora_done, 1);
-    mbar_init(lora_masked, kEpiWarps);
+    mbar_init(lora_masked, PM ? 2 * kEpiWarps : kEpiWarps);
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PM) {
+      // both CTAs of the pair allocate together; without a pair nothing runs
+      if (!bad_cfg) {
+        tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish_pair();
+      }
+    } else {
+      tmem_alloc(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   // both CTAs of a pair have their barriers set up before either arrives remotely
@@ -525,11 +561,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const int m0 = ps.mt * UROWS + rank * C::BM;
-          mbar_arrive_expect_tx(&full[s], C::A_BYTES);
-          if (!is_lora_step(ps.i))
-            tma_load_2d(sA + s * C::A_BYTES, &tmA, &full[s], kstep(ps.i) * 64, m0);
-          else
-            tma_load_2d(sA + s * C::A_BYTES, &tmL, &full[s], 0, m0);
+          const CUtensorMap* map = is_lora_step(ps.i) ? &tmL : &tmA;
+          const int32_t x = is_lora_step(ps.i) ? 0 : kstep(ps.i) * 64;
+          if constexpr (PM) {
+            // both CTAs' tiles complete on the even CTA's barrier
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::A_BYTES);
+            tma_load_2d_pair(sA + s * C::A_BYTES, map, mapa_shared(smem_u32(&full[s]), 0u), x, m0);
+          } else {
+            mbar_arrive_expect_tx(&full[s], C::A_BYTES);
+            tma_load_2d(sA + s * C::A_BYTES, map, &full[s], x, m0);
+          }
           issued = q + 1;
           if (++s == STAGES) {
             s = 0;
@@ -539,15 +580,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (*abort_flag) {
           // let every issued copy land before the CTA can exit
-          for (int64_t q = (issued > STAGES ? issued - STAGES : 0); q < issued; ++q)
-            mbar_wait(&full[q % STAGES], (uint32_t)(q / STAGES) & 1u, DERR_TIMEOUT_DRAIN);
+          if (!PM || rank == 0) {
+            for (int64_t q = (issued > STAGES ? issued - STAGES : 0); q < issued; ++q)
+              mbar_wait(&full[q % STAGES], (uint32_t)(q / STAGES) & 1u, DERR_TIMEOUT_DRAIN);
+          } else if (issued > 0) {
+            // the odd CTA's copies complete on the even CTA's barriers: give
+            // them time to land (a tile copy takes microseconds)
+            const uint64_t t0 = globaltimer();
+            while (globaltimer() - t0 < 200000ull) __nanosleep(1000);
+          }
         }
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        constexpr uint32_t idesc_main = idesc_bf16_f32(128, BN, BWD ? 1u : 0u);
-        constexpr uint32_t idesc_kmaj = idesc_bf16_f32(128, BN, 0u);
+      // (PAIR = 2: the even CTA's thread issues for both CTAs)
+      if (lane == 0 && (!PM || rank == 0)) {
+        constexpr uint32_t MMA_M = PM ? 256 : 128;
+        constexpr uint32_t idesc_main = idesc_bf16_f32(MMA_M, BN, BWD ? 1u : 0u);
+        constexpr uint32_t idesc_kmaj = idesc_bf16_f32(MMA_M, BN, 0u);
         int64_t seg = 0;
         int ms_s = 0, ms_b = 0;
         uint32_t ms_ph = 0, ms_bph = 0;
@@ -557,7 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t seg_end = min(pe, (t + 1) * S);
           const int a = (int)(seg % NACC);
           const uint32_t aph = (uint32_t)(seg / NACC) & 1u;
-          if (!mbar_wait(&accempty[a], aph ^ 1u, DERR_TIMEOUT_ACC)) {
+          const bool acc_ok = PM ? mbar_wait_cluster(&accempty[a], aph ^ 1u, DERR_TIMEOUT_ACC)
+                                 : mbar_wait(&accempty[a], aph ^ 1u, DERR_TIMEOUT_ACC);
+          if (!acc_ok) {
             *abort_flag = 1u;
             break;
           }
@@ -576,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ms_bph ^= 1u;
             }
             bool ok = !*abort_flag && mbar_wait(&full[s], ph, DERR_TIMEOUT_FULL);
-            if constexpr (PAIR) ok = ok && mbar_wait_cluster(&bfull[b], bph, DERR_TIMEOUT_BFULL);
+            if constexpr (PAIR != 0) ok = ok && mbar_wait_cluster(&bfull[b], bph, DERR_TIMEOUT_BFULL);
             else ok = ok && mbar_wait(&bfull[b], bph, DERR_TIMEOUT_BFULL);
             if (!ok) {
               *abort_flag = 1u;
@@ -598,16 +650,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t adesc = smem_desc_sw128(a_base + u * 16384 + kk * 32, 16, 1024);
                 const uint32_t d = dbase + (uint32_t)(u * BN);
                 const uint32_t acc = (p2 > p || kk > 0) ? 1u : 0u;
-                tc_mma_f16(d, adesc, bdesc, is_lora ? idesc_kmaj : idesc_main, acc);
+                if constexpr (PM) tc_mma_f16_pair(d, adesc, bdesc, is_lora ? idesc_kmaj : idesc_main, acc);
+                else tc_mma_f16(d, adesc, bdesc, is_lora ? idesc_kmaj : idesc_main, acc);
               }
             }
-            tc_commit(&empty[s]);
-            if constexpr (PAIR) tc_commit_multicast(&bempty[b], (uint16_t)0x3);
-            else tc_commit(&bempty[b]);
+            if constexpr (PM) {
+              tc_commit_pair_multicast(&empty[s], (uint16_t)0x3);
+              tc_commit_pair_multicast(&bempty[b], (uint16_t)0x3);
+            } else {
+              tc_commit(&empty[s]);
+              if constexpr (PAIR == 1) tc_commit_multicast(&bempty[b], (uint16_t)0x3);
+              else tc_commit(&bempty[b]);
+            }
             if (BWD && is_lora) {
               // the epilogue masks s G A in TMEM before the main steps add on top
-              tc_commit(lora_done);
-              if (!mbar_wait(lora_masked, lora_ph, DERR_TIMEOUT_ACC)) {
+              if constexpr (PM) tc_commit_pair_multicast(lora_done, (uint16_t)0x3);
+              else tc_commit(lora_done);
+              const bool lm_ok = PM ? mbar_wait_cluster(lora_masked, lora_ph, DERR_TIMEOUT_ACC)
+                                    : mbar_wait(lora_masked, lora_ph, DERR_TIMEOUT_ACC);
+              if (!lm_ok) {
                 *abort_flag = 1u;
                 break;
               }
@@ -615,12 +676,29 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
             }
           }
-          tc_commit(&accfull[a]);
+          if constexpr (PM) tc_commit_pair_multicast(&accfull[a], (uint16_t)0x3);
+          else tc_commit(&accfull[a]);
           p = seg_end;
         }
         // every MMA this thread issued has completed before TMEM is freed
-        tc_commit(drain);
+        if constexpr (PM) tc_commit_pair(drain);
+        else tc_commit(drain);
         mbar_wait(drain, 0u, DERR_TIMEOUT_DRAIN);
+      } else if (PM && lane == 0) {
+        // odd CTA: forward each completed weight-buffer phase to the even CTA
+        int b = 0;
+        uint32_t bph = 0;
+        for (int64_t q = 0; q < pe - pb; ++q) {
+          if (*abort_flag || !mbar_wait(&bfull[b], bph, DERR_TIMEOUT_BFULL)) {
+            *abort_flag = 1u;
+            break;
+          }
+          mbar_arrive_cluster(mapa_shared(smem_u32(&bfull[b]), 0u));
+          if (++b == BSTAGES) {
+            b = 0;
+            bph ^= 1u;
+          }
+        }
       }
     } else if (warp < 2 + kDqWarps) {
       // ------------------------------------------------------------ dequant producers
@@ -653,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         Frag cur;
         read_frag<BWD, BN, PAIR>(cur, ring + (q % CS) * C::CODE_BYTES, t_idx);
         bool ok = !*abort_flag;
-        if constexpr (PAIR) ok = ok && mbar_wait_cluster(&bempty[b], bph ^ 1u, DERR_TIMEOUT_BEMPTY);
+        if constexpr (PAIR != 0) ok = ok && mbar_wait_cluster(&bempty[b], bph ^ 1u, DERR_TIMEOUT_BEMPTY);
         else ok = ok && mbar_wait(&bempty[b], bph ^ 1u, DERR_TIMEOUT_BEMPTY);
         if (!ok) {
           *abort_flag = 1u;
@@ -671,7 +749,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (PAIR) {
+          if constexpr (PM) {
+            // the even CTA's MMA reads this half where it lies
+            mbar_arrive(&bfull[b]);
+          } else if constexpr (PAIR == 1) {
             // this warp's share of the half tile is one contiguous block:
             // rows (K-major) or one 8-row contraction group (MN-major);
             // send it to the same place in the other CTA's buffer
@@ -695,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pc.next(S, args.mtiles);
       }
       cp_async_wait<0>();  // no copy may land after the CTA is gone
-      if constexpr (PAIR) {
+      if constexpr (PAIR != 0) {
         // the other CTA's MMA commits arrive on this CTA's buffer barriers:
         // wait for the last of them before the CTA can leave
         for (int k = 0; k < BSTAGES && !*abort_flag; ++k) {
@@ -716,6 +797,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = q4 * 32 + lane;
       // CTA holding this CTA's rows of the tile in unit u
       auto cta_of = [&](int64_t u) -> int64_t { return PAIR ? 2 * u + rank : u; };
+      // A CTA's fp32 partial tile is stored as float4 [BN/4][BM]: element
+      // (row, 4c..4c+3) at [c][row], so the 32 rows of a warp make one
+      // contiguous 512-byte access per column group.
+      auto part4 = [&](int64_t cta, int row, int cc) -> float4* {
+        return reinterpret_cast<float4*>(args.partial + cta * C::TILE_FLOATS) +
+               (int64_t)(cc / 4) * C::BM + row;
+      };
       int64_t seg = 0;
       uint32_t lora_ph = 0;
       for (int64_t p = pb; p < pe; ++seg) {
@@ -755,7 +843,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(lora_masked);
+          if (lane == 0) {
+            if (PM && rank == 1) mbar_arrive_cluster(mapa_shared(smem_u32(lora_masked), 0u));
+            else mbar_arrive(lora_masked);
+          }
         }
         const bool ok = !*abort_flag && mbar_wait_backoff(&accfull[a], aph, DERR_TIMEOUT_ACC);
         tc_fence_after();
@@ -766,7 +857,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool finisher = (i0 == 0 && kb < S);
         const bool writer = !whole && !finisher;  // a later piece: hand it over
         (void)kb;
-        float* part = args.partial + (int64_t)blockIdx.x * C::TILE_FLOATS;
         int64_t u_last = unit;
         if (finisher) {
           u_last = sk_cta_of(t * S + S - 1, I, U);
@@ -813,10 +903,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float4 pv[4];
             const bool piece = row_ok && !writer && u_last > unit;
             if (piece) {
-              const float4* src = reinterpret_cast<const float4*>(
-                  args.partial + cta_of(unit + 1) * C::TILE_FLOATS + (int64_t)row * BN + cc);
+              const float4* src = part4(cta_of(unit + 1), row, cc);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) pv[e] = src[e];
+              for (int e = 0; e < 4; ++e) pv[e] = src[(int64_t)e * C::BM];
             }
             tmem_ld_wait();
             if (!row_ok) continue;
@@ -824,10 +913,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(acc[e]);
             if (writer) {
-              float4* dst = reinterpret_cast<float4*>(part + (int64_t)row * BN + cc);
+              float4* dst = part4(blockIdx.x, row, cc);
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                dst[(int64_t)e * C::BM] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
               continue;
             }
             // finisher: add the later pieces in step order
@@ -841,11 +930,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
             for (int64_t uu = unit + 2; uu <= u_last; ++uu) {
-              const float4* src = reinterpret_cast<const float4*>(
-                  args.partial + cta_of(uu) * C::TILE_FLOATS + (int64_t)row * BN + cc);
+              const float4* src = part4(cta_of(uu), row, cc);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const float4 q = src[e];
+                const float4 q = src[(int64_t)e * C::BM];
                 v[4 * e] += q.x;
                 v[4 * e + 1] += q.y;
                 v[4 * e + 2] += q.z;
@@ -887,7 +975,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&accempty[a]);
+        if (lane == 0) {
+          if (PM && rank == 1) mbar_arrive_cluster(mapa_shared(smem_u32(&accempty[a]), 0u));
+          else mbar_arrive(&accempty[a]);
+        }
         p = seg_end;
       }
     }
@@ -898,7 +989,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (PAIR && !bad_cfg) cluster_sync();
   else __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PM) {
+      if (!bad_cfg) tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    } else {
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+  }
 }
 
 // ------------------------------------------------------------------------ LoRA weight gradients
@@ -1470,7 +1567,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 // iterations per CTA so tiny problems are not shredded into partials.
 constexpr int64_t kMinSteps = 8;
 
-template <bool BWD, int UM, int BN, bool PAIR>
+template <bool BWD, int UM, int BN, int PAIR>
 cudaError_t set_smem_attr() {
   static cudaError_t e = cudaFuncSetAttribute(k_nf4_gemm<BWD, UM, BN, PAIR>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1478,17 +1575,28 @@ cudaError_t set_smem_attr() {
   return e;
 }
 
+// How a pair of CTAs shares a weight tile: 2 = one MMA across both CTAs
+// (the default), 1 = each CTA issues its own MMAs on a full-width tile that
+// both CTAs fill (WS_NF4_PAIR_MMA=0).
+int pair_mode() {
+  static const int m = [] {
+    const char* v = getenv("WS_NF4_PAIR_MMA");
+    return (v && v[0] == '0') ? 1 : 2;
+  }();
+  return m;
+}
+
 // Pairs of CTAs that can be resident at once (one CTA per SM).
-template <bool BWD, int BN>
+template <bool BWD, int BN, int PAIR>
 int64_t pair_capacity_of() {
   static int64_t cap = -1;
   if (cap < 0) {
     cap = 0;
-    if (set_smem_attr<BWD, 2, BN, true>() == cudaSuccess) {
+    if (set_smem_attr<BWD, 2, BN, PAIR>() == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * (unsigned)(device_sm_count() / 2));
       cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = Cfg<BWD, 2, BN, true>::SMEM_BYTES;
+      cfg.dynamicSmemBytes = Cfg<BWD, 2, BN, PAIR>::SMEM_BYTES;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = 2;
@@ -1497,7 +1605,7 @@ int64_t pair_capacity_of() {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, k_nf4_gemm<BWD, 2, BN, true>, &cfg) == cudaSuccess)
+      if (cudaOccupancyMaxActiveClusters(&n, k_nf4_gemm<BWD, 2, BN, PAIR>, &cfg) == cudaSuccess)
         cap = n;
       else
         cudaGetLastError();
@@ -1508,7 +1616,7 @@ int64_t pair_capacity_of() {
   return cap;
 }
 
-template <bool BWD, int UM, int BN, bool PAIR>
+template <bool BWD, int UM, int BN, int PAIR>
 cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& tA,
                        const CUtensorMap& tL, cudaStream_t st) {
   using C = Cfg<BWD, UM, BN, PAIR>;
@@ -1537,7 +1645,7 @@ cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& 
     return !(v && v[0] == '0');
   }();
   cfg.attrs = coop ? attr : attr + 1;
-  cfg.numAttrs = (coop ? 1 : 0) + (PAIR ? 1 : 0);
+  cfg.numAttrs = (coop ? 1 : 0) + (PAIR != 0 ? 1 : 0);
   note_launch();
   return cudaLaunchKernelEx(&cfg, k_nf4_gemm<BWD, UM, BN, PAIR>, tA, tL, a);
 }
@@ -1590,8 +1698,12 @@ int device_sm_count() {
 }
 
 int64_t pair_capacity(bool bwd, int bn) {
-  if (bwd) return bn == 256 ? pair_capacity_of<true, 256>() : pair_capacity_of<true, 128>();
-  return bn == 256 ? pair_capacity_of<false, 256>() : pair_capacity_of<false, 128>();
+  if (pair_mode() == 2) {
+    if (bwd) return bn == 256 ? pair_capacity_of<true, 256, 2>() : pair_capacity_of<true, 128, 2>();
+    return bn == 256 ? pair_capacity_of<false, 256, 2>() : pair_capacity_of<false, 128, 2>();
+  }
+  if (bwd) return bn == 256 ? pair_capacity_of<true, 256, 1>() : pair_capacity_of<true, 128, 1>();
+  return bn == 256 ? pair_capacity_of<false, 256, 1>() : pair_capacity_of<false, 128, 1>();
 }
 
 int64_t grid_units(const GemmPlan& p, bool has_lora) {
@@ -1690,21 +1802,30 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
   }
 
   if (partial == nullptr && grid_units(p, has_lora) > 1) return cudaErrorInvalidValue;
+  const bool pm = pair_mode() == 2;
   if (!p.bwd) {
-    if (p.pair) {
-      if (p.bn == 256) return launch_cfg<false, 2, 256, true>(p, a, tA, tL, st);
-      return launch_cfg<false, 2, 128, true>(p, a, tA, tL, st);
+    if (p.pair && pm) {
+      if (p.bn == 256) return launch_cfg<false, 2, 256, 2>(p, a, tA, tL, st);
+      return launch_cfg<false, 2, 128, 2>(p, a, tA, tL, st);
     }
-    if (p.um == 2 && p.bn == 256) return launch_cfg<false, 2, 256, false>(p, a, tA, tL, st);
-    if (p.um == 2) return launch_cfg<false, 2, 128, false>(p, a, tA, tL, st);
-    return launch_cfg<false, 1, 128, false>(p, a, tA, tL, st);
+    if (p.pair) {
+      if (p.bn == 256) return launch_cfg<false, 2, 256, 1>(p, a, tA, tL, st);
+      return launch_cfg<false, 2, 128, 1>(p, a, tA, tL, st);
+    }
+    if (p.um == 2 && p.bn == 256) return launch_cfg<false, 2, 256, 0>(p, a, tA, tL, st);
+    if (p.um == 2) return launch_cfg<false, 2, 128, 0>(p, a, tA, tL, st);
+    return launch_cfg<false, 1, 128, 0>(p, a, tA, tL, st);
+  }
+  if (p.pair && pm) {
+    if (p.bn == 256) return launch_cfg<true, 2, 256, 2>(p, a, tA, tL, st);
+    return launch_cfg<true, 2, 128, 2>(p, a, tA, tL, st);
   }
   if (p.pair) {
-    if (p.bn == 256) return launch_cfg<true, 2, 256, true>(p, a, tA, tL, st);
-    return launch_cfg<true, 2, 128, true>(p, a, tA, tL, st);
+    if (p.bn == 256) return launch_cfg<true, 2, 256, 1>(p, a, tA, tL, st);
+    return launch_cfg<true, 2, 128, 1>(p, a, tA, tL, st);
   }
-  if (p.um == 2) return launch_cfg<true, 2, 128, false>(p, a, tA, tL, st);
-  return launch_cfg<true, 1, 128, false>(p, a, tA, tL, st);
+  if (p.um == 2) return launch_cfg<true, 2, 128, 0>(p, a, tA, tL, st);
+  return launch_cfg<true, 1, 128, 0>(p, a, tA, tL, st);
 }
 
 // ------------------------------------------------------------------------ skinny products (host)
