@@ -82,6 +82,7 @@ constexpr int kDqWarps = 8;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kDqWarps + kEpiWarps) * 32;
 constexpr int kDqThreads = kDqWarps * 32;
+constexpr int kFinRing = 8;  // finisher: partial-tile entries in flight per epilogue warp
 
 // Dequant work of one thread per step.  A CTA fills the whole BN-wide
 // weight tile itself, or -- as one CTA of a pair sharing the tile -- the half
@@ -147,6 +148,7 @@ struct Cfg {
   static_assert(BN == 128 || BN == 256, "BN");
   static_assert(!PAIR || UM == 2, "a pair shares one weight tile between two 256-row halves");
   static_assert(PAIR >= 0 && PAIR <= 2, "pair mode");
+  static_assert(OFF_CODE >= (uint32_t)(kEpiWarps * kFinRing * 2048), "finisher ring fits the stages");
 };
 
 // CTA of the stream-K schedule that owns iteration i: ranges are
@@ -822,9 +824,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t lm0 = (t % args.mtiles) * UROWS + rank * C::BM;
           const int64_t ln0 = (t / args.mtiles) * BN;
           const uint32_t lbase = tmem + (uint32_t)(a * C::ACC_COLS);
-#pragma unroll 1
+          // this thread's mask words (its row, this warp's columns), all
+          // loaded at once: one memory round trip instead of one per chunk
+          constexpr int MW = (BN / 2) / 32;
+          uint32_t mw[UM * MW];
+#pragma unroll
           for (int u = 0; u < UM; ++u) {
             const int64_t m = lm0 + u * 128 + r;
+#pragma unroll
+            for (int w = 0; w < MW; ++w) {
+              const int64_t n = ln0 + half * (BN / 2) + 32 * w;
+              mw[u * MW + w] = (lok && m < args.M && n < args.Nout) ? args.mask[(m * args.Nout + n) >> 5] : 0u;
+            }
+          }
+#pragma unroll 1
+          for (int u = 0; u < UM; ++u) {
 #pragma unroll 1
             for (int cc = half * (BN / 2); cc < (half + 1) * (BN / 2); cc += 16) {
               const int64_t n = ln0 + cc;
@@ -832,8 +846,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t taddr = lbase + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(u * BN + cc);
               uint32_t v[16];
               tmem_ld_32x32b_x16(taddr, v);
-              const uint32_t bits =
-                  (lok && m < args.M) ? args.mask[(m * args.Nout + n) >> 5] >> (n & 31) : 0u;
+              // select word (u, (cc - half * BN/2) / 32) without indexing the array at run time
+              const int wi = u * MW + (cc - half * (BN / 2)) / 32;
+              uint32_t word = 0u;
+#pragma unroll
+              for (int w = 0; w < UM * MW; ++w) word = (w == wi) ? mw[w] : word;
+              const uint32_t bits = word >> (cc & 31);
               tmem_ld_wait();
 #pragma unroll
               for (int e = 0; e < 16; ++e) v[e] = ((bits >> e) & 1u) ? v[e] : 0u;
@@ -887,59 +905,73 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (*fin_got == 0u) u_last = unit;  // timed out: store what is here, flagged as an error
         }
         const uint32_t dbase = tmem + (uint32_t)(a * C::ACC_COLS);
+        // 16-column chunks of this warp's columns that lie inside the output
+        constexpr int KCH = (BN / 2) / 16;
+        const int64_t cols_left = args.Nout - (n0 + half * (BN / 2));
+        const int kv = cols_left <= 0 ? 0 : (cols_left >= KCH * 16 ? KCH : (int)((cols_left + 15) / 16));
+        // A finisher's segment is its unit's last, so the main loop's shared
+        // memory is idle: the later pieces stream through a per-warp ring of
+        // kFinRing cp.async entries there (entry = one piece's 32 rows x 16
+        // columns), consumed chunk by chunk in step order.
+        const int P = finisher ? (int)(u_last - unit) : 0;
+        const int64_t r_total = (int64_t)P * UM * kv;
+        const uint32_t r_base = smem_u32(smem) + (uint32_t)(ew * kFinRing * 2048 + lane * 16);
+        int64_t r_issued = 0, r_used = 0;
+        auto r_issue = [&]() {
+          if (r_issued < r_total) {
+            const int k = (int)(r_issued / P), pp = (int)(r_issued % P) + 1;
+            const float4* src = part4(cta_of(unit + pp), (k / kv) * 128 + r, half * (BN / 2) + (k % kv) * 16);
+            const uint32_t dst = r_base + (uint32_t)((r_issued % kFinRing) * 2048);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) cp_async16(dst + (uint32_t)(e * 512), src + (int64_t)e * C::BM, 16u);
+          }
+          cp_async_commit();
+          ++r_issued;
+        };
+        if (P > 0)
+          for (int j = 0; j < kFinRing; ++j) r_issue();
 #pragma unroll 1
         for (int u = 0; u < UM; ++u) {
           const int row = u * 128 + r;
           const int64_t m = m0 + row;
           const bool row_ok = ok && m < args.M;
 #pragma unroll 1
-          for (int cc = half * (BN / 2); cc < (half + 1) * (BN / 2); cc += 16) {
+          for (int c = 0; c < kv; ++c) {
+            const int cc = half * (BN / 2) + c * 16;
             const int64_t n = n0 + cc;
-            if (n >= args.Nout) break;  // warp-uniform
             uint32_t acc[16];
             const uint32_t taddr = dbase + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(u * BN + cc);
             tmem_ld_32x32b_x16(taddr, acc);
-            // the first later piece's values load while the TMEM read is in flight
-            float4 pv[4];
-            const bool piece = row_ok && !writer && u_last > unit;
-            if (piece) {
-              const float4* src = part4(cta_of(unit + 1), row, cc);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) pv[e] = src[(int64_t)e * C::BM];
-            }
             tmem_ld_wait();
-            if (!row_ok) continue;
             float v[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(acc[e]);
             if (writer) {
+              if (!row_ok) continue;
               float4* dst = part4(blockIdx.x, row, cc);
 #pragma unroll
               for (int e = 0; e < 4; ++e)
                 dst[(int64_t)e * C::BM] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
               continue;
             }
-            // finisher: add the later pieces in step order
-            if (piece) {
+            // finisher: add the later pieces in step order (every thread
+            // consumes its ring entries, rows past M included)
+            for (int pp = 0; pp < P; ++pp) {
+              cp_async_wait<kFinRing - 1>();
+              const float4* sl = reinterpret_cast<const float4*>(
+                  smem + ew * kFinRing * 2048 + (int)(r_used % kFinRing) * 2048 + lane * 16);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                v[4 * e] += pv[e].x;
-                v[4 * e + 1] += pv[e].y;
-                v[4 * e + 2] += pv[e].z;
-                v[4 * e + 3] += pv[e].w;
-              }
-            }
-            for (int64_t uu = unit + 2; uu <= u_last; ++uu) {
-              const float4* src = part4(cta_of(uu), row, cc);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float4 q = src[(int64_t)e * C::BM];
+                const float4 q = sl[e * 32];
                 v[4 * e] += q.x;
                 v[4 * e + 1] += q.y;
                 v[4 * e + 2] += q.z;
                 v[4 * e + 3] += q.w;
               }
+              ++r_used;
+              r_issue();
             }
+            if (!row_ok) continue;
             if (args.out_f32) {
               float4* dst =
                   reinterpret_cast<float4*>(static_cast<float*>(args.out) + m * args.Nout + n);
@@ -967,6 +999,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if (P > 0) cp_async_wait<0>();
         if (writer) {
           // publish the piece: every epilogue thread's stores, then one flag
           __threadfence();
