@@ -433,8 +433,41 @@ WS_DEVINL bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t why) {
 
 #endif
 
+// ---- programmatic dependent launch ----------------------------------------------------
+// Kernels are launched with programmatic stream serialization: the next
+// kernel in the stream may be scheduled while this one still runs, does its
+// own setup (barriers, tensor memory, descriptors), and waits here before
+// its first access to global memory that an earlier kernel writes or reads.
+// Once past the wait every earlier kernel of the stream has completed and
+// its writes are visible.  Without that launch attribute the wait returns
+// at once.
+WS_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allows the next kernel of the stream to be scheduled (it still waits for
+// this grid to complete before touching data).
+WS_DEVINL void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 WS_DEVINL void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Host: launch with programmatic stream serialization (unless
+// WS_NF4_PDL=0).  Every kernel launched this way calls pdl_wait() before its
+// first dependent global access.
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
 }  // namespace ws

@@ -31,12 +31,14 @@ struct GemmArgs {
   const uint32_t* mask; // backward: dropout bits [M, K/32]
   void* out;            // [M, Nout] bf16 or fp32
   int out_f32, out_accum;
-  float* partial;       // [grid, BM, BN] fp32 partial tile of each CTA's cut first segment
+  float* partial;       // per CTA one fp32 partial tile (its cut first segment), stored as
+                        // float4 [BN/4][BM]
   uint32_t* flags;      // [grid] set to 1 once that partial is complete (ring words, zero
                         // before and after the launch)
   const uint8_t* codes; // the weight's packed codes [N, K/2]
   const float* absmax;  // the weight's block scales [K/64, N]
   int64_t wN, wK;       // the weight's shape
+  int epad;             // schedule-only steps charged per tile (see GemmPlan::epad)
 };
 
 // Tile configuration: a pure function of the shape and the SM count, so a
@@ -46,6 +48,10 @@ struct GemmPlan {
   bool pair;  // two CTAs of a cluster share each weight tile
   int um, bn;
   int mtiles, ntiles, nk;
+  // Stream-K ranges are cut over tiles of S + epad iterations, the last
+  // epad of which carry no work: a unit whose range ends more tiles (one
+  // accumulator drain each) gets fewer contraction steps.
+  int epad;
 };
 
 int device_sm_count();

@@ -23,6 +23,8 @@ __constant__ float c_levels_q[16] = {-1.0f,    -0.6962f, -0.5251f, -0.3949f, -0.
 // below v.
 __global__ void k_quantize_nf4(const uint16_t* __restrict__ W, int64_t N, int64_t K,
                                uint8_t* __restrict__ codes, float* __restrict__ absmax) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t nkb = K / 64;
   const int64_t blk = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x / 32);
   if (blk >= N * nkb) return;
@@ -53,6 +55,8 @@ __global__ void k_quantize_nf4(const uint16_t* __restrict__ W, int64_t N, int64_
 
 // ------------------------------------------------------------------------ mask regeneration
 __global__ void k_mask_gen(int64_t words, DropKey key, uint32_t* __restrict__ mask) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (w >= words) return;
   resolve_step(key);
@@ -104,7 +108,7 @@ cudaError_t run_quantize_nf4(const uint16_t* W, int64_t N, int64_t K, uint8_t* c
   const int64_t blocks = N * (K / 64);
   const int per = 8;  // warps per CTA
   note_launch();
-  k_quantize_nf4<<<(unsigned)((blocks + per - 1) / per), 32 * per, 0, st>>>(W, N, K, codes, absmax);
+  (void)launch_pdl(k_quantize_nf4, dim3((unsigned)((blocks + per - 1) / per)), dim3(32 * per), 0, st, W, N, K, codes, absmax);
   return cudaGetLastError();
 }
 
@@ -124,7 +128,7 @@ cudaError_t run_mask_gen(int64_t M, int64_t K, const DropKeyHost& key, uint32_t*
                          cudaStream_t st) {
   const int64_t words = M * K / 32;
   note_launch();
-  k_mask_gen<<<(unsigned)((words + 255) / 256), 256, 0, st>>>(words, to_dev(key), mask);
+  (void)launch_pdl(k_mask_gen, dim3((unsigned)((words + 255) / 256)), dim3(256), 0, st, words, to_dev(key), mask);
   return cudaGetLastError();
 }
 

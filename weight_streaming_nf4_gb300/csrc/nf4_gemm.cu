@@ -489,11 +489,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto kstep = [&](int i) { return lora_first ? i - 1 : i; };
   const int64_t T = (int64_t)args.mtiles * args.ntiles;
-  const int64_t I = T * S;
+  // ranges are cut over SV = S + epad iterations per tile; the last epad
+  // carry no work (a range boundary inside them moves to the next tile)
+  const int64_t SV = S + args.epad;
+  const int64_t I = T * SV;
   const int64_t U = PAIR ? gridDim.x / 2 : gridDim.x;
   const int64_t unit = PAIR ? blockIdx.x / 2 : blockIdx.x;
-  const int64_t pb = sk_begin(unit, I, U);
-  const int64_t pe = sk_begin(unit + 1, I, U);
+  auto real_of = [&](int64_t v) -> int64_t {
+    const int64_t t = v / SV, i = v % SV;
+    return i >= S ? (t + 1) * S : t * S + i;
+  };
+  const int64_t pb = real_of(sk_begin(unit, I, U));
+  const int64_t pe = real_of(sk_begin(unit + 1, I, U));
   const Pos pos0 = {(int)(pb % S), (int)((pb / S) % args.mtiles), (int)((pb / S) / args.mtiles)};
   constexpr int UROWS = PAIR ? 2 * C::BM : C::BM;  // activation rows per tile
 
@@ -546,6 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool skip = *skip_flag != 0u;
+  // setup done: from here on the earlier kernels' data is read and written
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (!skip) {
     if (warp == 0) {
@@ -877,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)kb;
         int64_t u_last = unit;
         if (finisher) {
-          u_last = sk_cta_of(t * S + S - 1, I, U);
+          u_last = sk_cta_of(t * SV + S - 1, I, U);  // unit holding the tile's last step
           // one thread waits for the later pieces (each CTA publishes at
           // most one); the barrier passes what it acquired to the others
           if (ew == 0 && lane == 0) {
@@ -1096,6 +1106,8 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+  pdl_launch_dependents();
   if (*skip_flag == 0u) {
     if (warp == 0) {
       if (lane == 0) {
@@ -1322,7 +1334,6 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   const int64_t s_begin = (int64_t)blockIdx.y * steps_per_chunk;
   const int64_t s_end = min(nsteps_total, s_begin + steps_per_chunk);
   const int nsteps = (int)(s_end > s_begin ? s_end - s_begin : 0);
-  if (MASKED) resolve_step(key);
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
     flags[0] = (*(volatile uint32_t*)&g_dev_error != 0u) ? 1u : 0u;
@@ -1348,6 +1359,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool skip = flags[0] != 0u;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (MASKED) resolve_step(key);
   if (!skip) {
     if (warp == 0) {
       if (lane == 0 && nsteps > 0) {
@@ -1596,6 +1610,11 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+#ifndef WS_GEMM_EPAD
+#define WS_GEMM_EPAD 10
+#endif
+constexpr int kEpadSteps = WS_GEMM_EPAD;
+
 // Persistent grid: one CTA per SM, but at least kMinSteps (tile, step)
 // iterations per CTA so tiny problems are not shredded into partials.
 constexpr int64_t kMinSteps = 8;
@@ -1607,6 +1626,18 @@ cudaError_t set_smem_attr() {
                                               (int)Cfg<BWD, UM, BN, PAIR>::SMEM_BYTES);
   return e;
 }
+
+}  // namespace
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("WS_NF4_PDL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
+namespace {
 
 // How a pair of CTAs shares a weight tile: 2 = one MMA across both CTAs
 // (the default), 1 = each CTA issues its own MMAs on a full-width tile that
@@ -1656,29 +1687,44 @@ cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& 
   cudaError_t e = set_smem_attr<BWD, UM, BN, PAIR>();
   if (e != cudaSuccess) return e;
   const int64_t G = grid_ctas(p, a.has_lora != 0);
-  // cooperative: all CTAs resident at once, so a finisher's wait for a
-  // later CTA's piece always ends
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)G);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 2;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  // WS_NF4_COOP=0 drops the cooperative attribute (the grid is sized to be
-  // resident anyway); profilers that cannot launch cooperative clusters
-  // need it.
+  // The grid is sized to be resident at once, so a finisher's wait for a
+  // later CTA's piece ends.  Cooperative launch guarantees it outright;
+  // WS_NF4_COOP=0 drops that attribute (profilers that cannot launch
+  // cooperative clusters need it).  With programmatic serialization the grid
+  // may start while the previous kernel still holds SMs, which a cooperative
+  // launch does not allow: CTAs the previous kernel delays start as its CTAs
+  // leave (it never waits on this grid), so the bounded waits still end.
   static const bool coop = [] {
     const char* v = getenv("WS_NF4_COOP");
     return !(v && v[0] == '0');
   }();
-  cfg.attrs = coop ? attr : attr + 1;
-  cfg.numAttrs = (coop ? 1 : 0) + (PAIR != 0 ? 1 : 0);
+  const bool pdl = pdl_enabled();
+  cudaLaunchAttribute attr[3];
+  int na = 0;
+  if (coop && !pdl) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+  }
+  if (PAIR != 0) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
   note_launch();
   return cudaLaunchKernelEx(&cfg, k_nf4_gemm<BWD, UM, BN, PAIR>, tA, tL, a);
 }
@@ -1778,6 +1824,15 @@ GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc) {
   p.mtiles = (int)((M + urows - 1) / urows);
   p.ntiles = (int)((Nout + p.bn - 1) / p.bn);
   p.nk = (int)(Kc / 64);
+  // A single accumulator (UM = 2, BN = 256) stalls the MMAs for the drain of
+  // every tile a unit ends: charge it in the schedule when units end about
+  // one tile each (with fewer tiles than units, ranges end mostly inside
+  // tiles and the finisher's wait for the later pieces dominates).
+  p.epad = 0;
+  if (p.um == 2 && p.bn == 256) {
+    const int64_t units = p.pair ? pair_capacity(bwd, 256) : device_sm_count();
+    if (units > 0 && (int64_t)p.mtiles * p.ntiles >= units) p.epad = kEpadSteps;
+  }
   return p;
 }
 
@@ -1828,6 +1883,7 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
   a.absmax = W.absmax;
   a.wN = N;
   a.wK = K;
+  a.epad = p.epad;
   a.flags = nullptr;
   if (grid_units(p, has_lora) > 1) {
     cudaError_t e = ring_slots((uint32_t)grid_ctas(p, has_lora), &a.flags);
@@ -1963,13 +2019,13 @@ cudaError_t run_skinny_tc(const uint16_t* X, const float* F, bool f_kj, int64_t 
   DropKey none{};
   note_launch();
   if (key && !f_kj)
-    k_skinny_tc<true, false><<<grid, kSkThreads, kSkSmem, st>>>(
+    (void)launch_pdl(k_skinny_tc<true, false>, dim3(grid), dim3(kSkThreads), kSkSmem, st, 
         tX, tF, F, M, K, spc, *key, mask_bytes, partial, counters, out, ext);
   else if (f_kj)
-    k_skinny_tc<false, true><<<grid, kSkThreads, kSkSmem, st>>>(
+    (void)launch_pdl(k_skinny_tc<false, true>, dim3(grid), dim3(kSkThreads), kSkSmem, st, 
         tX, tF, F, M, K, spc, none, nullptr, partial, counters, out, ext);
   else
-    k_skinny_tc<false, false><<<grid, kSkThreads, kSkSmem, st>>>(
+    (void)launch_pdl(k_skinny_tc<false, false>, dim3(grid), dim3(kSkThreads), kSkSmem, st, 
         tX, tF, F, M, K, spc, none, nullptr, partial, counters, out, ext);
   return cudaGetLastError();
 }
@@ -2001,9 +2057,9 @@ cudaError_t run_wgrad_tc(const float* P, const uint16_t* Q, const uint32_t* mask
   const dim3 grid((unsigned)((C + kWgBN - 1) / kWgBN));
   note_launch();
   if (mask)
-    k_wgrad_tc<true><<<grid, kWgThreads, kWgSmem, st>>>(tQ, P, mask, M, C, s, transpose_out, out);
+    (void)launch_pdl(k_wgrad_tc<true>, dim3(grid), dim3(kWgThreads), kWgSmem, st, tQ, P, mask, M, C, s, transpose_out, out);
   else
-    k_wgrad_tc<false><<<grid, kWgThreads, kWgSmem, st>>>(tQ, P, nullptr, M, C, s, transpose_out,
+    (void)launch_pdl(k_wgrad_tc<false>, dim3(grid), dim3(kWgThreads), kWgSmem, st, tQ, P, nullptr, M, C, s, transpose_out,
                                                          out);
   return cudaGetLastError();
 }

@@ -39,6 +39,8 @@ WS_DEVINL float block_sum_256(float v, float* red) {
 __global__ void __launch_bounds__(256) k_rmsnorm_fwd(const float* __restrict__ h, int64_t H,
                                                      float eps, uint16_t* __restrict__ out,
                                                      float* __restrict__ rstd) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float red[9];
   const int64_t m = blockIdx.x;
   const float4* row = reinterpret_cast<const float4*>(h + m * H);
@@ -66,6 +68,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(const float* __restrict__ x
                                                      const float* __restrict__ rstd,
                                                      const float* __restrict__ dy, int64_t H,
                                                      float* __restrict__ dx) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float red[9];
   const int64_t m = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + m * H);
@@ -99,6 +103,8 @@ WS_DEVINL float silu_sig(float g) { return 1.0f / (1.0f + expf(-g)); }
 // 8 elements per thread (n % 8 == 0)
 __global__ void k_silu_mul_fwd(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u,
                                int64_t n, uint16_t* __restrict__ act) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t i8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i8 * 8 >= n) return;
   const uint4 gv = reinterpret_cast<const uint4*>(g)[i8];
@@ -117,6 +123,8 @@ __global__ void k_silu_mul_fwd(const uint16_t* __restrict__ g, const uint16_t* _
 __global__ void k_silu_mul_bwd(const float* __restrict__ dact, const uint16_t* __restrict__ g,
                                const uint16_t* __restrict__ u, int64_t n, uint16_t* __restrict__ dg,
                                uint16_t* __restrict__ du) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t i8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i8 * 8 >= n) return;
   const uint4 gv = reinterpret_cast<const uint4*>(g)[i8];
@@ -142,6 +150,8 @@ __global__ void k_silu_mul_bwd(const float* __restrict__ dact, const uint16_t* _
 // vr[m, hh*hd + d] = v[m, (hh / rep)*hd + d]; 8 elements per thread
 __global__ void k_repeat_fwd(const uint16_t* __restrict__ v, int M, int H, int KV, int hd,
                              uint16_t* __restrict__ vr) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int i8 = blockIdx.x * blockDim.x + threadIdx.x;
   const int H8 = H / 8;
   if (i8 >= M * H8) return;
@@ -156,6 +166,8 @@ __global__ void k_repeat_fwd(const uint16_t* __restrict__ v, int M, int H, int K
 // 4 elements per thread
 __global__ void k_repeat_bwd(const float* __restrict__ dvr, int M, int H, int KV, int hd,
                              uint16_t* __restrict__ dv) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int i4 = blockIdx.x * blockDim.x + threadIdx.x;
   const int KV4 = KV / 4;
   if (i4 >= M * KV4) return;
@@ -176,6 +188,8 @@ __global__ void k_repeat_bwd(const float* __restrict__ dvr, int M, int H, int KV
 // out = h + float(y); 8 elements per thread
 __global__ void k_add_bf16(const float* __restrict__ h, const uint16_t* __restrict__ y, int64_t n,
                            float* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t i8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i8 * 8 >= n) return;
   const uint4 yv = reinterpret_cast<const uint4*>(y)[i8];
@@ -188,6 +202,8 @@ __global__ void k_add_bf16(const float* __restrict__ h, const uint16_t* __restri
 }
 
 __global__ void k_cast_bf16(const float* __restrict__ x, int64_t n, uint16_t* __restrict__ y) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t i8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i8 * 8 >= n) return;
   const float4 a = reinterpret_cast<const float4*>(x)[2 * i8];
@@ -201,6 +217,8 @@ constexpr int kLossBlocks = 256;
 __global__ void __launch_bounds__(256) k_loss_partial(const float* __restrict__ h, int64_t n,
                                                       float* __restrict__ partial,
                                                       float* __restrict__ dh, float inv_n) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float red[9];
   const int64_t per = (n + kLossBlocks - 1) / kLossBlocks;
   const int64_t b0 = (int64_t)blockIdx.x * per, b1 = min(n, b0 + per);
@@ -215,6 +233,8 @@ __global__ void __launch_bounds__(256) k_loss_partial(const float* __restrict__ 
 }
 __global__ void k_loss_final(const float* __restrict__ partial, float inv_n,
                              float* __restrict__ loss) {
+  pdl_wait();
+  pdl_launch_dependents();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   float s = 0.0f;
   for (int i = 0; i < kLossBlocks; ++i) s += partial[i];
@@ -235,6 +255,8 @@ WS_DEVINL void adam1(float& p, float g, float& m, float& v, float beta1, float b
 __global__ void k_adam(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
                        float* __restrict__ v, int64_t n, const uint32_t* __restrict__ step_dev,
                        float lr) {
+  pdl_wait();
+  pdl_launch_dependents();
   // bias corrections of this step, computed once by k_set_step
   const float step_size = lr * __uint_as_float(__ldg(step_dev + 2));
   const float bc2_sqrt = __uint_as_float(__ldg(step_dev + 3));
@@ -257,6 +279,8 @@ __global__ void k_adam(float* __restrict__ p, const float* __restrict__ g, float
 // The step word and, after it, Adam's bias corrections for step t = step + 1:
 // 1 / (1 - 0.9^t) and sqrt(1 - 0.999^t), computed in double, stored as fp32.
 __global__ void k_set_step(uint32_t* step_dev, uint32_t step) {
+  pdl_wait();
+  pdl_launch_dependents();
   const double t = (double)step + 1.0;
   step_dev[0] = step;
   step_dev[2] = __float_as_uint((float)(1.0 / (1.0 - pow(0.9, t))));
@@ -448,7 +472,7 @@ cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const
   float* h = at<float>(S, L.h);
   if (h != h_in) WS_TRY(cudaMemcpyAsync(h, h_in, (size_t)M * H * 4, cudaMemcpyDeviceToDevice, st));
   note_launch();
-  k_rmsnorm_fwd<<<(unsigned)M, 256, 0, st>>>(h, H, x.c.eps, at<uint16_t>(S, L.a), at<float>(S, L.rstd1));
+  (void)launch_pdl(k_rmsnorm_fwd, dim3((unsigned)M), dim3(256), 0, st, h, H, x.c.eps, at<uint16_t>(S, L.a), at<float>(S, L.rstd1));
   WS_TRY(cudaGetLastError());
   if (with_qk) {
     WS_TRY(lin(WS_LIN_Q, at<uint16_t>(S, L.a), at<uint16_t>(ws, x.WSL.qout)));
@@ -456,27 +480,27 @@ cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const
   }
   WS_TRY(lin(WS_LIN_V, at<uint16_t>(S, L.a), at<uint16_t>(S, L.v)));
   note_launch();
-  k_repeat_fwd<<<nblk(M * H / 8), 256, 0, st>>>(at<uint16_t>(S, L.v), (int)M, (int)H, (int)KV,
+  (void)launch_pdl(k_repeat_fwd, dim3(nblk(M * H / 8)), dim3(256), 0, st, at<uint16_t>(S, L.v), (int)M, (int)H, (int)KV,
                                                 (int)x.c.head_dim, at<uint16_t>(S, L.vr));
   WS_TRY(cudaGetLastError());
   uint16_t* y = at<uint16_t>(ws, x.WSL.yout);
   WS_TRY(lin(WS_LIN_O, at<uint16_t>(S, L.vr), y));
   note_launch();
-  k_add_bf16<<<nblk(M * H / 8), 256, 0, st>>>(h, y, M * H, at<float>(S, L.h1));
+  (void)launch_pdl(k_add_bf16, dim3(nblk(M * H / 8)), dim3(256), 0, st, h, y, M * H, at<float>(S, L.h1));
   WS_TRY(cudaGetLastError());
   note_launch();
-  k_rmsnorm_fwd<<<(unsigned)M, 256, 0, st>>>(at<float>(S, L.h1), H, x.c.eps, at<uint16_t>(S, L.b),
+  (void)launch_pdl(k_rmsnorm_fwd, dim3((unsigned)M), dim3(256), 0, st, at<float>(S, L.h1), H, x.c.eps, at<uint16_t>(S, L.b),
                                             at<float>(S, L.rstd2));
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_GATE, at<uint16_t>(S, L.b), at<uint16_t>(S, L.g)));
   WS_TRY(lin(WS_LIN_UP, at<uint16_t>(S, L.b), at<uint16_t>(S, L.u)));
   note_launch();
-  k_silu_mul_fwd<<<nblk(M * I / 8), 256, 0, st>>>(at<uint16_t>(S, L.g), at<uint16_t>(S, L.u), M * I,
+  (void)launch_pdl(k_silu_mul_fwd, dim3(nblk(M * I / 8)), dim3(256), 0, st, at<uint16_t>(S, L.g), at<uint16_t>(S, L.u), M * I,
                                               at<uint16_t>(S, L.act));
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_DOWN, at<uint16_t>(S, L.act), y));
   note_launch();
-  k_add_bf16<<<nblk(M * H / 8), 256, 0, st>>>(at<float>(S, L.h1), y, M * H, h_out);
+  (void)launch_pdl(k_add_bf16, dim3(nblk(M * H / 8)), dim3(256), 0, st, at<float>(S, L.h1), y, M * H, h_out);
   return cudaGetLastError();
 }
 
@@ -506,29 +530,29 @@ cudaError_t layer_bwd(const Ctx& x, const void* block, int lib, int layer, const
   uint16_t* dv = at<uint16_t>(ws, x.WSL.dv);
 
   note_launch();
-  k_cast_bf16<<<nblk(M * H / 8), 256, 0, st>>>(dh, M * H, y1);
+  (void)launch_pdl(k_cast_bf16, dim3(nblk(M * H / 8)), dim3(256), 0, st, dh, M * H, y1);
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_DOWN, at<const uint16_t>(S, L.act), y1, dact, 0));
   note_launch();
-  k_silu_mul_bwd<<<nblk(M * I / 8), 256, 0, st>>>(dact, at<const uint16_t>(S, L.g),
+  (void)launch_pdl(k_silu_mul_bwd, dim3(nblk(M * I / 8)), dim3(256), 0, st, dact, at<const uint16_t>(S, L.g),
                                               at<const uint16_t>(S, L.u), M * I, dg, du);
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_GATE, at<const uint16_t>(S, L.b), dg, db, 0));
   WS_TRY(lin(WS_LIN_UP, at<const uint16_t>(S, L.b), du, db, 1));
   note_launch();
-  k_rmsnorm_bwd<<<(unsigned)M, 256, 0, st>>>(at<const float>(S, L.h1), at<const float>(S, L.rstd2),
+  (void)launch_pdl(k_rmsnorm_bwd, dim3((unsigned)M), dim3(256), 0, st, at<const float>(S, L.h1), at<const float>(S, L.rstd2),
                                              db, H, dh);
   WS_TRY(cudaGetLastError());
   note_launch();
-  k_cast_bf16<<<nblk(M * H / 8), 256, 0, st>>>(dh, M * H, y1);
+  (void)launch_pdl(k_cast_bf16, dim3(nblk(M * H / 8)), dim3(256), 0, st, dh, M * H, y1);
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_O, at<const uint16_t>(S, L.vr), y1, dvr, 0));
   note_launch();
-  k_repeat_bwd<<<nblk(M * KV / 4), 256, 0, st>>>(dvr, (int)M, (int)H, (int)KV, (int)x.c.head_dim, dv);
+  (void)launch_pdl(k_repeat_bwd, dim3(nblk(M * KV / 4)), dim3(256), 0, st, dvr, (int)M, (int)H, (int)KV, (int)x.c.head_dim, dv);
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_V, at<const uint16_t>(S, L.a), dv, db, 0));
   note_launch();
-  k_rmsnorm_bwd<<<(unsigned)M, 256, 0, st>>>(at<const float>(S, L.h), at<const float>(S, L.rstd1),
+  (void)launch_pdl(k_rmsnorm_bwd, dim3((unsigned)M), dim3(256), 0, st, at<const float>(S, L.h), at<const float>(S, L.rstd1),
                                              db, H, dh);
   WS_TRY(cudaGetLastError());
   // q and k feed only the replaced attention core: exactly zero gradient
@@ -661,23 +685,23 @@ cudaError_t loss_and_grad(const ws_stack_cfg& c, int block_layers_ws, const floa
   float* part = at<float>(ws, L.lossp);
   const float inv_n = (float)(1.0 / (double)n);
   note_launch();
-  k_loss_partial<<<kLossBlocks, 256, 0, st>>>(h, n, part, dh, inv_n);
+  (void)launch_pdl(k_loss_partial, dim3(kLossBlocks), dim3(256), 0, st, h, n, part, dh, inv_n);
   WS_TRY(cudaGetLastError());
   note_launch();
-  k_loss_final<<<1, 32, 0, st>>>(part, inv_n, loss);
+  (void)launch_pdl(k_loss_final, dim3(1), dim3(32), 0, st, part, inv_n, loss);
   return cudaGetLastError();
 }
 
 cudaError_t adam_step(float* p, const float* g, float* m, float* v, int64_t n,
                       const uint32_t* step_dev, float lr, cudaStream_t st) {
   note_launch();
-  k_adam<<<nblk(n / 4), 256, 0, st>>>(p, g, m, v, n, step_dev, lr);
+  (void)launch_pdl(k_adam, dim3(nblk(n / 4)), dim3(256), 0, st, p, g, m, v, n, step_dev, lr);
   return cudaGetLastError();
 }
 
 cudaError_t set_step(uint32_t* step_dev, uint32_t step, cudaStream_t st) {
   note_launch();
-  k_set_step<<<1, 1, 0, st>>>(step_dev, step);
+  (void)launch_pdl(k_set_step, dim3(1), dim3(1), 0, st, step_dev, step);
   return cudaGetLastError();
 }
 
