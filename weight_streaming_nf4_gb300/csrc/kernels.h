@@ -19,6 +19,10 @@ struct NF4View {
   int64_t N, K;
 };
 
+// Linears of one grouped launch at most (q, k, v share the attention
+// input; gate and up share the MLP input).
+constexpr int kMaxGroups = 3;
+
 // Arguments of one dequant-GEMM launch (see nf4_gemm.cu).
 struct GemmArgs {
   int64_t M;            // activation rows
@@ -39,6 +43,18 @@ struct GemmArgs {
   const float* absmax;  // the weight's block scales [K/64, N]
   int64_t wN, wK;       // the weight's shape
   int epad;             // schedule-only steps charged per tile (see GemmPlan::epad)
+  // Forward only: ngroups linears that read the same activation, side by
+  // side along the output columns.  Group g owns output columns
+  // [gcol[g], gcol[g+1]) (multiples of the tile width), with its own weight
+  // (gcodes, gabsmax; wN = its width), LoRA factor glora_F, output gout
+  // (row pitch = its width) and LoRA activation rows [g*M, (g+1)*M) of the
+  // lora map.  ngroups = 1 uses codes / absmax / lora_F / out above.
+  int ngroups;
+  int64_t gcol[kMaxGroups + 1];
+  const uint8_t* gcodes[kMaxGroups];
+  const float* gabsmax[kMaxGroups];
+  const float* glora_F[kMaxGroups];
+  void* gout[kMaxGroups];
 };
 
 // Tile configuration: a pure function of the shape and the SM count, so a
@@ -77,6 +93,15 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
                          const uint32_t* mask, void* out, int out_f32, int out_accum,
                          float* partial, cudaStream_t st);
 
+// Forward of ng linears sharing the activation act [M, K] in one launch:
+// out[g] = act . W[g]'^T + s * lora_act[g] . F[g]^T, lora_act [ng][M][64]
+// contiguous.  p = plan_gemm(false, M, sum of widths, K); every width a
+// multiple of p.bn (else cudaErrorInvalidValue).
+cudaError_t run_nf4_gemm_group(const GemmPlan& p, int ng, const NF4View* W, const uint16_t* act,
+                               int64_t M, const uint16_t* lora_act, const float* const* lora_F,
+                               float lora_scale, uint16_t* const* out, float* partial,
+                               cudaStream_t st);
+
 // ---- small kernels (lora_small.cu) ----------------------------------------------------
 struct DropKeyHost {
   uint32_t k0, k1, c1, c2, c3, thresh, drop_all;
@@ -94,6 +119,13 @@ size_t skinny_partial_bytes(int64_t M, int64_t K);
 cudaError_t run_skinny_tc(const uint16_t* X, const float* F, bool f_kj, int64_t M, int64_t K,
                           const DropKey* key, uint8_t* mask_bytes, float* partial, float* out,
                           uint16_t* ext, cudaStream_t st);
+// The same for ng <= kMaxGroups factors F[g] ([16][K], A layout) applied to
+// one X under ng dropout masks (keys[g]) in one launch: out[g], ext[g],
+// mask_bytes[g] (entries may be NULL), partial[g] (skinny_partial_bytes each).
+cudaError_t run_skinny_tc_group(const uint16_t* X, int ng, const float* const* F, int64_t M,
+                                int64_t K, const DropKey* keys, uint8_t* const* mask_bytes,
+                                float* const* partial, float* const* out, uint16_t* const* ext,
+                                cudaStream_t st);
 // U = (mask . x) A^T [M,16] fp32; Uext [M,64] bf16 hi/lo; mask bits (optional).
 cudaError_t run_lora_down(const uint16_t* x, const float* A, int64_t M, int64_t K,
                           const DropKeyHost& key, float* U, uint16_t* Uext, uint32_t* mask_out,
@@ -118,6 +150,13 @@ size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t linear_fwd(const NF4View& W, const uint16_t* x, const float* A, const float* B,
                        int64_t M, float scale, const DropKeyHost& key, uint16_t* y, float* U,
                        uint32_t* mask, void* ws, cudaStream_t st);
+// ng linears reading the same x: one LoRA-down launch, one GEMM for the
+// first ng_gemm of them and one GEMM for each of the others.
+size_t linear_group_workspace_bytes(int64_t M, int ng, const int64_t* N, int64_t K);
+cudaError_t linear_fwd_group(int ng, int ng_gemm, const NF4View* W, const uint16_t* x, const float* const* A,
+                             const float* const* B, int64_t M, float scale, const DropKeyHost* keys,
+                             uint16_t* const* y, float* const* U, uint32_t* const* mask, void* ws,
+                             cudaStream_t st);
 cudaError_t linear_bwd(const NF4View& W, const uint16_t* x, const float* A, const float* B,
                        int64_t M, float scale, const DropKeyHost& key, const float* U,
                        const uint32_t* mask, const uint16_t* dY, void* dX, int dX_f32,

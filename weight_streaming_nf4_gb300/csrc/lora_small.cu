@@ -186,6 +186,103 @@ cudaError_t linear_fwd(const NF4View& W, const uint16_t* x, const float* A, cons
                       reinterpret_cast<float*>(w + L.split), st);
 }
 
+// ------------------------------------------------------------------------ linears sharing x
+// Workspace of a group (each piece 256-aligned):
+//   ext     [ng][M][64] bf16   U split factors, contiguous (one TMA map)
+//   skinny  ng x skinny_partial_bytes(M, K)
+//   split   max over the grouped plan and the one-launch-per-linear plans
+namespace {
+struct GrpWs {
+  size_t ext, skinny, skinny_each, split, total;
+};
+GrpWs grp_ws_layout(int64_t M, int ng, const int64_t* N, int64_t K) {
+  GrpWs w{};
+  size_t off = 0;
+  w.ext = off;
+  off += align256((size_t)ng * (size_t)M * 64 * 2);
+  w.skinny = off;
+  w.skinny_each = align256(skinny_partial_bytes(M, K));
+  off += (size_t)ng * w.skinny_each;
+  w.split = off;
+  int64_t Nsum = 0;
+  size_t sp = 0;
+  for (int g = 0; g < ng; ++g) {
+    Nsum += N[g];
+    const size_t b = gemm_partial_bytes(plan_gemm(false, M, N[g], K), M, N[g]);
+    if (b > sp) sp = b;
+  }
+  (void)Nsum;
+  int64_t Npre = N[0];
+  for (int g = 1; g < ng; ++g) {
+    Npre += N[g];
+    const size_t b = gemm_partial_bytes(plan_gemm(false, M, Npre, K), M, Npre);
+    if (b > sp) sp = b;
+  }
+  off += align256(sp);
+  w.total = off;
+  return w;
+}
+}  // namespace
+
+size_t linear_group_workspace_bytes(int64_t M, int ng, const int64_t* N, int64_t K) {
+  return grp_ws_layout(M, ng, N, K).total;
+}
+
+// One LoRA-down launch for all ng linears (ng dropout masks of the same x;
+// each linear's U, bits and split factor are the same as from its own
+// launch), then one GEMM over the concatenated output columns of the first
+// ng_gemm linears and one GEMM per remaining linear (whose result then
+// equals a lone forward of that linear bit for bit).  A width that is not a
+// multiple of the grouped plan's tile width falls back to one GEMM per
+// linear.
+cudaError_t linear_fwd_group(int ng, int ng_gemm, const NF4View* W, const uint16_t* x, const float* const* A,
+                             const float* const* B, int64_t M, float scale, const DropKeyHost* keys,
+                             uint16_t* const* y, float* const* U, uint32_t* const* mask, void* ws,
+                             cudaStream_t st) {
+  if (ng < 1 || ng > kMaxGroups || ng_gemm < 0 || ng_gemm > ng) return cudaErrorInvalidValue;
+  const int64_t K = W[0].K;
+  int64_t N[kMaxGroups];
+  int64_t Nsum = 0;
+  for (int g = 0; g < ng; ++g) {
+    if (W[g].K != K) return cudaErrorInvalidValue;
+    N[g] = W[g].N;
+    Nsum += N[g];
+  }
+  const GrpWs L = grp_ws_layout(M, ng, N, K);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* ext = reinterpret_cast<uint16_t*>(w + L.ext);
+  float* split = reinterpret_cast<float*>(w + L.split);
+  DropKey dk[kMaxGroups];
+  uint16_t* exts[kMaxGroups];
+  float* parts[kMaxGroups];
+  uint8_t* mb[kMaxGroups];
+  for (int g = 0; g < ng; ++g) {
+    dk[g] = to_dev(keys[g]);
+    exts[g] = ext + (size_t)g * (size_t)M * 64;
+    parts[g] = reinterpret_cast<float*>(w + L.skinny + (size_t)g * L.skinny_each);
+    mb[g] = reinterpret_cast<uint8_t*>(mask[g]);
+  }
+  cudaError_t e = run_skinny_tc_group(x, ng, A, M, K, dk, mb, parts, U, exts, st);
+  if (e != cudaSuccess) return e;
+  int first_single = 0;
+  if (ng_gemm > 1) {
+    int64_t Ng = 0;
+    for (int g = 0; g < ng_gemm; ++g) Ng += N[g];
+    const GemmPlan p = plan_gemm(false, M, Ng, K);
+    bool fits = true;
+    for (int g = 0; g < ng_gemm; ++g) fits = fits && (N[g] % p.bn == 0);
+    if (fits) {
+      e = run_nf4_gemm_group(p, ng_gemm, W, x, M, ext, B, scale, y, split, st);
+      if (e != cudaSuccess) return e;
+      first_single = ng_gemm;
+    }
+  }
+  for (int g = first_single; g < ng && e == cudaSuccess; ++g)
+    e = run_nf4_gemm(plan_gemm(false, M, N[g], K), W[g], x, M, exts[g], B[g], scale, nullptr, y[g],
+                     0, 0, split, st);
+  return e;
+}
+
 cudaError_t linear_bwd(const NF4View& W, const uint16_t* x, const float* A, const float* B,
                        int64_t M, float scale, const DropKeyHost& key, const float* U,
                        const uint32_t* mask, const uint16_t* dY, void* dX, int dX_f32,

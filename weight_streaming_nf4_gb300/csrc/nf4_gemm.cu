@@ -40,6 +40,7 @@
 // accumulator serves both terms.
 #define WS_GEMM_TU 1
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -276,21 +277,22 @@ WS_DEVINL void cp_async_v(uint32_t dst, const void* src, bool in) {
 // contraction index) and 2*VB weight columns (the output index).
 // Rows / columns past the weight's edge read as zero codes with scale 0.
 template <bool BWD, int BN, int PAIR>
-WS_DEVINL void fetch_codes(uint32_t slot, const GemmArgs& g, int i, int n0, int rank, int t) {
+WS_DEVINL void fetch_codes(uint32_t slot, const uint8_t* codes, const float* absmax, int64_t wN,
+                           int64_t wK, int i, int64_t n0, int rank, int t) {
   using D = DqGeo<BWD, BN, PAIR>;
-  const int64_t kb = g.wK / 2;  // code bytes per weight row
+  const int64_t kb = wK / 2;  // code bytes per weight row
   const int c0 = PAIR ? rank * D::COLS : 0;
   const uint32_t sc = slot + (uint32_t)(D::NV * kDqThreads * D::VB);
   if constexpr (!BWD) {
     const int j = c0 + t / D::TPR, part = t % D::TPR;
     const int64_t n = (int64_t)n0 + j;
-    const bool in = n < g.wN;
+    const bool in = n < wN;
     const int64_t nn = in ? n : 0;
-    const uint8_t* src = g.codes + nn * kb + (int64_t)i * 32 + part * (32 / D::TPR);
+    const uint8_t* src = codes + nn * kb + (int64_t)i * 32 + part * (32 / D::TPR);
 #pragma unroll
     for (int v = 0; v < D::NV; ++v)
       cp_async_v<D::VB>(slot + (uint32_t)((v * kDqThreads + t) * D::VB), src + D::VB * v, in);
-    cp_async4(sc + (uint32_t)(t * 4), g.absmax + (int64_t)i * g.wN + nn, in ? 4u : 0u);
+    cp_async4(sc + (uint32_t)(t * 4), absmax + (int64_t)i * wN + nn, in ? 4u : 0u);
   } else {
     constexpr int SEGS = D::COLS / (2 * D::VB);
 #pragma unroll
@@ -299,11 +301,11 @@ WS_DEVINL void fetch_codes(uint32_t slot, const GemmArgs& g, int i, int n0, int 
       const int c = item / SEGS, seg = item % SEGS;
       const int64_t r = (int64_t)i * 64 + c;
       const int64_t col = (int64_t)n0 + c0 + seg * 2 * D::VB;
-      const bool in = r < g.wN && col < g.wK;
+      const bool in = r < wN && col < wK;
       const int64_t rr = in ? r : 0, cl = in ? col : 0;
       cp_async_v<D::VB>(slot + (uint32_t)((it * kDqThreads + t) * D::VB),
-                        g.codes + rr * kb + cl / 2, in);
-      cp_async4(sc + (uint32_t)((it * kDqThreads + t) * 4), g.absmax + (cl / 64) * g.wN + rr,
+                        codes + rr * kb + cl / 2, in);
+      cp_async4(sc + (uint32_t)((it * kDqThreads + t) * 4), absmax + (cl / 64) * wN + rr,
                 in ? 4u : 0u);
     }
   }
@@ -413,6 +415,43 @@ WS_DEVINL void lora_tile(const float* F, int64_t rows_total, int64_t ld, int n0,
     else val = make_uint4(0u, 0u, 0u, 0u);
     sts128(Bt + j * 128 + ((cc ^ (j & 7)) << 4), val.x, val.y, val.z, val.w);
   }
+}
+
+// The linear a forward tile belongs to (grouped launches; see GemmArgs):
+// selected with compares, so the parameter arrays are never indexed at run
+// time.
+struct TileGrp {
+  const uint8_t* codes;
+  const float* absmax;
+  const float* lora_F;
+  void* out;
+  int64_t c0;     // first output column of the group
+  int64_t width;  // its output columns (its weight's N; row pitch of its output)
+  int g;
+};
+WS_DEVINL TileGrp tile_grp(const GemmArgs& a, int64_t n0) {
+  TileGrp r;
+  if (a.ngroups <= 1) {
+    r.codes = a.codes;
+    r.absmax = a.absmax;
+    r.lora_F = a.lora_F;
+    r.out = a.out;
+    r.c0 = 0;
+    r.width = a.Nout;
+    r.g = 0;
+    return r;
+  }
+  const bool g1 = n0 >= a.gcol[1];
+  const bool g2 = a.ngroups > 2 && n0 >= a.gcol[2];
+  r.g = g2 ? 2 : (g1 ? 1 : 0);
+  r.codes = g2 ? a.gcodes[2] : (g1 ? a.gcodes[1] : a.gcodes[0]);
+  r.absmax = g2 ? a.gabsmax[2] : (g1 ? a.gabsmax[1] : a.gabsmax[0]);
+  r.lora_F = g2 ? a.glora_F[2] : (g1 ? a.glora_F[1] : a.glora_F[0]);
+  r.out = g2 ? a.gout[2] : (g1 ? a.gout[1] : a.gout[0]);
+  r.c0 = g2 ? a.gcol[2] : (g1 ? a.gcol[1] : 0);
+  const int64_t c1 = g2 ? a.gcol[3] : (g1 ? a.gcol[2] : a.gcol[1]);
+  r.width = c1 - r.c0;
+  return r;
 }
 
 // Position of a (tile, step) iteration: step i of tile (mt, nt).
@@ -575,13 +614,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m0 = ps.mt * UROWS + rank * C::BM;
           const CUtensorMap* map = is_lora_step(ps.i) ? &tmL : &tmA;
           const int32_t x = is_lora_step(ps.i) ? 0 : kstep(ps.i) * 64;
+          // a grouped forward's LoRA activation rows of group g start at g * M
+          const int32_t y = m0 + ((!BWD && is_lora_step(ps.i)) ? (int32_t)(tile_grp(args, (int64_t)ps.nt * BN).g * args.M) : 0);
           if constexpr (PM) {
             // both CTAs' tiles complete on the even CTA's barrier
             if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::A_BYTES);
-            tma_load_2d_pair(sA + s * C::A_BYTES, map, mapa_shared(smem_u32(&full[s]), 0u), x, m0);
+            tma_load_2d_pair(sA + s * C::A_BYTES, map, mapa_shared(smem_u32(&full[s]), 0u), x, y);
           } else {
             mbar_arrive_expect_tx(&full[s], C::A_BYTES);
-            tma_load_2d(sA + s * C::A_BYTES, map, &full[s], x, m0);
+            tma_load_2d(sA + s * C::A_BYTES, map, &full[s], x, y);
           }
           issued = q + 1;
           if (++s == STAGES) {
@@ -728,9 +769,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       Pos pf = pos0;  // position of the next fetch
       int64_t fq = 0;
       auto fetch = [&]() {
-        if (fq < n_it && !is_lora_step(pf.i))
-          fetch_codes<BWD, BN, PAIR>(smem_u32(ring + (fq % CS) * C::CODE_BYTES), args,
-                                     kstep(pf.i), pf.nt * BN, rank, t_idx);
+        if (fq < n_it && !is_lora_step(pf.i)) {
+          const uint32_t slot = smem_u32(ring + (fq % CS) * C::CODE_BYTES);
+          const int64_t nb = (int64_t)pf.nt * BN;
+          if constexpr (BWD) {
+            fetch_codes<BWD, BN, PAIR>(slot, args.codes, args.absmax, args.wN, args.wK,
+                                       kstep(pf.i), nb, rank, t_idx);
+          } else {
+            const TileGrp tg = tile_grp(args, nb);
+            fetch_codes<BWD, BN, PAIR>(slot, tg.codes, tg.absmax, tg.width, args.wK, kstep(pf.i),
+                                       nb - tg.c0, rank, t_idx);
+          }
+        }
         cp_async_commit();
         pf.next(S, args.mtiles);
         ++fq;
@@ -755,8 +805,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!BWD) dequant_fwd<BN, PAIR>(cur, Bt, rank, t_idx);
           else dequant_bwd<BN, PAIR>(cur, Bt, rank, t_idx);
         } else {
-          lora_tile<BWD, BN, PAIR>(args.lora_F, args.Nout, args.Nout, pc.nt * BN, args.lora_scale,
-                                   Bt, rank, t_idx);
+          const TileGrp tg = tile_grp(args, (int64_t)pc.nt * BN);
+          lora_tile<BWD, BN, PAIR>(tg.lora_F, tg.width, tg.width, (int)((int64_t)pc.nt * BN - tg.c0),
+                                   args.lora_scale, Bt, rank, t_idx);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -916,8 +967,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t dbase = tmem + (uint32_t)(a * C::ACC_COLS);
         // 16-column chunks of this warp's columns that lie inside the output
+        // (of this tile's linear, for a grouped forward)
+        const TileGrp og = tile_grp(args, n0);
         constexpr int KCH = (BN / 2) / 16;
-        const int64_t cols_left = args.Nout - (n0 + half * (BN / 2));
+        const int64_t cols_left = og.width - (n0 - og.c0 + half * (BN / 2));
         const int kv = cols_left <= 0 ? 0 : (cols_left >= KCH * 16 ? KCH : (int)((cols_left + 15) / 16));
         // A finisher's segment is its unit's last, so the main loop's shared
         // memory is idle: the later pieces stream through a per-warp ring of
@@ -982,9 +1035,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               r_issue();
             }
             if (!row_ok) continue;
+            const int64_t o_off = m * og.width + (n - og.c0);
             if (args.out_f32) {
-              float4* dst =
-                  reinterpret_cast<float4*>(static_cast<float*>(args.out) + m * args.Nout + n);
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(og.out) + o_off);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 float4 o = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
@@ -998,8 +1051,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dst[e] = o;
               }
             } else {
-              uint4* dst =
-                  reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.out) + m * args.Nout + n);
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(og.out) + o_off);
 #pragma unroll
               for (int e = 0; e < 2; ++e)
                 dst[e] = make_uint4(pack_bf16x2(v[8 * e], v[8 * e + 1]),
@@ -1306,14 +1358,43 @@ constexpr uint32_t kSkB = 64 * 128;     // B operand: 48 rows used of 64
 constexpr uint32_t kSkSmem =
     kSkStages * (kSkX + kSkF + kSkB) + (3 * kSkStages + 1) * 8 + 16 + 1024;
 
+// Launch parameters: one X for every group; group g = blockIdx.z has its
+// own factor, dropout key and outputs (linears that read the same input run
+// in one launch).
+struct SkArgs {
+  CUtensorMap tmX;
+  CUtensorMap tmF[kMaxGroups];  // A factors [16][K] fp32 (F_KJ = false)
+  const float* F[kMaxGroups];
+  DropKey key[kMaxGroups];
+  uint8_t* mask_bytes[kMaxGroups];
+  float* partial[kMaxGroups];
+  uint32_t* counters[kMaxGroups];
+  float* out[kMaxGroups];
+  uint16_t* ext[kMaxGroups];
+  int64_t M, K;
+  int steps_per_chunk;
+};
+// Element g of a parameter array, chosen with compares (no run-time indexing).
+template <class T>
+WS_DEVINL T pick_group(const T (&a)[kMaxGroups], int g) {
+  return g == 2 ? a[2] : (g == 1 ? a[1] : a[0]);
+}
+
 // F_KJ: the factor is given as [K][16] (B), else as [16][K] (A).
 template <bool MASKED, bool F_KJ>
-__global__ void __launch_bounds__(kSkThreads, 1)
-    k_skinny_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmF,
-                const float* __restrict__ F, int64_t M, int64_t K, int steps_per_chunk,
-                DropKey key, uint8_t* __restrict__ mask_bytes, float* __restrict__ partial,
-                uint32_t* __restrict__ counters, float* __restrict__ out,
-                uint16_t* __restrict__ ext) {
+__global__ void __launch_bounds__(kSkThreads, 1) k_skinny_tc(const __grid_constant__ SkArgs sa) {
+  const int grp = (int)blockIdx.z;
+  const CUtensorMap* tmX = &sa.tmX;
+  const CUtensorMap* tmF = grp == 2 ? &sa.tmF[2] : (grp == 1 ? &sa.tmF[1] : &sa.tmF[0]);
+  const float* __restrict__ F = pick_group(sa.F, grp);
+  DropKey key = pick_group(sa.key, grp);
+  uint8_t* __restrict__ mask_bytes = pick_group(sa.mask_bytes, grp);
+  float* __restrict__ partial = pick_group(sa.partial, grp);
+  uint32_t* __restrict__ counters = pick_group(sa.counters, grp);
+  float* __restrict__ out = pick_group(sa.out, grp);
+  uint16_t* __restrict__ ext = pick_group(sa.ext, grp);
+  const int64_t M = sa.M, K = sa.K;
+  const int steps_per_chunk = sa.steps_per_chunk;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1375,9 +1456,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
           }
           const int k0 = (int)((s_begin + i) * 64);
           mbar_arrive_expect_tx(&full[st], kSkX + kSkF);
-          tma_load_2d(sX + st * kSkX, &tmX, &full[st], k0, (int)m0);
+          tma_load_2d(sX + st * kSkX, tmX, &full[st], k0, (int)m0);
           if (F_KJ) bulk_load(sF + st * kSkF, F + (int64_t)k0 * 16, kSkF, &full[st]);
-          else tma_load_2d(sF + st * kSkF, &tmF, &full[st], k0, 0);
+          else tma_load_2d(sF + st * kSkF, tmF, &full[st], k0, 0);
           issued = i + 1;
         }
         if (*abort_flag)
@@ -1845,6 +1926,37 @@ size_t gemm_partial_bytes(const GemmPlan& p, int64_t M, int64_t Nout) {
   return (size_t)G * (size_t)(128 * p.um) * (size_t)p.bn * sizeof(float);
 }
 
+namespace {
+// The kernel instantiation of a plan.
+cudaError_t dispatch_gemm(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& tA,
+                          const CUtensorMap& tL, cudaStream_t st) {
+  const bool pm = pair_mode() == 2;
+  if (!p.bwd) {
+    if (p.pair && pm) {
+      if (p.bn == 256) return launch_cfg<false, 2, 256, 2>(p, a, tA, tL, st);
+      return launch_cfg<false, 2, 128, 2>(p, a, tA, tL, st);
+    }
+    if (p.pair) {
+      if (p.bn == 256) return launch_cfg<false, 2, 256, 1>(p, a, tA, tL, st);
+      return launch_cfg<false, 2, 128, 1>(p, a, tA, tL, st);
+    }
+    if (p.um == 2 && p.bn == 256) return launch_cfg<false, 2, 256, 0>(p, a, tA, tL, st);
+    if (p.um == 2) return launch_cfg<false, 2, 128, 0>(p, a, tA, tL, st);
+    return launch_cfg<false, 1, 128, 0>(p, a, tA, tL, st);
+  }
+  if (p.pair && pm) {
+    if (p.bn == 256) return launch_cfg<true, 2, 256, 2>(p, a, tA, tL, st);
+    return launch_cfg<true, 2, 128, 2>(p, a, tA, tL, st);
+  }
+  if (p.pair) {
+    if (p.bn == 256) return launch_cfg<true, 2, 256, 1>(p, a, tA, tL, st);
+    return launch_cfg<true, 2, 128, 1>(p, a, tA, tL, st);
+  }
+  if (p.um == 2) return launch_cfg<true, 2, 128, 0>(p, a, tA, tL, st);
+  return launch_cfg<true, 1, 128, 0>(p, a, tA, tL, st);
+}
+}  // namespace
+
 cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* act, int64_t M,
                          const uint16_t* lora_act, const float* lora_F, float lora_scale,
                          const uint32_t* mask, void* out, int out_f32, int out_accum,
@@ -1891,30 +2003,59 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
   }
 
   if (partial == nullptr && grid_units(p, has_lora) > 1) return cudaErrorInvalidValue;
-  const bool pm = pair_mode() == 2;
-  if (!p.bwd) {
-    if (p.pair && pm) {
-      if (p.bn == 256) return launch_cfg<false, 2, 256, 2>(p, a, tA, tL, st);
-      return launch_cfg<false, 2, 128, 2>(p, a, tA, tL, st);
-    }
-    if (p.pair) {
-      if (p.bn == 256) return launch_cfg<false, 2, 256, 1>(p, a, tA, tL, st);
-      return launch_cfg<false, 2, 128, 1>(p, a, tA, tL, st);
-    }
-    if (p.um == 2 && p.bn == 256) return launch_cfg<false, 2, 256, 0>(p, a, tA, tL, st);
-    if (p.um == 2) return launch_cfg<false, 2, 128, 0>(p, a, tA, tL, st);
-    return launch_cfg<false, 1, 128, 0>(p, a, tA, tL, st);
+  return dispatch_gemm(p, a, tA, tL, st);
+}
+
+cudaError_t run_nf4_gemm_group(const GemmPlan& p, int ng, const NF4View* W, const uint16_t* act,
+                               int64_t M, const uint16_t* lora_act, const float* const* lora_F,
+                               float lora_scale, uint16_t* const* out, float* partial,
+                               cudaStream_t st) {
+  if (!encode_fn()) return cudaErrorNotSupported;
+  if (ng < 1 || ng > kMaxGroups || p.bwd || lora_act == nullptr) return cudaErrorInvalidValue;
+  const int64_t K = W[0].K;
+  GemmArgs a{};
+  a.ngroups = ng;
+  a.gcol[0] = 0;
+  for (int g = 0; g < ng; ++g) {
+    if (W[g].K != K || W[g].N % p.bn != 0) return cudaErrorInvalidValue;
+    a.gcol[g + 1] = a.gcol[g] + W[g].N;
+    a.gcodes[g] = W[g].codes;
+    a.gabsmax[g] = W[g].absmax;
+    a.glora_F[g] = lora_F[g];
+    a.gout[g] = out[g];
   }
-  if (p.pair && pm) {
-    if (p.bn == 256) return launch_cfg<true, 2, 256, 2>(p, a, tA, tL, st);
-    return launch_cfg<true, 2, 128, 2>(p, a, tA, tL, st);
+  const int64_t Nsum = a.gcol[ng];
+  // group 0 also fills the single-linear fields (ng = 1 reads those)
+  a.codes = W[0].codes;
+  a.absmax = W[0].absmax;
+  a.lora_F = lora_F[0];
+  a.out = out[0];
+  a.wN = W[0].N;
+  if (p.ntiles != (int)(Nsum / p.bn) || p.nk != (int)(K / 64)) return cudaErrorInvalidValue;
+  const int BM = 128 * p.um;
+  CUtensorMap tA, tL;
+  bool ok = make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, (uint64_t)K, (uint64_t)M,
+                     (uint64_t)K * 2, 64, (uint32_t)BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&tL, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lora_act, 64, (uint64_t)(ng * M), 128,
+                      64, (uint32_t)BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
+  a.M = M;
+  a.Nout = Nsum;
+  a.nk_total = p.nk;
+  a.mtiles = p.mtiles;
+  a.ntiles = p.ntiles;
+  a.has_lora = 1;
+  a.lora_scale = lora_scale;
+  a.partial = partial;
+  a.wK = K;
+  a.epad = p.epad;
+  a.flags = nullptr;
+  if (grid_units(p, true) > 1) {
+    cudaError_t e = ring_slots((uint32_t)grid_ctas(p, true), &a.flags);
+    if (e != cudaSuccess) return e;
+    if (partial == nullptr) return cudaErrorInvalidValue;
   }
-  if (p.pair) {
-    if (p.bn == 256) return launch_cfg<true, 2, 256, 1>(p, a, tA, tL, st);
-    return launch_cfg<true, 2, 128, 1>(p, a, tA, tL, st);
-  }
-  if (p.um == 2) return launch_cfg<true, 2, 128, 0>(p, a, tA, tL, st);
-  return launch_cfg<true, 1, 128, 0>(p, a, tA, tL, st);
+  return dispatch_gemm(p, a, tA, tL, st);
 }
 
 // ------------------------------------------------------------------------ skinny products (host)
@@ -1984,28 +2125,43 @@ cudaError_t ring_clear() {
   return cudaMemset(base, 0, (size_t)kRingWords * sizeof(uint32_t));
 }
 
-cudaError_t run_skinny_tc(const uint16_t* X, const float* F, bool f_kj, int64_t M, int64_t K,
-                          const DropKey* key, uint8_t* mask_bytes, float* partial, float* out,
-                          uint16_t* ext, cudaStream_t st) {
+namespace {
+cudaError_t skinny_launch(const uint16_t* X, int ng, const float* const* F, bool f_kj, int64_t M,
+                          int64_t K, const DropKey* keys, uint8_t* const* mask_bytes,
+                          float* const* partial, float* const* out, uint16_t* const* ext,
+                          cudaStream_t st) {
   if (!encode_fn()) return cudaErrorNotSupported;
-  if (K % 64 != 0 || M < 1) return cudaErrorInvalidValue;
-  // the factor slices are fetched with 16-byte copies
-  if ((reinterpret_cast<uintptr_t>(F) & 15u) != 0u) return cudaErrorInvalidValue;
+  if (K % 64 != 0 || M < 1 || ng < 1 || ng > kMaxGroups) return cudaErrorInvalidValue;
   const int64_t atoms = (M + 127) / 128;
   const int chunks = skinny_tc_chunks(M, K);
   const int64_t steps = K / 64;
   const int spc = (int)((steps + chunks - 1) / chunks);
   uint32_t* counters = nullptr;
-  cudaError_t e = ring_slots((uint32_t)atoms, &counters);
+  cudaError_t e = ring_slots((uint32_t)(atoms * ng), &counters);
   if (e != cudaSuccess) return e;
-  CUtensorMap tX, tF;
-  if (!make_map(&tX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2,
-                64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+  SkArgs sa;
+  memset(&sa, 0, sizeof(sa));
+  if (!make_map(&sa.tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)K, (uint64_t)M,
+                (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  if (f_kj) tF = tX;
-  else if (!make_map(&tF, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, F, (uint64_t)K, 16, (uint64_t)K * 4, 64,
-                     16, CU_TENSOR_MAP_SWIZZLE_NONE))
-    return cudaErrorInvalidValue;
+  for (int g = 0; g < ng; ++g) {
+    // the factor slices are fetched with 16-byte copies
+    if ((reinterpret_cast<uintptr_t>(F[g]) & 15u) != 0u) return cudaErrorInvalidValue;
+    if (f_kj) sa.tmF[g] = sa.tmX;
+    else if (!make_map(&sa.tmF[g], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, F[g], (uint64_t)K, 16,
+                       (uint64_t)K * 4, 64, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    sa.F[g] = F[g];
+    if (keys) sa.key[g] = keys[g];
+    sa.mask_bytes[g] = mask_bytes ? mask_bytes[g] : nullptr;
+    sa.partial[g] = partial[g];
+    sa.counters[g] = counters + g * atoms;
+    sa.out[g] = out[g];
+    sa.ext[g] = ext[g];
+  }
+  sa.M = M;
+  sa.K = K;
+  sa.steps_per_chunk = spc;
   static cudaError_t a0 = cudaFuncSetAttribute(
       k_skinny_tc<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSkSmem);
   static cudaError_t a1 = cudaFuncSetAttribute(
@@ -2015,19 +2171,29 @@ cudaError_t run_skinny_tc(const uint16_t* X, const float* F, bool f_kj, int64_t 
   if (a0 != cudaSuccess) return a0;
   if (a1 != cudaSuccess) return a1;
   if (a2 != cudaSuccess) return a2;
-  const dim3 grid((unsigned)atoms, (unsigned)chunks);
-  DropKey none{};
+  const dim3 grid((unsigned)atoms, (unsigned)chunks, (unsigned)ng);
   note_launch();
-  if (key && !f_kj)
-    (void)launch_pdl(k_skinny_tc<true, false>, dim3(grid), dim3(kSkThreads), kSkSmem, st, 
-        tX, tF, F, M, K, spc, *key, mask_bytes, partial, counters, out, ext);
+  if (keys && !f_kj)
+    (void)launch_pdl(k_skinny_tc<true, false>, grid, dim3(kSkThreads), kSkSmem, st, sa);
   else if (f_kj)
-    (void)launch_pdl(k_skinny_tc<false, true>, dim3(grid), dim3(kSkThreads), kSkSmem, st, 
-        tX, tF, F, M, K, spc, none, nullptr, partial, counters, out, ext);
+    (void)launch_pdl(k_skinny_tc<false, true>, grid, dim3(kSkThreads), kSkSmem, st, sa);
   else
-    (void)launch_pdl(k_skinny_tc<false, false>, dim3(grid), dim3(kSkThreads), kSkSmem, st, 
-        tX, tF, F, M, K, spc, none, nullptr, partial, counters, out, ext);
+    (void)launch_pdl(k_skinny_tc<false, false>, grid, dim3(kSkThreads), kSkSmem, st, sa);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t run_skinny_tc(const uint16_t* X, const float* F, bool f_kj, int64_t M, int64_t K,
+                          const DropKey* key, uint8_t* mask_bytes, float* partial, float* out,
+                          uint16_t* ext, cudaStream_t st) {
+  return skinny_launch(X, 1, &F, f_kj, M, K, key, &mask_bytes, &partial, &out, &ext, st);
+}
+
+cudaError_t run_skinny_tc_group(const uint16_t* X, int ng, const float* const* F, int64_t M,
+                                int64_t K, const DropKey* keys, uint8_t* const* mask_bytes,
+                                float* const* partial, float* const* out, uint16_t* const* ext,
+                                cudaStream_t st) {
+  return skinny_launch(X, ng, F, false, M, K, keys, mask_bytes, partial, out, ext, st);
 }
 
 // ------------------------------------------------------------------------ weight gradients (host)

@@ -388,6 +388,13 @@ WsLayout ws_layout(const ws_stack_cfg& c, int block_layers) {
     const size_t b = linear_workspace_bytes(c.M, s.N[i], s.K[i]);
     if (b > lin) lin = b;
   }
+  // the forward runs q, k, v and gate, up as groups (one launch each)
+  const int64_t nqkv[3] = {s.N[WS_LIN_Q], s.N[WS_LIN_K], s.N[WS_LIN_V]};
+  const int64_t ngu[2] = {s.N[WS_LIN_GATE], s.N[WS_LIN_UP]};
+  const size_t g3 = linear_group_workspace_bytes(c.M, 3, nqkv, s.K[WS_LIN_Q]);
+  const size_t g2 = linear_group_workspace_bytes(c.M, 2, ngu, s.K[WS_LIN_GATE]);
+  if (g3 > lin) lin = g3;
+  if (g2 > lin) lin = g2;
   L.lin = take(lin);
   L.blk = take((size_t)block_layers * saved_layout(c).total);
   L.qout = take(M * H * 2);
@@ -469,16 +476,40 @@ cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const
                       key_of(x, step, layer, li), out, at<float>(S, L.U[li]),
                       at<uint32_t>(S, L.mask[li]), lws, st);
   };
+  // linears reading the same input: one LoRA-down launch and one GEMM
+  auto lin_group = [&](int ng, int ng_gemm, const int* li, const uint16_t* in,
+                       uint16_t* const* outs) {
+    NF4View W[kMaxGroups];
+    const float* A[kMaxGroups];
+    const float* B[kMaxGroups];
+    DropKeyHost keys[kMaxGroups];
+    float* U[kMaxGroups];
+    uint32_t* mk[kMaxGroups];
+    for (int g = 0; g < ng; ++g) {
+      W[g] = wview(x, block, lib, li[g]);
+      A[g] = P + x.PL.A[li[g]];
+      B[g] = P + x.PL.B[li[g]];
+      keys[g] = key_of(x, step, layer, li[g]);
+      U[g] = at<float>(S, L.U[li[g]]);
+      mk[g] = at<uint32_t>(S, L.mask[li[g]]);
+    }
+    return linear_fwd_group(ng, ng_gemm, W, in, A, B, M, x.scale, keys, outs, U, mk, lws, st);
+  };
   float* h = at<float>(S, L.h);
   if (h != h_in) WS_TRY(cudaMemcpyAsync(h, h_in, (size_t)M * H * 4, cudaMemcpyDeviceToDevice, st));
   note_launch();
   (void)launch_pdl(k_rmsnorm_fwd, dim3((unsigned)M), dim3(256), 0, st, h, H, x.c.eps, at<uint16_t>(S, L.a), at<float>(S, L.rstd1));
   WS_TRY(cudaGetLastError());
   if (with_qk) {
-    WS_TRY(lin(WS_LIN_Q, at<uint16_t>(S, L.a), at<uint16_t>(ws, x.WSL.qout)));
-    WS_TRY(lin(WS_LIN_K, at<uint16_t>(S, L.a), at<uint16_t>(ws, x.WSL.kout)));
+    // v gets a GEMM of its own, as in a recompute (which skips q and k), so
+    // both passes produce the same v bit for bit
+    const int li[3] = {WS_LIN_Q, WS_LIN_K, WS_LIN_V};
+    uint16_t* outs[3] = {at<uint16_t>(ws, x.WSL.qout), at<uint16_t>(ws, x.WSL.kout),
+                         at<uint16_t>(S, L.v)};
+    WS_TRY(lin_group(3, 2, li, at<uint16_t>(S, L.a), outs));
+  } else {
+    WS_TRY(lin(WS_LIN_V, at<uint16_t>(S, L.a), at<uint16_t>(S, L.v)));
   }
-  WS_TRY(lin(WS_LIN_V, at<uint16_t>(S, L.a), at<uint16_t>(S, L.v)));
   note_launch();
   (void)launch_pdl(k_repeat_fwd, dim3(nblk(M * H / 8)), dim3(256), 0, st, at<uint16_t>(S, L.v), (int)M, (int)H, (int)KV,
                                                 (int)x.c.head_dim, at<uint16_t>(S, L.vr));
@@ -492,8 +523,11 @@ cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const
   (void)launch_pdl(k_rmsnorm_fwd, dim3((unsigned)M), dim3(256), 0, st, at<float>(S, L.h1), H, x.c.eps, at<uint16_t>(S, L.b),
                                             at<float>(S, L.rstd2));
   WS_TRY(cudaGetLastError());
-  WS_TRY(lin(WS_LIN_GATE, at<uint16_t>(S, L.b), at<uint16_t>(S, L.g)));
-  WS_TRY(lin(WS_LIN_UP, at<uint16_t>(S, L.b), at<uint16_t>(S, L.u)));
+  {
+    const int li[2] = {WS_LIN_GATE, WS_LIN_UP};
+    uint16_t* outs[2] = {at<uint16_t>(S, L.g), at<uint16_t>(S, L.u)};
+    WS_TRY(lin_group(2, 2, li, at<uint16_t>(S, L.b), outs));
+  }
   note_launch();
   (void)launch_pdl(k_silu_mul_fwd, dim3(nblk(M * I / 8)), dim3(256), 0, st, at<uint16_t>(S, L.g), at<uint16_t>(S, L.u), M * I,
                                               at<uint16_t>(S, L.act));
