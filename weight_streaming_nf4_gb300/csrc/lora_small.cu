@@ -4,6 +4,11 @@
 // the kernels (the tensor-core kernels live in nf4_gemm.cu).  Every
 // reduction runs in a fixed order: no atomics on data.
 #include <math.h>
+#include <stdlib.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -172,6 +177,48 @@ LinWs lin_ws_layout(int64_t M, int64_t N, int64_t K) {
 
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K) { return lin_ws_layout(M, N, K).total; }
 
+// ------------------------------------------------------------------------ side stream
+// A library-owned stream (and a fork / join event pair) per device and
+// caller stream: work that depends only on inputs ready at the fork runs
+// there beside the caller's stream and is joined back before anything that
+// needs it.  Under stream capture the fork and join become graph edges.
+// WS_NF4_SIDE=0 keeps everything on the caller's stream.
+namespace {
+struct Side {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+std::map<std::pair<int, cudaStream_t>, Side> g_side;
+
+bool side_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("WS_NF4_SIDE");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
+cudaError_t side_of(cudaStream_t st, Side* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  Side& sd = g_side[std::make_pair(dev, st)];
+  if (sd.s == nullptr) {
+    e = cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      g_side.erase(std::make_pair(dev, st));
+      return e;
+    }
+  }
+  *out = sd;
+  return cudaSuccess;
+}
+}  // namespace
+
 cudaError_t linear_fwd(const NF4View& W, const uint16_t* x, const float* A, const float* B,
                        int64_t M, float scale, const DropKeyHost& key, uint16_t* y, float* U,
                        uint32_t* mask, void* ws, cudaStream_t st) {
@@ -299,16 +346,26 @@ cudaError_t linear_bwd(const NF4View& W, const uint16_t* x, const float* A, cons
     if (e != cudaSuccess) return e;
     mask = m;
   }
+  // dB needs only U and dY: on the side stream it runs beside G and dA and
+  // is joined back before dX (so the persistent GEMM starts on an idle GPU)
+  Side side;
+  const bool use_side = dB != nullptr && side_enabled() && side_of(st, &side) == cudaSuccess;
+  if (use_side) {
+    e = cudaEventRecord(side.fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side.s, side.fork, 0);
+    if (e == cudaSuccess) e = run_wgrad_tc(U, dY, nullptr, M, W.N, scale, dB, 0, wg, side.s);
+    if (e == cudaSuccess) e = cudaEventRecord(side.join, side.s);
+    if (e != cudaSuccess) return e;
+  }
   e = run_lora_G(dY, B, M, W.N, G, Gext, reinterpret_cast<float*>(w + L.skinny), st);
+  if (e == cudaSuccess && dB && !use_side) e = run_wgrad_tc(U, dY, nullptr, M, W.N, scale, dB, 0, wg, st);
+  if (e == cudaSuccess && dA) e = run_wgrad_tc(G, x, mask, M, W.K, scale, dA, 1, wg, st);
+  // join even after an error, so a capture is never left with an unjoined stream
+  if (use_side) {
+    const cudaError_t ej = cudaStreamWaitEvent(st, side.join, 0);
+    if (e == cudaSuccess) e = ej;
+  }
   if (e != cudaSuccess) return e;
-  if (dB) {
-    e = run_wgrad_tc(U, dY, nullptr, M, W.N, scale, dB, 0, wg, st);
-    if (e != cudaSuccess) return e;
-  }
-  if (dA) {
-    e = run_wgrad_tc(G, x, mask, M, W.K, scale, dA, 1, wg, st);
-    if (e != cudaSuccess) return e;
-  }
   if (dX) {
     const GemmPlan p = plan_gemm(true, M, W.K, W.N);
     e = run_nf4_gemm(p, W, dY, M, Gext, A, scale, mask, dX, dX_f32, dX_accum,
