@@ -126,6 +126,10 @@ cudaError_t run_skinny_tc_group(const uint16_t* X, int ng, const float* const* F
                                 int64_t K, const DropKey* keys, uint8_t* const* mask_bytes,
                                 float* const* partial, float* const* out, uint16_t* const* ext,
                                 cudaStream_t st);
+// G[g] = dY[g] B[g] for ng linears with the same M and N in one launch.
+cudaError_t run_skinny_G_group(int ng, const uint16_t* const* dY, const float* const* B, int64_t M,
+                               int64_t N, float* const* partial, float* const* G,
+                               uint16_t* const* Gext, cudaStream_t st);
 // U = (mask . x) A^T [M,16] fp32; Uext [M,64] bf16 hi/lo; mask bits (optional).
 cudaError_t run_lora_down(const uint16_t* x, const float* A, int64_t M, int64_t K,
                           const DropKeyHost& key, float* U, uint16_t* Uext, uint32_t* mask_out,
@@ -141,6 +145,10 @@ cudaError_t run_mask_gen(int64_t M, int64_t K, const DropKeyHost& key, uint32_t*
 // [M, C/32] when not NULL).  out layout is [C,16] (dB) or, when
 // transpose_out, [16,C] (dA).  One fixed summation order; no workspace.
 size_t wgrad_tc_bytes(int64_t M, int64_t C);
+// ng weight gradients with the same M, C and s in one launch (masks: all or none).
+cudaError_t run_wgrad_tc_group(int ng, const float* const* P, const uint16_t* const* Q,
+                               const uint32_t* const* mask, int64_t M, int64_t C, float s,
+                               float* const* out, int transpose_out, cudaStream_t st);
 cudaError_t run_wgrad_tc(const float* P, const uint16_t* Q, const uint32_t* mask, int64_t M,
                          int64_t C, float s, float* out, int transpose_out, void* ws,
                          cudaStream_t st);
@@ -157,6 +165,14 @@ cudaError_t linear_fwd_group(int ng, int ng_gemm, const NF4View* W, const uint16
                              const float* const* B, int64_t M, float scale, const DropKeyHost* keys,
                              uint16_t* const* y, float* const* U, uint32_t* const* mask, void* ws,
                              cudaStream_t st);
+// ng linears of one shape reading the same x, each with its own dY; their
+// input gradients summed into dX.
+size_t linear_bwd_group_workspace_bytes(int64_t M, int ng, int64_t N, int64_t K);
+cudaError_t linear_bwd_group(int ng, const NF4View* W, const uint16_t* x, const float* const* A,
+                             const float* const* B, int64_t M, float scale, const DropKeyHost* keys,
+                             const float* const* U, const uint32_t* const* mask,
+                             const uint16_t* const* dY, void* dX, int dX_f32, int dX_accum,
+                             float* const* dA, float* const* dB, void* ws, cudaStream_t st);
 cudaError_t linear_bwd(const NF4View& W, const uint16_t* x, const float* A, const float* B,
                        int64_t M, float scale, const DropKeyHost& key, const float* U,
                        const uint32_t* mask, const uint16_t* dY, void* dX, int dX_f32,

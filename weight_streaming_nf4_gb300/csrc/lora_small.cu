@@ -374,4 +374,103 @@ cudaError_t linear_bwd(const NF4View& W, const uint16_t* x, const float* A, cons
   return e;
 }
 
+// ------------------------------------------------------------------------ linears sharing x (backward)
+// Per linear: Gext [M,64] bf16, G [M,16] fp32, mask [M,K/32] (when the
+// caller kept none), skinny partials; then the split partials of one
+// input-gradient plan (all linears have the same shape).
+namespace {
+struct BwdGrpWs {
+  size_t ext, G, mask, skinny, per, split, total;
+};
+BwdGrpWs bwd_grp_ws_layout(int64_t M, int ng, int64_t N, int64_t K) {
+  BwdGrpWs w{};
+  w.ext = 0;
+  w.G = align256((size_t)M * 64 * 2);
+  w.mask = w.G + align256((size_t)M * 16 * 4);
+  w.skinny = w.mask + align256((size_t)M * (size_t)(K / 32) * 4);
+  w.per = w.skinny + align256(skinny_partial_bytes(M, N));
+  w.split = (size_t)ng * w.per;
+  w.total = w.split + align256(gemm_partial_bytes(plan_gemm(true, M, K, N), M, K));
+  return w;
+}
+}  // namespace
+
+size_t linear_bwd_group_workspace_bytes(int64_t M, int ng, int64_t N, int64_t K) {
+  return bwd_grp_ws_layout(M, ng, N, K).total;
+}
+
+// ng linears of the same shape reading the same x, each with its own dY:
+// the G products in one launch, the dA weight gradients in one launch, the
+// dB weight gradients in one launch on the side stream, then the input
+// gradients one GEMM after the other into dX (the first one written, or
+// added when dX_accum, the others added).  Each result equals the one-linear
+// backward's bit for bit.
+cudaError_t linear_bwd_group(int ng, const NF4View* W, const uint16_t* x, const float* const* A,
+                             const float* const* B, int64_t M, float scale, const DropKeyHost* keys,
+                             const float* const* U, const uint32_t* const* mask,
+                             const uint16_t* const* dY, void* dX, int dX_f32, int dX_accum,
+                             float* const* dA, float* const* dB, void* ws, cudaStream_t st) {
+  if (ng < 1 || ng > kMaxGroups) return cudaErrorInvalidValue;
+  const int64_t N = W[0].N, K = W[0].K;
+  bool any_dA = false, any_dB = false;
+  for (int g = 0; g < ng; ++g) {
+    if (W[g].N != N || W[g].K != K) return cudaErrorInvalidValue;
+    any_dA = any_dA || dA[g] != nullptr;
+    any_dB = any_dB || dB[g] != nullptr;
+  }
+  for (int g = 0; g < ng; ++g)
+    if ((dA[g] != nullptr) != any_dA || (dB[g] != nullptr) != any_dB) return cudaErrorInvalidValue;
+  const BwdGrpWs L = bwd_grp_ws_layout(M, ng, N, K);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* Gext[kMaxGroups];
+  float* G[kMaxGroups];
+  float* part[kMaxGroups];
+  const uint32_t* mk[kMaxGroups];
+  cudaError_t e = cudaSuccess;
+  for (int g = 0; g < ng && e == cudaSuccess; ++g) {
+    uint8_t* base = w + (size_t)g * L.per;
+    Gext[g] = reinterpret_cast<uint16_t*>(base + L.ext);
+    G[g] = reinterpret_cast<float*>(base + L.G);
+    part[g] = reinterpret_cast<float*>(base + L.skinny);
+    mk[g] = mask[g];
+    if (mk[g] == nullptr) {
+      uint32_t* m = reinterpret_cast<uint32_t*>(base + L.mask);
+      e = run_mask_gen(M, K, keys[g], m, st);
+      mk[g] = m;
+    }
+  }
+  if (e != cudaSuccess) return e;
+  Side side;
+  const bool use_side = any_dB && side_enabled() && side_of(st, &side) == cudaSuccess;
+  if (use_side) {
+    e = cudaEventRecord(side.fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side.s, side.fork, 0);
+    if (e == cudaSuccess) e = run_wgrad_tc_group(ng, U, dY, nullptr, M, N, scale, dB, 0, side.s);
+    if (e == cudaSuccess) e = cudaEventRecord(side.join, side.s);
+    if (e != cudaSuccess) return e;
+  }
+  e = run_skinny_G_group(ng, dY, B, M, N, part, G, Gext, st);
+  if (e == cudaSuccess && any_dB && !use_side)
+    e = run_wgrad_tc_group(ng, U, dY, nullptr, M, N, scale, dB, 0, st);
+  if (e == cudaSuccess && any_dA) {
+    const float* Gc[kMaxGroups];
+    const uint16_t* xs[kMaxGroups];
+    for (int g = 0; g < ng; ++g) {
+      Gc[g] = G[g];
+      xs[g] = x;
+    }
+    e = run_wgrad_tc_group(ng, Gc, xs, mk, M, K, scale, dA, 1, st);
+  }
+  if (use_side) {
+    const cudaError_t ej = cudaStreamWaitEvent(st, side.join, 0);
+    if (e == cudaSuccess) e = ej;
+  }
+  if (e != cudaSuccess || dX == nullptr) return e;
+  const GemmPlan p = plan_gemm(true, M, K, N);
+  for (int g = 0; g < ng && e == cudaSuccess; ++g)
+    e = run_nf4_gemm(p, W[g], dY[g], M, Gext[g], A[g], scale, mk[g], dX, dX_f32,
+                     g > 0 ? 1 : dX_accum, reinterpret_cast<float*>(w + L.split), st);
+  return e;
+}
+
 }  // namespace ws

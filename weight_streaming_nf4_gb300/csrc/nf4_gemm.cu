@@ -1103,6 +1103,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   D = 128 x 128 fp32 in TMEM; rows j and 16+j add up to P^T Q.
 // One CTA per 128 columns runs every token step, so the sum over tokens
 // has one fixed order and the result is written straight out.
+// Element g of a parameter array, chosen with compares (no run-time indexing).
+template <class T>
+WS_DEVINL T pick_group(const T (&a)[kMaxGroups], int g) {
+  return g == 2 ? a[2] : (g == 1 ? a[1] : a[0]);
+}
+
+// Launch parameters of the weight-gradient kernel: group g = blockIdx.y
+// (LoRA factors of linears with the same M and C in one launch).
+struct WgArgs {
+  CUtensorMap tmQ[kMaxGroups];
+  const float* P[kMaxGroups];
+  const uint32_t* mask[kMaxGroups];
+  float* out[kMaxGroups];
+  int64_t M, C;
+  float s;
+  int transpose_out;
+};
 constexpr int kWgThreads = 192;
 constexpr int kWgStages = 4;
 constexpr int kWgBN = 128;
@@ -1115,9 +1132,16 @@ constexpr uint32_t kWgSmem =
 
 template <bool MASKED>
 __global__ void __launch_bounds__(kWgThreads, 1)
-    k_wgrad_tc(const __grid_constant__ CUtensorMap tmQ, const float* __restrict__ P,
-               const uint32_t* __restrict__ mask, int64_t M, int64_t C, float s,
-               int transpose_out, float* __restrict__ out) {
+    k_wgrad_tc(const __grid_constant__ WgArgs wa) {
+  // group g = blockIdx.y: its own Q, P, mask and output (same M, C, s)
+  const int grp = (int)blockIdx.y;
+  const CUtensorMap* tmQ = grp == 2 ? &wa.tmQ[2] : (grp == 1 ? &wa.tmQ[1] : &wa.tmQ[0]);
+  const float* __restrict__ P = pick_group(wa.P, grp);
+  const uint32_t* __restrict__ mask = pick_group(wa.mask, grp);
+  float* __restrict__ out = pick_group(wa.out, grp);
+  const int64_t M = wa.M, C = wa.C;
+  const float s = wa.s;
+  const int transpose_out = wa.transpose_out;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1174,8 +1198,8 @@ __global__ void __launch_bounds__(kWgThreads, 1)
           const int t0 = i * 64;
           const int64_t rows = M - t0 < 64 ? M - t0 : 64;
           mbar_arrive_expect_tx(&full[st], kWgB + (uint32_t)rows * 64u);
-          tma_load_2d(sB + st * kWgB, &tmQ, &full[st], (int)c0, t0);
-          tma_load_2d(sB + st * kWgB + 8192, &tmQ, &full[st], (int)(c0 + 64), t0);
+          tma_load_2d(sB + st * kWgB, tmQ, &full[st], (int)c0, t0);
+          tma_load_2d(sB + st * kWgB + 8192, tmQ, &full[st], (int)(c0 + 64), t0);
           bulk_load(sP + st * kWgP, P + (int64_t)t0 * 16, (uint32_t)rows * 64u, &full[st]);
           issued = i + 1;
         }
@@ -1358,11 +1382,10 @@ constexpr uint32_t kSkB = 64 * 128;     // B operand: 48 rows used of 64
 constexpr uint32_t kSkSmem =
     kSkStages * (kSkX + kSkF + kSkB) + (3 * kSkStages + 1) * 8 + 16 + 1024;
 
-// Launch parameters: one X for every group; group g = blockIdx.z has its
-// own factor, dropout key and outputs (linears that read the same input run
-// in one launch).
+// Launch parameters: group g = blockIdx.z has its own X, factor, dropout
+// key and outputs (the LoRA products of several linears in one launch).
 struct SkArgs {
-  CUtensorMap tmX;
+  CUtensorMap tmX[kMaxGroups];  // X of each group (the same map for a forward group)
   CUtensorMap tmF[kMaxGroups];  // A factors [16][K] fp32 (F_KJ = false)
   const float* F[kMaxGroups];
   DropKey key[kMaxGroups];
@@ -1374,17 +1397,11 @@ struct SkArgs {
   int64_t M, K;
   int steps_per_chunk;
 };
-// Element g of a parameter array, chosen with compares (no run-time indexing).
-template <class T>
-WS_DEVINL T pick_group(const T (&a)[kMaxGroups], int g) {
-  return g == 2 ? a[2] : (g == 1 ? a[1] : a[0]);
-}
-
 // F_KJ: the factor is given as [K][16] (B), else as [16][K] (A).
 template <bool MASKED, bool F_KJ>
 __global__ void __launch_bounds__(kSkThreads, 1) k_skinny_tc(const __grid_constant__ SkArgs sa) {
   const int grp = (int)blockIdx.z;
-  const CUtensorMap* tmX = &sa.tmX;
+  const CUtensorMap* tmX = grp == 2 ? &sa.tmX[2] : (grp == 1 ? &sa.tmX[1] : &sa.tmX[0]);
   const CUtensorMap* tmF = grp == 2 ? &sa.tmF[2] : (grp == 1 ? &sa.tmF[1] : &sa.tmF[0]);
   const float* __restrict__ F = pick_group(sa.F, grp);
   DropKey key = pick_group(sa.key, grp);
@@ -2126,7 +2143,7 @@ cudaError_t ring_clear() {
 }
 
 namespace {
-cudaError_t skinny_launch(const uint16_t* X, int ng, const float* const* F, bool f_kj, int64_t M,
+cudaError_t skinny_launch(const uint16_t* const* X, int ng, const float* const* F, bool f_kj, int64_t M,
                           int64_t K, const DropKey* keys, uint8_t* const* mask_bytes,
                           float* const* partial, float* const* out, uint16_t* const* ext,
                           cudaStream_t st) {
@@ -2141,13 +2158,14 @@ cudaError_t skinny_launch(const uint16_t* X, int ng, const float* const* F, bool
   if (e != cudaSuccess) return e;
   SkArgs sa;
   memset(&sa, 0, sizeof(sa));
-  if (!make_map(&sa.tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)K, (uint64_t)M,
-                (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
   for (int g = 0; g < ng; ++g) {
+    if (g > 0 && X[g] == X[g - 1]) sa.tmX[g] = sa.tmX[g - 1];
+    else if (!make_map(&sa.tmX[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X[g], (uint64_t)K, (uint64_t)M,
+                       (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
     // the factor slices are fetched with 16-byte copies
     if ((reinterpret_cast<uintptr_t>(F[g]) & 15u) != 0u) return cudaErrorInvalidValue;
-    if (f_kj) sa.tmF[g] = sa.tmX;
+    if (f_kj) sa.tmF[g] = sa.tmX[g];
     else if (!make_map(&sa.tmF[g], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, F[g], (uint64_t)K, 16,
                        (uint64_t)K * 4, 64, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
@@ -2186,14 +2204,22 @@ cudaError_t skinny_launch(const uint16_t* X, int ng, const float* const* F, bool
 cudaError_t run_skinny_tc(const uint16_t* X, const float* F, bool f_kj, int64_t M, int64_t K,
                           const DropKey* key, uint8_t* mask_bytes, float* partial, float* out,
                           uint16_t* ext, cudaStream_t st) {
-  return skinny_launch(X, 1, &F, f_kj, M, K, key, &mask_bytes, &partial, &out, &ext, st);
+  return skinny_launch(&X, 1, &F, f_kj, M, K, key, &mask_bytes, &partial, &out, &ext, st);
 }
 
 cudaError_t run_skinny_tc_group(const uint16_t* X, int ng, const float* const* F, int64_t M,
                                 int64_t K, const DropKey* keys, uint8_t* const* mask_bytes,
                                 float* const* partial, float* const* out, uint16_t* const* ext,
                                 cudaStream_t st) {
-  return skinny_launch(X, ng, F, false, M, K, keys, mask_bytes, partial, out, ext, st);
+  const uint16_t* Xs[kMaxGroups];
+  for (int g = 0; g < ng && g < kMaxGroups; ++g) Xs[g] = X;
+  return skinny_launch(Xs, ng, F, false, M, K, keys, mask_bytes, partial, out, ext, st);
+}
+
+cudaError_t run_skinny_G_group(int ng, const uint16_t* const* dY, const float* const* B, int64_t M,
+                               int64_t N, float* const* partial, float* const* G,
+                               uint16_t* const* Gext, cudaStream_t st) {
+  return skinny_launch(dY, ng, B, true, M, N, nullptr, nullptr, partial, G, Gext, st);
 }
 
 // ------------------------------------------------------------------------ weight gradients (host)
@@ -2203,31 +2229,53 @@ size_t wgrad_tc_bytes(int64_t M, int64_t C) {
   return 0;
 }
 
-cudaError_t run_wgrad_tc(const float* P, const uint16_t* Q, const uint32_t* mask, int64_t M,
-                         int64_t C, float s, float* out, int transpose_out, void* ws,
-                         cudaStream_t st) {
-  (void)ws;
+cudaError_t run_wgrad_tc_group(int ng, const float* const* P, const uint16_t* const* Q,
+                               const uint32_t* const* mask, int64_t M, int64_t C, float s,
+                               float* const* out, int transpose_out, cudaStream_t st) {
   if (!encode_fn()) return cudaErrorNotSupported;
-  // P rows are fetched with 16-byte bulk copies
-  if ((reinterpret_cast<uintptr_t>(P) & 15u) != 0u) return cudaErrorInvalidValue;
-  CUtensorMap tQ;
-  if (!make_map(&tQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, (uint64_t)C, (uint64_t)M, (uint64_t)C * 2,
-                64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
+  if (ng < 1 || ng > kMaxGroups) return cudaErrorInvalidValue;
+  WgArgs wa;
+  memset(&wa, 0, sizeof(wa));
+  bool masked = false;
+  for (int g = 0; g < ng; ++g) {
+    // P rows are fetched with 16-byte bulk copies
+    if ((reinterpret_cast<uintptr_t>(P[g]) & 15u) != 0u) return cudaErrorInvalidValue;
+    if (g > 0 && Q[g] == Q[g - 1]) wa.tmQ[g] = wa.tmQ[g - 1];
+    else if (!make_map(&wa.tmQ[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q[g], (uint64_t)C, (uint64_t)M,
+                       (uint64_t)C * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    wa.P[g] = P[g];
+    wa.mask[g] = mask ? mask[g] : nullptr;
+    wa.out[g] = out[g];
+    masked = masked || wa.mask[g] != nullptr;
+  }
+  // one launch masks every group or none
+  for (int g = 0; g < ng; ++g)
+    if ((wa.mask[g] != nullptr) != masked) return cudaErrorInvalidValue;
+  wa.M = M;
+  wa.C = C;
+  wa.s = s;
+  wa.transpose_out = transpose_out;
   static cudaError_t attr0 = cudaFuncSetAttribute(
       k_wgrad_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWgSmem);
   static cudaError_t attr1 = cudaFuncSetAttribute(
       k_wgrad_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWgSmem);
   if (attr0 != cudaSuccess) return attr0;
   if (attr1 != cudaSuccess) return attr1;
-  const dim3 grid((unsigned)((C + kWgBN - 1) / kWgBN));
+  const dim3 grid((unsigned)((C + kWgBN - 1) / kWgBN), (unsigned)ng);
   note_launch();
-  if (mask)
-    (void)launch_pdl(k_wgrad_tc<true>, dim3(grid), dim3(kWgThreads), kWgSmem, st, tQ, P, mask, M, C, s, transpose_out, out);
+  if (masked)
+    (void)launch_pdl(k_wgrad_tc<true>, grid, dim3(kWgThreads), kWgSmem, st, wa);
   else
-    (void)launch_pdl(k_wgrad_tc<false>, dim3(grid), dim3(kWgThreads), kWgSmem, st, tQ, P, nullptr, M, C, s, transpose_out,
-                                                         out);
+    (void)launch_pdl(k_wgrad_tc<false>, grid, dim3(kWgThreads), kWgSmem, st, wa);
   return cudaGetLastError();
+}
+
+cudaError_t run_wgrad_tc(const float* P, const uint16_t* Q, const uint32_t* mask, int64_t M,
+                         int64_t C, float s, float* out, int transpose_out, void* ws,
+                         cudaStream_t st) {
+  (void)ws;
+  return run_wgrad_tc_group(1, &P, &Q, &mask, M, C, s, &out, transpose_out, st);
 }
 
 }  // namespace ws

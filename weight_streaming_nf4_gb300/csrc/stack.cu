@@ -395,6 +395,8 @@ WsLayout ws_layout(const ws_stack_cfg& c, int block_layers) {
   const size_t g2 = linear_group_workspace_bytes(c.M, 2, ngu, s.K[WS_LIN_GATE]);
   if (g3 > lin) lin = g3;
   if (g2 > lin) lin = g2;
+  const size_t b2 = linear_bwd_group_workspace_bytes(c.M, 2, s.N[WS_LIN_GATE], s.K[WS_LIN_GATE]);
+  if (b2 > lin) lin = b2;
   L.lin = take(lin);
   L.blk = take((size_t)block_layers * saved_layout(c).total);
   L.qout = take(M * H * 2);
@@ -571,8 +573,31 @@ cudaError_t layer_bwd(const Ctx& x, const void* block, int lib, int layer, const
   (void)launch_pdl(k_silu_mul_bwd, dim3(nblk(M * I / 8)), dim3(256), 0, st, dact, at<const uint16_t>(S, L.g),
                                               at<const uint16_t>(S, L.u), M * I, dg, du);
   WS_TRY(cudaGetLastError());
-  WS_TRY(lin(WS_LIN_GATE, at<const uint16_t>(S, L.b), dg, db, 0));
-  WS_TRY(lin(WS_LIN_UP, at<const uint16_t>(S, L.b), du, db, 1));
+  {
+    // gate and up read the same input: their LoRA products share launches
+    const int li[2] = {WS_LIN_GATE, WS_LIN_UP};
+    NF4View W[2];
+    const float* A[2];
+    const float* B[2];
+    DropKeyHost keys[2];
+    const float* U[2];
+    const uint32_t* mk[2];
+    const uint16_t* dYs[2] = {dg, du};
+    float* dAs[2];
+    float* dBs[2];
+    for (int g = 0; g < 2; ++g) {
+      W[g] = wview(x, block, lib, li[g]);
+      A[g] = P + x.PL.A[li[g]];
+      B[g] = P + x.PL.B[li[g]];
+      keys[g] = key_of(x, step, layer, li[g]);
+      U[g] = at<const float>(S, L.U[li[g]]);
+      mk[g] = at<const uint32_t>(S, L.mask[li[g]]);
+      dAs[g] = Gd + x.PL.A[li[g]];
+      dBs[g] = Gd + x.PL.B[li[g]];
+    }
+    WS_TRY(linear_bwd_group(2, W, at<const uint16_t>(S, L.b), A, B, M, x.scale, keys, U, mk, dYs,
+                            db, 1, 0, dAs, dBs, lws, st));
+  }
   note_launch();
   (void)launch_pdl(k_rmsnorm_bwd, dim3((unsigned)M), dim3(256), 0, st, at<const float>(S, L.h1), at<const float>(S, L.rstd2),
                                              db, H, dh);
