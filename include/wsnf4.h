@@ -32,7 +32,15 @@
  *    documented as "device" must be device (or managed) memory of the current
  *    CUDA device; "pinned" means cudaHostAlloc'd / registered host memory.
  *  - Execution: all work is enqueued asynchronously on the given stream(s);
- *    no call synchronises the host except ws_device_error.
+ *    no call synchronises the host except ws_device_error.  Kernels are
+ *    launched with programmatic dependent launch (each waits for the
+ *    previous kernel of its stream before touching data; WS_NF4_PDL=0 in
+ *    the environment turns it off).  The LoRA backward forks part of its
+ *    work onto a library-owned side stream and joins it back before the
+ *    call's last kernel: the first such call for a (device, caller stream)
+ *    pair creates that stream and two events, which live until the process
+ *    exits (WS_NF4_SIDE=0 keeps everything on the caller's stream).  Under
+ *    stream capture the fork and join become graph edges.
  *  - Alignment: every device pointer must be 16-byte aligned
  *    (WS_ERR_ALIGN otherwise).
  *  - Shapes: K % 64 == 0 and N % 64 == 0 for NF4 weights; M >= 1;

@@ -20,15 +20,20 @@
 // one dequantised weight tile), BN output columns, 64-deep contraction steps.
 //
 // Schedule: the (tile, step) iterations of the whole problem are cut into
-// gridDim.x equal contiguous ranges, one per CTA (stream-K), launched
-// cooperatively so every CTA is resident.  A tile cut by range boundaries is
-// finished by the CTA holding its first steps -- that is always the last
-// segment of that CTA's range, so it runs after the other pieces were made:
-// it adds the later CTAs' fp32 partial tiles to its own accumulator in step
-// order (after waiting, with a time limit, for their completion flags) and
-// stores the tile.  Every other tile is stored by its CTA directly.  The cut
-// points depend only on the shape and the grid size, so results are
-// deterministic and identical run to run.  No atomics on data.
+// contiguous ranges, one per unit (a CTA, or a pair of CTAs), on a grid
+// sized so that every CTA is resident at once (stream-K).  A tile cut by
+// range boundaries is finished by the unit holding its first steps -- that
+// is always the last segment of that unit's range, so it runs after the
+// other pieces were made: it adds the later units' fp32 partial tiles to its
+// own accumulator in step order (after waiting, with a time limit, for
+// their completion flags) and stores the tile.  Every other tile is stored
+// by its unit directly.  The cut points depend only on the shape and the
+// grid size, so results are deterministic and identical run to run.  No
+// atomics on data.
+//
+// Grouped forward: linears that read the same activation (q and k, gate and
+// up) run as one launch over their concatenated output columns; each tile
+// takes its weight, LoRA factor and output from its linear.
 //
 // The LoRA terms use the same tensor cores: the forward appends one 64-deep
 // step whose A operand is [U_hi | U_lo | U_hi | 0] and whose B operand is
