@@ -168,7 +168,8 @@ def arm_config(world):
 
 
 def run_reference(args, rank):
-    if rank != 0:
+    from weight_streaming_nf4_gb300 import replicas
+    if not replicas.is_reporter(rank):
         return
     M_s = 64
     run, flops, cores, _ = oracle_sample(M_s, SHAPE_32B["H"], SHAPE_32B["KV"], SHAPE_32B["I"])
@@ -520,15 +521,11 @@ def main():
     # the eager resident step (one launch per kernel), for comparison with the graph replay
     t_eager = time_steps(torch, dist, res, h0s, 2, 1, stream)
 
-    def wmax(t):
-        if dist is None:
-            return t
-        x = torch.tensor([t], device=dev)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        return float(x.item())
-    t_res, t_stm = wmax(t_res), wmax(t_stm)
-    value = world * flops * args.steps / t_res / 1e12
-    e2e_val = world * flops * args.steps / t_stm / 1e12
+    from weight_streaming_nf4_gb300 import replicas
+    t_res = replicas.max_over_ranks(t_res, dist, dev)
+    t_stm = replicas.max_over_ranks(t_stm, dist, dev)
+    value = replicas.whole_job_rate(flops, args.steps, world, t_res) / 1e12
+    e2e_val = replicas.whole_job_rate(flops, args.steps, world, t_stm) / 1e12
     nb = cfg.n_layers // BLOCK
     bb = res.sizes["block_bytes"]
     # the two turnaround blocks are not reloaded, and a replayed step starts from
