@@ -395,6 +395,32 @@ def profile_gemm(torch, which):
     print(json.dumps({"profile_gemm": which, "M": M, "N": N, "K": K}))
 
 
+def profile_lora(torch, which):
+    """One 32B-shaped NF4-LoRA linear, ws_lora_linear_fwd then _bwd, three
+    times at M=512: the skinny products, weight gradients and dequant GEMM
+    of one linear (a few hundred MB on the device), for an ncu capture of the
+    LoRA-side kernels."""
+    from weight_streaming_nf4_gb300 import ops
+    dev = torch.device("cuda:0")
+    H, KV, I = SHAPE_32B["H"], SHAPE_32B["KV"], SHAPE_32B["I"]
+    N, K = dict(gate=(I, H), down=(H, I), o=(H, H))[which]
+    M = SHAPE_32B["M"]
+    W = (torch.randn(N, K, device=dev) * 0.02).to(torch.bfloat16)
+    codes, absmax = ops.quantize_nf4(W)
+    Wn = ops.NF4Weight(codes, absmax, N, K)
+    A = (torch.rand(16, K, device=dev) * 2 - 1) / (K ** 0.5)
+    B = torch.randn(N, 16, device=dev) * 0.01
+    x = torch.randn(M, K, device=dev).to(torch.bfloat16)
+    dY = torch.randn(M, N, device=dev).to(torch.bfloat16)
+    key = ops.dropout_key(linear=6)
+    for _ in range(3):
+        y, U, mask = ops.lora_linear_fwd(Wn, x, A, B, key)
+        ops.lora_linear_bwd(Wn, x, A, B, key, U, mask, dY)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    print(json.dumps({"profile_lora": which, "M": M, "N": N, "K": K}))
+
+
 def h2d_peak(torch, dev):
     n = 1 << 30
     src = torch.empty(n, dtype=torch.uint8).pin_memory()
@@ -446,6 +472,9 @@ def main():
     ap.add_argument("--profile-roofline", action="store_true",
                     help="only launch the roofline's dequant GEMM calls twice on an 8-layer "
                          "image; for an ncu capture of their DRAM traffic")
+    ap.add_argument("--profile-lora", choices=["gate", "down", "o"], default=None,
+                    help="only run ws_lora_linear_fwd + _bwd three times on one 32B linear shape "
+                         "at M=512; for an ncu capture of the LoRA-side kernels")
     ap.add_argument("--profile-gemm", choices=["gate", "down", "o"], default=None,
                     help="only launch the dequant GEMM (forward + input gradient) twice on one "
                          "32B linear shape at M=512; for an ncu capture of that kernel")
@@ -461,6 +490,9 @@ def main():
     import torch
     if args.profile_gemm:
         profile_gemm(torch, args.profile_gemm)
+        return
+    if args.profile_lora:
+        profile_lora(torch, args.profile_lora)
         return
     if args.profile_roofline:
         profile_roofline(torch)
