@@ -30,5 +30,10 @@ from .binding import (  # noqa: F401
     rmsnorm_bf16,
     silu_mul_bf16,
     repeat_kv,
+    rmsnorm_f64,
+    rmsnorm_bwd,
+    silu_mul_f64,
+    silu_mul_bwd,
+    repeat_kv_bwd,
     LIN_NAMES,
 )

@@ -65,6 +65,12 @@ def lib():
         L.orc_rmsnorm_bf16.argtypes = [i64, i64, C.c_double, P, P, P]
         L.orc_silu_mul_bf16.argtypes = [i64, P, P, P]
         L.orc_repeat_kv.argtypes = [i64, i64, i64, i64, P, P]
+        L.orc_stack_fwd_bwd_mb.argtypes = [P, C.c_uint32, C.c_uint32, C.c_int, P, P, P, P, P, P]
+        L.orc_silu_mul_f64.argtypes = [i64, P, P, P]
+        L.orc_rmsnorm_f64.argtypes = [i64, i64, C.c_double, C.c_int, P, P, P]
+        L.orc_rmsnorm_bwd_add.argtypes = [i64, i64, P, P, P, P]
+        L.orc_silu_mul_bwd.argtypes = [i64, C.c_int, P, P, P, P, P]
+        L.orc_repeat_kv_bwd.argtypes = [i64, i64, i64, i64, C.c_int, P, P]
         _lib = L
     return _lib
 
@@ -226,8 +232,12 @@ class StackCfg:
         return [(H, H), (KV, H), (KV, H), (H, H), (I, H), (I, H), (H, I)]
 
 
-def stack_fwd_bwd(cfg: StackCfg, step: int, Wq, A, B, h0, backward=True):
-    """Wq/A/B: lists indexed [layer*7 + linear].  Returns (loss, h_L, dA, dB)."""
+def stack_fwd_bwd(cfg: StackCfg, step: int, Wq, A, B, h0, backward=True, microbatch=0,
+                  n_micro=1):
+    """Wq/A/B: lists indexed [layer*7 + linear].  Returns (loss, h_L, dA, dB).
+    With gradient accumulation over n_micro micro-batches, one call covers
+    micro-batch `microbatch` (its dropout keys) and returns its share of the
+    step loss and gradients (see orc_stack_fwd_bwd_mb)."""
     L = lib()
     n = cfg.n_layers * 7
     assert len(Wq) == len(A) == len(B) == n
@@ -253,8 +263,8 @@ def stack_fwd_bwd(cfg: StackCfg, step: int, Wq, A, B, h0, backward=True):
     else:
         dA = dB = None
         pdA = pdB = None
-    L.orc_stack_fwd_bwd(C.byref(cc), step, C.byref(prm), _p(h0), C.byref(loss), _p(h_out),
-                        pdA, pdB)
+    L.orc_stack_fwd_bwd_mb(C.byref(cc), step, microbatch, n_micro, C.byref(prm), _p(h0),
+                           C.byref(loss), _p(h_out), pdA, pdB)
     return loss.value, h_out, dA, dB
 
 
@@ -290,3 +300,53 @@ def adam_step(p, g, m, v, t, lr=2e-4, beta1=0.9, beta2=0.999, eps=1e-8):
         assert a.dtype == np.float64 and a.flags.c_contiguous
     lib().orc_adam_step(p.size, _p(p), _p(g), _p(m), _p(v), int(t), lr, beta1, beta2, eps)
 
+
+
+def rmsnorm_f64(x, eps=1e-6, round_bf16=False):
+    """x: [M, H] -> (y [M, H] double (bf16-valued when round_bf16), rstd [M])."""
+    x = _c(x, np.float64)
+    M, H = x.shape
+    y = np.empty((M, H), np.float64)
+    rstd = np.empty(M, np.float64)
+    lib().orc_rmsnorm_f64(M, H, eps, 1 if round_bf16 else 0, _p(x), _p(y), _p(rstd))
+    return y, rstd
+
+
+def rmsnorm_bwd(x, rstd, dy, dx=None):
+    """dx + (rstd dy - rstd^3 x (dy . x) / H) per row (dx = 0 when not given)."""
+    x = _c(x, np.float64)
+    M, H = x.shape
+    out = np.zeros((M, H), np.float64) if dx is None else _c(dx, np.float64).copy()
+    lib().orc_rmsnorm_bwd_add(M, H, _p(x), _p(_c(rstd, np.float64)), _p(_c(dy, np.float64)),
+                              _p(out))
+    return out
+
+
+def silu_mul_f64(g, u):
+    """act = SiLU(g) u in double, unrounded (g, u doubles)."""
+    g = _c(g, np.float64)
+    u = _c(u, np.float64)
+    act = np.empty_like(g)
+    lib().orc_silu_mul_f64(g.size, _p(g), _p(u), _p(act))
+    return act
+
+
+def silu_mul_bwd(dact, g, u, round_bf16=True):
+    """Gradients (dg, du) of act = SiLU(g) u for upstream dact (doubles)."""
+    dact = _c(dact, np.float64)
+    g = _c(g, np.float64)
+    u = _c(u, np.float64)
+    dg = np.empty_like(dact)
+    du = np.empty_like(dact)
+    lib().orc_silu_mul_bwd(dact.size, 1 if round_bf16 else 0, _p(dact), _p(g), _p(u), _p(dg),
+                           _p(du))
+    return dg, du
+
+
+def repeat_kv_bwd(dvr, KV, head_dim, round_bf16=True):
+    """dvr [M, H] -> dv [M, KV]: the sum over the query heads sharing each kv head."""
+    dvr = _c(dvr, np.float64)
+    M, H = dvr.shape
+    dv = np.empty((M, KV), np.float64)
+    lib().orc_repeat_kv_bwd(M, H, KV, head_dim, 1 if round_bf16 else 0, _p(dvr), _p(dv))
+    return dv

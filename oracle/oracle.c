@@ -58,15 +58,19 @@ double orc_bf16_to_f64(uint16_t b) { return (double)bits_f32((uint32_t)b << 16);
 uint16_t orc_f64_to_bf16(double d) {
   if (d == 0.0) return signbit(d) ? 0x8000 : 0x0000;
   double a = fabs(d);
-  if (a < 1.1754943508222875e-38) {
-    /* bf16 subnormal range: the float path is exact enough here */
-    return orc_f32_to_bf16((float)d);
-  }
   int e;
-  double m = frexp(a, &e);               /* a = m * 2^e, m in [0.5, 1) */
-  double s = nearbyint(ldexp(m, 8));     /* 8 significant bits, RNE    */
-  double r = ldexp(s, e - 8);            /* exactly representable      */
-  float rf = (float)r;                   /* exact                      */
+  double q;
+  if (a < 1.1754943508222875e-38) {
+    /* bf16 subnormal range: a fixed quantum of 2^-133 */
+    q = nearbyint(ldexp(a, 133));        /* one rounding, RNE          */
+    e = -133;
+  } else {
+    double m = frexp(a, &e);             /* a = m * 2^e, m in [0.5, 1) */
+    q = nearbyint(ldexp(m, 8));          /* 8 significant bits, RNE    */
+    e -= 8;
+  }
+  double r = ldexp(q, e);                /* exactly representable      */
+  float rf = (float)r;                   /* exact (or inf past the top) */
   uint16_t b = (uint16_t)(f32_bits(rf) >> 16);
   return d < 0 ? (uint16_t)(b | 0x8000) : b;
 }
@@ -418,6 +422,25 @@ static void rmsnorm_bwd(const orc_stack_cfg* c, int64_t H, const double* x,
 
 static double sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
 
+/* SwiGLU product act = SiLU(g) u = g sigmoid(g) u, and its partial
+ * derivatives for an upstream gradient d: d/du = d g sigmoid(g),
+ * d/dg = d u sigmoid(g) (1 + g (1 - sigmoid(g))). */
+static double silu_mul1(double g, double u) { return g * sigmoid(g) * u; }
+static void silu_mul_bwd1(double d, double g, double u, double* dg, double* du) {
+  const double sg = sigmoid(g);
+  *du = d * g * sg;
+  *dg = d * u * sg * (1.0 + g * (1.0 - sg));
+}
+
+/* Backward of the kv-head repeat: kv head kh collects the rep query heads
+ * kh*rep .. kh*rep + rep - 1 that read it. */
+static double repeat_kv_bwd1(const double* dvr_row, int64_t rep, int64_t hd, int64_t kh,
+                             int64_t d) {
+  double sum = 0.0;
+  for (int64_t t = 0; t < rep; ++t) sum += dvr_row[(kh * rep + t) * hd + d];
+  return sum;
+}
+
 typedef struct {
   double *h, *a, *rstd1, *v, *vr, *h1, *b, *rstd2, *g, *u, *act;
   uint32_t* mask[ORC_NLIN];
@@ -427,6 +450,13 @@ void orc_stack_fwd_bwd(const orc_stack_cfg* c, uint32_t step,
                        const orc_stack_params* prm, const double* h0,
                        double* loss, double* h_out, double* const* dA,
                        double* const* dB) {
+  orc_stack_fwd_bwd_mb(c, step, 0, 1, prm, h0, loss, h_out, dA, dB);
+}
+
+void orc_stack_fwd_bwd_mb(const orc_stack_cfg* c, uint32_t step, uint32_t microbatch,
+                          int n_micro, const orc_stack_params* prm, const double* h0,
+                          double* loss, double* h_out, double* const* dA,
+                          double* const* dB) {
   const int64_t M = c->M, H = c->H, KV = c->KV, I = c->I, hd = c->head_dim;
   const int L = c->n_layers;
   const int64_t rep = H / KV;
@@ -443,7 +473,7 @@ void orc_stack_fwd_bwd(const orc_stack_cfg* c, uint32_t step,
     layer_saved* s = &S[l];
     for (int li = 0; li < ORC_NLIN; ++li) {
       s->mask[li] = (uint32_t*)malloc(sizeof(uint32_t) * M * nK[li] / 32);
-      orc_dropout_mask(c->seed, step, (uint32_t)l, (uint32_t)li, 0, c->p, M,
+      orc_dropout_mask(c->seed, step, (uint32_t)l, (uint32_t)li, microbatch, c->p, M,
                        nK[li], s->mask[li]);
     }
     const int base = l * ORC_NLIN;
@@ -490,7 +520,7 @@ void orc_stack_fwd_bwd(const orc_stack_cfg* c, uint32_t step,
     for (int64_t i = 0; i < M * I; ++i) {
       s->g[i] = rb(c, s->g[i]);
       s->u[i] = rb(c, s->u[i]);
-      s->act[i] = rb(c, s->g[i] * sigmoid(s->g[i]) * s->u[i]);
+      s->act[i] = rb(c, silu_mul1(s->g[i], s->u[i]));
     }
     double* d = scratch;
     lin_fwd(c, H, I, s->act, prm->Wq[base + ORC_DOWN], prm->A[base + ORC_DOWN],
@@ -500,12 +530,13 @@ void orc_stack_fwd_bwd(const orc_stack_cfg* c, uint32_t step,
 
   double ss = 0.0;
   for (int64_t i = 0; i < M * H; ++i) ss += h[i] * h[i];
-  *loss = 0.5 * ss / (double)(M * H);
+  /* this micro-batch's share of the step loss (1/n_micro) sum_mb 0.5 mean(h^2) */
+  *loss = 0.5 * ss / (double)(M * H) / (double)n_micro;
   if (h_out) memcpy(h_out, h, sizeof(double) * M * H);
 
   if (dA && dB) {
     double* dh = (double*)malloc(sizeof(double) * M * H);
-    for (int64_t i = 0; i < M * H; ++i) dh[i] = h[i] / (double)(M * H);
+    for (int64_t i = 0; i < M * H; ++i) dh[i] = h[i] / ((double)(M * H) * (double)n_micro);
     double* dYb = (double*)malloc(sizeof(double) * M * (H > I ? H : I));
     double* dx = (double*)malloc(sizeof(double) * M * (H > I ? H : I));
     double* dx2 = (double*)malloc(sizeof(double) * M * H);
@@ -523,9 +554,10 @@ void orc_stack_fwd_bwd(const orc_stack_cfg* c, uint32_t step,
       double* dg = (double*)malloc(sizeof(double) * M * I);
       double* du = (double*)malloc(sizeof(double) * M * I);
       for (int64_t i = 0; i < M * I; ++i) {
-        double g = s->g[i], sg = sigmoid(g);
-        du[i] = rb(c, dact[i] * g * sg);
-        dg[i] = rb(c, dact[i] * s->u[i] * sg * (1.0 + g * (1.0 - sg)));
+        double gi, ui;
+        silu_mul_bwd1(dact[i], s->g[i], s->u[i], &gi, &ui);
+        dg[i] = rb(c, gi);
+        du[i] = rb(c, ui);
       }
       double* db = dx2;
       memset(db, 0, sizeof(double) * M * H);
@@ -550,12 +582,8 @@ void orc_stack_fwd_bwd(const orc_stack_cfg* c, uint32_t step,
       double* dv = dYb;
       for (int64_t m = 0; m < M; ++m)
         for (int64_t kh = 0; kh < KV / hd; ++kh)
-          for (int64_t d = 0; d < hd; ++d) {
-            double sum = 0.0;
-            for (int64_t t = 0; t < rep; ++t)
-              sum += dvr[m * H + (kh * rep + t) * hd + d];
-            dv[m * KV + kh * hd + d] = rb(c, sum);
-          }
+          for (int64_t d = 0; d < hd; ++d)
+            dv[m * KV + kh * hd + d] = rb(c, repeat_kv_bwd1(dvr + m * H, rep, hd, kh, d));
       double* da = dx2;
       memset(da, 0, sizeof(double) * M * H);
       lin_bwd(c, KV, H, s->a, prm->Wq[base + ORC_V], prm->A[base + ORC_V],
@@ -610,10 +638,50 @@ void orc_rmsnorm_bf16(int64_t M, int64_t H, double eps, const double* x, uint16_
 }
 
 void orc_silu_mul_bf16(int64_t n, const uint16_t* g, const uint16_t* u, uint16_t* act) {
+  for (int64_t i = 0; i < n; ++i) act[i] = orc_f64_to_bf16(silu_mul1(bf(g[i]), bf(u[i])));
+}
+
+void orc_silu_mul_f64(int64_t n, const double* g, const double* u, double* act) {
+  for (int64_t i = 0; i < n; ++i) act[i] = silu_mul1(g[i], u[i]);
+}
+
+void orc_rmsnorm_f64(int64_t M, int64_t H, double eps, int round_bf16, const double* x,
+                     double* y, double* rstd) {
+  orc_stack_cfg c;
+  memset(&c, 0, sizeof(c));
+  c.M = M;
+  c.eps = eps;
+  c.round_bf16 = round_bf16;
+  rmsnorm_fwd(&c, H, x, y, rstd);
+}
+
+void orc_rmsnorm_bwd_add(int64_t M, int64_t H, const double* x, const double* rstd,
+                         const double* dy, double* dx) {
+  orc_stack_cfg c;
+  memset(&c, 0, sizeof(c));
+  c.M = M;
+  rmsnorm_bwd(&c, H, x, rstd, dy, dx);
+}
+
+void orc_silu_mul_bwd(int64_t n, int round_bf16, const double* dact, const double* g,
+                      const double* u, double* dg, double* du) {
   for (int64_t i = 0; i < n; ++i) {
-    double gv = bf(g[i]);
-    act[i] = orc_f64_to_bf16(gv * sigmoid(gv) * bf(u[i]));
+    double a, b;
+    silu_mul_bwd1(dact[i], g[i], u[i], &a, &b);
+    dg[i] = round_bf16 ? bf(orc_f64_to_bf16(a)) : a;
+    du[i] = round_bf16 ? bf(orc_f64_to_bf16(b)) : b;
   }
+}
+
+void orc_repeat_kv_bwd(int64_t M, int64_t H, int64_t KV, int64_t head_dim, int round_bf16,
+                       const double* dvr, double* dv) {
+  const int64_t rep = H / KV;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t kh = 0; kh < KV / head_dim; ++kh)
+      for (int64_t d = 0; d < head_dim; ++d) {
+        const double v = repeat_kv_bwd1(dvr + m * H, rep, head_dim, kh, d);
+        dv[m * KV + kh * head_dim + d] = round_bf16 ? bf(orc_f64_to_bf16(v)) : v;
+      }
 }
 
 void orc_repeat_kv(int64_t M, int64_t H, int64_t KV, int64_t head_dim, const uint16_t* v,

@@ -121,6 +121,16 @@ void orc_stack_fwd_bwd(const orc_stack_cfg* cfg, uint32_t step,
                        const orc_stack_params* prm, const double* h0,
                        double* loss, double* h_out,
                        double* const* dA, double* const* dB);
+/* The same for micro-batch `microbatch` of a step with gradient
+ * accumulation over n_micro micro-batches: the dropout keys carry the
+ * micro-batch index, and the step loss is the mean over the micro-batches,
+ * so this call returns its share 0.5 mean(h_L^2) / n_micro and the
+ * gradients of that share (the step's gradient is the sum over the
+ * micro-batches). */
+void orc_stack_fwd_bwd_mb(const orc_stack_cfg* cfg, uint32_t step, uint32_t microbatch,
+                          int n_micro, const orc_stack_params* prm, const double* h0,
+                          double* loss, double* h_out,
+                          double* const* dA, double* const* dB);
 
 /* The stack's pointwise / row pieces on their own (x in double):
  * RMSNorm with unit gain -> bf16 bits, rstd per row;
@@ -131,6 +141,23 @@ void orc_rmsnorm_bf16(int64_t M, int64_t H, double eps, const double* x, uint16_
 void orc_silu_mul_bf16(int64_t n, const uint16_t* g, const uint16_t* u, uint16_t* act);
 void orc_repeat_kv(int64_t M, int64_t H, int64_t KV, int64_t head_dim, const uint16_t* v,
                    uint16_t* vr);
+/* The same pieces as the stack computes them, in double; round_bf16 != 0
+ * rounds each output to bf16 where the stack stores bf16 (the normalised
+ * row; the SwiGLU input gradients dg, du; the repeat's input gradient dv).
+ *   SwiGLU:    act = g sigmoid(g) u (unrounded);
+ *   RMSNorm:   y = x rstd, rstd = 1 / sqrt(mean(x^2) + eps) per row;
+ *   its backward ADDS rstd dy - rstd^3 x (dy . x) / H to dx;
+ *   SwiGLU backward: du = d g sigmoid(g), dg = d u sigmoid(g)(1 + g(1 - sigmoid(g)));
+ *   repeat backward: dv[m, kh*hd + d] = sum_t dvr[m, (kh*rep + t)*hd + d]. */
+void orc_silu_mul_f64(int64_t n, const double* g, const double* u, double* act);
+void orc_rmsnorm_f64(int64_t M, int64_t H, double eps, int round_bf16, const double* x,
+                     double* y, double* rstd);
+void orc_rmsnorm_bwd_add(int64_t M, int64_t H, const double* x, const double* rstd,
+                         const double* dy, double* dx);
+void orc_silu_mul_bwd(int64_t n, int round_bf16, const double* dact, const double* g,
+                      const double* u, double* dg, double* du);
+void orc_repeat_kv_bwd(int64_t M, int64_t H, int64_t KV, int64_t head_dim, int round_bf16,
+                       const double* dvr, double* dv);
 
 /* PyTorch-default Adam (betas 0.9/0.999, eps 1e-8, no weight decay,
  * bias-corrected), one step t >= 1, in double. */

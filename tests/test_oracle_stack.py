@@ -105,3 +105,47 @@ def test_adam_constant_gradient_closed_form(orc):
         orc.adam_step(p, g.copy(), m, v, t, lr=lr, eps=eps)
         np.testing.assert_allclose(p, p0 - t * lr * g / (np.abs(g) + eps), rtol=1e-12, atol=1e-15)
     assert p[0] == p0[0]
+
+
+def test_gradient_accumulation_micro_batches(orc):
+    """A step with gradient accumulation over two micro-batches: the step
+    loss is the mean of the micro-batch losses and its gradient the sum of
+    the micro-batch calls' gradients (central differences of the step loss in
+    the exact mode); the micro-batch index enters the dropout keys, and one
+    micro-batch reduces to the plain step."""
+    cfg = orc.StackCfg(M=4, H=64, KV=32, I=128, head_dim=16, n_layers=1, r=2, p=0.25,
+                       round_bf16=False)
+    Wq, A, B = _toy(orc, cfg, seed=3)
+    h0s = [synth.stack_h0(3, 10 + mb, cfg.M, cfg.H).astype(np.float64) for mb in range(2)]
+
+    def step(Aa, Bb, backward=True):
+        tot, gA, gB = 0.0, None, None
+        for mb in range(2):
+            loss, _, dA, dB = orc.stack_fwd_bwd(cfg, 4, Wq, Aa, Bb, h0s[mb], backward=backward,
+                                                microbatch=mb, n_micro=2)
+            tot += loss
+            if backward:
+                gA = dA if gA is None else [x + y for x, y in zip(gA, dA)]
+                gB = dB if gB is None else [x + y for x, y in zip(gB, dB)]
+        return tot, gA, gB
+
+    _, gA, gB = step(A, B)
+    h = 2.0 ** -15
+    for li, which, pos in [(2, 0, (1, 5)), (3, 1, (7, 0)), (4, 0, (0, 9)), (6, 1, (3, 1))]:
+        arr = A if which == 0 else B
+        ap, am = [a.copy() for a in arr], [a.copy() for a in arr]
+        ap[li][pos] += h
+        am[li][pos] -= h
+        lp = step(ap, B, False)[0] if which == 0 else step(A, ap, False)[0]
+        lm = step(am, B, False)[0] if which == 0 else step(A, am, False)[0]
+        fd = (lp - lm) / (float(ap[li][pos]) - float(am[li][pos]))
+        g = (gA if which == 0 else gB)[li][pos]
+        assert abs(fd - g) <= 2e-6 * max(abs(g), 1e-6) + 1e-9, (li, which, fd, g)
+    # other micro-batch index, other masks: same input, other loss
+    l0 = orc.stack_fwd_bwd(cfg, 4, Wq, A, B, h0s[0], backward=False, microbatch=0, n_micro=2)[0]
+    l1 = orc.stack_fwd_bwd(cfg, 4, Wq, A, B, h0s[0], backward=False, microbatch=1, n_micro=2)[0]
+    assert l0 != l1
+    # one micro-batch is the plain step
+    r1 = orc.stack_fwd_bwd(cfg, 4, Wq, A, B, h0s[0])
+    r2 = orc.stack_fwd_bwd(cfg, 4, Wq, A, B, h0s[0], microbatch=0, n_micro=1)
+    assert r1[0] == r2[0] and all(np.array_equal(x, y) for x, y in zip(r1[2], r2[2]))
