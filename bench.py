@@ -194,22 +194,26 @@ def run_reference(args, rank):
 
 # ------------------------------------------------------------------------------ our arm
 class Graphed:
-    """A StackRun whose step is replayed from one captured CUDA graph."""
+    """A StackRun whose step is replayed from one captured CUDA graph (for a
+    streamed run, with timing events around every block copy)."""
 
     def __init__(self, ops, run, lr, stream):
         l0 = ops.kernel_launches()
         self.run, self.stream = run, stream
-        self.g = run.graph(lr, stream)
+        self.g = run.graph(lr, stream, time_copies=run.streamed)
         self.launches_per_step = ops.kernel_launches() - l0
         self.loss = run.loss
 
     def step(self, s, h0):
         self.g.step(s, h0, self.stream)
 
+    def copy_times_ms(self):
+        return self.g.copy_times_ms()
 
-def make_runs(ops, StackRun, torch, cfg, dev, streamed=True):
-    gens = {}
 
+def make_runs(ops, StackRun, torch, cfg, dev, streamed=True, resident=True):
+    """The streamed run (quantised straight into its pinned image) and the
+    resident run (a device copy of the same image)."""
     def gen(layer, lin):
         g = torch.Generator(device=dev)
         g.manual_seed(1_000_003 * layer + 7919 * lin + 17)
@@ -223,24 +227,29 @@ def make_runs(ops, StackRun, torch, cfg, dev, streamed=True):
         A = (torch.rand(16, K, generator=g, device=dev) * 2 - 1) / (K ** 0.5)
         B = torch.randn(N, 16, generator=g, device=dev) * 0.01
         return A, B
-    res = StackRun(cfg, BLOCK, False, wfn, pfn, device=dev)
-    stm = StackRun(cfg, BLOCK, True, wfn, pfn, device=dev, image_from=res) if streamed else None
+    stm = StackRun(cfg, BLOCK, True, wfn, pfn, device=dev) if streamed else None
+    res = None
+    if resident:
+        res = StackRun(cfg, BLOCK, False, wfn, pfn, device=dev, image_from=stm)
     return res, stm
 
 
-def time_steps(torch, dist, run, h0s, K, W, stream, e2e=None, nvtx=False):
-    """W warm-up steps, then K timed steps bracketed by barrier + sync."""
+def time_steps(torch, dist, run, h0s, K, W, stream, e2e=None, nvtx=False, losses=None):
+    """W warm-up steps, then K timed steps bracketed by barrier + sync.
+    Returns (seconds of the K steps, per-step ms from events on the stream).
+    losses: a device tensor [W + K] that receives every step's loss."""
     for i in range(W):
         run.step(i, h0s[i % len(h0s)])
+        if losses is not None:
+            losses[i:i + 1].copy_(run.loss)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
     if nvtx:
         torch.cuda.nvtx.range_push("timed")
-    e0.record(stream)
+    ev[0].record(stream)
     for i in range(K):
         s = W + i
         if e2e is None:
@@ -250,13 +259,142 @@ def time_steps(torch, dist, run, h0s, K, W, stream, e2e=None, nvtx=False):
             dev_h0.copy_(host_h0[s % len(host_h0)], non_blocking=True)
             run.step(s, dev_h0)
             host_loss[s].copy_(run.loss, non_blocking=True)
-    e1.record(stream)
+        if losses is not None:
+            losses[s:s + 1].copy_(run.loss)
+        ev[i + 1].record(stream)
     if nvtx:
         torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    return e0.elapsed_time(e1) / 1e3
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(K)]
+    return ev[0].elapsed_time(ev[K]) / 1e3, per
+
+
+def dist_ms(v):
+    v = list(v)
+    if not v:
+        return None
+    med = statistics.median(v)
+    return {"median": med, "min": min(v), "max": max(v), "mean": sum(v) / len(v), "n": len(v),
+            "n_above_1.2x_median": sum(1 for x in v if x > 1.2 * med)}
+
+
+def streamed_breakdown(torch, gstm, h0s, first_step, n, stream, t_compute_ms, block_bytes):
+    """n more streamed steps, each read back on its own: step time (events on
+    the compute stream), the copy stream's busy time (the sum of its block
+    copies' durations, from timing events captured in the graph) and the
+    per-copy rates.  Overlap per step = (T_compute + T_copy - T_step) / T_copy
+    with T_compute the resident step's median."""
+    steps, busy, rates, overlap = [], [], [], []
+    for i in range(n):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gstm.step(first_step + i, h0s[i % len(h0s)])
+        e1.record(stream)
+        e1.synchronize()
+        t = e0.elapsed_time(e1)
+        cp = gstm.copy_times_ms()
+        tc = sum(cp)
+        steps.append(t)
+        busy.append(tc)
+        rates += [block_bytes / (c / 1e3) / 1e9 for c in cp if c > 0]
+        overlap.append(max(0.0, min(1.0, (t_compute_ms + tc - t) / tc)) if tc > 0 else None)
+    ov = [o for o in overlap if o is not None]
+    return {"step_ms": dist_ms(steps), "copy_busy_ms": dist_ms(busy),
+            "copy_gbs": dist_ms(rates), "copies_per_step": len(cp),
+            "overlap_fraction": dist_ms(ov)}
+
+
+def measure_stack(ops, StackRun, torch, dist, cfg, dev, steps, warmup, e2e=True):
+    """Resident and streamed steps of one stack shape, both replayed from
+    CUDA graphs: timings, the streamed step's copy and overlap breakdown, the
+    bitwise comparison of every step, and the runs' device footprints."""
+    t0 = time.time()
+    res, stm = make_runs(ops, StackRun, torch, cfg, dev)
+    setup_s = time.time() - t0
+    M, H = cfg.M, cfg.H
+    nh0 = 4
+    h0s = [torch.randn(M * H, device=dev, generator=torch.Generator(device=dev).manual_seed(s))
+           for s in range(nh0)]
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+    gres = Graphed(ops, res, 2e-4, stream)
+    gstm = Graphed(ops, stm, 2e-4, stream)
+    n_all = warmup + steps
+    loss_res = torch.zeros(n_all, device=dev)
+    loss_stm = torch.zeros(n_all, device=dev)
+    # ---- resident step, replayed from one CUDA graph
+    torch.cuda.reset_peak_memory_stats(dev)
+    base_alloc = torch.cuda.memory_allocated(dev)
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", 0))) as clk:
+        t_res, per_res = time_steps(torch, dist, gres, h0s, steps, warmup, stream, nvtx=True,
+                                    losses=loss_res)
+    clocks = clk.summary()
+    # ---- streamed step through the public API with host buffers (e2e)
+    host_h0 = [h.cpu().pin_memory() for h in h0s]
+    dev_h0 = torch.empty(M * H, device=dev)
+    host_loss = torch.zeros(n_all, 1).pin_memory()
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", 0))) as clk2:
+        t_stm, per_stm = time_steps(torch, dist, gstm, h0s, steps, warmup, stream,
+                                    e2e=(host_h0, dev_h0, host_loss) if e2e else None,
+                                    losses=loss_stm)
+    clocks2 = clk2.summary()
+    alloc_growth = torch.cuda.max_memory_allocated(dev) - base_alloc - dev_h0.numel() * 4
+    err = ops.device_error()
+    # every step's loss, and after the same steps the whole optimizer state
+    bitwise = {"loss_every_step": bool(torch.equal(loss_res, loss_stm))}
+    for name in ("params", "grads", "adam_m", "adam_v"):
+        bitwise[name] = bool(torch.equal(getattr(res, name), getattr(stm, name)))
+    bitwise["all"] = all(bitwise.values())
+    bitwise["steps"] = n_all
+    nb = cfg.n_layers // BLOCK
+    bb = res.sizes["block_bytes"]
+    breakdown = streamed_breakdown(torch, gstm, h0s, n_all, 6, stream,
+                                   statistics.median(per_res), bb)
+    out = {
+        "t_res": t_res, "t_stm": t_stm, "per_res": per_res, "per_stm": per_stm,
+        "clocks": clocks, "clocks2": clocks2, "device_error_flags": err, "setup_s": setup_s,
+        "bitwise": bitwise, "breakdown": breakdown, "res": res, "stm": stm, "gres": gres,
+        "launches_per_step": gres.launches_per_step,
+        # the two turnaround blocks are not reloaded, and a replayed step starts from
+        # the window the previous step left (blocks 0 and 1)
+        "h2d_w": (2 * nb - 4) * bb, "block_bytes": bb, "nb": nb,
+        "alloc_growth_during_steps": int(alloc_growth),
+    }
+    torch.cuda.set_stream(torch.cuda.default_stream(dev))
+    return out
+
+
+def streaming_report(m, link_gbs, steps):
+    s_res, s_stm = m["t_res"] / steps, m["t_stm"] / steps
+    med_res = statistics.median(m["per_res"]) / 1e3
+    med_stm = statistics.median(m["per_stm"]) / 1e3
+    h2d_w = m["h2d_w"]
+    bd = m["breakdown"]
+    return {
+        "s_per_step_streamed": s_stm, "s_per_step_resident": s_res,
+        "s_per_step_streamed_median": med_stm, "s_per_step_resident_median": med_res,
+        "step_ms_streamed": dist_ms(m["per_stm"]), "step_ms_resident": dist_ms(m["per_res"]),
+        "slowdown": s_stm / s_res, "slowdown_median": med_stm / med_res,
+        "h2d_bytes_per_step": h2d_w, "block_copies_per_step": bd["copies_per_step"],
+        "h2d_link_peak_gbs": link_gbs,
+        "h2d_effective_gbs": h2d_w / s_stm / 1e9,
+        "h2d_effective_gbs_median_step": h2d_w / med_stm / 1e9,
+        "h2d_frac_of_link": (h2d_w / s_stm / 1e9) / link_gbs,
+        "h2d_frac_of_link_median_step": (h2d_w / med_stm / 1e9) / link_gbs,
+        "copy_floor_s_at_link_peak": h2d_w / (link_gbs * 1e9),
+        "breakdown_of_6_extra_steps": bd,
+        "bitwise_streamed_eq_resident": m["bitwise"],
+        "device_bytes_streamed": m["stm"].device_bytes(),
+        "device_bytes_resident": m["res"].device_bytes(),
+        "library_static_device_bytes": (48 << 20) + (4 << 20),
+        "torch_alloc_growth_during_steps": m["alloc_growth_during_steps"],
+        "pinned_host_bytes": m["nb"] * m["block_bytes"],
+        "setup_s": m["setup_s"], "device_error_flags": m["device_error_flags"],
+    }
 
 
 def roofline_calls(ops, torch, res, cfg):
@@ -439,6 +577,67 @@ def h2d_peak(torch, dev):
     return best
 
 
+def profile_link(torch):
+    """Host-link measurements: pinned host -> HBM copies of 32B-block size
+    (one cudaMemcpyAsync each, or cut into pieces, or split over two
+    streams), per-copy rates, the same copies beside a tensor-core load, and
+    the distribution over ~20 s of back-to-back copies."""
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    bb, nb = 1097072640, 16
+    host = torch.empty(nb * bb, dtype=torch.uint8, pin_memory=True)
+    host[::4096] = 1
+    win = torch.empty(2 * bb, dtype=torch.uint8, device=dev)
+    cs = torch.cuda.Stream(device=dev)
+
+    def copies(n, piece=None):
+        evs = []
+        with torch.cuda.stream(cs):
+            for i in range(n):
+                src = host[(i % nb) * bb:((i % nb) + 1) * bb]
+                dst = win[(i % 2) * bb:((i % 2) + 1) * bb]
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(cs)
+                if piece is None:
+                    dst.copy_(src, non_blocking=True)
+                else:
+                    for o in range(0, bb, piece):
+                        dst[o:o + piece].copy_(src[o:o + piece], non_blocking=True)
+                e1.record(cs)
+                evs.append((e0, e1))
+        torch.cuda.synchronize()
+        return [bb / (a.elapsed_time(b) / 1e3) / 1e9 for a, b in evs]
+
+    def d(g):
+        g = sorted(g)
+        return {"n": len(g), "min": round(g[0], 1), "median": round(statistics.median(g), 1),
+                "max": round(g[-1], 1), "below_0.8x_median": sum(1 for x in g if x < 0.8 * statistics.median(g))}
+    copies(4)
+    out = {"block_bytes": bb, "whole_block": d(copies(48)), "pieces_128MB": d(copies(32, 128 << 20)),
+           "pieces_32MB": d(copies(32, 32 << 20))}
+    a = torch.randn(8192, 8192, device=dev, dtype=torch.bfloat16)
+    b = torch.randn(8192, 8192, device=dev, dtype=torch.bfloat16)
+    ms = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(ms):
+        for _ in range(400):
+            a @ b
+    out["beside_bf16_matmul"] = d(copies(24))
+    torch.cuda.synchronize()
+    t_end = time.time() + 20
+    long = []
+    while time.time() < t_end:
+        long += copies(16)
+    out["back_to_back_20s"] = d(long)
+    hist = {}
+    for g in long:
+        k = int(g // 20) * 20
+        hist[k] = hist.get(k, 0) + 1
+    out["back_to_back_20s_histogram_gbs_bins_of_20"] = dict(sorted(hist.items()))
+    print(json.dumps({"profile_link": out}))
+
+
 def traffic_counters():
     """Per-launch DRAM traffic of the dominant kernel from the committed ncu
     summary, valid only while the kernel source is unchanged."""
@@ -458,6 +657,27 @@ def traffic_counters():
     return None
 
 
+SHAPE_72B = dict(M=512, H=8192, KV=1024, I=29568, head_dim=128, n_layers=80)
+
+
+def host_mem_available():
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except Exception:
+        pass
+    return None
+
+
+def release_host_cache(torch):
+    torch.cuda.empty_cache()
+    try:
+        torch._C._host_emptyCache()
+    except Exception:
+        pass
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -465,7 +685,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--quick", action="store_true", help="skip the 7B sub-benchmark")
+    ap.add_argument("--quick", action="store_true", help="skip the 7B and 72B sub-benchmarks")
+    ap.add_argument("--no-72b", action="store_true", help="skip the 72B-shaped streamed run")
     ap.add_argument("--profile-step", action="store_true",
                     help="only the resident run: W warm-up steps and one step inside the NVTX "
                          "range 'timed'; for an ncu launch list of one step")
@@ -475,6 +696,9 @@ def main():
     ap.add_argument("--profile-lora", choices=["gate", "down", "o"], default=None,
                     help="only run ws_lora_linear_fwd + _bwd three times on one 32B linear shape "
                          "at M=512; for an ncu capture of the LoRA-side kernels")
+    ap.add_argument("--profile-link", action="store_true",
+                    help="only measure pinned host -> HBM copies (block-sized, pieces, beside a "
+                         "matmul, 20 s back to back) and print their rate distributions")
     ap.add_argument("--profile-gemm", choices=["gate", "down", "o"], default=None,
                     help="only launch the dequant GEMM (forward + input gradient) twice on one "
                          "32B linear shape at M=512; for an ncu capture of that kernel")
@@ -497,21 +721,22 @@ def main():
     if args.profile_roofline:
         profile_roofline(torch)
         return
+    if args.profile_link:
+        profile_link(torch)
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    from weight_streaming_nf4_gb300 import ops
+    from weight_streaming_nf4_gb300 import ops, replicas
     from weight_streaming_nf4_gb300.stack import StackRun
     pk = peaks()
 
     cfg = ops.StackCfg(**SHAPE_32B)
     M, H = cfg.M, cfg.H
     flops = step_flops(M, H, cfg.KV, cfg.I, cfg.n_layers)
-    t_setup = time.time()
-    torch.cuda.reset_peak_memory_stats(dev)
     if args.profile_step:
         res, _ = make_runs(ops, StackRun, torch, cfg, dev, streamed=False)
         h0 = torch.randn(M * H, device=dev)
@@ -519,82 +744,32 @@ def main():
         assert ops.device_error() == 0
         print(json.dumps({"profile_step": "resident", "launches": ops.kernel_launches()}))
         return
-    res, stm = make_runs(ops, StackRun, torch, cfg, dev)
-    setup_s = time.time() - t_setup
-    nh0 = 4
-    h0s = [torch.randn(M * H, device=dev, generator=torch.Generator(device=dev).manual_seed(s))
-           for s in range(nh0)]
-    torch.cuda.synchronize()
-    stream = torch.cuda.Stream(device=dev)
-    torch.cuda.set_stream(stream)
-    gres = Graphed(ops, res, 2e-4, stream)
-    gstm = Graphed(ops, stm, 2e-4, stream)
-
-    # ---- resident step (value), replayed from one CUDA graph
-    with ClockSampler(local) as clk:
-        t_res = time_steps(torch, dist, gres, h0s, args.steps, args.warmup, stream, nvtx=True)
-    launches_res = gres.launches_per_step * args.steps
-    clocks = clk.summary()
-    # ---- streamed step through the public API with host buffers (e2e)
-    host_h0 = [h.cpu().pin_memory() for h in h0s]
-    dev_h0 = torch.empty(M * H, device=dev)
-    host_loss = torch.zeros(args.warmup + args.steps, 1).pin_memory()
-    with ClockSampler(local) as clk2:
-        t_stm = time_steps(torch, dist, gstm, h0s, args.steps, args.warmup, stream,
-                           e2e=(host_h0, dev_h0, host_loss))
-    clocks2 = clk2.summary()
-    err = ops.device_error()
-    # bitwise check of the two modes on one extra step
-    gres.step(1000, h0s[0])
-    gstm.step(1000, h0s[0])
-    torch.cuda.synchronize()
-    bitwise = bool(torch.equal(res.loss, stm.loss) and torch.equal(res.params, stm.params)
-                   and torch.equal(res.adam_v, stm.adam_v))
-    # the eager resident step (one launch per kernel), for comparison with the graph replay
-    t_eager = time_steps(torch, dist, res, h0s, 2, 1, stream)
-
-    from weight_streaming_nf4_gb300 import replicas
-    t_res = replicas.max_over_ranks(t_res, dist, dev)
-    t_stm = replicas.max_over_ranks(t_stm, dist, dev)
+    m = measure_stack(ops, StackRun, torch, dist, cfg, dev, args.steps, args.warmup)
+    t_res = replicas.max_over_ranks(m["t_res"], dist, dev)
+    t_stm = replicas.max_over_ranks(m["t_stm"], dist, dev)
     value = replicas.whole_job_rate(flops, args.steps, world, t_res) / 1e12
     e2e_val = replicas.whole_job_rate(flops, args.steps, world, t_stm) / 1e12
-    nb = cfg.n_layers // BLOCK
-    bb = res.sizes["block_bytes"]
-    # the two turnaround blocks are not reloaded, and a replayed step starts from
-    # the window the previous step left (blocks 0 and 1)
-    h2d_w = (2 * nb - 4) * bb
-    h2d_bytes = h2d_w + M * H * 4
+    h2d_bytes = m["h2d_w"] + M * H * 4
 
     extra = {}
     if rank == 0:
+        res = m["res"]
         roof = gemm_roofline(ops, torch, res, cfg, pk["bf16"])
         roof["traffic"] = traffic_counters()
         link = h2d_peak(torch, dev)
-        peak_res = torch.cuda.max_memory_allocated(dev)
         extra["roofline"] = {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac",
                                                    "traffic")}
         extra["roofline"]["kernel"] = ("k_nf4_gemm (fwd + input-gradient), the 7 linear shapes "
                                        "of 8 layers, M=512")
         extra["roofline"]["peak_kind"] = ("bf16 dense burst, " + pk["src"])
         extra["roofline"]["avg_launch_us"] = roof["avg_launch_us"]
-        t_copy = h2d_w / (link * 1e9)
-        s_res, s_stm = t_res / args.steps, t_stm / args.steps
-        extra["streaming"] = {
-            "s_per_step_streamed": s_stm, "s_per_step_resident": s_res,
-            "s_per_step_resident_eager": t_eager / 2,
-            "slowdown": s_stm / s_res,
-            "h2d_bytes_per_step": h2d_w, "h2d_link_peak_gbs": link,
-            "h2d_effective_gbs": h2d_w / s_stm / 1e9,
-            "h2d_frac_of_link": (h2d_w / s_stm / 1e9) / link,
-            "copy_time_at_link_peak_s": t_copy,
-            "overlap_fraction": max(0.0, min(1.0, (s_res + t_copy - s_stm) / t_copy)),
-            "bitwise_streamed_eq_resident": bitwise,
-            "device_bytes_streamed": stm.device_bytes(), "device_bytes_resident": res.device_bytes(),
-            "torch_peak_allocated_bytes": peak_res,
-            "pinned_host_bytes": nb * bb,
-        }
+        extra["streaming"] = streaming_report(m, link, args.steps)
+        # the eager resident step (one launch per kernel), for comparison with the graph replay
+        t_eager, _ = time_steps(torch, None, res, [torch.zeros(M * H, device=dev)], 2, 1,
+                                torch.cuda.current_stream())
+        extra["streaming"]["s_per_step_resident_eager"] = t_eager / 2
         if not args.quick:
-            extra["linear_7b"] = {f"M{m}": linear_7b(ops, torch, dev, m) for m in (512, 2048)}
+            extra["linear_7b"] = {f"M{mm}": linear_7b(ops, torch, dev, mm) for mm in (512, 2048)}
         if world == 1 and not args.no_cpu_baseline:
             run, cflops, cores, _ = oracle_sample(256, H, cfg.KV, cfg.I)
             tc = run()
@@ -602,6 +777,7 @@ def main():
                 "value": cflops / tc / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
                 "sample": (f"one 32B-shaped layer's 7 NF4-LoRA linears fwd+bwd on 256 of 512 tokens "
                            f"({cflops / 1e9:.1f} GFLOP, {tc:.1f} s), plain C oracle fp64")}
+    out = None
     if rank == 0:
         out = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
@@ -612,12 +788,37 @@ def main():
             "config": arm_config(world),
             "pct_bf16_peak": 100.0 * value / world / pk["bf16_sustained"],
             "e2e": {"value": e2e_val, "unit": "TFLOPS", "h2d_bytes_per_step": h2d_bytes,
-                    "d2h_bytes_per_step": 4, "s_per_step": t_stm / args.steps},
-            "gpu_launches": int(launches_res),
-            "clocks": clocks, "clocks_streamed": clocks2,
-            "device_error_flags": err, "setup_s": setup_s,
+                    "d2h_bytes_per_step": 4, "s_per_step": t_stm / args.steps,
+                    "s_per_step_median": statistics.median(m["per_stm"]) / 1e3},
+            "gpu_launches": int(m["launches_per_step"] * args.steps),
+            "clocks": m["clocks"], "clocks_streamed": m["clocks2"],
+            "device_error_flags": m["device_error_flags"], "setup_s": m["setup_s"],
         }
         out.update(extra)
+    # ---- the 72B-shaped stack, streamed and resident (one GPU only)
+    if rank == 0 and world == 1 and not args.quick and not args.no_72b:
+        del m, res
+        release_host_cache(torch)
+        cfg72 = ops.StackCfg(**SHAPE_72B)
+        need = nf4_bytes(cfg72.H, cfg72.KV, cfg72.I, cfg72.n_layers)
+        avail = host_mem_available()
+        if avail is not None and avail < need + (16 << 30):
+            out["qwen72b"] = {"skipped": f"host memory available {avail} < pinned image {need} + 16 GiB"}
+        else:
+            k72 = min(args.steps, 5)
+            m72 = measure_stack(ops, StackRun, torch, None, cfg72, dev, k72, 3)
+            rep = streaming_report(m72, extra["streaming"]["h2d_link_peak_gbs"], k72)
+            f72 = step_flops(cfg72.M, cfg72.H, cfg72.KV, cfg72.I, cfg72.n_layers)
+            rep["workload"] = ("qwen2.5-72b-shaped stack, 80 layers, H 8192, kv 1024, I 29568, "
+                               "seq 512, blocks of 4, 2-slot window")
+            rep["steps"] = k72
+            rep["tflops_resident"] = f72 * k72 / m72["t_res"] / 1e12
+            rep["tflops_streamed"] = f72 * k72 / m72["t_stm"] / 1e12
+            rep["host_mem_available_bytes"] = avail
+            out["qwen72b"] = rep
+            del m72
+            release_host_cache(torch)
+    if rank == 0:
         print(json.dumps(out))
     if dist is not None:
         dist.destroy_process_group()

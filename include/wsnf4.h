@@ -2,24 +2,25 @@
  * wsnf4.h -- C ABI of libwsnf4.so: the streamed frozen-NF4-base LoRA linear
  * on one GB300 (sm_103a).
  *
- * The method (Poros, "Blockwise residency for frozen-base QLoRA"):
- *  - the frozen base is stored as 4-bit NormalFloat (NF4) with one fp32
- *    absmax per 64 consecutive weights of a row; NF4 is the only precision
- *    whose streamed run is gated bit-for-bit against a resident run
- *    (docs, "Limitations" page, section "What 0.00e+00 means");
- *  - every linear computes y = x W'^T + (alpha/r) B A dropout(x) and the
- *    backward "propagates gradients only to the adapters and block inputs.
- *    Frozen weights are never differentiated" (research page "Poros");
- *  - frozen blocks pass through a small GPU window with asynchronous
- *    prefetch; activations are kept only at block boundaries; the backward
- *    walks the blocks in reverse, reloads each, recomputes its forward with
- *    the same dropout randomness and back-propagates (research page
- *    "Poros", paragraphs "Poros replaces persistent residency..." and
- *    "The rest of the training step...");
- *  - recomputation must redraw identical dropout masks (research page,
- *    "The catch is dropout" / "RNG state capture").  Here masks come from a
+ * The method (Poros, blockwise residency for frozen-base QLoRA).  Citations
+ * name the page and its section; the research page "Poros" has no section
+ * headings, so its paragraphs are named by their subject.
+ *  - The frozen base is stored as 4-bit NormalFloat (NF4), one fp32 absmax
+ *    per 64 consecutive weights of a row; NF4 is the precision whose
+ *    streamed run is held bit for bit to a resident run ("Limitations",
+ *    section "What 0.00e+00 means").
+ *  - Every linear computes y = x W'^T + (alpha/r) B A dropout(x); the
+ *    backward produces gradients for the adapters and the block inputs
+ *    only, never for the frozen weights ("Poros", training-step paragraph).
+ *  - Frozen blocks pass through a small GPU window that is prefetched
+ *    asynchronously; only block-boundary activations are kept; the backward
+ *    visits the blocks in reverse, reloads each one, recomputes its forward
+ *    and back-propagates ("Poros", streamed-residency and training-step
+ *    paragraphs).
+ *  - The recompute must draw the forward's dropout masks again ("Poros",
+ *    dropout and RNG-capture paragraphs).  Here masks come from a
  *    counter-based Philox4x32-10 keyed by (seed, step, layer, linear,
- *    micro-batch): no RNG state is captured or restored.
+ *    micro-batch), so nothing is snapshotted or restored.
  *
  * Conventions for every entry point:
  *  - Return value: ws_status (0 = WS_OK).  Argument and shape errors are
@@ -89,6 +90,11 @@ enum {
 
 enum { WS_DTYPE_BF16 = 0, WS_DTYPE_F32 = 1 };
 
+/* Accumulation flags of ws_lora_linear_bwd. */
+enum { WS_ACC_DX = 1,     /* add the input gradient into an fp32 dX          */
+       WS_ACC_GRADS = 2   /* add dA and dB into the existing gradients        */
+};
+
 /* Linear ids inside a layer of the synthetic stack. */
 enum { WS_LIN_Q = 0, WS_LIN_K = 1, WS_LIN_V = 2, WS_LIN_O = 3,
        WS_LIN_GATE = 4, WS_LIN_UP = 5, WS_LIN_DOWN = 6, WS_NLIN = 7 };
@@ -125,15 +131,36 @@ const char* ws_status_string(ws_status st);
 /* Reads (and clears) the library's device error word, which kernels set when
  * a bounded wait times out.  Synchronises the current device.  *flags = 0
  * means no kernel reported a problem.  Returns WS_ERR_TIMEOUT if a flag was
- * set, WS_OK otherwise. */
+ * set, WS_OK otherwise.  Every wait in the library's kernels gives up after
+ * one second of wall-clock time: the kernel then sets a bit below, lets its
+ * copies in flight land, frees its tensor memory and returns; kernels that
+ * start while the word is set skip their work, until the word is read and
+ * cleared here (which also clears the library's cross-CTA words). */
+enum { WS_DERR_PIPELINE_MASK = 0x3F, /* a pipeline barrier wait inside a kernel gave up  */
+       WS_DERR_BAD_CONFIG = 0x40,    /* a kernel refused its launch configuration       */
+       WS_DERR_TIMEOUT_PEER = 0x80   /* a wait for another CTA's published result gave up */
+};
 ws_status ws_device_error(uint32_t* flags);
+
+/* Failure-detection self-check (no counterpart on the method's pages; it
+ * exercises the bounded waits above).  Launches one small kernel on `stream`
+ * that waits for a cross-CTA completion word that nothing sets, through the
+ * same bounded wait the dequant GEMM's stream-K finisher uses, but giving up
+ * after limit_us microseconds (1 .. 1000000) instead of one second.  The
+ * wait gives up, sets WS_DERR_TIMEOUT_PEER and the kernel returns; the CUDA
+ * context stays usable, and the next ws_device_error reports and clears it.
+ * Nothing faults or traps. */
+ws_status ws_selfcheck_bounded_wait(uint32_t limit_us, ws_stream_t stream);
 
 /* Number of CUDA kernels this library has launched in the process so far
  * (host-side counter; copies are not counted). */
 uint64_t ws_kernel_launches(void);
 
 /* ---- NF4 quantisation ------------------------------------------------------ */
-/* Quantises a bf16 weight W [N, K] (device) into NF4 codes [N, K/2] and
+/* The frozen base's precision ("Limitations", section "What 0.00e+00 means";
+ * the research page "Poros", block-streamed NF4 loader paragraphs, where
+ * each tensor is quantised as it is loaded).
+ * Quantises a bf16 weight W [N, K] (device) into NF4 codes [N, K/2] and
  * block-major absmax [K/64, N] (device, caller-allocated).
  * Per 64-block: absmax = max |w| (fp32); v = w / absmax as an IEEE fp32
  * division; code = number of the 15 midpoints mid_i = fp32(fp32(c_i +
@@ -150,7 +177,9 @@ ws_status ws_quantize_nf4(const uint16_t* W, int64_t N, int64_t K, uint8_t* code
 /* Workspace (device bytes) needed by ws_lora_linear_fwd / _bwd for a shape. */
 ws_status ws_lora_workspace_size(ws_lora_shape sh, size_t* bytes);
 
-/* y = x W'^T + s * U B^T with U = (mask . x) A^T and s = (alpha/r)/(1-p)
+/* The forward of one NF4-LoRA linear ("Poros", training-step paragraph: the
+ * frozen base is only read; the adapter sees dropout(x)).
+ * y = x W'^T + s * U B^T with U = (mask . x) A^T and s = (alpha/r)/(1-p)
  * (inverted dropout folded into the scale).  W' is the NF4 weight
  * dequantised on the fly inside the tensor-core GEMM; nothing dequantised
  * is ever written to memory.
@@ -168,26 +197,30 @@ ws_status ws_lora_linear_fwd(const ws_nf4* W, const uint16_t* x, const float* A,
                              void* workspace, size_t ws_bytes, ws_stream_t stream);
 
 /* ---- LoRA linear backward ------------------------------------------------ */
-/* Given dY [M,N] bf16 computes
+/* The backward of one linear: gradients for the adapters and the input only,
+ * none for the frozen weight ("Poros", training-step paragraph).
+ * Given dY [M,N] bf16 computes
  *   G  = dY B                              (fp32, internal)
  *   dB = s dY^T U_saved                    [N, r] fp32 (overwritten)
  *   dA = s G^T (mask . x)                  [r, K] fp32 (overwritten)
  *   dX = dY W' + s (G A) . mask            [M, K] bf16 or fp32
- * dX_dtype: WS_DTYPE_BF16 or WS_DTYPE_F32; dX_accumulate != 0 adds into an
- * existing fp32 dX (fixed order: the new contribution is added to the old
- * value once, in fp32).  mask_saved may be NULL: the masks are then
+ * dX_dtype: WS_DTYPE_BF16 or WS_DTYPE_F32.  accumulate is a set of WS_ACC_*
+ * flags: WS_ACC_DX adds into an existing fp32 dX, WS_ACC_GRADS adds dA and
+ * dB into the existing gradients (gradient accumulation over micro-batches);
+ * either way the new contribution is added to the old value once, in fp32,
+ * after its own fixed-order sum.  mask_saved may be NULL: the masks are then
  * regenerated from `key` (bit-identical to the forward's).
  * No atomics: dA, dB and split contractions are reduced in a fixed order. */
 ws_status ws_lora_linear_bwd(const ws_nf4* W, const uint16_t* x, const float* A,
                              const float* B, ws_lora_shape sh, ws_dropout_key key,
                              const float* U_saved, const uint32_t* mask_saved,
                              const uint16_t* dY, void* dX, int32_t dX_dtype,
-                             int32_t dX_accumulate, float* dA, float* dB,
+                             int32_t accumulate, float* dA, float* dB,
                              void* workspace, size_t ws_bytes, ws_stream_t stream);
 
 /* ---- the frozen NF4 product alone ---------------------------------------------- */
 /* The dequant GEMM of the LoRA linear without adapter or dropout (a frozen NF4
- * linear):
+ * linear; the base term of the training-step paragraph of "Poros"):
  *   transpose_w == 0:  out[M,N] = act[M,K] W'^T   (forward)
  *   transpose_w != 0:  out[M,K] = act[M,N] W'     (input gradient)
  * act bf16 (device); out bf16 or fp32 (out_dtype) (device); workspace >=
@@ -209,10 +242,14 @@ ws_status ws_nf4_matmul(const ws_nf4* W, const uint16_t* act, int64_t M, int32_t
  * completion flags) lives in a
  * file-scope device array of WS_NOALLOC_SCRATCH_BYTES (48 MiB) inside the
  * library, which every GPU that loads the library holds until the process
- * exits.  Nothing is allocated or freed by the call.
+ * exits.  Only the partial tiles live in that array; the completion flags
+ * of the split come from the library's shared ring of cross-CTA words,
+ * which every launch of the library uses and leaves at zero.  Nothing is
+ * allocated or freed by the call.
  *  - The first call on a device looks up that device's address of the
- *    array (cudaGetSymbolAddress, once per device, with the device current);
- *    make that first call before any stream capture.
+ *    array, and of the flag ring, with cudaGetSymbolAddress (once per
+ *    device, with the device current); make that first call before any
+ *    stream capture.
  *  - Every call shares the one array: calls that overlap on the GPU (other
  *    streams, other host threads) race on it and must be serialised by the
  *    caller.  Each call overwrites all scratch it reads, so no clearing is
@@ -227,7 +264,9 @@ ws_status ws_nf4_matmul_noalloc(const ws_nf4* W, const uint16_t* act, int64_t M,
                                 ws_stream_t stream);
 
 /* ---- the synthetic stack ----------------------------------------------------- */
-/* One layer: h -> RMSNorm -> q,k,v (NF4-LoRA) -> v repeated across the
+/* The transformer layers the method trains, with the attention core replaced
+ * ("Poros", learning-problem paragraph: the layer computation is that of a
+ * resident run).  One layer: h -> RMSNorm -> q,k,v (NF4-LoRA) -> v repeated across the
  * H/head_dim query heads (head h reads kv head h / (H/KV)) in place of the
  * attention core -> o -> residual; -> RMSNorm -> gate, up -> SiLU(gate)*up
  * -> down -> residual.  RMSNorm has unit gain and eps `eps`, computed in
@@ -282,33 +321,59 @@ ws_status ws_stack_saved_offset(const ws_stack_cfg* cfg, int32_t field, int32_t 
 ws_status ws_stack_param_offset(const ws_stack_cfg* cfg, int32_t layer, int32_t lin,
                                 int64_t* off_A, int64_t* off_B);
 
-/* Forward of layers [first_layer, first_layer + n_layers) whose NF4
+/* Intermediate gradients of a layer's backward inside the stack workspace
+ * (for inspection; after ws_block_backward_recompute they hold the values of
+ * the block's first layer, the last one processed):
+ *   WS_WK_Y1    bf16 [M,H]  bf16(dh1), the o projection's dY
+ *   WS_WK_DACT  fp32 [M,I]  gradient at act (the down projection's dX)
+ *   WS_WK_DG, WS_WK_DU  bf16 [M,I]  gradients at the gate and up outputs
+ *   WS_WK_DB    fp32 [M,H]  gradient at b (sum of the gate and up dX)
+ *   WS_WK_DH1   fp32 [M,H]  gradient at h1 (layer output gradient + RMSNorm2 backward)
+ *   WS_WK_DVR   fp32 [M,H]  gradient at repeat(v) (the o projection's dX)
+ *   WS_WK_DV    bf16 [M,KV] gradient at v (sum over the query heads of each kv head)
+ *   WS_WK_DA    fp32 [M,H]  gradient at a (the v projection's dX)
+ *   WS_WK_YOUT  bf16 [M,H]  the last forward linear output (the down projection's y) */
+enum { WS_WK_Y1 = 0, WS_WK_DACT = 1, WS_WK_DG = 2, WS_WK_DU = 3, WS_WK_DB = 4, WS_WK_DH1 = 5,
+       WS_WK_DVR = 6, WS_WK_DV = 7, WS_WK_DA = 8, WS_WK_YOUT = 9 };
+ws_status ws_stack_workspace_offset(const ws_stack_cfg* cfg, int32_t block_layers, int32_t field,
+                                    size_t* offset);
+
+/* The forward of one block ("Poros", streamed-residency paragraph: a block
+ * is loaded, run forward, and only its boundary activation is kept).
+ * Forward of layers [first_layer, first_layer + n_layers) whose NF4
  * weights are the block image at `block_weights` (device).  h_in / h_out
  * [M, H] fp32 (device; may not alias).  params: device LoRA parameters.
  * saved: device area of n_layers * saved_bytes_layer that receives every
  * activation the backward needs (resident mode), or NULL to keep nothing
- * (streamed mode: only h_out survives).  step keys the dropout masks. */
+ * (streamed mode: only h_out survives).  step and microbatch key the
+ * dropout masks. */
 ws_status ws_block_forward(const ws_stack_cfg* cfg, const void* block_weights,
                            int32_t first_layer, int32_t n_layers, const float* params,
-                           uint32_t step, const float* h_in, float* h_out, void* saved,
-                           void* workspace, size_t ws_bytes, ws_stream_t stream);
+                           uint32_t step, uint32_t microbatch, const float* h_in, float* h_out,
+                           void* saved, void* workspace, size_t ws_bytes, ws_stream_t stream);
 
-/* Backward of the same layers.  If `saved` is NULL the block's forward is
+/* The backward of one block ("Poros", streamed-residency and RNG-capture
+ * paragraphs: the block is reloaded, its forward recomputed with the same
+ * dropout, then differentiated for the adapters and the block input).
+ * Backward of the same layers.  If `saved` is NULL the block's forward is
  * first recomputed from the boundary activation h_in (same kernels, same
  * Philox keys, hence bit-identical intermediates) into the workspace; if
  * `saved` is the area ws_block_forward filled, it is used directly
  * (resident mode).  dh_out [M,H] fp32 is the gradient at the block output;
  * dh_in (may alias dh_out) receives the gradient at the block input.
  * grads: device LoRA gradients (same layout as params); the block's entries
- * are overwritten. */
+ * are overwritten, or, with grad_accumulate != 0, added to (gradient
+ * accumulation over micro-batches). */
 ws_status ws_block_backward_recompute(const ws_stack_cfg* cfg, const void* block_weights,
                                       int32_t first_layer, int32_t n_layers,
-                                      const float* params, uint32_t step, const float* h_in,
-                                      const void* saved, const float* dh_out, float* dh_in,
-                                      float* grads, void* workspace, size_t ws_bytes,
-                                      ws_stream_t stream);
+                                      const float* params, uint32_t step, uint32_t microbatch,
+                                      const float* h_in, const void* saved, const float* dh_out,
+                                      float* dh_in, float* grads, int32_t grad_accumulate,
+                                      void* workspace, size_t ws_bytes, ws_stream_t stream);
 
-/* Copy one block (bytes) from pinned host memory to a device window slot
+/* The window's prefetch ("Poros", training-step paragraph: frozen blocks pass
+ * through a small GPU window, prefetched asynchronously on CUDA streams).
+ * Copy one block (bytes) from pinned host memory to a device window slot
  * on `copy_stream`.  If wait_event is not NULL the copy first waits for it
  * (the slot's previous user is done); if done_event is not NULL it is
  * recorded after the copy.  A pageable source gives WS_ERR_NOT_PINNED. */
@@ -325,15 +390,18 @@ typedef struct {
   float* grads;             /* device: n_params                                        */
   float* adam_m;            /* device: n_params, first moment                          */
   float* adam_v;            /* device: n_params, second moment                         */
-  float* boundary;          /* device: (n_blocks + 1) * M * H fp32 block-boundary h    */
+  float* boundary;          /* device: n_micro * (n_blocks + 1) * M * H fp32 block-boundary h */
   void* saved;              /* device: n_layers * saved_bytes_layer (resident), else NULL */
-  float* dh;                /* device: 2 * M * H fp32 gradient ping-pong               */
+  float* dh;                /* device: max(2, n_micro) * M * H fp32 gradients            */
   void* workspace;          /* device: workspace_bytes                                  */
   size_t workspace_bytes;
   float* loss;              /* device: 1 float, receives the loss                      */
 } ws_stack_buffers;
 
-/* One full training step of the stack: forward over the blocks, loss,
+/* One training step ("Poros", training-step paragraph: streamed forward,
+ * reverse-order reload-recompute-backward, then one optimizer step equal to
+ * a resident run's).
+ * One full training step of the stack: forward over the blocks, loss,
  * backward over the blocks in reverse, one Adam step (PyTorch defaults:
  * betas 0.9 / 0.999, eps 1e-8, bias-corrected, no weight decay) with
  * learning rate lr at Adam step t = step + 1.
@@ -350,6 +418,34 @@ typedef struct {
 ws_status ws_stack_train_step(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
                               const ws_stack_buffers* buf, uint32_t step, const float* h0,
                               float lr, ws_stream_t compute, ws_stream_t copy_stream);
+
+/* Gradient accumulation ("Poros", block-major and parity-gate paragraphs:
+ * the pages run accumulation at 2 and 4 micro-batches and refuse the
+ * block-major order with dropout, because their sequential RNG would be
+ * consumed in another order).  Here every micro-batch has its own dropout
+ * keys (the micro-batch index is in the Philox counter), so the order in
+ * which micro-batches and blocks are visited changes nothing:
+ *   WS_GA_MICROBATCH_MAJOR  forward and backward of micro-batch 0, then 1, ...;
+ *   WS_GA_BLOCK_MAJOR       (streamed) each block is loaded once per
+ *                           direction and every micro-batch runs through it.
+ * The step loss is the mean of the micro-batch losses; adapter gradients are
+ * summed in micro-batch order (micro-batch 0 writes, the others add), so
+ * both orders and a resident run are bitwise identical.  A resident run
+ * ignores `order`.  h0 holds n_micro inputs [n_micro, M, H]; the buffers
+ * grow as ws_stack_buffers states.
+ * time_copies != 0 (graphs of streamed steps only) records timing events
+ * around every block copy; ws_stack_graph_copy_times reads them. */
+enum { WS_GA_MICROBATCH_MAJOR = 0, WS_GA_BLOCK_MAJOR = 1 };
+typedef struct {
+  int32_t n_micro;      /* micro-batches per step, >= 1 */
+  int32_t order;        /* WS_GA_*                       */
+  int32_t time_copies;  /* 0 or 1                        */
+} ws_step_opts;
+/* opts == NULL: one micro-batch, no timing (ws_stack_train_step). */
+ws_status ws_stack_train_step_ex(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
+                                 const ws_step_opts* opts, const ws_stack_buffers* buf,
+                                 uint32_t step, const float* h0, float lr, ws_stream_t compute,
+                                 ws_stream_t copy_stream);
 
 /* ---- the same step as one CUDA graph ---------------------------------------------
  * ws_stack_graph_create captures everything ws_stack_train_step enqueues
@@ -375,6 +471,16 @@ typedef struct ws_step_graph ws_step_graph;
 ws_status ws_stack_graph_create(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
                                 const ws_stack_buffers* buf, float lr, ws_stream_t compute,
                                 ws_stream_t copy_stream, ws_step_graph** out);
+ws_status ws_stack_graph_create_ex(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
+                                   const ws_step_opts* opts, const ws_stack_buffers* buf, float lr,
+                                   ws_stream_t compute, ws_stream_t copy_stream,
+                                   ws_step_graph** out);
+/* Durations (ms) of the block copies of the graph's last replay, in issue
+ * order, from the timing events of a graph created with time_copies: *n
+ * receives their number, the first `capacity` go to ms.  Waits for the
+ * replay's last copy.  WS_ERR_INVALID if the graph times no copies or has
+ * not been replayed. */
+ws_status ws_stack_graph_copy_times(ws_step_graph* g, float* ms, int32_t capacity, int32_t* n);
 ws_status ws_stack_graph_step(ws_step_graph* g, uint32_t step, const float* h0,
                               ws_stream_t compute);
 ws_status ws_stack_graph_destroy(ws_step_graph* g);

@@ -135,6 +135,24 @@ def test_dx_accumulate(ops, orc):
     assert torch.equal(acc, base + dX)
 
 
+def test_grad_accumulate(ops, orc):
+    """WS_ACC_GRADS adds dA and dB into the given gradients: one fp32 add of
+    the fresh gradient, bitwise; the input gradient is unaffected."""
+    M, N, K = 192, 512, 1024
+    d, W, key = _linear(ops, orc, M, N, K, "gacc", lin=2)
+    x, A, B, dY = bf16_to_dev(d["x"]), f32_to_dev(d["A"]), f32_to_dev(d["B"]), bf16_to_dev(d["dY"])
+    _, U, mask = ops.lora_linear_fwd(W, x, A, B, key)
+    dX, dA, dB = ops.lora_linear_bwd(W, x, A, B, key, U, mask, dY, dX_f32=True)
+    a0 = torch.randn_like(dA)
+    b0 = torch.randn_like(dB)
+    a, b = a0.clone(), b0.clone()
+    dX2, _, _ = ops.lora_linear_bwd(W, x, A, B, key, U, mask, dY, dX_f32=True, dA=a, dB=b,
+                                    grad_accumulate=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a, a0 + dA) and torch.equal(b, b0 + dB)
+    assert torch.equal(dX2, dX)
+
+
 @pytest.mark.parametrize("M,N,K,lin", [(512, 18944, 3584, 4), (512, 3584, 18944, 6),
                                         (2048, 512, 3584, 2)])
 def test_full_size_sampled_rows(ops, orc, M, N, K, lin):

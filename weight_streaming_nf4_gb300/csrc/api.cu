@@ -82,6 +82,11 @@ ws_status ws_device_error(uint32_t* flags) {
   return *flags ? WS_ERR_TIMEOUT : WS_OK;
 }
 
+ws_status ws_selfcheck_bounded_wait(uint32_t limit_us, ws_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000u) return WS_ERR_INVALID;
+  return cuda_status(run_wait_selfcheck(limit_us, (cudaStream_t)stream));
+}
+
 ws_status ws_quantize_nf4(const uint16_t* W, int64_t N, int64_t K, uint8_t* codes, float* absmax,
                           ws_stream_t stream) {
   if (!W || !codes || !absmax) return WS_ERR_INVALID;
@@ -117,12 +122,14 @@ ws_status ws_lora_linear_fwd(const ws_nf4* W, const uint16_t* x, const float* A,
 ws_status ws_lora_linear_bwd(const ws_nf4* W, const uint16_t* x, const float* A, const float* B,
                              ws_lora_shape sh, ws_dropout_key key, const float* U_saved,
                              const uint32_t* mask_saved, const uint16_t* dY, void* dX,
-                             int32_t dX_dtype, int32_t dX_accumulate, float* dA, float* dB,
+                             int32_t dX_dtype, int32_t accumulate, float* dA, float* dB,
                              void* workspace, size_t ws_bytes, ws_stream_t stream) {
   ws_status s = check_linear(W, sh, key);
   if (s != WS_OK) return s;
   if (!x || !A || !B || !U_saved || !dY || !dX || !dA || !dB || !workspace) return WS_ERR_INVALID;
   if (dX_dtype != WS_DTYPE_BF16 && dX_dtype != WS_DTYPE_F32) return WS_ERR_INVALID;
+  if (accumulate & ~(WS_ACC_DX | WS_ACC_GRADS)) return WS_ERR_INVALID;
+  const int dX_accumulate = (accumulate & WS_ACC_DX) ? 1 : 0;
   if (dX_accumulate && dX_dtype != WS_DTYPE_F32) return WS_ERR_INVALID;
   if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(U_saved) || !aligned16(dY) ||
       !aligned16(dX) || !aligned16(dA) || !aligned16(dB) || !aligned16(workspace) ||
@@ -131,8 +138,9 @@ ws_status ws_lora_linear_bwd(const ws_nf4* W, const uint16_t* x, const float* A,
   if (ws_bytes < linear_workspace_bytes(sh.M, sh.N, sh.K)) return WS_ERR_OOM;
   return cuda_status(linear_bwd(view_of(W), x, A, B, sh.M, lora_scale(sh, key.p),
                                 make_drop_key(key), U_saved, mask_saved, dY, dX,
-                                dX_dtype == WS_DTYPE_F32 ? 1 : 0, dX_accumulate ? 1 : 0, dA, dB,
-                                workspace, (cudaStream_t)stream));
+                                dX_dtype == WS_DTYPE_F32 ? 1 : 0, dX_accumulate, dA, dB,
+                                (accumulate & WS_ACC_GRADS) ? 1 : 0, workspace,
+                                (cudaStream_t)stream));
 }
 
 ws_status ws_nf4_matmul_workspace_size(int64_t M, int64_t N, int64_t K, int32_t transpose_w,
@@ -218,6 +226,14 @@ ws_status ws_stack_saved_offset(const ws_stack_cfg* cfg, int32_t field, int32_t 
   return stack_saved_offset(*cfg, field, lin, offset) ? WS_OK : WS_ERR_INVALID;
 }
 
+ws_status ws_stack_workspace_offset(const ws_stack_cfg* cfg, int32_t block_layers, int32_t field,
+                                   size_t* offset) {
+  ws_status s = stack_check(cfg);
+  if (s != WS_OK) return s;
+  if (!offset || block_layers < 1 || block_layers > cfg->n_layers) return WS_ERR_INVALID;
+  return stack_ws_offset(*cfg, block_layers, field, offset) ? WS_OK : WS_ERR_INVALID;
+}
+
 ws_status ws_stack_param_offset(const ws_stack_cfg* cfg, int32_t layer, int32_t lin,
                                 int64_t* off_A, int64_t* off_B) {
   ws_status s = stack_check(cfg);
@@ -229,32 +245,34 @@ ws_status ws_stack_param_offset(const ws_stack_cfg* cfg, int32_t layer, int32_t 
 }
 
 ws_status ws_block_forward(const ws_stack_cfg* cfg, const void* block_weights, int32_t first_layer,
-                           int32_t n_layers, const float* params, uint32_t step, const float* h_in,
-                           float* h_out, void* saved, void* workspace, size_t ws_bytes,
-                           ws_stream_t stream) {
+                           int32_t n_layers, const float* params, uint32_t step, uint32_t microbatch,
+                           const float* h_in, float* h_out, void* saved, void* workspace,
+                           size_t ws_bytes, ws_stream_t stream) {
   ws_status s = stack_check(cfg);
   if (s != WS_OK) return s;
   if (!block_weights || !params || !h_in || !h_out || !workspace) return WS_ERR_INVALID;
   if (n_layers < 1 || first_layer < 0 || first_layer + n_layers > cfg->n_layers) return WS_ERR_SHAPE;
-  if (h_in == h_out) return WS_ERR_INVALID;
+  if (h_in == h_out || microbatch > 0xFFFFFFu) return WS_ERR_INVALID;
   if (!aligned16(block_weights) || !aligned16(params) || !aligned16(h_in) || !aligned16(h_out) ||
       !aligned16(workspace) || (saved && !aligned16(saved)))
     return WS_ERR_ALIGN;
   if (ws_bytes < stack_ws_bytes(*cfg, n_layers)) return WS_ERR_OOM;
   return cuda_status(block_forward(*cfg, n_layers, block_weights, first_layer, n_layers, params,
-                                   step, nullptr, h_in, h_out, saved, workspace,
+                                   step, microbatch, nullptr, h_in, h_out, saved, workspace,
                                    (cudaStream_t)stream));
 }
 
 ws_status ws_block_backward_recompute(const ws_stack_cfg* cfg, const void* block_weights,
                                       int32_t first_layer, int32_t n_layers, const float* params,
-                                      uint32_t step, const float* h_in, const void* saved,
-                                      const float* dh_out, float* dh_in, float* grads,
-                                      void* workspace, size_t ws_bytes, ws_stream_t stream) {
+                                      uint32_t step, uint32_t microbatch, const float* h_in,
+                                      const void* saved, const float* dh_out, float* dh_in,
+                                      float* grads, int32_t grad_accumulate, void* workspace,
+                                      size_t ws_bytes, ws_stream_t stream) {
   ws_status s = stack_check(cfg);
   if (s != WS_OK) return s;
   if (!block_weights || !params || !dh_out || !dh_in || !grads || !workspace) return WS_ERR_INVALID;
   if (!saved && !h_in) return WS_ERR_INVALID;
+  if (microbatch > 0xFFFFFFu) return WS_ERR_INVALID;
   if (n_layers < 1 || first_layer < 0 || first_layer + n_layers > cfg->n_layers) return WS_ERR_SHAPE;
   if (!aligned16(block_weights) || !aligned16(params) || !aligned16(dh_out) || !aligned16(dh_in) ||
       !aligned16(grads) || !aligned16(workspace) || (saved && !aligned16(saved)) ||
@@ -262,8 +280,8 @@ ws_status ws_block_backward_recompute(const ws_stack_cfg* cfg, const void* block
     return WS_ERR_ALIGN;
   if (ws_bytes < stack_ws_bytes(*cfg, n_layers)) return WS_ERR_OOM;
   return cuda_status(block_backward(*cfg, n_layers, block_weights, first_layer, n_layers, params,
-                                    step, nullptr, h_in, saved, dh_out, dh_in, grads, workspace,
-                                    (cudaStream_t)stream));
+                                    step, microbatch, nullptr, h_in, saved, dh_out, dh_in, grads,
+                                    grad_accumulate ? 1 : 0, workspace, (cudaStream_t)stream));
 }
 
 ws_status ws_stream_block_h2d(const void* pinned_src, void* dev_dst, size_t bytes,
@@ -291,10 +309,17 @@ ws_status ws_stream_block_h2d(const void* pinned_src, void* dev_dst, size_t byte
 // ---------------------------------------------------------------------------- training step
 namespace {
 
+// Events of one step: the window slots' loaded / freed events, the fork and
+// join of the copy stream and, when copies are timed, one start / end pair
+// per block copy (recorded as external events so they become nodes of a
+// captured graph and carry the replay's timestamps).
 struct StepEvents {
   cudaEvent_t loaded[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr};
   cudaEvent_t fork = nullptr, join = nullptr;
-  cudaError_t create() {
+  int n_timed = 0, cap_timed = 0;
+  cudaEvent_t* t0 = nullptr;
+  cudaEvent_t* t1 = nullptr;
+  cudaError_t create(int copies_to_time) {
     cudaError_t e = cudaSuccess;
     for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
       e = cudaEventCreateWithFlags(&loaded[i], cudaEventDisableTiming);
@@ -302,6 +327,16 @@ struct StepEvents {
     }
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+    if (e == cudaSuccess && copies_to_time > 0) {
+      t0 = new (std::nothrow) cudaEvent_t[copies_to_time]();
+      t1 = new (std::nothrow) cudaEvent_t[copies_to_time]();
+      if (!t0 || !t1) return cudaErrorMemoryAllocation;
+      for (int i = 0; i < copies_to_time && e == cudaSuccess; ++i) {
+        e = cudaEventCreate(&t0[i]);
+        if (e == cudaSuccess) e = cudaEventCreate(&t1[i]);
+      }
+      cap_timed = copies_to_time;
+    }
     return e;
   }
   void destroy() {
@@ -313,8 +348,35 @@ struct StepEvents {
     if (fork) cudaEventDestroy(fork);
     if (join) cudaEventDestroy(join);
     fork = join = nullptr;
+    for (int i = 0; i < cap_timed; ++i) {
+      if (t0 && t0[i]) cudaEventDestroy(t0[i]);
+      if (t1 && t1[i]) cudaEventDestroy(t1[i]);
+    }
+    delete[] t0;
+    delete[] t1;
+    t0 = t1 = nullptr;
+    cap_timed = n_timed = 0;
   }
 };
+
+struct StepOpts {
+  int n_micro = 1;
+  int order = WS_GA_MICROBATCH_MAJOR;
+  bool time_copies = false;
+};
+
+ws_status read_opts(const ws_step_opts* o, StepOpts* out) {
+  StepOpts r;
+  if (o) {
+    if (o->n_micro < 1 || o->n_micro > 0xFFFFFF) return WS_ERR_INVALID;
+    if (o->order != WS_GA_MICROBATCH_MAJOR && o->order != WS_GA_BLOCK_MAJOR) return WS_ERR_INVALID;
+    r.n_micro = o->n_micro;
+    r.order = o->order;
+    r.time_copies = o->time_copies != 0;
+  }
+  *out = r;
+  return WS_OK;
+}
 
 ws_status check_step(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
                      const ws_stack_buffers* buf, const void* copy_stream) {
@@ -334,20 +396,28 @@ ws_status check_step(const ws_stack_cfg* cfg, int32_t block_layers, int32_t stre
   return WS_OK;
 }
 
-// Everything of one step after the step word and boundary[0] (= h0) are
-// set.  Reads the step from the device word, so eager calls and graph
-// replays run the same kernels with the same arguments.
+// Everything of one step after the step word and the micro-batches' block-0
+// boundaries (= h0) are set.  Reads the step from the device word, so eager
+// calls and graph replays run the same kernels with the same arguments.
 //
 // Streamed mode keeps a 2-slot window: slot s holds block b with s = b % 2.
 // The copy of block b+1 is issued before block b's compute so it runs on the
 // copy engine meanwhile; a copy into a slot waits for the compute stream's
 // last use of that slot.  A block still resident in its slot (the last two at
-// the forward/backward turnaround) is not copied again.  The copy stream is
-// forked from and joined back into the compute stream, so the whole step
-// can be captured as one graph.
+// the forward/backward turnaround, or between micro-batches) is not copied
+// again.  The copy stream is forked from and joined back into the compute
+// stream, so the whole step can be captured as one graph.
 // warm: the window already holds blocks 0 and 1 (slots 0 and 1), as the
 // previous step's backward left it; their copies are skipped.
-ws_status step_body(const ws_stack_cfg& cfg, int block_layers, bool streamed,
+//
+// Gradient accumulation over n_micro micro-batches (each with its own h0,
+// boundary activations, output gradient and dropout keys): micro-batch-major
+// runs the whole forward and backward of one micro-batch after the other;
+// block-major (streamed) loads each block once per direction and runs every
+// micro-batch through it.  Both add the micro-batches' adapter gradients in
+// the same order (micro-batch 0 writes, the others add), so the two orders,
+// and a resident run, give bitwise the same step.
+ws_status step_body(const ws_stack_cfg& cfg, int block_layers, bool streamed, const StepOpts& o,
                     const ws_stack_buffers& buf, float lr, cudaStream_t cs, cudaStream_t ps,
                     StepEvents& ev, bool warm = false) {
   const int nb = cfg.n_layers / block_layers;
@@ -355,7 +425,7 @@ ws_status step_body(const ws_stack_cfg& cfg, int block_layers, bool streamed,
   const size_t slayer = stack_saved_layer(cfg);
   const int64_t MH = cfg.M * cfg.H;
   const int64_t np = stack_n_params(cfg);
-  float* bnd = buf.boundary;
+  const int nm = o.n_micro;
   const uint32_t* stepw = stack_step_word(cfg, block_layers, buf.workspace);
   int slot_block[2] = {-1, -1};
   bool slot_used[2] = {false, false};
@@ -366,22 +436,31 @@ ws_status step_body(const ws_stack_cfg& cfg, int block_layers, bool streamed,
   }
   const uint8_t* host = static_cast<const uint8_t*>(buf.host_weights);
   uint8_t* window = static_cast<uint8_t*>(buf.window);
+  ev.n_timed = 0;
 #define WS_STEP_TRY(x)                          \
   do {                                          \
     if ((x) != cudaSuccess) return WS_ERR_CUDA; \
   } while (0)
   auto ensure = [&](int blk) -> ws_status {
+    if (blk < 0 || blk >= nb) return WS_OK;
     const int sl = blk % 2;
     if (slot_block[sl] == blk) return WS_OK;
+    cudaStream_t st = ps;
+    if (slot_used[sl] && cudaStreamWaitEvent(st, ev.freed[sl], 0) != cudaSuccess) return WS_ERR_CUDA;
+    const bool timed = ev.n_timed < ev.cap_timed;
+    if (timed && cudaEventRecordWithFlags(ev.t0[ev.n_timed], st, cudaEventRecordExternal) != cudaSuccess)
+      return WS_ERR_CUDA;
     ws_status r = ws_stream_block_h2d(host + (size_t)blk * bbytes, window + (size_t)sl * bbytes,
-                                      bbytes, (ws_stream_t)ps,
-                                      slot_used[sl] ? (ws_event_t)ev.freed[sl] : nullptr,
-                                      (ws_event_t)ev.loaded[sl]);
-    if (r == WS_OK) {
-      slot_block[sl] = blk;
-      slot_copied[sl] = true;
+                                      bbytes, (ws_stream_t)st, nullptr, (ws_event_t)ev.loaded[sl]);
+    if (r != WS_OK) return r;
+    if (timed) {
+      if (cudaEventRecordWithFlags(ev.t1[ev.n_timed], st, cudaEventRecordExternal) != cudaSuccess)
+        return WS_ERR_CUDA;
+      ++ev.n_timed;
     }
-    return r;
+    slot_block[sl] = blk;
+    slot_copied[sl] = true;
+    return WS_OK;
   };
   // the compute stream waits for a slot's copy only if one was issued in this step
   auto wait_loaded = [&](int blk) -> cudaError_t {
@@ -392,42 +471,60 @@ ws_status step_body(const ws_stack_cfg& cfg, int block_layers, bool streamed,
     if (streamed) return window + (size_t)(blk % 2) * bbytes;
     return static_cast<const uint8_t*>(buf.dev_weights) + (size_t)blk * bbytes;
   };
+  auto bnd = [&](int mb, int b) { return buf.boundary + ((size_t)mb * (nb + 1) + b) * MH; };
+  auto dh = [&](int mb) { return buf.dh + (size_t)mb * MH; };
+  auto saved = [&](int b) -> void* {
+    return streamed ? nullptr : static_cast<uint8_t*>(buf.saved) + (size_t)b * block_layers * slayer;
+  };
+  auto release = [&](int b) -> cudaError_t {
+    if (!streamed) return cudaSuccess;
+    slot_used[b % 2] = true;
+    return cudaEventRecord(ev.freed[b % 2], cs);
+  };
+  auto fwd = [&](int b, int mb) {
+    return block_forward(cfg, block_layers, block_ptr(b), b * block_layers, block_layers,
+                         buf.params, 0u, (uint32_t)mb, stepw, bnd(mb, b), bnd(mb, b + 1),
+                         saved(b), buf.workspace, cs);
+  };
+  auto bwd = [&](int b, int mb) {
+    return block_backward(cfg, block_layers, block_ptr(b), b * block_layers, block_layers,
+                          buf.params, 0u, (uint32_t)mb, stepw, bnd(mb, b), saved(b), dh(mb),
+                          dh(mb), buf.grads, mb > 0 ? 1 : 0, buf.workspace, cs);
+  };
+  auto loss = [&](int mb) {
+    return loss_and_grad(cfg, block_layers, bnd(mb, nb), dh(mb), buf.loss, nm, mb > 0 ? 1 : 0,
+                         buf.workspace, cs);
+  };
   ws_status rc = WS_OK;
   if (streamed) {
     WS_STEP_TRY(cudaEventRecord(ev.fork, cs));
     WS_STEP_TRY(cudaStreamWaitEvent(ps, ev.fork, 0));
   }
-  // ---- forward
-  if (streamed && (rc = ensure(0)) != WS_OK) return rc;
-  for (int b = 0; b < nb; ++b) {
-    if (streamed && b + 1 < nb && (rc = ensure(b + 1)) != WS_OK) return rc;
-    if (streamed) WS_STEP_TRY(wait_loaded(b));
-    void* sv = streamed ? nullptr : static_cast<uint8_t*>(buf.saved) + (size_t)b * block_layers * slayer;
-    WS_STEP_TRY(block_forward(cfg, block_layers, block_ptr(b), b * block_layers, block_layers,
-                              buf.params, 0u, stepw, bnd + (size_t)b * MH, bnd + (size_t)(b + 1) * MH,
-                              sv, buf.workspace, cs));
-    if (streamed) {
-      slot_used[b % 2] = true;
-      WS_STEP_TRY(cudaEventRecord(ev.freed[b % 2], cs));
+  // Micro-batch-major in a resident run; block-major only changes the order
+  // of a streamed run (a resident run loads nothing).
+  const bool block_major = streamed && o.order == WS_GA_BLOCK_MAJOR;
+  const int passes = block_major ? 1 : nm;
+  for (int pass = 0; pass < passes; ++pass) {
+    const int mb0 = block_major ? 0 : pass, mb1 = block_major ? nm : pass + 1;
+    // ---- forward
+    if (streamed && (rc = ensure(0)) != WS_OK) return rc;
+    for (int b = 0; b < nb; ++b) {
+      if (streamed && (rc = ensure(b + 1)) != WS_OK) return rc;
+      if (streamed) WS_STEP_TRY(wait_loaded(b));
+      for (int mb = mb0; mb < mb1; ++mb) WS_STEP_TRY(fwd(b, mb));
+      WS_STEP_TRY(release(b));
     }
-  }
-  // ---- loss
-  WS_STEP_TRY(loss_and_grad(cfg, block_layers, bnd + (size_t)nb * MH, buf.dh, buf.loss, buf.workspace, cs));
-  // ---- backward, blocks in reverse
-  for (int b = nb - 1; b >= 0; --b) {
-    if (streamed) {
-      if ((rc = ensure(b)) != WS_OK) return rc;
-      if (b - 1 >= 0 && (rc = ensure(b - 1)) != WS_OK) return rc;
-      WS_STEP_TRY(wait_loaded(b));
-    }
-    const void* sv =
-        streamed ? nullptr : static_cast<uint8_t*>(buf.saved) + (size_t)b * block_layers * slayer;
-    WS_STEP_TRY(block_backward(cfg, block_layers, block_ptr(b), b * block_layers, block_layers,
-                               buf.params, 0u, stepw, bnd + (size_t)b * MH, sv, buf.dh, buf.dh,
-                               buf.grads, buf.workspace, cs));
-    if (streamed) {
-      slot_used[b % 2] = true;
-      WS_STEP_TRY(cudaEventRecord(ev.freed[b % 2], cs));
+    // ---- loss
+    for (int mb = mb0; mb < mb1; ++mb) WS_STEP_TRY(loss(mb));
+    // ---- backward, blocks in reverse
+    for (int b = nb - 1; b >= 0; --b) {
+      if (streamed) {
+        if ((rc = ensure(b)) != WS_OK) return rc;
+        if ((rc = ensure(b - 1)) != WS_OK) return rc;
+        WS_STEP_TRY(wait_loaded(b));
+      }
+      for (int mb = mb0; mb < mb1; ++mb) WS_STEP_TRY(bwd(b, mb));
+      WS_STEP_TRY(release(b));
     }
   }
   // ---- optimizer
@@ -440,13 +537,23 @@ ws_status step_body(const ws_stack_cfg& cfg, int block_layers, bool streamed,
   return WS_OK;
 }
 
-ws_status step_prologue(const ws_stack_cfg& cfg, int block_layers, const ws_stack_buffers& buf,
-                        uint32_t step, const float* h0, cudaStream_t cs) {
+// The block copies one step can issue at most (for timing events).
+int max_copies(const ws_stack_cfg& cfg, int block_layers, const StepOpts& o) {
+  const int nb = cfg.n_layers / block_layers;
+  return 2 * nb * (o.order == WS_GA_BLOCK_MAJOR ? 1 : o.n_micro);
+}
+
+ws_status step_prologue(const ws_stack_cfg& cfg, int block_layers, const StepOpts& o,
+                        const ws_stack_buffers& buf, uint32_t step, const float* h0,
+                        cudaStream_t cs) {
   uint32_t* stepw = stack_step_word(cfg, block_layers, buf.workspace);
   if (set_step(stepw, step, cs) != cudaSuccess) return WS_ERR_CUDA;
-  if (cudaMemcpyAsync(buf.boundary, h0, (size_t)(cfg.M * cfg.H) * 4, cudaMemcpyDeviceToDevice,
-                      cs) != cudaSuccess)
-    return WS_ERR_CUDA;
+  const int nb = cfg.n_layers / block_layers;
+  const size_t MH = (size_t)(cfg.M * cfg.H);
+  for (int mb = 0; mb < o.n_micro; ++mb)
+    if (cudaMemcpyAsync(buf.boundary + (size_t)mb * (nb + 1) * MH, h0 + (size_t)mb * MH, MH * 4,
+                        cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
+      return WS_ERR_CUDA;
   return WS_OK;
 }
 
@@ -459,51 +566,69 @@ ws_status step_prologue(const ws_stack_cfg& cfg, int block_layers, const ws_stac
 struct ws_step_graph {
   ws_stack_cfg cfg;
   int32_t block_layers;
+  StepOpts opts;
   ws_stack_buffers buf;
   StepEvents ev[2];
   cudaGraph_t graph[2] = {nullptr, nullptr};
   cudaGraphExec_t exec[2] = {nullptr, nullptr};
   bool warm_ok = false;   // a warm capture exists
   bool window_warm = false;
+  int last = -1;          // capture replayed last
 };
 
 extern "C" {
 
-ws_status ws_stack_train_step(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
-                              const ws_stack_buffers* buf, uint32_t step, const float* h0, float lr,
-                              ws_stream_t compute, ws_stream_t copy_stream) {
+ws_status ws_stack_train_step_ex(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
+                                 const ws_step_opts* opts, const ws_stack_buffers* buf,
+                                 uint32_t step, const float* h0, float lr, ws_stream_t compute,
+                                 ws_stream_t copy_stream) {
   ws_status s = check_step(cfg, block_layers, streamed, buf, copy_stream);
   if (s != WS_OK) return s;
+  StepOpts o;
+  if ((s = read_opts(opts, &o)) != WS_OK) return s;
+  if (o.time_copies) return WS_ERR_INVALID;  // timed copies are read from a graph
   if (!h0) return WS_ERR_INVALID;
   const cudaStream_t cs = (cudaStream_t)compute;
-  s = step_prologue(*cfg, block_layers, *buf, step, h0, cs);
+  s = step_prologue(*cfg, block_layers, o, *buf, step, h0, cs);
   if (s != WS_OK) return s;
   StepEvents ev;
-  if (streamed && ev.create() != cudaSuccess) {
+  if (streamed && ev.create(0) != cudaSuccess) {
     ev.destroy();
     return WS_ERR_CUDA;
   }
-  s = step_body(*cfg, block_layers, streamed != 0, *buf, lr, cs, (cudaStream_t)copy_stream, ev);
+  s = step_body(*cfg, block_layers, streamed != 0, o, *buf, lr, cs, (cudaStream_t)copy_stream, ev);
   ev.destroy();
   return s;
 }
 
-ws_status ws_stack_graph_create(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
-                                const ws_stack_buffers* buf, float lr, ws_stream_t compute,
-                                ws_stream_t copy_stream, ws_step_graph** out) {
+ws_status ws_stack_train_step(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
+                              const ws_stack_buffers* buf, uint32_t step, const float* h0, float lr,
+                              ws_stream_t compute, ws_stream_t copy_stream) {
+  return ws_stack_train_step_ex(cfg, block_layers, streamed, nullptr, buf, step, h0, lr, compute,
+                                copy_stream);
+}
+
+ws_status ws_stack_graph_create_ex(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
+                                   const ws_step_opts* opts, const ws_stack_buffers* buf, float lr,
+                                   ws_stream_t compute, ws_stream_t copy_stream,
+                                   ws_step_graph** out) {
   if (!out) return WS_ERR_INVALID;
   *out = nullptr;
   ws_status s = check_step(cfg, block_layers, streamed, buf, copy_stream);
   if (s != WS_OK) return s;
+  StepOpts o;
+  if ((s = read_opts(opts, &o)) != WS_OK) return s;
+  if (o.time_copies && !streamed) return WS_ERR_INVALID;
   ws_step_graph* g = new (std::nothrow) ws_step_graph();
   if (!g) return WS_ERR_OOM;
   g->cfg = *cfg;
   g->block_layers = block_layers;
+  g->opts = o;
   g->buf = *buf;
   const cudaStream_t cs = (cudaStream_t)compute;
   g->warm_ok = streamed != 0 && cfg->n_layers / block_layers >= 2;
   for (int v = 0; v < (g->warm_ok ? 2 : 1) && s == WS_OK; ++v) {
-    if (g->ev[v].create() != cudaSuccess) {
+    if (g->ev[v].create(o.time_copies ? max_copies(*cfg, block_layers, o) : 0) != cudaSuccess) {
       s = WS_ERR_CUDA;
       break;
     }
@@ -511,7 +636,7 @@ ws_status ws_stack_graph_create(const ws_stack_cfg* cfg, int32_t block_layers, i
       s = WS_ERR_CUDA;
       break;
     }
-    s = step_body(*cfg, block_layers, streamed != 0, *buf, lr, cs, (cudaStream_t)copy_stream,
+    s = step_body(*cfg, block_layers, streamed != 0, o, *buf, lr, cs, (cudaStream_t)copy_stream,
                   g->ev[v], v == 1);
     cudaGraph_t graph = nullptr;
     const cudaError_t ec = cudaStreamEndCapture(cs, &graph);
@@ -528,15 +653,39 @@ ws_status ws_stack_graph_create(const ws_stack_cfg* cfg, int32_t block_layers, i
   return WS_OK;
 }
 
+ws_status ws_stack_graph_create(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,
+                                const ws_stack_buffers* buf, float lr, ws_stream_t compute,
+                                ws_stream_t copy_stream, ws_step_graph** out) {
+  return ws_stack_graph_create_ex(cfg, block_layers, streamed, nullptr, buf, lr, compute,
+                                  copy_stream, out);
+}
+
 ws_status ws_stack_graph_step(ws_step_graph* g, uint32_t step, const float* h0,
                               ws_stream_t compute) {
   if (!g || !h0) return WS_ERR_INVALID;
   const cudaStream_t cs = (cudaStream_t)compute;
-  ws_status s = step_prologue(g->cfg, g->block_layers, g->buf, step, h0, cs);
+  ws_status s = step_prologue(g->cfg, g->block_layers, g->opts, g->buf, step, h0, cs);
   if (s != WS_OK) return s;
   const int v = (g->warm_ok && g->window_warm) ? 1 : 0;
   if (cudaGraphLaunch(g->exec[v], cs) != cudaSuccess) return WS_ERR_CUDA;
   g->window_warm = g->warm_ok;
+  g->last = v;
+  return WS_OK;
+}
+
+ws_status ws_stack_graph_copy_times(ws_step_graph* g, float* ms, int32_t capacity, int32_t* n) {
+  if (!g || !n || (capacity > 0 && !ms)) return WS_ERR_INVALID;
+  *n = 0;
+  if (g->last < 0 || g->ev[g->last].cap_timed == 0) return WS_ERR_INVALID;
+  const StepEvents& ev = g->ev[g->last];
+  if (cudaEventSynchronize(ev.t1[ev.n_timed > 0 ? ev.n_timed - 1 : 0]) != cudaSuccess)
+    return WS_ERR_CUDA;
+  for (int i = 0; i < ev.n_timed; ++i) {
+    float t = 0.0f;
+    if (cudaEventElapsedTime(&t, ev.t0[i], ev.t1[i]) != cudaSuccess) return WS_ERR_CUDA;
+    if (i < capacity) ms[i] = t;
+  }
+  *n = ev.n_timed;
   return WS_OK;
 }
 

@@ -16,6 +16,8 @@ namespace ws {
 
 // ---- error word -------------------------------------------------------------
 // Bit flags a kernel ORs into the library's device error word.
+// (The public bits in wsnf4.h: WS_DERR_PIPELINE_MASK covers bits 0-5,
+// WS_DERR_BAD_CONFIG is bit 6, WS_DERR_TIMEOUT_PEER bit 7.)
 enum : uint32_t {
   DERR_TIMEOUT_FULL = 1u << 0,
   DERR_TIMEOUT_EMPTY = 1u << 1,
@@ -23,9 +25,12 @@ enum : uint32_t {
   DERR_TIMEOUT_BEMPTY = 1u << 3,
   DERR_TIMEOUT_ACC = 1u << 4,
   DERR_TIMEOUT_DRAIN = 1u << 5,
-  DERR_BAD_CONFIG = 1u << 6,
-  DERR_TIMEOUT_PEER = 1u << 7,
+  DERR_BAD_CONFIG = WS_DERR_BAD_CONFIG,
+  DERR_TIMEOUT_PEER = WS_DERR_TIMEOUT_PEER,
 };
+static_assert((DERR_TIMEOUT_FULL | DERR_TIMEOUT_EMPTY | DERR_TIMEOUT_BFULL | DERR_TIMEOUT_BEMPTY |
+               DERR_TIMEOUT_ACC | DERR_TIMEOUT_DRAIN) == WS_DERR_PIPELINE_MASK,
+              "device error bits");
 
 #ifdef WS_GEMM_TU
 // Device error word of the library, owned by the GEMM translation unit (the
@@ -169,6 +174,24 @@ WS_DEVINL uint32_t ld_acquire_gpu(const uint32_t* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+#ifdef WS_GEMM_TU
+// Bounded wait (acquire) for a cross-CTA word to hold `expect`: polls with a
+// short sleep; after limit_ns of wall-clock time it records `why` in the
+// device error word and returns false.
+WS_DEVINL bool wait_flag_bounded(const uint32_t* f, uint32_t expect, uint64_t limit_ns,
+                                 uint32_t why) {
+  if (ld_acquire_gpu(f) == expect) return true;
+  const uint64_t t0 = globaltimer();
+  while (ld_acquire_gpu(f) != expect) {
+    __nanosleep(128);
+    if (globaltimer() - t0 > limit_ns) {
+      atomicOr(&g_dev_error, why);
+      return false;
+    }
+  }
+  return true;
+}
+#endif
 WS_DEVINL void st_release_gpu(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

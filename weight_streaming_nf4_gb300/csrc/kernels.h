@@ -81,6 +81,8 @@ cudaError_t noalloc_scratch(float** ptr, size_t* bytes);
 // Counts every kernel launch the library makes (reported by ws_kernel_launches).
 void note_launch();
 cudaError_t read_and_clear_dev_error(uint32_t* flags);
+// One kernel that waits (bounded by limit_us) for a ring word nothing sets.
+cudaError_t run_wait_selfcheck(uint32_t limit_us, cudaStream_t st);
 // n zeroed cross-CTA words that the launch using them leaves zeroed again.
 cudaError_t ring_slots(uint32_t n, uint32_t** out);
 GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc);
@@ -143,15 +145,17 @@ cudaError_t run_mask_gen(int64_t M, int64_t K, const DropKeyHost& key, uint32_t*
 // Weight gradient of a LoRA factor on the tensor cores (nf4_gemm.cu):
 // out = s * P^T Q~ with P [M,16] fp32, Q [M,C] bf16 (masked by `mask`
 // [M, C/32] when not NULL).  out layout is [C,16] (dB) or, when
-// transpose_out, [16,C] (dA).  One fixed summation order; no workspace.
+// transpose_out, [16,C] (dA).  accumulate != 0: out = out + s * P^T Q~
+// (one fp32 add per element after the fixed-order sum).  No workspace.
 size_t wgrad_tc_bytes(int64_t M, int64_t C);
 // ng weight gradients with the same M, C and s in one launch (masks: all or none).
 cudaError_t run_wgrad_tc_group(int ng, const float* const* P, const uint16_t* const* Q,
                                const uint32_t* const* mask, int64_t M, int64_t C, float s,
-                               float* const* out, int transpose_out, cudaStream_t st);
+                               float* const* out, int transpose_out, int accumulate,
+                               cudaStream_t st);
 cudaError_t run_wgrad_tc(const float* P, const uint16_t* Q, const uint32_t* mask, int64_t M,
-                         int64_t C, float s, float* out, int transpose_out, void* ws,
-                         cudaStream_t st);
+                         int64_t C, float s, float* out, int transpose_out, int accumulate,
+                         void* ws, cudaStream_t st);
 
 // ---- one LoRA linear (linear.cu) --------------------------------------------------------
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
@@ -168,15 +172,19 @@ cudaError_t linear_fwd_group(int ng, int ng_gemm, const NF4View* W, const uint16
 // ng linears of one shape reading the same x, each with its own dY; their
 // input gradients summed into dX.
 size_t linear_bwd_group_workspace_bytes(int64_t M, int ng, int64_t N, int64_t K);
+// grad_accum != 0 adds dA, dB into the existing gradients (gradient
+// accumulation over micro-batches) instead of overwriting them.
 cudaError_t linear_bwd_group(int ng, const NF4View* W, const uint16_t* x, const float* const* A,
                              const float* const* B, int64_t M, float scale, const DropKeyHost* keys,
                              const float* const* U, const uint32_t* const* mask,
                              const uint16_t* const* dY, void* dX, int dX_f32, int dX_accum,
-                             float* const* dA, float* const* dB, void* ws, cudaStream_t st);
+                             float* const* dA, float* const* dB, int grad_accum, void* ws,
+                             cudaStream_t st);
 cudaError_t linear_bwd(const NF4View& W, const uint16_t* x, const float* A, const float* B,
                        int64_t M, float scale, const DropKeyHost& key, const float* U,
                        const uint32_t* mask, const uint16_t* dY, void* dX, int dX_f32,
-                       int dX_accum, float* dA, float* dB, void* ws, cudaStream_t st);
+                       int dX_accum, float* dA, float* dB, int grad_accum, void* ws,
+                       cudaStream_t st);
 
 }  // namespace ws
 
@@ -191,20 +199,27 @@ void stack_weight_offset(const ws_stack_cfg& c, int layer_in_block, int lin, siz
                          size_t* off_absmax);
 void stack_param_offset(const ws_stack_cfg& c, int layer, int lin, int64_t* off_A, int64_t* off_B);
 bool stack_saved_offset(const ws_stack_cfg& c, int field, int lin, size_t* off);
-// step_dev: device step word for the dropout keys (NULL: use `step`).
+// step_dev: device step word for the dropout keys (NULL: use `step`);
+// mb: micro-batch index of the dropout keys.
 cudaError_t block_forward(const ws_stack_cfg& c, int block_layers_ws, const void* block,
                           int first_layer, int n_layers, const float* params, uint32_t step,
-                          const uint32_t* step_dev, const float* h_in, float* h_out, void* saved,
-                          void* ws, cudaStream_t st);
+                          uint32_t mb, const uint32_t* step_dev, const float* h_in, float* h_out,
+                          void* saved, void* ws, cudaStream_t st);
+// grad_accum != 0: the block's adapter gradients are added to `grads`.
 cudaError_t block_backward(const ws_stack_cfg& c, int block_layers_ws, const void* block,
                            int first_layer, int n_layers, const float* params, uint32_t step,
-                           const uint32_t* step_dev, const float* h_in, const void* saved,
-                           const float* dh_out, float* dh_in, float* grads, void* ws,
-                           cudaStream_t st);
+                           uint32_t mb, const uint32_t* step_dev, const float* h_in,
+                           const void* saved, const float* dh_out, float* dh_in, float* grads,
+                           int grad_accum, void* ws, cudaStream_t st);
 // Device word reserved in the stack workspace for the step counter.
 uint32_t* stack_step_word(const ws_stack_cfg& c, int block_layers, void* ws);
+// Byte offset of a backward intermediate (WS_WK_*) in the stack workspace.
+bool stack_ws_offset(const ws_stack_cfg& c, int block_layers, int field, size_t* off);
+// Loss of one micro-batch's final activation h and its gradient dh, as its
+// share of the step loss (mean over n_micro micro-batches); accumulate != 0
+// adds the share to *loss.
 cudaError_t loss_and_grad(const ws_stack_cfg& c, int block_layers_ws, const float* h, float* dh,
-                          float* loss, void* ws, cudaStream_t st);
+                          float* loss, int n_micro, int accumulate, void* ws, cudaStream_t st);
 // Adam at step t = *step_dev + 1 (bias corrections computed on the device).
 cudaError_t adam_step(float* p, const float* g, float* m, float* v, int64_t n,
                       const uint32_t* step_dev, float lr, cudaStream_t st);

@@ -333,7 +333,8 @@ cudaError_t linear_fwd_group(int ng, int ng_gemm, const NF4View* W, const uint16
 cudaError_t linear_bwd(const NF4View& W, const uint16_t* x, const float* A, const float* B,
                        int64_t M, float scale, const DropKeyHost& key, const float* U,
                        const uint32_t* mask, const uint16_t* dY, void* dX, int dX_f32,
-                       int dX_accum, float* dA, float* dB, void* ws, cudaStream_t st) {
+                       int dX_accum, float* dA, float* dB, int grad_accum, void* ws,
+                       cudaStream_t st) {
   const LinWs L = lin_ws_layout(M, W.N, W.K);
   uint8_t* w = static_cast<uint8_t*>(ws);
   uint16_t* Gext = reinterpret_cast<uint16_t*>(w + L.ext);
@@ -353,13 +354,14 @@ cudaError_t linear_bwd(const NF4View& W, const uint16_t* x, const float* A, cons
   if (use_side) {
     e = cudaEventRecord(side.fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side.s, side.fork, 0);
-    if (e == cudaSuccess) e = run_wgrad_tc(U, dY, nullptr, M, W.N, scale, dB, 0, wg, side.s);
+    if (e == cudaSuccess) e = run_wgrad_tc(U, dY, nullptr, M, W.N, scale, dB, 0, grad_accum, wg, side.s);
     if (e == cudaSuccess) e = cudaEventRecord(side.join, side.s);
     if (e != cudaSuccess) return e;
   }
   e = run_lora_G(dY, B, M, W.N, G, Gext, reinterpret_cast<float*>(w + L.skinny), st);
-  if (e == cudaSuccess && dB && !use_side) e = run_wgrad_tc(U, dY, nullptr, M, W.N, scale, dB, 0, wg, st);
-  if (e == cudaSuccess && dA) e = run_wgrad_tc(G, x, mask, M, W.K, scale, dA, 1, wg, st);
+  if (e == cudaSuccess && dB && !use_side)
+    e = run_wgrad_tc(U, dY, nullptr, M, W.N, scale, dB, 0, grad_accum, wg, st);
+  if (e == cudaSuccess && dA) e = run_wgrad_tc(G, x, mask, M, W.K, scale, dA, 1, grad_accum, wg, st);
   // join even after an error, so a capture is never left with an unjoined stream
   if (use_side) {
     const cudaError_t ej = cudaStreamWaitEvent(st, side.join, 0);
@@ -409,7 +411,8 @@ cudaError_t linear_bwd_group(int ng, const NF4View* W, const uint16_t* x, const 
                              const float* const* B, int64_t M, float scale, const DropKeyHost* keys,
                              const float* const* U, const uint32_t* const* mask,
                              const uint16_t* const* dY, void* dX, int dX_f32, int dX_accum,
-                             float* const* dA, float* const* dB, void* ws, cudaStream_t st) {
+                             float* const* dA, float* const* dB, int grad_accum, void* ws,
+                             cudaStream_t st) {
   if (ng < 1 || ng > kMaxGroups) return cudaErrorInvalidValue;
   const int64_t N = W[0].N, K = W[0].K;
   bool any_dA = false, any_dB = false;
@@ -445,13 +448,13 @@ cudaError_t linear_bwd_group(int ng, const NF4View* W, const uint16_t* x, const 
   if (use_side) {
     e = cudaEventRecord(side.fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side.s, side.fork, 0);
-    if (e == cudaSuccess) e = run_wgrad_tc_group(ng, U, dY, nullptr, M, N, scale, dB, 0, side.s);
+    if (e == cudaSuccess) e = run_wgrad_tc_group(ng, U, dY, nullptr, M, N, scale, dB, 0, grad_accum, side.s);
     if (e == cudaSuccess) e = cudaEventRecord(side.join, side.s);
     if (e != cudaSuccess) return e;
   }
   e = run_skinny_G_group(ng, dY, B, M, N, part, G, Gext, st);
   if (e == cudaSuccess && any_dB && !use_side)
-    e = run_wgrad_tc_group(ng, U, dY, nullptr, M, N, scale, dB, 0, st);
+    e = run_wgrad_tc_group(ng, U, dY, nullptr, M, N, scale, dB, 0, grad_accum, st);
   if (e == cudaSuccess && any_dA) {
     const float* Gc[kMaxGroups];
     const uint16_t* xs[kMaxGroups];
@@ -459,7 +462,7 @@ cudaError_t linear_bwd_group(int ng, const NF4View* W, const uint16_t* x, const 
       Gc[g] = G[g];
       xs[g] = x;
     }
-    e = run_wgrad_tc_group(ng, Gc, xs, mk, M, K, scale, dA, 1, st);
+    e = run_wgrad_tc_group(ng, Gc, xs, mk, M, K, scale, dA, 1, grad_accum, st);
   }
   if (use_side) {
     const cudaError_t ej = cudaStreamWaitEvent(st, side.join, 0);

@@ -948,20 +948,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // most one); the barrier passes what it acquired to the others
           if (ew == 0 && lane == 0) {
             bool got = ok;
-            for (int64_t u = unit + 1; u <= u_last && got; ++u) {
-              const uint32_t* f = args.flags + cta_of(u);
-              if (ld_acquire_gpu(f) != 1u) {
-                const uint64_t t0 = globaltimer();
-                while (ld_acquire_gpu(f) != 1u) {
-                  __nanosleep(128);
-                  if (globaltimer() - t0 > kWaitLimitNs) {
-                    atomicOr(&g_dev_error, DERR_TIMEOUT_PEER);
-                    got = false;
-                    break;
-                  }
-                }
-              }
-            }
+            for (int64_t u = unit + 1; u <= u_last && got; ++u)
+              got = wait_flag_bounded(args.flags + cta_of(u), 1u, kWaitLimitNs, DERR_TIMEOUT_PEER);
             *fin_got = got ? 1u : 0u;
             // consumed: the flags go back to zero for the next launch using them
             if (got)
@@ -1124,6 +1112,7 @@ struct WgArgs {
   int64_t M, C;
   float s;
   int transpose_out;
+  int accumulate;  // out = out + s P^T Q~ (gradient accumulation) instead of overwriting
 };
 constexpr int kWgThreads = 192;
 constexpr int kWgStages = 4;
@@ -1147,6 +1136,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   const int64_t M = wa.M, C = wa.C;
   const float s = wa.s;
   const int transpose_out = wa.transpose_out;
+  const bool accumulate = wa.accumulate != 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1342,19 +1332,24 @@ __global__ void __launch_bounds__(kWgThreads, 1)
               float* dst = out + (int64_t)lane * C + cb;
               if (ncol == 32 && ((C & 3) == 0)) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                  reinterpret_cast<float4*>(dst)[e] =
-                      make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                for (int e = 0; e < 8; ++e) {
+                  float4 o = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                  if (accumulate) {
+                    const float4 q = reinterpret_cast<const float4*>(dst)[e];
+                    o = make_float4(q.x + o.x, q.y + o.y, q.z + o.z, q.w + o.w);
+                  }
+                  reinterpret_cast<float4*>(dst)[e] = o;
+                }
               } else {
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
-                  if (e < ncol) dst[e] = v[e];
+                  if (e < ncol) dst[e] = accumulate ? dst[e] + v[e] : v[e];
               }
             } else {
               float* dst = out + cb * 16 + lane;
 #pragma unroll
               for (int e = 0; e < 32; ++e)
-                if (e < ncol) dst[(int64_t)e * 16] = v[e];
+                if (e < ncol) dst[(int64_t)e * 16] = accumulate ? dst[(int64_t)e * 16] + v[e] : v[e];
             }
           }
         }
@@ -2080,6 +2075,27 @@ cudaError_t run_nf4_gemm_group(const GemmPlan& p, int ng, const NF4View* W, cons
   return dispatch_gemm(p, a, tA, tL, st);
 }
 
+// ------------------------------------------------------------------------ bounded-wait self-check
+// One thread waits, through the finisher's bounded wait but with the given
+// limit, for a ring word that nothing sets; it gives up, records the peer
+// timeout bit and returns.
+__global__ void k_wait_selfcheck(const uint32_t* word, uint64_t limit_ns) {
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0 && blockIdx.x == 0)
+    (void)wait_flag_bounded(word, 1u, limit_ns, DERR_TIMEOUT_PEER);
+}
+
+cudaError_t run_wait_selfcheck(uint32_t limit_us, cudaStream_t st) {
+  uint32_t* word = nullptr;
+  cudaError_t e = ring_slots(1, &word);
+  if (e != cudaSuccess) return e;
+  note_launch();
+  (void)launch_pdl(k_wait_selfcheck, dim3(1), dim3(32), 0, st, (const uint32_t*)word,
+                   (uint64_t)limit_us * 1000ull);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------------ skinny products (host)
 int skinny_tc_chunks(int64_t M, int64_t K) {
   const int64_t atoms = (M + 127) / 128;
@@ -2236,7 +2252,8 @@ size_t wgrad_tc_bytes(int64_t M, int64_t C) {
 
 cudaError_t run_wgrad_tc_group(int ng, const float* const* P, const uint16_t* const* Q,
                                const uint32_t* const* mask, int64_t M, int64_t C, float s,
-                               float* const* out, int transpose_out, cudaStream_t st) {
+                               float* const* out, int transpose_out, int accumulate,
+                               cudaStream_t st) {
   if (!encode_fn()) return cudaErrorNotSupported;
   if (ng < 1 || ng > kMaxGroups) return cudaErrorInvalidValue;
   WgArgs wa;
@@ -2261,6 +2278,7 @@ cudaError_t run_wgrad_tc_group(int ng, const float* const* P, const uint16_t* co
   wa.C = C;
   wa.s = s;
   wa.transpose_out = transpose_out;
+  wa.accumulate = accumulate;
   static cudaError_t attr0 = cudaFuncSetAttribute(
       k_wgrad_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWgSmem);
   static cudaError_t attr1 = cudaFuncSetAttribute(
@@ -2277,10 +2295,10 @@ cudaError_t run_wgrad_tc_group(int ng, const float* const* P, const uint16_t* co
 }
 
 cudaError_t run_wgrad_tc(const float* P, const uint16_t* Q, const uint32_t* mask, int64_t M,
-                         int64_t C, float s, float* out, int transpose_out, void* ws,
-                         cudaStream_t st) {
+                         int64_t C, float s, float* out, int transpose_out, int accumulate,
+                         void* ws, cudaStream_t st) {
   (void)ws;
-  return run_wgrad_tc_group(1, &P, &Q, &mask, M, C, s, &out, transpose_out, st);
+  return run_wgrad_tc_group(1, &P, &Q, &mask, M, C, s, &out, transpose_out, accumulate, st);
 }
 
 }  // namespace ws

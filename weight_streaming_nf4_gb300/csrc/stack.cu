@@ -63,11 +63,11 @@ __global__ void __launch_bounds__(256) k_rmsnorm_fwd(const float* __restrict__ h
   }
 }
 
-// dx += rstd*dy - rstd^3 * x * (dy . x) / H
+// dx_out = dx_in + (rstd*dy - rstd^3 * x * (dy . x) / H); dx_out may be dx_in
 __global__ void __launch_bounds__(256) k_rmsnorm_bwd(const float* __restrict__ x,
                                                      const float* __restrict__ rstd,
                                                      const float* __restrict__ dy, int64_t H,
-                                                     float* __restrict__ dx) {
+                                                     const float* dx_in, float* dx_out) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float red[9];
@@ -86,10 +86,11 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bwd(const float* __restrict__ x
   dot = block_sum_256(dot, red);
   const float rs = rstd[m];
   const float coef = rs * rs * rs * dot / (float)H;
-  float4* o = reinterpret_cast<float4*>(dx + m * H);
+  const float4* in = reinterpret_cast<const float4*>(dx_in + m * H);
+  float4* o = reinterpret_cast<float4*>(dx_out + m * H);
   for (int i = threadIdx.x; i < H4; i += 256) {
     const float4 a = dr[i], b = xr[i];
-    float4 v = o[i];
+    float4 v = in[i];
     v.x += rs * a.x - coef * b.x;
     v.y += rs * a.y - coef * b.y;
     v.z += rs * a.z - coef * b.z;
@@ -231,14 +232,16 @@ __global__ void __launch_bounds__(256) k_loss_partial(const float* __restrict__ 
   s = block_sum_256(s, red);
   if (threadIdx.x == 0) partial[blockIdx.x] = s;
 }
-__global__ void k_loss_final(const float* __restrict__ partial, float inv_n,
+// accumulate != 0: add this micro-batch's share to the step loss (micro-batches in order)
+__global__ void k_loss_final(const float* __restrict__ partial, float inv_n, int accumulate,
                              float* __restrict__ loss) {
   pdl_wait();
   pdl_launch_dependents();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   float s = 0.0f;
   for (int i = 0; i < kLossBlocks; ++i) s += partial[i];
-  *loss = 0.5f * s * inv_n;
+  const float l = 0.5f * s * inv_n;
+  *loss = accumulate ? *loss + l : l;
 }
 
 // PyTorch-default Adam (no weight decay, bias-corrected); 4 parameters per
@@ -371,7 +374,7 @@ ParamLayout param_layout(const ws_stack_cfg& c) {
 }
 
 struct WsLayout {
-  size_t lin, blk, qout, kout, yout, y1, dact, dg, du, db, dvr, dv, lossp, stepw, total;
+  size_t lin, blk, qout, kout, yout, y1, dact, dg, du, db, dh1, dvr, dv, da, lossp, stepw, total;
 };
 WsLayout ws_layout(const ws_stack_cfg& c, int block_layers) {
   const Shapes s = shapes_of(c);
@@ -407,8 +410,10 @@ WsLayout ws_layout(const ws_stack_cfg& c, int block_layers) {
   L.dg = take(M * I * 2);
   L.du = take(M * I * 2);
   L.db = take(M * H * 4);
+  L.dh1 = take(M * H * 4);
   L.dvr = take(M * H * 4);
   L.dv = take(M * KV * 2);
+  L.da = take(M * H * 4);
   L.lossp = take(kLossBlocks * 4);
   L.stepw = take(16);
   L.total = o;
@@ -449,13 +454,13 @@ NF4View wview(const Ctx& x, const void* block, int layer_in_block, int lin) {
   return v;
 }
 
-DropKeyHost key_of(const Ctx& x, uint32_t step, int layer, int lin) {
+DropKeyHost key_of(const Ctx& x, uint32_t step, int layer, int lin, uint32_t mb) {
   ws_dropout_key k{};
   k.seed = x.c.seed;
   k.step = step;
   k.layer = (uint32_t)layer;
   k.linear = (uint32_t)lin;
-  k.microbatch = 0;
+  k.microbatch = mb;
   k.p = x.c.p;
   DropKeyHost h = make_drop_key(k);
   h.step_dev = x.step_dev;
@@ -466,7 +471,8 @@ DropKeyHost key_of(const Ctx& x, uint32_t step, int layer, int lin) {
 // q and k projections (the first forward does; a recompute skips them since
 // nothing downstream reads them).
 cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const float* params,
-                      uint32_t step, const float* h_in, float* h_out, uint8_t* S, bool with_qk) {
+                      uint32_t step, uint32_t mb, const float* h_in, float* h_out, uint8_t* S,
+                      bool with_qk) {
   const int64_t M = x.c.M, H = x.c.H, KV = x.c.KV, I = x.c.I;
   const SavedLayout& L = x.SL;
   cudaStream_t st = x.st;
@@ -475,7 +481,7 @@ cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const
   const float* P = params + (int64_t)layer * x.PL.layer_floats;
   auto lin = [&](int li, const uint16_t* in, uint16_t* out) {
     return linear_fwd(wview(x, block, lib, li), in, P + x.PL.A[li], P + x.PL.B[li], M, x.scale,
-                      key_of(x, step, layer, li), out, at<float>(S, L.U[li]),
+                      key_of(x, step, layer, li, mb), out, at<float>(S, L.U[li]),
                       at<uint32_t>(S, L.mask[li]), lws, st);
   };
   // linears reading the same input: one LoRA-down launch and one GEMM
@@ -491,7 +497,7 @@ cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const
       W[g] = wview(x, block, lib, li[g]);
       A[g] = P + x.PL.A[li[g]];
       B[g] = P + x.PL.B[li[g]];
-      keys[g] = key_of(x, step, layer, li[g]);
+      keys[g] = key_of(x, step, layer, li[g], mb);
       U[g] = at<float>(S, L.U[li[g]]);
       mk[g] = at<uint32_t>(S, L.mask[li[g]]);
     }
@@ -541,9 +547,13 @@ cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const
 }
 
 // Backward of one layer from its saved slot S; dh holds the gradient at
-// the layer output on entry and at the layer input on exit.
+// the layer output on entry and at the layer input on exit.  gacc != 0 adds
+// the adapter gradients into `grads` (gradient accumulation) instead of
+// overwriting them.  Every intermediate gradient has a workspace buffer of
+// its own, so after the call they all hold this layer's values.
 cudaError_t layer_bwd(const Ctx& x, const void* block, int lib, int layer, const float* params,
-                      uint32_t step, const uint8_t* S, float* dh, float* grads) {
+                      uint32_t step, uint32_t mb, const uint8_t* S, float* dh, float* grads,
+                      int gacc) {
   const int64_t M = x.c.M, H = x.c.H, KV = x.c.KV, I = x.c.I;
   const SavedLayout& L = x.SL;
   cudaStream_t st = x.st;
@@ -553,17 +563,19 @@ cudaError_t layer_bwd(const Ctx& x, const void* block, int lib, int layer, const
   float* Gd = grads + (int64_t)layer * x.PL.layer_floats;
   auto lin = [&](int li, const uint16_t* in, const uint16_t* dY, float* dX, int accum) {
     return linear_bwd(wview(x, block, lib, li), in, P + x.PL.A[li], P + x.PL.B[li], M, x.scale,
-                      key_of(x, step, layer, li), at<const float>(S, L.U[li]),
+                      key_of(x, step, layer, li, mb), at<const float>(S, L.U[li]),
                       at<const uint32_t>(S, L.mask[li]), dY, dX, 1, accum, Gd + x.PL.A[li],
-                      Gd + x.PL.B[li], lws, st);
+                      Gd + x.PL.B[li], gacc, lws, st);
   };
   uint16_t* y1 = at<uint16_t>(ws, x.WSL.y1);
   float* dact = at<float>(ws, x.WSL.dact);
   uint16_t* dg = at<uint16_t>(ws, x.WSL.dg);
   uint16_t* du = at<uint16_t>(ws, x.WSL.du);
   float* db = at<float>(ws, x.WSL.db);
+  float* dh1 = at<float>(ws, x.WSL.dh1);
   float* dvr = at<float>(ws, x.WSL.dvr);
   uint16_t* dv = at<uint16_t>(ws, x.WSL.dv);
+  float* da = at<float>(ws, x.WSL.da);
 
   note_launch();
   (void)launch_pdl(k_cast_bf16, dim3(nblk(M * H / 8)), dim3(256), 0, st, dh, M * H, y1);
@@ -589,35 +601,40 @@ cudaError_t layer_bwd(const Ctx& x, const void* block, int lib, int layer, const
       W[g] = wview(x, block, lib, li[g]);
       A[g] = P + x.PL.A[li[g]];
       B[g] = P + x.PL.B[li[g]];
-      keys[g] = key_of(x, step, layer, li[g]);
+      keys[g] = key_of(x, step, layer, li[g], mb);
       U[g] = at<const float>(S, L.U[li[g]]);
       mk[g] = at<const uint32_t>(S, L.mask[li[g]]);
       dAs[g] = Gd + x.PL.A[li[g]];
       dBs[g] = Gd + x.PL.B[li[g]];
     }
     WS_TRY(linear_bwd_group(2, W, at<const uint16_t>(S, L.b), A, B, M, x.scale, keys, U, mk, dYs,
-                            db, 1, 0, dAs, dBs, lws, st));
+                            db, 1, 0, dAs, dBs, gacc, lws, st));
   }
+  // dh1 = dh + RMSNorm2 backward (the residual passes dh through)
   note_launch();
   (void)launch_pdl(k_rmsnorm_bwd, dim3((unsigned)M), dim3(256), 0, st, at<const float>(S, L.h1), at<const float>(S, L.rstd2),
-                                             db, H, dh);
+                                             (const float*)db, H, (const float*)dh, dh1);
   WS_TRY(cudaGetLastError());
   note_launch();
-  (void)launch_pdl(k_cast_bf16, dim3(nblk(M * H / 8)), dim3(256), 0, st, dh, M * H, y1);
+  (void)launch_pdl(k_cast_bf16, dim3(nblk(M * H / 8)), dim3(256), 0, st, (const float*)dh1, M * H, y1);
   WS_TRY(cudaGetLastError());
   WS_TRY(lin(WS_LIN_O, at<const uint16_t>(S, L.vr), y1, dvr, 0));
   note_launch();
   (void)launch_pdl(k_repeat_bwd, dim3(nblk(M * KV / 4)), dim3(256), 0, st, dvr, (int)M, (int)H, (int)KV, (int)x.c.head_dim, dv);
   WS_TRY(cudaGetLastError());
-  WS_TRY(lin(WS_LIN_V, at<const uint16_t>(S, L.a), dv, db, 0));
+  WS_TRY(lin(WS_LIN_V, at<const uint16_t>(S, L.a), dv, da, 0));
+  // dh = dh1 + RMSNorm1 backward
   note_launch();
   (void)launch_pdl(k_rmsnorm_bwd, dim3((unsigned)M), dim3(256), 0, st, at<const float>(S, L.h), at<const float>(S, L.rstd1),
-                                             db, H, dh);
+                                             (const float*)da, H, (const float*)dh1, dh);
   WS_TRY(cudaGetLastError());
   // q and k feed only the replaced attention core: exactly zero gradient
-  for (int li : {WS_LIN_Q, WS_LIN_K}) {
-    WS_TRY(cudaMemsetAsync(Gd + x.PL.A[li], 0, sizeof(float) * 16 * (size_t)x.s.K[li], st));
-    WS_TRY(cudaMemsetAsync(Gd + x.PL.B[li], 0, sizeof(float) * 16 * (size_t)x.s.N[li], st));
+  // (already zero when accumulating)
+  if (!gacc) {
+    for (int li : {WS_LIN_Q, WS_LIN_K}) {
+      WS_TRY(cudaMemsetAsync(Gd + x.PL.A[li], 0, sizeof(float) * 16 * (size_t)x.s.K[li], st));
+      WS_TRY(cudaMemsetAsync(Gd + x.PL.B[li], 0, sizeof(float) * 16 * (size_t)x.s.N[li], st));
+    }
   }
   return cudaSuccess;
 }
@@ -660,6 +677,13 @@ size_t stack_ws_bytes(const ws_stack_cfg& c, int bl) { return ws_layout(c, bl).t
 uint32_t* stack_step_word(const ws_stack_cfg& c, int block_layers, void* ws) {
   return at<uint32_t>(ws, ws_layout(c, block_layers).stepw);
 }
+bool stack_ws_offset(const ws_stack_cfg& c, int block_layers, int field, size_t* off) {
+  const WsLayout L = ws_layout(c, block_layers);
+  const size_t f[] = {L.y1, L.dact, L.dg, L.du, L.db, L.dh1, L.dvr, L.dv, L.da, L.yout};
+  if (field < 0 || field >= (int)(sizeof(f) / sizeof(f[0]))) return false;
+  *off = f[field];
+  return true;
+}
 void stack_weight_offset(const ws_stack_cfg& c, int lib, int lin, size_t* oc, size_t* oa) {
   const WeightLayout L = weight_layout(c);
   *oc = (size_t)lib * L.layer_bytes + L.codes[lin];
@@ -686,8 +710,8 @@ void stack_param_offset(const ws_stack_cfg& c, int layer, int lin, int64_t* oA, 
 
 cudaError_t block_forward(const ws_stack_cfg& c, int block_layers_ws, const void* block,
                           int first_layer, int n_layers, const float* params, uint32_t step,
-                          const uint32_t* step_dev, const float* h_in, float* h_out, void* saved,
-                          void* ws, cudaStream_t st) {
+                          uint32_t mb, const uint32_t* step_dev, const float* h_in, float* h_out,
+                          void* saved, void* ws, cudaStream_t st) {
   const Ctx x = make_ctx(c, block_layers_ws, ws, st, step_dev);
   uint8_t* blk_area = static_cast<uint8_t*>(ws) + x.WSL.blk;
   // Layer i works in slot S_i: the caller's saved area (kept for the
@@ -702,16 +726,16 @@ cudaError_t block_forward(const ws_stack_cfg& c, int block_layers_ws, const void
     uint8_t* S = slot(i);
     const float* src = i == 0 ? h_in : at<float>(S, x.SL.h);
     float* dst = i == n_layers - 1 ? h_out : at<float>(slot(i + 1), x.SL.h);
-    WS_TRY(layer_fwd(x, block, i, first_layer + i, params, step, src, dst, S, true));
+    WS_TRY(layer_fwd(x, block, i, first_layer + i, params, step, mb, src, dst, S, true));
   }
   return cudaSuccess;
 }
 
 cudaError_t block_backward(const ws_stack_cfg& c, int block_layers_ws, const void* block,
                            int first_layer, int n_layers, const float* params, uint32_t step,
-                           const uint32_t* step_dev, const float* h_in, const void* saved,
-                           const float* dh_out, float* dh_in, float* grads, void* ws,
-                           cudaStream_t st) {
+                           uint32_t mb, const uint32_t* step_dev, const float* h_in,
+                           const void* saved, const float* dh_out, float* dh_in, float* grads,
+                           int grad_accum, void* ws, cudaStream_t st) {
   const Ctx x = make_ctx(c, block_layers_ws, ws, st, step_dev);
   const int64_t MH = c.M * c.H;
   const uint8_t* area = static_cast<const uint8_t*>(saved);
@@ -725,29 +749,31 @@ cudaError_t block_backward(const ws_stack_cfg& c, int block_layers_ws, const voi
       float* dst;
       if (i == n_layers - 1) dst = at<float>(static_cast<uint8_t*>(ws) + x.WSL.dvr, 0);  // unused output
       else dst = at<float>(blk + (size_t)(i + 1) * x.SL.total, x.SL.h);
-      WS_TRY(layer_fwd(x, block, i, first_layer + i, params, step, src, dst, S, false));
+      WS_TRY(layer_fwd(x, block, i, first_layer + i, params, step, mb, src, dst, S, false));
     }
     area = blk;
   }
   if (dh_in != dh_out)
     WS_TRY(cudaMemcpyAsync(dh_in, dh_out, (size_t)MH * 4, cudaMemcpyDeviceToDevice, st));
   for (int i = n_layers - 1; i >= 0; --i)
-    WS_TRY(layer_bwd(x, block, i, first_layer + i, params, step, area + (size_t)i * x.SL.total, dh_in,
-                     grads));
+    WS_TRY(layer_bwd(x, block, i, first_layer + i, params, step, mb, area + (size_t)i * x.SL.total,
+                     dh_in, grads, grad_accum));
   return cudaSuccess;
 }
 
 cudaError_t loss_and_grad(const ws_stack_cfg& c, int block_layers_ws, const float* h, float* dh,
-                          float* loss, void* ws, cudaStream_t st) {
+                          float* loss, int n_micro, int accumulate, void* ws, cudaStream_t st) {
   const WsLayout L = ws_layout(c, block_layers_ws);
   const int64_t n = c.M * c.H;
   float* part = at<float>(ws, L.lossp);
-  const float inv_n = (float)(1.0 / (double)n);
+  // the step loss is the mean over micro-batches: each one contributes
+  // 0.5 sum(h^2) / (n * n_micro), and its gradient is h / (n * n_micro)
+  const float inv_n = (float)(1.0 / ((double)n * (double)n_micro));
   note_launch();
   (void)launch_pdl(k_loss_partial, dim3(kLossBlocks), dim3(256), 0, st, h, n, part, dh, inv_n);
   WS_TRY(cudaGetLastError());
   note_launch();
-  (void)launch_pdl(k_loss_final, dim3(1), dim3(32), 0, st, part, inv_n, loss);
+  (void)launch_pdl(k_loss_final, dim3(1), dim3(32), 0, st, (const float*)part, inv_n, accumulate, loss);
   return cudaGetLastError();
 }
 

@@ -29,6 +29,8 @@ P = C.c_void_p
 i32, i64, u32, u64 = C.c_int32, C.c_int64, C.c_uint32, C.c_uint64
 
 WS_DTYPE_BF16, WS_DTYPE_F32 = 0, 1
+WS_ACC_DX, WS_ACC_GRADS = 1, 2
+GA_MICROBATCH_MAJOR, GA_BLOCK_MAJOR = 0, 1
 LIN = dict(q=0, k=1, v=2, o=3, gate=4, up=5, down=6)
 LIN_NAMES = ("q", "k", "v", "o", "gate", "up", "down")
 
@@ -59,6 +61,10 @@ class StackCfgC(C.Structure):
                 ("eps", C.c_float), ("seed", u64)]
 
 
+class StepOptsC(C.Structure):
+    _fields_ = [("n_micro", i32), ("order", i32), ("time_copies", i32)]
+
+
 class StackBuffersC(C.Structure):
     _fields_ = [("host_weights", P), ("dev_weights", P), ("window", P), ("params", P),
                 ("grads", P), ("adam_m", P), ("adam_v", P), ("boundary", P), ("saved", P),
@@ -75,6 +81,7 @@ def _sig(name, args):
 _lib.ws_status_string.restype = C.c_char_p
 _lib.ws_status_string.argtypes = [i32]
 _sig("ws_device_error", [C.POINTER(u32)])
+_sig("ws_selfcheck_bounded_wait", [u32, P])
 _lib.ws_kernel_launches.restype = u64
 _lib.ws_kernel_launches.argtypes = []
 _sig("ws_quantize_nf4", [P, i64, i64, P, P, P])
@@ -92,24 +99,32 @@ _sig("ws_stack_weight_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(C.c_si
                                 C.POINTER(C.c_size_t)])
 _sig("ws_stack_param_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(i64), C.POINTER(i64)])
 _sig("ws_stack_saved_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(C.c_size_t)])
-_sig("ws_block_forward", [C.POINTER(StackCfgC), P, i32, i32, P, u32, P, P, P, P, C.c_size_t, P])
-_sig("ws_block_backward_recompute", [C.POINTER(StackCfgC), P, i32, i32, P, u32, P, P, P, P, P,
-                                     P, C.c_size_t, P])
+_sig("ws_stack_workspace_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(C.c_size_t)])
+_sig("ws_block_forward", [C.POINTER(StackCfgC), P, i32, i32, P, u32, u32, P, P, P, P, C.c_size_t,
+                          P])
+_sig("ws_block_backward_recompute", [C.POINTER(StackCfgC), P, i32, i32, P, u32, u32, P, P, P, P,
+                                     P, i32, P, C.c_size_t, P])
 _sig("ws_stream_block_h2d", [P, P, C.c_size_t, P, P, P])
 _sig("ws_stack_train_step", [C.POINTER(StackCfgC), i32, i32, C.POINTER(StackBuffersC), u32, P,
                              C.c_float, P, P])
 _sig("ws_stack_graph_create", [C.POINTER(StackCfgC), i32, i32, C.POINTER(StackBuffersC), C.c_float,
                                P, P, C.POINTER(P)])
+_sig("ws_stack_train_step_ex", [C.POINTER(StackCfgC), i32, i32, C.POINTER(StepOptsC),
+                                C.POINTER(StackBuffersC), u32, P, C.c_float, P, P])
+_sig("ws_stack_graph_create_ex", [C.POINTER(StackCfgC), i32, i32, C.POINTER(StepOptsC),
+                                  C.POINTER(StackBuffersC), C.c_float, P, P, C.POINTER(P)])
+_sig("ws_stack_graph_copy_times", [P, C.POINTER(C.c_float), i32, C.POINTER(i32)])
 _sig("ws_stack_graph_step", [P, u32, P, P])
 _sig("ws_stack_graph_destroy", [P])
 
-EXPORTED = ("ws_status_string", "ws_device_error", "ws_kernel_launches", "ws_quantize_nf4", "ws_lora_workspace_size",
+EXPORTED = ("ws_status_string", "ws_device_error", "ws_selfcheck_bounded_wait", "ws_kernel_launches", "ws_quantize_nf4", "ws_lora_workspace_size",
             "ws_lora_linear_fwd", "ws_lora_linear_bwd", "ws_nf4_matmul_workspace_size",
             "ws_nf4_matmul", "ws_nf4_matmul_noalloc", "ws_stack_sizes",
             "ws_stack_weight_offset", "ws_stack_param_offset", "ws_stack_saved_offset",
-            "ws_block_forward", "ws_block_backward_recompute", "ws_stream_block_h2d",
-            "ws_stack_train_step", "ws_stack_graph_create", "ws_stack_graph_step",
-            "ws_stack_graph_destroy")
+            "ws_stack_workspace_offset", "ws_block_forward", "ws_block_backward_recompute",
+            "ws_stream_block_h2d", "ws_stack_train_step", "ws_stack_train_step_ex",
+            "ws_stack_graph_create", "ws_stack_graph_create_ex", "ws_stack_graph_copy_times",
+            "ws_stack_graph_step", "ws_stack_graph_destroy")
 
 
 def _check(fn, st):
@@ -142,6 +157,14 @@ def device_error() -> int:
     if st not in (0, -5):
         raise WsError("ws_device_error", st)
     return int(f.value)
+
+
+WS_DERR_PIPELINE_MASK, WS_DERR_BAD_CONFIG, WS_DERR_TIMEOUT_PEER = 0x3F, 0x40, 0x80
+
+
+def selfcheck_bounded_wait(limit_us: int, stream=None):
+    """Enqueue the bounded-wait self-check (a wait that gives up after limit_us)."""
+    _check("ws_selfcheck_bounded_wait", _lib.ws_selfcheck_bounded_wait(limit_us, _stream(stream)))
 
 
 # ------------------------------------------------------------------------------ a0
@@ -204,7 +227,9 @@ def lora_linear_fwd(W: NF4Weight, x, A, B, key: DropoutKey, alpha=32.0, y=None, 
 
 def lora_linear_bwd(W: NF4Weight, x, A, B, key: DropoutKey, U, mask, dY, alpha=32.0,
                     dX=None, dX_f32=False, accumulate=False, dA=None, dB=None, workspace=None,
-                    stream=None):
+                    stream=None, grad_accumulate=False):
+    """accumulate: add the input gradient into the given fp32 dX;
+    grad_accumulate: add dA, dB into the given gradients."""
     M, K = x.shape
     sh = LoraShape(M, W.N, W.K, A.shape[0], alpha)
     dev = x.device
@@ -220,7 +245,9 @@ def lora_linear_bwd(W: NF4Weight, x, A, B, key: DropoutKey, U, mask, dY, alpha=3
     dt = WS_DTYPE_F32 if dX.dtype == torch.float32 else WS_DTYPE_BF16
     _check("ws_lora_linear_bwd",
            _lib.ws_lora_linear_bwd(C.byref(w), _ptr(x), _ptr(A), _ptr(B), sh, key, _ptr(U),
-                                   _ptr(mask), _ptr(dY), _ptr(dX), dt, 1 if accumulate else 0,
+                                   _ptr(mask), _ptr(dY), _ptr(dX), dt,
+                                   (WS_ACC_DX if accumulate else 0)
+                                   | (WS_ACC_GRADS if grad_accumulate else 0),
                                    _ptr(dA), _ptr(dB), _ptr(workspace), workspace.numel(),
                                    _stream(stream)))
     return dX, dA, dB
@@ -334,23 +361,37 @@ def stack_saved_offset(cfg: StackCfg, field: str, lin: int = 0) -> int:
     return int(off.value)
 
 
+WORKSPACE_FIELDS = dict(y1=0, dact=1, dg=2, du=3, db=4, dh1=5, dvr=6, dv=7, da=8, yout=9)
+
+
+def stack_workspace_offset(cfg: StackCfg, block_layers: int, field: str) -> int:
+    off = C.c_size_t(0)
+    c = cfg.c()
+    _check("ws_stack_workspace_offset",
+           _lib.ws_stack_workspace_offset(C.byref(c), block_layers, WORKSPACE_FIELDS[field],
+                                          C.byref(off)))
+    return int(off.value)
+
+
 def block_forward(cfg: StackCfg, block_weights, first_layer, n_layers, params, step, h_in, h_out,
-                  saved, workspace, stream=None):
+                  saved, workspace, stream=None, microbatch=0):
     c = cfg.c()
     _check("ws_block_forward",
            _lib.ws_block_forward(C.byref(c), _ptr(block_weights), first_layer, n_layers,
-                                 _ptr(params), step, _ptr(h_in), _ptr(h_out), _ptr(saved),
-                                 _ptr(workspace), workspace.numel(), _stream(stream)))
+                                 _ptr(params), step, microbatch, _ptr(h_in), _ptr(h_out),
+                                 _ptr(saved), _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def block_backward_recompute(cfg: StackCfg, block_weights, first_layer, n_layers, params, step,
-                             h_in, saved, dh_out, dh_in, grads, workspace, stream=None):
+                             h_in, saved, dh_out, dh_in, grads, workspace, stream=None,
+                             microbatch=0, grad_accumulate=False):
     c = cfg.c()
     _check("ws_block_backward_recompute",
            _lib.ws_block_backward_recompute(C.byref(c), _ptr(block_weights), first_layer,
-                                            n_layers, _ptr(params), step, _ptr(h_in),
+                                            n_layers, _ptr(params), step, microbatch, _ptr(h_in),
                                             _ptr(saved), _ptr(dh_out), _ptr(dh_in), _ptr(grads),
-                                            _ptr(workspace), workspace.numel(), _stream(stream)))
+                                            1 if grad_accumulate else 0, _ptr(workspace),
+                                            workspace.numel(), _stream(stream)))
 
 
 def stream_block_h2d(pinned_src: torch.Tensor, dev_dst: torch.Tensor, nbytes: int = None,
@@ -364,33 +405,50 @@ def stream_block_h2d(pinned_src: torch.Tensor, dev_dst: torch.Tensor, nbytes: in
                                     C.c_void_p(done_event) if done_event else None))
 
 
+def step_opts(n_micro=1, order=GA_MICROBATCH_MAJOR, time_copies=False):
+    return StepOptsC(n_micro, order, 1 if time_copies else 0)
+
+
 def stack_train_step(cfg: StackCfg, block_layers: int, streamed: bool, bufs: StackBuffersC,
-                     step: int, h0, lr: float = 2e-4, stream=None, copy_stream=None):
+                     step: int, h0, lr: float = 2e-4, stream=None, copy_stream=None, opts=None):
+    """opts: StepOptsC (micro-batches and their order) or None for one micro-batch."""
     c = cfg.c()
-    _check("ws_stack_train_step",
-           _lib.ws_stack_train_step(C.byref(c), block_layers, 1 if streamed else 0,
-                                    C.byref(bufs), step, _ptr(h0), lr, _stream(stream),
-                                    _stream(copy_stream) if copy_stream is not None else None))
+    _check("ws_stack_train_step_ex",
+           _lib.ws_stack_train_step_ex(C.byref(c), block_layers, 1 if streamed else 0,
+                                       C.byref(opts) if opts is not None else None,
+                                       C.byref(bufs), step, _ptr(h0), lr, _stream(stream),
+                                       _stream(copy_stream) if copy_stream is not None else None))
 
 
 class StepGraph:
     """One training step of the stack captured as a CUDA graph
-    (ws_stack_graph_create); ``step`` replays it for any step number."""
+    (ws_stack_graph_create_ex); ``step`` replays it for any step number."""
 
     def __init__(self, cfg: StackCfg, block_layers: int, streamed: bool, bufs: StackBuffersC,
-                 lr: float, stream, copy_stream=None):
+                 lr: float, stream, copy_stream=None, opts=None):
         self._bufs = bufs  # the graph keeps these pointers
+        self._opts = opts
         c = cfg.c()
         h = C.c_void_p()
-        _check("ws_stack_graph_create",
-               _lib.ws_stack_graph_create(C.byref(c), block_layers, 1 if streamed else 0,
-                                          C.byref(bufs), lr, _stream(stream),
-                                          _stream(copy_stream) if copy_stream is not None else None,
-                                          C.byref(h)))
+        _check("ws_stack_graph_create_ex",
+               _lib.ws_stack_graph_create_ex(C.byref(c), block_layers, 1 if streamed else 0,
+                                             C.byref(opts) if opts is not None else None,
+                                             C.byref(bufs), lr, _stream(stream),
+                                             _stream(copy_stream) if copy_stream is not None
+                                             else None, C.byref(h)))
         self._h = h
 
     def step(self, step: int, h0, stream=None):
         _check("ws_stack_graph_step", _lib.ws_stack_graph_step(self._h, step, _ptr(h0), _stream(stream)))
+
+    def copy_times_ms(self):
+        """Durations (ms) of the block copies of the last replay (graphs made with time_copies)."""
+        n = i32(0)
+        cap = 4096
+        buf = (C.c_float * cap)()
+        _check("ws_stack_graph_copy_times",
+               _lib.ws_stack_graph_copy_times(self._h, buf, cap, C.byref(n)))
+        return [float(buf[i]) for i in range(min(n.value, cap))]
 
     def close(self):
         if self._h is not None and self._h.value:

@@ -17,13 +17,17 @@ from . import ops
 
 class StackRun:
     def __init__(self, cfg: ops.StackCfg, block_layers: int, streamed: bool, weight_fn,
-                 param_fn, device="cuda", image_from: "StackRun" = None):
+                 param_fn, device="cuda", image_from: "StackRun" = None, n_micro: int = 1,
+                 order: int = ops.GA_MICROBATCH_MAJOR):
         """weight_fn(layer, lin, N, K) -> bf16 [N, K] device tensor (the frozen base);
         param_fn(layer, lin, N, K) -> (A [16, K], B [N, 16]) fp32 device tensors.
-        image_from: a resident run of the same config whose quantised image is
-        copied instead of quantising again."""
+        image_from: another run of the same config (resident or streamed) whose
+        quantised image is copied instead of quantising again.  n_micro / order: gradient
+        accumulation over n_micro micro-batches per step (h0 [n_micro, M*H])."""
         assert cfg.n_layers % block_layers == 0
         self.cfg, self.bl, self.streamed = cfg, block_layers, streamed
+        self.n_micro, self.order = n_micro, order
+        self.opts = ops.step_opts(n_micro, order)
         self.nb = cfg.n_layers // block_layers
         sz = ops.stack_sizes(cfg, block_layers)
         self.sizes = sz
@@ -33,7 +37,9 @@ class StackRun:
         f32 = dict(dtype=torch.float32, device=dev)
         # ---- frozen NF4 base, quantised block by block
         stage = torch.empty(bb, dtype=torch.uint8, device=dev)
-        src_img = None if image_from is None else image_from.dev_weights
+        src_img = None
+        if image_from is not None:
+            src_img = image_from.host_weights if image_from.streamed else image_from.dev_weights
         if streamed:
             self.host_weights = torch.empty(self.nb * bb, dtype=torch.uint8, pin_memory=True)
             self.window = torch.empty(2 * bb, dtype=torch.uint8, device=dev)
@@ -46,6 +52,9 @@ class StackRun:
         for b in range(self.nb):
             img = stage if streamed else self.dev_weights[b * bb:(b + 1) * bb]
             if src_img is not None:
+                if streamed and src_img.device.type == "cpu":
+                    self.host_weights[b * bb:(b + 1) * bb].copy_(src_img[b * bb:(b + 1) * bb])
+                    continue
                 img.copy_(src_img[b * bb:(b + 1) * bb])
                 if streamed:
                     self.host_weights[b * bb:(b + 1) * bb].copy_(stage)
@@ -74,10 +83,10 @@ class StackRun:
         self.grads = torch.zeros(n, **f32)
         self.adam_m = torch.zeros(n, **f32)
         self.adam_v = torch.zeros(n, **f32)
-        self.boundary = torch.zeros((self.nb + 1) * M * H, **f32)
+        self.boundary = torch.zeros(n_micro * (self.nb + 1) * M * H, **f32)
         self.saved = None if streamed else torch.empty(cfg.n_layers * sz["saved_layer"],
                                                        dtype=torch.uint8, device=dev)
-        self.dh = torch.zeros(2 * M * H, **f32)
+        self.dh = torch.zeros(max(2, n_micro) * M * H, **f32)
         self.workspace = torch.empty(sz["workspace"], dtype=torch.uint8, device=dev)
         self.loss = torch.zeros(1, **f32)
         self.copy_stream = torch.cuda.Stream(device=dev) if streamed else None
@@ -90,12 +99,15 @@ class StackRun:
     def step(self, step: int, h0: torch.Tensor, lr: float = 2e-4, stream=None):
         """Enqueue one training step (ws_stack_train_step) on ``stream``."""
         ops.stack_train_step(self.cfg, self.bl, self.streamed, self.c, step, h0, lr, stream=stream,
-                             copy_stream=self.copy_stream)
+                             copy_stream=self.copy_stream, opts=self.opts)
 
-    def graph(self, lr: float, stream: torch.cuda.Stream) -> "ops.StepGraph":
+    def graph(self, lr: float, stream: torch.cuda.Stream, time_copies: bool = False) -> "ops.StepGraph":
         """Capture one training step as a CUDA graph on ``stream`` (a created
-        stream, not the default one); ``g.step(step, h0, stream)`` replays it."""
-        return ops.StepGraph(self.cfg, self.bl, self.streamed, self.c, lr, stream, self.copy_stream)
+        stream, not the default one); ``g.step(step, h0, stream)`` replays it.
+        time_copies (streamed runs): time every block copy of a replay."""
+        opts = ops.step_opts(self.n_micro, self.order, time_copies)
+        return ops.StepGraph(self.cfg, self.bl, self.streamed, self.c, lr, stream, self.copy_stream,
+                             opts=opts)
 
     def param(self, layer: int, lin: int, which: str, t: torch.Tensor = None):
         """View of A [16, K] or B [N, 16] of (layer, lin) inside a parameter-layout array."""
