@@ -316,6 +316,33 @@ enum { WS_SV_H = 0, WS_SV_A = 1, WS_SV_RSTD1 = 2, WS_SV_V = 3, WS_SV_VR = 4, WS_
 ws_status ws_stack_saved_offset(const ws_stack_cfg* cfg, int32_t field, int32_t lin,
                                 size_t* offset);
 
+/* The streamed NF4 loader ("Poros", block-streamed NF4 loader paragraphs:
+ * one tensor is staged at a time, quantised and evicted before the next, so
+ * the whole base never sits on the GPU, and the result is byte-identical to a
+ * standard load).  ws_stack_put_weight_nf4 quantises one bf16 weight
+ * W [N, K] (device; (N, K) must be linear `lin`'s shape) of layer `layer`
+ * into its place in a stack image that holds all n_layers / block_layers
+ * blocks back to back:
+ *   image on the device: quantised straight into place;
+ *   image in pinned host memory: quantised into `staging` (device, at least
+ *   ws_stack_loader_staging_bytes) and copied from there with
+ *   cudaMemcpyAsync on `stream` (the copy reads staging, so a later call on
+ *   the same stream may reuse it; a call on another stream may not until
+ *   this one's copy has completed).
+ * The caller feeds the tensors one at a time (its own W buffer can be freed
+ * or refilled after the call's work on `stream` is done), so the GPU holds
+ * one bf16 tensor and one tensor's NF4 at a time.  Bytes between the
+ * 256-aligned pieces of the image are not written: zero the image first for
+ * a byte-comparable result.  Errors: WS_ERR_SHAPE for a wrong (N, K),
+ * WS_ERR_OOM for a staging buffer too small, WS_ERR_INVALID for a layer or
+ * linear out of range, WS_ERR_NOT_PINNED for a host image that is not
+ * page-locked. */
+ws_status ws_stack_loader_staging_bytes(const ws_stack_cfg* cfg, size_t* bytes);
+ws_status ws_stack_put_weight_nf4(const ws_stack_cfg* cfg, int32_t block_layers, int32_t layer,
+                                  int32_t lin, const uint16_t* W, int64_t N, int64_t K,
+                                  void* image, void* staging, size_t staging_bytes,
+                                  ws_stream_t stream);
+
 /* Offsets (in floats) of A [r, K] and B [N, r] of (layer, lin) in the
  * parameter arrays (params, grads and both Adam moments share the layout). */
 ws_status ws_stack_param_offset(const ws_stack_cfg* cfg, int32_t layer, int32_t lin,
@@ -434,12 +461,17 @@ ws_status ws_stack_train_step(const ws_stack_cfg* cfg, int32_t block_layers, int
  * ignores `order`.  h0 holds n_micro inputs [n_micro, M, H]; the buffers
  * grow as ws_stack_buffers states.
  * time_copies != 0 (graphs of streamed steps only) records timing events
- * around every block copy; ws_stack_graph_copy_times reads them. */
+ * around every block copy; ws_stack_graph_copy_times reads them.
+ * copy_piece_bytes > 0 issues each block copy as consecutive
+ * cudaMemcpyAsync pieces of that size (a multiple of 256) instead of one
+ * copy; results are the same. */
 enum { WS_GA_MICROBATCH_MAJOR = 0, WS_GA_BLOCK_MAJOR = 1 };
 typedef struct {
-  int32_t n_micro;      /* micro-batches per step, >= 1 */
-  int32_t order;        /* WS_GA_*                       */
-  int32_t time_copies;  /* 0 or 1                        */
+  int32_t n_micro;           /* micro-batches per step, >= 1 */
+  int32_t order;             /* WS_GA_*                       */
+  int32_t time_copies;       /* 0 or 1                        */
+  int32_t reserved;          /* 0                             */
+  int64_t copy_piece_bytes;  /* 0: one copy per block         */
 } ws_step_opts;
 /* opts == NULL: one micro-batch, no timing (ws_stack_train_step). */
 ws_status ws_stack_train_step_ex(const ws_stack_cfg* cfg, int32_t block_layers, int32_t streamed,

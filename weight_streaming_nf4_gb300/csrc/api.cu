@@ -226,6 +226,68 @@ ws_status ws_stack_saved_offset(const ws_stack_cfg* cfg, int32_t field, int32_t 
   return stack_saved_offset(*cfg, field, lin, offset) ? WS_OK : WS_ERR_INVALID;
 }
 
+ws_status ws_stack_loader_staging_bytes(const ws_stack_cfg* cfg, size_t* bytes) {
+  ws_status s = stack_check(cfg);
+  if (s != WS_OK) return s;
+  if (!bytes) return WS_ERR_INVALID;
+  const int64_t N[WS_NLIN] = {cfg->H, cfg->KV, cfg->KV, cfg->H, cfg->I, cfg->I, cfg->H};
+  const int64_t K[WS_NLIN] = {cfg->H, cfg->H, cfg->H, cfg->H, cfg->H, cfg->H, cfg->I};
+  size_t mx = 0;
+  for (int i = 0; i < WS_NLIN; ++i) {
+    // codes, then the block scales 256 bytes further on
+    const size_t b = (((size_t)N[i] * (size_t)(K[i] / 2) + 255) & ~(size_t)255) +
+                     (size_t)(K[i] / 64) * (size_t)N[i] * 4;
+    if (b > mx) mx = b;
+  }
+  *bytes = mx;
+  return WS_OK;
+}
+
+ws_status ws_stack_put_weight_nf4(const ws_stack_cfg* cfg, int32_t block_layers, int32_t layer,
+                                  int32_t lin, const uint16_t* W, int64_t N, int64_t K,
+                                  void* image, void* staging, size_t staging_bytes,
+                                  ws_stream_t stream) {
+  ws_status s = stack_check(cfg);
+  if (s != WS_OK) return s;
+  if (!W || !image) return WS_ERR_INVALID;
+  if (block_layers < 1 || cfg->n_layers % block_layers) return WS_ERR_SHAPE;
+  if (layer < 0 || layer >= cfg->n_layers || lin < 0 || lin >= WS_NLIN) return WS_ERR_INVALID;
+  const int64_t Ns[WS_NLIN] = {cfg->H, cfg->KV, cfg->KV, cfg->H, cfg->I, cfg->I, cfg->H};
+  const int64_t Ks[WS_NLIN] = {cfg->H, cfg->H, cfg->H, cfg->H, cfg->H, cfg->H, cfg->I};
+  if (N != Ns[lin] || K != Ks[lin]) return WS_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(image)) return WS_ERR_ALIGN;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, image) != cudaSuccess) {
+    cudaGetLastError();
+    return WS_ERR_NOT_PINNED;
+  }
+  const bool host = attr.type == cudaMemoryTypeHost;
+  if (!host && attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return WS_ERR_NOT_PINNED;
+  size_t oc = 0, oa = 0;
+  const int blk = layer / block_layers, lib = layer % block_layers;
+  stack_weight_offset(*cfg, lib, lin, &oc, &oa);
+  const size_t base = (size_t)blk * stack_block_bytes(*cfg, block_layers);
+  uint8_t* img = static_cast<uint8_t*>(image) + base;
+  const size_t code_bytes = (size_t)N * (size_t)(K / 2);
+  const size_t scale_bytes = (size_t)(K / 64) * (size_t)N * 4;
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (!host)
+    return cuda_status(run_quantize_nf4(W, N, K, img + oc, reinterpret_cast<float*>(img + oa), st));
+  size_t need = 0;
+  ws_stack_loader_staging_bytes(cfg, &need);
+  if (!staging) return WS_ERR_INVALID;
+  if (!aligned16(staging)) return WS_ERR_ALIGN;
+  if (staging_bytes < need) return WS_ERR_OOM;
+  uint8_t* sg = static_cast<uint8_t*>(staging);
+  const size_t sa = (code_bytes + 255) & ~(size_t)255;
+  cudaError_t e = run_quantize_nf4(W, N, K, sg, reinterpret_cast<float*>(sg + sa), st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(img + oc, sg, code_bytes, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(img + oa, sg + sa, scale_bytes, cudaMemcpyDeviceToHost, st);
+  return cuda_status(e);
+}
+
 ws_status ws_stack_workspace_offset(const ws_stack_cfg* cfg, int32_t block_layers, int32_t field,
                                    size_t* offset) {
   ws_status s = stack_check(cfg);
@@ -363,6 +425,7 @@ struct StepOpts {
   int n_micro = 1;
   int order = WS_GA_MICROBATCH_MAJOR;
   bool time_copies = false;
+  size_t piece = 0;  // 0: one copy per block
 };
 
 ws_status read_opts(const ws_step_opts* o, StepOpts* out) {
@@ -370,9 +433,12 @@ ws_status read_opts(const ws_step_opts* o, StepOpts* out) {
   if (o) {
     if (o->n_micro < 1 || o->n_micro > 0xFFFFFF) return WS_ERR_INVALID;
     if (o->order != WS_GA_MICROBATCH_MAJOR && o->order != WS_GA_BLOCK_MAJOR) return WS_ERR_INVALID;
+    if (o->copy_piece_bytes < 0 || (o->copy_piece_bytes % 256) != 0 || o->reserved != 0)
+      return WS_ERR_INVALID;
     r.n_micro = o->n_micro;
     r.order = o->order;
     r.time_copies = o->time_copies != 0;
+    r.piece = (size_t)o->copy_piece_bytes;
   }
   *out = r;
   return WS_OK;
@@ -450,9 +516,14 @@ ws_status step_body(const ws_stack_cfg& cfg, int block_layers, bool streamed, co
     const bool timed = ev.n_timed < ev.cap_timed;
     if (timed && cudaEventRecordWithFlags(ev.t0[ev.n_timed], st, cudaEventRecordExternal) != cudaSuccess)
       return WS_ERR_CUDA;
-    ws_status r = ws_stream_block_h2d(host + (size_t)blk * bbytes, window + (size_t)sl * bbytes,
-                                      bbytes, (ws_stream_t)st, nullptr, (ws_event_t)ev.loaded[sl]);
-    if (r != WS_OK) return r;
+    const size_t piece = (o.piece == 0 || o.piece > bbytes) ? bbytes : o.piece;
+    for (size_t off = 0; off < bbytes; off += piece) {
+      const size_t n = bbytes - off < piece ? bbytes - off : piece;
+      ws_status r = ws_stream_block_h2d(host + (size_t)blk * bbytes + off,
+                                        window + (size_t)sl * bbytes + off, n, (ws_stream_t)st,
+                                        nullptr, off + n == bbytes ? (ws_event_t)ev.loaded[sl] : nullptr);
+      if (r != WS_OK) return r;
+    }
     if (timed) {
       if (cudaEventRecordWithFlags(ev.t1[ev.n_timed], st, cudaEventRecordExternal) != cudaSuccess)
         return WS_ERR_CUDA;

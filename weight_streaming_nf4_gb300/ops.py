@@ -62,7 +62,8 @@ class StackCfgC(C.Structure):
 
 
 class StepOptsC(C.Structure):
-    _fields_ = [("n_micro", i32), ("order", i32), ("time_copies", i32)]
+    _fields_ = [("n_micro", i32), ("order", i32), ("time_copies", i32), ("reserved", i32),
+                ("copy_piece_bytes", i64)]
 
 
 class StackBuffersC(C.Structure):
@@ -100,6 +101,8 @@ _sig("ws_stack_weight_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(C.c_si
 _sig("ws_stack_param_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(i64), C.POINTER(i64)])
 _sig("ws_stack_saved_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(C.c_size_t)])
 _sig("ws_stack_workspace_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(C.c_size_t)])
+_sig("ws_stack_loader_staging_bytes", [C.POINTER(StackCfgC), C.POINTER(C.c_size_t)])
+_sig("ws_stack_put_weight_nf4", [C.POINTER(StackCfgC), i32, i32, i32, P, i64, i64, P, P, C.c_size_t, P])
 _sig("ws_block_forward", [C.POINTER(StackCfgC), P, i32, i32, P, u32, u32, P, P, P, P, C.c_size_t,
                           P])
 _sig("ws_block_backward_recompute", [C.POINTER(StackCfgC), P, i32, i32, P, u32, u32, P, P, P, P,
@@ -121,7 +124,8 @@ EXPORTED = ("ws_status_string", "ws_device_error", "ws_selfcheck_bounded_wait", 
             "ws_lora_linear_fwd", "ws_lora_linear_bwd", "ws_nf4_matmul_workspace_size",
             "ws_nf4_matmul", "ws_nf4_matmul_noalloc", "ws_stack_sizes",
             "ws_stack_weight_offset", "ws_stack_param_offset", "ws_stack_saved_offset",
-            "ws_stack_workspace_offset", "ws_block_forward", "ws_block_backward_recompute",
+            "ws_stack_workspace_offset", "ws_stack_loader_staging_bytes", "ws_stack_put_weight_nf4",
+            "ws_block_forward", "ws_block_backward_recompute",
             "ws_stream_block_h2d", "ws_stack_train_step", "ws_stack_train_step_ex",
             "ws_stack_graph_create", "ws_stack_graph_create_ex", "ws_stack_graph_copy_times",
             "ws_stack_graph_step", "ws_stack_graph_destroy")
@@ -361,6 +365,25 @@ def stack_saved_offset(cfg: StackCfg, field: str, lin: int = 0) -> int:
     return int(off.value)
 
 
+def stack_loader_staging_bytes(cfg: StackCfg) -> int:
+    n = C.c_size_t(0)
+    c = cfg.c()
+    _check("ws_stack_loader_staging_bytes", _lib.ws_stack_loader_staging_bytes(C.byref(c), C.byref(n)))
+    return int(n.value)
+
+
+def stack_put_weight_nf4(cfg: StackCfg, block_layers: int, layer: int, lin: int, W, image,
+                         staging=None, stream=None):
+    """Quantise one bf16 weight W [N, K] (device) into its place in a stack image
+    (device, or pinned host through the device staging buffer)."""
+    c = cfg.c()
+    N, K = W.shape
+    _check("ws_stack_put_weight_nf4",
+           _lib.ws_stack_put_weight_nf4(C.byref(c), block_layers, layer, lin, _ptr(W), N, K,
+                                        _ptr(image), _ptr(staging),
+                                        0 if staging is None else staging.numel(), _stream(stream)))
+
+
 WORKSPACE_FIELDS = dict(y1=0, dact=1, dg=2, du=3, db=4, dh1=5, dvr=6, dv=7, da=8, yout=9)
 
 
@@ -405,8 +428,8 @@ def stream_block_h2d(pinned_src: torch.Tensor, dev_dst: torch.Tensor, nbytes: in
                                     C.c_void_p(done_event) if done_event else None))
 
 
-def step_opts(n_micro=1, order=GA_MICROBATCH_MAJOR, time_copies=False):
-    return StepOptsC(n_micro, order, 1 if time_copies else 0)
+def step_opts(n_micro=1, order=GA_MICROBATCH_MAJOR, time_copies=False, copy_piece_bytes=0):
+    return StepOptsC(n_micro, order, 1 if time_copies else 0, 0, copy_piece_bytes)
 
 
 def stack_train_step(cfg: StackCfg, block_layers: int, streamed: bool, bufs: StackBuffersC,

@@ -5,8 +5,10 @@ reads or writes (the library allocates nothing): the NF4 block images (a
 pinned host image plus a 2-slot HBM window when streamed, one HBM image when
 resident), LoRA parameters, gradients, Adam moments, block-boundary
 activations, saved activations (resident), the gradient buffer, the
-workspace and the loss scalar.  Weights are quantised on the GPU with
-``ws_quantize_nf4`` straight into the block images.
+workspace and the loss scalar.  Weights are quantised on the GPU by the
+streamed loader (``ws_stack_put_weight_nf4``), one tensor at a time, straight
+into the block image (device) or through a one-tensor staging buffer into
+the pinned image (host).
 """
 from __future__ import annotations
 
@@ -35,42 +37,34 @@ class StackRun:
         dev = torch.device(device)
         M, H = cfg.M, cfg.H
         f32 = dict(dtype=torch.float32, device=dev)
-        # ---- frozen NF4 base, quantised block by block
-        stage = torch.empty(bb, dtype=torch.uint8, device=dev)
-        src_img = None
-        if image_from is not None:
-            src_img = image_from.host_weights if image_from.streamed else image_from.dev_weights
+        # ---- frozen NF4 base: the images are zeroed (the bytes between the
+        # 256-aligned pieces then compare equal too) and filled one tensor at a
+        # time by the streamed loader (ws_stack_put_weight_nf4): the GPU holds
+        # one bf16 weight and one tensor's NF4 at a time
         if streamed:
-            self.host_weights = torch.empty(self.nb * bb, dtype=torch.uint8, pin_memory=True)
+            self.host_weights = torch.zeros(self.nb * bb, dtype=torch.uint8, pin_memory=True)
             self.window = torch.empty(2 * bb, dtype=torch.uint8, device=dev)
             self.dev_weights = None
         else:
             self.host_weights = None
             self.window = None
-            self.dev_weights = torch.empty(self.nb * bb, dtype=torch.uint8, device=dev)
+            self.dev_weights = torch.zeros(self.nb * bb, dtype=torch.uint8, device=dev)
+        image = self.host_weights if streamed else self.dev_weights
         shapes = cfg.shapes()
-        for b in range(self.nb):
-            img = stage if streamed else self.dev_weights[b * bb:(b + 1) * bb]
-            if src_img is not None:
-                if streamed and src_img.device.type == "cpu":
-                    self.host_weights[b * bb:(b + 1) * bb].copy_(src_img[b * bb:(b + 1) * bb])
-                    continue
-                img.copy_(src_img[b * bb:(b + 1) * bb])
-                if streamed:
-                    self.host_weights[b * bb:(b + 1) * bb].copy_(stage)
-                continue
-            for li in range(block_layers):
-                layer = b * block_layers + li
+        if image_from is not None:
+            src = image_from.host_weights if image_from.streamed else image_from.dev_weights
+            for b in range(self.nb):
+                image[b * bb:(b + 1) * bb].copy_(src[b * bb:(b + 1) * bb])
+        else:
+            staging = (torch.empty(ops.stack_loader_staging_bytes(cfg), dtype=torch.uint8,
+                                   device=dev) if streamed else None)
+            for layer in range(cfg.n_layers):
                 for lin, (N, K) in enumerate(shapes):
-                    oc, oa = ops.stack_weight_offset(cfg, li, lin)
-                    codes = img[oc:oc + N * K // 2].view(N, K // 2)
-                    absmax = img[oa:oa + 4 * N * K // 64].view(torch.float32).view(K // 64, N)
                     W = weight_fn(layer, lin, N, K)
-                    ops.quantize_nf4(W, codes, absmax)
+                    ops.stack_put_weight_nf4(cfg, block_layers, layer, lin, W, image, staging)
                     del W
-            if streamed:
-                self.host_weights[b * bb:(b + 1) * bb].copy_(stage)
-        del stage
+            torch.cuda.current_stream(dev).synchronize()
+            del staging
         # ---- LoRA parameters, gradients, Adam state
         n = sz["n_params"]
         self.params = torch.zeros(n, **f32)
@@ -101,11 +95,13 @@ class StackRun:
         ops.stack_train_step(self.cfg, self.bl, self.streamed, self.c, step, h0, lr, stream=stream,
                              copy_stream=self.copy_stream, opts=self.opts)
 
-    def graph(self, lr: float, stream: torch.cuda.Stream, time_copies: bool = False) -> "ops.StepGraph":
+    def graph(self, lr: float, stream: torch.cuda.Stream, time_copies: bool = False,
+              copy_piece_bytes: int = 0) -> "ops.StepGraph":
         """Capture one training step as a CUDA graph on ``stream`` (a created
         stream, not the default one); ``g.step(step, h0, stream)`` replays it.
-        time_copies (streamed runs): time every block copy of a replay."""
-        opts = ops.step_opts(self.n_micro, self.order, time_copies)
+        time_copies (streamed runs): time every block copy of a replay;
+        copy_piece_bytes: issue each block copy in pieces of that size."""
+        opts = ops.step_opts(self.n_micro, self.order, time_copies, copy_piece_bytes)
         return ops.StepGraph(self.cfg, self.bl, self.streamed, self.c, lr, stream, self.copy_stream,
                              opts=opts)
 
