@@ -687,6 +687,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the 7B and 72B sub-benchmarks")
     ap.add_argument("--no-72b", action="store_true", help="skip the 72B-shaped streamed run")
+    ap.add_argument("--no-bf16", action="store_true", help="skip the bf16-base 32B-shaped run")
     ap.add_argument("--profile-step", action="store_true",
                     help="only the resident run: W warm-up steps and one step inside the NVTX "
                          "range 'timed'; for an ncu launch list of one step")
@@ -796,8 +797,9 @@ def main():
         }
         out.update(extra)
     # ---- the 72B-shaped stack, streamed and resident (one GPU only)
-    if rank == 0 and world == 1 and not args.quick and not args.no_72b:
+    if rank == 0:
         del m, res
+    if rank == 0 and world == 1 and not args.quick and not args.no_72b:
         release_host_cache(torch)
         cfg72 = ops.StackCfg(**SHAPE_72B)
         need = nf4_bytes(cfg72.H, cfg72.KV, cfg72.I, cfg72.n_layers)
@@ -817,6 +819,26 @@ def main():
             rep["host_mem_available_bytes"] = avail
             out["qwen72b"] = rep
             del m72
+            release_host_cache(torch)
+    # ---- the 32B-shaped stack with a bf16 base (the pages' bf16 streaming mode)
+    if rank == 0 and world == 1 and not args.quick and not args.no_bf16:
+        release_host_cache(torch)
+        cfgb = ops.StackCfg(**SHAPE_32B, base=ops.BASE_BF16)
+        need = 2 * sum(N * K for N, K in lin_shapes(cfgb.H, cfgb.KV, cfgb.I)) * cfgb.n_layers
+        avail = host_mem_available()
+        if avail is not None and avail < need + (16 << 30):
+            out["bf16_base_32b"] = {"skipped": f"host memory available {avail} < pinned image {need} + 16 GiB"}
+        else:
+            kb = min(args.steps, 3)
+            mb = measure_stack(ops, StackRun, torch, None, cfgb, dev, kb, 3)
+            rep = streaming_report(mb, out["streaming"]["h2d_link_peak_gbs"], kb)
+            rep["workload"] = ("qwen2.5-32b-shaped stack with a bf16 base (2 bytes per weight), "
+                               "64 layers, seq 512, blocks of 4, 2-slot window")
+            rep["steps"] = kb
+            rep["tflops_resident"] = flops * kb / mb["t_res"] / 1e12
+            rep["tflops_streamed"] = flops * kb / mb["t_stm"] / 1e12
+            out["bf16_base_32b"] = rep
+            del mb
             release_host_cache(torch)
     if rank == 0:
         print(json.dumps(out))

@@ -106,6 +106,13 @@ typedef struct {
   int64_t N, K;
 } ws_nf4;
 
+/* A frozen bf16 weight [N, K], row-major (device pointer); the base of the
+ * bf16 streaming mode ("Limitations", section "bf16 LoRA (EXPERIMENTAL)"). */
+typedef struct {
+  const uint16_t* w;
+  int64_t N, K;
+} ws_bf16;
+
 /* Dropout key of one linear.  Element e = m*K + k of the LoRA input is kept
  * iff word (e & 3) of Philox4x32-10(counter = (e >> 2, linear | microbatch
  * << 8, layer, step), key = (seed_lo, seed_hi)) >= ceil(p * 2^32).
@@ -218,6 +225,22 @@ ws_status ws_lora_linear_bwd(const ws_nf4* W, const uint16_t* x, const float* A,
                              int32_t accumulate, float* dA, float* dB,
                              void* workspace, size_t ws_bytes, ws_stream_t stream);
 
+/* The same forward and backward with a bf16 base weight (the pages' bf16
+ * streaming mode, "Limitations", section "bf16 LoRA (EXPERIMENTAL)"): the
+ * weight tiles are loaded by TMA into the tensor-core operand layout instead
+ * of being dequantised; everything else, the shapes, arguments, workspace
+ * and errors, is that of ws_lora_linear_fwd / _bwd. */
+ws_status ws_lora_linear_fwd_bf16(const ws_bf16* W, const uint16_t* x, const float* A,
+                                  const float* B, ws_lora_shape sh, ws_dropout_key key,
+                                  uint16_t* y, float* U_saved, uint32_t* mask_saved,
+                                  void* workspace, size_t ws_bytes, ws_stream_t stream);
+ws_status ws_lora_linear_bwd_bf16(const ws_bf16* W, const uint16_t* x, const float* A,
+                                  const float* B, ws_lora_shape sh, ws_dropout_key key,
+                                  const float* U_saved, const uint32_t* mask_saved,
+                                  const uint16_t* dY, void* dX, int32_t dX_dtype,
+                                  int32_t accumulate, float* dA, float* dB, void* workspace,
+                                  size_t ws_bytes, ws_stream_t stream);
+
 /* ---- the frozen NF4 product alone ---------------------------------------------- */
 /* The dequant GEMM of the LoRA linear without adapter or dropout (a frozen NF4
  * linear; the base term of the training-step paragraph of "Poros"):
@@ -274,6 +297,7 @@ ws_status ws_nf4_matmul_noalloc(const ws_nf4* W, const uint16_t* act, int64_t M,
  * gradients that enter a linear as dY are bf16, all other activation
  * gradients are fp32.  q and k feed only the replaced attention core, so
  * their adapters receive exactly zero gradient.  loss = 0.5 mean(h_L^2). */
+enum { WS_BASE_NF4 = 0, WS_BASE_BF16 = 1 };
 typedef struct {
   int64_t M, H, KV, I, head_dim;
   int32_t n_layers;
@@ -282,10 +306,13 @@ typedef struct {
   double p;
   float eps;
   uint64_t seed;
+  int32_t base;  /* the frozen base's format: WS_BASE_NF4, or WS_BASE_BF16
+                    (the pages' bf16_bitwise mode: same engine and GEMM, the
+                    weights stream as bf16, 2 bytes per weight) */
 } ws_stack_cfg;
 
 /* Sizes of the stack's buffers for a given block size (layers per block):
- *   block_weight_bytes : NF4 bytes of one block (one window slot)
+ *   block_weight_bytes : base-weight bytes of one block (one window slot)
  *   n_params           : fp32 LoRA parameters of the whole stack (A then B
  *                        of every linear, see ws_stack_param_offset)
  *   saved_bytes_layer  : activations one layer keeps for its backward
@@ -295,8 +322,10 @@ ws_status ws_stack_sizes(const ws_stack_cfg* cfg, int32_t block_layers,
                          size_t* block_weight_bytes, int64_t* n_params,
                          size_t* saved_bytes_layer, size_t* workspace_bytes);
 
-/* Offsets inside a block's NF4 image of layer `layer_in_block`, linear `lin`:
- * codes at byte *off_codes, absmax at byte *off_absmax (both 256-aligned). */
+/* Offsets inside a block's image of layer `layer_in_block`, linear `lin`:
+ * NF4 base: codes at byte *off_codes, absmax at byte *off_absmax (both
+ * 256-aligned); bf16 base: the weight W [N, K] at *off_codes (256-aligned),
+ * and *off_absmax = *off_codes. */
 ws_status ws_stack_weight_offset(const ws_stack_cfg* cfg, int32_t layer_in_block, int32_t lin,
                                  size_t* off_codes, size_t* off_absmax);
 
@@ -319,7 +348,7 @@ ws_status ws_stack_saved_offset(const ws_stack_cfg* cfg, int32_t field, int32_t 
 /* The streamed NF4 loader ("Poros", block-streamed NF4 loader paragraphs:
  * one tensor is staged at a time, quantised and evicted before the next, so
  * the whole base never sits on the GPU, and the result is byte-identical to a
- * standard load).  ws_stack_put_weight_nf4 quantises one bf16 weight
+ * standard load).  For an NF4 base, ws_stack_put_weight quantises one bf16 weight
  * W [N, K] (device; (N, K) must be linear `lin`'s shape) of layer `layer`
  * into its place in a stack image that holds all n_layers / block_layers
  * blocks back to back:
@@ -336,12 +365,12 @@ ws_status ws_stack_saved_offset(const ws_stack_cfg* cfg, int32_t field, int32_t 
  * a byte-comparable result.  Errors: WS_ERR_SHAPE for a wrong (N, K),
  * WS_ERR_OOM for a staging buffer too small, WS_ERR_INVALID for a layer or
  * linear out of range, WS_ERR_NOT_PINNED for a host image that is not
- * page-locked. */
+ * page-locked.  For a bf16 base the weight is copied into place as it is
+ * (cudaMemcpyAsync; no staging is used, `staging` may be NULL). */
 ws_status ws_stack_loader_staging_bytes(const ws_stack_cfg* cfg, size_t* bytes);
-ws_status ws_stack_put_weight_nf4(const ws_stack_cfg* cfg, int32_t block_layers, int32_t layer,
-                                  int32_t lin, const uint16_t* W, int64_t N, int64_t K,
-                                  void* image, void* staging, size_t staging_bytes,
-                                  ws_stream_t stream);
+ws_status ws_stack_put_weight(const ws_stack_cfg* cfg, int32_t block_layers, int32_t layer,
+                              int32_t lin, const uint16_t* W, int64_t N, int64_t K, void* image,
+                              void* staging, size_t staging_bytes, ws_stream_t stream);
 
 /* Offsets (in floats) of A [r, K] and B [N, r] of (layer, lin) in the
  * parameter arrays (params, grads and both Adam moments share the layout). */

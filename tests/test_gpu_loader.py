@@ -1,4 +1,4 @@
-"""The streamed NF4 loader (ws_stack_put_weight_nf4): the stack image is
+"""The streamed NF4 loader (ws_stack_put_weight): the stack image is
 built one tensor at a time, straight into HBM or through a one-tensor device
 staging buffer into pinned host memory, so the GPU never holds more than one
 bf16 weight and its NF4 form (research page "Poros", block-streamed NF4 loader
@@ -60,8 +60,8 @@ def test_loader_images_are_byte_identical_to_the_oracle(ops, orc):
     for (layer, lin), w in W.items():
         Wd = bf16_to_dev(w)
         largest = max(largest, Wd.numel() * 2)
-        ops.stack_put_weight_nf4(cfg, bl, layer, lin, Wd, host, staging)
-        ops.stack_put_weight_nf4(cfg, bl, layer, lin, Wd, devimg)
+        ops.stack_put_weight(cfg, bl, layer, lin, Wd, host, staging)
+        ops.stack_put_weight(cfg, bl, layer, lin, Wd, devimg)
         del Wd
     torch.cuda.synchronize()
     assert ops.device_error() == 0
@@ -78,15 +78,15 @@ def test_loader_argument_errors(ops):
     staging = torch.empty(ops.stack_loader_staging_bytes(cfg), dtype=torch.uint8, device="cuda:0")
     W = torch.zeros(512, 256, dtype=torch.bfloat16, device="cuda:0")  # gate's shape
     with pytest.raises(ops.WsError) as e:
-        ops.stack_put_weight_nf4(cfg, 1, 0, 0, W, host, staging)     # q is [256, 256]
+        ops.stack_put_weight(cfg, 1, 0, 0, W, host, staging)     # q is [256, 256]
     assert e.value.status == -2
     with pytest.raises(ops.WsError) as e:
-        ops.stack_put_weight_nf4(cfg, 1, 0, 4, W, host, staging[:1024])
+        ops.stack_put_weight(cfg, 1, 0, 4, W, host, staging[:1024])
     assert e.value.status == -6
     with pytest.raises(ops.WsError) as e:
-        ops.stack_put_weight_nf4(cfg, 1, 2, 4, W, host, staging)     # layer out of range
+        ops.stack_put_weight(cfg, 1, 2, 4, W, host, staging)     # layer out of range
     assert e.value.status == -1
     pageable = torch.zeros(n, dtype=torch.uint8)
     with pytest.raises(ops.WsError) as e:
-        ops.stack_put_weight_nf4(cfg, 1, 0, 4, W, pageable, staging)
+        ops.stack_put_weight(cfg, 1, 0, 4, W, pageable, staging)
     assert e.value.status == -8

@@ -44,6 +44,7 @@ NF4View view_of(const ws_nf4* W) {
   NF4View v;
   v.codes = W->codes;
   v.absmax = W->absmax;
+  v.wbf16 = nullptr;
   v.N = W->N;
   v.K = W->K;
   return v;
@@ -137,6 +138,68 @@ ws_status ws_lora_linear_bwd(const ws_nf4* W, const uint16_t* x, const float* A,
     return WS_ERR_ALIGN;
   if (ws_bytes < linear_workspace_bytes(sh.M, sh.N, sh.K)) return WS_ERR_OOM;
   return cuda_status(linear_bwd(view_of(W), x, A, B, sh.M, lora_scale(sh, key.p),
+                                make_drop_key(key), U_saved, mask_saved, dY, dX,
+                                dX_dtype == WS_DTYPE_F32 ? 1 : 0, dX_accumulate, dA, dB,
+                                (accumulate & WS_ACC_GRADS) ? 1 : 0, workspace,
+                                (cudaStream_t)stream));
+}
+
+namespace {
+ws_status check_bf16(const ws_bf16* W, ws_lora_shape sh, const ws_dropout_key& key, ws_nf4* as) {
+  if (!W || !W->w) return WS_ERR_INVALID;
+  // the shape and key checks of the NF4 path, with the bf16 pointer standing in
+  *as = ws_nf4{reinterpret_cast<const uint8_t*>(W->w), reinterpret_cast<const float*>(W->w), W->N,
+               W->K};
+  return check_linear(as, sh, key);
+}
+NF4View view_of_bf16(const ws_bf16* W) {
+  NF4View v;
+  v.codes = nullptr;
+  v.absmax = nullptr;
+  v.wbf16 = W->w;
+  v.N = W->N;
+  v.K = W->K;
+  return v;
+}
+}  // namespace
+
+ws_status ws_lora_linear_fwd_bf16(const ws_bf16* W, const uint16_t* x, const float* A,
+                                  const float* B, ws_lora_shape sh, ws_dropout_key key,
+                                  uint16_t* y, float* U_saved, uint32_t* mask_saved,
+                                  void* workspace, size_t ws_bytes, ws_stream_t stream) {
+  ws_nf4 as;
+  ws_status s = check_bf16(W, sh, key, &as);
+  if (s != WS_OK) return s;
+  if (!x || !A || !B || !y || !U_saved || !workspace) return WS_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(y) || !aligned16(U_saved) ||
+      !aligned16(workspace) || (mask_saved && !aligned16(mask_saved)))
+    return WS_ERR_ALIGN;
+  if (ws_bytes < linear_workspace_bytes(sh.M, sh.N, sh.K)) return WS_ERR_OOM;
+  return cuda_status(linear_fwd(view_of_bf16(W), x, A, B, sh.M, lora_scale(sh, key.p),
+                                make_drop_key(key), y, U_saved, mask_saved, workspace,
+                                (cudaStream_t)stream));
+}
+
+ws_status ws_lora_linear_bwd_bf16(const ws_bf16* W, const uint16_t* x, const float* A,
+                                  const float* B, ws_lora_shape sh, ws_dropout_key key,
+                                  const float* U_saved, const uint32_t* mask_saved,
+                                  const uint16_t* dY, void* dX, int32_t dX_dtype,
+                                  int32_t accumulate, float* dA, float* dB, void* workspace,
+                                  size_t ws_bytes, ws_stream_t stream) {
+  ws_nf4 as;
+  ws_status s = check_bf16(W, sh, key, &as);
+  if (s != WS_OK) return s;
+  if (!x || !A || !B || !U_saved || !dY || !dX || !dA || !dB || !workspace) return WS_ERR_INVALID;
+  if (dX_dtype != WS_DTYPE_BF16 && dX_dtype != WS_DTYPE_F32) return WS_ERR_INVALID;
+  if (accumulate & ~(WS_ACC_DX | WS_ACC_GRADS)) return WS_ERR_INVALID;
+  const int dX_accumulate = (accumulate & WS_ACC_DX) ? 1 : 0;
+  if (dX_accumulate && dX_dtype != WS_DTYPE_F32) return WS_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(U_saved) || !aligned16(dY) ||
+      !aligned16(dX) || !aligned16(dA) || !aligned16(dB) || !aligned16(workspace) ||
+      (mask_saved && !aligned16(mask_saved)))
+    return WS_ERR_ALIGN;
+  if (ws_bytes < linear_workspace_bytes(sh.M, sh.N, sh.K)) return WS_ERR_OOM;
+  return cuda_status(linear_bwd(view_of_bf16(W), x, A, B, sh.M, lora_scale(sh, key.p),
                                 make_drop_key(key), U_saved, mask_saved, dY, dX,
                                 dX_dtype == WS_DTYPE_F32 ? 1 : 0, dX_accumulate, dA, dB,
                                 (accumulate & WS_ACC_GRADS) ? 1 : 0, workspace,
@@ -243,10 +306,9 @@ ws_status ws_stack_loader_staging_bytes(const ws_stack_cfg* cfg, size_t* bytes) 
   return WS_OK;
 }
 
-ws_status ws_stack_put_weight_nf4(const ws_stack_cfg* cfg, int32_t block_layers, int32_t layer,
-                                  int32_t lin, const uint16_t* W, int64_t N, int64_t K,
-                                  void* image, void* staging, size_t staging_bytes,
-                                  ws_stream_t stream) {
+ws_status ws_stack_put_weight(const ws_stack_cfg* cfg, int32_t block_layers, int32_t layer,
+                              int32_t lin, const uint16_t* W, int64_t N, int64_t K, void* image,
+                              void* staging, size_t staging_bytes, ws_stream_t stream) {
   ws_status s = stack_check(cfg);
   if (s != WS_OK) return s;
   if (!W || !image) return WS_ERR_INVALID;
@@ -269,9 +331,11 @@ ws_status ws_stack_put_weight_nf4(const ws_stack_cfg* cfg, int32_t block_layers,
   stack_weight_offset(*cfg, lib, lin, &oc, &oa);
   const size_t base = (size_t)blk * stack_block_bytes(*cfg, block_layers);
   uint8_t* img = static_cast<uint8_t*>(image) + base;
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (cfg->base == WS_BASE_BF16)
+    return cuda_status(cudaMemcpyAsync(img + oc, W, (size_t)N * (size_t)K * 2, cudaMemcpyDefault, st));
   const size_t code_bytes = (size_t)N * (size_t)(K / 2);
   const size_t scale_bytes = (size_t)(K / 64) * (size_t)N * 4;
-  const cudaStream_t st = (cudaStream_t)stream;
   if (!host)
     return cuda_status(run_quantize_nf4(W, N, K, img + oc, reinterpret_cast<float*>(img + oa), st));
   size_t need = 0;

@@ -13,10 +13,13 @@ typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_
                                     const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                     CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// A frozen base weight [N, K]: NF4 (codes, absmax) or, when wbf16 is set,
+// bf16 row-major (codes and absmax unused).
 struct NF4View {
   const uint8_t* codes;  // [N, K/2]
   const float* absmax;   // [K/64, N]
   int64_t N, K;
+  const uint16_t* wbf16 = nullptr;
 };
 
 // Linears of one grouped launch at most (q, k, v share the attention

@@ -112,7 +112,8 @@ struct DqGeo {
   static_assert(!BWD || (64 * COLS / (VB * 2)) % kDqThreads == 0, "dequant geometry");
 };
 
-template <bool BWD, int UM, int BN, int PAIR>
+// WB: the weight is bf16 and its tiles are loaded by TMA (no dequantisation).
+template <bool BWD, int UM, int BN, int PAIR, bool WB = false>
 struct Cfg {
   static constexpr int BM = 128 * UM;
   static constexpr uint32_t A_BYTES = BM * 128;   // BM rows x 64 bf16
@@ -126,7 +127,7 @@ struct Cfg {
 #endif
   // per-thread ring of fetched codes (cp.async), CSTAGES steps deep
   static constexpr int CSTAGES = WS_GEMM_CSTAGES;
-  static constexpr uint32_t CODE_BYTES = DqGeo<BWD, BN, PAIR>::SLOT_BYTES;
+  static constexpr uint32_t CODE_BYTES = WB ? 0u : DqGeo<BWD, BN, PAIR>::SLOT_BYTES;
   static constexpr int STAGES_RAW =
       (int)((220u * 1024u - BSTAGES * B_BYTES - CSTAGES * CODE_BYTES - 1024u) / A_BYTES);
   static constexpr int STAGES = STAGES_RAW > WS_GEMM_STAGES_MAX ? WS_GEMM_STAGES_MAX : STAGES_RAW;
@@ -138,9 +139,12 @@ struct Cfg {
   static constexpr uint32_t TMEM_COLS = ACC_COLS * ACC_BUFS;
   static constexpr int64_t TILE_FLOATS = (int64_t)BM * BN;
   // MN-major operand (backward): 64-element MN groups LBO apart, 8-row K
-  // groups SBO apart.
-  static constexpr uint32_t MN_LBO = 1024;
-  static constexpr uint32_t MN_SBO = (BW / 64) * 1024;
+  // groups SBO apart; MN_KK bytes per 16-deep slice.  The dequantiser
+  // interleaves the MN groups inside each 8-row group; a bf16 tile arrives
+  // as BW/64 TMA boxes of 64 rows x 64 columns, one 8 KB box per MN group.
+  static constexpr uint32_t MN_LBO = WB ? 8192u : 1024u;
+  static constexpr uint32_t MN_SBO = WB ? 1024u : (uint32_t)(BW / 64) * 1024u;
+  static constexpr uint32_t MN_KK = 2 * MN_SBO;
   static constexpr uint32_t OFF_A = 0;
   static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr uint32_t OFF_CODE = OFF_B + BSTAGES * B_BYTES;
@@ -153,6 +157,7 @@ struct Cfg {
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory");
   static_assert(BN == 128 || BN == 256, "BN");
   static_assert(!PAIR || UM == 2, "a pair shares one weight tile between two 256-row halves");
+  static_assert(!WB || PAIR != 1, "bf16 tiles are loaded by each CTA itself");
   static_assert(PAIR >= 0 && PAIR <= 2, "pair mode");
   static_assert(OFF_CODE >= (uint32_t)(kEpiWarps * kFinRing * 2048), "finisher ring fits the stages");
 };
@@ -489,11 +494,17 @@ struct Pos {
 //     arrive on both CTAs' barriers.  Nothing is copied between the CTAs.
 // The stream-K schedule runs over pairs; partial tiles and their flags stay
 // per CTA.
-template <bool BWD, int UM, int BN, int PAIR>
+// Tensor maps of bf16 weights (WB): the forward's group g uses m[g] (box 64
+// x BW rows of W [N_g, K]); the backward uses m[0] (box 64 x 64).
+struct WMaps {
+  CUtensorMap m[kMaxGroups];
+};
+
+template <bool BWD, int UM, int BN, int PAIR, bool WB>
 __global__ void __launch_bounds__(kThreads, 1)
     k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmL,
-               const GemmArgs args) {
-  using C = Cfg<BWD, UM, BN, PAIR>;
+               const GemmArgs args, const __grid_constant__ WMaps wm) {
+  using C = Cfg<BWD, UM, BN, PAIR, WB>;
   constexpr int STAGES = C::STAGES;
   constexpr int BSTAGES = C::BSTAGES;
   constexpr int NACC = C::ACC_BUFS;
@@ -694,22 +705,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const bool is_lora = is_lora_step(i);
-            const uint32_t a_base = smem_u32(sA + s * C::A_BYTES);
-            const uint32_t b_base = smem_u32(sB + b * C::B_BYTES);
+            // The descriptors of this step's operands are built once; each
+            // 16-deep slice and 128-row atom is then a plain add to the
+            // start-address field (address >> 4, which stays below 2^14 in
+            // shared memory, so the adds never carry out of the field).
+            const uint64_t adesc0 = smem_desc_sw128(smem_u32(sA + s * C::A_BYTES), 16, 1024);
+            const bool kmaj = !BWD || is_lora;
+            const uint64_t bdesc0 =
+                kmaj ? smem_desc_sw128(smem_u32(sB + b * C::B_BYTES), 16, 1024)
+                     : smem_desc_sw128(smem_u32(sB + b * C::B_BYTES), C::MN_LBO, C::MN_SBO);
+            const uint64_t bstep = kmaj ? 2u : (uint64_t)(C::MN_KK >> 4);
+            const uint32_t idesc = is_lora ? idesc_kmaj : idesc_main;
+            const uint32_t first = p2 > p ? 1u : 0u;  // accumulate from the first slice on
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              uint64_t bdesc;
-              if (!BWD || is_lora)
-                bdesc = smem_desc_sw128(b_base + kk * 32, 16, 1024);
-              else
-                bdesc = smem_desc_sw128(b_base + kk * 2 * C::MN_SBO, C::MN_LBO, C::MN_SBO);
+              const uint64_t bdesc = bdesc0 + (uint64_t)kk * bstep;
 #pragma unroll
               for (int u = 0; u < UM; ++u) {
-                const uint64_t adesc = smem_desc_sw128(a_base + u * 16384 + kk * 32, 16, 1024);
+                const uint64_t adesc = adesc0 + (uint64_t)(u * 1024 + kk * 2);
                 const uint32_t d = dbase + (uint32_t)(u * BN);
-                const uint32_t acc = (p2 > p || kk > 0) ? 1u : 0u;
-                if constexpr (PM) tc_mma_f16_pair(d, adesc, bdesc, is_lora ? idesc_kmaj : idesc_main, acc);
-                else tc_mma_f16(d, adesc, bdesc, is_lora ? idesc_kmaj : idesc_main, acc);
+                const uint32_t acc = kk > 0 ? 1u : first;
+                if constexpr (PM) tc_mma_f16_pair(d, adesc, bdesc, idesc, acc);
+                else tc_mma_f16(d, adesc, bdesc, idesc, acc);
               }
             }
             if constexpr (PM) {
@@ -774,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Pos pf = pos0;  // position of the next fetch
       int64_t fq = 0;
       auto fetch = [&]() {
-        if (fq < n_it && !is_lora_step(pf.i)) {
+        if (!WB && fq < n_it && !is_lora_step(pf.i)) {
           const uint32_t slot = smem_u32(ring + (fq % CS) * C::CODE_BYTES);
           const int64_t nb = (int64_t)pf.nt * BN;
           if constexpr (BWD) {
@@ -791,12 +808,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++fq;
       };
 #pragma unroll 1
-      for (int k = 0; k < CS - 1; ++k) fetch();
+      for (int k = 0; k < CS - 1; ++k)
+        if constexpr (!WB) fetch();
       for (int64_t q = 0; q < n_it; ++q) {
-        fetch();  // refills the slot read in the previous iteration
-        cp_async_wait<CS - 1>();
         Frag cur;
-        read_frag<BWD, BN, PAIR>(cur, ring + (q % CS) * C::CODE_BYTES, t_idx);
+        if constexpr (!WB) {
+          fetch();  // refills the slot read in the previous iteration
+          cp_async_wait<CS - 1>();
+          read_frag<BWD, BN, PAIR>(cur, ring + (q % CS) * C::CODE_BYTES, t_idx);
+        }
         bool ok = !*abort_flag;
         if constexpr (PAIR != 0) ok = ok && mbar_wait_cluster(&bempty[b], bph ^ 1u, DERR_TIMEOUT_BEMPTY);
         else ok = ok && mbar_wait(&bempty[b], bph ^ 1u, DERR_TIMEOUT_BEMPTY);
@@ -806,17 +826,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* Bt = sB + b * C::B_BYTES;
         const bool lora_step = is_lora_step(pc.i);
+        // bf16 weights: one thread loads the tile (this CTA's half of it in a
+        // pair) with TMA; its arrival carries the bytes, the other warps arrive
+        // as usual
+        const bool tma_step = WB && !lora_step;
         if (!lora_step) {
-          if (!BWD) dequant_fwd<BN, PAIR>(cur, Bt, rank, t_idx);
-          else dequant_bwd<BN, PAIR>(cur, Bt, rank, t_idx);
+          if constexpr (WB) {
+            if (warp == 2 && lane == 0) {
+              const int64_t nb = (int64_t)pc.nt * BN;
+              const int32_t kc = kstep(pc.i) * 64;
+              const int32_t half0 = PM ? rank * C::BW : 0;
+              mbar_arrive_expect_tx(&bfull[b], C::B_BYTES);
+              if constexpr (!BWD) {
+                const TileGrp tg = tile_grp(args, nb);
+                const CUtensorMap* m = tg.g == 2 ? &wm.m[2] : (tg.g == 1 ? &wm.m[1] : &wm.m[0]);
+                tma_load_2d(Bt, m, &bfull[b], kc, (int32_t)(nb - tg.c0) + half0);
+              } else {
+#pragma unroll
+                for (int j = 0; j < C::BW / 64; ++j)
+                  tma_load_2d(Bt + j * 8192, &wm.m[0], &bfull[b], (int32_t)nb + half0 + j * 64, kc);
+              }
+            }
+          } else {
+            if (!BWD) dequant_fwd<BN, PAIR>(cur, Bt, rank, t_idx);
+            else dequant_bwd<BN, PAIR>(cur, Bt, rank, t_idx);
+          }
         } else {
           const TileGrp tg = tile_grp(args, (int64_t)pc.nt * BN);
           lora_tile<BWD, BN, PAIR>(tg.lora_F, tg.width, tg.width, (int)((int64_t)pc.nt * BN - tg.c0),
                                    args.lora_scale, Bt, rank, t_idx);
         }
-        fence_proxy_async_smem();
+        if (!tma_step) fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 0 && !(tma_step && warp == 2)) {
           if constexpr (PM) {
             // the even CTA's MMA reads this half where it lies
             mbar_arrive(&bfull[b]);
@@ -844,6 +886,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         pc.next(S, args.mtiles);
       }
       cp_async_wait<0>();  // no copy may land after the CTA is gone
+      if (WB && *abort_flag && warp == 2 && lane == 0) {
+        // weight tiles this thread loaded may still be in flight: give them
+        // time to land (a tile copy takes microseconds)
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 200000ull) __nanosleep(1000);
+      }
       if constexpr (PAIR != 0) {
         // the other CTA's MMA commits arrive on this CTA's buffer barriers:
         // wait for the last of them before the CTA can leave
@@ -1713,15 +1761,22 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 #endif
 constexpr int kEpadSteps = WS_GEMM_EPAD;
 
+// 256-wide tiles when every unit's stream-K range covers at least this many
+// (tile, step) iterations.
+#ifndef WS_GEMM_BN256_MIN_STEPS
+#define WS_GEMM_BN256_MIN_STEPS 64
+#endif
+constexpr int64_t kBn256MinSteps = WS_GEMM_BN256_MIN_STEPS;
+
 // Persistent grid: one CTA per SM, but at least kMinSteps (tile, step)
 // iterations per CTA so tiny problems are not shredded into partials.
 constexpr int64_t kMinSteps = 8;
 
-template <bool BWD, int UM, int BN, int PAIR>
+template <bool BWD, int UM, int BN, int PAIR, bool WB = false>
 cudaError_t set_smem_attr() {
-  static cudaError_t e = cudaFuncSetAttribute(k_nf4_gemm<BWD, UM, BN, PAIR>,
+  static cudaError_t e = cudaFuncSetAttribute(k_nf4_gemm<BWD, UM, BN, PAIR, WB>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)Cfg<BWD, UM, BN, PAIR>::SMEM_BYTES);
+                                              (int)Cfg<BWD, UM, BN, PAIR, WB>::SMEM_BYTES);
   return e;
 }
 
@@ -1749,16 +1804,16 @@ int pair_mode() {
 }
 
 // Pairs of CTAs that can be resident at once (one CTA per SM).
-template <bool BWD, int BN, int PAIR>
+template <bool BWD, int BN, int PAIR, bool WB = false>
 int64_t pair_capacity_of() {
   static int64_t cap = -1;
   if (cap < 0) {
     cap = 0;
-    if (set_smem_attr<BWD, 2, BN, PAIR>() == cudaSuccess) {
+    if (set_smem_attr<BWD, 2, BN, PAIR, WB>() == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * (unsigned)(device_sm_count() / 2));
       cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = Cfg<BWD, 2, BN, PAIR>::SMEM_BYTES;
+      cfg.dynamicSmemBytes = Cfg<BWD, 2, BN, PAIR, WB>::SMEM_BYTES;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = 2;
@@ -1767,7 +1822,7 @@ int64_t pair_capacity_of() {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, k_nf4_gemm<BWD, 2, BN, PAIR>, &cfg) == cudaSuccess)
+      if (cudaOccupancyMaxActiveClusters(&n, k_nf4_gemm<BWD, 2, BN, PAIR, WB>, &cfg) == cudaSuccess)
         cap = n;
       else
         cudaGetLastError();
@@ -1778,13 +1833,16 @@ int64_t pair_capacity_of() {
   return cap;
 }
 
-template <bool BWD, int UM, int BN, int PAIR>
+template <bool BWD, int UM, int BN, int PAIR, bool WB = false>
 cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& tA,
-                       const CUtensorMap& tL, cudaStream_t st) {
-  using C = Cfg<BWD, UM, BN, PAIR>;
-  cudaError_t e = set_smem_attr<BWD, UM, BN, PAIR>();
+                       const CUtensorMap& tL, const WMaps& wm, cudaStream_t st) {
+  using C = Cfg<BWD, UM, BN, PAIR, WB>;
+  cudaError_t e = set_smem_attr<BWD, UM, BN, PAIR, WB>();
   if (e != cudaSuccess) return e;
   const int64_t G = grid_ctas(p, a.has_lora != 0);
+  // the plan sizes pair grids by the NF4 kernel's residency; the bf16
+  // variant (no code ring) must fit the same grid at once
+  if (WB && PAIR != 0 && G / 2 > pair_capacity_of<BWD, BN, PAIR, WB>()) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)G);
   cfg.blockDim = dim3(kThreads);
@@ -1824,7 +1882,7 @@ cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& 
   cfg.attrs = attr;
   cfg.numAttrs = na;
   note_launch();
-  return cudaLaunchKernelEx(&cfg, k_nf4_gemm<BWD, UM, BN, PAIR>, tA, tL, a);
+  return cudaLaunchKernelEx(&cfg, k_nf4_gemm<BWD, UM, BN, PAIR, WB>, tA, tL, a, wm);
 }
 
 }  // namespace
@@ -1917,7 +1975,7 @@ GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc) {
     // unit's stream-K range stays long (>= 64 steps).
     const int64_t units = p.pair ? pair_capacity(bwd, 256) : device_sm_count();
     const int64_t mt = (M + urows - 1) / urows, nt = (Nout + 255) / 256;
-    if (units > 0 && mt * nt * (Kc / 64 + 1) >= 64 * units) p.bn = 256;
+    if (units > 0 && mt * nt * (Kc / 64 + 1) >= kBn256MinSteps * units) p.bn = 256;
   }
   p.mtiles = (int)((M + urows - 1) / urows);
   p.ntiles = (int)((Nout + p.bn - 1) / p.bn);
@@ -1946,31 +2004,60 @@ size_t gemm_partial_bytes(const GemmPlan& p, int64_t M, int64_t Nout) {
 namespace {
 // The kernel instantiation of a plan.
 cudaError_t dispatch_gemm(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& tA,
-                          const CUtensorMap& tL, cudaStream_t st) {
+                          const CUtensorMap& tL, const WMaps& wm, cudaStream_t st) {
   const bool pm = pair_mode() == 2;
   if (!p.bwd) {
     if (p.pair && pm) {
-      if (p.bn == 256) return launch_cfg<false, 2, 256, 2>(p, a, tA, tL, st);
-      return launch_cfg<false, 2, 128, 2>(p, a, tA, tL, st);
+      if (p.bn == 256) return launch_cfg<false, 2, 256, 2>(p, a, tA, tL, wm, st);
+      return launch_cfg<false, 2, 128, 2>(p, a, tA, tL, wm, st);
     }
     if (p.pair) {
-      if (p.bn == 256) return launch_cfg<false, 2, 256, 1>(p, a, tA, tL, st);
-      return launch_cfg<false, 2, 128, 1>(p, a, tA, tL, st);
+      if (p.bn == 256) return launch_cfg<false, 2, 256, 1>(p, a, tA, tL, wm, st);
+      return launch_cfg<false, 2, 128, 1>(p, a, tA, tL, wm, st);
     }
-    if (p.um == 2 && p.bn == 256) return launch_cfg<false, 2, 256, 0>(p, a, tA, tL, st);
-    if (p.um == 2) return launch_cfg<false, 2, 128, 0>(p, a, tA, tL, st);
-    return launch_cfg<false, 1, 128, 0>(p, a, tA, tL, st);
+    if (p.um == 2 && p.bn == 256) return launch_cfg<false, 2, 256, 0>(p, a, tA, tL, wm, st);
+    if (p.um == 2) return launch_cfg<false, 2, 128, 0>(p, a, tA, tL, wm, st);
+    return launch_cfg<false, 1, 128, 0>(p, a, tA, tL, wm, st);
   }
   if (p.pair && pm) {
-    if (p.bn == 256) return launch_cfg<true, 2, 256, 2>(p, a, tA, tL, st);
-    return launch_cfg<true, 2, 128, 2>(p, a, tA, tL, st);
+    if (p.bn == 256) return launch_cfg<true, 2, 256, 2>(p, a, tA, tL, wm, st);
+    return launch_cfg<true, 2, 128, 2>(p, a, tA, tL, wm, st);
   }
   if (p.pair) {
-    if (p.bn == 256) return launch_cfg<true, 2, 256, 1>(p, a, tA, tL, st);
-    return launch_cfg<true, 2, 128, 1>(p, a, tA, tL, st);
+    if (p.bn == 256) return launch_cfg<true, 2, 256, 1>(p, a, tA, tL, wm, st);
+    return launch_cfg<true, 2, 128, 1>(p, a, tA, tL, wm, st);
   }
-  if (p.um == 2) return launch_cfg<true, 2, 128, 0>(p, a, tA, tL, st);
-  return launch_cfg<true, 1, 128, 0>(p, a, tA, tL, st);
+  if (p.um == 2) return launch_cfg<true, 2, 128, 0>(p, a, tA, tL, wm, st);
+  return launch_cfg<true, 1, 128, 0>(p, a, tA, tL, wm, st);
+}
+
+// The same for a bf16 weight: pairs always share the tile through the pair MMA.
+cudaError_t dispatch_gemm_wb(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& tA,
+                             const CUtensorMap& tL, const WMaps& wm, cudaStream_t st) {
+  if (!p.bwd) {
+    if (p.pair) {
+      if (p.bn == 256) return launch_cfg<false, 2, 256, 2, true>(p, a, tA, tL, wm, st);
+      return launch_cfg<false, 2, 128, 2, true>(p, a, tA, tL, wm, st);
+    }
+    if (p.um == 2 && p.bn == 256) return launch_cfg<false, 2, 256, 0, true>(p, a, tA, tL, wm, st);
+    if (p.um == 2) return launch_cfg<false, 2, 128, 0, true>(p, a, tA, tL, wm, st);
+    return launch_cfg<false, 1, 128, 0, true>(p, a, tA, tL, wm, st);
+  }
+  if (p.pair) {
+    if (p.bn == 256) return launch_cfg<true, 2, 256, 2, true>(p, a, tA, tL, wm, st);
+    return launch_cfg<true, 2, 128, 2, true>(p, a, tA, tL, wm, st);
+  }
+  if (p.um == 2) return launch_cfg<true, 2, 128, 0, true>(p, a, tA, tL, wm, st);
+  return launch_cfg<true, 1, 128, 0, true>(p, a, tA, tL, wm, st);
+}
+
+// Tensor maps of bf16 weights for a plan: rows of W [N, K] in boxes of
+// 64 x (this CTA's share of the tile's rows) for the forward, 64 x 64 for the
+// backward (which reads BW / 64 column groups per contraction step).
+bool make_wmap(CUtensorMap* m, const GemmPlan& p, const uint16_t* w, int64_t N, int64_t K) {
+  const uint32_t bw = (uint32_t)(p.pair ? p.bn / 2 : p.bn);
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, (uint64_t)K, (uint64_t)N,
+                  (uint64_t)K * 2, 64, p.bwd ? 64u : bw, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 }  // namespace
 
@@ -2020,7 +2107,13 @@ cudaError_t run_nf4_gemm(const GemmPlan& p, const NF4View& W, const uint16_t* ac
   }
 
   if (partial == nullptr && grid_units(p, has_lora) > 1) return cudaErrorInvalidValue;
-  return dispatch_gemm(p, a, tA, tL, st);
+  WMaps wm;
+  memset(&wm, 0, sizeof(wm));
+  if (W.wbf16) {
+    if (!make_wmap(&wm.m[0], p, W.wbf16, N, K)) return cudaErrorInvalidValue;
+    return dispatch_gemm_wb(p, a, tA, tL, wm, st);
+  }
+  return dispatch_gemm(p, a, tA, tL, wm, st);
 }
 
 cudaError_t run_nf4_gemm_group(const GemmPlan& p, int ng, const NF4View* W, const uint16_t* act,
@@ -2030,6 +2123,13 @@ cudaError_t run_nf4_gemm_group(const GemmPlan& p, int ng, const NF4View* W, cons
   if (!encode_fn()) return cudaErrorNotSupported;
   if (ng < 1 || ng > kMaxGroups || p.bwd || lora_act == nullptr) return cudaErrorInvalidValue;
   const int64_t K = W[0].K;
+  WMaps wm;
+  memset(&wm, 0, sizeof(wm));
+  const bool wb = W[0].wbf16 != nullptr;
+  for (int g = 0; g < ng; ++g) {
+    if ((W[g].wbf16 != nullptr) != wb) return cudaErrorInvalidValue;
+    if (wb && !make_wmap(&wm.m[g], p, W[g].wbf16, W[g].N, K)) return cudaErrorInvalidValue;
+  }
   GemmArgs a{};
   a.ngroups = ng;
   a.gcol[0] = 0;
@@ -2072,7 +2172,8 @@ cudaError_t run_nf4_gemm_group(const GemmPlan& p, int ng, const NF4View* W, cons
     if (e != cudaSuccess) return e;
     if (partial == nullptr) return cudaErrorInvalidValue;
   }
-  return dispatch_gemm(p, a, tA, tL, st);
+  if (wb) return dispatch_gemm_wb(p, a, tA, tL, wm, st);
+  return dispatch_gemm(p, a, tA, tL, wm, st);
 }
 
 // ------------------------------------------------------------------------ bounded-wait self-check

@@ -341,12 +341,19 @@ SavedLayout saved_layout(const ws_stack_cfg& c) {
 struct WeightLayout {
   size_t codes[WS_NLIN], absmax[WS_NLIN], layer_bytes;
 };
+// Per layer, the 7 linears in q,k,v,o,gate,up,down order, each piece
+// 256-aligned: NF4 codes then block scales, or the bf16 weight alone.
 WeightLayout weight_layout(const ws_stack_cfg& c) {
   const Shapes s = shapes_of(c);
   WeightLayout L{};
   size_t o = 0;
   for (int i = 0; i < WS_NLIN; ++i) {
     L.codes[i] = o;
+    if (c.base == WS_BASE_BF16) {
+      o += al256((size_t)s.N[i] * (size_t)s.K[i] * 2);
+      L.absmax[i] = L.codes[i];
+      continue;
+    }
     o += al256((size_t)s.N[i] * (size_t)(s.K[i] / 2));
     L.absmax[i] = o;
     o += al256((size_t)(s.K[i] / 64) * (size_t)s.N[i] * 4);
@@ -447,10 +454,16 @@ struct Ctx {
 NF4View wview(const Ctx& x, const void* block, int layer_in_block, int lin) {
   NF4View v;
   const uint8_t* base = static_cast<const uint8_t*>(block) + (size_t)layer_in_block * x.WL.layer_bytes;
-  v.codes = base + x.WL.codes[lin];
-  v.absmax = reinterpret_cast<const float*>(base + x.WL.absmax[lin]);
   v.N = x.s.N[lin];
   v.K = x.s.K[lin];
+  if (x.c.base == WS_BASE_BF16) {
+    v.codes = nullptr;
+    v.absmax = nullptr;
+    v.wbf16 = reinterpret_cast<const uint16_t*>(base + x.WL.codes[lin]);
+    return v;
+  }
+  v.codes = base + x.WL.codes[lin];
+  v.absmax = reinterpret_cast<const float*>(base + x.WL.absmax[lin]);
   return v;
 }
 
@@ -666,6 +679,7 @@ ws_status stack_check(const ws_stack_cfg* c) {
   if (c->H % c->KV || c->H % c->head_dim || c->KV % c->head_dim) return WS_ERR_SHAPE;
   if (c->r != 16) return WS_ERR_SHAPE;
   if (!(c->p >= 0.0 && c->p < 1.0)) return WS_ERR_INVALID;
+  if (c->base != WS_BASE_NF4 && c->base != WS_BASE_BF16) return WS_ERR_INVALID;
   if ((double)c->M * (double)c->I >= 17179869184.0) return WS_ERR_SHAPE;
   return WS_OK;
 }

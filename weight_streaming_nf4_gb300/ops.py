@@ -55,10 +55,17 @@ class LoraShape(C.Structure):
     _fields_ = [("M", i64), ("N", i64), ("K", i64), ("r", i32), ("alpha", C.c_float)]
 
 
+class Bf16W(C.Structure):
+    _fields_ = [("w", P), ("N", i64), ("K", i64)]
+
+
+BASE_NF4, BASE_BF16 = 0, 1
+
+
 class StackCfgC(C.Structure):
     _fields_ = [("M", i64), ("H", i64), ("KV", i64), ("I", i64), ("head_dim", i64),
                 ("n_layers", i32), ("r", i32), ("alpha", C.c_float), ("p", C.c_double),
-                ("eps", C.c_float), ("seed", u64)]
+                ("eps", C.c_float), ("seed", u64), ("base", i32)]
 
 
 class StepOptsC(C.Structure):
@@ -91,6 +98,10 @@ _sig("ws_lora_linear_fwd", [C.POINTER(Nf4), P, P, P, LoraShape, DropoutKey, P, P
                             C.c_size_t, P])
 _sig("ws_lora_linear_bwd", [C.POINTER(Nf4), P, P, P, LoraShape, DropoutKey, P, P, P, P, i32,
                             i32, P, P, P, C.c_size_t, P])
+_sig("ws_lora_linear_fwd_bf16", [C.POINTER(Bf16W), P, P, P, LoraShape, DropoutKey, P, P, P, P,
+                                 C.c_size_t, P])
+_sig("ws_lora_linear_bwd_bf16", [C.POINTER(Bf16W), P, P, P, LoraShape, DropoutKey, P, P, P, P, i32,
+                                 i32, P, P, P, C.c_size_t, P])
 _sig("ws_nf4_matmul_workspace_size", [i64, i64, i64, i32, C.POINTER(C.c_size_t)])
 _sig("ws_nf4_matmul", [C.POINTER(Nf4), P, i64, i32, P, i32, P, C.c_size_t, P])
 _sig("ws_nf4_matmul_noalloc", [C.POINTER(Nf4), P, i64, i32, P, i32, P])
@@ -102,7 +113,7 @@ _sig("ws_stack_param_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(i64), C
 _sig("ws_stack_saved_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(C.c_size_t)])
 _sig("ws_stack_workspace_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(C.c_size_t)])
 _sig("ws_stack_loader_staging_bytes", [C.POINTER(StackCfgC), C.POINTER(C.c_size_t)])
-_sig("ws_stack_put_weight_nf4", [C.POINTER(StackCfgC), i32, i32, i32, P, i64, i64, P, P, C.c_size_t, P])
+_sig("ws_stack_put_weight", [C.POINTER(StackCfgC), i32, i32, i32, P, i64, i64, P, P, C.c_size_t, P])
 _sig("ws_block_forward", [C.POINTER(StackCfgC), P, i32, i32, P, u32, u32, P, P, P, P, C.c_size_t,
                           P])
 _sig("ws_block_backward_recompute", [C.POINTER(StackCfgC), P, i32, i32, P, u32, u32, P, P, P, P,
@@ -121,10 +132,11 @@ _sig("ws_stack_graph_step", [P, u32, P, P])
 _sig("ws_stack_graph_destroy", [P])
 
 EXPORTED = ("ws_status_string", "ws_device_error", "ws_selfcheck_bounded_wait", "ws_kernel_launches", "ws_quantize_nf4", "ws_lora_workspace_size",
-            "ws_lora_linear_fwd", "ws_lora_linear_bwd", "ws_nf4_matmul_workspace_size",
+            "ws_lora_linear_fwd", "ws_lora_linear_bwd", "ws_lora_linear_fwd_bf16",
+            "ws_lora_linear_bwd_bf16", "ws_nf4_matmul_workspace_size",
             "ws_nf4_matmul", "ws_nf4_matmul_noalloc", "ws_stack_sizes",
             "ws_stack_weight_offset", "ws_stack_param_offset", "ws_stack_saved_offset",
-            "ws_stack_workspace_offset", "ws_stack_loader_staging_bytes", "ws_stack_put_weight_nf4",
+            "ws_stack_workspace_offset", "ws_stack_loader_staging_bytes", "ws_stack_put_weight",
             "ws_block_forward", "ws_block_backward_recompute",
             "ws_stream_block_h2d", "ws_stack_train_step", "ws_stack_train_step_ex",
             "ws_stack_graph_create", "ws_stack_graph_create_ex", "ws_stack_graph_copy_times",
@@ -197,6 +209,17 @@ class NF4Weight:
         return Nf4(self.codes.data_ptr(), self.absmax.data_ptr(), self.N, self.K)
 
 
+@dataclasses.dataclass
+class Bf16Weight:
+    """A frozen bf16 base weight W [N, K] (device)."""
+    w: torch.Tensor
+    N: int
+    K: int
+
+    def c(self):
+        return Bf16W(self.w.data_ptr(), self.N, self.K)
+
+
 def dropout_key(seed=0, step=0, layer=0, linear=0, microbatch=0, p=0.1):
     return DropoutKey(seed, step, layer, linear, microbatch, float(p))
 
@@ -222,10 +245,9 @@ def lora_linear_fwd(W: NF4Weight, x, A, B, key: DropoutKey, alpha=32.0, y=None, 
     if workspace is None:
         workspace = torch.empty(lora_workspace_size(M, W.N, W.K), dtype=torch.uint8, device=dev)
     w = W.c()
-    _check("ws_lora_linear_fwd",
-           _lib.ws_lora_linear_fwd(C.byref(w), _ptr(x), _ptr(A), _ptr(B), sh, key, _ptr(y),
-                                   _ptr(U), _ptr(mask), _ptr(workspace), workspace.numel(),
-                                   _stream(stream)))
+    fn = "ws_lora_linear_fwd_bf16" if isinstance(W, Bf16Weight) else "ws_lora_linear_fwd"
+    _check(fn, getattr(_lib, fn)(C.byref(w), _ptr(x), _ptr(A), _ptr(B), sh, key, _ptr(y), _ptr(U),
+                                 _ptr(mask), _ptr(workspace), workspace.numel(), _stream(stream)))
     return y, U, mask
 
 
@@ -247,8 +269,9 @@ def lora_linear_bwd(W: NF4Weight, x, A, B, key: DropoutKey, U, mask, dY, alpha=3
         workspace = torch.empty(lora_workspace_size(M, W.N, W.K), dtype=torch.uint8, device=dev)
     w = W.c()
     dt = WS_DTYPE_F32 if dX.dtype == torch.float32 else WS_DTYPE_BF16
-    _check("ws_lora_linear_bwd",
-           _lib.ws_lora_linear_bwd(C.byref(w), _ptr(x), _ptr(A), _ptr(B), sh, key, _ptr(U),
+    fn = "ws_lora_linear_bwd_bf16" if isinstance(W, Bf16Weight) else "ws_lora_linear_bwd"
+    _check(fn,
+           getattr(_lib, fn)(C.byref(w), _ptr(x), _ptr(A), _ptr(B), sh, key, _ptr(U),
                                    _ptr(mask), _ptr(dY), _ptr(dX), dt,
                                    (WS_ACC_DX if accumulate else 0)
                                    | (WS_ACC_GRADS if grad_accumulate else 0),
@@ -318,10 +341,11 @@ class StackCfg:
     p: float = 0.1
     eps: float = 1e-6
     seed: int = 0
+    base: int = BASE_NF4
 
     def c(self):
         return StackCfgC(self.M, self.H, self.KV, self.I, self.head_dim, self.n_layers, self.r,
-                         self.alpha, self.p, self.eps, self.seed)
+                         self.alpha, self.p, self.eps, self.seed, self.base)
 
     def shapes(self):
         H, KV, I = self.H, self.KV, self.I
@@ -372,14 +396,14 @@ def stack_loader_staging_bytes(cfg: StackCfg) -> int:
     return int(n.value)
 
 
-def stack_put_weight_nf4(cfg: StackCfg, block_layers: int, layer: int, lin: int, W, image,
+def stack_put_weight(cfg: StackCfg, block_layers: int, layer: int, lin: int, W, image,
                          staging=None, stream=None):
     """Quantise one bf16 weight W [N, K] (device) into its place in a stack image
     (device, or pinned host through the device staging buffer)."""
     c = cfg.c()
     N, K = W.shape
-    _check("ws_stack_put_weight_nf4",
-           _lib.ws_stack_put_weight_nf4(C.byref(c), block_layers, layer, lin, _ptr(W), N, K,
+    _check("ws_stack_put_weight",
+           _lib.ws_stack_put_weight(C.byref(c), block_layers, layer, lin, _ptr(W), N, K,
                                         _ptr(image), _ptr(staging),
                                         0 if staging is None else staging.numel(), _stream(stream)))
 

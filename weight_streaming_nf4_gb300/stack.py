@@ -6,7 +6,7 @@ pinned host image plus a 2-slot HBM window when streamed, one HBM image when
 resident), LoRA parameters, gradients, Adam moments, block-boundary
 activations, saved activations (resident), the gradient buffer, the
 workspace and the loss scalar.  Weights are quantised on the GPU by the
-streamed loader (``ws_stack_put_weight_nf4``), one tensor at a time, straight
+streamed loader (``ws_stack_put_weight``), one tensor at a time, straight
 into the block image (device) or through a one-tensor staging buffer into
 the pinned image (host).
 """
@@ -39,7 +39,7 @@ class StackRun:
         f32 = dict(dtype=torch.float32, device=dev)
         # ---- frozen NF4 base: the images are zeroed (the bytes between the
         # 256-aligned pieces then compare equal too) and filled one tensor at a
-        # time by the streamed loader (ws_stack_put_weight_nf4): the GPU holds
+        # time by the streamed loader (ws_stack_put_weight): the GPU holds
         # one bf16 weight and one tensor's NF4 at a time
         if streamed:
             self.host_weights = torch.zeros(self.nb * bb, dtype=torch.uint8, pin_memory=True)
@@ -61,7 +61,7 @@ class StackRun:
             for layer in range(cfg.n_layers):
                 for lin, (N, K) in enumerate(shapes):
                     W = weight_fn(layer, lin, N, K)
-                    ops.stack_put_weight_nf4(cfg, block_layers, layer, lin, W, image, staging)
+                    ops.stack_put_weight(cfg, block_layers, layer, lin, W, image, staging)
                     del W
             torch.cuda.current_stream(dev).synchronize()
             del staging
