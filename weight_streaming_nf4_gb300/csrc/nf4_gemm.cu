@@ -80,8 +80,16 @@ namespace {
 #ifndef WS_GEMM_STAGES_MAX
 #define WS_GEMM_STAGES_MAX 6
 #endif
-#ifndef WS_GEMM_CSTAGES
-#define WS_GEMM_CSTAGES 4
+// Bytes (KB) of the dequant threads' code ring: each thread fetches its codes
+// and block scales as many steps ahead as the ring holds (at least 4, at most
+// 16), so a narrower tile (shorter steps) fetches more steps ahead.
+#ifndef WS_GEMM_CODE_RING_KB
+#define WS_GEMM_CODE_RING_KB 20
+#endif
+// Shared memory (KB) the pipeline stages may take (the rest holds the
+// barriers and the alignment slack).
+#ifndef WS_GEMM_SMEM_BUDGET_KB
+#define WS_GEMM_SMEM_BUDGET_KB 220
 #endif
 
 constexpr int kDqWarps = 8;
@@ -106,7 +114,12 @@ struct DqGeo {
   // code bytes per vector and vectors per thread
   static constexpr int VB = BWD ? (PAIR ? 8 : 16) : (32 / (kDqThreads / COLS) >= 16 ? 16 : 8);
   static constexpr int NV = BWD ? (64 * COLS / (VB * 2)) / kDqThreads : (32 / TPR) / VB;
-  static constexpr int NS = BWD ? NV : 1;  // block scales per thread
+  // block scales per thread: one.  Backward items t*NV .. t*NV+NV-1 lie in
+  // one row and, NV*2*VB columns wide and aligned to that width, in one
+  // 64-column block, so they share one scale and one value table.
+  static constexpr int NS = 1;
+  static constexpr int SEGS = BWD ? COLS / (2 * VB) : 1;
+  static_assert(!BWD || (SEGS % NV == 0 && 64 % (NV * 2 * VB) == 0), "backward items share a scale");
   static constexpr uint32_t SLOT_BYTES = NV * kDqThreads * VB + NS * kDqThreads * 4;
   static_assert(NV >= 1 && NV <= 2, "dequant geometry");
   static_assert(!BWD || (64 * COLS / (VB * 2)) % kDqThreads == 0, "dequant geometry");
@@ -126,10 +139,13 @@ struct Cfg {
   static constexpr int BSTAGES = PM ? WS_GEMM_BSTAGES + 1 : WS_GEMM_BSTAGES;
 #endif
   // per-thread ring of fetched codes (cp.async), CSTAGES steps deep
-  static constexpr int CSTAGES = WS_GEMM_CSTAGES;
   static constexpr uint32_t CODE_BYTES = WB ? 0u : DqGeo<BWD, BN, PAIR>::SLOT_BYTES;
+  static constexpr int CSTAGES_RAW =
+      (int)((WS_GEMM_CODE_RING_KB * 1024u) / DqGeo<BWD, BN, PAIR>::SLOT_BYTES);
+  static constexpr int CSTAGES = CSTAGES_RAW < 4 ? 4 : (CSTAGES_RAW > 16 ? 16 : CSTAGES_RAW);
   static constexpr int STAGES_RAW =
-      (int)((220u * 1024u - BSTAGES * B_BYTES - CSTAGES * CODE_BYTES - 1024u) / A_BYTES);
+      (int)((WS_GEMM_SMEM_BUDGET_KB * 1024u - BSTAGES * B_BYTES - CSTAGES * CODE_BYTES - 1024u) /
+            A_BYTES);
   static constexpr int STAGES = STAGES_RAW > WS_GEMM_STAGES_MAX ? WS_GEMM_STAGES_MAX : STAGES_RAW;
   // one accumulator set
   static constexpr uint32_t ACC_COLS = UM * BN;
@@ -250,7 +266,7 @@ WS_DEVINL uint4 dq8(uint32_t w, const Nf4Table& t) {
 // Code words and block scales of one dequant thread for one step.
 struct Frag {
   uint32_t w[8];
-  float a[2];
+  float a[1];
 };
 
 // Asynchronous 16- / 8- / 4-byte global -> shared copies; src_bytes = 0
@@ -315,8 +331,8 @@ WS_DEVINL void fetch_codes(uint32_t slot, const uint8_t* codes, const float* abs
       const int64_t rr = in ? r : 0, cl = in ? col : 0;
       cp_async_v<D::VB>(slot + (uint32_t)((it * kDqThreads + t) * D::VB),
                         codes + rr * kb + cl / 2, in);
-      cp_async4(sc + (uint32_t)((it * kDqThreads + t) * 4), absmax + (cl / 64) * wN + rr,
-                in ? 4u : 0u);
+      if (it == 0)
+        cp_async4(sc + (uint32_t)(t * 4), absmax + (cl / 64) * wN + rr, in ? 4u : 0u);
     }
   }
 }
@@ -370,13 +386,13 @@ WS_DEVINL void dequant_bwd(const Frag& f, uint8_t* Bt, int rank, int t) {
   using D = DqGeo<true, BN, PAIR>;
   constexpr uint32_t SBO = ((PAIR == 2 ? BN / 2 : BN) / 64) * 1024;  // this CTA's buffer width
   constexpr int WPI = D::VB / 4;  // code words per item: 8 weights each
-  constexpr int SEGS = D::COLS / (2 * D::VB);
+  constexpr int SEGS = D::SEGS;
+  const Nf4Table tb = make_table(f.a[0]);  // the thread's items share one block scale
 #pragma unroll
   for (int it = 0; it < D::NV; ++it) {
     const int item = t * D::NV + it;
     const int c = item / SEGS, seg = item % SEGS;
     const int j0 = (PAIR == 1 ? rank * D::COLS : 0) + seg * 2 * D::VB;  // first buffer column
-    const Nf4Table tb = make_table(f.a[it]);
     const uint32_t grp = (uint32_t)((c >> 3) * SBO + (j0 / 64) * 1024 + (c & 7) * 128);
 #pragma unroll
     for (int q = 0; q < WPI; ++q) {
