@@ -35,5 +35,7 @@ from .binding import (  # noqa: F401
     silu_mul_f64,
     silu_mul_bwd,
     repeat_kv_bwd,
+    attention_fwd,
+    attention_bwd,
     LIN_NAMES,
 )

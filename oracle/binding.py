@@ -71,6 +71,8 @@ def lib():
         L.orc_rmsnorm_bwd_add.argtypes = [i64, i64, P, P, P, P]
         L.orc_silu_mul_bwd.argtypes = [i64, C.c_int, P, P, P, P, P]
         L.orc_repeat_kv_bwd.argtypes = [i64, i64, i64, i64, C.c_int, P, P]
+        L.orc_attention_fwd.argtypes = [i64, i64, i64, i64, i64, P, P, P, P, P]
+        L.orc_attention_bwd.argtypes = [i64, i64, i64, i64, i64, P, P, P, P, P, P, P]
         _lib = L
     return _lib
 
@@ -204,7 +206,7 @@ class _StackCfgC(C.Structure):
     _fields_ = [("M", C.c_int64), ("H", C.c_int64), ("KV", C.c_int64), ("I", C.c_int64),
                 ("head_dim", C.c_int64), ("n_layers", C.c_int), ("r", C.c_int),
                 ("alpha", C.c_double), ("p", C.c_double), ("eps", C.c_double),
-                ("seed", C.c_uint64), ("round_bf16", C.c_int)]
+                ("seed", C.c_uint64), ("round_bf16", C.c_int), ("attn", C.c_int)]
 
 
 class _StackParamsC(C.Structure):
@@ -225,6 +227,7 @@ class StackCfg:
     eps: float = 1e-6
     seed: int = 0
     round_bf16: bool = True
+    attn: int = 0  # 0: repeat(v) in place of attention; 1: causal attention core
 
     def shapes(self):
         """(N, K) of each linear in a layer, in q,k,v,o,gate,up,down order."""
@@ -251,7 +254,8 @@ def stack_fwd_bwd(cfg: StackCfg, step: int, Wq, A, B, h0, backward=True, microba
     prm = _StackParamsC(C.cast(arrW, C.c_void_p), C.cast(arrA, C.c_void_p),
                         C.cast(arrB, C.c_void_p))
     cc = _StackCfgC(cfg.M, cfg.H, cfg.KV, cfg.I, cfg.head_dim, cfg.n_layers, cfg.r,
-                    cfg.alpha, cfg.p, cfg.eps, cfg.seed, 1 if cfg.round_bf16 else 0)
+                    cfg.alpha, cfg.p, cfg.eps, cfg.seed, 1 if cfg.round_bf16 else 0,
+                    int(cfg.attn))
     loss = C.c_double(0.0)
     h_out = np.empty((cfg.M, cfg.H), np.float64)
     if backward:
@@ -266,6 +270,31 @@ def stack_fwd_bwd(cfg: StackCfg, step: int, Wq, A, B, h0, backward=True, microba
     L.orc_stack_fwd_bwd_mb(C.byref(cc), step, microbatch, n_micro, C.byref(prm), _p(h0),
                            C.byref(loss), _p(h_out), pdA, pdB)
     return loss.value, h_out, dA, dB
+
+
+def attention_fwd(q, k, v, n_seq, head_dim, want_lse=False):
+    """Causal attention with grouped kv heads.  q [M, nh*d], k/v [M, nkv*d]
+    (float, M = n_seq * S) -> o [M, nh*d] (and lse [nh, M]), in double."""
+    q, k, v = _c(q, np.float64), _c(k, np.float64), _c(v, np.float64)
+    M = q.shape[0]
+    nh, nkv = q.shape[1] // head_dim, k.shape[1] // head_dim
+    assert M % n_seq == 0 and k.shape == v.shape and k.shape[0] == M
+    o = np.empty_like(q)
+    lse = np.empty((nh, M), np.float64)
+    lib().orc_attention_fwd(n_seq, M // n_seq, nh, nkv, head_dim, _p(q), _p(k), _p(v), _p(o),
+                            _p(lse))
+    return (o, lse) if want_lse else o
+
+
+def attention_bwd(q, k, v, dO, n_seq, head_dim):
+    """Gradients (dq, dk, dv) of the causal attention for upstream dO, in double."""
+    q, k, v, dO = (_c(a, np.float64) for a in (q, k, v, dO))
+    M = q.shape[0]
+    nh, nkv = q.shape[1] // head_dim, k.shape[1] // head_dim
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    lib().orc_attention_bwd(n_seq, M // n_seq, nh, nkv, head_dim, _p(q), _p(k), _p(v), _p(dO),
+                            _p(dq), _p(dk), _p(dv))
+    return dq, dk, dv
 
 
 def rmsnorm_bf16(x, eps=1e-6):

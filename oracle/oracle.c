@@ -441,8 +441,114 @@ static double repeat_kv_bwd1(const double* dvr_row, int64_t rep, int64_t hd, int
   return sum;
 }
 
+/* ---- causal attention core ------------------------------------------------ */
+/* Scaled dot-product attention of Vaswani et al. (2017), causal, with grouped
+ * kv heads (Ainslie et al. 2023): query head h reads kv head h / (nh / nkv).
+ * Tokens are n_seq sequences of S, token t = b*S + i; q and o are [M, nh*d],
+ * k and v are [M, nkv*d] (M = n_seq*S), row-major.  For query i of sequence
+ * b and head h, over the keys j <= i of the same sequence:
+ *   s_j = (q_i . k_j) / sqrt(d),  p_j = exp(s_j - lse_i),
+ *   lse_i = log sum_{j<=i} exp(s_j),  o_i = sum_j p_j v_j.
+ * lse is stored [nh, M]. */
+static void attn_row_probs(int64_t S, int64_t nh, int64_t nkv, int64_t d, int64_t b, int64_t h,
+                           int64_t i, const double* q, const double* k, double* p,
+                           double* lse_out) {
+  const int64_t g = h / (nh / nkv);
+  const double sc = 1.0 / sqrt((double)d);
+  const double* qi = q + ((b * S + i) * nh + h) * d;
+  double mx = -INFINITY;
+  for (int64_t j = 0; j <= i; ++j) {
+    const double* kj = k + ((b * S + j) * nkv + g) * d;
+    double s = 0.0;
+    for (int64_t t = 0; t < d; ++t) s += qi[t] * kj[t];
+    p[j] = s * sc;
+    if (p[j] > mx) mx = p[j];
+  }
+  double l = 0.0;
+  for (int64_t j = 0; j <= i; ++j) l += exp(p[j] - mx);
+  const double lse = mx + log(l);
+  for (int64_t j = 0; j <= i; ++j) p[j] = exp(p[j] - lse);
+  if (lse_out) *lse_out = lse;
+}
+
+void orc_attention_fwd(int64_t n_seq, int64_t S, int64_t nh, int64_t nkv, int64_t d,
+                       const double* q, const double* k, const double* v, double* o,
+                       double* lse) {
+  const int64_t M = n_seq * S;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+  for (int64_t b = 0; b < n_seq; ++b)
+    for (int64_t h = 0; h < nh; ++h) {
+      const int64_t g = h / (nh / nkv);
+      double* p = (double*)malloc(sizeof(double) * (size_t)S);
+      for (int64_t i = 0; i < S; ++i) {
+        double l;
+        attn_row_probs(S, nh, nkv, d, b, h, i, q, k, p, &l);
+        if (lse) lse[h * M + b * S + i] = l;
+        double* oi = o + ((b * S + i) * nh + h) * d;
+        for (int64_t t = 0; t < d; ++t) {
+          double acc = 0.0;
+          for (int64_t j = 0; j <= i; ++j) acc += p[j] * v[((b * S + j) * nkv + g) * d + t];
+          oi[t] = acc;
+        }
+      }
+      free(p);
+    }
+}
+
+/* Gradients of the attention above for the upstream gradient dO [M, nh*d],
+ * by the chain rule through the softmax:
+ *   dv_j += p_ij dO_i,  dp_ij = dO_i . v_j,  D_i = sum_j p_ij dp_ij,
+ *   ds_ij = p_ij (dp_ij - D_i),
+ *   dq_i = sum_j ds_ij k_j / sqrt(d),  dk_j += ds_ij q_i / sqrt(d).
+ * dk and dv sum over the query heads that share a kv head.  dq, dk, dv are
+ * overwritten. */
+void orc_attention_bwd(int64_t n_seq, int64_t S, int64_t nh, int64_t nkv, int64_t d,
+                       const double* q, const double* k, const double* v, const double* dO,
+                       double* dq, double* dk, double* dv) {
+  const int64_t M = n_seq * S, rep = nh / nkv;
+  const double sc = 1.0 / sqrt((double)d);
+  memset(dq, 0, sizeof(double) * (size_t)(M * nh * d));
+  memset(dk, 0, sizeof(double) * (size_t)(M * nkv * d));
+  memset(dv, 0, sizeof(double) * (size_t)(M * nkv * d));
+  /* one (sequence, kv head) per task: its dk, dv rows have one writer */
+#pragma omp parallel for collapse(2) schedule(dynamic)
+  for (int64_t b = 0; b < n_seq; ++b)
+    for (int64_t g = 0; g < nkv; ++g) {
+      double* p = (double*)malloc(sizeof(double) * (size_t)S);
+      double* dp = (double*)malloc(sizeof(double) * (size_t)S);
+      for (int64_t h = g * rep; h < (g + 1) * rep; ++h)
+        for (int64_t i = 0; i < S; ++i) {
+          attn_row_probs(S, nh, nkv, d, b, h, i, q, k, p, NULL);
+          const double* dOi = dO + ((b * S + i) * nh + h) * d;
+          const double* qi = q + ((b * S + i) * nh + h) * d;
+          double D = 0.0;
+          for (int64_t j = 0; j <= i; ++j) {
+            const double* vj = v + ((b * S + j) * nkv + g) * d;
+            double s = 0.0;
+            for (int64_t t = 0; t < d; ++t) s += dOi[t] * vj[t];
+            dp[j] = s;
+            D += p[j] * s;
+          }
+          double* dqi = dq + ((b * S + i) * nh + h) * d;
+          for (int64_t j = 0; j <= i; ++j) {
+            const double ds = p[j] * (dp[j] - D);
+            const double* kj = k + ((b * S + j) * nkv + g) * d;
+            double* dkj = dk + ((b * S + j) * nkv + g) * d;
+            double* dvj = dv + ((b * S + j) * nkv + g) * d;
+            for (int64_t t = 0; t < d; ++t) {
+              dqi[t] += sc * ds * kj[t];
+              dkj[t] += sc * ds * qi[t];
+              dvj[t] += p[j] * dOi[t];
+            }
+          }
+        }
+      free(p);
+      free(dp);
+    }
+}
+
 typedef struct {
-  double *h, *a, *rstd1, *v, *vr, *h1, *b, *rstd2, *g, *u, *act;
+  double *h, *a, *rstd1, *q, *k, *v, *vr, *h1, *b, *rstd2, *g, *u, *act;
   uint32_t* mask[ORC_NLIN];
 } layer_saved;
 
@@ -482,26 +588,33 @@ void orc_stack_fwd_bwd_mb(const orc_stack_cfg* c, uint32_t step, uint32_t microb
     s->a = (double*)malloc(sizeof(double) * M * H);
     s->rstd1 = (double*)malloc(sizeof(double) * M);
     rmsnorm_fwd(c, H, h, s->a, s->rstd1);
-    /* q and k feed only the attention core that this construction replaces;
-     * they are computed for fidelity and then dropped. */
-    double* q = (double*)malloc(sizeof(double) * M * H);
+    /* q and k: with the attention core they are kept (bf16, as stored);
+     * with the repeat(v) stand-in nothing reads them, so they are computed
+     * for fidelity and dropped. */
+    s->q = (double*)malloc(sizeof(double) * M * H);
     lin_fwd(c, H, H, s->a, prm->Wq[base + ORC_Q], prm->A[base + ORC_Q],
-            prm->B[base + ORC_Q], s->mask[ORC_Q], scale, q);
-    free(q);
-    double* kk = (double*)malloc(sizeof(double) * M * KV);
+            prm->B[base + ORC_Q], s->mask[ORC_Q], scale, s->q);
+    s->k = (double*)malloc(sizeof(double) * M * KV);
     lin_fwd(c, KV, H, s->a, prm->Wq[base + ORC_K], prm->A[base + ORC_K],
-            prm->B[base + ORC_K], s->mask[ORC_K], scale, kk);
-    free(kk);
+            prm->B[base + ORC_K], s->mask[ORC_K], scale, s->k);
+    for (int64_t i = 0; i < M * H; ++i) s->q[i] = rb(c, s->q[i]);
+    for (int64_t i = 0; i < M * KV; ++i) s->k[i] = rb(c, s->k[i]);
     s->v = (double*)malloc(sizeof(double) * M * KV);
     lin_fwd(c, KV, H, s->a, prm->Wq[base + ORC_V], prm->A[base + ORC_V],
             prm->B[base + ORC_V], s->mask[ORC_V], scale, s->v);
     for (int64_t i = 0; i < M * KV; ++i) s->v[i] = rb(c, s->v[i]);
-    /* repeat_kv: query head hh reads kv head hh / rep */
     s->vr = (double*)malloc(sizeof(double) * M * H);
-    for (int64_t m = 0; m < M; ++m)
-      for (int64_t hh = 0; hh < H / hd; ++hh)
-        for (int64_t d = 0; d < hd; ++d)
-          s->vr[m * H + hh * hd + d] = s->v[m * KV + (hh / rep) * hd + d];
+    if (c->attn) {
+      /* causal attention over the M tokens (one sequence), output stored bf16 */
+      orc_attention_fwd(1, M, H / hd, KV / hd, hd, s->q, s->k, s->v, s->vr, NULL);
+      for (int64_t i = 0; i < M * H; ++i) s->vr[i] = rb(c, s->vr[i]);
+    } else {
+      /* repeat_kv: query head hh reads kv head hh / rep */
+      for (int64_t m = 0; m < M; ++m)
+        for (int64_t hh = 0; hh < H / hd; ++hh)
+          for (int64_t d = 0; d < hd; ++d)
+            s->vr[m * H + hh * hd + d] = s->v[m * KV + (hh / rep) * hd + d];
+    }
     double* o = scratch;
     lin_fwd(c, H, H, s->vr, prm->Wq[base + ORC_O], prm->A[base + ORC_O],
             prm->B[base + ORC_O], s->mask[ORC_O], scale, o);
@@ -578,22 +691,49 @@ void orc_stack_fwd_bwd_mb(const orc_stack_cfg* c, uint32_t step, uint32_t microb
       lin_bwd(c, H, H, s->vr, prm->Wq[base + ORC_O], prm->A[base + ORC_O],
               prm->B[base + ORC_O], s->mask[ORC_O], scale, dYb, dvr,
               dA[base + ORC_O], dB[base + ORC_O]);
-      /* repeat_kv backward: sum over the rep query heads of each kv head */
-      double* dv = dYb;
-      for (int64_t m = 0; m < M; ++m)
-        for (int64_t kh = 0; kh < KV / hd; ++kh)
-          for (int64_t d = 0; d < hd; ++d)
-            dv[m * KV + kh * hd + d] = rb(c, repeat_kv_bwd1(dvr + m * H, rep, hd, kh, d));
       double* da = dx2;
       memset(da, 0, sizeof(double) * M * H);
-      lin_bwd(c, KV, H, s->a, prm->Wq[base + ORC_V], prm->A[base + ORC_V],
-              prm->B[base + ORC_V], s->mask[ORC_V], scale, dv, da,
-              dA[base + ORC_V], dB[base + ORC_V]);
-      /* q and k receive no gradient: their outputs are unused */
-      memset(dA[base + ORC_Q], 0, sizeof(double) * c->r * H);
-      memset(dB[base + ORC_Q], 0, sizeof(double) * H * c->r);
-      memset(dA[base + ORC_K], 0, sizeof(double) * c->r * H);
-      memset(dB[base + ORC_K], 0, sizeof(double) * KV * c->r);
+      if (c->attn) {
+        /* attention backward from the bf16-stored upstream gradient; dq, dk,
+         * dv are stored bf16 (GEMM operands) */
+        for (int64_t i = 0; i < M * H; ++i) dvr[i] = rb(c, dvr[i]);
+        double* dq = (double*)malloc(sizeof(double) * M * H);
+        double* dk = (double*)malloc(sizeof(double) * M * KV);
+        double* dv = (double*)malloc(sizeof(double) * M * KV);
+        orc_attention_bwd(1, M, H / hd, KV / hd, hd, s->q, s->k, s->v, dvr, dq, dk, dv);
+        for (int64_t i = 0; i < M * H; ++i) dq[i] = rb(c, dq[i]);
+        for (int64_t i = 0; i < M * KV; ++i) {
+          dk[i] = rb(c, dk[i]);
+          dv[i] = rb(c, dv[i]);
+        }
+        lin_bwd(c, KV, H, s->a, prm->Wq[base + ORC_V], prm->A[base + ORC_V],
+                prm->B[base + ORC_V], s->mask[ORC_V], scale, dv, da,
+                dA[base + ORC_V], dB[base + ORC_V]);
+        lin_bwd(c, KV, H, s->a, prm->Wq[base + ORC_K], prm->A[base + ORC_K],
+                prm->B[base + ORC_K], s->mask[ORC_K], scale, dk, da,
+                dA[base + ORC_K], dB[base + ORC_K]);
+        lin_bwd(c, H, H, s->a, prm->Wq[base + ORC_Q], prm->A[base + ORC_Q],
+                prm->B[base + ORC_Q], s->mask[ORC_Q], scale, dq, da,
+                dA[base + ORC_Q], dB[base + ORC_Q]);
+        free(dq);
+        free(dk);
+        free(dv);
+      } else {
+        /* repeat_kv backward: sum over the rep query heads of each kv head */
+        double* dv = dYb;
+        for (int64_t m = 0; m < M; ++m)
+          for (int64_t kh = 0; kh < KV / hd; ++kh)
+            for (int64_t d = 0; d < hd; ++d)
+              dv[m * KV + kh * hd + d] = rb(c, repeat_kv_bwd1(dvr + m * H, rep, hd, kh, d));
+        lin_bwd(c, KV, H, s->a, prm->Wq[base + ORC_V], prm->A[base + ORC_V],
+                prm->B[base + ORC_V], s->mask[ORC_V], scale, dv, da,
+                dA[base + ORC_V], dB[base + ORC_V]);
+        /* q and k receive no gradient: their outputs are unused */
+        memset(dA[base + ORC_Q], 0, sizeof(double) * c->r * H);
+        memset(dB[base + ORC_Q], 0, sizeof(double) * H * c->r);
+        memset(dA[base + ORC_K], 0, sizeof(double) * c->r * H);
+        memset(dB[base + ORC_K], 0, sizeof(double) * KV * c->r);
+      }
       /* dh = dh1 + RMSNorm1 backward */
       rmsnorm_bwd(c, H, s->h, s->rstd1, da, dh);
     }
@@ -609,6 +749,8 @@ void orc_stack_fwd_bwd_mb(const orc_stack_cfg* c, uint32_t step, uint32_t microb
     free(s->h);
     free(s->a);
     free(s->rstd1);
+    free(s->q);
+    free(s->k);
     free(s->v);
     free(s->vr);
     free(s->h1);

@@ -91,7 +91,20 @@ void orc_lora_bwd(int64_t M, int64_t N, int64_t K, int r,
                   const int64_t* rows, int64_t nrows,
                   double* dX, double* dA, double* dB);
 
-/* ---- Synthetic stack (RMSNorm -> q,k,v -> repeat(v) -> o -> residual;
+/* ---- Causal attention core with grouped kv heads (scaled dot-product
+ * attention; query head h reads kv head h / (nh / nkv)).  n_seq sequences of
+ * S tokens, token t = b*S + i; q, o [M, nh*d]; k, v [M, nkv*d]; M = n_seq*S.
+ *   o_i = sum_{j<=i} p_ij v_j,  p_ij = exp(q_i.k_j / sqrt(d) - lse_i),
+ *   lse_i = log sum_{j<=i} exp(q_i.k_j / sqrt(d))   (lse [nh, M], may be NULL).
+ * The backward overwrites dq, dk, dv with the gradients for upstream dO. */
+void orc_attention_fwd(int64_t n_seq, int64_t S, int64_t nh, int64_t nkv, int64_t d,
+                       const double* q, const double* k, const double* v, double* o,
+                       double* lse);
+void orc_attention_bwd(int64_t n_seq, int64_t S, int64_t nh, int64_t nkv, int64_t d,
+                       const double* q, const double* k, const double* v, const double* dO,
+                       double* dq, double* dk, double* dv);
+
+/* ---- Synthetic stack (RMSNorm -> q,k,v -> repeat(v) or attention -> o -> residual;
  *      RMSNorm -> gate,up -> SiLU(gate)*up -> down -> residual) ---------- */
 typedef struct {
   int64_t M, H, KV, I, head_dim;
@@ -100,6 +113,7 @@ typedef struct {
   double alpha, p, eps;
   uint64_t seed;
   int round_bf16;   /* 1: round to bf16 at the stored-bf16 points; 0: exact */
+  int attn;         /* 0: repeat(v) in place of attention; 1: causal attention core */
 } orc_stack_cfg;
 
 /* Linear ids inside a layer. */
