@@ -286,18 +286,61 @@ ws_status ws_nf4_matmul_noalloc(const ws_nf4* W, const uint16_t* act, int64_t M,
                                 int32_t transpose_w, void* out, int32_t out_dtype,
                                 ws_stream_t stream);
 
+/* ---- attention core ---------------------------------------------------------- */
+/* The attention of the trained model, which streaming leaves unchanged (the
+ * research page "Poros", the paragraph saying the learning problem itself is
+ * unchanged).  The pages print no formula; this is scaled dot-product
+ * attention (Vaswani et al., 2017), causal, with grouped kv heads (Ainslie et
+ * al., 2023): query head h reads kv head h / (n_heads / n_kv_heads).
+ * Tokens are n_seq sequences of seq_len, token t = b*seq_len + i, M =
+ * n_seq*seq_len.  All pointers are device memory, 16-byte aligned:
+ *   q [M, n_heads*head_dim], k and v [M, n_kv_heads*head_dim]   bf16
+ *   o [M, n_heads*head_dim] bf16 and, if o32 != NULL, the same in fp32
+ *   lse [n_heads, M] fp32: ln sum_{j<=i} exp(q_i.k_j / sqrt(head_dim))
+ *   o_i = sum_{j<=i} exp(q_i.k_j / sqrt(head_dim) - lse_i) v_j.
+ * head_dim is 64 or 128; n_heads a multiple of n_kv_heads; seq_len >= 1.
+ * The probabilities enter the tensor-core products as two bf16 parts (about
+ * 16 significant bits); every sum has a fixed order, so results repeat bit
+ * for bit.  WS_ERR_SHAPE / WS_ERR_ALIGN / WS_ERR_INVALID on bad arguments,
+ * before anything is launched. */
+ws_status ws_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           int32_t n_seq, int32_t seq_len, int32_t n_heads, int32_t n_kv_heads,
+                           int32_t head_dim, uint16_t* o, float* o32, float* lse,
+                           ws_stream_t stream);
+/* Workspace of ws_attention_bwd for M = n_seq*seq_len tokens. */
+ws_status ws_attention_workspace_size(int64_t M, int32_t n_heads, int32_t head_dim, size_t* bytes);
+/* Gradients for the upstream gradient dO [M, n_heads*head_dim] bf16, given the
+ * forward's o32 and lse: dq [M, n_heads*head_dim], dk and dv [M,
+ * n_kv_heads*head_dim], bf16 (overwritten).  With p the probabilities,
+ * D_i = dO_i . o_i, ds_ij = p_ij (dO_i . v_j - D_i): dq_i = sum_j ds_ij k_j /
+ * sqrt(head_dim), dk_j = sum_i ds_ij q_i / sqrt(head_dim), dv_j = sum_i p_ij
+ * dO_i, dk and dv summed over the query heads sharing the kv head (in head
+ * order).  workspace: device, ws_attention_workspace_size bytes. */
+ws_status ws_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const float* o32, const float* lse, const uint16_t* dO,
+                           int32_t n_seq, int32_t seq_len, int32_t n_heads, int32_t n_kv_heads,
+                           int32_t head_dim, uint16_t* dq, uint16_t* dk, uint16_t* dv,
+                           void* workspace, size_t workspace_bytes, ws_stream_t stream);
+
 /* ---- the synthetic stack ----------------------------------------------------- */
-/* The transformer layers the method trains, with the attention core replaced
- * ("Poros", learning-problem paragraph: the layer computation is that of a
- * resident run).  One layer: h -> RMSNorm -> q,k,v (NF4-LoRA) -> v repeated across the
- * H/head_dim query heads (head h reads kv head h / (H/KV)) in place of the
- * attention core -> o -> residual; -> RMSNorm -> gate, up -> SiLU(gate)*up
- * -> down -> residual.  RMSNorm has unit gain and eps `eps`, computed in
- * fp32; the residual stream is fp32; linear inputs and outputs are bf16;
- * gradients that enter a linear as dY are bf16, all other activation
- * gradients are fp32.  q and k feed only the replaced attention core, so
- * their adapters receive exactly zero gradient.  loss = 0.5 mean(h_L^2). */
+/* The transformer layers the method trains ("Poros", learning-problem
+ * paragraph: the layer computation is that of a resident run).  One layer:
+ * h -> RMSNorm -> q,k,v (NF4-LoRA) -> attention -> o -> residual; -> RMSNorm
+ * -> gate, up -> SiLU(gate)*up -> down -> residual.  The attention is
+ *   attn = WS_ATTN_REPEAT_V: v repeated across the H/head_dim query heads
+ *          (head h reads kv head h / (H/KV)) in place of the attention core;
+ *          q and k then feed nothing, so their adapters receive exactly zero
+ *          gradient;
+ *   attn = WS_ATTN_CAUSAL: the causal attention core above (ws_attention_fwd)
+ *          over the M tokens as one sequence, with H/head_dim query heads
+ *          and KV/head_dim kv heads (head_dim 64 or 128).
+ * RMSNorm has unit gain and eps `eps`, computed in fp32; the residual stream
+ * is fp32; linear inputs and outputs are bf16; gradients that enter a linear
+ * as dY are bf16 (with the attention core also the o projection's input
+ * gradient dO, and dq, dk, dv), all other activation gradients are fp32.
+ * loss = 0.5 mean(h_L^2). */
 enum { WS_BASE_NF4 = 0, WS_BASE_BF16 = 1 };
+enum { WS_ATTN_REPEAT_V = 0, WS_ATTN_CAUSAL = 1 };
 typedef struct {
   int64_t M, H, KV, I, head_dim;
   int32_t n_layers;
@@ -309,6 +352,7 @@ typedef struct {
   int32_t base;  /* the frozen base's format: WS_BASE_NF4, or WS_BASE_BF16
                     (the pages' bf16_bitwise mode: same engine and GEMM, the
                     weights stream as bf16, 2 bytes per weight) */
+  int32_t attn;  /* WS_ATTN_REPEAT_V or WS_ATTN_CAUSAL */
 } ws_stack_cfg;
 
 /* Sizes of the stack's buffers for a given block size (layers per block):
@@ -332,13 +376,17 @@ ws_status ws_stack_weight_offset(const ws_stack_cfg* cfg, int32_t layer_in_block
 /* Activations one layer keeps for its backward (the `saved` areas of
  * ws_block_forward / ws_stack_buffers, one slot of saved_bytes_layer per
  * layer): the layer input h [M,H] fp32, a = RMSNorm(h) [M,H] bf16, rstd1 [M]
- * fp32, v [M,KV] bf16, vr = repeat(v) [M,H] bf16, h1 = h + o [M,H] fp32,
- * b = RMSNorm(h1) [M,H] bf16, rstd2 [M] fp32, gate and up outputs [M,I]
- * bf16, act = SiLU(gate)*up [M,I] bf16, and per linear its U [M,16] fp32 and
- * dropout mask [M,K/32] uint32. */
+ * fp32, v [M,KV] bf16, vr = the attention output (repeat(v), or the
+ * attention core's o) [M,H] bf16, h1 = h + o [M,H] fp32, b = RMSNorm(h1)
+ * [M,H] bf16, rstd2 [M] fp32, gate and up outputs [M,I] bf16, act =
+ * SiLU(gate)*up [M,I] bf16, and per linear its U [M,16] fp32 and dropout
+ * mask [M,K/32] uint32.  With the attention core also q [M,H] and k [M,KV]
+ * bf16, the attention output in fp32 [M,H] and its log-sum-exp [H/head_dim,
+ * M] fp32 (zero bytes otherwise). */
 enum { WS_SV_H = 0, WS_SV_A = 1, WS_SV_RSTD1 = 2, WS_SV_V = 3, WS_SV_VR = 4, WS_SV_H1 = 5,
        WS_SV_B = 6, WS_SV_RSTD2 = 7, WS_SV_GATE = 8, WS_SV_UP = 9, WS_SV_ACT = 10,
-       WS_SV_LORA_U = 11, WS_SV_MASK = 12 };
+       WS_SV_LORA_U = 11, WS_SV_MASK = 12, WS_SV_Q = 13, WS_SV_K = 14, WS_SV_O32 = 15,
+       WS_SV_LSE = 16 };
 
 /* Byte offset of field `field` (for WS_SV_LORA_U / WS_SV_MASK: of linear
  * `lin`) inside one layer's saved slot. */
@@ -385,12 +433,19 @@ ws_status ws_stack_param_offset(const ws_stack_cfg* cfg, int32_t layer, int32_t 
  *   WS_WK_DG, WS_WK_DU  bf16 [M,I]  gradients at the gate and up outputs
  *   WS_WK_DB    fp32 [M,H]  gradient at b (sum of the gate and up dX)
  *   WS_WK_DH1   fp32 [M,H]  gradient at h1 (layer output gradient + RMSNorm2 backward)
- *   WS_WK_DVR   fp32 [M,H]  gradient at repeat(v) (the o projection's dX)
+ *   WS_WK_DVR   fp32 [M,H]  gradient at repeat(v) (the o projection's dX;
+ *                           repeat(v) stack only)
  *   WS_WK_DV    bf16 [M,KV] gradient at v (sum over the query heads of each kv head)
- *   WS_WK_DA    fp32 [M,H]  gradient at a (the v projection's dX)
- *   WS_WK_YOUT  bf16 [M,H]  the last forward linear output (the down projection's y) */
+ *   WS_WK_DA    fp32 [M,H]  gradient at a (the v projection's dX, plus the k and q
+ *                           projections' with the attention core)
+ *   WS_WK_YOUT  bf16 [M,H]  the last forward linear output (the down projection's y)
+ *   WS_WK_DO    bf16 [M,H]  gradient at the attention output (the o projection's dX;
+ *                           attention core only)
+ *   WS_WK_DQ    bf16 [M,H]  gradient at q (attention core only)
+ *   WS_WK_DK    bf16 [M,KV] gradient at k (attention core only) */
 enum { WS_WK_Y1 = 0, WS_WK_DACT = 1, WS_WK_DG = 2, WS_WK_DU = 3, WS_WK_DB = 4, WS_WK_DH1 = 5,
-       WS_WK_DVR = 6, WS_WK_DV = 7, WS_WK_DA = 8, WS_WK_YOUT = 9 };
+       WS_WK_DVR = 6, WS_WK_DV = 7, WS_WK_DA = 8, WS_WK_YOUT = 9, WS_WK_DO = 10,
+       WS_WK_DQ = 11, WS_WK_DK = 12 };
 ws_status ws_stack_workspace_offset(const ws_stack_cfg* cfg, int32_t block_layers, int32_t field,
                                     size_t* offset);
 

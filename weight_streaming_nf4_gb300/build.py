@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libwsnf4.so")
-SOURCES = ["nf4_gemm.cu", "lora_small.cu", "stack.cu", "api.cu"]
+SOURCES = ["nf4_gemm.cu", "lora_small.cu", "stack.cu", "api.cu", "attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -96,6 +96,57 @@ ws_status ws_quantize_nf4(const uint16_t* W, int64_t N, int64_t K, uint8_t* code
   return cuda_status(run_quantize_nf4(W, N, K, codes, absmax, (cudaStream_t)stream));
 }
 
+namespace {
+ws_status attn_check(int32_t n_seq, int32_t seq_len, int32_t nh, int32_t nkv, int32_t hd) {
+  if (n_seq < 1 || seq_len < 1 || nh < 1 || nkv < 1) return WS_ERR_SHAPE;
+  if (hd != 64 && hd != 128) return WS_ERR_SHAPE;
+  if (nh % nkv) return WS_ERR_SHAPE;
+  if ((int64_t)n_seq * seq_len >= (1ll << 31)) return WS_ERR_SHAPE;
+  return WS_OK;
+}
+}  // namespace
+
+ws_status ws_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           int32_t n_seq, int32_t seq_len, int32_t n_heads, int32_t n_kv_heads,
+                           int32_t head_dim, uint16_t* o, float* o32, float* lse,
+                           ws_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return WS_ERR_INVALID;
+  const ws_status c = attn_check(n_seq, seq_len, n_heads, n_kv_heads, head_dim);
+  if (c != WS_OK) return c;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (o32 && !aligned16(o32)))
+    return WS_ERR_ALIGN;
+  return cuda_status(run_attn_fwd(q, k, v, n_seq, seq_len, n_heads, n_kv_heads, head_dim, o, o32,
+                                  lse, (cudaStream_t)stream));
+}
+
+ws_status ws_attention_workspace_size(int64_t M, int32_t n_heads, int32_t head_dim,
+                                      size_t* bytes) {
+  if (!bytes) return WS_ERR_INVALID;
+  if (M < 1 || n_heads < 1 || (head_dim != 64 && head_dim != 128)) return WS_ERR_SHAPE;
+  *bytes = attn_bwd_workspace_bytes(M, n_heads, head_dim);
+  return WS_OK;
+}
+
+ws_status ws_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const float* o32, const float* lse, const uint16_t* dO,
+                           int32_t n_seq, int32_t seq_len, int32_t n_heads, int32_t n_kv_heads,
+                           int32_t head_dim, uint16_t* dq, uint16_t* dk, uint16_t* dv,
+                           void* workspace, size_t workspace_bytes, ws_stream_t stream) {
+  if (!q || !k || !v || !o32 || !lse || !dO || !dq || !dk || !dv || !workspace)
+    return WS_ERR_INVALID;
+  const ws_status c = attn_check(n_seq, seq_len, n_heads, n_kv_heads, head_dim);
+  if (c != WS_OK) return c;
+  const int64_t M = (int64_t)n_seq * seq_len;
+  if (workspace_bytes < attn_bwd_workspace_bytes(M, n_heads, head_dim)) return WS_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o32) || !aligned16(lse) ||
+      !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(workspace))
+    return WS_ERR_ALIGN;
+  return cuda_status(run_attn_bwd(q, k, v, o32, lse, dO, n_seq, seq_len, n_heads, n_kv_heads,
+                                  head_dim, dq, dk, dv, workspace, (cudaStream_t)stream));
+}
+
 ws_status ws_lora_workspace_size(ws_lora_shape sh, size_t* bytes) {
   if (!bytes) return WS_ERR_INVALID;
   if (sh.M < 1 || sh.N < 64 || sh.K < 64 || sh.N % 64 || sh.K % 64 || sh.r != 16)

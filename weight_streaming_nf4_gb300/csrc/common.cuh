@@ -32,10 +32,11 @@ static_assert((DERR_TIMEOUT_FULL | DERR_TIMEOUT_EMPTY | DERR_TIMEOUT_BFULL | DER
                DERR_TIMEOUT_ACC | DERR_TIMEOUT_DRAIN) == WS_DERR_PIPELINE_MASK,
               "device error bits");
 
-#ifdef WS_GEMM_TU
-// Device error word of the library, owned by the GEMM translation unit (the
-// only one with spin-waits); read and cleared through ws_device_error.
-__device__ uint32_t g_dev_error = 0;
+#if defined(WS_GEMM_TU) || defined(WS_ATTN_TU)
+// Device error word of a translation unit with spin-waits (the GEMM unit and
+// the attention unit each own one); ws_device_error reads and clears both.
+static __device__ uint32_t g_dev_error = 0;
+#define WS_HAS_WAITS 1
 #endif
 
 // Wall-clock limit of one wait (ns).  Pipeline waits in these kernels are
@@ -107,6 +108,9 @@ WS_DEVINL uint32_t keep4(const DropKey& k, uint64_t e0) {
 WS_DEVINL uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+WS_DEVINL void sts128(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
+}
 
 // ---- mbarrier --------------------------------------------------------------------------
 WS_DEVINL void mbar_init(uint64_t* bar, uint32_t count) {
@@ -137,7 +141,7 @@ WS_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-#ifdef WS_GEMM_TU
+#ifdef WS_HAS_WAITS
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (and records `why` in the device error word) on timeout.
 WS_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t why) {
@@ -174,7 +178,7 @@ WS_DEVINL uint32_t ld_acquire_gpu(const uint32_t* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-#ifdef WS_GEMM_TU
+#ifdef WS_HAS_WAITS
 // Bounded wait (acquire) for a cross-CTA word to hold `expect`: polls with a
 // short sleep; after limit_ns of wall-clock time it records `why` in the
 // device error word and returns false.
@@ -322,7 +326,6 @@ WS_DEVINL uint32_t warp_id() { return threadIdx.x >> 5; }
 WS_DEVINL uint32_t lane_id() { return threadIdx.x & 31; }
 WS_DEVINL bool elect_lane0() { return lane_id() == 0; }
 
-// Named barrier among `nthreads` threads (id 1..15; id 0 is __syncthreads).
 // ---- thread-block clusters ------------------------------------------------------------
 WS_DEVINL uint32_t cluster_nctarank() {
   uint32_t r;
@@ -440,7 +443,7 @@ WS_DEVINL void cluster_sync() {
                    : "memory");
 }
 
-#ifdef WS_GEMM_TU
+#ifdef WS_HAS_WAITS
 // Same, acquiring at cluster scope (arrivals released by the other CTA of a pair).
 WS_DEVINL bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t why) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
@@ -469,6 +472,7 @@ WS_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // this grid to complete before touching data).
 WS_DEVINL void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Named barrier among `nthreads` threads (id 1..15; id 0 is __syncthreads).
 WS_DEVINL void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

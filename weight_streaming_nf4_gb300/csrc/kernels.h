@@ -160,6 +160,27 @@ cudaError_t run_wgrad_tc(const float* P, const uint16_t* Q, const uint32_t* mask
                          int64_t C, float s, float* out, int transpose_out, int accumulate,
                          void* ws, cudaStream_t st);
 
+// 2-D bf16 tensor map with the 128-byte swizzle: `inner` contiguous elements,
+// `outer` rows pitch_bytes apart, box {box_inner, box_outer} (nf4_gemm.cu).
+bool tmap_bf16_sw128(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// ---- attention core (attention.cu) ----------------------------------------------------
+// Causal attention with grouped kv heads over n_seq sequences of S tokens:
+// q [M, nh*hd], k, v [M, nkv*hd] bf16 (M = n_seq*S, hd 64 or 128).  Forward:
+// o [M, nh*hd] bf16, o32 (optional) the same in fp32, lse [nh, M] natural
+// log-sum-exp.  Backward from dO [M, nh*hd] bf16, the forward's o32 and lse:
+// dq [M, nh*hd], dk, dv [M, nkv*hd] bf16; ws of attn_bwd_workspace_bytes.
+cudaError_t attn_read_and_clear_dev_error(uint32_t* flags);
+size_t attn_bwd_workspace_bytes(int64_t M, int nh, int head_dim);
+cudaError_t run_attn_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, int n_seq,
+                         int S, int nh, int nkv, int hd, uint16_t* o, float* o32, float* lse,
+                         cudaStream_t st);
+cudaError_t run_attn_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         const float* o32, const float* lse, const uint16_t* dO, int n_seq, int S,
+                         int nh, int nkv, int hd, uint16_t* dq, uint16_t* dk, uint16_t* dv,
+                         void* ws, cudaStream_t st);
+
 // ---- one LoRA linear (linear.cu) --------------------------------------------------------
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t linear_fwd(const NF4View& W, const uint16_t* x, const float* A, const float* B,

@@ -66,7 +66,12 @@ cudaError_t read_and_clear_dev_error(uint32_t* flags) {
     if (e != cudaSuccess) return e;
   }
   const uint32_t zero = 0;
-  return cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(uint32_t));
+  e = cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  uint32_t attn = 0;
+  e = attn_read_and_clear_dev_error(&attn);
+  *flags |= attn;
+  return e;
 }
 
 
@@ -184,10 +189,6 @@ __host__ __device__ inline int64_t sk_cta_of(int64_t i, int64_t I, int64_t G) {
   return ((i + 1) * G + I - 1) / I - 1;
 }
 __host__ __device__ inline int64_t sk_begin(int64_t g, int64_t I, int64_t G) { return g * I / G; }
-
-WS_DEVINL void sts128(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
-}
 
 // Two IEEE fp32 products (round to nearest) in one packed instruction.
 WS_DEVINL void mul2_rn(float x0, float x1, float s, float& r0, float& r1) {
@@ -1797,6 +1798,13 @@ cudaError_t set_smem_attr() {
 }
 
 }  // namespace
+
+bool tmap_bf16_sw128(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+  return encode_fn() && make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, outer,
+                                 pitch_bytes, box_inner, box_outer,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
+}
 
 bool pdl_enabled() {
   static const bool on = [] {

@@ -309,7 +309,9 @@ Shapes shapes_of(const ws_stack_cfg& c) {
 }
 
 struct SavedLayout {
-  size_t h, a, rstd1, v, vr, h1, b, rstd2, g, u, act, U[WS_NLIN], mask[WS_NLIN], total;
+  size_t h, a, rstd1, v, vr, h1, b, rstd2, g, u, act, U[WS_NLIN], mask[WS_NLIN];
+  size_t q, k, o32, lse;  // attention core only (zero bytes with repeat(v))
+  size_t total;
 };
 SavedLayout saved_layout(const ws_stack_cfg& c) {
   const Shapes s = shapes_of(c);
@@ -334,6 +336,11 @@ SavedLayout saved_layout(const ws_stack_cfg& c) {
   L.act = take(M * I * 2);
   for (int i = 0; i < WS_NLIN; ++i) L.U[i] = take(M * 16 * 4);
   for (int i = 0; i < WS_NLIN; ++i) L.mask[i] = take(M * (size_t)(s.K[i] / 32) * 4);
+  const bool at = c.attn == WS_ATTN_CAUSAL;
+  L.q = take(at ? M * H * 2 : 0);
+  L.k = take(at ? M * KV * 2 : 0);
+  L.o32 = take(at ? M * H * 4 : 0);
+  L.lse = take(at ? (H / (size_t)c.head_dim) * M * 4 : 0);
   L.total = o;
   return L;
 }
@@ -381,7 +388,9 @@ ParamLayout param_layout(const ws_stack_cfg& c) {
 }
 
 struct WsLayout {
-  size_t lin, blk, qout, kout, yout, y1, dact, dg, du, db, dh1, dvr, dv, da, lossp, stepw, total;
+  size_t lin, blk, qout, kout, yout, y1, dact, dg, du, db, dh1, dvr, dv, da, lossp, stepw;
+  size_t dob, dq, dk, attn;  // attention core only
+  size_t total;
 };
 WsLayout ws_layout(const ws_stack_cfg& c, int block_layers) {
   const Shapes s = shapes_of(c);
@@ -423,6 +432,11 @@ WsLayout ws_layout(const ws_stack_cfg& c, int block_layers) {
   L.da = take(M * H * 4);
   L.lossp = take(kLossBlocks * 4);
   L.stepw = take(16);
+  const bool at = c.attn == WS_ATTN_CAUSAL;
+  L.dob = take(at ? M * H * 2 : 0);
+  L.dq = take(at ? M * H * 2 : 0);
+  L.dk = take(at ? M * KV * 2 : 0);
+  L.attn = take(at ? attn_bwd_workspace_bytes(c.M, (int)(c.H / c.head_dim), (int)c.head_dim) : 0);
   L.total = o;
   return L;
 }
@@ -521,20 +535,30 @@ cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const
   note_launch();
   (void)launch_pdl(k_rmsnorm_fwd, dim3((unsigned)M), dim3(256), 0, st, h, H, x.c.eps, at<uint16_t>(S, L.a), at<float>(S, L.rstd1));
   WS_TRY(cudaGetLastError());
-  if (with_qk) {
-    // v gets a GEMM of its own, as in a recompute (which skips q and k), so
-    // both passes produce the same v bit for bit
+  const bool attn = x.c.attn == WS_ATTN_CAUSAL;
+  if (with_qk || attn) {
+    // v gets a GEMM of its own, as in a recompute of the repeat(v) stack
+    // (which skips q and k), so both passes produce the same v bit for bit
     const int li[3] = {WS_LIN_Q, WS_LIN_K, WS_LIN_V};
-    uint16_t* outs[3] = {at<uint16_t>(ws, x.WSL.qout), at<uint16_t>(ws, x.WSL.kout),
+    uint16_t* outs[3] = {attn ? at<uint16_t>(S, L.q) : at<uint16_t>(ws, x.WSL.qout),
+                         attn ? at<uint16_t>(S, L.k) : at<uint16_t>(ws, x.WSL.kout),
                          at<uint16_t>(S, L.v)};
     WS_TRY(lin_group(3, 2, li, at<uint16_t>(S, L.a), outs));
   } else {
     WS_TRY(lin(WS_LIN_V, at<uint16_t>(S, L.a), at<uint16_t>(S, L.v)));
   }
-  note_launch();
-  (void)launch_pdl(k_repeat_fwd, dim3(nblk(M * H / 8)), dim3(256), 0, st, at<uint16_t>(S, L.v), (int)M, (int)H, (int)KV,
-                                                (int)x.c.head_dim, at<uint16_t>(S, L.vr));
-  WS_TRY(cudaGetLastError());
+  if (attn) {
+    // causal attention over the M tokens as one sequence
+    const int hd = (int)x.c.head_dim;
+    WS_TRY(run_attn_fwd(at<uint16_t>(S, L.q), at<uint16_t>(S, L.k), at<uint16_t>(S, L.v), 1,
+                        (int)M, (int)(H / hd), (int)(KV / hd), hd, at<uint16_t>(S, L.vr),
+                        at<float>(S, L.o32), at<float>(S, L.lse), st));
+  } else {
+    note_launch();
+    (void)launch_pdl(k_repeat_fwd, dim3(nblk(M * H / 8)), dim3(256), 0, st, at<uint16_t>(S, L.v),
+                     (int)M, (int)H, (int)KV, (int)x.c.head_dim, at<uint16_t>(S, L.vr));
+    WS_TRY(cudaGetLastError());
+  }
   uint16_t* y = at<uint16_t>(ws, x.WSL.yout);
   WS_TRY(lin(WS_LIN_O, at<uint16_t>(S, L.vr), y));
   note_launch();
@@ -631,6 +655,31 @@ cudaError_t layer_bwd(const Ctx& x, const void* block, int lib, int layer, const
   note_launch();
   (void)launch_pdl(k_cast_bf16, dim3(nblk(M * H / 8)), dim3(256), 0, st, (const float*)dh1, M * H, y1);
   WS_TRY(cudaGetLastError());
+  if (x.c.attn == WS_ATTN_CAUSAL) {
+    // o projection's input gradient as bf16 dO, the attention backward, then
+    // the v, k and q projections, their input gradients summed into da
+    const int hd = (int)x.c.head_dim;
+    uint16_t* dob = at<uint16_t>(ws, x.WSL.dob);
+    uint16_t* dq = at<uint16_t>(ws, x.WSL.dq);
+    uint16_t* dk = at<uint16_t>(ws, x.WSL.dk);
+    WS_TRY(linear_bwd(wview(x, block, lib, WS_LIN_O), at<const uint16_t>(S, L.vr),
+                      P + x.PL.A[WS_LIN_O], P + x.PL.B[WS_LIN_O], M, x.scale,
+                      key_of(x, step, layer, WS_LIN_O, mb), at<const float>(S, L.U[WS_LIN_O]),
+                      at<const uint32_t>(S, L.mask[WS_LIN_O]), y1, dob, 0, 0,
+                      Gd + x.PL.A[WS_LIN_O], Gd + x.PL.B[WS_LIN_O], gacc, lws, st));
+    WS_TRY(run_attn_bwd(at<const uint16_t>(S, L.q), at<const uint16_t>(S, L.k),
+                        at<const uint16_t>(S, L.v), at<const float>(S, L.o32),
+                        at<const float>(S, L.lse), dob, 1, (int)M, (int)(H / hd), (int)(KV / hd),
+                        hd, dq, dk, dv, ws + x.WSL.attn, st));
+    WS_TRY(lin(WS_LIN_V, at<const uint16_t>(S, L.a), dv, da, 0));
+    WS_TRY(lin(WS_LIN_K, at<const uint16_t>(S, L.a), dk, da, 1));
+    WS_TRY(lin(WS_LIN_Q, at<const uint16_t>(S, L.a), dq, da, 1));
+    note_launch();
+    (void)launch_pdl(k_rmsnorm_bwd, dim3((unsigned)M), dim3(256), 0, st,
+                     at<const float>(S, L.h), at<const float>(S, L.rstd1), (const float*)da, H,
+                     (const float*)dh1, dh);
+    return cudaGetLastError();
+  }
   WS_TRY(lin(WS_LIN_O, at<const uint16_t>(S, L.vr), y1, dvr, 0));
   note_launch();
   (void)launch_pdl(k_repeat_bwd, dim3(nblk(M * KV / 4)), dim3(256), 0, st, dvr, (int)M, (int)H, (int)KV, (int)x.c.head_dim, dv);
@@ -680,6 +729,9 @@ ws_status stack_check(const ws_stack_cfg* c) {
   if (c->r != 16) return WS_ERR_SHAPE;
   if (!(c->p >= 0.0 && c->p < 1.0)) return WS_ERR_INVALID;
   if (c->base != WS_BASE_NF4 && c->base != WS_BASE_BF16) return WS_ERR_INVALID;
+  if (c->attn != WS_ATTN_REPEAT_V && c->attn != WS_ATTN_CAUSAL) return WS_ERR_INVALID;
+  if (c->attn == WS_ATTN_CAUSAL && ((c->head_dim != 64 && c->head_dim != 128) || c->M >= (1ll << 31)))
+    return WS_ERR_SHAPE;
   if ((double)c->M * (double)c->I >= 17179869184.0) return WS_ERR_SHAPE;
   return WS_OK;
 }
@@ -693,7 +745,8 @@ uint32_t* stack_step_word(const ws_stack_cfg& c, int block_layers, void* ws) {
 }
 bool stack_ws_offset(const ws_stack_cfg& c, int block_layers, int field, size_t* off) {
   const WsLayout L = ws_layout(c, block_layers);
-  const size_t f[] = {L.y1, L.dact, L.dg, L.du, L.db, L.dh1, L.dvr, L.dv, L.da, L.yout};
+  const size_t f[] = {L.y1, L.dact, L.dg, L.du, L.db, L.dh1, L.dvr, L.dv, L.da, L.yout, L.dob,
+                      L.dq, L.dk};
   if (field < 0 || field >= (int)(sizeof(f) / sizeof(f[0]))) return false;
   *off = f[field];
   return true;
@@ -708,6 +761,11 @@ bool stack_saved_offset(const ws_stack_cfg& c, int field, int lin, size_t* off) 
   const size_t f[] = {L.h, L.a, L.rstd1, L.v, L.vr, L.h1, L.b, L.rstd2, L.g, L.u, L.act};
   if (field >= 0 && field <= WS_SV_ACT) {
     *off = f[field];
+    return true;
+  }
+  if (field >= WS_SV_Q && field <= WS_SV_LSE) {
+    const size_t g[] = {L.q, L.k, L.o32, L.lse};
+    *off = g[field - WS_SV_Q];
     return true;
   }
   if (lin < 0 || lin >= WS_NLIN) return false;

@@ -60,12 +60,13 @@ class Bf16W(C.Structure):
 
 
 BASE_NF4, BASE_BF16 = 0, 1
+ATTN_REPEAT_V, ATTN_CAUSAL = 0, 1
 
 
 class StackCfgC(C.Structure):
     _fields_ = [("M", i64), ("H", i64), ("KV", i64), ("I", i64), ("head_dim", i64),
                 ("n_layers", i32), ("r", i32), ("alpha", C.c_float), ("p", C.c_double),
-                ("eps", C.c_float), ("seed", u64), ("base", i32)]
+                ("eps", C.c_float), ("seed", u64), ("base", i32), ("attn", i32)]
 
 
 class StepOptsC(C.Structure):
@@ -105,6 +106,9 @@ _sig("ws_lora_linear_bwd_bf16", [C.POINTER(Bf16W), P, P, P, LoraShape, DropoutKe
 _sig("ws_nf4_matmul_workspace_size", [i64, i64, i64, i32, C.POINTER(C.c_size_t)])
 _sig("ws_nf4_matmul", [C.POINTER(Nf4), P, i64, i32, P, i32, P, C.c_size_t, P])
 _sig("ws_nf4_matmul_noalloc", [C.POINTER(Nf4), P, i64, i32, P, i32, P])
+_sig("ws_attention_fwd", [P, P, P, i32, i32, i32, i32, i32, P, P, P, P])
+_sig("ws_attention_workspace_size", [i64, i32, i32, C.POINTER(C.c_size_t)])
+_sig("ws_attention_bwd", [P, P, P, P, P, P, i32, i32, i32, i32, i32, P, P, P, P, C.c_size_t, P])
 _sig("ws_stack_sizes", [C.POINTER(StackCfgC), i32, C.POINTER(C.c_size_t), C.POINTER(i64),
                         C.POINTER(C.c_size_t), C.POINTER(C.c_size_t)])
 _sig("ws_stack_weight_offset", [C.POINTER(StackCfgC), i32, i32, C.POINTER(C.c_size_t),
@@ -134,7 +138,8 @@ _sig("ws_stack_graph_destroy", [P])
 EXPORTED = ("ws_status_string", "ws_device_error", "ws_selfcheck_bounded_wait", "ws_kernel_launches", "ws_quantize_nf4", "ws_lora_workspace_size",
             "ws_lora_linear_fwd", "ws_lora_linear_bwd", "ws_lora_linear_fwd_bf16",
             "ws_lora_linear_bwd_bf16", "ws_nf4_matmul_workspace_size",
-            "ws_nf4_matmul", "ws_nf4_matmul_noalloc", "ws_stack_sizes",
+            "ws_nf4_matmul", "ws_nf4_matmul_noalloc", "ws_attention_fwd",
+            "ws_attention_workspace_size", "ws_attention_bwd", "ws_stack_sizes",
             "ws_stack_weight_offset", "ws_stack_param_offset", "ws_stack_saved_offset",
             "ws_stack_workspace_offset", "ws_stack_loader_staging_bytes", "ws_stack_put_weight",
             "ws_block_forward", "ws_block_backward_recompute",
@@ -327,6 +332,52 @@ def nf4_matmul_noalloc(W: NF4Weight, act, transpose_w=False, out=None, out_f32=F
     return out
 
 
+# ------------------------------------------------------------------------------ attention
+def attention_fwd(q, k, v, n_seq: int, head_dim: int, o=None, o32=None, lse=None,
+                  want_o32=True, stream=None):
+    """Causal attention with grouped kv heads (ws_attention_fwd).  q [M, nh*hd],
+    k/v [M, nkv*hd] bf16 (M = n_seq * seq_len).  Returns (o bf16, o32 fp32 or
+    None, lse [nh, M])."""
+    M = q.shape[0]
+    nh, nkv = q.shape[1] // head_dim, k.shape[1] // head_dim
+    assert M % n_seq == 0
+    if o is None:
+        o = torch.empty((M, nh * head_dim), dtype=torch.bfloat16, device=q.device)
+    if o32 is None and want_o32:
+        o32 = torch.empty((M, nh * head_dim), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((nh, M), dtype=torch.float32, device=q.device)
+    _check("ws_attention_fwd",
+           _lib.ws_attention_fwd(_ptr(q), _ptr(k), _ptr(v), n_seq, M // n_seq, nh, nkv, head_dim,
+                                 _ptr(o), _ptr(o32), _ptr(lse), _stream(stream)))
+    return o, o32, lse
+
+
+def attention_workspace_size(M: int, n_heads: int, head_dim: int) -> int:
+    n = C.c_size_t(0)
+    _check("ws_attention_workspace_size",
+           _lib.ws_attention_workspace_size(M, n_heads, head_dim, C.byref(n)))
+    return int(n.value)
+
+
+def attention_bwd(q, k, v, o32, lse, dO, n_seq: int, head_dim: int, dq=None, dk=None, dv=None,
+                  workspace=None, stream=None):
+    """Gradients (dq, dk, dv) bf16 of the causal attention (ws_attention_bwd)."""
+    M = q.shape[0]
+    nh, nkv = q.shape[1] // head_dim, k.shape[1] // head_dim
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(attention_workspace_size(M, nh, head_dim), dtype=torch.uint8,
+                                device=q.device)
+    _check("ws_attention_bwd",
+           _lib.ws_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o32), _ptr(lse), _ptr(dO), n_seq,
+                                 M // n_seq, nh, nkv, head_dim, _ptr(dq), _ptr(dk), _ptr(dv),
+                                 _ptr(workspace), workspace.numel(), _stream(stream)))
+    return dq, dk, dv
+
+
 # ------------------------------------------------------------------------------ stack
 @dataclasses.dataclass
 class StackCfg:
@@ -342,10 +393,11 @@ class StackCfg:
     eps: float = 1e-6
     seed: int = 0
     base: int = BASE_NF4
+    attn: int = ATTN_REPEAT_V
 
     def c(self):
         return StackCfgC(self.M, self.H, self.KV, self.I, self.head_dim, self.n_layers, self.r,
-                         self.alpha, self.p, self.eps, self.seed, self.base)
+                         self.alpha, self.p, self.eps, self.seed, self.base, self.attn)
 
     def shapes(self):
         H, KV, I = self.H, self.KV, self.I
@@ -378,7 +430,7 @@ def stack_param_offset(cfg: StackCfg, layer: int, lin: int):
 
 
 SAVED_FIELDS = dict(h=0, a=1, rstd1=2, v=3, vr=4, h1=5, b=6, rstd2=7, gate=8, up=9, act=10,
-                    lora_u=11, mask=12)
+                    lora_u=11, mask=12, q=13, k=14, o32=15, lse=16)
 
 
 def stack_saved_offset(cfg: StackCfg, field: str, lin: int = 0) -> int:
@@ -408,7 +460,8 @@ def stack_put_weight(cfg: StackCfg, block_layers: int, layer: int, lin: int, W, 
                                         0 if staging is None else staging.numel(), _stream(stream)))
 
 
-WORKSPACE_FIELDS = dict(y1=0, dact=1, dg=2, du=3, db=4, dh1=5, dvr=6, dv=7, da=8, yout=9)
+WORKSPACE_FIELDS = dict(y1=0, dact=1, dg=2, du=3, db=4, dh1=5, dvr=6, dv=7, da=8, yout=9, do=10,
+                        dq=11, dk=12)
 
 
 def stack_workspace_offset(cfg: StackCfg, block_layers: int, field: str) -> int:
