@@ -559,6 +559,83 @@ def profile_lora(torch, which):
     print(json.dumps({"profile_lora": which, "M": M, "N": N, "K": K}))
 
 
+def attn_inputs(torch, dev, S, nh, nkv, d):
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242)
+    mk = lambda w: torch.randn(S, w * d, generator=g, device=dev).to(torch.bfloat16)
+    return mk(nh), mk(nkv), mk(nkv), mk(nh)
+
+
+def attention_32b(ops, torch, dev, reps=50):
+    """The attention core at the 32B layer's shape (one sequence of 512 tokens,
+    40 query heads over 8 kv heads, head_dim 128): forward and backward timed
+    with CUDA events over `reps` back-to-back calls each.  Algorithmic flops:
+    the causal half of the two forward products (QK^T, PV) and of the five
+    backward ones (QK^T, dO V^T, dQ, dK, dV)."""
+    S, nh, nkv, d = SHAPE_32B["M"], 40, 8, 128
+    q, k, v, dO = attn_inputs(torch, dev, S, nh, nkv, d)
+    ws = torch.empty(ops.attention_workspace_size(S, nh, d), dtype=torch.uint8, device=dev)
+    o, o32, lse = ops.attention_fwd(q, k, v, 1, d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    st = torch.cuda.current_stream()
+    for _ in range(5):
+        ops.attention_fwd(q, k, v, 1, d, o=o, o32=o32, lse=lse)
+        ops.attention_bwd(q, k, v, o32, lse, dO, 1, d, dq, dk, dv, ws)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    ev[0].record(st)
+    for _ in range(reps):
+        ops.attention_fwd(q, k, v, 1, d, o=o, o32=o32, lse=lse)
+    ev[1].record(st)
+    for _ in range(reps):
+        ops.attention_bwd(q, k, v, o32, lse, dO, 1, d, dq, dk, dv, ws)
+    ev[2].record(st)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    tf = ev[0].elapsed_time(ev[1]) / reps * 1e-3
+    tb = ev[1].elapsed_time(ev[2]) / reps * 1e-3
+    f_fwd = 2 * 2.0 * (S * (S + 1) / 2) * d * nh
+    return {"workload": "causal attention, 1 x 512 tokens, 40 query heads over 8 kv heads, "
+                        "head_dim 128 (the 32B layer)",
+            "fwd_us": tf * 1e6, "bwd_us": tb * 1e6,
+            "fwd_tflops": f_fwd / tf / 1e12, "bwd_tflops": 2.5 * f_fwd / tb / 1e12,
+            "per_step_ms_64_layers": 64 * (tf + tb) * 1e3,
+            "launches": {"fwd": 1, "bwd": 3}}
+
+
+def attention_stack_32b(ops, StackRun, torch, dev, steps):
+    """The resident 32B-shaped step with the causal attention core in place of
+    repeat(v): ms per step (graph replay, median of `steps`)."""
+    cfg = ops.StackCfg(**SHAPE_32B, attn=ops.ATTN_CAUSAL)
+    res, _ = make_runs(ops, StackRun, torch, cfg, dev, streamed=False)
+    st = torch.cuda.Stream(device=dev)
+    g = Graphed(ops, res, 2e-4, st)
+    h0 = torch.randn(cfg.M * cfg.H, device=dev)
+    with torch.cuda.stream(st):
+        _, per = time_steps(torch, None, g, [h0], steps, 3, st)
+    assert ops.device_error() == 0
+    loss = float(res.loss.item())
+    del g, res
+    return {"workload": "qwen2.5-32b-shaped stack, 64 layers, seq 512, causal attention core, "
+                        "resident", "ms_per_step_median": statistics.median(per),
+            "steps": steps, "loss_finite": bool(loss == loss)}
+
+
+def profile_attention(torch):
+    """The attention core at the 32B layer's shape, forward and backward three
+    times (a few MB on the device), for an ncu capture of its kernels."""
+    from weight_streaming_nf4_gb300 import ops
+    dev = torch.device("cuda:0")
+    S, nh, nkv, d = SHAPE_32B["M"], 40, 8, 128
+    q, k, v, dO = attn_inputs(torch, dev, S, nh, nkv, d)
+    for _ in range(3):
+        o, o32, lse = ops.attention_fwd(q, k, v, 1, d)
+        ops.attention_bwd(q, k, v, o32, lse, dO, 1, d)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    print(json.dumps({"profile_attention": "32b layer", "S": S, "nh": nh, "nkv": nkv, "d": d}))
+
+
 def h2d_peak(torch, dev):
     n = 1 << 30
     src = torch.empty(n, dtype=torch.uint8).pin_memory()
@@ -700,6 +777,11 @@ def main():
     ap.add_argument("--profile-link", action="store_true",
                     help="only measure pinned host -> HBM copies (block-sized, pieces, beside a "
                          "matmul, 20 s back to back) and print their rate distributions")
+    ap.add_argument("--no-attn", action="store_true",
+                    help="skip the attention-core measurements (kernels and 32B resident step)")
+    ap.add_argument("--profile-attention", action="store_true",
+                    help="only run the attention core fwd + bwd three times at the 32B layer's "
+                         "shape; for an ncu capture of its kernels")
     ap.add_argument("--profile-gemm", choices=["gate", "down", "o"], default=None,
                     help="only launch the dequant GEMM (forward + input gradient) twice on one "
                          "32B linear shape at M=512; for an ncu capture of that kernel")
@@ -724,6 +806,9 @@ def main():
         return
     if args.profile_link:
         profile_link(torch)
+        return
+    if args.profile_attention:
+        profile_attention(torch)
         return
     dist = None
     if world > 1:
@@ -771,6 +856,8 @@ def main():
         extra["streaming"]["s_per_step_resident_eager"] = t_eager / 2
         if not args.quick:
             extra["linear_7b"] = {f"M{mm}": linear_7b(ops, torch, dev, mm) for mm in (512, 2048)}
+        if not args.no_attn:
+            extra["attention_32b"] = attention_32b(ops, torch, dev)
         if world == 1 and not args.no_cpu_baseline:
             run, cflops, cores, _ = oracle_sample(256, H, cfg.KV, cfg.I)
             tc = run()
@@ -799,6 +886,9 @@ def main():
     # ---- the 72B-shaped stack, streamed and resident (one GPU only)
     if rank == 0:
         del m, res
+    if rank == 0 and world == 1 and not args.quick and not args.no_attn:
+        out["attention_32b"]["stack_resident"] = attention_stack_32b(
+            ops, StackRun, torch, dev, min(max(args.steps, 3), 10))
     if rank == 0 and world == 1 and not args.quick and not args.no_72b:
         release_host_cache(torch)
         cfg72 = ops.StackCfg(**SHAPE_72B)
