@@ -276,12 +276,14 @@ size_t linear_group_workspace_bytes(int64_t M, int ng, const int64_t* N, int64_t
 }
 
 // One LoRA-down launch for all ng linears (ng dropout masks of the same x;
-// each linear's U, bits and split factor are the same as from its own
-// launch), then one GEMM over the concatenated output columns of the first
-// ng_gemm linears and one GEMM per remaining linear (whose result then
-// equals a lone forward of that linear bit for bit).  A width that is not a
-// multiple of the grouped plan's tile width falls back to one GEMM per
-// linear.
+// the bits are those of each linear's own key, U is summed in k-chunks sized
+// for the whole launch, so it can differ in the last bits from a launch of
+// that linear alone), then one GEMM over the concatenated output columns of
+// the first ng_gemm linears and one GEMM per remaining linear.  A width that
+// is not a multiple of the grouped plan's tile width falls back to one GEMM
+// per linear.  y[g] == NULL skips linear g's GEMM (its U and bits are still
+// produced), so a pass that needs only some outputs of a group reproduces
+// them bit for bit; the grouped GEMM runs only if all its y are given.
 cudaError_t linear_fwd_group(int ng, int ng_gemm, const NF4View* W, const uint16_t* x, const float* const* A,
                              const float* const* B, int64_t M, float scale, const DropKeyHost* keys,
                              uint16_t* const* y, float* const* U, uint32_t* const* mask, void* ws,
@@ -312,7 +314,14 @@ cudaError_t linear_fwd_group(int ng, int ng_gemm, const NF4View* W, const uint16
   cudaError_t e = run_skinny_tc_group(x, ng, A, M, K, dk, mb, parts, U, exts, st);
   if (e != cudaSuccess) return e;
   int first_single = 0;
-  if (ng_gemm > 1) {
+  bool all_y = true, no_y = true;
+  for (int g = 0; g < ng_gemm; ++g) {
+    all_y = all_y && y[g] != nullptr;
+    no_y = no_y && y[g] == nullptr;
+  }
+  if (ng_gemm > 1 && !all_y && !no_y) return cudaErrorInvalidValue;
+  if (ng_gemm > 1 && no_y) first_single = ng_gemm;
+  if (ng_gemm > 1 && all_y) {
     int64_t Ng = 0;
     for (int g = 0; g < ng_gemm; ++g) Ng += N[g];
     const GemmPlan p = plan_gemm(false, M, Ng, K);
@@ -325,8 +334,9 @@ cudaError_t linear_fwd_group(int ng, int ng_gemm, const NF4View* W, const uint16
     }
   }
   for (int g = first_single; g < ng && e == cudaSuccess; ++g)
-    e = run_nf4_gemm(plan_gemm(false, M, N[g], K), W[g], x, M, exts[g], B[g], scale, nullptr, y[g],
-                     0, 0, split, st);
+    if (y[g])
+      e = run_nf4_gemm(plan_gemm(false, M, N[g], K), W[g], x, M, exts[g], B[g], scale, nullptr,
+                       y[g], 0, 0, split, st);
   return e;
 }
 

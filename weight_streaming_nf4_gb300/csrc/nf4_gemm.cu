@@ -2222,10 +2222,12 @@ cudaError_t run_wait_selfcheck(uint32_t limit_us, cudaStream_t st) {
 }
 
 // ------------------------------------------------------------------------ skinny products (host)
-int skinny_tc_chunks(int64_t M, int64_t K) {
+// k-chunks per 128-row block: the whole launch (ng groups) fits one wave of
+// one CTA per SM, so no CTA waits for another's slot.
+int skinny_tc_chunks(int64_t M, int64_t K, int ng = 1) {
   const int64_t atoms = (M + 127) / 128;
   const int64_t steps = K / 64;
-  int64_t ch = device_sm_count() / (atoms > 0 ? atoms : 1);
+  int64_t ch = device_sm_count() / ((atoms > 0 ? atoms : 1) * (ng > 0 ? ng : 1));
   if (ch > steps) ch = steps;
   if (ch < 1) ch = 1;
   const int64_t spc = (steps + ch - 1) / ch;
@@ -2296,7 +2298,7 @@ cudaError_t skinny_launch(const uint16_t* const* X, int ng, const float* const* 
   if (!encode_fn()) return cudaErrorNotSupported;
   if (K % 64 != 0 || M < 1 || ng < 1 || ng > kMaxGroups) return cudaErrorInvalidValue;
   const int64_t atoms = (M + 127) / 128;
-  const int chunks = skinny_tc_chunks(M, K);
+  const int chunks = skinny_tc_chunks(M, K, ng);
   const int64_t steps = K / 64;
   const int spc = (int)((steps + chunks - 1) / chunks);
   uint32_t* counters = nullptr;

@@ -536,16 +536,17 @@ cudaError_t layer_fwd(const Ctx& x, const void* block, int lib, int layer, const
   (void)launch_pdl(k_rmsnorm_fwd, dim3((unsigned)M), dim3(256), 0, st, h, H, x.c.eps, at<uint16_t>(S, L.a), at<float>(S, L.rstd1));
   WS_TRY(cudaGetLastError());
   const bool attn = x.c.attn == WS_ATTN_CAUSAL;
-  if (with_qk || attn) {
-    // v gets a GEMM of its own, as in a recompute of the repeat(v) stack
-    // (which skips q and k), so both passes produce the same v bit for bit
+  {
+    // q, k, v share one LoRA-down launch and q + k one GEMM; v gets a GEMM
+    // of its own.  A recompute of the repeat(v) stack needs only v: it runs
+    // the same LoRA-down launch (so v's U is the forward's bit for bit) and
+    // v's GEMM alone.
+    const bool qk = with_qk || attn;
     const int li[3] = {WS_LIN_Q, WS_LIN_K, WS_LIN_V};
-    uint16_t* outs[3] = {attn ? at<uint16_t>(S, L.q) : at<uint16_t>(ws, x.WSL.qout),
-                         attn ? at<uint16_t>(S, L.k) : at<uint16_t>(ws, x.WSL.kout),
+    uint16_t* outs[3] = {qk ? (attn ? at<uint16_t>(S, L.q) : at<uint16_t>(ws, x.WSL.qout)) : nullptr,
+                         qk ? (attn ? at<uint16_t>(S, L.k) : at<uint16_t>(ws, x.WSL.kout)) : nullptr,
                          at<uint16_t>(S, L.v)};
     WS_TRY(lin_group(3, 2, li, at<uint16_t>(S, L.a), outs));
-  } else {
-    WS_TRY(lin(WS_LIN_V, at<uint16_t>(S, L.a), at<uint16_t>(S, L.v)));
   }
   if (attn) {
     // causal attention over the M tokens as one sequence
