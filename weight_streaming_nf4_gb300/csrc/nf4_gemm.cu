@@ -82,6 +82,13 @@ namespace {
 #ifndef WS_GEMM_BSTAGES
 #define WS_GEMM_BSTAGES 3
 #endif
+// One barrier and one commit per pipeline step on the pair MMA (0: an
+// activation barrier and a weight-buffer barrier, each with its commit).
+#ifndef WS_GEMM_MERGED_BARRIERS
+#define WS_GEMM_MERGED_BARRIERS 1
+#endif
+constexpr bool kMergedBarriers = WS_GEMM_MERGED_BARRIERS != 0;
+
 #ifndef WS_GEMM_STAGES_MAX
 #define WS_GEMM_STAGES_MAX 6
 #endif
@@ -151,7 +158,13 @@ struct Cfg {
   static constexpr int STAGES_RAW =
       (int)((WS_GEMM_SMEM_BUDGET_KB * 1024u - BSTAGES * B_BYTES - CSTAGES * CODE_BYTES - 1024u) /
             A_BYTES);
-  static constexpr int STAGES = STAGES_RAW > WS_GEMM_STAGES_MAX ? WS_GEMM_STAGES_MAX : STAGES_RAW;
+  static constexpr int STAGES_FREE = STAGES_RAW > WS_GEMM_STAGES_MAX ? WS_GEMM_STAGES_MAX : STAGES_RAW;
+  // Pair MMA: an activation stage and a weight buffer are filled and freed
+  // together (as many stages as buffers), so one barrier per stage says
+  // "both operands ready" and one MMA commit frees both: one wait and one
+  // commit per step for the MMA thread instead of two each.
+  static constexpr bool MERGED = PM && kMergedBarriers;
+  static constexpr int STAGES = MERGED ? BSTAGES : STAGES_FREE;
   // one accumulator set
   static constexpr uint32_t ACC_COLS = UM * BN;
   // double-buffer the accumulator when TMEM has room, so the epilogue of
@@ -174,6 +187,7 @@ struct Cfg {
   static constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
   static_assert(STAGES >= 2, "pipeline needs two stages");
+  static_assert(!MERGED || STAGES_RAW >= BSTAGES, "merged stages fit the shared memory");
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns");
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory");
   static_assert(BN == 128 || BN == 256, "BN");
@@ -585,7 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // an earlier kernel already gave up: do nothing rather than queue more work
     *skip_flag = (bad_cfg || *(volatile uint32_t*)&g_dev_error != 0u || pe <= pb) ? 1u : 0u;
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      // merged: the even CTA's full[s] also counts both CTAs' weight halves
+      // (its own dequant warps and the odd CTA's forwarding thread)
+      mbar_init(&full[s], (C::MERGED && rank == 0) ? 1 + kDqWarps + 1 : 1);
       mbar_init(&empty[s], 1);
     }
     // PAIR = 2: the even CTA's full / bfull / accempty / lora_masked count
@@ -666,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (*abort_flag) {
           // let every issued copy land before the CTA can exit
-          if (!PM || rank == 0) {
+          if ((!PM || rank == 0) && !C::MERGED) {
             for (int64_t q = (issued > STAGES ? issued - STAGES : 0); q < issued; ++q)
               mbar_wait(&full[q % STAGES], (uint32_t)(q / STAGES) & 1u, DERR_TIMEOUT_DRAIN);
           } else if (issued > 0) {
@@ -713,9 +729,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               ms_b = 0;
               ms_bph ^= 1u;
             }
-            bool ok = !*abort_flag && mbar_wait(&full[s], ph, DERR_TIMEOUT_FULL);
-            if constexpr (PAIR != 0) ok = ok && mbar_wait_cluster(&bfull[b], bph, DERR_TIMEOUT_BFULL);
-            else ok = ok && mbar_wait(&bfull[b], bph, DERR_TIMEOUT_BFULL);
+            bool ok = !*abort_flag;
+            if constexpr (C::MERGED) {
+              ok = ok && mbar_wait_cluster(&full[s], ph, DERR_TIMEOUT_FULL);
+            } else {
+              ok = ok && mbar_wait(&full[s], ph, DERR_TIMEOUT_FULL);
+              if constexpr (PAIR != 0) ok = ok && mbar_wait_cluster(&bfull[b], bph, DERR_TIMEOUT_BFULL);
+              else ok = ok && mbar_wait(&bfull[b], bph, DERR_TIMEOUT_BFULL);
+            }
             if (!ok) {
               *abort_flag = 1u;
               break;
@@ -746,7 +767,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else tc_mma_f16(d, adesc, bdesc, idesc, acc);
               }
             }
-            if constexpr (PM) {
+            if constexpr (C::MERGED) {
+              tc_commit_pair_multicast(&empty[s], (uint16_t)0x3);
+            } else if constexpr (PM) {
               tc_commit_pair_multicast(&empty[s], (uint16_t)0x3);
               tc_commit_pair_multicast(&bempty[b], (uint16_t)0x3);
             } else {
@@ -785,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *abort_flag = 1u;
             break;
           }
-          mbar_arrive_cluster(mapa_shared(smem_u32(&bfull[b]), 0u));
+          mbar_arrive_cluster(mapa_shared(smem_u32(C::MERGED ? &full[b] : &bfull[b]), 0u));
           if (++b == BSTAGES) {
             b = 0;
             bph ^= 1u;
@@ -835,8 +858,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           read_frag<BWD, BN, PAIR>(cur, ring + (q % CS) * C::CODE_BYTES, t_idx);
         }
         bool ok = !*abort_flag;
-        if constexpr (PAIR != 0) ok = ok && mbar_wait_cluster(&bempty[b], bph ^ 1u, DERR_TIMEOUT_BEMPTY);
-        else ok = ok && mbar_wait(&bempty[b], bph ^ 1u, DERR_TIMEOUT_BEMPTY);
+        // merged: stage b's commit frees the buffer (b equals the stage index)
+        uint64_t* freed = C::MERGED ? &empty[b] : &bempty[b];
+        if constexpr (PAIR != 0) ok = ok && mbar_wait_cluster(freed, bph ^ 1u, DERR_TIMEOUT_BEMPTY);
+        else ok = ok && mbar_wait(freed, bph ^ 1u, DERR_TIMEOUT_BEMPTY);
         if (!ok) {
           *abort_flag = 1u;
           break;
@@ -853,15 +878,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int64_t nb = (int64_t)pc.nt * BN;
               const int32_t kc = kstep(pc.i) * 64;
               const int32_t half0 = PM ? rank * C::BW : 0;
-              mbar_arrive_expect_tx(&bfull[b], C::B_BYTES);
+              // merged, even CTA: the stage barrier; else this CTA's buffer barrier
+              uint64_t* wbar = (C::MERGED && rank == 0) ? &full[b] : &bfull[b];
+              mbar_arrive_expect_tx(wbar, C::B_BYTES);
               if constexpr (!BWD) {
                 const TileGrp tg = tile_grp(args, nb);
                 const CUtensorMap* m = tg.g == 2 ? &wm.m[2] : (tg.g == 1 ? &wm.m[1] : &wm.m[0]);
-                tma_load_2d(Bt, m, &bfull[b], kc, (int32_t)(nb - tg.c0) + half0);
+                tma_load_2d(Bt, m, wbar, kc, (int32_t)(nb - tg.c0) + half0);
               } else {
 #pragma unroll
                 for (int j = 0; j < C::BW / 64; ++j)
-                  tma_load_2d(Bt + j * 8192, &wm.m[0], &bfull[b], (int32_t)nb + half0 + j * 64, kc);
+                  tma_load_2d(Bt + j * 8192, &wm.m[0], wbar, (int32_t)nb + half0 + j * 64, kc);
               }
             }
           } else {
@@ -878,19 +905,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && !(tma_step && warp == 2)) {
           if constexpr (PM) {
             // the even CTA's MMA reads this half where it lies
-            mbar_arrive(&bfull[b]);
+            mbar_arrive((C::MERGED && rank == 0) ? &full[b] : &bfull[b]);
           } else if constexpr (PAIR == 1) {
             // this warp's share of the half tile is one contiguous block:
             // rows (K-major) or one 8-row contraction group (MN-major);
             // send it to the same place in the other CTA's buffer
-            constexpr uint32_t WB = C::B_BYTES / 16;
+            constexpr uint32_t kShare = C::B_BYTES / 16;
             const int dw = warp - 2;
             const uint32_t off =
                 (BWD && !lora_step)
                     ? (uint32_t)(dw * (int)C::MN_SBO + rank * (BN / 128) * 1024)
                     : (uint32_t)((rank * (BN / 2) + dw * (BN / 16)) * 128);
-            mbar_arrive_expect_tx(&bfull[b], WB);
-            bulk_copy_to_peer(mapa_shared(smem_u32(Bt + off), peer), Bt + off, WB,
+            mbar_arrive_expect_tx(&bfull[b], kShare);
+            bulk_copy_to_peer(mapa_shared(smem_u32(Bt + off), peer), Bt + off, kShare,
                               mapa_shared(smem_u32(&bfull[b]), peer));
           } else {
             mbar_arrive(&bfull[b]);
@@ -913,7 +940,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the other CTA's MMA commits arrive on this CTA's buffer barriers:
         // wait for the last of them before the CTA can leave
         for (int k = 0; k < BSTAGES && !*abort_flag; ++k) {
-          if (!mbar_wait_cluster(&bempty[b], bph ^ 1u, DERR_TIMEOUT_DRAIN)) break;
+          if (!mbar_wait_cluster(C::MERGED ? &empty[b] : &bempty[b], bph ^ 1u, DERR_TIMEOUT_DRAIN))
+            break;
           if (++b == BSTAGES) {
             b = 0;
             bph ^= 1u;
@@ -1866,7 +1894,8 @@ cudaError_t launch_cfg(const GemmPlan& p, const GemmArgs& a, const CUtensorMap& 
   const int64_t G = grid_ctas(p, a.has_lora != 0);
   // the plan sizes pair grids by the NF4 kernel's residency; the bf16
   // variant (no code ring) must fit the same grid at once
-  if (WB && PAIR != 0 && G / 2 > pair_capacity_of<BWD, BN, PAIR, WB>()) return cudaErrorInvalidConfiguration;
+  if (WB && PAIR != 0 && G / 2 > pair_capacity_of<BWD, BN, PAIR, WB>())
+    return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)G);
   cfg.blockDim = dim3(kThreads);
