@@ -468,50 +468,99 @@ def profile_roofline(torch):
 
 
 def linear_7b(ops, torch, dev, M, reps=5):
-    """Seven 7B-layer NF4-LoRA linears, ws_lora_linear_fwd + ws_lora_linear_bwd
-    each, weights rotated over 4 layer copies (larger than L2)."""
+    """Seven 7B-layer NF4-LoRA linears forward + backward, weights rotated over
+    4 layer copies (larger than L2), two ways: one ws_lora_linear_fwd / _bwd
+    call per linear, and the grouped calls a layer makes (q, k, v and gate, up
+    forward together; k, v and gate, up backward together)."""
     H, KV, I = SHAPE_7B["H"], SHAPE_7B["KV"], SHAPE_7B["I"]
+    shapes = lin_shapes(H, KV, I)
     copies = []
     for c in range(4):
         lins = []
-        for li, (N, K) in enumerate(lin_shapes(H, KV, I)):
+        xa = torch.randn(M, H, device=dev).to(torch.bfloat16)      # q, k, v, gate, up input
+        for li, (N, K) in enumerate(shapes):
             W = (torch.randn(N, K, device=dev) * 0.02).to(torch.bfloat16)
             codes, absmax = ops.quantize_nf4(W)
             del W
             A = (torch.rand(16, K, device=dev) * 2 - 1) / (K ** 0.5)
             B = torch.randn(N, 16, device=dev) * 0.01
-            x = torch.randn(M, K, device=dev).to(torch.bfloat16)
+            x = xa if li in (0, 1, 2, 4, 5) else torch.randn(M, K, device=dev).to(torch.bfloat16)
             dY = torch.randn(M, N, device=dev).to(torch.bfloat16)
             y = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
             U = torch.empty(M, 16, device=dev)
             mask = torch.empty(M, K // 32, device=dev, dtype=torch.int32)
-            dX = torch.empty(M, K, device=dev, dtype=torch.bfloat16)
+            dX = torch.empty(M, K, device=dev, dtype=torch.float32)
             dA, dB = torch.empty_like(A), torch.empty_like(B)
             ws = torch.empty(ops.lora_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
-            lins.append((ops.NF4Weight(codes, absmax, N, K), x, A, B, dY, y, U, mask, dX, dA, dB,
-                         ws, ops.dropout_key(linear=li)))
-        copies.append(lins)
-    flops = sum(4 * M * N * K + 6 * M * 16 * (N + K) for N, K in lin_shapes(H, KV, I))
+            lins.append(dict(W=ops.NF4Weight(codes, absmax, N, K), x=x, A=A, B=B, dY=dY, y=y,
+                             U=U, mask=mask, dX=dX, dA=dA, dB=dB, ws=ws,
+                             key=ops.dropout_key(linear=li)))
+        gws = torch.empty(max(ops.lora_group_workspace_size([H, KV, KV], M, H),
+                              ops.lora_group_workspace_size([KV, KV], M, H),
+                              ops.lora_group_workspace_size([H], M, H),
+                              ops.lora_group_workspace_size([I, I], M, H),
+                              ops.lora_group_workspace_size([H], M, I)),
+                          dtype=torch.uint8, device=dev)
+        copies.append((lins, gws))
+    flops = sum(4 * M * N * K + 6 * M * 16 * (N + K) for N, K in shapes)
 
-    def one(lins):
-        for (W, x, A, B, dY, y, U, mask, dX, dA, dB, ws, key) in lins:
-            ops.lora_linear_fwd(W, x, A, B, key, y=y, U=U, mask=mask, workspace=ws)
-            ops.lora_linear_bwd(W, x, A, B, key, U, mask, dY, dX=dX, dA=dA, dB=dB, workspace=ws)
-    for c in copies:
-        one(c)
-    torch.cuda.synchronize()
-    st = torch.cuda.current_stream()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for r in range(reps):
+    def single(c):
+        lins, _ = c
+        for l in lins:
+            ops.lora_linear_fwd(l["W"], l["x"], l["A"], l["B"], l["key"], y=l["y"], U=l["U"],
+                                mask=l["mask"], workspace=l["ws"])
+        for l in lins:
+            ops.lora_linear_bwd(l["W"], l["x"], l["A"], l["B"], l["key"], l["U"], l["mask"],
+                                l["dY"], dX=l["dX"], dA=l["dA"], dB=l["dB"], workspace=l["ws"])
+
+    def grouped(c):
+        lins, gws = c
+
+        def fwd(ids):
+            ls = [lins[i] for i in ids]
+            ops.lora_linear_fwd_group([l["W"] for l in ls], ls[0]["x"], [l["A"] for l in ls],
+                                      [l["B"] for l in ls], [l["key"] for l in ls],
+                                      ys=[l["y"] for l in ls], Us=[l["U"] for l in ls],
+                                      masks=[l["mask"] for l in ls], workspace=gws)
+
+        def bwd(ids):
+            ls = [lins[i] for i in ids]
+            ops.lora_linear_bwd_group([l["W"] for l in ls], ls[0]["x"], [l["A"] for l in ls],
+                                      [l["B"] for l in ls], [l["key"] for l in ls],
+                                      [l["U"] for l in ls], [l["mask"] for l in ls],
+                                      [l["dY"] for l in ls], dX=ls[0]["dX"],
+                                      dAs=[l["dA"] for l in ls], dBs=[l["dB"] for l in ls],
+                                      workspace=gws)
+        fwd((0, 1, 2))
+        fwd((3,))
+        fwd((4, 5))
+        fwd((6,))
+        bwd((6,))
+        bwd((4, 5))
+        bwd((3,))
+        bwd((1, 2))
+        bwd((0,))
+
+    out = {}
+    for name, one in (("per_linear", single), ("grouped", grouped)):
         for c in copies:
             one(c)
-    e1.record(st)
-    torch.cuda.synchronize()
-    t = e0.elapsed_time(e1) / 1e3
-    n = reps * len(copies)
-    return dict(tflops=flops * n / t / 1e12, ms_per_layer=1e3 * t / n, flops_per_layer=flops)
+        torch.cuda.synchronize()
+        st = torch.cuda.current_stream()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for r in range(reps):
+            for c in copies:
+                one(c)
+        e1.record(st)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3
+        n = reps * len(copies)
+        out[name] = dict(tflops=flops * n / t / 1e12, ms_per_layer=1e3 * t / n)
+    out["flops_per_layer"] = flops
+    out["tflops"] = max(out["per_linear"]["tflops"], out["grouped"]["tflops"])
+    return out
 
 
 def profile_gemm(torch, which):

@@ -203,6 +203,40 @@ ws_status ws_lora_linear_fwd(const ws_nf4* W, const uint16_t* x, const float* A,
                              uint16_t* y, float* U_saved, uint32_t* mask_saved,
                              void* workspace, size_t ws_bytes, ws_stream_t stream);
 
+/* The forward of ng (1..3) NF4-LoRA linears that read the same input x (a
+ * layer's q, k, v, or its gate and up): the same computation per linear as
+ * ws_lora_linear_fwd, in fewer, fuller launches: one LoRA-down launch draws
+ * every linear's dropout mask and U, and one dequant GEMM covers their
+ * concatenated outputs when every width is a multiple of the GEMM's tile
+ * width (else one GEMM per linear).  Arrays are indexed by linear g < ng:
+ * W[g] [N_g, K] (every K equal), A[g] [r, K], B[g] [N_g, r], keys[g],
+ * y[g] [M, N_g] bf16, U_saved[g] [M, r] fp32, mask_saved[g] (entries may be
+ * NULL).  sh gives M, K, r, alpha (its N is ignored).  U and y can differ in
+ * the last bits from single-linear calls (the LoRA-down sums run in
+ * k-chunks sized for the whole launch); a given grouping always gives the
+ * same bits.  workspace >= ws_lora_group_workspace_size. */
+ws_status ws_lora_group_workspace_size(int32_t ng, const int64_t* N, int64_t M, int64_t K,
+                                       size_t* bytes);
+ws_status ws_lora_linear_fwd_group(int32_t ng, const ws_nf4* W, const uint16_t* x,
+                                   const float* const* A, const float* const* B, ws_lora_shape sh,
+                                   const ws_dropout_key* keys, uint16_t* const* y,
+                                   float* const* U_saved, uint32_t* const* mask_saved,
+                                   void* workspace, size_t ws_bytes, ws_stream_t stream);
+/* The backward of ng (1..3) linears of one shape [N, K] that read the same x
+ * (a layer's k and v, or gate and up), each with its own dY[g]: G, dB and dA
+ * of every linear as in ws_lora_linear_bwd, their input gradients summed into
+ * one dX (linear 0 first), with the skinny products and weight gradients of
+ * all ng in one launch each.  accumulate: WS_ACC_* as for ws_lora_linear_bwd;
+ * dX is fp32 (WS_DTYPE_F32) whenever ng > 1.
+ * workspace >= ws_lora_group_workspace_size with every N_g = N. */
+ws_status ws_lora_linear_bwd_group(int32_t ng, const ws_nf4* W, const uint16_t* x,
+                                   const float* const* A, const float* const* B, ws_lora_shape sh,
+                                   const ws_dropout_key* keys, const float* const* U_saved,
+                                   const uint32_t* const* mask_saved, const uint16_t* const* dY,
+                                   void* dX, int32_t dX_dtype, int32_t accumulate,
+                                   float* const* dA, float* const* dB, void* workspace,
+                                   size_t ws_bytes, ws_stream_t stream);
+
 /* ---- LoRA linear backward ------------------------------------------------ */
 /* The backward of one linear: gradients for the adapters and the input only,
  * none for the frozen weight ("Poros", training-step paragraph).

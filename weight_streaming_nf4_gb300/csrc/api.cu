@@ -195,6 +195,103 @@ ws_status ws_lora_linear_bwd(const ws_nf4* W, const uint16_t* x, const float* A,
                                 (cudaStream_t)stream));
 }
 
+ws_status ws_lora_group_workspace_size(int32_t ng, const int64_t* N, int64_t M, int64_t K,
+                                       size_t* bytes) {
+  if (!bytes || !N) return WS_ERR_INVALID;
+  if (ng < 1 || ng > kMaxGroups || M < 1 || K < 64 || K % 64) return WS_ERR_SHAPE;
+  bool same = true;
+  for (int g = 0; g < ng; ++g) {
+    if (N[g] < 64 || N[g] % 64) return WS_ERR_SHAPE;
+    same = same && N[g] == N[0];
+  }
+  size_t b = linear_group_workspace_bytes(M, ng, N, K);
+  if (same) {
+    const size_t bb = linear_bwd_group_workspace_bytes(M, ng, N[0], K);
+    if (bb > b) b = bb;
+  }
+  *bytes = b;
+  return WS_OK;
+}
+
+ws_status ws_lora_linear_fwd_group(int32_t ng, const ws_nf4* W, const uint16_t* x,
+                                   const float* const* A, const float* const* B, ws_lora_shape sh,
+                                   const ws_dropout_key* keys, uint16_t* const* y,
+                                   float* const* U_saved, uint32_t* const* mask_saved,
+                                   void* workspace, size_t ws_bytes, ws_stream_t stream) {
+  if (ng < 1 || ng > kMaxGroups || !W || !A || !B || !keys || !y || !U_saved || !x || !workspace)
+    return WS_ERR_INVALID;
+  NF4View v[kMaxGroups];
+  DropKeyHost k[kMaxGroups];
+  int64_t N[kMaxGroups];
+  uint32_t* mk[kMaxGroups];
+  float scale = 0.0f;
+  for (int g = 0; g < ng; ++g) {
+    ws_lora_shape sg = sh;
+    sg.N = W[g].N;
+    const ws_status s = check_linear(&W[g], sg, keys[g]);
+    if (s != WS_OK) return s;
+    if (W[g].K != sh.K) return WS_ERR_SHAPE;
+    if (keys[g].p != keys[0].p) return WS_ERR_INVALID;
+    if (!A[g] || !B[g] || !y[g] || !U_saved[g]) return WS_ERR_INVALID;
+    if (!aligned16(A[g]) || !aligned16(B[g]) || !aligned16(y[g]) || !aligned16(U_saved[g]) ||
+        (mask_saved && mask_saved[g] && !aligned16(mask_saved[g])))
+      return WS_ERR_ALIGN;
+    v[g] = view_of(&W[g]);
+    k[g] = make_drop_key(keys[g]);
+    N[g] = W[g].N;
+    mk[g] = mask_saved ? mask_saved[g] : nullptr;
+    scale = lora_scale(sg, keys[g].p);
+  }
+  if (!aligned16(x) || !aligned16(workspace)) return WS_ERR_ALIGN;
+  if (ws_bytes < linear_group_workspace_bytes(sh.M, ng, N, sh.K)) return WS_ERR_OOM;
+  return cuda_status(linear_fwd_group(ng, ng, v, x, A, B, sh.M, scale, k, y, U_saved, mk,
+                                      workspace, (cudaStream_t)stream));
+}
+
+ws_status ws_lora_linear_bwd_group(int32_t ng, const ws_nf4* W, const uint16_t* x,
+                                   const float* const* A, const float* const* B, ws_lora_shape sh,
+                                   const ws_dropout_key* keys, const float* const* U_saved,
+                                   const uint32_t* const* mask_saved, const uint16_t* const* dY,
+                                   void* dX, int32_t dX_dtype, int32_t accumulate,
+                                   float* const* dA, float* const* dB, void* workspace,
+                                   size_t ws_bytes, ws_stream_t stream) {
+  if (ng < 1 || ng > kMaxGroups || !W || !A || !B || !keys || !U_saved || !dY || !dX || !dA ||
+      !dB || !x || !workspace)
+    return WS_ERR_INVALID;
+  if (dX_dtype != WS_DTYPE_BF16 && dX_dtype != WS_DTYPE_F32) return WS_ERR_INVALID;
+  if (accumulate & ~(WS_ACC_DX | WS_ACC_GRADS)) return WS_ERR_INVALID;
+  const int dX_accumulate = (accumulate & WS_ACC_DX) ? 1 : 0;
+  // the sum over linears is taken in fp32
+  if ((dX_accumulate || ng > 1) && dX_dtype != WS_DTYPE_F32) return WS_ERR_INVALID;
+  NF4View v[kMaxGroups];
+  DropKeyHost k[kMaxGroups];
+  const uint32_t* mk[kMaxGroups];
+  float scale = 0.0f;
+  for (int g = 0; g < ng; ++g) {
+    ws_lora_shape sg = sh;
+    sg.N = W[0].N;
+    const ws_status s = check_linear(&W[g], sg, keys[g]);
+    if (s != WS_OK) return s;
+    if (W[g].K != sh.K) return WS_ERR_SHAPE;
+    if (keys[g].p != keys[0].p) return WS_ERR_INVALID;
+    if (!A[g] || !B[g] || !U_saved[g] || !dY[g] || !dA[g] || !dB[g]) return WS_ERR_INVALID;
+    if (!aligned16(A[g]) || !aligned16(B[g]) || !aligned16(U_saved[g]) || !aligned16(dY[g]) ||
+        !aligned16(dA[g]) || !aligned16(dB[g]) ||
+        (mask_saved && mask_saved[g] && !aligned16(mask_saved[g])))
+      return WS_ERR_ALIGN;
+    v[g] = view_of(&W[g]);
+    k[g] = make_drop_key(keys[g]);
+    mk[g] = mask_saved ? mask_saved[g] : nullptr;
+    scale = lora_scale(sg, keys[g].p);
+  }
+  if (!aligned16(x) || !aligned16(dX) || !aligned16(workspace)) return WS_ERR_ALIGN;
+  if (ws_bytes < linear_bwd_group_workspace_bytes(sh.M, ng, W[0].N, sh.K)) return WS_ERR_OOM;
+  return cuda_status(linear_bwd_group(ng, v, x, A, B, sh.M, scale, k, U_saved, mk, dY, dX,
+                                      dX_dtype == WS_DTYPE_F32 ? 1 : 0, dX_accumulate, dA, dB,
+                                      (accumulate & WS_ACC_GRADS) ? 1 : 0, workspace,
+                                      (cudaStream_t)stream));
+}
+
 namespace {
 ws_status check_bf16(const ws_bf16* W, ws_lora_shape sh, const ws_dropout_key& key, ws_nf4* as) {
   if (!W || !W->w) return WS_ERR_INVALID;

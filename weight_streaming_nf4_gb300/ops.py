@@ -106,6 +106,10 @@ _sig("ws_lora_linear_bwd_bf16", [C.POINTER(Bf16W), P, P, P, LoraShape, DropoutKe
 _sig("ws_nf4_matmul_workspace_size", [i64, i64, i64, i32, C.POINTER(C.c_size_t)])
 _sig("ws_nf4_matmul", [C.POINTER(Nf4), P, i64, i32, P, i32, P, C.c_size_t, P])
 _sig("ws_nf4_matmul_noalloc", [C.POINTER(Nf4), P, i64, i32, P, i32, P])
+_sig("ws_lora_group_workspace_size", [i32, P, i64, i64, C.POINTER(C.c_size_t)])
+_sig("ws_lora_linear_fwd_group", [i32, P, P, P, P, LoraShape, P, P, P, P, P, C.c_size_t, P])
+_sig("ws_lora_linear_bwd_group", [i32, P, P, P, P, LoraShape, P, P, P, P, P, i32, i32, P, P, P,
+                                  C.c_size_t, P])
 _sig("ws_attention_fwd", [P, P, P, i32, i32, i32, i32, i32, P, P, P, P])
 _sig("ws_attention_workspace_size", [i64, i32, i32, C.POINTER(C.c_size_t)])
 _sig("ws_attention_bwd", [P, P, P, P, P, P, i32, i32, i32, i32, i32, P, P, P, P, C.c_size_t, P])
@@ -138,7 +142,8 @@ _sig("ws_stack_graph_destroy", [P])
 EXPORTED = ("ws_status_string", "ws_device_error", "ws_selfcheck_bounded_wait", "ws_kernel_launches", "ws_quantize_nf4", "ws_lora_workspace_size",
             "ws_lora_linear_fwd", "ws_lora_linear_bwd", "ws_lora_linear_fwd_bf16",
             "ws_lora_linear_bwd_bf16", "ws_nf4_matmul_workspace_size",
-            "ws_nf4_matmul", "ws_nf4_matmul_noalloc", "ws_attention_fwd",
+            "ws_nf4_matmul", "ws_nf4_matmul_noalloc", "ws_lora_group_workspace_size",
+            "ws_lora_linear_fwd_group", "ws_lora_linear_bwd_group", "ws_attention_fwd",
             "ws_attention_workspace_size", "ws_attention_bwd", "ws_stack_sizes",
             "ws_stack_weight_offset", "ws_stack_param_offset", "ws_stack_saved_offset",
             "ws_stack_workspace_offset", "ws_stack_loader_staging_bytes", "ws_stack_put_weight",
@@ -283,6 +288,73 @@ def lora_linear_bwd(W: NF4Weight, x, A, B, key: DropoutKey, U, mask, dY, alpha=3
                                    _ptr(dA), _ptr(dB), _ptr(workspace), workspace.numel(),
                                    _stream(stream)))
     return dX, dA, dB
+
+
+def _ptrs(ts):
+    """A C array of device pointers (None entries -> NULL; ts None -> a NULL array)."""
+    if ts is None:
+        return None
+    return (C.c_void_p * len(ts))(*[None if t is None else t.data_ptr() for t in ts])
+
+
+def lora_group_workspace_size(Ns, M, K) -> int:
+    n = C.c_size_t(0)
+    arr = (i64 * len(Ns))(*Ns)
+    _check("ws_lora_group_workspace_size",
+           _lib.ws_lora_group_workspace_size(len(Ns), arr, M, K, C.byref(n)))
+    return int(n.value)
+
+
+def lora_linear_fwd_group(Ws, x, As, Bs, keys, alpha=32.0, ys=None, Us=None, masks=None,
+                          workspace=None, stream=None):
+    """ws_lora_linear_fwd_group: ng linears reading the same x [M, K].  Returns
+    (ys, Us, masks) lists."""
+    ng = len(Ws)
+    M, K = x.shape
+    dev = x.device
+    ys = ys or [torch.empty((M, W.N), dtype=torch.bfloat16, device=dev) for W in Ws]
+    Us = Us or [torch.empty((M, A.shape[0]), dtype=torch.float32, device=dev) for A in As]
+    masks = masks or [torch.empty((M, K // 32), dtype=torch.int32, device=dev) for _ in Ws]
+    if workspace is None:
+        workspace = torch.empty(lora_group_workspace_size([W.N for W in Ws], M, K),
+                                dtype=torch.uint8, device=dev)
+    ws_arr = (Nf4 * ng)(*[W.c() for W in Ws])
+    key_arr = (DropoutKey * ng)(*keys)
+    sh = LoraShape(M, Ws[0].N, K, As[0].shape[0], alpha)
+    _check("ws_lora_linear_fwd_group",
+           _lib.ws_lora_linear_fwd_group(ng, ws_arr, _ptr(x), _ptrs(As), _ptrs(Bs), sh, key_arr,
+                                         _ptrs(ys), _ptrs(Us), _ptrs(masks), _ptr(workspace),
+                                         workspace.numel(), _stream(stream)))
+    return ys, Us, masks
+
+
+def lora_linear_bwd_group(Ws, x, As, Bs, keys, Us, masks, dYs, alpha=32.0, dX=None,
+                          accumulate=False, dAs=None, dBs=None, workspace=None, stream=None,
+                          grad_accumulate=False):
+    """ws_lora_linear_bwd_group: ng linears of one shape reading the same x,
+    their input gradients summed into one fp32 dX.  Returns (dX, dAs, dBs)."""
+    ng = len(Ws)
+    M, K = x.shape
+    dev = x.device
+    if dX is None:
+        dX = torch.empty((M, K), dtype=torch.float32, device=dev)
+    dAs = dAs or [torch.empty_like(A) for A in As]
+    dBs = dBs or [torch.empty_like(B) for B in Bs]
+    if workspace is None:
+        workspace = torch.empty(lora_group_workspace_size([W.N for W in Ws], M, K),
+                                dtype=torch.uint8, device=dev)
+    ws_arr = (Nf4 * ng)(*[W.c() for W in Ws])
+    key_arr = (DropoutKey * ng)(*keys)
+    sh = LoraShape(M, Ws[0].N, K, As[0].shape[0], alpha)
+    dt = WS_DTYPE_F32 if dX.dtype == torch.float32 else WS_DTYPE_BF16
+    _check("ws_lora_linear_bwd_group",
+           _lib.ws_lora_linear_bwd_group(ng, ws_arr, _ptr(x), _ptrs(As), _ptrs(Bs), sh, key_arr,
+                                         _ptrs(Us), _ptrs(masks), _ptrs(dYs), _ptr(dX), dt,
+                                         (WS_ACC_DX if accumulate else 0)
+                                         | (WS_ACC_GRADS if grad_accumulate else 0),
+                                         _ptrs(dAs), _ptrs(dBs), _ptr(workspace),
+                                         workspace.numel(), _stream(stream)))
+    return dX, dAs, dBs
 
 
 def nf4_matmul_workspace_size(M, N, K, transpose_w=False) -> int:
