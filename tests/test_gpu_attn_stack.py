@@ -145,3 +145,28 @@ def test_attention_stack_streamed_equals_resident(ops):
     for name in ("params", "grads", "adam_m", "adam_v"):
         assert torch.equal(getattr(res, name), getattr(stm, name)), name
     assert np.isfinite(float(res.loss.item()))
+
+
+@pytest.mark.parametrize("order", ["mb", "block"])
+def test_attention_stack_grad_accumulation_bitwise(ops, order):
+    """Gradient accumulation over 2 micro-batches with the attention core:
+    streamed (either order) equals resident bitwise over 2 steps."""
+    from weight_streaming_nf4_gb300.stack import StackRun
+    cfg = ops.StackCfg(M=256, H=896, KV=128, I=4864, head_dim=64, n_layers=4,
+                       attn=ops.ATTN_CAUSAL)
+    o = ops.GA_MICROBATCH_MAJOR if order == "mb" else ops.GA_BLOCK_MAJOR
+    wfn, pfn = _fns(7)
+    res = StackRun(cfg, 2, False, wfn, pfn, n_micro=2, order=o)
+    stm = StackRun(cfg, 2, True, wfn, pfn, n_micro=2, order=o)
+    from weight_streaming_nf4_gb300 import synth
+    for step in range(2):
+        h0 = torch.cat([f32_to_dev(synth.stack_h0(cfg.seed + mb, step, cfg.M, cfg.H)).reshape(-1)
+                        for mb in range(2)])
+        res.step(step, h0)
+        stm.step(step, h0)
+        torch.cuda.synchronize()
+        assert torch.equal(res.loss, stm.loss), step
+        assert torch.equal(res.grads, stm.grads), step
+    assert ops.device_error() == 0
+    for name in ("params", "adam_m", "adam_v"):
+        assert torch.equal(getattr(res, name), getattr(stm, name)), name

@@ -416,6 +416,9 @@ WsLayout ws_layout(const ws_stack_cfg& c, int block_layers) {
   if (g2 > lin) lin = g2;
   const size_t b2 = linear_bwd_group_workspace_bytes(c.M, 2, s.N[WS_LIN_GATE], s.K[WS_LIN_GATE]);
   if (b2 > lin) lin = b2;
+  // the attention core's backward runs v and k as one group
+  const size_t b3 = linear_bwd_group_workspace_bytes(c.M, 2, s.N[WS_LIN_K], s.K[WS_LIN_K]);
+  if (b3 > lin) lin = b3;
   L.lin = take(lin);
   L.blk = take((size_t)block_layers * saved_layout(c).total);
   L.qout = take(M * H * 2);
@@ -672,8 +675,32 @@ cudaError_t layer_bwd(const Ctx& x, const void* block, int lib, int layer, const
                         at<const uint16_t>(S, L.v), at<const float>(S, L.o32),
                         at<const float>(S, L.lse), dob, 1, (int)M, (int)(H / hd), (int)(KV / hd),
                         hd, dq, dk, dv, ws + x.WSL.attn, st));
-    WS_TRY(lin(WS_LIN_V, at<const uint16_t>(S, L.a), dv, da, 0));
-    WS_TRY(lin(WS_LIN_K, at<const uint16_t>(S, L.a), dk, da, 1));
+    {
+      // v and k have one shape and read the same input: their LoRA products
+      // and weight gradients share launches; da = dX_v + dX_k, then + dX_q
+      const int li[2] = {WS_LIN_V, WS_LIN_K};
+      NF4View W[2];
+      const float* A[2];
+      const float* B[2];
+      DropKeyHost keys[2];
+      const float* U[2];
+      const uint32_t* mk[2];
+      const uint16_t* dYs[2] = {dv, dk};
+      float* dAs[2];
+      float* dBs[2];
+      for (int g = 0; g < 2; ++g) {
+        W[g] = wview(x, block, lib, li[g]);
+        A[g] = P + x.PL.A[li[g]];
+        B[g] = P + x.PL.B[li[g]];
+        keys[g] = key_of(x, step, layer, li[g], mb);
+        U[g] = at<const float>(S, L.U[li[g]]);
+        mk[g] = at<const uint32_t>(S, L.mask[li[g]]);
+        dAs[g] = Gd + x.PL.A[li[g]];
+        dBs[g] = Gd + x.PL.B[li[g]];
+      }
+      WS_TRY(linear_bwd_group(2, W, at<const uint16_t>(S, L.a), A, B, M, x.scale, keys, U, mk, dYs,
+                              da, 1, 0, dAs, dBs, gacc, lws, st));
+    }
     WS_TRY(lin(WS_LIN_Q, at<const uint16_t>(S, L.a), dq, da, 1));
     note_launch();
     (void)launch_pdl(k_rmsnorm_bwd, dim3((unsigned)M), dim3(256), 0, st,
