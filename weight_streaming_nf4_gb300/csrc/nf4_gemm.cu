@@ -92,6 +92,15 @@ constexpr bool kMergedBarriers = WS_GEMM_MERGED_BARRIERS != 0;
 #ifndef WS_GEMM_STAGES_MAX
 #define WS_GEMM_STAGES_MAX 6
 #endif
+// Forward dequant warps load their codes and block scales straight into
+// registers, two steps ahead (1), instead of through a ring in shared memory
+// (0).  The input gradient keeps the ring: its 8-byte code items, gathered
+// from 64 weight rows per step, lose a fifth of the rate when loaded into
+// registers.
+#ifndef WS_GEMM_REG_CODES
+#define WS_GEMM_REG_CODES 1
+#endif
+constexpr bool kRegCodes = WS_GEMM_REG_CODES != 0;
 // Bytes (KB) of the dequant threads' code ring: each thread fetches its codes
 // and block scales as many steps ahead as the ring holds (at least 4, at most
 // 16), so a narrower tile (shorter steps) fetches more steps ahead.
@@ -151,7 +160,8 @@ struct Cfg {
   static constexpr int BSTAGES = PM ? WS_GEMM_BSTAGES + 1 : WS_GEMM_BSTAGES;
 #endif
   // per-thread ring of fetched codes (cp.async), CSTAGES steps deep
-  static constexpr uint32_t CODE_BYTES = WB ? 0u : DqGeo<BWD, BN, PAIR>::SLOT_BYTES;
+  static constexpr bool REG_CODES = kRegCodes && !BWD;
+  static constexpr uint32_t CODE_BYTES = (WB || REG_CODES) ? 0u : DqGeo<BWD, BN, PAIR>::SLOT_BYTES;
   static constexpr int CSTAGES_RAW =
       (int)((WS_GEMM_CODE_RING_KB * 1024u) / DqGeo<BWD, BN, PAIR>::SLOT_BYTES);
   static constexpr int CSTAGES = CSTAGES_RAW < 4 ? 4 : (CSTAGES_RAW > 16 ? 16 : CSTAGES_RAW);
@@ -372,6 +382,52 @@ WS_DEVINL void read_frag(Frag& f, const uint8_t* slot, int t) {
   }
 #pragma unroll
   for (int v = 0; v < D::NS; ++v) f.a[v] = sc[v * kDqThreads + t];
+}
+
+// The codes and scale fetch_codes + read_frag give a thread, loaded straight
+// into registers on the read-only path (zero codes and scale past the edge).
+template <bool BWD, int BN, int PAIR>
+WS_DEVINL void load_frag(Frag& f, const uint8_t* codes, const float* absmax, int64_t wN,
+                         int64_t wK, int i, int64_t n0, int rank, int t) {
+  using D = DqGeo<BWD, BN, PAIR>;
+  const int64_t kb = wK / 2;
+  const int c0 = PAIR ? rank * D::COLS : 0;
+  auto ld = [&](const uint8_t* p, bool in, int v) {
+    if constexpr (D::VB == 16) {
+      const uint4 x = in ? __ldg(reinterpret_cast<const uint4*>(p)) : make_uint4(0u, 0u, 0u, 0u);
+      f.w[4 * v] = x.x;
+      f.w[4 * v + 1] = x.y;
+      f.w[4 * v + 2] = x.z;
+      f.w[4 * v + 3] = x.w;
+    } else {
+      const uint2 x = in ? __ldg(reinterpret_cast<const uint2*>(p)) : make_uint2(0u, 0u);
+      f.w[2 * v] = x.x;
+      f.w[2 * v + 1] = x.y;
+    }
+  };
+  if constexpr (!BWD) {
+    const int j = c0 + t / D::TPR, part = t % D::TPR;
+    const int64_t n = (int64_t)n0 + j;
+    const bool in = n < wN;
+    const int64_t nn = in ? n : 0;
+    const uint8_t* src = codes + nn * kb + (int64_t)i * 32 + part * (32 / D::TPR);
+#pragma unroll
+    for (int v = 0; v < D::NV; ++v) ld(src + D::VB * v, in, v);
+    f.a[0] = in ? __ldg(absmax + (int64_t)i * wN + nn) : 0.0f;
+  } else {
+    constexpr int SEGS = D::COLS / (2 * D::VB);
+#pragma unroll
+    for (int it = 0; it < D::NV; ++it) {
+      const int item = t * D::NV + it;
+      const int c = item / SEGS, seg = item % SEGS;
+      const int64_t r = (int64_t)i * 64 + c;
+      const int64_t col = (int64_t)n0 + c0 + seg * 2 * D::VB;
+      const bool in = r < wN && col < wK;
+      const int64_t rr = in ? r : 0, cl = in ? col : 0;
+      ld(codes + rr * kb + cl / 2, in, it);
+      if (it == 0) f.a[0] = in ? __ldg(absmax + (cl / 64) * wN + rr) : 0.0f;
+    }
+  }
 }
 
 // Forward weight tile, K-major 128B-swizzled: row j = output column n0 + j,
@@ -831,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Pos pf = pos0;  // position of the next fetch
       int64_t fq = 0;
       auto fetch = [&]() {
-        if (!WB && fq < n_it && !is_lora_step(pf.i)) {
+        if (!WB && !C::REG_CODES && fq < n_it && !is_lora_step(pf.i)) {
           const uint32_t slot = smem_u32(ring + (fq % CS) * C::CODE_BYTES);
           const int64_t nb = (int64_t)pf.nt * BN;
           if constexpr (BWD) {
@@ -847,12 +903,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         pf.next(S, args.mtiles);
         ++fq;
       };
+      // register pipeline: f0, f1 hold the codes of the next two steps
+      Frag f0{}, f1{};
+      auto load_next = [&](Frag& f) {
+        if (!WB && C::REG_CODES && fq < n_it && !is_lora_step(pf.i)) {
+          const int64_t nb = (int64_t)pf.nt * BN;
+          if constexpr (BWD) {
+            load_frag<BWD, BN, PAIR>(f, args.codes, args.absmax, args.wN, args.wK, kstep(pf.i),
+                                     nb, rank, t_idx);
+          } else {
+            const TileGrp tg = tile_grp(args, nb);
+            load_frag<BWD, BN, PAIR>(f, tg.codes, tg.absmax, tg.width, args.wK, kstep(pf.i),
+                                     nb - tg.c0, rank, t_idx);
+          }
+        }
+        pf.next(S, args.mtiles);
+        ++fq;
+      };
+      if constexpr (!WB && C::REG_CODES) {
+        load_next(f0);
+        load_next(f1);
+      }
 #pragma unroll 1
       for (int k = 0; k < CS - 1; ++k)
-        if constexpr (!WB) fetch();
+        if constexpr (!WB && !C::REG_CODES) fetch();
       for (int64_t q = 0; q < n_it; ++q) {
         Frag cur;
-        if constexpr (!WB) {
+        if constexpr (!WB && C::REG_CODES) {
+          cur = f0;
+          f0 = f1;
+          load_next(f1);  // the step after next
+        } else if constexpr (!WB) {
           fetch();  // refills the slot read in the previous iteration
           cp_async_wait<CS - 1>();
           read_frag<BWD, BN, PAIR>(cur, ring + (q % CS) * C::CODE_BYTES, t_idx);
