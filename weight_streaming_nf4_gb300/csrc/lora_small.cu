@@ -186,7 +186,7 @@ size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K) { return lin_ws_l
 namespace {
 struct Side {
   cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, fork2 = nullptr;
 };
 std::mutex g_side_mu;
 std::map<std::pair<int, cudaStream_t>, Side> g_side;
@@ -195,6 +195,17 @@ bool side_enabled() {
   static const bool on = [] {
     const char* v = getenv("WS_NF4_SIDE");
     return !(v && v[0] == '0');
+  }();
+  return on;
+}
+// dA joins dB on the side stream once G is ready, and both run beside the
+// input gradient's GEMM (joined after it: the GEMM's persistent CTAs take the
+// SMs the short weight-gradient launches leave; 5% off the 32B step).
+// WS_NF4_SIDE=1 joins them before the GEMM instead.
+bool side_late() {
+  static const bool on = [] {
+    const char* v = getenv("WS_NF4_SIDE");
+    return !(v && v[0] == '1');
   }();
   return on;
 }
@@ -209,6 +220,7 @@ cudaError_t side_of(cudaStream_t st, Side* out) {
     e = cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.fork2, cudaEventDisableTiming);
     if (e != cudaSuccess) {
       g_side.erase(std::make_pair(dev, st));
       return e;
@@ -357,31 +369,45 @@ cudaError_t linear_bwd(const NF4View& W, const uint16_t* x, const float* A, cons
     if (e != cudaSuccess) return e;
     mask = m;
   }
-  // dB needs only U and dY: on the side stream it runs beside G and dA and
-  // is joined back before dX (so the persistent GEMM starts on an idle GPU)
+  // dB needs only U and dY: on the side stream it runs beside G; dA follows
+  // it there once G is ready, and both overlap the input gradient's GEMM
   Side side;
   const bool use_side = dB != nullptr && side_enabled() && side_of(st, &side) == cudaSuccess;
+  const bool late = use_side && side_late() && dX != nullptr;
   if (use_side) {
     e = cudaEventRecord(side.fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side.s, side.fork, 0);
     if (e == cudaSuccess) e = run_wgrad_tc(U, dY, nullptr, M, W.N, scale, dB, 0, grad_accum, wg, side.s);
-    if (e == cudaSuccess) e = cudaEventRecord(side.join, side.s);
+    if (e == cudaSuccess && !late) e = cudaEventRecord(side.join, side.s);
     if (e != cudaSuccess) return e;
   }
   e = run_lora_G(dY, B, M, W.N, G, Gext, reinterpret_cast<float*>(w + L.skinny), st);
   if (e == cudaSuccess && dB && !use_side)
     e = run_wgrad_tc(U, dY, nullptr, M, W.N, scale, dB, 0, grad_accum, wg, st);
-  if (e == cudaSuccess && dA) e = run_wgrad_tc(G, x, mask, M, W.K, scale, dA, 1, grad_accum, wg, st);
+  if (e == cudaSuccess && dA) {
+    if (late) {
+      // dA needs G: the side stream waits for it, then runs beside the GEMM
+      e = cudaEventRecord(side.fork2, st);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(side.s, side.fork2, 0);
+      if (e == cudaSuccess) e = run_wgrad_tc(G, x, mask, M, W.K, scale, dA, 1, grad_accum, wg, side.s);
+    } else {
+      e = run_wgrad_tc(G, x, mask, M, W.K, scale, dA, 1, grad_accum, wg, st);
+    }
+  }
   // join even after an error, so a capture is never left with an unjoined stream
-  if (use_side) {
+  if (use_side && !late) {
     const cudaError_t ej = cudaStreamWaitEvent(st, side.join, 0);
     if (e == cudaSuccess) e = ej;
   }
-  if (e != cudaSuccess) return e;
-  if (dX) {
+  if (e == cudaSuccess && dX) {
     const GemmPlan p = plan_gemm(true, M, W.K, W.N);
     e = run_nf4_gemm(p, W, dY, M, Gext, A, scale, mask, dX, dX_f32, dX_accum,
                      reinterpret_cast<float*>(w + L.split), st);
+  }
+  if (late) {
+    cudaError_t ej = cudaEventRecord(side.join, side.s);
+    if (ej == cudaSuccess) ej = cudaStreamWaitEvent(st, side.join, 0);
+    if (e == cudaSuccess) e = ej;
   }
   return e;
 }
@@ -455,11 +481,12 @@ cudaError_t linear_bwd_group(int ng, const NF4View* W, const uint16_t* x, const 
   if (e != cudaSuccess) return e;
   Side side;
   const bool use_side = any_dB && side_enabled() && side_of(st, &side) == cudaSuccess;
+  const bool late = use_side && side_late() && dX != nullptr;
   if (use_side) {
     e = cudaEventRecord(side.fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side.s, side.fork, 0);
     if (e == cudaSuccess) e = run_wgrad_tc_group(ng, U, dY, nullptr, M, N, scale, dB, 0, grad_accum, side.s);
-    if (e == cudaSuccess) e = cudaEventRecord(side.join, side.s);
+    if (e == cudaSuccess && !late) e = cudaEventRecord(side.join, side.s);
     if (e != cudaSuccess) return e;
   }
   e = run_skinny_G_group(ng, dY, B, M, N, part, G, Gext, st);
@@ -472,17 +499,29 @@ cudaError_t linear_bwd_group(int ng, const NF4View* W, const uint16_t* x, const 
       Gc[g] = G[g];
       xs[g] = x;
     }
-    e = run_wgrad_tc_group(ng, Gc, xs, mk, M, K, scale, dA, 1, grad_accum, st);
+    if (late) {
+      e = cudaEventRecord(side.fork2, st);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(side.s, side.fork2, 0);
+      if (e == cudaSuccess) e = run_wgrad_tc_group(ng, Gc, xs, mk, M, K, scale, dA, 1, grad_accum, side.s);
+    } else {
+      e = run_wgrad_tc_group(ng, Gc, xs, mk, M, K, scale, dA, 1, grad_accum, st);
+    }
   }
-  if (use_side) {
+  if (use_side && !late) {
     const cudaError_t ej = cudaStreamWaitEvent(st, side.join, 0);
     if (e == cudaSuccess) e = ej;
   }
-  if (e != cudaSuccess || dX == nullptr) return e;
-  const GemmPlan p = plan_gemm(true, M, K, N);
-  for (int g = 0; g < ng && e == cudaSuccess; ++g)
-    e = run_nf4_gemm(p, W[g], dY[g], M, Gext[g], A[g], scale, mk[g], dX, dX_f32,
-                     g > 0 ? 1 : dX_accum, reinterpret_cast<float*>(w + L.split), st);
+  if (e == cudaSuccess && dX != nullptr) {
+    const GemmPlan p = plan_gemm(true, M, K, N);
+    for (int g = 0; g < ng && e == cudaSuccess; ++g)
+      e = run_nf4_gemm(p, W[g], dY[g], M, Gext[g], A[g], scale, mk[g], dX, dX_f32,
+                       g > 0 ? 1 : dX_accum, reinterpret_cast<float*>(w + L.split), st);
+  }
+  if (late) {
+    cudaError_t ej = cudaEventRecord(side.join, side.s);
+    if (ej == cudaSuccess) ej = cudaStreamWaitEvent(st, side.join, 0);
+    if (e == cudaSuccess) e = ej;
+  }
   return e;
 }
 
