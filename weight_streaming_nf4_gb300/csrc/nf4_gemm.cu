@@ -88,6 +88,16 @@ namespace {
 #define WS_GEMM_MERGED_BARRIERS 1
 #endif
 constexpr bool kMergedBarriers = WS_GEMM_MERGED_BARRIERS != 0;
+// Paired handovers per configuration, a bit mask: 1 forward 128-wide tiles,
+// 2 forward 256-wide, 4 input gradient 128-wide, 8 input gradient 256-wide.
+// On for the 128-wide tiles, whose steps are short enough for the per-step
+// handshake to bound them (32B step 77.3 -> 76.4 ms); the 256-wide tiles,
+// whose MMAs take as long as the decode, lose a step of prefetch slack
+// (waiting for the later buffer) and run slower paired.
+#ifndef WS_GEMM_PAIR_STEPS
+#define WS_GEMM_PAIR_STEPS 5
+#endif
+constexpr int kPairSteps = WS_GEMM_PAIR_STEPS;
 
 #ifndef WS_GEMM_STAGES_MAX
 #define WS_GEMM_STAGES_MAX 6
@@ -175,6 +185,14 @@ struct Cfg {
   // commit per step for the MMA thread instead of two each.
   static constexpr bool MERGED = PM && kMergedBarriers;
   static constexpr int STAGES = MERGED ? BSTAGES : STAGES_FREE;
+  // Merged NF4 stages are handed over in pairs: the dequant warps fill the
+  // weight buffers of two consecutive steps, then make one arrival on the
+  // even stage's barrier, which then stands for both buffers (the odd
+  // stage's barrier counts only its activation copy).  One wait, one fence
+  // and one arrival per two steps: the per-step handshake, not the decode,
+  // bounds the producers' rate.
+  static constexpr bool PAIRSTEP = MERGED && !WB && (BSTAGES % 2 == 0) &&
+                                   ((kPairSteps >> ((BWD ? 2 : 0) + (BN == 256 ? 1 : 0))) & 1) != 0;
   // one accumulator set
   static constexpr uint32_t ACC_COLS = UM * BN;
   // double-buffer the accumulator when TMEM has room, so the epilogue of
@@ -657,7 +675,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < STAGES; ++s) {
       // merged: the even CTA's full[s] also counts both CTAs' weight halves
       // (its own dequant warps and the odd CTA's forwarding thread)
-      mbar_init(&full[s], (C::MERGED && rank == 0) ? 1 + kDqWarps + 1 : 1);
+      const bool dq_here = C::MERGED && rank == 0 && (!C::PAIRSTEP || (s & 1) == 0);
+      mbar_init(&full[s], dq_here ? 1 + kDqWarps + 1 : 1);
       mbar_init(&empty[s], 1);
     }
     // PAIR = 2: the even CTA's full / bfull / accempty / lora_masked count
@@ -859,14 +878,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // odd CTA: forward each completed weight-buffer phase to the even CTA
         int b = 0;
         uint32_t bph = 0;
-        for (int64_t q = 0; q < pe - pb; ++q) {
+        constexpr int QS = C::PAIRSTEP ? 2 : 1;  // steps per handover
+        for (int64_t q = 0; q < pe - pb; q += QS) {
           if (*abort_flag || !mbar_wait(&bfull[b], bph, DERR_TIMEOUT_BFULL)) {
             *abort_flag = 1u;
             break;
           }
           mbar_arrive_cluster(mapa_shared(smem_u32(C::MERGED ? &full[b] : &bfull[b]), 0u));
-          if (++b == BSTAGES) {
-            b = 0;
+          if ((b += QS) >= BSTAGES) {
+            b -= BSTAGES;
             bph ^= 1u;
           }
         }
@@ -924,43 +944,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_next(f0);
         load_next(f1);
       }
+      // paired steps keep one ring slot more between a read and its refill
 #pragma unroll 1
-      for (int k = 0; k < CS - 1; ++k)
+      for (int k = 0; k < CS - (C::PAIRSTEP ? 2 : 1); ++k)
         if constexpr (!WB && !C::REG_CODES) fetch();
-      for (int64_t q = 0; q < n_it; ++q) {
-        Frag cur;
-        if constexpr (!WB && C::REG_CODES) {
-          cur = f0;
-          f0 = f1;
-          load_next(f1);  // the step after next
-        } else if constexpr (!WB) {
-          fetch();  // refills the slot read in the previous iteration
-          cp_async_wait<CS - 1>();
-          read_frag<BWD, BN, PAIR>(cur, ring + (q % CS) * C::CODE_BYTES, t_idx);
-        }
-        bool ok = !*abort_flag;
-        // merged: stage b's commit frees the buffer (b equals the stage index)
-        uint64_t* freed = C::MERGED ? &empty[b] : &bempty[b];
-        if constexpr (PAIR != 0) ok = ok && mbar_wait_cluster(freed, bph ^ 1u, DERR_TIMEOUT_BEMPTY);
-        else ok = ok && mbar_wait(freed, bph ^ 1u, DERR_TIMEOUT_BEMPTY);
-        if (!ok) {
-          *abort_flag = 1u;
-          break;
-        }
-        uint8_t* Bt = sB + b * C::B_BYTES;
-        const bool lora_step = is_lora_step(pc.i);
-        // bf16 weights: one thread loads the tile (this CTA's half of it in a
-        // pair) with TMA; its arrival carries the bytes, the other warps arrive
-        // as usual
+      // Fill weight buffer bb for the step at position ps: decode the codes
+      // in cur, build the LoRA factor tile, or (bf16 weights) have one
+      // thread load the tile (this CTA's half of it in a pair) with TMA,
+      // whose arrival carries the bytes.  Returns whether the tile came by TMA.
+      auto fill = [&](const Frag& cur, int bb, const Pos& ps) -> bool {
+        uint8_t* Bt = sB + bb * C::B_BYTES;
+        const bool lora_step = is_lora_step(ps.i);
         const bool tma_step = WB && !lora_step;
         if (!lora_step) {
           if constexpr (WB) {
             if (warp == 2 && lane == 0) {
-              const int64_t nb = (int64_t)pc.nt * BN;
-              const int32_t kc = kstep(pc.i) * 64;
+              const int64_t nb = (int64_t)ps.nt * BN;
+              const int32_t kc = kstep(ps.i) * 64;
               const int32_t half0 = PM ? rank * C::BW : 0;
               // merged, even CTA: the stage barrier; else this CTA's buffer barrier
-              uint64_t* wbar = (C::MERGED && rank == 0) ? &full[b] : &bfull[b];
+              uint64_t* wbar = (C::MERGED && rank == 0) ? &full[bb] : &bfull[bb];
               mbar_arrive_expect_tx(wbar, C::B_BYTES);
               if constexpr (!BWD) {
                 const TileGrp tg = tile_grp(args, nb);
@@ -977,38 +980,116 @@ __global__ void __launch_bounds__(kThreads, 1)
             else dequant_bwd<BN, PAIR>(cur, Bt, rank, t_idx);
           }
         } else {
-          const TileGrp tg = tile_grp(args, (int64_t)pc.nt * BN);
-          lora_tile<BWD, BN, PAIR>(tg.lora_F, tg.width, tg.width, (int)((int64_t)pc.nt * BN - tg.c0),
+          const TileGrp tg = tile_grp(args, (int64_t)ps.nt * BN);
+          lora_tile<BWD, BN, PAIR>(tg.lora_F, tg.width, tg.width, (int)((int64_t)ps.nt * BN - tg.c0),
                                    args.lora_scale, Bt, rank, t_idx);
         }
-        if (!tma_step) fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && !(tma_step && warp == 2)) {
-          if constexpr (PM) {
-            // the even CTA's MMA reads this half where it lies
-            mbar_arrive((C::MERGED && rank == 0) ? &full[b] : &bfull[b]);
-          } else if constexpr (PAIR == 1) {
-            // this warp's share of the half tile is one contiguous block:
-            // rows (K-major) or one 8-row contraction group (MN-major);
-            // send it to the same place in the other CTA's buffer
-            constexpr uint32_t kShare = C::B_BYTES / 16;
-            const int dw = warp - 2;
-            const uint32_t off =
-                (BWD && !lora_step)
-                    ? (uint32_t)(dw * (int)C::MN_SBO + rank * (BN / 128) * 1024)
-                    : (uint32_t)((rank * (BN / 2) + dw * (BN / 16)) * 128);
-            mbar_arrive_expect_tx(&bfull[b], kShare);
-            bulk_copy_to_peer(mapa_shared(smem_u32(Bt + off), peer), Bt + off, kShare,
-                              mapa_shared(smem_u32(&bfull[b]), peer));
+        return tma_step;
+      };
+      if constexpr (C::PAIRSTEP) {
+        // Two steps per handover (merged pair MMA, NF4 codes): wait until the
+        // later of the two buffers is free (the MMA commits complete in issue
+        // order, so the earlier one is free too), fill both, then one fence
+        // and one arrival on the even buffer's barrier (the odd CTA's on its
+        // own buffer barrier, which its forwarding thread passes on).
+        for (int64_t q = 0; q < n_it; q += 2) {
+          const bool two = q + 1 < n_it;
+          Frag c0, c1;
+          if constexpr (C::REG_CODES) {
+            c0 = f0;
+            c1 = f1;
+            load_next(f0);  // two steps ahead
+            load_next(f1);
           } else {
-            mbar_arrive(&bfull[b]);
+            fetch();  // refill the slots read in the previous iteration
+            fetch();
+            cp_async_wait<CS - 2>();
+            read_frag<BWD, BN, PAIR>(c0, ring + (q % CS) * C::CODE_BYTES, t_idx);
+            read_frag<BWD, BN, PAIR>(c1, ring + ((q + 1) % CS) * C::CODE_BYTES, t_idx);
+          }
+          const int bw = two ? b + 1 : b;
+          if (*abort_flag || !mbar_wait_cluster(&empty[bw], bph ^ 1u, DERR_TIMEOUT_BEMPTY)) {
+            *abort_flag = 1u;
+            break;
+          }
+          Pos p1 = pc;
+          p1.next(S, args.mtiles);
+          fill(c0, b, pc);
+          if (two) fill(c1, b + 1, p1);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(rank == 0 ? &full[b] : &bfull[b]);
+          pc = p1;
+          pc.next(S, args.mtiles);
+          if ((b += two ? 2 : 1) >= BSTAGES) {
+            b -= BSTAGES;
+            bph ^= 1u;
           }
         }
-        if (++b == BSTAGES) {
-          b = 0;
-          bph ^= 1u;
+      } else {
+        // One pipeline step; f holds its codes (register pipeline) and is
+        // refilled with those of the step two ahead.  The loop below runs the
+        // step twice per iteration, on f0 then f1, so a fragment is only
+        // overwritten after its own use.
+        auto dq_step = [&](int64_t q, Frag& f) -> bool {
+          Frag cur;
+          if constexpr (!WB && C::REG_CODES) {
+            cur = f;
+            load_next(f);  // the step after next
+          } else if constexpr (!WB) {
+            (void)f;
+            fetch();  // refills the slot read in the previous iteration
+            cp_async_wait<CS - 1>();
+            read_frag<BWD, BN, PAIR>(cur, ring + (q % CS) * C::CODE_BYTES, t_idx);
+          } else {
+            (void)f;
+          }
+          bool ok = !*abort_flag;
+          // merged: stage b's commit frees the buffer (b equals the stage index)
+          uint64_t* freed = C::MERGED ? &empty[b] : &bempty[b];
+          if constexpr (PAIR != 0) ok = ok && mbar_wait_cluster(freed, bph ^ 1u, DERR_TIMEOUT_BEMPTY);
+          else ok = ok && mbar_wait(freed, bph ^ 1u, DERR_TIMEOUT_BEMPTY);
+          if (!ok) {
+            *abort_flag = 1u;
+            return false;
+          }
+          const bool lora_step = is_lora_step(pc.i);
+          const bool tma_step = fill(cur, b, pc);
+          uint8_t* Bt = sB + b * C::B_BYTES;
+          if (!tma_step) fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && !(tma_step && warp == 2)) {
+            if constexpr (PM) {
+              // the even CTA's MMA reads this half where it lies
+              mbar_arrive((C::MERGED && rank == 0) ? &full[b] : &bfull[b]);
+            } else if constexpr (PAIR == 1) {
+              // this warp's share of the half tile is one contiguous block:
+              // rows (K-major) or one 8-row contraction group (MN-major);
+              // send it to the same place in the other CTA's buffer
+              constexpr uint32_t kShare = C::B_BYTES / 16;
+              const int dw = warp - 2;
+              const uint32_t off =
+                  (BWD && !lora_step)
+                      ? (uint32_t)(dw * (int)C::MN_SBO + rank * (BN / 128) * 1024)
+                      : (uint32_t)((rank * (BN / 2) + dw * (BN / 16)) * 128);
+              mbar_arrive_expect_tx(&bfull[b], kShare);
+              bulk_copy_to_peer(mapa_shared(smem_u32(Bt + off), peer), Bt + off, kShare,
+                                mapa_shared(smem_u32(&bfull[b]), peer));
+            } else {
+              mbar_arrive(&bfull[b]);
+            }
+          }
+          if (++b == BSTAGES) {
+            b = 0;
+            bph ^= 1u;
+          }
+          pc.next(S, args.mtiles);
+          return true;
+        };
+        for (int64_t q = 0; q < n_it; q += 2) {
+          if (!dq_step(q, f0)) break;
+          if (q + 1 < n_it && !dq_step(q + 1, f1)) break;
         }
-        pc.next(S, args.mtiles);
       }
       cp_async_wait<0>();  // no copy may land after the CTA is gone
       if (WB && *abort_flag && warp == 2 && lane == 0) {
@@ -1144,22 +1225,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         // kFinRing cp.async entries there (entry = one piece's 32 rows x 16
         // columns), consumed chunk by chunk in step order.
         const int P = finisher ? (int)(u_last - unit) : 0;
-        const int64_t r_total = (int64_t)P * UM * kv;
         const uint32_t r_base = smem_u32(smem) + (uint32_t)(ew * kFinRing * 2048 + lane * 16);
-        int64_t r_issued = 0, r_used = 0;
-        auto r_issue = [&]() {
-          if (r_issued < r_total) {
-            const int k = (int)(r_issued / P), pp = (int)(r_issued % P) + 1;
-            const float4* src = part4(cta_of(unit + pp), (k / kv) * 128 + r, half * (BN / 2) + (k % kv) * 16);
-            const uint32_t dst = r_base + (uint32_t)((r_issued % kFinRing) * 2048);
+        // Entries are issued in consumption order -- chunk k = (u, c) of this
+        // warp, then piece 1 .. P -- with the position kept as counters (no
+        // divisions in the loop).  Every call commits one group, so group g
+        // always holds entry g (or nothing, past the last); an entry is
+        // refilled right after it is consumed, so the slot to fill is always
+        // the one just read.
+        int ri_pp = 1, ri_k = 0, slot = 0;
+        auto r_issue = [&](int into) {
+          if (ri_k < UM * kv) {
+            const int u = (UM == 2 && ri_k >= kv) ? 1 : 0;
+            const float4* src = part4(cta_of(unit + ri_pp), u * 128 + r, half * (BN / 2) + (ri_k - u * kv) * 16);
+            const uint32_t dst = r_base + (uint32_t)(into * 2048);
 #pragma unroll
             for (int e = 0; e < 4; ++e) cp_async16(dst + (uint32_t)(e * 512), src + (int64_t)e * C::BM, 16u);
+            if (++ri_pp > P) {
+              ri_pp = 1;
+              ++ri_k;
+            }
           }
           cp_async_commit();
-          ++r_issued;
         };
         if (P > 0)
-          for (int j = 0; j < kFinRing; ++j) r_issue();
+          for (int j = 0; j < kFinRing; ++j) r_issue(j);
 #pragma unroll 1
         for (int u = 0; u < UM; ++u) {
           const int row = u * 128 + r;
@@ -1189,7 +1278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int pp = 0; pp < P; ++pp) {
               cp_async_wait<kFinRing - 1>();
               const float4* sl = reinterpret_cast<const float4*>(
-                  smem + ew * kFinRing * 2048 + (int)(r_used % kFinRing) * 2048 + lane * 16);
+                  smem + ew * kFinRing * 2048 + slot * 2048 + lane * 16);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const float4 q = sl[e * 32];
@@ -1198,8 +1287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v[4 * e + 2] += q.z;
                 v[4 * e + 3] += q.w;
               }
-              ++r_used;
-              r_issue();
+              r_issue(slot);
+              if (++slot == kFinRing) slot = 0;
             }
             if (!row_ok) continue;
             const int64_t o_off = m * og.width + (n - og.c0);
