@@ -1861,74 +1861,74 @@ __global__ void __launch_bounds__(kSkThreads, 1) k_skinny_tc(const __grid_consta
           for (int e = 0; e < 4; ++e)
             dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
         }
-        // the last chunk of this row block to finish sums them all in order
+        if (!ok) *abort_flag = 1u;
+      }
+      // The last chunk of this row block to finish sums them all, in chunk
+      // order, with all eight warps: two threads per row, eight columns each
+      // (each column's sum keeps its order), sixteen chunks in flight.
+      __threadfence();
+      named_bar_sync(1, 256);
+      if (warp == 2 && lane == 0) {
+        const uint32_t done = atomicAdd(counters + blockIdx.x, 1u);
+        if (done >= (uint32_t)chunks) atomicOr(&g_dev_error, DERR_BAD_CONFIG);  // left over
+        flags[1] = (done == (uint32_t)chunks - 1u) ? 1u : 0u;
+      }
+      named_bar_sync(1, 256);
+      if (flags[1] != 0u) {
         __threadfence();
-        named_bar_sync(1, 128);
-        if (warp == 2 && lane == 0) {
-          const uint32_t done = atomicAdd(counters + blockIdx.x, 1u);
-          if (done >= (uint32_t)chunks) atomicOr(&g_dev_error, DERR_BAD_CONFIG);  // left over
-          flags[1] = (done == (uint32_t)chunks - 1u) ? 1u : 0u;
-        }
-        named_bar_sync(1, 128);
-        if (flags[1] != 0u) {
-          __threadfence();
-          if (ok && m < M) {
-            // chunks are added in index order; loads run eight chunks ahead
-            float acc[16];
+        const int h = t >> 7;  // column half
+        const int64_t m = m0 + (t & 127);
+        if (!*abort_flag && m < M) {
+          float acc[8];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-            const float4* src = reinterpret_cast<const float4*>(partial + m * 16);
-            const int64_t cstride = M * 4;  // float4 per chunk
-            int c = 0;
-            for (; c + 8 <= chunks; c += 8) {
-              float4 q[8][4];
+          for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+          const float4* src = reinterpret_cast<const float4*>(partial + m * 16) + 2 * h;
+          const int64_t cstride = M * 4;  // float4 per chunk
+          int c = 0;
+          for (; c + 16 <= chunks; c += 16) {
+            float4 q[16][2];
 #pragma unroll
-              for (int u = 0; u < 8; ++u)
+            for (int u = 0; u < 16; ++u)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) q[u][e] = __ldcg(src + (int64_t)(c + u) * cstride + e);
+              for (int e = 0; e < 2; ++e) q[u][e] = __ldcg(src + (int64_t)(c + u) * cstride + e);
 #pragma unroll
-              for (int u = 0; u < 8; ++u)
+            for (int u = 0; u < 16; ++u)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  acc[4 * e] += q[u][e].x;
-                  acc[4 * e + 1] += q[u][e].y;
-                  acc[4 * e + 2] += q[u][e].z;
-                  acc[4 * e + 3] += q[u][e].w;
-                }
-            }
-            for (; c < chunks; ++c) {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float4 q = __ldcg(src + (int64_t)c * cstride + e);
-                acc[4 * e] += q.x;
-                acc[4 * e + 1] += q.y;
-                acc[4 * e + 2] += q.z;
-                acc[4 * e + 3] += q.w;
+              for (int e = 0; e < 2; ++e) {
+                acc[4 * e] += q[u][e].x;
+                acc[4 * e + 1] += q[u][e].y;
+                acc[4 * e + 2] += q[u][e].z;
+                acc[4 * e + 3] += q[u][e].w;
               }
-            }
-            float4* o = reinterpret_cast<float4*>(out + m * 16);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              o[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
-            // [hi | lo | hi | 0] bf16 row for the tensor-core LoRA step
-            uint32_t hi[8], lo[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              hi[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
-              lo[e] = pack_bf16x2(acc[2 * e] - bf16_lo(hi[e]), acc[2 * e + 1] - bf16_hi(hi[e]));
-            }
-            uint4* x4 = reinterpret_cast<uint4*>(ext + m * 64);
-            x4[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            x4[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-            x4[2] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            x4[3] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-            x4[4] = x4[0];
-            x4[5] = x4[1];
-            x4[6] = make_uint4(0u, 0u, 0u, 0u);
-            x4[7] = make_uint4(0u, 0u, 0u, 0u);
           }
-          if (warp == 2 && lane == 0) counters[blockIdx.x] = 0u;  // ready for the next launch
+          for (; c < chunks; ++c) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float4 q = __ldcg(src + (int64_t)c * cstride + e);
+              acc[4 * e] += q.x;
+              acc[4 * e + 1] += q.y;
+              acc[4 * e + 2] += q.z;
+              acc[4 * e + 3] += q.w;
+            }
+          }
+          float4* o = reinterpret_cast<float4*>(out + m * 16) + 2 * h;
+          o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+          o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+          // [hi | lo | hi | 0] bf16 row for the tensor-core LoRA step; this
+          // thread's eight columns of each part
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hi[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
+            lo[e] = pack_bf16x2(acc[2 * e] - bf16_lo(hi[e]), acc[2 * e + 1] - bf16_hi(hi[e]));
+          }
+          uint4* x4 = reinterpret_cast<uint4*>(ext + m * 64);
+          x4[h] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          x4[2 + h] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          x4[4 + h] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          x4[6 + h] = make_uint4(0u, 0u, 0u, 0u);
         }
+        if (warp == 2 && lane == 0) counters[blockIdx.x] = 0u;  // ready for the next launch
       }
     }
   }
@@ -2433,6 +2433,9 @@ int skinny_tc_chunks(int64_t M, int64_t K, int ng = 1) {
   return (int)((steps + spc - 1) / spc);
 }
 
+// Chunks (CTAs per row block) of the unmasked products G = dY B at most.
+constexpr int kSkChunksG = 10;
+
 size_t skinny_partial_bytes(int64_t M, int64_t K) {
   return (size_t)skinny_tc_chunks(M, K) * (size_t)M * 16 * sizeof(float);
 }
@@ -2497,8 +2500,14 @@ cudaError_t skinny_launch(const uint16_t* const* X, int ng, const float* const* 
   if (!encode_fn()) return cudaErrorNotSupported;
   if (K % 64 != 0 || M < 1 || ng < 1 || ng > kMaxGroups) return cudaErrorInvalidValue;
   const int64_t atoms = (M + 127) / 128;
-  const int chunks = skinny_tc_chunks(M, K, ng);
+  int chunks = skinny_tc_chunks(M, K, ng);
   const int64_t steps = K / 64;
+  if (f_kj && chunks > kSkChunksG) {
+    // G = dY B draws no dropout bits, so its steps are short: fewer, longer
+    // chunks leave the last CTA of a row block fewer partial sums to add
+    const int64_t sp = (steps + kSkChunksG - 1) / kSkChunksG;
+    chunks = (int)((steps + sp - 1) / sp);
+  }
   const int spc = (int)((steps + chunks - 1) / chunks);
   uint32_t* counters = nullptr;
   cudaError_t e = ring_slots((uint32_t)(atoms * ng), &counters);
