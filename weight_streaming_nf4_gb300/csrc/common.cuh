@@ -354,6 +354,16 @@ WS_DEVINL void mbar_arrive_cluster(uint32_t cbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar)
                : "memory");
 }
+// The same arrival with release at CTA scope (the instruction's default
+// semantics): orders this CTA's earlier shared-memory writes and completed
+// tensor-memory accesses before it, which is all a pair partner needs when
+// the data handed over lies in this CTA's own shared or tensor memory.  A
+// cluster-scope release costs about as much as a pipeline step of the
+// dequant GEMM (its forwarding thread's release alone held the 256-wide
+// steps at 0.8 us).
+WS_DEVINL void mbar_arrive_remote(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
 WS_DEVINL bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

@@ -90,12 +90,10 @@ namespace {
 constexpr bool kMergedBarriers = WS_GEMM_MERGED_BARRIERS != 0;
 // Paired handovers per configuration, a bit mask: 1 forward 128-wide tiles,
 // 2 forward 256-wide, 4 input gradient 128-wide, 8 input gradient 256-wide.
-// On for the 128-wide tiles, whose steps are short enough for the per-step
-// handshake to bound them (32B step 77.3 -> 76.4 ms); the 256-wide tiles,
-// whose MMAs take as long as the decode, lose a step of prefetch slack
-// (waiting for the later buffer) and run slower paired.
+// On for all: the per-step handshake bounds the steps (32B step 73.6 -> 72.2
+// ms against per-step handovers for the 256-wide tiles).
 #ifndef WS_GEMM_PAIR_STEPS
-#define WS_GEMM_PAIR_STEPS 5
+#define WS_GEMM_PAIR_STEPS 15
 #endif
 constexpr int kPairSteps = WS_GEMM_PAIR_STEPS;
 
@@ -682,8 +680,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // PAIR = 2: the even CTA's full / bfull / accempty / lora_masked count
     // both CTAs' producers and epilogues: the odd CTA's dequant warps arrive
     // on its own bfull, and one forwarding thread passes each completed
-    // phase on to the even CTA (one cluster-scope release per step instead
-    // of one per warp)
+    // phase on to the even CTA (one remote arrival per handover instead of
+    // one per warp)
     for (int b = 0; b < BSTAGES; ++b) {
       mbar_init(&bfull[b], (PM && rank == 0) ? kDqWarps + 1 : kDqWarps);
       mbar_init(&bempty[b], PAIR == 1 ? 2 : 1);
@@ -884,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *abort_flag = 1u;
             break;
           }
-          mbar_arrive_cluster(mapa_shared(smem_u32(C::MERGED ? &full[b] : &bfull[b]), 0u));
+          mbar_arrive_remote(mapa_shared(smem_u32(C::MERGED ? &full[b] : &bfull[b]), 0u));
           if ((b += QS) >= BSTAGES) {
             b -= BSTAGES;
             bph ^= 1u;
@@ -1183,7 +1181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            if (PM && rank == 1) mbar_arrive_cluster(mapa_shared(smem_u32(lora_masked), 0u));
+            if (PM && rank == 1) mbar_arrive_remote(mapa_shared(smem_u32(lora_masked), 0u));
             else mbar_arrive(lora_masked);
           }
         }
@@ -1327,7 +1325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (PM && rank == 1) mbar_arrive_cluster(mapa_shared(smem_u32(&accempty[a]), 0u));
+          if (PM && rank == 1) mbar_arrive_remote(mapa_shared(smem_u32(&accempty[a]), 0u));
           else mbar_arrive(&accempty[a]);
         }
         p = seg_end;
