@@ -1215,6 +1215,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 16-column chunks of this warp's columns that lie inside the output
         // (of this tile's linear, for a grouped forward)
         const TileGrp og = tile_grp(args, n0);
+        // 32-byte stores need 32-byte aligned rows of the output
+        const bool v8_out = (reinterpret_cast<uintptr_t>(og.out) & 31u) == 0u &&
+                            (og.width & (args.out_f32 ? 7 : 15)) == 0;
         constexpr int KCH = (BN / 2) / 16;
         const int64_t cols_left = og.width - (n0 - og.c0 + half * (BN / 2));
         const int kv = cols_left <= 0 ? 0 : (cols_left >= KCH * 16 ? KCH : (int)((cols_left + 15) / 16));
@@ -1290,7 +1293,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!row_ok) continue;
             const int64_t o_off = m * og.width + (n - og.c0);
-            if (args.out_f32) {
+            if (v8_out) {
+              // one 32-byte store per 8 fp32 or 16 bf16 values: whole
+              // sectors (16-byte stores of the rows of a warp write half
+              // sectors and held every accumulator drain back)
+              if (args.out_f32) {
+                float* dst = static_cast<float*>(og.out) + o_off;
+                if (args.out_accum) {
+                  const float4* d4 = reinterpret_cast<const float4*>(dst);
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const float4 q = d4[e];
+                    v[4 * e] = q.x + v[4 * e];
+                    v[4 * e + 1] = q.y + v[4 * e + 1];
+                    v[4 * e + 2] = q.z + v[4 * e + 2];
+                    v[4 * e + 3] = q.w + v[4 * e + 3];
+                  }
+                }
+                st_global_v8(dst, __float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                             __float_as_uint(v[3]), __float_as_uint(v[4]), __float_as_uint(v[5]),
+                             __float_as_uint(v[6]), __float_as_uint(v[7]));
+                st_global_v8(dst + 8, __float_as_uint(v[8]), __float_as_uint(v[9]), __float_as_uint(v[10]),
+                             __float_as_uint(v[11]), __float_as_uint(v[12]), __float_as_uint(v[13]),
+                             __float_as_uint(v[14]), __float_as_uint(v[15]));
+              } else {
+                st_global_v8(static_cast<uint16_t*>(og.out) + o_off, pack_bf16x2(v[0], v[1]),
+                             pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]),
+                             pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]),
+                             pack_bf16x2(v[12], v[13]), pack_bf16x2(v[14], v[15]));
+              }
+            } else if (args.out_f32) {
               float4* dst = reinterpret_cast<float4*>(static_cast<float*>(og.out) + o_off);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
