@@ -111,6 +111,14 @@ WS_DEVINL uint32_t smem_u32(const void* p) {
 WS_DEVINL void sts128(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
 }
+// One 32-byte global load (p 32-byte aligned).
+WS_DEVINL void ld_global_v8(const void* p, uint32_t* r) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "l"(p)
+               : "memory");
+}
 // One 32-byte global store (p 32-byte aligned).
 WS_DEVINL void st_global_v8(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
                             uint32_t f, uint32_t g, uint32_t h) {

@@ -1300,15 +1300,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (args.out_f32) {
                 float* dst = static_cast<float*>(og.out) + o_off;
                 if (args.out_accum) {
-                  const float4* d4 = reinterpret_cast<const float4*>(dst);
+                  uint32_t q[16];
+                  ld_global_v8(dst, q);
+                  ld_global_v8(dst + 8, q + 8);
 #pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    const float4 q = d4[e];
-                    v[4 * e] = q.x + v[4 * e];
-                    v[4 * e + 1] = q.y + v[4 * e + 1];
-                    v[4 * e + 2] = q.z + v[4 * e + 2];
-                    v[4 * e + 3] = q.w + v[4 * e + 3];
-                  }
+                  for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(q[e]) + v[e];
                 }
                 st_global_v8(dst, __float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
                              __float_as_uint(v[3]), __float_as_uint(v[4]), __float_as_uint(v[5]),
