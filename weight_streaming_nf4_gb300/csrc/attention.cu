@@ -384,6 +384,9 @@ __global__ void __launch_bounds__(kAtThreads, 1) k_attn_fwd(const __grid_constan
       const int64_t row = row0 + r;
       const bool valid = qi < S && row < a.M;
       const int64_t ld = (int64_t)a.nh * D;
+      // 32-byte stores need 32-byte aligned rows
+      const bool v8 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0u && (ld & 15) == 0 &&
+                      (!a.o32 || (reinterpret_cast<uintptr_t>(a.o32) & 31u) == 0u);
 #pragma unroll
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t acc[32];
@@ -394,16 +397,35 @@ __global__ void __launch_bounds__(kAtThreads, 1) k_attn_fwd(const __grid_constan
 #pragma unroll
         for (int e = 0; e < 32; ++e) ov[e] = __fdiv_rn(__uint_as_float(acc[e]), l);
         uint16_t* dst = a.o + row * ld + h * D + cc;
+        if (v8) {
+          // whole 32-byte sectors per store (a warp's lanes hold different rows)
 #pragma unroll
-        for (int e = 0; e < 32; e += 8)
-          *reinterpret_cast<uint4*>(dst + e) =
-              make_uint4(pack_bf16x2(ov[e], ov[e + 1]), pack_bf16x2(ov[e + 2], ov[e + 3]),
-                         pack_bf16x2(ov[e + 4], ov[e + 5]), pack_bf16x2(ov[e + 6], ov[e + 7]));
+          for (int e = 0; e < 32; e += 16)
+            st_global_v8(dst + e, pack_bf16x2(ov[e], ov[e + 1]), pack_bf16x2(ov[e + 2], ov[e + 3]),
+                         pack_bf16x2(ov[e + 4], ov[e + 5]), pack_bf16x2(ov[e + 6], ov[e + 7]),
+                         pack_bf16x2(ov[e + 8], ov[e + 9]), pack_bf16x2(ov[e + 10], ov[e + 11]),
+                         pack_bf16x2(ov[e + 12], ov[e + 13]), pack_bf16x2(ov[e + 14], ov[e + 15]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8)
+            *reinterpret_cast<uint4*>(dst + e) =
+                make_uint4(pack_bf16x2(ov[e], ov[e + 1]), pack_bf16x2(ov[e + 2], ov[e + 3]),
+                           pack_bf16x2(ov[e + 4], ov[e + 5]), pack_bf16x2(ov[e + 6], ov[e + 7]));
+        }
         if (a.o32) {
           float* d32 = a.o32 + row * ld + h * D + cc;
+          if (v8) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(d32 + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
+            for (int e = 0; e < 32; e += 8)
+              st_global_v8(d32 + e, __float_as_uint(ov[e]), __float_as_uint(ov[e + 1]),
+                           __float_as_uint(ov[e + 2]), __float_as_uint(ov[e + 3]),
+                           __float_as_uint(ov[e + 4]), __float_as_uint(ov[e + 5]),
+                           __float_as_uint(ov[e + 6]), __float_as_uint(ov[e + 7]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(d32 + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
+          }
         }
       }
       if (valid) a.lse[(int64_t)h * a.M + row] = lse2 * kLn2;
@@ -661,13 +683,19 @@ WS_DEVINL void attn_dq_tile(const AttnDqArgs& a, uint8_t* smem, int qt, int h, i
         if (!valid) continue;
         uint16_t* dst = a.dq + row * ld + h * D + cc;
         const float sc = a.scale;
+        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 8)
-          *reinterpret_cast<uint4*>(dst + e) = make_uint4(
-              pack_bf16x2(sc * __uint_as_float(acc[e]), sc * __uint_as_float(acc[e + 1])),
-              pack_bf16x2(sc * __uint_as_float(acc[e + 2]), sc * __uint_as_float(acc[e + 3])),
-              pack_bf16x2(sc * __uint_as_float(acc[e + 4]), sc * __uint_as_float(acc[e + 5])),
-              pack_bf16x2(sc * __uint_as_float(acc[e + 6]), sc * __uint_as_float(acc[e + 7])));
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(sc * __uint_as_float(acc[2 * e]), sc * __uint_as_float(acc[2 * e + 1]));
+        if ((reinterpret_cast<uintptr_t>(a.dq) & 31u) == 0u && (ld & 15) == 0) {
+          // whole 32-byte sectors per store
+          st_global_v8(dst, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+          st_global_v8(dst + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<uint4*>(dst + 8 * e) = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
       }
     }
   }
@@ -924,14 +952,32 @@ WS_DEVINL void attn_dkv_tile(const AttnDkvArgs& a, uint8_t* smem, int kt, int h,
         tmem_ld_32x32b_x32(trow + TM_DK + cc, ak);
         tmem_ld_wait();
         if (!valid) continue;
+        if ((reinterpret_cast<uintptr_t>(a.dk_part) & 31u) != 0u) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          *reinterpret_cast<float4*>(dvp + cc + e) =
-              make_float4(__uint_as_float(av[e]), __uint_as_float(av[e + 1]),
-                          __uint_as_float(av[e + 2]), __uint_as_float(av[e + 3]));
-          *reinterpret_cast<float4*>(dkp + cc + e) = make_float4(
-              a.scale * __uint_as_float(ak[e]), a.scale * __uint_as_float(ak[e + 1]),
-              a.scale * __uint_as_float(ak[e + 2]), a.scale * __uint_as_float(ak[e + 3]));
+          for (int e = 0; e < 32; e += 4) {
+            *reinterpret_cast<float4*>(dvp + cc + e) =
+                make_float4(__uint_as_float(av[e]), __uint_as_float(av[e + 1]),
+                            __uint_as_float(av[e + 2]), __uint_as_float(av[e + 3]));
+            *reinterpret_cast<float4*>(dkp + cc + e) = make_float4(
+                a.scale * __uint_as_float(ak[e]), a.scale * __uint_as_float(ak[e + 1]),
+                a.scale * __uint_as_float(ak[e + 2]), a.scale * __uint_as_float(ak[e + 3]));
+          }
+          continue;
+        }
+        // whole 32-byte sectors per store (rows of D fp32 values keep the
+        // 32-byte alignment of the workspace)
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          st_global_v8(dvp + cc + e, av[e], av[e + 1], av[e + 2], av[e + 3], av[e + 4], av[e + 5],
+                       av[e + 6], av[e + 7]);
+          st_global_v8(dkp + cc + e, __float_as_uint(a.scale * __uint_as_float(ak[e])),
+                       __float_as_uint(a.scale * __uint_as_float(ak[e + 1])),
+                       __float_as_uint(a.scale * __uint_as_float(ak[e + 2])),
+                       __float_as_uint(a.scale * __uint_as_float(ak[e + 3])),
+                       __float_as_uint(a.scale * __uint_as_float(ak[e + 4])),
+                       __float_as_uint(a.scale * __uint_as_float(ak[e + 5])),
+                       __float_as_uint(a.scale * __uint_as_float(ak[e + 6])),
+                       __float_as_uint(a.scale * __uint_as_float(ak[e + 7])));
         }
       }
     }
