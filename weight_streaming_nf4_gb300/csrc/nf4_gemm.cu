@@ -1882,10 +1882,21 @@ __global__ void __launch_bounds__(kSkThreads, 1) k_skinny_tc(const __grid_consta
           for (int j = 0; j < 16; ++j) v[j] = 0.0f;
         }
         if (ok && m < M) {
-          float4* dst = reinterpret_cast<float4*>(partial + ((int64_t)blockIdx.y * M + m) * 16);
+          float* dst = partial + ((int64_t)blockIdx.y * M + m) * 16;
+          if ((reinterpret_cast<uintptr_t>(partial) & 31u) == 0u) {
+            // whole 32-byte sectors (a warp's lanes hold different rows)
+            st_global_v8(dst, __float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                         __float_as_uint(v[3]), __float_as_uint(v[4]), __float_as_uint(v[5]),
+                         __float_as_uint(v[6]), __float_as_uint(v[7]));
+            st_global_v8(dst + 8, __float_as_uint(v[8]), __float_as_uint(v[9]), __float_as_uint(v[10]),
+                         __float_as_uint(v[11]), __float_as_uint(v[12]), __float_as_uint(v[13]),
+                         __float_as_uint(v[14]), __float_as_uint(v[15]));
+          } else {
+            float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+            for (int e = 0; e < 4; ++e)
+              d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+          }
         }
         if (!ok) *abort_flag = 1u;
       }
