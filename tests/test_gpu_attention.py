@@ -124,6 +124,39 @@ def test_attention_repeats_bitwise_and_batches_split(ops):
     assert ops.device_error() == 0
 
 
+def test_attention_outputs_only_16_byte_aligned(ops):
+    """O, the fp32 O, dQ and the backward workspace (the per-head dK/dV
+    partials) starting 16 bytes into 32-byte aligned allocations take the
+    16-byte store path; the results hold the same bits."""
+    g = torch.Generator().manual_seed(5)
+    S, nh, nkv, d = 256, 8, 2, 128
+    q = (torch.randn(S, nh * d, generator=g)).to(torch.bfloat16).cuda()
+    k = (torch.randn(S, nkv * d, generator=g)).to(torch.bfloat16).cuda()
+    v = (torch.randn(S, nkv * d, generator=g)).to(torch.bfloat16).cuda()
+    dO = (torch.randn(S, nh * d, generator=g)).to(torch.bfloat16).cuda()
+
+    def shifted(shape, dtype, elems16):
+        n = int(np.prod(shape))
+        buf = torch.empty(n + 64, dtype=dtype, device="cuda")
+        assert buf.data_ptr() % 32 == 0
+        return buf[elems16:elems16 + n].view(shape)
+
+    o, o32, lse = ops.attention_fwd(q, k, v, 1, d)
+    o2 = shifted((S, nh * d), torch.bfloat16, 8)
+    o32b = shifted((S, nh * d), torch.float32, 4)
+    ops.attention_fwd(q, k, v, 1, d, o=o2, o32=o32b)
+    dq, dk, dv = ops.attention_bwd(q, k, v, o32, lse, dO, 1, d)
+    wsz = ops.attention_workspace_size(S, nh, d)
+    ws = torch.empty(wsz + 64, dtype=torch.uint8, device="cuda")[16:16 + wsz]
+    dq2 = shifted((S, nh * d), torch.bfloat16, 8)
+    _, dk2, dv2 = ops.attention_bwd(q, k, v, o32, lse, dO, 1, d, dq=dq2, workspace=ws)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    assert o2.data_ptr() % 32 == 16 and ws.data_ptr() % 32 == 16
+    assert torch.equal(o, o2) and torch.equal(o32, o32b)
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+
+
 def test_attention_rejects_bad_arguments(ops):
     q = torch.zeros((128, 256), dtype=torch.bfloat16, device="cuda")
     k = torch.zeros((128, 96), dtype=torch.bfloat16, device="cuda")

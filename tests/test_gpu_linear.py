@@ -192,3 +192,42 @@ def test_nf4_matmul_alone(ops, orc, M, N, K):
     dXo, _, _ = orc.lora_bwd(d["x"], Wq, zA, zB, None, d["dY"], 0.0)
     assert rel(to_f64(y), yo) <= TOL
     assert rel(to_f64(dX), dXo) <= 1e-4
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 896, 1088), (512, 3584, 3584)])
+def test_outputs_only_16_byte_aligned(ops, orc, M, N, K):
+    """Outputs whose rows start 16 (not 32) bytes into an allocation take the
+    16-byte store path of the epilogues; they hold the same bits as outputs
+    at 32-byte aligned addresses (y, the bf16 and fp32 input gradients, and
+    the accumulating fp32 input gradient)."""
+    d, W, key = _linear(ops, orc, M, N, K, f"al{M}x{N}", lin=1, layer=1, step=3)
+    x, A, B, dY = bf16_to_dev(d["x"]), f32_to_dev(d["A"]), f32_to_dev(d["B"]), bf16_to_dev(d["dY"])
+
+    def shifted(shape, dtype, elems16):
+        n = int(np.prod(shape))
+        buf = torch.empty(n + 64, dtype=dtype, device="cuda")
+        assert buf.data_ptr() % 32 == 0
+        return buf[elems16:elems16 + n].view(shape)
+
+    y, U, mask = ops.lora_linear_fwd(W, x, A, B, key)
+    y2 = shifted((M, N), torch.bfloat16, 8)
+    ops.lora_linear_fwd(W, x, A, B, key, y=y2)
+    dXb, _, _ = ops.lora_linear_bwd(W, x, A, B, key, U, mask, dY)
+    dXb2 = shifted((M, K), torch.bfloat16, 8)
+    ops.lora_linear_bwd(W, x, A, B, key, U, mask, dY, dX=dXb2)
+    dXf, _, _ = ops.lora_linear_bwd(W, x, A, B, key, U, mask, dY, dX_f32=True)
+    dXf2 = shifted((M, K), torch.float32, 4)
+    ops.lora_linear_bwd(W, x, A, B, key, U, mask, dY, dX=dXf2)
+    base = torch.randn(M, K, device="cuda")
+    acc1 = base.clone()
+    ops.lora_linear_bwd(W, x, A, B, key, U, mask, dY, dX=acc1, accumulate=True)
+    acc2 = shifted((M, K), torch.float32, 4)
+    acc2.copy_(base)
+    ops.lora_linear_bwd(W, x, A, B, key, U, mask, dY, dX=acc2, accumulate=True)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    assert y2.data_ptr() % 32 == 16 and dXf2.data_ptr() % 32 == 16
+    assert torch.equal(y, y2)
+    assert torch.equal(dXb, dXb2)
+    assert torch.equal(dXf, dXf2)
+    assert torch.equal(acc1, acc2)
