@@ -152,6 +152,20 @@ struct DqGeo {
   static constexpr uint32_t SLOT_BYTES = NV * kDqThreads * VB + NS * kDqThreads * 4;
   static_assert(NV >= 1 && NV <= 2, "dequant geometry");
   static_assert(!BWD || (64 * COLS / (VB * 2)) % kDqThreads == 0, "dequant geometry");
+  // Backward: item it of thread t is (contraction row c, segment seg).  A
+  // thread's NV items are consecutive segments of one row (one 64-column
+  // block: one scale); the eight lanes of each quarter warp take eight
+  // consecutive rows of one segment group, so their 16-byte stores into the
+  // swizzled tile land in eight different bank groups (lanes of one row in
+  // the two 64-column halves hit the same banks).
+  static constexpr int SG = BWD ? SEGS / NV : 1;  // segment groups per row
+  static_assert(!BWD || (SEGS % NV == 0 && 32 % SG == 0), "backward item mapping");
+  WS_DEVINL static void item(int t, int it, int& c, int& seg) {
+    constexpr int RPW = 32 / SG;  // rows per warp
+    const int l = t & 31;
+    c = (t >> 5) * RPW + l % RPW;
+    seg = (l / RPW) * NV + it;
+  }
 };
 
 // WB: the weight is bf16 and its tiles are loaded by TMA (no dequantisation).
@@ -361,11 +375,10 @@ WS_DEVINL void fetch_codes(uint32_t slot, const uint8_t* codes, const float* abs
       cp_async_v<D::VB>(slot + (uint32_t)((v * kDqThreads + t) * D::VB), src + D::VB * v, in);
     cp_async4(sc + (uint32_t)(t * 4), absmax + (int64_t)i * wN + nn, in ? 4u : 0u);
   } else {
-    constexpr int SEGS = D::COLS / (2 * D::VB);
 #pragma unroll
     for (int it = 0; it < D::NV; ++it) {
-      const int item = t * D::NV + it;  // a warp's items cover whole 8-row groups
-      const int c = item / SEGS, seg = item % SEGS;
+      int c, seg;
+      D::item(t, it, c, seg);
       const int64_t r = (int64_t)i * 64 + c;
       const int64_t col = (int64_t)n0 + c0 + seg * 2 * D::VB;
       const bool in = r < wN && col < wK;
@@ -431,11 +444,10 @@ WS_DEVINL void load_frag(Frag& f, const uint8_t* codes, const float* absmax, int
     for (int v = 0; v < D::NV; ++v) ld(src + D::VB * v, in, v);
     f.a[0] = in ? __ldg(absmax + (int64_t)i * wN + nn) : 0.0f;
   } else {
-    constexpr int SEGS = D::COLS / (2 * D::VB);
 #pragma unroll
     for (int it = 0; it < D::NV; ++it) {
-      const int item = t * D::NV + it;
-      const int c = item / SEGS, seg = item % SEGS;
+      int c, seg;
+      D::item(t, it, c, seg);
       const int64_t r = (int64_t)i * 64 + c;
       const int64_t col = (int64_t)n0 + c0 + seg * 2 * D::VB;
       const bool in = r < wN && col < wK;
@@ -473,12 +485,11 @@ WS_DEVINL void dequant_bwd(const Frag& f, uint8_t* Bt, int rank, int t) {
   using D = DqGeo<true, BN, PAIR>;
   constexpr uint32_t SBO = ((PAIR == 2 ? BN / 2 : BN) / 64) * 1024;  // this CTA's buffer width
   constexpr int WPI = D::VB / 4;  // code words per item: 8 weights each
-  constexpr int SEGS = D::SEGS;
   const Nf4Table tb = make_table(f.a[0]);  // the thread's items share one block scale
 #pragma unroll
   for (int it = 0; it < D::NV; ++it) {
-    const int item = t * D::NV + it;
-    const int c = item / SEGS, seg = item % SEGS;
+    int c, seg;
+    D::item(t, it, c, seg);
     const int j0 = (PAIR == 1 ? rank * D::COLS : 0) + seg * 2 * D::VB;  // first buffer column
     const uint32_t grp = (uint32_t)((c >> 3) * SBO + (j0 / 64) * 1024 + (c & 7) * 128);
 #pragma unroll
