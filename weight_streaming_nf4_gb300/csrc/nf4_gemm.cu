@@ -1775,7 +1775,11 @@ __global__ void __launch_bounds__(kSkThreads, 1) k_skinny_tc(const __grid_consta
           mbar_arrive_expect_tx(&full[st], kSkX + kSkF);
           tma_load_2d(sX + st * kSkX, tmX, &full[st], k0, (int)m0);
           if (F_KJ) bulk_load(sF + st * kSkF, F + (int64_t)k0 * 16, kSkF, &full[st]);
-          else tma_load_2d(sF + st * kSkF, tmF, &full[st], k0, 0);
+          else {
+            // two 32-column boxes, 128-byte swizzled (see the reads below)
+            tma_load_2d(sF + st * kSkF, tmF, &full[st], k0, 0);
+            tma_load_2d(sF + st * kSkF + kSkF / 2, tmF, &full[st], k0 + 32, 0);
+          }
           issued = i + 1;
         }
         if (*abort_flag)
@@ -1822,7 +1826,25 @@ __global__ void __launch_bounds__(kSkThreads, 1) k_skinny_tc(const __grid_consta
           const float* fs = reinterpret_cast<const float*>(sF + st * kSkF);
           float f[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = F_KJ ? fs[(kc * 8 + e) * 16 + jj] : fs[jj * 64 + kc * 8 + e];
+          for (int e = 0; e < 8; ++e) {
+            if (F_KJ) f[e] = fs[(kc * 8 + e) * 16 + jj];
+          }
+          if (!F_KJ) {
+            // row jj, columns 8 kc .. 8 kc + 7 of the [16][64] slice, held as
+            // two [16][32] boxes whose 16-byte chunks are XOR-swizzled by the
+            // row: the eight rows of a quarter warp read eight different
+            // bank groups (unswizzled, the rows' 256-byte pitch put all
+            // sixteen on the same banks)
+            const uint8_t* half = sF + st * kSkF + (kc >> 2) * (kSkF / 2) + jj * 128;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const float4 v = *reinterpret_cast<const float4*>(half + ((((kc & 3) * 2 + q) ^ (jj & 7)) << 4));
+              f[4 * q] = v.x;
+              f[4 * q + 1] = v.y;
+              f[4 * q + 2] = v.z;
+              f[4 * q + 3] = v.w;
+            }
+          }
           uint32_t w[3][4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -2571,7 +2593,7 @@ cudaError_t skinny_launch(const uint16_t* const* X, int ng, const float* const* 
     if ((reinterpret_cast<uintptr_t>(F[g]) & 15u) != 0u) return cudaErrorInvalidValue;
     if (f_kj) sa.tmF[g] = sa.tmX[g];
     else if (!make_map(&sa.tmF[g], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, F[g], (uint64_t)K, 16,
-                       (uint64_t)K * 4, 64, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+                       (uint64_t)K * 4, 32, 16, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
     sa.F[g] = F[g];
     if (keys) sa.key[g] = keys[g];
