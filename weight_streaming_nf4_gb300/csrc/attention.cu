@@ -83,7 +83,7 @@ WS_DEVINL float ex2(float x) {
   return y;
 }
 
-// One verdict per warp: true only if v holds in every lane.  The row warps
+// One answer per warp: true only if v holds in every lane.  The row warps
 // wait on barriers lane by lane; deciding to stop as a warp keeps their
 // later warp-wide steps (__syncwarp, tensor-memory loads) convergent.
 WS_DEVINL bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
