@@ -2047,9 +2047,12 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 constexpr int kEpadSteps = WS_GEMM_EPAD;
 
 // 256-wide tiles when every unit's stream-K range covers at least this many
-// (tile, step) iterations.
+// (tile, step) iterations (a 256-wide pair MMA step costs about what a
+// 128-wide one does; below ~20 steps per unit the finisher's partial tiles
+// outweigh that: 32B q/o 44 against 41 us at 21 steps, 7B down 98 against
+// 109 us at 55).
 #ifndef WS_GEMM_BN256_MIN_STEPS
-#define WS_GEMM_BN256_MIN_STEPS 64
+#define WS_GEMM_BN256_MIN_STEPS 32
 #endif
 constexpr int64_t kBn256MinSteps = WS_GEMM_BN256_MIN_STEPS;
 
@@ -2265,7 +2268,7 @@ GemmPlan plan_gemm(bool bwd, int64_t M, int64_t Nout, int64_t Kc) {
   if (p.um == 2 && (!bwd || p.pair)) {
     // A 256-wide tile reads less shared memory per flop (256-wide MMAs) but
     // has a single accumulator (no epilogue overlap): worth it when each
-    // unit's stream-K range stays long (>= 64 steps).
+    // unit's stream-K range stays long enough (kBn256MinSteps).
     const int64_t units = p.pair ? pair_capacity(bwd, 256) : device_sm_count();
     const int64_t mt = (M + urows - 1) / urows, nt = (Nout + 255) / 256;
     if (units > 0 && mt * nt * (Kc / 64 + 1) >= kBn256MinSteps * units) p.bn = 256;
