@@ -1815,6 +1815,19 @@ __global__ void __launch_bounds__(kSkThreads, 1) k_skinny_tc(const __grid_consta
         const int st = i % kSkStages;
         const uint32_t ph = (uint32_t)(i / kSkStages) & 1u;
         const int64_t k0 = (s_begin + i) * 64;
+        // U: the dropout bits depend on the position only, so they are drawn
+        // (and stored) before the tile is waited for, beside its copy
+        uint32_t bits8[4];
+        if (MASKED) {
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int ch = t + it * 256;  // 0..1023: row r, 8-column chunk q
+            const int64_t m = m0 + (ch >> 3);
+            const uint64_t e0 = (uint64_t)m * (uint64_t)K + (uint64_t)(k0 + (ch & 7) * 8);
+            bits8[it] = keep4(key, e0) | (keep4(key, e0 + 4) << 4);
+            if (mask_bytes && m < M) mask_bytes[e0 >> 3] = (uint8_t)bits8[it];
+          }
+        }
         if (*abort_flag || !mbar_wait(&full[st], ph, DERR_TIMEOUT_FULL)) {
           *abort_flag = 1u;
           break;
@@ -1873,9 +1886,7 @@ __global__ void __launch_bounds__(kSkThreads, 1) k_skinny_tc(const __grid_consta
             const int r = ch >> 3, q = ch & 7;
             const int64_t m = m0 + r;
             if (m >= M) continue;
-            const uint64_t e0 = (uint64_t)m * (uint64_t)K + (uint64_t)(k0 + q * 8);
-            const uint32_t bits = keep4(key, e0) | (keep4(key, e0 + 4) << 4);
-            if (mask_bytes) mask_bytes[e0 >> 3] = (uint8_t)bits;
+            const uint32_t bits = bits8[it];
             if (bits == 0xFFu) continue;
             uint4* p4 = reinterpret_cast<uint4*>(tile + r * 128 + ((q ^ (r & 7)) << 4));
             uint4 v = *p4;
